@@ -1,0 +1,388 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+* the OCP E4M3 encoding landmarks (tests/golden/ocp_e4m3_landmarks.txt);
+* torch's float8_e4m3fn conversion (a library routine, round-to-nearest-even)
+  for every in-range value, exhaustively over bf16 bit patterns;
+* hand-worked block quantisations (tests/golden/mx_worked_examples.txt);
+* closed forms: power-of-two blocks round-trip exactly, all-zero blocks,
+  single-outlier saturation;
+* exact rational arithmetic (fractions.Fraction) for the block-scaled GEMM;
+* torch.nn.functional.silu for SiLU;
+* the whole MLP rebuilt from torch pieces (float8 conversion, fp64 matmul);
+* the quantisation-error band against the unquantised fp64 SwiGLU MLP.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------------ E4M3 table
+def _torch_e4m3_decode(code: int) -> float:
+    return float(torch.tensor([code], dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64))
+
+
+def test_e4m3_table_matches_ocp_landmarks():
+    table = oracle.e4m3_table()
+    with open(os.path.join(GOLDEN, "ocp_e4m3_landmarks.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            code_s, val_s = line.split()[:2]
+            assert table[int(code_s, 16)] == float.fromhex(val_s), line
+
+
+def test_e4m3_table_matches_torch_decode():
+    table = oracle.e4m3_table()
+    assert len(table) == 127
+    for c in range(127):
+        assert table[c] == _torch_e4m3_decode(c), c
+    assert np.all(np.diff(table) > 0)
+
+
+def _torch_e4m3_code(t: np.ndarray) -> np.ndarray:
+    """Magnitude code of torch's float8_e4m3fn conversion (valid for 0 <= t <= 448).
+
+    torch converts float64 through float32, which could round twice, so the
+    inputs must be float32 values (or so small that they round to zero)."""
+    t = np.ascontiguousarray(t, np.float64)
+    t32 = t.astype(np.float32)
+    assert np.all((t32.astype(np.float64) == t) | (t < 2.0 ** -12))
+    x = torch.from_numpy(t32)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy() & 0x7F
+
+
+def test_e4m3_rounding_matches_torch_random():
+    rng = np.random.default_rng(123)
+    t = np.concatenate([rng.uniform(0, 448, 4000), rng.uniform(0, 1e-2, 2000),
+                        np.exp(rng.uniform(-12, math.log(448), 4000))]).astype(np.float32)
+    ours = np.array([oracle.e4m3_round_code(v) for v in t])
+    assert np.array_equal(ours, _torch_e4m3_code(t))
+
+
+def test_e4m3_rounding_all_midpoints_and_values():
+    table = oracle.e4m3_table()
+    mids = ((table[:-1] + table[1:]) / 2).astype(np.float32)   # exact in float32
+    pts = np.concatenate([table.astype(np.float32), mids, np.nextafter(mids, np.float32(0)),
+                          np.nextafter(mids, np.float32(1000))])
+    ours = np.array([oracle.e4m3_round_code(v) for v in pts])
+    assert np.array_equal(ours, _torch_e4m3_code(pts))
+    # saturation: everything above 448 maps to the largest finite code
+    for v in (448.0, 448.0001, 463.99, 464.0, 480.0, 1e6):
+        assert oracle.e4m3_round_code(v) == 0x7E
+
+
+def test_quantize_exhaustive_bf16_against_torch():
+    """Every finite bf16 pattern, placed in blocks with a known amax, quantises
+    exactly as torch's float8 conversion of v * 2^-e (in range)."""
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.bf16_bits_to_f64(bits)
+    finite = np.isfinite(vals)
+    bits, vals = bits[finite], vals[finite]
+    for amax_exp in (-130, -60, -8, 0, 5, 40, 120):
+        # each block: 31 arbitrary entries no larger than amax plus amax itself
+        amax = 2.0 ** amax_exp * 1.5
+        ok = np.abs(vals) <= amax
+        sel = vals[ok]
+        n = (len(sel) // 31) * 31
+        blocks = sel[:n].reshape(-1, 31)
+        blocks = np.concatenate([blocks, np.full((blocks.shape[0], 1), amax)], axis=1)
+        codes, scales = oracle.quantize_f64(blocks)
+        e = oracle.block_exponent(amax)
+        assert np.all(scales == e + 127)
+        t = np.abs(blocks) * 2.0 ** (-e)
+        expect = _torch_e4m3_code(np.minimum(t, 448.0)) | np.where(np.signbit(blocks), 0x80, 0)
+        assert np.array_equal(codes, expect.astype(np.uint8)), amax_exp
+
+
+# ------------------------------------------------------------------ worked examples
+def _parse_worked():
+    out = []
+    with open(os.path.join(GOLDEN, "mx_worked_examples.txt")) as f:
+        for line in f:
+            if line.startswith("#") or "|" not in line:
+                continue
+            head, body = line.split("|")
+            entries = []
+            for tok in body.split():
+                v, c = tok.split("=")
+                entries.append((float.fromhex(v), int(c, 16)))
+            out.append((int(head.strip(), 16), entries))
+    return out
+
+
+def test_worked_examples():
+    cases = _parse_worked()
+    assert len(cases) >= 7
+    for scale_byte, entries in cases:
+        block = np.zeros((1, 32))
+        for i, (v, _) in enumerate(entries):
+            block[0, i] = v
+        codes, scales = oracle.quantize_f64(block)
+        assert scales[0, 0] == scale_byte, (scale_byte, entries)
+        for i, (_, c) in enumerate(entries):
+            assert codes[0, i] == c, (i, entries[i], hex(codes[0, i]))
+        assert np.all(codes[0, len(entries):] == 0)
+
+
+# ------------------------------------------------------------------ closed forms
+@pytest.mark.parametrize("a", [-120, -20, -3, 0, 7, 60, 127])
+def test_power_of_two_block_round_trips(a):
+    """amax = 2^a gives scale byte a - 8 + 127 (clamped); every value that is
+    E4M3-representable after scaling by 2^(8-a) survives quantise/dequantise."""
+    e = max(-127, a - 8)
+    vals = [2.0 ** a]
+    for k in range(a - 14, a + 1):          # normal range after scaling: 3 mantissa bits
+        for m in range(8):
+            v = (1 + m / 8) * 2.0 ** k
+            if v <= 2.0 ** a and k - e >= -6:
+                vals.append(v)
+    for k in range(a - 17, a - 14):         # subnormal range: multiples of 2^-9 after scaling
+        if k - e >= -9:
+            vals.append(2.0 ** k)
+    vals = np.array(vals)
+    n = (len(vals) + 31) // 32 * 32
+    blocks = np.zeros(n)
+    blocks[:len(vals)] = vals
+    blocks = blocks.reshape(-1, 32)
+    blocks[:, 0] = 2.0 ** a                    # every block carries the amax
+    codes, scales = oracle.quantize_f64(blocks)
+    assert np.all(scales == e + 127)
+    assert np.array_equal(oracle.dequantize(codes, scales), blocks)
+
+
+def test_zero_blocks_and_negative_zero():
+    block = np.zeros((2, 32))
+    block[1, ::2] = -0.0
+    codes, scales = oracle.quantize_f64(block)
+    assert np.all(scales == 0)
+    assert np.all(codes[0] == 0)
+    assert np.all(codes[1, ::2] == 0x80) and np.all(codes[1, 1::2] == 0)
+    assert np.all(oracle.dequantize(codes, scales) == 0)
+
+
+@pytest.mark.parametrize("a", [-50, 0, 13])
+def test_single_outlier_saturates(a):
+    block = np.full((1, 32), 2.0 ** (a - 6))
+    block[0, 5] = 1.9 * 2.0 ** a
+    codes, scales = oracle.quantize_f64(block)
+    assert scales[0, 0] == a - 8 + 127
+    assert codes[0, 5] == 0x7E                 # 1.9 * 2^8 = 486.4 > 448
+    assert oracle.dequantize(codes, scales)[0, 5] == 448.0 * 2.0 ** (a - 8)
+    # the others: 2^(a-6) * 2^(8-a) = 4 = 2^2 -> E = 9, m = 0 -> code 0x48
+    assert np.all(np.delete(codes[0], 5) == 0x48)
+
+
+def test_block_exponent_closed_form():
+    rng = np.random.default_rng(5)
+    for amax in np.exp(rng.uniform(-80, 80, 500)):
+        e = oracle.block_exponent(amax)
+        assert 2.0 ** (e + 8) <= amax < 2.0 ** (e + 9)
+    assert oracle.block_exponent(0.0) == -127
+    assert oracle.block_exponent(2.0 ** -140) == -127
+    assert oracle.block_exponent(5e-324) == -127
+
+
+# ------------------------------------------------------------------ GEMM, exact
+def _exact_value(code: int, scale: int) -> Fraction:
+    """Exact rational value of an MXFP8 element, decoded from the bits here."""
+    E, m = (code >> 3) & 0xF, code & 7
+    mag = Fraction(m, 8) * Fraction(2) ** -6 if E == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (E - 7)
+    mag *= Fraction(2) ** (scale - 127)
+    return -mag if code & 0x80 else mag
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 3, 32), (2, 4, 64), (4, 2, 128), (3, 5, 96)])
+def test_gemm_exact_rational(M, N, K):
+    rng = np.random.default_rng(M * 100 + N * 10 + K)
+    a = inputs.bf16_bits_from_f32(rng.standard_normal((M, K)).astype(np.float32))
+    b = inputs.bf16_bits_from_f32((rng.standard_normal((N, K)) * 0.1).astype(np.float32))
+    bc, bs = oracle.quantize_bf16(b)
+    res = oracle.gemm(a, bc, bs)
+    ac, as_ = res["a_codes"], res["a_scales"]
+    for i in range(M):
+        for j in range(N):
+            s = sum(_exact_value(int(ac[i, k]), int(as_[i, k // 32])) *
+                    _exact_value(int(bc[j, k]), int(bs[j, k // 32])) for k in range(K))
+            assert res["c"][i, j] == float(s)
+
+
+# ------------------------------------------------------------------ SiLU
+def test_silu_matches_torch():
+    g = np.concatenate([np.linspace(-40, 40, 2001), [-800.0, 800.0, 0.0, -0.0]])
+    ref = torch.nn.functional.silu(torch.from_numpy(g)).numpy()
+    ours = oracle.silu(g)
+    np.testing.assert_allclose(ours, ref, rtol=1e-15, atol=1e-300)
+
+
+# ------------------------------------------------------------------ bf16 rounding
+def test_round_bf16_matches_torch_on_float32_inputs():
+    rng = np.random.default_rng(9)
+    f = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.uniform(-30, 30, 20000),
+                        [0.0, -0.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8]]).astype(np.float32)
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.round_bf16_bits(f.astype(np.float64)), ref)
+
+
+def test_round_bf16_single_rounding():
+    # 1 + 2^-8 + 2^-30: just above the bf16 midpoint between 1 and 1 + 2^-7.
+    # Rounding directly gives 1 + 2^-7; going through float32 first would drop
+    # the 2^-30, land on the midpoint and round to 1.
+    y = np.array([1.0 + 2.0 ** -8 + 2.0 ** -30, -(1.0 + 2.0 ** -8 + 2.0 ** -30)])
+    got = oracle.bf16_bits_to_f64(oracle.round_bf16_bits(y))
+    assert got[0] == 1.0 + 2.0 ** -7 and got[1] == -(1.0 + 2.0 ** -7)
+
+
+# ------------------------------------------------------------------ scale layout
+def test_tiled_layout_worked_offsets():
+    rows, K = 256, 256
+    sc = np.zeros((rows, K // 32), np.uint8)
+    with open(os.path.join(GOLDEN, "tiled_scale_layout_examples.txt")) as f:
+        pts = [tuple(int(t) for t in line.split()) for line in f
+               if line.strip() and not line.startswith("#")]
+    for n, (r, kb, off) in enumerate(pts):
+        sc[r, kb] = n + 1
+    tiled = oracle.scales_rowmajor_to_tiled(sc)
+    assert tiled.size == oracle.tiled_scale_bytes(rows, K) == 2 * 2 * 512
+    for n, (r, kb, off) in enumerate(pts):
+        assert tiled[off] == n + 1, (r, kb, off)
+
+
+def test_tiled_layout_is_a_permutation():
+    rows, K = 384, 512
+    sc = np.arange(rows * (K // 32), dtype=np.int64).reshape(rows, K // 32)
+    tiled = oracle.mx_oracle._tiled_offsets(rows, K // 32)
+    assert len(np.unique(tiled)) == tiled.size == oracle.tiled_scale_bytes(rows, K)
+    # each 512-byte tile holds one 128-row x 4-block patch
+    tile_of = tiled // 512
+    for rt in range(3):
+        for kg in range(4):
+            patch = tile_of[rt * 128:(rt + 1) * 128, kg * 4:(kg + 1) * 4]
+            assert np.all(patch == rt * 4 + kg)
+    rm = (sc % 251).astype(np.uint8)
+    back = oracle.scales_tiled_to_rowmajor(oracle.scales_rowmajor_to_tiled(rm), rows, K)
+    assert np.array_equal(back, rm)
+
+
+# ------------------------------------------------------------------ the MLP, rebuilt from torch
+def _torch_mx_qdq(v: torch.Tensor) -> torch.Tensor:
+    """MXFP8 quantise/dequantise from torch pieces: the block exponent from
+    torch.frexp, the element rounding from torch's float8_e4m3fn conversion
+    (saturation applied first, as the MX rule saturates)."""
+    rows, K = v.shape
+    blk = v.reshape(rows, K // 32, 32)
+    amax = blk.abs().amax(dim=-1, keepdim=True)
+    _, ex = torch.frexp(amax)
+    e = torch.where(amax == 0, torch.full_like(ex, -127), (ex - 1 - 8).clamp(-127, 127))
+    scale = torch.ldexp(torch.ones_like(amax), e.to(torch.float64))
+    t = (blk / scale).clamp(-448.0, 448.0)
+    q = t.to(torch.float8_e4m3fn).to(torch.float64)
+    return (q * scale).reshape(rows, K)
+
+
+def _torch_mlp(x, wg, wu, wd, quantize=True):
+    qd = _torch_mx_qdq if quantize else (lambda a: a)
+    xq, wgq, wuq, wdq = qd(x), qd(wg), qd(wu), qd(wd)
+    g = xq @ wgq.T
+    u = xq @ wuq.T
+    h = torch.nn.functional.silu(g) * u
+    return qd(h) @ wdq.T, h
+
+
+def _small_layer(M=5, H=256, I=384, seed=11, **kw):
+    wl = inputs.make_workload_small("t", M, H, I, seed, **kw)
+    x = inputs.make_activations(wl)
+    wg, wu, wd = inputs.make_layer(wl, 0)
+    return x, wg, wu, wd
+
+
+def _f64(bits):
+    return torch.from_numpy(oracle.bf16_bits_to_f64(bits))
+
+
+@pytest.mark.parametrize("kw", [{}, {"zero_block_frac": 0.05}, {"token_scale_log10": (-2.0, 2.0)}])
+def test_mlp_matches_torch_rebuild(kw):
+    x, wg, wu, wd = _small_layer(**kw)
+    qw = oracle.quantize_weights(wg, wu, wd)
+    res = oracle.swiglu_mlp(x, qw)
+    y_t, h_t = _torch_mlp(_f64(x), _f64(wg), _f64(wu), _f64(wd))
+    np.testing.assert_allclose(res["h"], h_t.numpy(), rtol=1e-12, atol=1e-300)
+    assert oracle.rel_l2(res["y"], y_t.numpy()) < 1e-12
+    # y_bf16 is the single rounding of y
+    assert np.array_equal(res["y_bf16"], oracle.round_bf16_bits(y_t.numpy()))
+
+
+def test_mlp_quantisation_error_band():
+    """rel-L2 of the quantised MLP against the unquantised fp64 SwiGLU MLP lies
+    within 2x of the estimate built from each tensor's own round-trip error."""
+    x, wg, wu, wd = _small_layer(M=16, H=512, I=1024, seed=3)
+    qw = oracle.quantize_weights(wg, wu, wd)
+    res = oracle.swiglu_mlp(x, qw)
+    xf, wgf, wuf, wdf = (_f64(a) for a in (x, wg, wu, wd))
+    y_ref, h_ref = _torch_mlp(xf, wgf, wuf, wdf, quantize=False)
+    rt = lambda a: oracle.rel_l2(oracle.quant_dequant(a.numpy()), a.numpy())
+    ex, eg, eu, ed, eh = rt(xf), rt(wgf), rt(wuf), rt(wdf), rt(h_ref)
+    est = math.sqrt(2 * ex ** 2 + eg ** 2 + eu ** 2 + eh ** 2 + ed ** 2)
+    got = oracle.rel_l2(res["y"], y_ref.numpy())
+    assert 0.5 * est < got < 2.0 * est, (got, est)
+    assert 0.01 < got < 0.2
+
+
+def test_oracle_is_deterministic():
+    x, wg, wu, wd = _small_layer(seed=4)
+    a = oracle.swiglu_mlp(x, oracle.quantize_weights(wg, wu, wd))
+    b = oracle.swiglu_mlp(x, oracle.quantize_weights(wg, wu, wd))
+    assert np.array_equal(a["y_bf16"], b["y_bf16"]) and np.array_equal(a["h_codes"], b["h_codes"])
+
+
+def test_sampled_rows_equal_full():
+    x, wg, wu, wd = _small_layer(seed=6)
+    qw = oracle.quantize_weights(wg, wu, wd)
+    full = oracle.swiglu_mlp(x, qw)
+    rows = np.array([0, 7, 100, 255])
+    part = oracle.swiglu_mlp(x, qw, rows_down=rows)
+    assert np.array_equal(part["y_bf16"], full["y_bf16"][:, rows])
+
+
+# ------------------------------------------------------------------ planted mistakes
+def _pin_error(y_candidate, x, wg, wu, wd):
+    y_t, _ = _torch_mlp(_f64(x), _f64(wg), _f64(wu), _f64(wd))
+    return oracle.rel_l2(y_candidate, y_t.numpy())
+
+
+@pytest.mark.parametrize("mistake", ["swap_gate_up", "skip_h_requant", "scale_rule_minus7",
+                                     "transpose_down", "scale_layout"])
+def test_planted_mistakes_are_caught(mistake):
+    """Each plausible oracle bug, planted here on the CPU, breaks the torch
+    rebuild pin by far more than its 1e-12 tolerance."""
+    x, wg, wu, wd = _small_layer(M=4, H=256, I=256, seed=8)
+    qw = oracle.quantize_weights(wg, wu, wd)
+    I = wg.shape[0]
+    xd = oracle.dequantize(*oracle.quantize_bf16(x))
+    wgu = oracle.dequantize(qw["gateup_codes"], qw["gateup_scales"])
+    wdd = oracle.dequantize(qw["down_codes"], qw["down_scales"])
+    g, u = xd @ wgu[:I].T, xd @ wgu[I:].T
+    if mistake == "swap_gate_up":
+        g, u = u, g
+    h = oracle.silu(g) * u
+    hd = h if mistake == "skip_h_requant" else oracle.quant_dequant(h)
+    if mistake == "scale_rule_minus7":
+        c, s = oracle.quantize_f64(h)
+        hd = oracle.dequantize(c, (s.astype(np.int64) + 1).astype(np.uint8))
+    if mistake == "transpose_down":
+        wdd = wdd.T
+    if mistake == "scale_layout":
+        # scales read in the tiled order as if they were row-major (the pages' bug)
+        tiled = oracle.scales_rowmajor_to_tiled(qw["down_scales"])
+        wrong = tiled[: qw["down_scales"].size].reshape(qw["down_scales"].shape)
+        wdd = oracle.dequantize(qw["down_codes"], wrong)
+    y = hd @ wdd.T
+    assert _pin_error(y, x, wg, wu, wd) > 1e-3
