@@ -1,0 +1,438 @@
+"""Benchmark of the fused MXFP8 SwiGLU MLP on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload m16] [--no-sweep]
+
+One step = one call of the hot path (quantise x, gate/up block-scaled GEMM,
+SiLU(g) * u, requantise, down GEMM) on one batch of M tokens of the workload.
+The headline workload is m16 (M = 16, H = 2560, I = 9728, one layer).  Weights
+are rotated over enough quantised copies that every call streams its weights
+from HBM (the copies together exceed twice the 129 MB L2).  Rank 0 prints ONE
+JSON line.
+
+Multi-GPU: replicas only -- every rank runs its own copy of the workload, no
+collective on the data path; the ranks only meet at the timing barrier and the
+max-over-ranks of the elapsed time.
+
+--impl reference times the CPU oracle (fp64, the test infrastructure) on the
+host cores instead, on the same workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MXFP8 SwiGLU MLP tokens/s and HBM GB/s (% roofline) at M=1/16/64/128"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(M, H, I):
+    """Codes + scales of the three weight matrices, x read, y written."""
+    return 3 * H * I + 3 * H * I // 32 + 2 * M * H + 2 * M * H
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples with host timestamps."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((ts, float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            flags = r[3][1:5]
+            for n, v in zip(names, flags):
+                if v.strip().lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ---------------------------------------------------------------- GPU workload
+class MlpBench:
+    def __init__(self, fs, wl, M, device, seed_layers=None, use_numpy=False):
+        import numpy as np
+        import torch
+
+        from workloads import inputs
+
+        self.fs, self.M, self.H, self.I = fs, M, wl.H, wl.I
+        per_layer = wl.weight_bytes
+        n_layers = wl.layers
+        copies = max(n_layers, -(-2 * L2_BYTES // per_layer) + 1)
+        self.weights = []
+        for c in range(copies):
+            layer = c % n_layers
+            if use_numpy:
+                wg, wu, wd = (torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).to(device).view(torch.bfloat16)
+                              for b in inputs.make_layer(wl, layer))
+            else:
+                wg, wu, wd = inputs.make_layer_torch(wl, layer, device)
+            self.weights.append(fs.prepare_mlp_weights(wg, wu, wd))
+            del wg, wu, wd
+        if use_numpy:
+            xb = inputs.make_activations(wl, M)
+            self.x = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).to(device).view(torch.bfloat16)
+        else:
+            self.x = inputs.make_activations_torch(wl, M, device)
+        self.y = torch.empty((M, self.H), dtype=torch.bfloat16, device=device)
+        self.ws = fs.Workspace(M, self.H, self.I, device=device)
+        self.copies = copies
+        torch.cuda.synchronize()
+
+    def call(self, i, fused=True, stream=None, x=None, y=None):
+        w = self.weights[i % self.copies]
+        f = self.fs.fsops_mxfp8_swiglu_mlp if fused else self.fs.fsops_mxfp8_swiglu_mlp_unfused
+        f(self.x if x is None else x, w.gateup_codes, w.down_codes, w.scales, self.y if y is None else y,
+          self.M, self.H, self.I, stream)
+
+    def capture(self, nsteps, fused, stream, start=0):
+        import torch
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(nsteps):
+                self.call(start + i, fused, stream)
+        return g
+
+    def timed(self, steps, fused, warmup, stream, chunk=256):
+        """Device time of exactly `steps` calls (graph replays), in seconds."""
+        import torch
+
+        chunk = max(self.copies, (min(chunk, steps) // self.copies) * self.copies) if steps >= self.copies else steps
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                self.call(i, fused, stream)
+            g_main = self.capture(chunk, fused, stream) if steps >= chunk else None
+            rem = steps - (steps // chunk) * chunk if g_main is not None else steps
+            g_rem = self.capture(rem, fused, stream) if rem > 0 else None
+            g_main and g_main.replay()
+            g_rem and g_rem.replay()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            t_host0 = time.time()
+            e0.record(stream)
+            for _ in range(steps // chunk if g_main is not None else 0):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            e1.record(stream)
+            e1.synchronize()
+            t_host1 = time.time()
+        return e0.elapsed_time(e1) / 1e3, (t_host0, t_host1)
+
+    def per_launch(self, n, stream):
+        """Mean duration of single fused launches, each bracketed by events on its stream."""
+        import torch
+
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for i, (a, b) in enumerate(evs):
+                a.record(stream)
+                self.call(i, True, stream)
+                b.record(stream)
+        stream.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
+
+    def e2e(self, steps, warmup, stream):
+        """Through the public API with host buffers: H2D x, the call, D2H y, every step."""
+        import torch
+
+        x_host = torch.empty_like(self.x, device="cpu").pin_memory()
+        x_host.copy_(self.x.cpu())
+        y_host = torch.empty_like(self.y, device="cpu").pin_memory()
+        x_dev = torch.empty_like(self.x)
+        with torch.cuda.stream(stream):
+            for i in range(warmup + steps):
+                if i == warmup:
+                    stream.synchronize()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                x_dev.copy_(x_host, non_blocking=True)
+                self.call(i, True, stream, x=x_dev)
+                y_host.copy_(self.y, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+        nbytes = self.x.numel() * 2
+        return e0.elapsed_time(e1) / 1e3, nbytes, self.y.numel() * 2
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import mxfp8_swiglu_mlp_gb300 as fs
+    from workloads import inputs
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(device=device)
+    hbm_peak, peak_kind = peaks()
+    wl = inputs.WORKLOADS[args.workload]
+    M, H, I = wl.M, wl.H, wl.I
+    B = algorithmic_bytes(M, H, I)
+
+    bench = MlpBench(fs, wl, M, device, use_numpy=False)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    dt, (h0, h1) = bench.timed(args.steps, True, args.warmup, stream)
+    if world > 1:
+        t = torch.tensor([dt], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+        torch.distributed.barrier()
+    time.sleep(0.1)
+    sampler.stop()
+    clocks = sampler.summary(h0, h1)
+
+    t_launch = bench.per_launch(min(args.steps, 200), stream)
+    ms_per_step = dt / args.steps * 1e3
+    value = world * M * args.steps / dt
+    achieved = B / t_launch / 1e9
+
+    n_e2e = min(args.steps, 5000)
+    e2e_t, h2d, d2h = bench.e2e(n_e2e, args.warmup, stream)
+    e2e_val = world * M * n_e2e / e2e_t
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": "%s: fused MXFP8 SwiGLU MLP, M=%d, H=%d, I=%d, one layer per step" % (wl.name, M, H, I),
+                   "M": M, "H": H, "I": I, "weight_copies_rotated": bench.copies,
+                   "l2": "inputs larger than L2: %d rotated weight copies, %.0f MB" %
+                         (bench.copies, bench.copies * wl.weight_bytes / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "timing": "CUDA graph replays of exactly `steps` calls, CUDA events on the launching stream"},
+        "weight_GBps": round(value / world / M * wl.weight_bytes / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "mx_persistent_kernel (fused MLP)", "bytes_per_launch": B,
+                     "launch_us": round(t_launch * 1e6, 3)},
+        "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "api": "fsops_mxfp8_swiglu_mlp via ctypes, pinned host buffers"},
+        "gpu_launches": args.steps,
+        "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+    }
+    if rank == 0 and not args.no_sweep:
+        out["sweep"] = sweep(fs, device, stream, hbm_peak, args)
+    if rank == 0 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(wl)
+    del bench
+    return out
+
+
+def sweep(fs, device, stream, hbm_peak, args):
+    """Fused and three-launch numbers at M = 1, 16, 64, 128 (the metric's points)."""
+    import torch
+
+    from workloads import inputs
+
+    res = {}
+    for name in ("m1", "m16", "m64", "m128"):
+        wl = inputs.WORKLOADS[name]
+        b = MlpBench(fs, wl, wl.M, device)
+        B = algorithmic_bytes(wl.M, wl.H, wl.I)
+        n = max(64, min(4096, int(0.25 / (B / hbm_peak / 1e9 * 1.5))))
+        n = (n // b.copies + 1) * b.copies
+        entry = {"M": wl.M, "H": wl.H, "I": wl.I, "layers": wl.layers, "copies": b.copies, "steps": n}
+        for fused in (True, False):
+            dt, _ = b.timed(n, fused, 5, stream)
+            t = dt / n
+            key = "fused" if fused else "unfused_3_launches"
+            entry[key] = {"tokens_per_s": round(wl.M / t, 1), "us_per_call": round(t * 1e6, 3),
+                          "GBps": round(B / t / 1e9, 1), "frac_hbm": round(B / t / 1e9 / hbm_peak, 4)}
+        tl = b.per_launch(min(n, 200), stream)
+        entry["fused"]["launch_us"] = round(tl * 1e6, 3)
+        entry["fused"]["launch_frac_hbm"] = round(B / tl / 1e9 / hbm_peak, 4)
+        fl = 2.0 * wl.M * 3 * wl.H * wl.I
+        entry["fused"]["tensor_TFLOPs"] = round(fl / tl / 1e12, 1)
+        res[name] = entry
+        del b
+        torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline(wl):
+    """The oracle as it stands, timed on this host on one full layer of the workload."""
+    import numpy as np
+
+    import oracle
+    from workloads import inputs
+
+    x = inputs.make_activations(wl)
+    wg, wu, wd = inputs.make_layer(wl, 0)
+    qw = oracle.quantize_weights(wg, wu, wd)
+    t0 = time.time()
+    reps = 0
+    while True:
+        oracle.swiglu_mlp(x, qw)
+        reps += 1
+        if time.time() - t0 > 8.0 or reps >= 20:
+            break
+    dt = (time.time() - t0) / reps
+    return {"value": round(wl.M / dt, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "%d full %s layer(s) (M=%d tokens each): x quantisation, weight dequantisation, "
+                      "fp64 GEMMs, SiLU, requantisation; %.2f s per layer" % (reps, wl.name, wl.M, dt)}
+
+
+def _slice_layer(qw, I, s):
+    """Oracle inputs for the first s intermediate features of a layer."""
+    return {"gateup_codes": __import__("numpy").concatenate([qw["gateup_codes"][:s], qw["gateup_codes"][I:I + s]]),
+            "gateup_scales": __import__("numpy").concatenate([qw["gateup_scales"][:s], qw["gateup_scales"][I:I + s]]),
+            "down_codes": qw["down_codes"][:, :s].copy(), "down_scales": qw["down_scales"][:, :s // 32].copy()}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm (rank 0 only).
+
+    Each step is a bounded sample of the workload: a full layer if K + W full
+    layers fit in about two minutes, otherwise the layer restricted to its
+    first s intermediate features (s a multiple of 128), with tokens/s scaled
+    by s / I (the fraction of the layer's work a step does)."""
+    import oracle
+    from workloads import inputs
+
+    if rank != 0:
+        return None
+    wl = inputs.WORKLOADS[args.workload]
+    x = inputs.make_activations(wl)
+    wg, wu, wd = inputs.make_layer(wl, 0)
+    qw = oracle.quantize_weights(wg, wu, wd)
+    t0 = time.time()
+    oracle.swiglu_mlp(x, qw)
+    t_full = time.time() - t0
+    budget = 120.0
+    s = wl.I
+    if (args.steps + args.warmup) * t_full > budget:
+        s = int(wl.I * budget / ((args.steps + args.warmup) * t_full)) // 128 * 128
+        s = max(128, min(wl.I, s))
+    sample = qw if s == wl.I else _slice_layer(qw, wl.I, s)
+    for _ in range(args.warmup):
+        oracle.swiglu_mlp(x, sample)
+    t0 = time.time()
+    for _ in range(args.steps):
+        oracle.swiglu_mlp(x, sample)
+    dt = time.time() - t0
+    value = wl.M * (s / wl.I) * args.steps / dt
+    desc = ("one full %s layer" % wl.name) if s == wl.I else (
+        "the %s layer restricted to its first %d of %d intermediate features (tokens/s scaled by %d/%d)" %
+        (wl.name, s, wl.I, s, wl.I))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "%s: MXFP8 SwiGLU MLP, M=%d, H=%d, I=%d, one layer per step" % (wl.name, wl.M, wl.H,
+                                                                                              wl.I),
+                   "M": wl.M, "H": wl.H, "I": wl.I},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": "each step: " + desc + " through the fp64 oracle"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="m16")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        import torch
+
+        torch.distributed.init_process_group("nccl")
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

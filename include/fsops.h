@@ -1,0 +1,209 @@
+/*
+ * fsops.h -- C ABI of the GB300 (sm_103a) MXFP8 SwiGLU MLP library.
+ *
+ * The operation (Fish Audio, "How we made our TTS API free: the inference
+ * engineering behind S2.1 Pro", and its copy on X, "We Made Our Best Voice
+ * Model Free"): the feed-forward block of an autoregressive decoder at decode
+ * shapes (M <= 128 tokens per step; X copy, "The GPU problem you're paying
+ * for"), a SwiGLU MLP -- gate/up projection, SiLU(gate) * up, down projection
+ * (X copy, "Custom kernels for the shapes TTS actually uses"; p2, "Por que
+ * cuBLAS no era suficiente") -- computed on MXFP8 operands: OCP E4M3 elements
+ * with one UE8M0 power-of-two scale per 32 consecutive elements along K (p2,
+ * "Estrategia de cuantizacion FP8").  The fused entry point keeps the
+ * intermediate on chip / in L2 instead of the bf16 round trip through HBM
+ * that separate launches make (p2, "Resultados de benchmark del kernel").
+ *
+ * Quantisation rule (OCP MX): per 32-block, e = floor(log2(amax)) - 8 clamped
+ * to [-127, 127] (amax == 0 gives e = -127); scale byte = e + 127; element =
+ * E4M3 round-to-nearest-even of v * 2^-e, magnitudes above 448 saturate to
+ * 448, sign kept (a negative value that rounds to zero is code 0x80).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *     aligned.  The library never allocates, frees or synchronises inside a
+ *     compute call; calls are asynchronous on `stream` (a cudaStream_t, NULL =
+ *     legacy default stream) and may be captured in a CUDA graph.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     rejected call launches nothing and touches no device memory.
+ *   - Matrices are row-major.  Weights are [rows, K] with K contiguous
+ *     (K-major); activations are [M, K].
+ *   - Inputs must be finite; NaN or Inf inputs give unspecified results.
+ *   - No C++ exception crosses this interface.
+ *
+ * Scale layouts (fsops_scale_layout):
+ *   FSOPS_SCALES_ROWMAJOR: [rows, K/32] bytes, block index fastest.
+ *   FSOPS_SCALES_TCGEN05:  the layout the tcgen05 block-scaled MMA reads.
+ *     Rows are grouped in tiles of 128 and K-blocks in groups of 4; each
+ *     (row tile rt, group kg) is 512 contiguous bytes at offset
+ *     (rt * (K/128) + kg) * 512, and entry (r, kb) sits at
+ *     (r % 32) * 16 + ((r % 128) / 32) * 4 + (kb % 4) inside it.  Rows past
+ *     the end of the matrix inside the last tile are padding (byte 0).
+ *     K must be a multiple of 128.  Buffer size: fsops_scale_bytes().
+ *   Scales handed to the GEMM and MLP entry points must be in the TCGEN05
+ *   layout.  Handing over another layout is not detected; it silently gives
+ *   wrong numbers at normal speed (the failure the Fish Audio post describes
+ *   for its own scale-layout bug, p2 "Estrategia de cuantizacion FP8").
+ */
+#ifndef FSOPS_H
+#define FSOPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FSOPS_OK = 0,
+  FSOPS_ERR_INVALID_ARG = 1,      /* null pointer, bad enum, missing or too small workspace */
+  FSOPS_ERR_UNSUPPORTED_SHAPE = 2,/* a size outside the documented limits */
+  FSOPS_ERR_MISALIGNED = 3,       /* a pointer that is not 16-byte aligned */
+  FSOPS_ERR_CUDA = 4,             /* a CUDA runtime call or a launch failed */
+  FSOPS_ERR_TIMEOUT = 5,          /* a kernel wait ran out (read with fsops_read_kernel_status) */
+  FSOPS_ERR_NO_DEVICE = 6         /* the current device is not an sm_100-class GPU */
+} fsops_status;
+
+typedef enum { FSOPS_SCALES_ROWMAJOR = 0, FSOPS_SCALES_TCGEN05 = 1 } fsops_scale_layout;
+
+typedef enum { FSOPS_DTYPE_BF16 = 0, FSOPS_DTYPE_F32 = 1, FSOPS_DTYPE_MXFP8 = 2 } fsops_dtype;
+
+/* Scales of the two MLP weights, both in the FSOPS_SCALES_TCGEN05 layout. */
+typedef struct {
+  const uint8_t* gateup; /* of W_gateup [2I, H] */
+  const uint8_t* down;   /* of W_down [H, I] */
+} fsops_mlp_scales;
+
+/* ------------------------------------------------------------------------
+ * fsops_quantize_mxfp8 -- bf16 -> MXFP8 (activation quantisation and scale
+ * packing in one launch: the first of the two fused kernels in p2,
+ * "Resultados de benchmark del kernel"; also the offline weight quantiser).
+ *   x_bf16  [rows, ld] bf16, the first K columns are quantised; ld % 8 == 0.
+ *   codes   [rows, K] E4M3 bytes (row stride K).
+ *   scales  UE8M0 bytes in `layout`; fsops_scale_bytes(rows, K, layout) bytes.
+ *   rows >= 0 (0 is a no-op), K % 32 == 0 (ROWMAJOR) or K % 128 == 0 (TCGEN05),
+ *   rows * K < 2^31.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
+ */
+fsops_status fsops_quantize_mxfp8(const void* x_bf16, int rows, int K, int ld, uint8_t* codes,
+                                  uint8_t* scales, fsops_scale_layout layout, void* stream);
+
+/* Size in bytes of a scale buffer for a [rows, K] matrix (0 for an invalid layout). */
+size_t fsops_scale_bytes(int rows, int K, fsops_scale_layout layout);
+
+/* ------------------------------------------------------------------------
+ * fsops_mxfp8_gemm -- C[M, N] = A^[M, K] * B^[N, K]^T, the block-scaled
+ * MXFP8 GEMM (p2 "Estrategia de cuantizacion FP8": mxfp8 1x32; the raw linear
+ * that reads MXFP8 weights with a fixed scale stride).  A is bf16 and is
+ * quantised inside the same launch; B is MXFP8 (codes + TCGEN05 scales);
+ * C is bf16 (round-to-nearest-even of the fp32 accumulation).
+ *   1 <= M <= 128; N % 128 == 0; K % 128 == 0; N, K <= 65536.
+ *   workspace: device scratch of at least fsops_gemm_workspace_bytes(M, N, K)
+ *   bytes, all zero before its first use.  A successful call leaves its
+ *   counters and split-K accumulators zero again, so the same workspace can be
+ *   reused without clearing; after a call that reported an error (see
+ *   fsops_read_kernel_status) zero it again.  One call at a time per
+ *   workspace: calls that share a workspace must be ordered (same stream).
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
+ */
+fsops_status fsops_mxfp8_gemm(const void* a_bf16, const uint8_t* b_codes, const uint8_t* b_scales,
+                              void* c_bf16, int M, int N, int K, void* workspace, size_t ws_bytes,
+                              void* stream);
+
+/* General form of fsops_mxfp8_gemm.
+ *   a_dtype FSOPS_DTYPE_BF16: `a` is bf16 [M, K], quantised in-kernel, a_scales must be NULL.
+ *   a_dtype FSOPS_DTYPE_MXFP8: `a` is E4M3 codes [M, K], a_scales its TCGEN05
+ *     scales (K/128 tiles of 512 bytes, rows past M are ignored).
+ *   c_dtype FSOPS_DTYPE_BF16 or FSOPS_DTYPE_F32.  Other limits as above.
+ */
+fsops_status fsops_mxfp8_gemm_ex(const void* a, const uint8_t* a_scales, fsops_dtype a_dtype,
+                                 const uint8_t* b_codes, const uint8_t* b_scales, void* c,
+                                 fsops_dtype c_dtype, int M, int N, int K, void* workspace,
+                                 size_t ws_bytes, void* stream);
+
+size_t fsops_gemm_workspace_bytes(int M, int N, int K);
+
+/* ------------------------------------------------------------------------
+ * fsops_swiglu_quantize_mxfp8 -- h = SiLU(g) * u, requantised to MXFP8 along
+ * I (the second fused kernel of p2 "Resultados de benchmark del kernel": the
+ * SwiGLU prologue inside the down GEMM's activation quantisation).
+ *   gu      [M, 2I] fp32 in the paired order of W_gateup's rows: columns
+ *           128j..128j+63 are gate features 64j..64j+63, columns
+ *           128j+64..128j+127 the up features 64j..64j+63 (this is what
+ *           fsops_mxfp8_gemm_ex writes for A = x and B = W_gateup).
+ *   h_codes [M, I] E4M3;  h_scales TCGEN05 layout, I/128 tiles of 512 bytes.
+ *   1 <= M <= 128, I % 128 == 0.
+ */
+fsops_status fsops_swiglu_quantize_mxfp8(const float* gu, int M, int I, uint8_t* h_codes,
+                                         uint8_t* h_scales, void* stream);
+
+/* ------------------------------------------------------------------------
+ * fsops_mxfp8_swiglu_mlp -- the whole block in ONE launch:
+ *   x^ = MXFP8(x);  g = x^ Wg^T, u = x^ Wu^T (fp32 accumulate);
+ *   h = SiLU(g) * u (fp32);  h^ = MXFP8(h) along I;  y = bf16(h^ Wd^T).
+ *   x_bf16   [M, H] bf16.
+ *   w_gateup [2I, H] E4M3, W_gate and W_up paired in blocks of 64 rows:
+ *            rows 128j..128j+63 are W_gate rows 64j..64j+63 and rows
+ *            128j+64..128j+127 are W_up rows 64j..64j+63 (so one 128-row tile
+ *            and its 512-byte scale tile hold a gate/up pair).
+ *   w_down   [H, I] E4M3.
+ *   scales   TCGEN05 scales of both.
+ *   y_bf16   [M, H] bf16.
+ *   1 <= M <= 128; H % 128 == 0; I % 128 == 0; H, I <= 65536.
+ * Uses the workspace registered with fsops_set_workspace for the current
+ * device (INVALID_ARG if none or too small).  Calls on one device are ordered
+ * by the caller (one stream, or events); concurrent calls would share the
+ * workspace.
+ */
+fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup, const uint8_t* w_down,
+                                    const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I,
+                                    void* stream);
+
+/* The same computation as three launches with the intermediates in HBM (the
+ * unfused baseline of p2 "Por que cuBLAS no era suficiente"): GEMM gate/up
+ * with fp32 output [M, 2I], SwiGLU + requantisation, GEMM down.  Same
+ * arguments, limits and workspace as fsops_mxfp8_swiglu_mlp. */
+fsops_status fsops_mxfp8_swiglu_mlp_unfused(const void* x_bf16, const uint8_t* w_gateup,
+                                            const uint8_t* w_down, const fsops_mlp_scales* scales,
+                                            void* y_bf16, int M, int H, int I, void* stream);
+
+/* Workspace bytes the MLP entry points need on the current device (0 if the
+ * shape is unsupported). */
+size_t fsops_mlp_workspace_bytes(int M, int H, int I);
+
+/* Register `ws` (device memory of `bytes` bytes, 256-byte aligned) as the MLP
+ * workspace of the current device, replacing any earlier one.  Zeroes all of
+ * it and synchronises the device: call it outside stream capture, before the
+ * first MLP call, and again after a call that reported an error.
+ * ws == NULL unregisters. */
+fsops_status fsops_set_workspace(void* ws, size_t bytes);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics.
+ * fsops_read_kernel_status: synchronously reads and clears the status word
+ * that the kernels write into a workspace when a bounded wait runs out
+ * (workspace NULL = the registered MLP workspace of the current device).
+ * *word is 0 when no kernel failed; otherwise bits 31..24 hold an
+ * fsops_status, bits 23..16 the wait site and bits 15..0 the block index.
+ * After a failure the workspace counters are reset by the kernel itself. */
+fsops_status fsops_read_kernel_status(void* workspace, uint32_t* word);
+
+/* Upper bound, in nanoseconds, for every wait inside the kernels launched
+ * after this call (default 1e9).  Applies to the calling process. */
+fsops_status fsops_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook: kernels launched after this call wait for `n` more arrivals on
+ * their cross-block readiness counters (quantised activations, finished
+ * SwiGLU tiles) than any launch produces, so those waits run out and report
+ * FSOPS_ERR_TIMEOUT.  0 (the default) disables it. */
+fsops_status fsops_debug_set_extra_arrivals(uint32_t n);
+
+const char* fsops_status_string(fsops_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fsops_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FSOPS_H */

@@ -1,0 +1,523 @@
+// fsops_api.cu -- host side of the C ABI declared in include/fsops.h:
+// argument validation, workspace layout, TMA descriptor encoding, launches.
+// No function here allocates device memory or synchronises, except
+// fsops_set_workspace and fsops_read_kernel_status, which say so.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fsops.h"
+#include "mx_internal.h"
+
+using namespace fsops;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kCtlRegionBytes = 16384;
+
+struct DeviceInfo {
+  bool init = false;
+  bool ok = false;
+  int sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+Workspace g_ws[kMaxDevices];
+
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+#ifdef FSOPS_TRACE
+unsigned long long* g_trace = nullptr;
+#endif
+std::atomic<uint32_t> g_extra{0};
+// Weight tiles (16 KB each) a block keeps in flight: 4 x 16 KB x 152 SMs is
+// about 10 MB, enough to cover the HBM latency at full bandwidth without
+// queueing that inflates every other round trip.
+std::atomic<int> g_max_inflight{4};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+fsops_status current_device(int* dev_out, const DeviceInfo** info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return FSOPS_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    d.init = true;
+    int major = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
+      d.ok = (major == 10);
+      d.sms = sms;
+    }
+    cudaGetLastError();
+    // tuning knob: weight tiles in flight per block (FSOPS_MAX_INFLIGHT=1..12)
+    if (const char* env = std::getenv("FSOPS_MAX_INFLIGHT")) {
+      const int v = std::atoi(env);
+      if (v >= 1 && v <= kMaxStages) g_max_inflight.store(v);
+    }
+    if (g_encode == nullptr) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+              cudaSuccess &&
+          q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      cudaGetLastError();
+    }
+  }
+  if (!d.ok || g_encode == nullptr) return FSOPS_ERR_NO_DEVICE;
+  *dev_out = dev;
+  *info = &d;
+  return FSOPS_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int npad_of(int M) { return (M + 15) / 16 * 16; }
+
+int stages_for(int npad) {
+  const uint32_t sb = stage_bytes_for(npad);
+  int s = static_cast<int>((kMaxSmem - 1024 - kSmemCtlBytes - kSmemXchgBytes) / sb);
+  if (s > kMaxStages) s = kMaxStages;
+  return s;
+}
+// Independent accumulators per tile: small N makes each MMA short, so the
+// dependency through a single accumulator would serialise the four MMAs of a
+// stage; more chains let them overlap (their sum is taken in the epilogue).
+int chains_for(int npad) {
+  if (const char* env = std::getenv("FSOPS_MMA_CHAINS")) {
+    const int v = std::atoi(env);
+    if ((v == 1 || v == 2 || v == 4) && v * npad <= 256) return v;
+  }
+  return npad <= 32 ? 4 : (npad <= 112 ? 2 : 1);
+}
+// Accumulator buffers: as many as TMEM holds next to the scale-tile ring (at most 4).
+int nacc_for(int npad, int stages) {
+  int n = (static_cast<int>(kTmemCols) - static_cast<int>(kSfColsPerStage) * stages) / (chains_for(npad) * npad);
+  return n > 4 ? 4 : n;
+}
+// Small M: every block quantises the k-chunks of x it needs itself (no
+// grid-wide exchange before the first MMA).  Large M: x is quantised once,
+// each block a slice, and shared through L2.
+int local_xq_for(int npad) {
+  if (const char* env = std::getenv("FSOPS_LOCAL_XQ")) return std::atoi(env) != 0 && npad <= 32;
+  return npad <= 32 ? 1 : 0;
+}
+size_t smem_for(int npad) {
+  return static_cast<size_t>(stages_for(npad)) * stage_bytes_for(npad) + kSmemXchgBytes + kSmemCtlBytes + 1024;
+}
+// fp32 accumulators of split tiles: [tiles][M][128]
+size_t accum_bytes(int M, int tiles) { return round_up(static_cast<size_t>(tiles) * M * 128 * 4, 1024); }
+
+// ---------------------------------------------------------------- workspace layouts
+struct GemmLayout {
+  size_t ctl, xq, xq_sf, part, total;
+};
+GemmLayout gemm_layout(int M, int N, int K) {
+  GemmLayout l;
+  l.ctl = 0;
+  l.xq = kCtlRegionBytes;
+  l.xq_sf = l.xq + round_up(static_cast<size_t>(M) * K, 1024);
+  l.part = l.xq_sf + round_up(static_cast<size_t>(K / 128) * 512, 1024);
+  l.total = l.part + accum_bytes(M, N / 128);
+  return l;
+}
+struct MlpLayout {
+  size_t ctl, xq, xq_sf, hq, hq_sf, part0, part1, gu, total;
+};
+MlpLayout mlp_layout(int M, int H, int I) {
+  MlpLayout l;
+  l.ctl = 0;
+  l.xq = kCtlRegionBytes;
+  l.xq_sf = l.xq + round_up(static_cast<size_t>(M) * H, 1024);
+  l.hq = l.xq_sf + round_up(static_cast<size_t>(H / 128) * 512, 1024);
+  l.hq_sf = l.hq + round_up(static_cast<size_t>(M) * I, 1024);
+  l.part0 = l.hq_sf + round_up(static_cast<size_t>(I / 128) * 512, 1024);
+  l.part1 = l.part0 + accum_bytes(M, I / 64);
+  l.gu = l.part1 + accum_bytes(M, H / 128);
+  l.total = l.gu + round_up(static_cast<size_t>(M) * 2 * I * 4, 1024);
+  return l;
+}
+// control words: header | hflags[I/128] | tile counters phase 0 | tile counters phase 1
+size_t ctl_words_needed(int I_chunks, int T0, int T1) { return kCtlHeaderWords + I_chunks + T0 + T1; }
+
+bool encode_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+void init_common(KernelArgs& a, int M, uint32_t* ctl) {
+  std::memset(&a, 0, sizeof(a));
+  a.M = M;
+  a.npad = npad_of(M);
+  a.nstages = stages_for(a.npad);
+  a.nacc = nacc_for(a.npad, a.nstages);
+  a.chains = chains_for(a.npad);
+  a.max_inflight = g_max_inflight.load() < a.nstages ? g_max_inflight.load() : a.nstages;
+  a.stage_bytes = stage_bytes_for(a.npad);
+  a.timeout_ns = g_timeout_ns.load();
+  a.extra_xready = g_extra.load();
+  a.ctl = ctl;
+#ifdef FSOPS_TRACE
+  a.trace = g_trace;
+#endif
+}
+
+fsops_status launch(const KernelArgs& a, int grid, cudaStream_t stream) {
+  cudaError_t e = launch_mx_kernel(a, grid, smem_for(a.npad), stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FSOPS_ERR_CUDA;
+  }
+  return FSOPS_OK;
+}
+
+bool gemm_shape_ok(int M, int N, int K) {
+  return M >= 1 && M <= 128 && N >= 128 && K >= 128 && N % 128 == 0 && K % 128 == 0 && N <= 65536 &&
+         K <= 65536;
+}
+
+// Plain GEMM (one phase) with the operand pointers already validated.
+// `ctl` is the control region, `xq`/`xq_sf` receive the quantised A (bf16 A
+// only), `part` holds the split-K partial sums.
+fsops_status gemm_impl(const void* a, const uint8_t* a_scales, bool a_bf16, const uint8_t* b_codes,
+                       const uint8_t* b_scales, void* c, bool c_f32, int M, int N, int K, uint8_t* ctl,
+                       uint8_t* xq, uint8_t* xq_sf, uint8_t* part, const DeviceInfo* di, cudaStream_t stream) {
+  const int grid = di->sms;
+  KernelArgs ka;
+  init_common(ka, M, reinterpret_cast<uint32_t*>(ctl));
+  ka.nphases = 1;
+  PhaseArgs& p = ka.ph[0];
+  p.sf_w = b_scales;
+  p.KS = K / kTileK;
+  p.T = N / kTileRows;
+  p.epi = kEpiStore;
+  p.out_ld = N;
+  p.tile_cnt = ka.ctl + kCtlHeaderWords;
+  p.accum = reinterpret_cast<float*>(part);
+  const uint8_t* act_codes;
+  if (a_bf16) {
+    ka.x = static_cast<const uint16_t*>(a);
+    ka.xq_codes = xq;
+    ka.xq_sf = xq_sf;
+    ka.H = K;
+    act_codes = ka.xq_codes;
+    p.sf_act = ka.xq_sf;
+    ka.local_xq = local_xq_for(ka.npad);
+    p.dep = ka.local_xq ? kDepNone : kDepXReady;
+  } else {
+    act_codes = static_cast<const uint8_t*>(a);
+    p.sf_act = a_scales;
+    p.dep = kDepNone;
+  }
+  ka.out = c;
+  ka.out_f32 = c_f32 ? 1 : 0;
+  if (!encode_map(&ka.tm_w[0], b_codes, K, N, kTileRows) || !encode_map(&ka.tm_act[0], act_codes, K, M, ka.npad))
+    return FSOPS_ERR_INVALID_ARG;
+  return launch(ka, grid, stream);
+}
+
+fsops_status check_ws(int dev, size_t need, uint8_t** ws) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_ws[dev].ptr == nullptr || g_ws[dev].bytes < need) return FSOPS_ERR_INVALID_ARG;
+  *ws = static_cast<uint8_t*>(g_ws[dev].ptr);
+  return FSOPS_OK;
+}
+
+fsops_status mlp_validate(const void* x, const uint8_t* wgu, const uint8_t* wd, const fsops_mlp_scales* sc,
+                          const void* y, int M, int H, int I) {
+  if (x == nullptr || wgu == nullptr || wd == nullptr || sc == nullptr || sc->gateup == nullptr ||
+      sc->down == nullptr || y == nullptr)
+    return FSOPS_ERR_INVALID_ARG;
+  if (M < 1 || M > 128 || H < 128 || I < 128 || H % 128 != 0 || I % 128 != 0 || H > 65536 || I > 65536)
+    return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(wgu) || !aligned16(wd) || !aligned16(sc->gateup) || !aligned16(sc->down) ||
+      !aligned16(y))
+    return FSOPS_ERR_MISALIGNED;
+  return FSOPS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fsops_version(void) { return 100; }
+
+const char* fsops_status_string(fsops_status s) {
+  switch (s) {
+    case FSOPS_OK: return "ok";
+    case FSOPS_ERR_INVALID_ARG: return "invalid argument";
+    case FSOPS_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case FSOPS_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FSOPS_ERR_CUDA: return "CUDA error";
+    case FSOPS_ERR_TIMEOUT: return "kernel wait timed out";
+    case FSOPS_ERR_NO_DEVICE: return "no sm_100-class device current";
+  }
+  return "unknown status";
+}
+
+size_t fsops_scale_bytes(int rows, int K, fsops_scale_layout layout) {
+  if (rows < 0 || K < 0) return 0;
+  if (layout == FSOPS_SCALES_ROWMAJOR) return static_cast<size_t>(rows) * (K / 32);
+  if (layout == FSOPS_SCALES_TCGEN05)
+    return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((K + 127) / 128) * 512;
+  return 0;
+}
+
+fsops_status fsops_quantize_mxfp8(const void* x_bf16, int rows, int K, int ld, uint8_t* codes, uint8_t* scales,
+                                  fsops_scale_layout layout, void* stream) {
+  if (layout != FSOPS_SCALES_ROWMAJOR && layout != FSOPS_SCALES_TCGEN05) return FSOPS_ERR_INVALID_ARG;
+  if (rows < 0 || K <= 0 || ld < K) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (K % (layout == FSOPS_SCALES_TCGEN05 ? 128 : 32) != 0 || ld % 8 != 0) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(rows) * ld >= (1LL << 31)) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return FSOPS_OK;
+  if (x_bf16 == nullptr || codes == nullptr || scales == nullptr) return FSOPS_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(codes)) return FSOPS_ERR_MISALIGNED;
+  int dev;
+  const DeviceInfo* di;
+  fsops_status st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  cudaError_t e = launch_quantize(static_cast<const uint16_t*>(x_bf16), rows, K, ld, codes, scales,
+                                  layout == FSOPS_SCALES_TCGEN05 ? 1 : 0, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FSOPS_ERR_CUDA;
+  }
+  return FSOPS_OK;
+}
+
+size_t fsops_gemm_workspace_bytes(int M, int N, int K) {
+  if (!gemm_shape_ok(M, N, K)) return 0;
+  int dev;
+  const DeviceInfo* di;
+  if (current_device(&dev, &di) != FSOPS_OK) return 0;
+  return gemm_layout(M, N, K).total;
+}
+
+fsops_status fsops_mxfp8_gemm_ex(const void* a, const uint8_t* a_scales, fsops_dtype a_dtype,
+                                 const uint8_t* b_codes, const uint8_t* b_scales, void* c, fsops_dtype c_dtype,
+                                 int M, int N, int K, void* workspace, size_t ws_bytes, void* stream) {
+  if (a == nullptr || b_codes == nullptr || b_scales == nullptr || c == nullptr || workspace == nullptr)
+    return FSOPS_ERR_INVALID_ARG;
+  if (a_dtype != FSOPS_DTYPE_BF16 && a_dtype != FSOPS_DTYPE_MXFP8) return FSOPS_ERR_INVALID_ARG;
+  if (c_dtype != FSOPS_DTYPE_BF16 && c_dtype != FSOPS_DTYPE_F32) return FSOPS_ERR_INVALID_ARG;
+  if ((a_dtype == FSOPS_DTYPE_BF16) != (a_scales == nullptr)) return FSOPS_ERR_INVALID_ARG;
+  if (!gemm_shape_ok(M, N, K)) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(a) || !aligned16(b_codes) || !aligned16(b_scales) || !aligned16(c) || !aligned16(workspace) ||
+      (a_scales != nullptr && !aligned16(a_scales)))
+    return FSOPS_ERR_MISALIGNED;
+  int dev;
+  const DeviceInfo* di;
+  fsops_status st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  const GemmLayout l = gemm_layout(M, N, K);
+  if (ws_bytes < l.total) return FSOPS_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return gemm_impl(a, a_scales, a_dtype == FSOPS_DTYPE_BF16, b_codes, b_scales, c, c_dtype == FSOPS_DTYPE_F32, M,
+                   N, K, ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.part, di, static_cast<cudaStream_t>(stream));
+}
+
+fsops_status fsops_mxfp8_gemm(const void* a_bf16, const uint8_t* b_codes, const uint8_t* b_scales, void* c_bf16,
+                              int M, int N, int K, void* workspace, size_t ws_bytes, void* stream) {
+  return fsops_mxfp8_gemm_ex(a_bf16, nullptr, FSOPS_DTYPE_BF16, b_codes, b_scales, c_bf16, FSOPS_DTYPE_BF16, M, N,
+                             K, workspace, ws_bytes, stream);
+}
+
+fsops_status fsops_swiglu_quantize_mxfp8(const float* gu, int M, int I, uint8_t* h_codes, uint8_t* h_scales,
+                                         void* stream) {
+  if (gu == nullptr || h_codes == nullptr || h_scales == nullptr) return FSOPS_ERR_INVALID_ARG;
+  if (M < 1 || M > 128 || I < 128 || I % 128 != 0 || I > 65536) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(gu) || !aligned16(h_codes)) return FSOPS_ERR_MISALIGNED;
+  int dev;
+  const DeviceInfo* di;
+  fsops_status st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  cudaError_t e = launch_swiglu_quantize(gu, M, I, h_codes, h_scales, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FSOPS_ERR_CUDA;
+  }
+  return FSOPS_OK;
+}
+
+size_t fsops_mlp_workspace_bytes(int M, int H, int I) {
+  if (M < 1 || M > 128 || H < 128 || I < 128 || H % 128 != 0 || I % 128 != 0 || H > 65536 || I > 65536) return 0;
+  int dev;
+  const DeviceInfo* di;
+  if (current_device(&dev, &di) != FSOPS_OK) return 0;
+  return mlp_layout(M, H, I).total;
+}
+
+fsops_status fsops_set_workspace(void* ws, size_t bytes) {
+  int dev;
+  const DeviceInfo* di;
+  fsops_status st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  if (ws != nullptr && ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)) return FSOPS_ERR_MISALIGNED;
+  if (ws != nullptr && bytes < kCtlRegionBytes) return FSOPS_ERR_INVALID_ARG;
+  if (ws != nullptr) {
+    if (cudaMemset(ws, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+      cudaGetLastError();
+      return FSOPS_ERR_CUDA;
+    }
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_ws[dev].ptr = ws;
+  g_ws[dev].bytes = ws != nullptr ? bytes : 0;
+  return FSOPS_OK;
+}
+
+fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup, const uint8_t* w_down,
+                                    const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I,
+                                    void* stream) {
+  fsops_status st = mlp_validate(x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I);
+  if (st != FSOPS_OK) return st;
+  int dev;
+  const DeviceInfo* di;
+  st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  const int grid = di->sms;
+  const MlpLayout l = mlp_layout(M, H, I);
+  uint8_t* ws;
+  st = check_ws(dev, l.total, &ws);
+  if (st != FSOPS_OK) return st;
+
+  KernelArgs ka;
+  init_common(ka, M, reinterpret_cast<uint32_t*>(ws + l.ctl));
+  const int Ic = I / 128;           // 128-feature chunks of the intermediate (phase-1 k-stages)
+  const int T0 = I / kPairFeatures; // gate/up pair tiles
+  const int T1 = H / kTileRows;     // down-projection tiles
+  if (ctl_words_needed(Ic, T0, T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  ka.hflags = ka.ctl + kCtlHeaderWords;
+  ka.nphases = 2;
+  ka.x = static_cast<const uint16_t*>(x_bf16);
+  ka.xq_codes = ws + l.xq;
+  ka.xq_sf = ws + l.xq_sf;
+  ka.H = H;
+  ka.hq_codes = ws + l.hq;
+  ka.hq_sf = ws + l.hq_sf;
+  ka.I = I;
+  ka.out = y_bf16;
+  ka.out_f32 = 0;
+  // phase 0: gate/up, tile t = rows [128t, 128t+128) of the paired W_gateup
+  PhaseArgs& p0 = ka.ph[0];
+  p0.sf_w = scales->gateup;
+  p0.sf_act = ka.xq_sf;
+  p0.tile_cnt = ka.hflags + Ic;
+  p0.accum = reinterpret_cast<float*>(ws + l.part0);
+  p0.KS = H / kTileK;
+  p0.T = T0;
+  ka.local_xq = local_xq_for(ka.npad);
+  p0.dep = ka.local_xq ? kDepNone : kDepXReady;
+  p0.epi = kEpiSwiGLU;
+  p0.out_ld = I;
+  // phase 1: down projection, tile t = rows [128t, 128t+128) of W_down
+  PhaseArgs& p1 = ka.ph[1];
+  p1.sf_w = scales->down;
+  p1.sf_act = ka.hq_sf;
+  p1.tile_cnt = p0.tile_cnt + T0;
+  p1.accum = reinterpret_cast<float*>(ws + l.part1);
+  p1.KS = I / kTileK;
+  p1.T = T1;
+  p1.dep = kDepHFlags;
+  p1.epi = kEpiStore;
+  p1.out_ld = H;
+  if (!encode_map(&ka.tm_w[0], w_gateup, H, 2 * I, kTileRows) ||
+      !encode_map(&ka.tm_act[0], ka.xq_codes, H, M, ka.npad) || !encode_map(&ka.tm_w[1], w_down, I, H, kTileRows) ||
+      !encode_map(&ka.tm_act[1], ka.hq_codes, I, M, ka.npad))
+    return FSOPS_ERR_INVALID_ARG;
+  return launch(ka, grid, static_cast<cudaStream_t>(stream));
+}
+
+fsops_status fsops_mxfp8_swiglu_mlp_unfused(const void* x_bf16, const uint8_t* w_gateup, const uint8_t* w_down,
+                                            const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I,
+                                            void* stream) {
+  fsops_status st = mlp_validate(x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I);
+  if (st != FSOPS_OK) return st;
+  int dev;
+  const DeviceInfo* di;
+  st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  const MlpLayout l = mlp_layout(M, H, I);
+  uint8_t* ws;
+  st = check_ws(dev, l.total, &ws);
+  if (st != FSOPS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* gu = reinterpret_cast<float*>(ws + l.gu);
+  // launch 1: gate/up GEMM, x quantised in-kernel, fp32 [M, 2I] to HBM
+  st = gemm_impl(x_bf16, nullptr, true, w_gateup, scales->gateup, gu, true, M, 2 * I, H, ws + l.ctl, ws + l.xq,
+                 ws + l.xq_sf, ws + l.part0, di, s);
+  if (st != FSOPS_OK) return st;
+  // launch 2: SiLU(g) * u, requantised to MXFP8, to HBM
+  cudaError_t e = launch_swiglu_quantize(gu, M, I, ws + l.hq, ws + l.hq_sf, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FSOPS_ERR_CUDA;
+  }
+  // launch 3: down GEMM on the requantised intermediate
+  return gemm_impl(ws + l.hq, ws + l.hq_sf, false, w_down, scales->down, y_bf16, false, M, H, I, ws + l.ctl,
+                   nullptr, nullptr, ws + l.part1, di, s);
+}
+
+fsops_status fsops_read_kernel_status(void* workspace, uint32_t* word) {
+  if (word == nullptr) return FSOPS_ERR_INVALID_ARG;
+  if (workspace == nullptr) {
+    int dev;
+    const DeviceInfo* di;
+    fsops_status st = current_device(&dev, &di);
+    if (st != FSOPS_OK) return st;
+    std::lock_guard<std::mutex> lk(g_mu);
+    workspace = g_ws[dev].ptr;
+    if (workspace == nullptr) return FSOPS_ERR_INVALID_ARG;
+  }
+  uint32_t v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(workspace, 0, sizeof(v)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return FSOPS_ERR_CUDA;
+  }
+  *word = v;
+  return FSOPS_OK;
+}
+
+fsops_status fsops_set_wait_timeout_ns(uint64_t ns) {
+  if (ns == 0) return FSOPS_ERR_INVALID_ARG;
+  g_timeout_ns.store(ns);
+  return FSOPS_OK;
+}
+
+fsops_status fsops_debug_set_extra_arrivals(uint32_t n) {
+  g_extra.store(n);
+  return FSOPS_OK;
+}
+
+#ifdef FSOPS_TRACE
+// Profiling builds only: device buffer of [grid][64] uint64 timeline stamps.
+fsops_status fsops_debug_set_trace_buffer(void* buf) {
+  g_trace = static_cast<unsigned long long*>(buf);
+  return FSOPS_OK;
+}
+#endif
+
+}  // extern "C"

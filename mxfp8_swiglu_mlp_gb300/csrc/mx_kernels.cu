@@ -1,0 +1,804 @@
+// mx_kernels.cu -- the sm_103a kernels of the MXFP8 SwiGLU MLP.
+//
+//   mx_persistent_kernel   one launch per GEMM or per whole MLP: cooperative
+//                          grid of one block per SM; TMA streams weight tiles,
+//                          tcgen05 block-scaled MMAs accumulate in TMEM,
+//                          stream-K split of the K loop over all blocks.
+//   quantize_kernel        bf16 -> E4M3 + UE8M0 (row-major or tiled scales).
+//   swiglu_quantize_kernel SiLU(g) * u -> E4M3 + UE8M0 (the unfused path).
+//
+// Quantisation rule (OCP MX, as the Fish Audio post's mxfp8 format uses it,
+// p2 "Estrategia de cuantizacion FP8"): for each 32-block, the UE8M0 byte is
+// max(biased_exponent(amax) - 8, 0), i.e. e = floor(log2 amax) - 8 clamped at
+// -127; elements are v * 2^-e converted to E4M3 with round-to-nearest-even
+// and saturation (cvt ... satfinite).  v * 2^-e is exact in fp32 wherever the
+// rounding can depend on it, so the codes are bit-exact with an exact
+// computation.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "mx_internal.h"
+#include "sm103.cuh"
+
+namespace fsops {
+using namespace dev;
+
+// ======================================================================
+// MXFP8 helpers (fp32 in, codes out)
+// ======================================================================
+__device__ __forceinline__ uint32_t ue8m0_from_amax(float amax) {
+  const int be = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  return static_cast<uint32_t>(be > 8 ? be - 8 : 0);
+}
+// 2^-e for scale byte s = e + 127 (s <= 246 for finite fp32 inputs).
+__device__ __forceinline__ float inv_scale_from_ue8m0(uint32_t s) {
+  return __uint_as_float((254u - s) << 23);
+}
+__device__ __forceinline__ uint32_t e4m3_code(float v) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ uint32_t tiled_sf_offset(int r, int kb, int n_kg) {
+  return static_cast<uint32_t>(((r >> 7) * n_kg + (kb >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 +
+                               (kb & 3));
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Quantise one 32-element bf16 block already in registers (raw = 64 bytes)
+// into 32 codes packed four to a word; returns the scale byte.
+__device__ __forceinline__ uint32_t quantize_block_pack(const uint4 (&raw)[4], uint32_t (&packed)[8]) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(raw);
+  uint32_t amax_bits = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    amax_bits = max(amax_bits, (w[i] & 0x7FFFu) << 16);
+    amax_bits = max(amax_bits, w[i] & 0x7FFF0000u);
+  }
+  const uint32_t s = ue8m0_from_amax(__uint_as_float(amax_bits));
+  const float inv = inv_scale_from_ue8m0(s);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t c0 = e4m3_code(bf16_lo(w[2 * i]) * inv);
+    const uint32_t c1 = e4m3_code(bf16_hi(w[2 * i]) * inv);
+    const uint32_t c2 = e4m3_code(bf16_lo(w[2 * i + 1]) * inv);
+    const uint32_t c3 = e4m3_code(bf16_hi(w[2 * i + 1]) * inv);
+    packed[i] = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+  }
+  return s;
+}
+// Same, storing the 32 codes at `dst` (16-byte aligned).
+__device__ __forceinline__ uint32_t quantize_block_regs(const uint4 (&raw)[4], uint8_t* dst) {
+  uint32_t packed[8];
+  const uint32_t s = quantize_block_pack(raw, packed);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  d[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  return s;
+}
+
+// Same, loading the block from `src` (16-byte aligned) first.
+__device__ __forceinline__ uint32_t quantize_block_bf16(const uint16_t* src, uint8_t* dst) {
+  uint4 raw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+  return quantize_block_regs(raw, dst);
+}
+
+// ======================================================================
+// Standalone quantiser: one thread per 32-block.
+// ======================================================================
+__global__ void quantize_kernel(const uint16_t* __restrict__ x, int rows, int rows_pad, int K, int ld,
+                                uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int tiled) {
+  const int nb = K / 32;
+  const long long total = static_cast<long long>(rows_pad) * nb;
+  for (long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; b < total;
+       b += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(b / nb), kb = static_cast<int>(b % nb);
+    uint32_t s = 0;
+    if (r < rows) s = quantize_block_bf16(x + static_cast<long long>(r) * ld + kb * 32,
+                                          codes + static_cast<long long>(r) * K + kb * 32);
+    if (tiled) {
+      scales[tiled_sf_offset(r, kb, K / 128)] = static_cast<uint8_t>(s);
+    } else if (r < rows) {
+      scales[static_cast<long long>(r) * nb + kb] = static_cast<uint8_t>(s);
+    }
+  }
+}
+
+cudaError_t launch_quantize(const uint16_t* x, int rows, int K, int ld, uint8_t* codes, uint8_t* scales,
+                            int tiled, cudaStream_t stream) {
+  const int rows_pad = tiled ? (rows + 127) / 128 * 128 : rows;
+  const long long total = static_cast<long long>(rows_pad) * (K / 32);
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 65535LL * 16) blocks = 65535LL * 16;
+  quantize_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(x, rows, rows_pad, K, ld, codes,
+                                                                          scales, tiled);
+  return cudaGetLastError();
+}
+
+// ======================================================================
+// SwiGLU + requantisation (the middle launch of the unfused path).
+// ======================================================================
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+__global__ void swiglu_quantize_kernel(const float* __restrict__ gu, int M, int npad, int I,
+                                       uint8_t* __restrict__ hc, uint8_t* __restrict__ hs) {
+  const int nb = I / 32;
+  const int total = npad * nb;
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < total; b += gridDim.x * blockDim.x) {
+    const int m = b / nb, kb = b % nb;
+    uint32_t s = 0;
+    if (m < M) {
+      // gu columns follow the W_gateup row order: 128-column block j holds gate
+      // features 64j..64j+63, then up features 64j..64j+63
+      const int f0 = kb * 32;
+      const float* g = gu + static_cast<long long>(m) * 2 * I + 2 * (f0 / kPairFeatures) * kPairFeatures +
+                       (f0 % kPairFeatures);
+      const float* u = g + kPairFeatures;
+      float h[32];
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 gv = __ldg(reinterpret_cast<const float4*>(g + i));
+        const float4 uv = __ldg(reinterpret_cast<const float4*>(u + i));
+        h[i] = silu_mul(gv.x, uv.x);
+        h[i + 1] = silu_mul(gv.y, uv.y);
+        h[i + 2] = silu_mul(gv.z, uv.z);
+        h[i + 3] = silu_mul(gv.w, uv.w);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+      s = ue8m0_from_amax(amax);
+      const float inv = inv_scale_from_ue8m0(s);
+      uint32_t packed[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        packed[i] = e4m3_code(h[4 * i] * inv) | (e4m3_code(h[4 * i + 1] * inv) << 8) |
+                    (e4m3_code(h[4 * i + 2] * inv) << 16) | (e4m3_code(h[4 * i + 3] * inv) << 24);
+      uint4* d = reinterpret_cast<uint4*>(hc + static_cast<long long>(m) * I + kb * 32);
+      d[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      d[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    }
+    hs[tiled_sf_offset(m, kb, I / 128)] = static_cast<uint8_t>(s);
+  }
+}
+
+cudaError_t launch_swiglu_quantize(const float* gu, int M, int I, uint8_t* hc, uint8_t* hs,
+                                   cudaStream_t stream) {
+  const int npad = (M + 15) / 16 * 16;
+  const int total = npad * (I / 32);
+  const int threads = 128;
+  const int blocks = (total + threads - 1) / threads;
+  swiglu_quantize_kernel<<<blocks, threads, 0, stream>>>(gu, M, npad, I, hc, hs);
+  return cudaGetLastError();
+}
+
+// ======================================================================
+// The persistent block-scaled GEMM / fused MLP kernel.
+//
+// Roles (one block per SM, 8 warps):
+//   warp 0 lane 0  weight producer: TMA of 128 x 128 B weight tiles + their
+//                  512-byte scale tiles into a ring of shared-memory stages
+//   warp 1 lane 0  activation producer: waits until its operand exists (the
+//                  grid-wide x quantisation, or the SwiGLU tiles of the
+//                  k-range) and TMA-loads the npad x 128 B activation tile
+//   warp 2 lane 0  MMA issuer: tcgen05.cp of both scale tiles into TMEM, four
+//                  kind::mxf8f6f4 block-scaled MMAs (K = 32 each) per stage
+//   warps 4-7      quantise this block's slice of x, then drain accumulators
+//                  (TMEM lanes 0..127 = tile rows) into the epilogue
+// ======================================================================
+struct Ctx {
+  volatile int* abort_flag;
+  volatile uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+__device__ __noinline__ void raise_error(const Ctx& cx, uint32_t code, uint32_t site) {
+  *cx.abort_flag = 1;
+  const uint32_t word = (code << 24) | ((site & 0xFFu) << 16) | (blockIdx.x & 0xFFFFu);
+  atomicCAS(const_cast<uint32_t*>(cx.status), 0u, word);
+}
+
+// Bounded wait on an mbarrier phase.  Gives up (returns false) when the block
+// was told to abort, another block reported an error, or the timeout passes.
+__device__ __forceinline__ bool wait_mbar(const Ctx& cx, uint64_t* bar, uint32_t parity, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++n & 15u) == 0) {
+      if (*cx.abort_flag || *cx.status != 0) { *cx.abort_flag = 1; return false; }
+      if (globaltimer_ns() - t0 > cx.timeout_ns) { raise_error(cx, 5u, site); return false; }
+    }
+  }
+  return true;
+}
+// Bounded wait used only while tearing down (no abort check, fixed limit).
+__device__ __forceinline__ void drain_mbar(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+// Bounded spin until every counter p[0..n) is >= target.  The polls are
+// relaxed loads issued together (one round trip per try); an acquire fence
+// follows the successful try.
+__device__ __forceinline__ bool wait_counters(const Ctx& cx, const uint32_t* p, int n, uint32_t target,
+                                              uint32_t site) {
+  uint64_t t0 = 0;
+  for (;;) {
+    bool all = true;
+    for (int i = 0; i < n; ++i) all &= (ld_relaxed_gpu(p + i) >= target);
+    if (all) break;
+    if (t0 == 0) t0 = globaltimer_ns();
+    if (*cx.abort_flag || *cx.status != 0) { *cx.abort_flag = 1; return false; }
+    if (globaltimer_ns() - t0 > cx.timeout_ns) { raise_error(cx, 5u, site); return false; }
+    __nanosleep(20);
+  }
+  fence_acq_rel_gpu();
+  return true;
+}
+
+// Timeline stamps for profiling builds (compiled with -DFSOPS_TRACE).
+#ifdef FSOPS_TRACE
+#define FSOPS_STAMP(idx)                                                         \
+  do {                                                                           \
+    if (a.trace != nullptr) a.trace[blockIdx.x * 64 + (idx)] = globaltimer_ns(); \
+  } while (0)
+#define FSOPS_STAMP_IF(cond, idx) \
+  do {                            \
+    if (cond) FSOPS_STAMP(idx);   \
+  } while (0)
+#else
+#define FSOPS_STAMP(idx) \
+  do {                   \
+  } while (0)
+#define FSOPS_STAMP_IF(cond, idx) \
+  do {                            \
+  } while (0)
+#endif
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ long long range_begin(long long c, long long U, long long G) { return c * U / G; }
+// The block whose range holds unit u.
+__device__ __forceinline__ long long owner_of(long long u, long long U, long long G) {
+  return ((u + 1) * G + U - 1) / U - 1;
+}
+
+// Walks the segments (tile, ks0, ks1) of one phase assigned to this block.
+struct SegIter {
+  long long u, ue;
+  int KS;
+  __device__ SegIter(const PhaseArgs& p, long long G) {
+    const long long U = static_cast<long long>(p.T) * p.KS;
+    u = range_begin(blockIdx.x, U, G);
+    ue = range_begin(blockIdx.x + 1, U, G);
+    KS = p.KS;
+  }
+  __device__ bool next(int& t, int& ks0, int& ks1) {
+    if (u >= ue) return false;
+    t = static_cast<int>(u / KS);
+    ks0 = static_cast<int>(u % KS);
+    const long long rem = ue - u;
+    ks1 = static_cast<int>(min(static_cast<long long>(KS), ks0 + rem));
+    u += ks1 - ks0;
+    return true;
+  }
+};
+
+// ----------------------------------------------------------------------------
+// Epilogues.  Thread et (0..127) owns row et of the tile; v[j] is its value
+// for token c0 + j.
+// ----------------------------------------------------------------------------
+
+// Plain GEMM output: C[tok, 128 t + et].
+__device__ __forceinline__ void epi_store_chunk(const KernelArgs& a, const PhaseArgs& p, int t, int c0,
+                                                const float (&v)[16], int et) {
+  const long long col = static_cast<long long>(t) * kTileRows + et;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int tok = c0 + j;
+    if (tok < a.M) {
+      const long long o = static_cast<long long>(tok) * p.out_ld + col;
+      if (a.out_f32) static_cast<float*>(a.out)[o] = v[j];
+      else static_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16_rn(v[j]);
+    }
+  }
+}
+
+// SwiGLU + requantisation of one gate/up pair tile t (intermediate features
+// 64t..64t+63; rows 0..63 gate, 64..127 up).  The chunk goes through shared
+// memory so that each warp sees gate and up of the same feature: warp w then
+// handles features 64t + 32 (w & 1) + lane for tokens c0 + 8 (w >> 1) + 0..7;
+// a warp holds exactly one 32-feature MX block per token.
+__device__ __forceinline__ void epi_swiglu_chunk(const KernelArgs& a, int t, int c0, const float (&v)[16], int et,
+                                                 float* xchg) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) xchg[j * 128 + et] = v[j];
+  epi_bar();
+  const int lane = et & 31, w = et >> 5;
+  const int fh = w & 1, th = w >> 1;
+  const int f = t * kPairFeatures + 32 * fh + lane;
+  const int kb = f >> 5;  // MX block along I
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) {
+    const int j = 8 * th + jj;
+    const int tok = c0 + j;
+    if (tok >= a.M) break;  // uniform over the warp
+    const float g = xchg[j * 128 + 32 * fh + lane];
+    const float u = xchg[j * 128 + 64 + 32 * fh + lane];
+    const float h = silu_mul(g, u);
+    float amax = fabsf(h);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const uint32_t s = ue8m0_from_amax(amax);
+    const uint32_t code = e4m3_code(h * inv_scale_from_ue8m0(s));
+    a.hq_codes[static_cast<long long>(tok) * a.I + f] = static_cast<uint8_t>(code);
+    if (lane == 0) a.hq_sf[(kb >> 2) * 512 + (tok & 31) * 16 + (tok >> 5) * 4 + (kb & 3)] = static_cast<uint8_t>(s);
+  }
+  epi_bar();  // xchg is reused by the next chunk
+}
+
+// After every chunk of SwiGLU tile t has been written: publish it.  Each
+// writer orders its stores before later async-proxy (TMA) reads, the barrier
+// orders all of them before thread 0's release-add.
+__device__ __forceinline__ void publish_swiglu_tile(const KernelArgs& a, int t, int et) {
+  fence_proxy_async_global();
+  epi_bar();
+  if (et == 0) red_add_release_gpu(a.hflags + (t >> 1), 1u);
+}
+
+// 16 columns of this thread's TMEM lane, summed over the accumulator chains.
+__device__ __forceinline__ void tmem_chunk_sum(uint32_t taddr, int chains, int npad, float (&v)[16]) {
+  uint32_t r[16];
+  tmem_ld16(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+  for (int c = 1; c < chains; ++c) {
+    tmem_ld16(taddr + c * npad, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[j]);
+  }
+}
+
+// Local activation tiles (small M): epilogue thread et < 4 * npad owns the
+// 32-element block (row et / 4, block et % 4) of a 128-wide k-chunk of x.
+__device__ __forceinline__ void load_x_block(const KernelArgs& a, int ks, int et, uint4 (&raw)[4]) {
+  const int r = et >> 2, j = et & 3;
+  if (r < a.M) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<long long>(r) * a.H + ks * kTileK + 32 * j);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + i);
+  }
+}
+// Quantise the block into the stage's activation tile (128-byte swizzled rows,
+// as the TMA would have written them) and its scale tile; rows >= M get zeros.
+__device__ __forceinline__ void store_x_block(const KernelArgs& a, uint8_t* st, int et, const uint4 (&raw)[4]) {
+  const int r = et >> 2, j = et & 3;
+  uint32_t s = 0;
+  uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+  if (r < a.M) {
+    uint32_t pk[8];
+    s = quantize_block_pack(raw, pk);
+    c0 = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    c1 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  }
+  uint8_t* row = st + stage_off_b() + r * 128;
+  *reinterpret_cast<uint4*>(row + (((2 * j) ^ (r & 7)) << 4)) = c0;
+  *reinterpret_cast<uint4*>(row + (((2 * j + 1) ^ (r & 7)) << 4)) = c1;
+  st[stage_off_sfb(a.npad) + (r & 31) * 16 + (r >> 5) * 4 + j] = static_cast<uint8_t>(s);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid_constant__ KernelArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = a.nstages;
+  float* xchg = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * a.stage_bytes);
+  uint8_t* ctl_smem = reinterpret_cast<uint8_t*>(xchg) + kSmemXchgBytes;
+  uint64_t* full_w = reinterpret_cast<uint64_t*>(ctl_smem);
+  uint64_t* full_a = full_w + kMaxStages;
+  uint64_t* empty = full_a + kMaxStages;
+  uint64_t* acc_full = empty + kMaxStages;
+  uint64_t* acc_empty = acc_full + 4;
+  uint64_t* drain = acc_empty + 4;
+  uint64_t* x_issued = drain + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_issued + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long G = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_w[s], 1);
+      mbar_init(&full_a[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+    }
+    mbar_init(drain, 1);
+    mbar_init(x_issued, 128);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int p = 0; p < a.nphases; ++p) {
+      tma_prefetch_desc(&a.tm_w[p]);
+      tma_prefetch_desc(&a.tm_act[p]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) FSOPS_STAMP(0);
+
+  Ctx cx;
+  cx.abort_flag = abort_flag;
+  cx.status = a.ctl + kCtlStatus;
+  cx.timeout_ns = a.timeout_ns;
+
+  const int npad = a.npad;
+  const uint32_t acc_cols = static_cast<uint32_t>(a.chains * npad);
+  const uint32_t sf_base = static_cast<uint32_t>(a.nacc) * acc_cols;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ weight producer
+    const uint64_t pol = l2_policy_evict_first();
+    uint32_t issued_mask = 0, issued_parity = 0;
+    int stage = 0;
+    uint32_t round = 0;
+    // the stage `a.max_inflight` loads back: issuing waits until it has landed,
+    // so that a block never has more than max_inflight weight tiles in flight
+    // (deeper queues only add latency to every other memory round trip)
+    int lag_stage = 0;
+    uint32_t lag_round = 0, n_issued = 0;
+    bool ok = true;
+    // let the epilogue warps' loads of x enter the memory system first
+    if (a.x != nullptr && !a.local_xq) ok = wait_mbar(cx, x_issued, 0, kSiteEmpty);
+    for (int p = 0; p < a.nphases && ok; ++p) {
+      const PhaseArgs& ph = a.ph[p];
+      SegIter it(ph, G);
+      int t, ks0, ks1;
+      while (ok && it.next(t, ks0, ks1)) {
+        for (int ks = ks0; ks < ks1; ++ks) {
+          if (!wait_mbar(cx, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty)) { ok = false; break; }
+          if (n_issued >= static_cast<uint32_t>(a.max_inflight)) {
+            if (!wait_mbar(cx, &full_w[lag_stage], lag_round & 1u, kSiteFullW)) { ok = false; break; }
+            if (++lag_stage == S) { lag_stage = 0; ++lag_round; }
+          }
+          FSOPS_STAMP_IF(n_issued < 24, 40 + n_issued);
+          ++n_issued;
+          uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
+          mbar_arrive_expect_tx(&full_w[stage], 16384u + 512u);
+          tma_load_2d(st + stage_off_a(), &a.tm_w[p], &full_w[stage], ks * kTileK, t * kTileRows, pol);
+          bulk_load(st + stage_off_sfa(npad), ph.sf_w + (static_cast<size_t>(t) * ph.KS + ks) * 512, 512,
+                    &full_w[stage], pol);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | ((round & 1u) << stage);
+          if (++stage == S) { stage = 0; ++round; }
+        }
+      }
+    }
+    if (!ok) *abort_flag = 1;
+    for (int s = 0; s < S; ++s)
+      if (issued_mask & (1u << s)) drain_mbar(&full_w[s], (issued_parity >> s) & 1u, 200000000ull);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ activation producer
+    const uint64_t pol = l2_policy_evict_last();
+    uint32_t issued_mask = 0, issued_parity = 0;
+    int stage = 0;
+    uint32_t round = 0;
+    bool ok = true, x_ready = false, h_seen = false;
+    for (int p = 0; p < a.nphases && ok; ++p) {
+      const PhaseArgs& ph = a.ph[p];
+      SegIter it(ph, G);
+      int t, ks0, ks1;
+      while (ok && it.next(t, ks0, ks1)) {
+        if (p == 0 && a.local_xq) {
+          // the epilogue warps fill these stages' activation tiles
+          for (int ks = ks0; ks < ks1; ++ks)
+            if (++stage == S) { stage = 0; ++round; }
+          continue;
+        }
+        for (int ks = ks0; ks < ks1; ++ks) {
+          if (!wait_mbar(cx, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty)) { ok = false; break; }
+          if (ph.dep == kDepXReady && !x_ready) {
+            if (!wait_counters(cx, a.ctl + kCtlXReady, 1, static_cast<uint32_t>(G) + a.extra_xready,
+                               kSiteXReady)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_global();
+            x_ready = true;
+            FSOPS_STAMP(2);
+          } else if (ph.dep == kDepHFlags && ks == ks0) {
+            // the whole k-range of the segment: both SwiGLU tiles of every 128-feature chunk
+            if (!wait_counters(cx, a.hflags + ks0, ks1 - ks0, 2u + a.extra_xready, kSiteHFlag)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_global();
+            if (!h_seen) FSOPS_STAMP(5);
+            h_seen = true;
+            FSOPS_STAMP(6);
+          }
+          uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
+          mbar_arrive_expect_tx(&full_a[stage], 128u * npad + 512u);
+          tma_load_2d(st + stage_off_b(), &a.tm_act[p], &full_a[stage], ks * kTileK, 0, pol);
+          bulk_load(st + stage_off_sfb(npad), ph.sf_act + static_cast<size_t>(ks) * 512, 512, &full_a[stage], pol);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | ((round & 1u) << stage);
+          if (++stage == S) { stage = 0; ++round; }
+        }
+      }
+    }
+    if (!ok) *abort_flag = 1;
+    for (int s = 0; s < S; ++s)
+      if (issued_mask & (1u << s)) drain_mbar(&full_a[s], (issued_parity >> s) & 1u, 200000000ull);
+  } else if (warp == 2 && lane == 0) {
+    // ------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t round = 0;
+    int acc = 0;
+    uint32_t acc_round = 0;
+    bool ok = true;
+    const uint32_t idesc0 = idesc_mxf8_e4m3(static_cast<uint32_t>(npad), 0, 0);
+    uint32_t n_mma = 0;
+    for (int p = 0; p < a.nphases && ok; ++p) {
+      const PhaseArgs& ph = a.ph[p];
+      SegIter it(ph, G);
+      int t, ks0, ks1;
+      while (ok && it.next(t, ks0, ks1)) {
+        if (!wait_mbar(cx, &acc_empty[acc], (acc_round & 1u) ^ 1u, kSiteAccEmpty)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + acc * acc_cols;
+        for (int ks = ks0; ks < ks1; ++ks) {
+          if (!wait_mbar(cx, &full_w[stage], round & 1u, kSiteFullW) ||
+              !wait_mbar(cx, &full_a[stage], round & 1u, kSiteFullA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          FSOPS_STAMP_IF(n_mma < 24, 16 + n_mma);
+          ++n_mma;
+          uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
+          const uint32_t sfc = tmem + sf_base + kSfColsPerStage * stage;
+          tc_cp_32x128b_warpx4(sfc, smem_desc(smem_u32(st + stage_off_sfa(npad)), 0, 128, kSwizzleNone));
+          tc_cp_32x128b_warpx4(sfc + 4, smem_desc(smem_u32(st + stage_off_sfb(npad)), 0, 128, kSwizzleNone));
+          const uint32_t sa = smem_u32(st + stage_off_a());
+          const uint32_t sb = smem_u32(st + stage_off_b());
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            // scale byte k of each 32-bit TMEM scale word belongs to K-block k of
+            // the stage; k-step k accumulates into chain k % chains, so up to
+            // four MMAs of a stage are independent of each other
+            const uint32_t idesc = idesc0 | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+            const uint32_t chain = static_cast<uint32_t>(k % a.chains);
+            tc_mma_mxf8(d + chain * npad, smem_desc(sa + 32 * k, 16, 1024, kSwizzle128B),
+                        smem_desc(sb + 32 * k, 16, 1024, kSwizzle128B), idesc, sfc, sfc + 4,
+                        (ks > ks0 || k >= a.chains) ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == S) { stage = 0; ++round; }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[acc]);
+        if (++acc == a.nacc) { acc = 0; ++acc_round; }
+        FSOPS_STAMP(p == 0 ? 7 : 11);
+      }
+    }
+    if (!ok) *abort_flag = 1;
+    // wait until every tcgen05 operation issued by this thread has completed
+    tc_commit(drain);
+    drain_mbar(drain, 0, 200000000ull);
+  } else if (warp >= 4) {
+    // ------------------------------------------------ epilogue warps
+    const int et = threadIdx.x - 128;  // TMEM lane = row within the tile
+    const int ew = et >> 5;
+    // (1) quantise this block's slice of x: the 32-blocks [b0, b1) of the
+    // row-major [npad, H/32] block grid (rows >= M only get a zero scale)
+    if (a.x != nullptr && !a.local_xq) {
+      const int nbk = a.H / 32;
+      const long long NB = static_cast<long long>(npad) * nbk;
+      const long long b0 = range_begin(blockIdx.x, NB, G), b1 = range_begin(blockIdx.x + 1, NB, G);
+      long long b = b0 + et;
+      // issue the first block's loads before the weight stream starts
+      uint4 raw[4];
+      bool have = false;
+      if (b < b1) {
+        const int m = static_cast<int>(b / nbk), kb = static_cast<int>(b % nbk);
+        if (m < a.M) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<long long>(m) * a.H + kb * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) raw[i] = __ldcg(src + i);
+          have = true;
+        }
+      }
+      mbar_arrive(x_issued);
+      for (; b < b1; b += 128) {
+        const int m = static_cast<int>(b / nbk), kb = static_cast<int>(b % nbk);
+        uint32_t s = 0;
+        if (m < a.M) {
+          if (!have) {
+            const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<long long>(m) * a.H + kb * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) raw[i] = __ldcg(src + i);
+          }
+          s = quantize_block_regs(raw, a.xq_codes + static_cast<long long>(m) * a.H + kb * 32);
+        }
+        have = false;
+        a.xq_sf[(kb >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (kb & 3)] = static_cast<uint8_t>(s);
+      }
+      fence_proxy_async_global();
+      epi_bar();
+      if (et == 0) {
+        red_add_release_gpu(a.ctl + kCtlXReady, 1u);
+        FSOPS_STAMP(1);
+      }
+    }
+    // (2) accumulator tiles (and, with local_xq, phase 0's activation tiles)
+    int acc = 0;
+    uint32_t acc_round = 0;
+    int xstage = 0;
+    uint32_t xround = 0;
+    bool ok = true;
+    for (int p = 0; p < a.nphases && ok; ++p) {
+      const PhaseArgs& ph = a.ph[p];
+      const long long U = static_cast<long long>(ph.T) * ph.KS;
+      SegIter it(ph, G);
+      int t, ks0, ks1;
+      while (ok && it.next(t, ks0, ks1)) {
+        if (p == 0 && a.local_xq) {
+          // produce this segment's activation tiles: quantise x[:, 128 ks ..] straight
+          // into each stage, loads running two stages ahead
+          const bool mine = et < 4 * npad;
+          uint4 ra[4], rb[4], rc[4];
+          const int n = ks1 - ks0;
+          if (mine && n > 0) load_x_block(a, ks0, et, ra);
+          if (mine && n > 1) load_x_block(a, ks0 + 1, et, rb);
+          for (int i = 0; i < n && ok; ++i) {
+            if (mine && i + 2 < n) {
+              if (i % 3 == 0) load_x_block(a, ks0 + i + 2, et, rc);
+              else if (i % 3 == 1) load_x_block(a, ks0 + i + 2, et, ra);
+              else load_x_block(a, ks0 + i + 2, et, rb);
+            }
+            if (!wait_mbar(cx, &empty[xstage], (xround & 1u) ^ 1u, kSiteEmpty)) { ok = false; break; }
+            uint8_t* st = smem + static_cast<size_t>(xstage) * a.stage_bytes;
+            if (mine) {
+              if (i % 3 == 0) store_x_block(a, st, et, ra);
+              else if (i % 3 == 1) store_x_block(a, st, et, rb);
+              else store_x_block(a, st, et, rc);
+            }
+            fence_proxy_async_shared();
+            epi_bar();
+            if (et == 0) mbar_arrive(&full_a[xstage]);
+            if (++xstage == S) { xstage = 0; ++xround; }
+          }
+          if (!ok) break;
+        }
+        if (!wait_mbar(cx, &acc_full[acc], acc_round & 1u, kSiteAccFull)) { ok = false; break; }
+        tc_fence_after();
+        if (et == 0) FSOPS_STAMP(p == 0 ? 3 : 8);
+        const uint32_t tacc = tmem + (static_cast<uint32_t>(ew * 32) << 16) + acc * acc_cols;
+        if (ks0 == 0 && ks1 == ph.KS) {
+          // the whole K range of tile t is in this accumulator
+          for (int c0 = 0; c0 < a.M; c0 += 16) {
+            float v[16];
+            tmem_chunk_sum(tacc + c0, a.chains, npad, v);
+            if (ph.epi == kEpiSwiGLU) epi_swiglu_chunk(a, t, c0, v, et, xchg);
+            else epi_store_chunk(a, ph, t, c0, v, et);
+          }
+          tc_fence_before();
+          mbar_arrive(&acc_empty[acc]);
+          if (ph.epi == kEpiSwiGLU) publish_swiglu_tile(a, t, et);
+        } else {
+          // The K range of tile t is split over several blocks: add this
+          // block's fp32 sums into the tile's accumulator in L2; the block
+          // that arrives last reads the total, finishes the tile and leaves
+          // the accumulator zero for the next launch.
+          float* accg = ph.accum + static_cast<long long>(t) * a.M * 128 + et;
+          for (int c0 = 0; c0 < a.M; c0 += 16) {
+            float v[16];
+            tmem_chunk_sum(tacc + c0, a.chains, npad, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < a.M) atomicAdd(accg + static_cast<long long>(c0 + j) * 128, v[j]);
+          }
+          tc_fence_before();
+          mbar_arrive(&acc_empty[acc]);
+          const long long cf = owner_of(static_cast<long long>(t) * ph.KS, U, G);
+          const long long cl = owner_of(static_cast<long long>(t) * ph.KS + ph.KS - 1, U, G);
+          // with U >= G every block owns at least one unit; with U < G each owns at most one
+          const uint32_t expected = static_cast<uint32_t>(U >= G ? cl - cf + 1 : ph.KS);
+          // the barrier orders every thread's adds before thread 0's acq_rel
+          // counter update, which in turn orders the last arriver's reads
+          epi_bar();
+          if (et == 0) {
+            const uint32_t old = atom_add_acq_rel_gpu(ph.tile_cnt + t, 1u);
+            *bcast = (old + 1 == expected) ? 1 : 0;
+          }
+          epi_bar();
+          const bool last = *bcast != 0;
+          epi_bar();
+          if (last) {
+            for (int c0 = 0; c0 < a.M; c0 += 16) {
+              float v[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                v[j] = 0.f;
+                if (c0 + j < a.M) {
+                  float* q = accg + static_cast<long long>(c0 + j) * 128;
+                  v[j] = __ldcg(q);
+                  __stcg(q, 0.f);
+                }
+              }
+              if (ph.epi == kEpiSwiGLU) epi_swiglu_chunk(a, t, c0, v, et, xchg);
+              else epi_store_chunk(a, ph, t, c0, v, et);
+            }
+            if (ph.epi == kEpiSwiGLU) publish_swiglu_tile(a, t, et);
+          }
+        }
+        if (++acc == a.nacc) { acc = 0; ++acc_round; }
+        if (et == 0) FSOPS_STAMP(p == 0 ? 4 : 9);
+      }
+    }
+    if (!ok) *abort_flag = 1;
+  }
+
+  // ------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0) {
+    FSOPS_STAMP(10);
+    __threadfence();
+    const uint32_t old = atom_add_acq_rel_gpu(a.ctl + kCtlDone, 1u);
+    if (old + 1 == static_cast<uint32_t>(G)) {
+      // every block has finished: leave the control words zero for the next launch
+      for (int p = 0; p < a.nphases; ++p)
+        for (int t = 0; t < a.ph[p].T; ++t) a.ph[p].tile_cnt[t] = 0u;
+      if (a.hflags != nullptr)
+        for (int t = 0; t < a.I / 128; ++t) a.hflags[t] = 0u;
+      a.ctl[kCtlXReady] = 0u;
+      __threadfence();
+      a.ctl[kCtlDone] = 0u;
+    }
+  }
+}
+
+cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(mx_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kMaxSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mx_persistent_kernel, a);
+}
+
+}  // namespace fsops

@@ -1,0 +1,116 @@
+"""The C ABI library loads without a GPU, exports every function that
+include/fsops.h declares, and rejects bad arguments on the host before any
+CUDA call (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "fsops.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(fsops_[a-z0-9_]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def fs():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import mxfp8_swiglu_mlp_gb300 as fs
+
+    return fs
+
+
+def test_every_declared_symbol_is_exported(fs):
+    names = _declared_functions()
+    assert len(names) >= 15, names
+    for n in names:
+        assert hasattr(fs.lib, n), n
+
+
+def test_status_strings(fs):
+    for s in range(7):
+        assert fs.fsops_status_string(s) != "unknown status"
+    assert fs.fsops_status_string(99) == "unknown status"
+    assert fs.fsops_version() >= 100
+
+
+def test_scale_bytes(fs):
+    assert fs.fsops_scale_bytes(300, 384, fs.SCALES_ROWMAJOR) == 300 * 12
+    assert fs.fsops_scale_bytes(300, 384, fs.SCALES_TCGEN05) == 3 * 3 * 512
+    assert fs.fsops_scale_bytes(1, 128, fs.SCALES_TCGEN05) == 512
+    assert fs.fsops_scale_bytes(10, 128, 7) == 0
+
+
+FAKE = 0x100000  # 16-byte aligned, never dereferenced: every call below fails validation first
+
+
+def test_mlp_validation(fs):
+    lib = fs.lib
+    sc = fs._MlpScales(FAKE, FAKE)
+    call = lambda x=FAKE, w1=FAKE, w2=FAKE, s=ctypes.byref(sc), y=FAKE, M=16, H=256, I=256: \
+        lib.fsops_mxfp8_swiglu_mlp(x, w1, w2, s, y, M, H, I, None)
+    assert call(x=None) == fs.ERR_INVALID_ARG
+    assert call(y=None) == fs.ERR_INVALID_ARG
+    assert call(s=None) == fs.ERR_INVALID_ARG
+    for M in (0, 129, -1):
+        assert call(M=M) == fs.ERR_UNSUPPORTED_SHAPE
+    for H, I in ((200, 256), (256, 100), (0, 256), (128 * 513, 256)):
+        assert call(H=H, I=I) == fs.ERR_UNSUPPORTED_SHAPE
+    assert call(x=FAKE + 2) == fs.ERR_MISALIGNED
+    assert call(w2=FAKE + 8) == fs.ERR_MISALIGNED
+    assert call(y=FAKE + 4) == fs.ERR_MISALIGNED
+    bad = fs._MlpScales(FAKE + 1, FAKE)
+    assert call(s=ctypes.byref(bad)) == fs.ERR_MISALIGNED
+    nul = fs._MlpScales(None, FAKE)
+    assert call(s=ctypes.byref(nul)) == fs.ERR_INVALID_ARG
+    assert lib.fsops_mxfp8_swiglu_mlp_unfused(FAKE, FAKE, FAKE, ctypes.byref(sc), FAKE, 0, 256, 256, None) \
+        == fs.ERR_UNSUPPORTED_SHAPE
+
+
+def test_gemm_validation(fs):
+    lib = fs.lib
+    g = lambda a=FAKE, asc=None, adt=fs.DTYPE_BF16, b=FAKE, bs=FAKE, c=FAKE, cdt=fs.DTYPE_BF16, M=4, N=256, K=256, \
+        ws=FAKE, n=1 << 30: lib.fsops_mxfp8_gemm_ex(a, asc, adt, b, bs, c, cdt, M, N, K, ws, n, None)
+    assert g(a=None) == fs.ERR_INVALID_ARG
+    assert g(ws=None) == fs.ERR_INVALID_ARG
+    assert g(adt=fs.DTYPE_F32) == fs.ERR_INVALID_ARG
+    assert g(cdt=fs.DTYPE_MXFP8) == fs.ERR_INVALID_ARG
+    assert g(asc=FAKE) == fs.ERR_INVALID_ARG                 # bf16 A takes no scales
+    assert g(adt=fs.DTYPE_MXFP8) == fs.ERR_INVALID_ARG      # MXFP8 A needs scales
+    for M, N, K in ((0, 256, 256), (129, 256, 256), (4, 200, 256), (4, 256, 100), (4, 256, 65536 + 128)):
+        assert g(M=M, N=N, K=K) == fs.ERR_UNSUPPORTED_SHAPE
+    assert g(c=FAKE + 2) == fs.ERR_MISALIGNED
+    assert g(b=FAKE + 8) == fs.ERR_MISALIGNED
+    assert lib.fsops_mxfp8_gemm(FAKE, FAKE, FAKE, FAKE, 0, 256, 256, FAKE, 1 << 30, None) == fs.ERR_UNSUPPORTED_SHAPE
+
+
+def test_quantize_validation(fs):
+    lib = fs.lib
+    q = lambda x=FAKE, rows=4, K=256, ld=256, c=FAKE, s=FAKE, layout=fs.SCALES_TCGEN05: \
+        lib.fsops_quantize_mxfp8(x, rows, K, ld, c, s, layout, None)
+    assert q(layout=5) == fs.ERR_INVALID_ARG
+    assert q(K=96) == fs.ERR_UNSUPPORTED_SHAPE                # tiled layout wants K % 128
+    assert q(K=100, layout=fs.SCALES_ROWMAJOR, ld=104) == fs.ERR_UNSUPPORTED_SHAPE
+    assert q(ld=100) == fs.ERR_UNSUPPORTED_SHAPE              # ld < K
+    assert q(ld=260) == fs.ERR_UNSUPPORTED_SHAPE              # ld % 8
+    assert q(rows=-1) == fs.ERR_UNSUPPORTED_SHAPE
+    assert q(rows=0, x=None) == fs.OK                         # empty input: nothing to do
+    assert q(x=None) == fs.ERR_INVALID_ARG
+    assert q(x=FAKE + 2) == fs.ERR_MISALIGNED
+    assert lib.fsops_swiglu_quantize_mxfp8(FAKE, 0, 256, FAKE, FAKE, None) == fs.ERR_UNSUPPORTED_SHAPE
+    assert lib.fsops_swiglu_quantize_mxfp8(FAKE, 4, 200, FAKE, FAKE, None) == fs.ERR_UNSUPPORTED_SHAPE
+    assert lib.fsops_swiglu_quantize_mxfp8(None, 4, 256, FAKE, FAKE, None) == fs.ERR_INVALID_ARG
+
+
+def test_size_queries_reject_bad_shapes(fs):
+    assert fs.fsops_mlp_workspace_bytes(0, 256, 256) == 0
+    assert fs.fsops_gemm_workspace_bytes(4, 100, 256) == 0
+    assert fs.lib.fsops_set_wait_timeout_ns(0) == fs.ERR_INVALID_ARG

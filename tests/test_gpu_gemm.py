@@ -1,0 +1,108 @@
+"""Block-scaled MXFP8 GEMM (fsops_mxfp8_gemm / _ex) against the oracle's fp64
+GEMM of the dequantised operands."""
+import numpy as np
+import pytest
+
+import oracle
+from workloads import inputs
+from tests._util import to_dev_u16, from_dev_bf16, bf16_bits_to_f64, rel_l2, max_abs_norm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fs():
+    import mxfp8_swiglu_mlp_gb300 as fs
+
+    return fs
+
+
+def _operands(M, N, K, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    a = inputs.bf16_bits_from_f32(rng.standard_normal((M, K), dtype=np.float32))
+    w = rng.standard_normal((N, K), dtype=np.float32) / np.sqrt(K)
+    w.reshape(-1)[rng.choice(N * K, max(1, N * K // 1000), replace=False)] *= 20
+    return a, inputs.bf16_bits_from_f32(w)
+
+
+def _gpu_gemm(fs, a_bits, b_bits, c_f32=False, prequant=False):
+    import torch
+
+    M, K = a_bits.shape
+    N = b_bits.shape[0]
+    bc, bs = fs.quantize_weight(to_dev_u16(b_bits))
+    ws_n = fs.fsops_gemm_workspace_bytes(M, N, K)
+    ws = torch.zeros(ws_n, dtype=torch.uint8, device="cuda")
+    c = torch.empty((M, N), dtype=torch.float32 if c_f32 else torch.bfloat16, device="cuda")
+    outs = []
+    for _ in range(2):  # the second call reuses the workspace the first one left behind
+        if prequant:
+            ac, asc = fs.quantize_weight(to_dev_u16(a_bits))
+            fs.fsops_mxfp8_gemm_ex(ac, asc, fs.DTYPE_MXFP8, bc, bs, c, fs.DTYPE_F32 if c_f32 else fs.DTYPE_BF16,
+                                   M, N, K, ws, ws_n)
+        elif c_f32:
+            fs.fsops_mxfp8_gemm_ex(to_dev_u16(a_bits), None, fs.DTYPE_BF16, bc, bs, c, fs.DTYPE_F32, M, N, K, ws,
+                                   ws_n)
+        else:
+            fs.fsops_mxfp8_gemm(to_dev_u16(a_bits), bc, bs, c, M, N, K, ws, ws_n)
+        torch.cuda.synchronize()
+        assert fs.fsops_read_kernel_status(ws) == 0
+        assert int(ws[:8192].count_nonzero()) == 0, "control words not reset"
+        outs.append(c.cpu().numpy().astype(np.float64) if c_f32 else bf16_bits_to_f64(from_dev_bf16(c)))
+    # split-K sums are added in arrival order: repeated calls agree to fp32
+    # rounding (a bf16 output can then differ by one bf16 step in a few places)
+    assert rel_l2(outs[1], outs[0]) < (1e-6 if c_f32 else 1e-3)
+    if not c_f32:
+        assert np.mean(outs[1] == outs[0]) > 0.99
+    return outs[1]
+
+
+SHAPES = [(1, 256, 128), (3, 384, 256), (16, 512, 1024), (17, 256, 384), (64, 1024, 512), (127, 128, 256),
+          (128, 768, 2048), (2, 2560, 9728)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_gemm_fp32_out_matches_oracle(fs, M, N, K):
+    a, b = _operands(M, N, K, seed=M * 1000 + N + K)
+    bc, bs = oracle.quantize_bf16(b)
+    ref = oracle.gemm(a, bc, bs)["c"]
+    got = _gpu_gemm(fs, a, b, c_f32=True)
+    assert rel_l2(got, ref) < 1e-5, rel_l2(got, ref)
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES[:6])
+def test_gemm_bf16_out_matches_oracle(fs, M, N, K):
+    a, b = _operands(M, N, K, seed=M + N + K)
+    bc, bs = oracle.quantize_bf16(b)
+    res = oracle.gemm(a, bc, bs)
+    got = _gpu_gemm(fs, a, b)
+    ref = bf16_bits_to_f64(res["c_bf16"])
+    assert rel_l2(got, ref) < 2e-3
+    assert max_abs_norm(got, ref) < 1e-2
+    # fp32 accumulation differs from fp64 only in the last bits: most outputs are the same bf16
+    assert np.mean(got == ref) > 0.9
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 384, 256), (128, 512, 640)])
+def test_gemm_prequantised_a(fs, M, N, K):
+    a, b = _operands(M, N, K, seed=7 * M + K)
+    bc, bs = oracle.quantize_bf16(b)
+    ref = oracle.gemm(a, bc, bs)["c"]
+    got = _gpu_gemm(fs, a, b, c_f32=True, prequant=True)
+    assert rel_l2(got, ref) < 1e-5
+
+
+def test_gemm_zero_blocks_and_scale_spread(fs):
+    M, N, K = 8, 256, 512
+    rng = np.random.default_rng(11)
+    a = rng.standard_normal((M, K)).astype(np.float32) * (10.0 ** rng.uniform(-3, 3, (M, 1)))
+    a[:, 64:96] = 0.0
+    b = rng.standard_normal((N, K)).astype(np.float32) * 0.05
+    b.reshape(-1, 32)[rng.choice(N * K // 32, N * K // 320, replace=False)] = 0.0
+    a, b = inputs.bf16_bits_from_f32(a), inputs.bf16_bits_from_f32(b)
+    bc, bs = oracle.quantize_bf16(b)
+    ref = oracle.gemm(a, bc, bs)["c"]
+    got = _gpu_gemm(fs, a, b, c_f32=True)
+    assert rel_l2(got, ref) < 1e-5
+    for m in range(M):
+        assert rel_l2(got[m], ref[m]) < 1e-5
