@@ -41,9 +41,10 @@ std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 unsigned long long* g_trace = nullptr;
 #endif
 std::atomic<uint32_t> g_extra{0};
-// Weight tiles (16 KB each) a block keeps in flight: 4 x 16 KB x 152 SMs is
-// about 10 MB, enough to cover the HBM latency at full bandwidth without
-// queueing that inflates every other round trip.
+// Weight tiles (32 KB each) a block keeps in flight: 4 x 32 KB per SM covers
+// the loaded HBM latency (~1.5 us) at the SM's share of the bandwidth even
+// when only half the SMs stream; deeper queues only add latency to every other
+// memory round trip.
 std::atomic<int> g_max_inflight{4};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -89,39 +90,31 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int npad_of(int M) { return (M + 15) / 16 * 16; }
 
-int stages_for(int npad) {
-  const uint32_t sb = stage_bytes_for(npad);
-  int s = static_cast<int>((kMaxSmem - 1024 - kSmemCtlBytes - kSmemXchgBytes) / sb);
+// Accumulators are staged through shared memory (and all four epilogue warps
+// share the work) when the tokens fit one TMEM lane quarter.
+int stage_tmem_for(int npad) { return npad <= 32 ? 1 : 0; }
+// Small M: every block quantises the k-chunks of x it needs itself (no
+// grid-wide exchange before the first MMA; one warp, two 32-blocks per lane per
+// stage).  Larger M: x is quantised once, each block a slice, shared through L2.
+int local_xq_for(int npad) {
+  if (const char* env = std::getenv("FSOPS_LOCAL_XQ")) return std::atoi(env) != 0 && npad <= 16;
+  return npad <= 16 ? 1 : 0;
+}
+// Shared memory besides the stage ring (local_xq is only used with x quantised in-kernel).
+uint32_t extra_smem(int npad, int local_xq) {
+  return (stage_tmem_for(npad) ? stg_bytes_for(npad) : 0u) + (local_xq ? xring_bytes_for(npad) : 0u) +
+         kSmemCtlBytes + 1024u;
+}
+int stages_for(int npad, int local_xq) {
+  int s = static_cast<int>((kMaxSmem - extra_smem(npad, local_xq)) / stage_bytes_for(npad));
   if (s > kMaxStages) s = kMaxStages;
   return s;
 }
-// Independent accumulators per tile: small N makes each MMA short, so the
-// dependency through a single accumulator would serialise the four MMAs of a
-// stage; more chains let them overlap (their sum is taken in the epilogue).
-int chains_for(int npad) {
-  if (const char* env = std::getenv("FSOPS_MMA_CHAINS")) {
-    const int v = std::atoi(env);
-    if ((v == 1 || v == 2 || v == 4) && v * npad <= 256) return v;
-  }
-  return npad <= 32 ? 4 : (npad <= 112 ? 2 : 1);
+size_t smem_for(int npad, int local_xq) {
+  return static_cast<size_t>(stages_for(npad, local_xq)) * stage_bytes_for(npad) + extra_smem(npad, local_xq);
 }
-// Accumulator buffers: as many as TMEM holds next to the scale-tile ring (at most 4).
-int nacc_for(int npad, int stages) {
-  int n = (static_cast<int>(kTmemCols) - static_cast<int>(kSfColsPerStage) * stages) / (chains_for(npad) * npad);
-  return n > 4 ? 4 : n;
-}
-// Small M: every block quantises the k-chunks of x it needs itself (no
-// grid-wide exchange before the first MMA).  Large M: x is quantised once,
-// each block a slice, and shared through L2.
-int local_xq_for(int npad) {
-  if (const char* env = std::getenv("FSOPS_LOCAL_XQ")) return std::atoi(env) != 0 && npad <= 32;
-  return npad <= 32 ? 1 : 0;
-}
-size_t smem_for(int npad) {
-  return static_cast<size_t>(stages_for(npad)) * stage_bytes_for(npad) + kSmemXchgBytes + kSmemCtlBytes + 1024;
-}
-// fp32 accumulators of split tiles: [tiles][M][128]
-size_t accum_bytes(int M, int tiles) { return round_up(static_cast<size_t>(tiles) * M * 128 * 4, 1024); }
+// fp32 accumulators of split tiles: [tiles][M][256]
+size_t accum_bytes(int M, int tiles) { return round_up(static_cast<size_t>(tiles) * M * kTileRows * 4, 1024); }
 
 // ---------------------------------------------------------------- workspace layouts
 struct GemmLayout {
@@ -133,7 +126,7 @@ GemmLayout gemm_layout(int M, int N, int K) {
   l.xq = kCtlRegionBytes;
   l.xq_sf = l.xq + round_up(static_cast<size_t>(M) * K, 1024);
   l.part = l.xq_sf + round_up(static_cast<size_t>(K / 128) * 512, 1024);
-  l.total = l.part + accum_bytes(M, N / 128);
+  l.total = l.part + accum_bytes(M, (N + kTileRows - 1) / kTileRows);
   return l;
 }
 struct MlpLayout {
@@ -147,8 +140,8 @@ MlpLayout mlp_layout(int M, int H, int I) {
   l.hq = l.xq_sf + round_up(static_cast<size_t>(H / 128) * 512, 1024);
   l.hq_sf = l.hq + round_up(static_cast<size_t>(M) * I, 1024);
   l.part0 = l.hq_sf + round_up(static_cast<size_t>(I / 128) * 512, 1024);
-  l.part1 = l.part0 + accum_bytes(M, I / 64);
-  l.gu = l.part1 + accum_bytes(M, H / 128);
+  l.part1 = l.part0 + accum_bytes(M, I / kPairFeatures);
+  l.gu = l.part1 + accum_bytes(M, (H + kTileRows - 1) / kTileRows);
   l.total = l.gu + round_up(static_cast<size_t>(M) * 2 * I * 4, 1024);
   return l;
 }
@@ -166,13 +159,28 @@ bool encode_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows)
   return r == CUDA_SUCCESS;
 }
 
+int whole_tiles_enabled() {
+  if (const char* env = std::getenv("FSOPS_WHOLE_TILES")) return std::atoi(env) != 0;
+  return 1;
+}
+// bf16 x [M, H] for the local quantisation: box npad rows x 128 elements.
+bool encode_x_map(CUtensorMap* m, const void* x, int H, int M, int npad) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(npad)};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 void init_common(KernelArgs& a, int M, uint32_t* ctl) {
   std::memset(&a, 0, sizeof(a));
   a.M = M;
   a.npad = npad_of(M);
-  a.nstages = stages_for(a.npad);
-  a.nacc = nacc_for(a.npad, a.nstages);
-  a.chains = chains_for(a.npad);
+  a.nstages = stages_for(a.npad, 0);  // set again once local_xq is known
+  a.stage_tmem = stage_tmem_for(a.npad);
   a.max_inflight = g_max_inflight.load() < a.nstages ? g_max_inflight.load() : a.nstages;
   a.stage_bytes = stage_bytes_for(a.npad);
   a.timeout_ns = g_timeout_ns.load();
@@ -183,8 +191,10 @@ void init_common(KernelArgs& a, int M, uint32_t* ctl) {
 #endif
 }
 
-fsops_status launch(const KernelArgs& a, int grid, cudaStream_t stream) {
-  cudaError_t e = launch_mx_kernel(a, grid, smem_for(a.npad), stream);
+fsops_status launch(KernelArgs& a, int grid, cudaStream_t stream) {
+  a.nstages = stages_for(a.npad, a.local_xq);
+  if (a.max_inflight > a.nstages) a.max_inflight = a.nstages;
+  cudaError_t e = launch_mx_kernel(a, grid, smem_for(a.npad, a.local_xq), stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FSOPS_ERR_CUDA;
@@ -210,7 +220,8 @@ fsops_status gemm_impl(const void* a, const uint8_t* a_scales, bool a_bf16, cons
   PhaseArgs& p = ka.ph[0];
   p.sf_w = b_scales;
   p.KS = K / kTileK;
-  p.T = N / kTileRows;
+  p.T = (N + kTileRows - 1) / kTileRows;
+  p.rows = N;
   p.epi = kEpiStore;
   p.out_ld = N;
   p.tile_cnt = ka.ctl + kCtlHeaderWords;
@@ -225,6 +236,7 @@ fsops_status gemm_impl(const void* a, const uint8_t* a_scales, bool a_bf16, cons
     p.sf_act = ka.xq_sf;
     ka.local_xq = local_xq_for(ka.npad);
     p.dep = ka.local_xq ? kDepNone : kDepXReady;
+    if (ka.local_xq && !encode_x_map(&ka.tm_x, a, K, M, ka.npad)) return FSOPS_ERR_INVALID_ARG;
   } else {
     act_codes = static_cast<const uint8_t*>(a);
     p.sf_act = a_scales;
@@ -404,9 +416,9 @@ fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup,
 
   KernelArgs ka;
   init_common(ka, M, reinterpret_cast<uint32_t*>(ws + l.ctl));
-  const int Ic = I / 128;           // 128-feature chunks of the intermediate (phase-1 k-stages)
-  const int T0 = I / kPairFeatures; // gate/up pair tiles
-  const int T1 = H / kTileRows;     // down-projection tiles
+  const int Ic = I / 128;                          // 128-feature chunks (phase-1 k-stages)
+  const int T0 = I / kPairFeatures;                // gate/up pair tiles
+  const int T1 = (H + kTileRows - 1) / kTileRows;  // down-projection tiles
   if (ctl_words_needed(Ic, T0, T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
   ka.hflags = ka.ctl + kCtlHeaderWords;
   ka.nphases = 2;
@@ -419,7 +431,7 @@ fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup,
   ka.I = I;
   ka.out = y_bf16;
   ka.out_f32 = 0;
-  // phase 0: gate/up, tile t = rows [128t, 128t+128) of the paired W_gateup
+  // phase 0: gate/up, tile t = rows [256t, 256t+256) of the paired W_gateup
   PhaseArgs& p0 = ka.ph[0];
   p0.sf_w = scales->gateup;
   p0.sf_act = ka.xq_sf;
@@ -427,11 +439,16 @@ fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup,
   p0.accum = reinterpret_cast<float*>(ws + l.part0);
   p0.KS = H / kTileK;
   p0.T = T0;
+  p0.rows = 2 * I;
+  // one whole gate/up tile per block when the tiles fit the grid: the SwiGLU
+  // then needs no split-K reduction before it
+  p0.whole_tiles = (T0 <= grid && whole_tiles_enabled()) ? 1 : 0;
   ka.local_xq = local_xq_for(ka.npad);
   p0.dep = ka.local_xq ? kDepNone : kDepXReady;
+  if (ka.local_xq && !encode_x_map(&ka.tm_x, x_bf16, H, M, ka.npad)) return FSOPS_ERR_INVALID_ARG;
   p0.epi = kEpiSwiGLU;
   p0.out_ld = I;
-  // phase 1: down projection, tile t = rows [128t, 128t+128) of W_down
+  // phase 1: down projection, tile t = rows [256t, 256t+256) of W_down
   PhaseArgs& p1 = ka.ph[1];
   p1.sf_w = scales->down;
   p1.sf_act = ka.hq_sf;
@@ -439,6 +456,7 @@ fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup,
   p1.accum = reinterpret_cast<float*>(ws + l.part1);
   p1.KS = I / kTileK;
   p1.T = T1;
+  p1.rows = H;
   p1.dep = kDepHFlags;
   p1.epi = kEpiStore;
   p1.out_ld = H;

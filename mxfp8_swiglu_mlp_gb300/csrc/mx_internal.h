@@ -25,39 +25,44 @@ enum : int { kDepNone = 0, kDepXReady = 1, kDepHFlags = 2 };
 enum : int { kEpiSwiGLU = 0, kEpiStore = 1 };
 
 constexpr int kThreads = 256;       // 8 warps: 0 weight TMA, 1 activation TMA, 2 MMA, 3 idle, 4-7 epilogue
-constexpr int kMaxStages = 12;
+constexpr int kMaxStages = 8;
 constexpr int kTileK = 128;         // K elements (bytes) per pipeline stage
-constexpr int kTileRows = 128;      // weight rows per tile = M of the tcgen05 instruction
+constexpr int kTileRows = 256;      // weight rows per tile = N of the tcgen05 instruction
+constexpr int kMmaM = 128;          // M of the tcgen05 instruction: token rows (padded)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxSmem = 232448;    // 227 KB opt-in per block
 
-// W_gateup row order: 128-row blocks j = [W_gate rows 64j..64j+63; W_up rows
-// 64j..64j+63], so one 128-row tile holds a gate/up pair for 64 intermediate
-// features and its scales form one 512-byte scale tile.
-constexpr int kPairFeatures = 64;
+// W_gateup row order: 256-row blocks j = [W_gate rows 128j..128j+127; W_up
+// rows 128j..128j+127], so one weight tile holds a gate/up pair for 128
+// intermediate features (its two 512-byte scale tiles are the gate and the up
+// scales of those features).
+constexpr int kPairFeatures = 128;
 
-// One GEMM phase of the persistent kernel: T tiles of 128 weight rows times KS
-// k-stages of 128, split evenly over the grid (stream-K).
+// One GEMM phase of the persistent kernel: T tiles of 256 weight rows times
+// KS k-stages of 128, split evenly over the grid (stream-K).
 struct PhaseArgs {
   const uint8_t* sf_w;    // weight scales (tiled layout)
   const uint8_t* sf_act;  // activation scales (tiled layout, row tile 0)
   uint32_t* tile_cnt;     // [T] arrival counters for split tiles
-  float* accum;           // [T][M][128] fp32 sums of split tiles, zero between launches
+  float* accum;           // [T][256][M] fp32 sums of split tiles (column-major), zero between launches
   int KS;                 // K / 128
-  int T;                  // number of tiles (rows / 128)
+  int T;                  // number of tiles (ceil(rows / 256))
+  int rows;               // weight rows (a multiple of 128)
+  int whole_tiles;        // 1: block t < T does all of tile t (requires T <= grid), no split-K
   int dep;                // what the activation loads wait for (kDep*)
   int epi;                // epilogue kind (kEpi*)
   int out_ld;             // row stride (elements) of the plain output
 };
 
 struct KernelArgs {
-  CUtensorMap tm_w[2];    // weight codes [rows, K] u8, box 128 x 128, 128B swizzle
-  CUtensorMap tm_act[2];  // activation codes [M, K] u8, box 128 x npad, 128B swizzle
+  CUtensorMap tm_w[2];    // weight codes [rows, K] u8, box 256 x 128, 128B swizzle
+  CUtensorMap tm_act[2];  // activation codes [M, K] u8, box npad x 128, 128B swizzle
+  CUtensorMap tm_x;       // bf16 x [M, H], box npad x 128 elements, no swizzle (local_xq only)
   PhaseArgs ph[2];
   int nphases;
-  // in-kernel activation quantisation (x != nullptr)
+  // activation quantisation (x != nullptr)
   const uint16_t* x;      // bf16 [M, H]
-  uint8_t* xq_codes;      // [M, H]
+  uint8_t* xq_codes;      // [M, H] (grid-wide quantisation only)
   uint8_t* xq_sf;         // tiled, H / 128 tiles
   int H;
   // SwiGLU epilogue output
@@ -69,13 +74,12 @@ struct KernelArgs {
   int out_f32;
   // control
   uint32_t* ctl;          // kCtlHeaderWords words
-  uint32_t* hflags;       // [I / 128]: SwiGLU tiles finished per 128-feature chunk (2 when ready)
+  uint32_t* hflags;       // [I / 128]: 1 once SwiGLU tile t (features 128t..128t+127) is written
   int M;
-  int npad;               // M rounded up to 16 (the MMA N)
+  int npad;               // M rounded up to 16: activation rows held in shared memory
   int nstages;
-  int nacc;               // accumulator buffers in TMEM
-  int chains;             // independent accumulators per tile (k-step k adds into chain k % chains)
-  int local_xq;           // 1: phase 0's activation tiles are quantised from x by each block itself
+  int local_xq;           // 1: phase 0's activation tiles are quantised from x by each block itself (npad <= 32)
+  int stage_tmem;         // 1: accumulators are copied to shared memory before the epilogue (M <= 32)
   int max_inflight;       // weight tiles a block may have in flight at once
   uint32_t stage_bytes;
   uint64_t timeout_ns;
@@ -83,19 +87,30 @@ struct KernelArgs {
   unsigned long long* trace;  // [grid][64] %globaltimer stamps, builds with FSOPS_TRACE only
 };
 
-// Shared-memory stage layout: A (weights, 128 x 128 B), B (activations,
-// npad x 128 B), the A scale tile and the B scale tile (512 B each).
-__host__ __device__ constexpr uint32_t stage_off_a() { return 0; }
-__host__ __device__ constexpr uint32_t stage_off_b() { return 16384; }
-__host__ __device__ inline uint32_t stage_off_sfa(int npad) { return 16384u + 128u * npad; }
-__host__ __device__ inline uint32_t stage_off_sfb(int npad) { return 16384u + 128u * npad + 512u; }
+// Shared-memory stage layout: X (activations, npad x 128 B), W (weights,
+// 256 x 128 B), two weight scale tiles, one activation scale tile.  The MMA
+// reads 128 activation rows; rows past npad alias the start of W and only
+// produce accumulator lanes that are never read.
+__host__ __device__ inline uint32_t stage_off_w(int npad) { return 128u * npad; }
+__host__ __device__ inline uint32_t stage_off_sfw(int npad) { return 128u * npad + 32768u; }
+__host__ __device__ inline uint32_t stage_off_sfx(int npad) { return 128u * npad + 32768u + 1024u; }
 __host__ __device__ inline uint32_t stage_bytes_for(int npad) {
-  return (16384u + 128u * npad + 1024u + 1023u) & ~1023u;
+  return (128u * npad + 32768u + 1536u + 1023u) & ~1023u;
 }
 constexpr uint32_t kSmemCtlBytes = 1024;
-constexpr uint32_t kSmemXchgBytes = 16 * 128 * 4;  // one 16-token chunk of a 128-row tile, fp32
-// TMEM columns of one stage's scale tiles (A, then B).
-constexpr uint32_t kSfColsPerStage = 8;
+// fp32 staging of one accumulator (npad <= 32 tokens x 256 columns, padded rows)
+constexpr int kStageLd = 260;
+__host__ __device__ inline uint32_t stg_bytes_for(int npad) {
+  return (static_cast<uint32_t>(npad) * kStageLd * 4u + 1023u) & ~1023u;
+}
+// With local_xq: a ring of bf16 x tiles (npad x 128 elements each) that the
+// activation producer warp fills by TMA and quantises into the stages.
+constexpr int kMaxXSlots = 4;
+__host__ __device__ inline uint32_t xring_bytes_for(int npad) { return kMaxXSlots * 256u * npad; }
+// TMEM columns: accumulator [0, 256), then per pipeline stage 12 scale columns
+// (activation tile: 4, weight tiles: 8).
+constexpr uint32_t kAccCols = 256;
+constexpr uint32_t kSfColsPerStage = 12;
 
 // Launch wrappers (mx_kernels.cu).
 cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStream_t stream);

@@ -121,7 +121,8 @@ cudaError_t launch_quantize(const uint16_t* x, int rows, int K, int ld, uint8_t*
 // ======================================================================
 // SwiGLU + requantisation (the middle launch of the unfused path).
 // ======================================================================
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+// SiLU(g) * u = g * sigmoid(g) * u; for g -> -inf the reciprocal of inf is 0.
+__device__ __forceinline__ float silu_mul(float g, float u) { return g * __frcp_rn(1.0f + __expf(-g)) * u; }
 
 __global__ void swiglu_quantize_kernel(const float* __restrict__ gu, int M, int npad, int I,
                                        uint8_t* __restrict__ hc, uint8_t* __restrict__ hs) {
@@ -178,16 +179,23 @@ cudaError_t launch_swiglu_quantize(const float* gu, int M, int I, uint8_t* hc, u
 // ======================================================================
 // The persistent block-scaled GEMM / fused MLP kernel.
 //
+// Orientation: D[token, weight row] = X[token, :] . W[row, :]^T.  The tcgen05
+// instruction's A operand is the activation tile (M = 128 token rows, npad of
+// them real) and its B operand is a 256-row weight tile (N = 256).  A
+// block-scaled MMA of M = 128, K = 32 takes the same time for every N up to
+// 256, so this orientation moves 8 KB of weights per instruction; the
+// accumulator holds one token per TMEM lane and one weight row per column.
+//
 // Roles (one block per SM, 8 warps):
-//   warp 0 lane 0  weight producer: TMA of 128 x 128 B weight tiles + their
-//                  512-byte scale tiles into a ring of shared-memory stages
+//   warp 0 lane 0  weight producer: TMA of 256 x 128 B weight tiles and their
+//                  two 512-byte scale tiles into a ring of stages
 //   warp 1 lane 0  activation producer: waits until its operand exists (the
-//                  grid-wide x quantisation, or the SwiGLU tiles of the
-//                  k-range) and TMA-loads the npad x 128 B activation tile
-//   warp 2 lane 0  MMA issuer: tcgen05.cp of both scale tiles into TMEM, four
-//                  kind::mxf8f6f4 block-scaled MMAs (K = 32 each) per stage
-//   warps 4-7      quantise this block's slice of x, then drain accumulators
-//                  (TMEM lanes 0..127 = tile rows) into the epilogue
+//                  grid-wide x quantisation, or the SwiGLU tile of the k-chunk)
+//                  and TMA-loads the npad x 128 B activation tile
+//   warp 2 lane 0  MMA issuer: tcgen05.cp of the three scale tiles into TMEM,
+//                  four kind::mxf8f6f4 block-scaled MMAs (K = 32 each) per stage
+//   warps 4-7      quantise x (grid slice, or each stage's tile when M <= 32),
+//                  then run the epilogue of every accumulator
 // ======================================================================
 struct Ctx {
   volatile int* abort_flag;
@@ -273,10 +281,15 @@ struct SegIter {
   long long u, ue;
   int KS;
   __device__ SegIter(const PhaseArgs& p, long long G) {
-    const long long U = static_cast<long long>(p.T) * p.KS;
-    u = range_begin(blockIdx.x, U, G);
-    ue = range_begin(blockIdx.x + 1, U, G);
     KS = p.KS;
+    if (p.whole_tiles) {
+      u = blockIdx.x < p.T ? static_cast<long long>(blockIdx.x) * KS : 0;
+      ue = blockIdx.x < p.T ? u + KS : 0;
+    } else {
+      const long long U = static_cast<long long>(p.T) * p.KS;
+      u = range_begin(blockIdx.x, U, G);
+      ue = range_begin(blockIdx.x + 1, U, G);
+    }
   }
   __device__ bool next(int& t, int& ks0, int& ks1) {
     if (u >= ue) return false;
@@ -290,96 +303,74 @@ struct SegIter {
 };
 
 // ----------------------------------------------------------------------------
-// Epilogues.  Thread et (0..127) owns row et of the tile; v[j] is its value
-// for token c0 + j.
+// Epilogue pieces.  A tile's result row for token r is 256 fp32 values (128
+// when the weight matrix ends half way through the tile).
 // ----------------------------------------------------------------------------
 
-// Plain GEMM output: C[tok, 128 t + et].
-__device__ __forceinline__ void epi_store_chunk(const KernelArgs& a, const PhaseArgs& p, int t, int c0,
-                                                const float (&v)[16], int et) {
-  const long long col = static_cast<long long>(t) * kTileRows + et;
+// SwiGLU + requantisation of 32 intermediate features 128 t + 32 b of token r:
+// g[i], u[i] are the gate and up sums of those features.
+__device__ __forceinline__ void swiglu_block(const KernelArgs& a, int t, int b, int r, const float* g,
+                                             const float* u) {
+  float h[32];
+  float amax = 0.f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int tok = c0 + j;
-    if (tok < a.M) {
-      const long long o = static_cast<long long>(tok) * p.out_ld + col;
-      if (a.out_f32) static_cast<float*>(a.out)[o] = v[j];
-      else static_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16_rn(v[j]);
+  for (int i = 0; i < 32; ++i) {
+    h[i] = silu_mul(g[i], u[i]);
+    amax = fmaxf(amax, fabsf(h[i]));
+  }
+  const uint32_t s = ue8m0_from_amax(amax);
+  const float inv = inv_scale_from_ue8m0(s);
+  uint32_t pk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    pk[i] = e4m3_code(h[4 * i] * inv) | (e4m3_code(h[4 * i + 1] * inv) << 8) |
+            (e4m3_code(h[4 * i + 2] * inv) << 16) | (e4m3_code(h[4 * i + 3] * inv) << 24);
+  uint4* dst = reinterpret_cast<uint4*>(a.hq_codes + static_cast<long long>(r) * a.I + t * kPairFeatures + 32 * b);
+  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  a.hq_sf[t * 512 + (r & 31) * 16 + (r >> 5) * 4 + b] = static_cast<uint8_t>(s);
+}
+
+// Plain output: 8 consecutive columns c..c+7 of token r.
+__device__ __forceinline__ void store8(const KernelArgs& a, const PhaseArgs& p, int r, long long col,
+                                       const float* v) {
+  const long long o = static_cast<long long>(r) * p.out_ld + col;
+  if (a.out_f32) {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(a.out) + o);
+    d[0] = make_float4(v[0], v[1], v[2], v[3]);
+    d[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + o) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Epilogue over a tile staged in shared memory (M <= 32): stg[r * kStageLd + c].
+__device__ __forceinline__ void finish_staged(const KernelArgs& a, const PhaseArgs& ph, int t, int ncols,
+                                              const float* stg, int et) {
+  if (ph.epi == kEpiSwiGLU) {
+    const int r = et >> 2, b = et & 3;
+    if (r < a.M) swiglu_block(a, t, b, r, stg + r * kStageLd + 32 * b, stg + r * kStageLd + 128 + 32 * b);
+  } else {
+    const int per_row = ncols / 8;
+    for (int item = et; item < a.M * per_row; item += 128) {
+      const int r = item / per_row, c = (item % per_row) * 8;
+      store8(a, ph, r, static_cast<long long>(t) * kTileRows + c, stg + r * kStageLd + c);
     }
   }
 }
 
-// SwiGLU + requantisation of one gate/up pair tile t (intermediate features
-// 64t..64t+63; rows 0..63 gate, 64..127 up).  The chunk goes through shared
-// memory so that each warp sees gate and up of the same feature: warp w then
-// handles features 64t + 32 (w & 1) + lane for tokens c0 + 8 (w >> 1) + 0..7;
-// a warp holds exactly one 32-feature MX block per token.
-__device__ __forceinline__ void epi_swiglu_chunk(const KernelArgs& a, int t, int c0, const float (&v)[16], int et,
-                                                 float* xchg) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j) xchg[j * 128 + et] = v[j];
-  epi_bar();
-  const int lane = et & 31, w = et >> 5;
-  const int fh = w & 1, th = w >> 1;
-  const int f = t * kPairFeatures + 32 * fh + lane;
-  const int kb = f >> 5;  // MX block along I
-#pragma unroll
-  for (int jj = 0; jj < 8; ++jj) {
-    const int j = 8 * th + jj;
-    const int tok = c0 + j;
-    if (tok >= a.M) break;  // uniform over the warp
-    const float g = xchg[j * 128 + 32 * fh + lane];
-    const float u = xchg[j * 128 + 64 + 32 * fh + lane];
-    const float h = silu_mul(g, u);
-    float amax = fabsf(h);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    const uint32_t s = ue8m0_from_amax(amax);
-    const uint32_t code = e4m3_code(h * inv_scale_from_ue8m0(s));
-    a.hq_codes[static_cast<long long>(tok) * a.I + f] = static_cast<uint8_t>(code);
-    if (lane == 0) a.hq_sf[(kb >> 2) * 512 + (tok & 31) * 16 + (tok >> 5) * 4 + (kb & 3)] = static_cast<uint8_t>(s);
-  }
-  epi_bar();  // xchg is reused by the next chunk
-}
-
-// After every chunk of SwiGLU tile t has been written: publish it.  Each
-// writer orders its stores before later async-proxy (TMA) reads, the barrier
-// orders all of them before thread 0's release-add.
-__device__ __forceinline__ void publish_swiglu_tile(const KernelArgs& a, int t, int et) {
-  fence_proxy_async_global();
-  epi_bar();
-  if (et == 0) red_add_release_gpu(a.hflags + (t >> 1), 1u);
-}
-
-// 16 columns of this thread's TMEM lane, summed over the accumulator chains.
-__device__ __forceinline__ void tmem_chunk_sum(uint32_t taddr, int chains, int npad, float (&v)[16]) {
-  uint32_t r[16];
-  tmem_ld16(taddr, r);
-  tmem_ld_wait();
-#pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-  for (int c = 1; c < chains; ++c) {
-    tmem_ld16(taddr + c * npad, r);
-    tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[j]);
-  }
-}
-
-// Local activation tiles (small M): epilogue thread et < 4 * npad owns the
-// 32-element block (row et / 4, block et % 4) of a 128-wide k-chunk of x.
-__device__ __forceinline__ void load_x_block(const KernelArgs& a, int ks, int et, uint4 (&raw)[4]) {
-  const int r = et >> 2, j = et & 3;
-  if (r < a.M) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<long long>(r) * a.H + ks * kTileK + 32 * j);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + i);
-  }
-}
-// Quantise the block into the stage's activation tile (128-byte swizzled rows,
-// as the TMA would have written them) and its scale tile; rows >= M get zeros.
-__device__ __forceinline__ void store_x_block(const KernelArgs& a, uint8_t* st, int et, const uint4 (&raw)[4]) {
-  const int r = et >> 2, j = et & 3;
+// Local activation tiles (M <= 32): block b of a stage is the 32-element block
+// (row b / 4, block b % 4) of a 128-wide k-chunk of x.  Quantise it into the
+// stage's activation tile (128-byte swizzled rows, as the TMA would have
+// written them) and its scale tile; rows >= M get zeros.
+__device__ __forceinline__ void store_x_block(const KernelArgs& a, uint8_t* st, int b, const uint4 (&raw)[4]) {
+  const int r = b >> 2, j = b & 3;
   uint32_t s = 0;
   uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
   if (r < a.M) {
@@ -388,26 +379,37 @@ __device__ __forceinline__ void store_x_block(const KernelArgs& a, uint8_t* st, 
     c0 = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     c1 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
   }
-  uint8_t* row = st + stage_off_b() + r * 128;
+  uint8_t* row = st + r * 128;
   *reinterpret_cast<uint4*>(row + (((2 * j) ^ (r & 7)) << 4)) = c0;
   *reinterpret_cast<uint4*>(row + (((2 * j + 1) ^ (r & 7)) << 4)) = c1;
-  st[stage_off_sfb(a.npad) + (r & 31) * 16 + (r >> 5) * 4 + j] = static_cast<uint8_t>(s);
+  st[stage_off_sfx(a.npad) + (r & 31) * 16 + (r >> 5) * 4 + j] = static_cast<uint8_t>(s);
+}
+
+// 16 accumulator columns c0.. of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  tmem_ld16(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid_constant__ KernelArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.nstages;
-  float* xchg = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * a.stage_bytes);
-  uint8_t* ctl_smem = reinterpret_cast<uint8_t*>(xchg) + kSmemXchgBytes;
+  float* stg = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * a.stage_bytes);
+  uint8_t* xring = reinterpret_cast<uint8_t*>(stg) + (a.stage_tmem ? stg_bytes_for(a.npad) : 0u);
+  uint8_t* ctl_smem = xring + (a.local_xq ? xring_bytes_for(a.npad) : 0u);
   uint64_t* full_w = reinterpret_cast<uint64_t*>(ctl_smem);
   uint64_t* full_a = full_w + kMaxStages;
   uint64_t* empty = full_a + kMaxStages;
   uint64_t* acc_full = empty + kMaxStages;
-  uint64_t* acc_empty = acc_full + 4;
-  uint64_t* drain = acc_empty + 4;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
   uint64_t* x_issued = drain + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_issued + 1);
+  uint64_t* x_full = x_issued + 1;          // [kMaxXSlots] bf16 x tile landed (local_xq)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_full + kMaxXSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
@@ -420,12 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       mbar_init(&full_a[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 128);
-    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 128);
     mbar_init(drain, 1);
     mbar_init(x_issued, 128);
+    for (int i = 0; i < kMaxXSlots; ++i) mbar_init(&x_full[i], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -438,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       tma_prefetch_desc(&a.tm_w[p]);
       tma_prefetch_desc(&a.tm_act[p]);
     }
+    if (a.local_xq) tma_prefetch_desc(&a.tm_x);
   }
   tc_fence_before();
   __syncthreads();
@@ -451,8 +453,6 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   cx.timeout_ns = a.timeout_ns;
 
   const int npad = a.npad;
-  const uint32_t acc_cols = static_cast<uint32_t>(a.chains * npad);
-  const uint32_t sf_base = static_cast<uint32_t>(a.nacc) * acc_cols;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ weight producer
@@ -460,9 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     uint32_t issued_mask = 0, issued_parity = 0;
     int stage = 0;
     uint32_t round = 0;
-    // the stage `a.max_inflight` loads back: issuing waits until it has landed,
-    // so that a block never has more than max_inflight weight tiles in flight
-    // (deeper queues only add latency to every other memory round trip)
+    // issuing waits until the load `max_inflight` stages back has landed
     int lag_stage = 0;
     uint32_t lag_round = 0, n_issued = 0;
     bool ok = true;
@@ -473,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       SegIter it(ph, G);
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
+        const bool v1 = t * kTileRows + 128 < ph.rows;
         for (int ks = ks0; ks < ks1; ++ks) {
           if (!wait_mbar(cx, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty)) { ok = false; break; }
           if (n_issued >= static_cast<uint32_t>(a.max_inflight)) {
@@ -482,10 +481,11 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           FSOPS_STAMP_IF(n_issued < 24, 40 + n_issued);
           ++n_issued;
           uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
-          mbar_arrive_expect_tx(&full_w[stage], 16384u + 512u);
-          tma_load_2d(st + stage_off_a(), &a.tm_w[p], &full_w[stage], ks * kTileK, t * kTileRows, pol);
-          bulk_load(st + stage_off_sfa(npad), ph.sf_w + (static_cast<size_t>(t) * ph.KS + ks) * 512, 512,
-                    &full_w[stage], pol);
+          mbar_arrive_expect_tx(&full_w[stage], 32768u + (v1 ? 1024u : 512u));
+          tma_load_2d(st + stage_off_w(npad), &a.tm_w[p], &full_w[stage], ks * kTileK, t * kTileRows, pol);
+          const uint8_t* sfw = ph.sf_w + (static_cast<size_t>(2 * t) * ph.KS + ks) * 512;
+          bulk_load(st + stage_off_sfw(npad), sfw, 512, &full_w[stage], pol);
+          if (v1) bulk_load(st + stage_off_sfw(npad) + 512, sfw + static_cast<size_t>(ph.KS) * 512, 512, &full_w[stage], pol);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | ((round & 1u) << stage);
           if (++stage == S) { stage = 0; ++round; }
@@ -495,20 +495,71 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     if (!ok) *abort_flag = 1;
     for (int s = 0; s < S; ++s)
       if (issued_mask & (1u << s)) drain_mbar(&full_w[s], (issued_parity >> s) & 1u, 200000000ull);
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------ activation producer
+    // Lane 0 issues the TMA loads.  With local_xq the whole warp quantises
+    // phase 0's activation tiles itself: lane 0 streams the bf16 x tiles of the
+    // segment into a ring (kMaxXSlots ahead), every lane quantises its 32-blocks
+    // straight into the stage, in step with the stage ring.
     const uint64_t pol = l2_policy_evict_last();
     uint32_t issued_mask = 0, issued_parity = 0;
     int stage = 0;
     uint32_t round = 0;
     bool ok = true, x_ready = false, h_seen = false;
+    uint32_t xc = 0;  // x tiles streamed so far (slot xc % kMaxXSlots, parity (xc / kMaxXSlots) & 1)
+    uint32_t xmask = 0, xparity = 0;
     for (int p = 0; p < a.nphases && ok; ++p) {
       const PhaseArgs& ph = a.ph[p];
       SegIter it(ph, G);
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
         if (p == 0 && a.local_xq) {
-          // the epilogue warps fill these stages' activation tiles
+          const int n = ks1 - ks0;
+          auto issue_x = [&](int i) {  // lane 0: x tile of stage ks0 + i into its slot
+            const uint32_t c = xc + i, slot = c % kMaxXSlots;
+            mbar_arrive_expect_tx(&x_full[slot], 256u * npad);
+            tma_load_2d(xring + slot * 256 * npad, &a.tm_x, &x_full[slot], (ks0 + i) * kTileK, 0, pol);
+            xmask |= 1u << slot;
+            xparity = (xparity & ~(1u << slot)) | (((c / kMaxXSlots) & 1u) << slot);
+          };
+          if (lane == 0)
+            for (int i = 0; i < n && i < kMaxXSlots; ++i) issue_x(i);
+          for (int i = 0; i < n; ++i) {
+            const uint32_t c = xc + i, slot = c % kMaxXSlots;
+            ok = __all_sync(0xFFFFFFFFu, wait_mbar(cx, &x_full[slot], (c / kMaxXSlots) & 1u, kSiteFullA));
+            if (!ok) break;
+            // each lane: blocks b = lane, lane + 32, ... of the npad x 4 block grid
+            uint4 raw[2][4];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int b = lane + 32 * q;
+              if (b < 4 * npad) {
+                const uint4* src = reinterpret_cast<const uint4*>(xring + slot * 256 * npad + (b >> 2) * 256 + (b & 3) * 64);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) raw[q][k] = src[k];
+              }
+            }
+            // the slot may be refilled once every lane has read it
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0 && i + kMaxXSlots < n) issue_x(i + kMaxXSlots);
+            ok = __all_sync(0xFFFFFFFFu, wait_mbar(cx, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty));
+            if (!ok) break;
+            uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int b = lane + 32 * q;
+              if (b < 4 * npad) store_x_block(a, st, b, raw[q]);
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full_a[stage]);
+            if (++stage == S) { stage = 0; ++round; }
+          }
+          xc += n;
+          continue;
+        }
+        if (lane != 0) {
           for (int ks = ks0; ks < ks1; ++ks)
             if (++stage == S) { stage = 0; ++round; }
           continue;
@@ -525,8 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
             x_ready = true;
             FSOPS_STAMP(2);
           } else if (ph.dep == kDepHFlags && ks == ks0) {
-            // the whole k-range of the segment: both SwiGLU tiles of every 128-feature chunk
-            if (!wait_counters(cx, a.hflags + ks0, ks1 - ks0, 2u + a.extra_xready, kSiteHFlag)) {
+            // the whole k-range of the segment: the SwiGLU tile of every 128-feature chunk
+            if (!wait_counters(cx, a.hflags + ks0, ks1 - ks0, 1u + a.extra_xready, kSiteHFlag)) {
               ok = false;
               break;
             }
@@ -537,8 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           }
           uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
           mbar_arrive_expect_tx(&full_a[stage], 128u * npad + 512u);
-          tma_load_2d(st + stage_off_b(), &a.tm_act[p], &full_a[stage], ks * kTileK, 0, pol);
-          bulk_load(st + stage_off_sfb(npad), ph.sf_act + static_cast<size_t>(ks) * 512, 512, &full_a[stage], pol);
+          tma_load_2d(st, &a.tm_act[p], &full_a[stage], ks * kTileK, 0, pol);
+          bulk_load(st + stage_off_sfx(npad), ph.sf_act + static_cast<size_t>(ks) * 512, 512, &full_a[stage], pol);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | ((round & 1u) << stage);
           if (++stage == S) { stage = 0; ++round; }
@@ -546,25 +597,27 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       }
     }
     if (!ok) *abort_flag = 1;
-    for (int s = 0; s < S; ++s)
-      if (issued_mask & (1u << s)) drain_mbar(&full_a[s], (issued_parity >> s) & 1u, 200000000ull);
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s)
+        if (issued_mask & (1u << s)) drain_mbar(&full_a[s], (issued_parity >> s) & 1u, 200000000ull);
+      for (int s = 0; s < kMaxXSlots; ++s)
+        if (xmask & (1u << s)) drain_mbar(&x_full[s], (xparity >> s) & 1u, 200000000ull);
+    }
   } else if (warp == 2 && lane == 0) {
     // ------------------------------------------------ MMA issuer
     int stage = 0;
-    uint32_t round = 0;
-    int acc = 0;
-    uint32_t acc_round = 0;
+    uint32_t round = 0, acc_round = 0, n_mma = 0;
     bool ok = true;
-    const uint32_t idesc0 = idesc_mxf8_e4m3(static_cast<uint32_t>(npad), 0, 0);
-    uint32_t n_mma = 0;
+    const uint32_t sf_base = tmem + kAccCols;
     for (int p = 0; p < a.nphases && ok; ++p) {
       const PhaseArgs& ph = a.ph[p];
       SegIter it(ph, G);
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
-        if (!wait_mbar(cx, &acc_empty[acc], (acc_round & 1u) ^ 1u, kSiteAccEmpty)) { ok = false; break; }
+        const bool v1 = t * kTileRows + 128 < ph.rows;
+        const uint32_t idesc0 = idesc_mxf8_e4m3(v1 ? 256u : 128u, 0, 0);
+        if (!wait_mbar(cx, acc_empty, (acc_round & 1u) ^ 1u, kSiteAccEmpty)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d = tmem + acc * acc_cols;
         for (int ks = ks0; ks < ks1; ++ks) {
           if (!wait_mbar(cx, &full_w[stage], round & 1u, kSiteFullW) ||
               !wait_mbar(cx, &full_a[stage], round & 1u, kSiteFullA)) {
@@ -575,28 +628,28 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           FSOPS_STAMP_IF(n_mma < 24, 16 + n_mma);
           ++n_mma;
           uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
-          const uint32_t sfc = tmem + sf_base + kSfColsPerStage * stage;
-          tc_cp_32x128b_warpx4(sfc, smem_desc(smem_u32(st + stage_off_sfa(npad)), 0, 128, kSwizzleNone));
-          tc_cp_32x128b_warpx4(sfc + 4, smem_desc(smem_u32(st + stage_off_sfb(npad)), 0, 128, kSwizzleNone));
-          const uint32_t sa = smem_u32(st + stage_off_a());
-          const uint32_t sb = smem_u32(st + stage_off_b());
+          const uint32_t sfc = sf_base + kSfColsPerStage * stage;
+          // A scales (tokens): lanes = row % 32, columns sfc + row / 32.
+          // B scales (weight rows n): lanes n % 32, columns sfc + 4 + n / 32.
+          tc_cp_32x128b_warpx4(sfc, smem_desc(smem_u32(st + stage_off_sfx(npad)), 0, 128, kSwizzleNone));
+          tc_cp_32x128b_warpx4(sfc + 4, smem_desc(smem_u32(st + stage_off_sfw(npad)), 0, 128, kSwizzleNone));
+          if (v1) tc_cp_32x128b_warpx4(sfc + 8, smem_desc(smem_u32(st + stage_off_sfw(npad) + 512), 0, 128, kSwizzleNone));
+          const uint32_t sx = smem_u32(st);
+          const uint32_t sw = smem_u32(st + stage_off_w(npad));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            // scale byte k of each 32-bit TMEM scale word belongs to K-block k of
-            // the stage; k-step k accumulates into chain k % chains, so up to
-            // four MMAs of a stage are independent of each other
+            // scale byte k of each 32-bit TMEM scale word belongs to K-block k of the stage
             const uint32_t idesc = idesc0 | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
-            const uint32_t chain = static_cast<uint32_t>(k % a.chains);
-            tc_mma_mxf8(d + chain * npad, smem_desc(sa + 32 * k, 16, 1024, kSwizzle128B),
-                        smem_desc(sb + 32 * k, 16, 1024, kSwizzle128B), idesc, sfc, sfc + 4,
-                        (ks > ks0 || k >= a.chains) ? 1u : 0u);
+            tc_mma_mxf8(tmem, smem_desc(sx + 32 * k, 16, 1024, kSwizzle128B),
+                        smem_desc(sw + 32 * k, 16, 1024, kSwizzle128B), idesc, sfc, sfc + 4,
+                        (ks > ks0 || k > 0) ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
           if (++stage == S) { stage = 0; ++round; }
         }
         if (!ok) break;
-        tc_commit(&acc_full[acc]);
-        if (++acc == a.nacc) { acc = 0; ++acc_round; }
+        tc_commit(acc_full);
+        ++acc_round;
         FSOPS_STAMP(p == 0 ? 7 : 11);
       }
     }
@@ -606,19 +659,18 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     drain_mbar(drain, 0, 200000000ull);
   } else if (warp >= 4) {
     // ------------------------------------------------ epilogue warps
-    const int et = threadIdx.x - 128;  // TMEM lane = row within the tile
+    const int et = threadIdx.x - 128;  // token row of the accumulator (TMEM lane)
     const int ew = et >> 5;
-    // (1) quantise this block's slice of x: the 32-blocks [b0, b1) of the
-    // row-major [npad, H/32] block grid (rows >= M only get a zero scale)
+    // (1) grid-wide: quantise this block's slice of x, the 32-blocks [b0, b1)
+    // of the row-major [npad, H/32] block grid (rows >= M only get a zero scale)
     if (a.x != nullptr && !a.local_xq) {
       const int nbk = a.H / 32;
       const long long NB = static_cast<long long>(npad) * nbk;
       const long long b0 = range_begin(blockIdx.x, NB, G), b1 = range_begin(blockIdx.x + 1, NB, G);
       long long b = b0 + et;
-      // issue the first block's loads before the weight stream starts
       uint4 raw[4];
       bool have = false;
-      if (b < b1) {
+      if (b < b1) {  // issue the first block's loads before the weight stream starts
         const int m = static_cast<int>(b / nbk), kb = static_cast<int>(b % nbk);
         if (m < a.M) {
           const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<long long>(m) * a.H + kb * 32);
@@ -649,76 +701,90 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
         FSOPS_STAMP(1);
       }
     }
-    // (2) accumulator tiles (and, with local_xq, phase 0's activation tiles)
-    int acc = 0;
+    // (2) accumulators
     uint32_t acc_round = 0;
-    int xstage = 0;
-    uint32_t xround = 0;
     bool ok = true;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(ew * 32) << 16);
     for (int p = 0; p < a.nphases && ok; ++p) {
       const PhaseArgs& ph = a.ph[p];
       const long long U = static_cast<long long>(ph.T) * ph.KS;
       SegIter it(ph, G);
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
-        if (p == 0 && a.local_xq) {
-          // produce this segment's activation tiles: quantise x[:, 128 ks ..] straight
-          // into each stage, loads running two stages ahead
-          const bool mine = et < 4 * npad;
-          uint4 ra[4], rb[4], rc[4];
-          const int n = ks1 - ks0;
-          if (mine && n > 0) load_x_block(a, ks0, et, ra);
-          if (mine && n > 1) load_x_block(a, ks0 + 1, et, rb);
-          for (int i = 0; i < n && ok; ++i) {
-            if (mine && i + 2 < n) {
-              if (i % 3 == 0) load_x_block(a, ks0 + i + 2, et, rc);
-              else if (i % 3 == 1) load_x_block(a, ks0 + i + 2, et, ra);
-              else load_x_block(a, ks0 + i + 2, et, rb);
-            }
-            if (!wait_mbar(cx, &empty[xstage], (xround & 1u) ^ 1u, kSiteEmpty)) { ok = false; break; }
-            uint8_t* st = smem + static_cast<size_t>(xstage) * a.stage_bytes;
-            if (mine) {
-              if (i % 3 == 0) store_x_block(a, st, et, ra);
-              else if (i % 3 == 1) store_x_block(a, st, et, rb);
-              else store_x_block(a, st, et, rc);
-            }
-            fence_proxy_async_shared();
-            epi_bar();
-            if (et == 0) mbar_arrive(&full_a[xstage]);
-            if (++xstage == S) { xstage = 0; ++xround; }
-          }
-          if (!ok) break;
-        }
-        if (!wait_mbar(cx, &acc_full[acc], acc_round & 1u, kSiteAccFull)) { ok = false; break; }
+        if (!wait_mbar(cx, acc_full, acc_round & 1u, kSiteAccFull)) { ok = false; break; }
+        ++acc_round;
         tc_fence_after();
         if (et == 0) FSOPS_STAMP(p == 0 ? 3 : 8);
-        const uint32_t tacc = tmem + (static_cast<uint32_t>(ew * 32) << 16) + acc * acc_cols;
-        if (ks0 == 0 && ks1 == ph.KS) {
-          // the whole K range of tile t is in this accumulator
-          for (int c0 = 0; c0 < a.M; c0 += 16) {
-            float v[16];
-            tmem_chunk_sum(tacc + c0, a.chains, npad, v);
-            if (ph.epi == kEpiSwiGLU) epi_swiglu_chunk(a, t, c0, v, et, xchg);
-            else epi_store_chunk(a, ph, t, c0, v, et);
-          }
-          tc_fence_before();
-          mbar_arrive(&acc_empty[acc]);
-          if (ph.epi == kEpiSwiGLU) publish_swiglu_tile(a, t, et);
-        } else {
-          // The K range of tile t is split over several blocks: add this
-          // block's fp32 sums into the tile's accumulator in L2; the block
-          // that arrives last reads the total, finishes the tile and leaves
-          // the accumulator zero for the next launch.
-          float* accg = ph.accum + static_cast<long long>(t) * a.M * 128 + et;
-          for (int c0 = 0; c0 < a.M; c0 += 16) {
-            float v[16];
-            tmem_chunk_sum(tacc + c0, a.chains, npad, v);
+        const bool whole = (ks0 == 0 && ks1 == ph.KS);
+        const int ncols = (t * kTileRows + 128 < ph.rows) ? 256 : 128;
+        float* accg = ph.accum + static_cast<long long>(t) * a.M * kTileRows;  // [256][M]
+        if (a.stage_tmem) {
+          // M <= 32: warp 4 copies TMEM lanes 0..31 to shared memory and the
+          // accumulator is released at once; all four warps share the rest
+          if (ew == 0) {
+            for (int c0 = 0; c0 < ncols; c0 += 16) {
+              float v[16];
+              tmem_ld16f(tlane + c0, v);
+              if (lane < a.M) {
+                float4* d = reinterpret_cast<float4*>(stg + lane * kStageLd + c0);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < a.M) atomicAdd(accg + static_cast<long long>(c0 + j) * 128, v[j]);
+                for (int q = 0; q < 4; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+              }
+            }
           }
           tc_fence_before();
-          mbar_arrive(&acc_empty[acc]);
+          epi_bar();
+          mbar_arrive(acc_empty);
+          if (!whole) {
+            // column-major sums: consecutive threads add consecutive tokens of a column
+            for (int item = et; item < a.M * ncols; item += 128) {
+              const int c = item / a.M, r = item % a.M;
+              red_add_f32(accg + item, stg[r * kStageLd + c]);
+            }
+          }
+        } else {
+          // M > 32: thread et owns token et
+          if (whole) {
+            if (ph.epi == kEpiSwiGLU) {
+              for (int b = 0; b < 4; ++b) {
+                float g[32], u[32];
+                tmem_ld16f(tlane + 32 * b, *reinterpret_cast<float(*)[16]>(g));
+                tmem_ld16f(tlane + 32 * b + 16, *reinterpret_cast<float(*)[16]>(g + 16));
+                tmem_ld16f(tlane + 128 + 32 * b, *reinterpret_cast<float(*)[16]>(u));
+                tmem_ld16f(tlane + 128 + 32 * b + 16, *reinterpret_cast<float(*)[16]>(u + 16));
+                if (et < a.M) swiglu_block(a, t, b, et, g, u);
+              }
+            } else {
+              for (int c0 = 0; c0 < ncols; c0 += 16) {
+                float v[16];
+                tmem_ld16f(tlane + c0, v);
+                if (et < a.M) {
+                  store8(a, ph, et, static_cast<long long>(t) * kTileRows + c0, v);
+                  store8(a, ph, et, static_cast<long long>(t) * kTileRows + c0 + 8, v + 8);
+                }
+              }
+            }
+          } else {
+            for (int c0 = 0; c0 < ncols; c0 += 16) {
+              float v[16];
+              tmem_ld16f(tlane + c0, v);
+              if (et < a.M) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) red_add_f32(accg + static_cast<long long>(c0 + j) * a.M + et, v[j]);
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(acc_empty);
+        }
+        if (whole) {
+          if (a.stage_tmem) finish_staged(a, ph, t, ncols, stg, et);
+        } else {
+          // The K range of tile t is split over several blocks: every block
+          // added its sums into the tile's accumulator in L2; the block that
+          // arrives last reads the total, finishes the tile and leaves the
+          // accumulator zero for the next launch.
+          // (whole_tiles phases never get here)
           const long long cf = owner_of(static_cast<long long>(t) * ph.KS, U, G);
           const long long cl = owner_of(static_cast<long long>(t) * ph.KS + ph.KS - 1, U, G);
           // with U >= G every block owns at least one unit; with U < G each owns at most one
@@ -734,24 +800,61 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           const bool last = *bcast != 0;
           epi_bar();
           if (last) {
-            for (int c0 = 0; c0 < a.M; c0 += 16) {
-              float v[16];
+            if (a.stage_tmem) {
+              // all loads first (no global store in between to order them behind)
+              for (int item = et; item < a.M * ncols; item += 128) {
+                const int c = item / a.M, r = item % a.M;
+                stg[r * kStageLd + c] = __ldcg(accg + item);
+              }
+              epi_bar();
+              finish_staged(a, ph, t, ncols, stg, et);
+            } else if (et < a.M) {
+              // column c of token et sits at accg[c * M + et]: a warp reads 32
+              // consecutive floats; a batch of loads is issued before any store
+              const float* col = accg + et;
+              if (ph.epi == kEpiSwiGLU) {
+                for (int b = 0; b < 4; ++b) {
+                  float g[32], u[32];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                v[j] = 0.f;
-                if (c0 + j < a.M) {
-                  float* q = accg + static_cast<long long>(c0 + j) * 128;
-                  v[j] = __ldcg(q);
-                  __stcg(q, 0.f);
+                  for (int i = 0; i < 32; ++i) {
+                    g[i] = __ldcg(col + static_cast<long long>(32 * b + i) * a.M);
+                    u[i] = __ldcg(col + static_cast<long long>(128 + 32 * b + i) * a.M);
+                  }
+                  swiglu_block(a, t, b, et, g, u);
+                }
+              } else {
+                for (int c0 = 0; c0 < ncols; c0 += 16) {
+                  float v[16];
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) v[i] = __ldcg(col + static_cast<long long>(c0 + i) * a.M);
+                  store8(a, ph, et, static_cast<long long>(t) * kTileRows + c0, v);
+                  store8(a, ph, et, static_cast<long long>(t) * kTileRows + c0 + 8, v + 8);
                 }
               }
-              if (ph.epi == kEpiSwiGLU) epi_swiglu_chunk(a, t, c0, v, et, xchg);
-              else epi_store_chunk(a, ph, t, c0, v, et);
             }
-            if (ph.epi == kEpiSwiGLU) publish_swiglu_tile(a, t, et);
+            // leave the tile's accumulator zero for the next launch
+            epi_bar();
+            {
+              float4* z = reinterpret_cast<float4*>(accg);
+              const int n4 = a.M * ncols / 4;
+              for (int i = et; i < n4; i += 128) __stcg(z + i, make_float4(0.f, 0.f, 0.f, 0.f));
+            }
+          }
+          if (!last) {
+            if (et == 0) FSOPS_STAMP(p == 0 ? 4 : 9);
+            if (a.stage_tmem) epi_bar();  // stg is reused by the next accumulator
+            continue;
           }
         }
-        if (++acc == a.nacc) { acc = 0; ++acc_round; }
+        if (ph.epi == kEpiSwiGLU) {
+          // publish tile t: each writer orders its stores before later TMA
+          // reads, the barrier orders all of them before the release-add
+          fence_proxy_async_global();
+          epi_bar();
+          if (et == 0) red_add_release_gpu(a.hflags + t, 1u);
+        } else if (a.stage_tmem) {
+          epi_bar();  // stg is reused by the next accumulator
+        }
         if (et == 0) FSOPS_STAMP(p == 0 ? 4 : 9);
       }
     }
