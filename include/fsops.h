@@ -167,6 +167,29 @@ fsops_status fsops_mxfp8_swiglu_mlp_unfused(const void* x_bf16, const uint8_t* w
                                             const uint8_t* w_down, const fsops_mlp_scales* scales,
                                             void* y_bf16, int M, int H, int I, void* stream);
 
+/* fsops_mxfp8_swiglu_mlp_noalloc -- the same single-launch MLP, for callers
+ * that cannot allocate device memory: code running inside a framework or
+ * plugin host that owns every device allocation, paths that must not call an
+ * allocator (cudaMalloc may synchronise the device), or deployments with a
+ * fixed memory budget.  It has no counterpart in the paper; it is a packaging
+ * of fsops_mxfp8_swiglu_mlp.
+ *   Arguments, layouts and limits as fsops_mxfp8_swiglu_mlp, except that no
+ *   workspace is used: the scratch is one fixed 8 MiB buffer per device inside
+ *   the library's device image, present from library load until process exit.
+ *   A shape whose scratch does not fit in 8 MiB is rejected with
+ *   FSOPS_ERR_UNSUPPORTED_SHAPE before anything is launched (with one gate/up
+ *   tile per block it needs about 16 KiB + M*(H+I) bytes + 1 KiB*M*ceil(H/256)).
+ *   The first call on a device looks up the buffer's device address
+ *   (cudaGetSymbolAddress); make that first call outside any stream capture.
+ *   Each call clears the counters and accumulators it needs with
+ *   cudaMemsetAsync on `stream`, then launches the kernel; neither step
+ *   allocates.  All calls on a device share the one buffer, so calls whose
+ *   execution overlaps on the GPU (different streams without ordering) race;
+ *   order them. */
+fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w_gateup,
+                                            const uint8_t* w_down, const fsops_mlp_scales* scales,
+                                            void* y_bf16, int M, int H, int I, void* stream);
+
 /* Workspace bytes the MLP entry points need on the current device (0 if the
  * shape is unsupported). */
 size_t fsops_mlp_workspace_bytes(int M, int H, int I);

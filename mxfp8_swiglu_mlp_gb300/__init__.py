@@ -23,7 +23,7 @@ __all__ = [
     "ERR_TIMEOUT", "ERR_NO_DEVICE", "SCALES_ROWMAJOR", "SCALES_TCGEN05", "DTYPE_BF16", "DTYPE_F32",
     "DTYPE_MXFP8", "fsops_quantize_mxfp8", "fsops_scale_bytes", "fsops_mxfp8_gemm", "fsops_mxfp8_gemm_ex",
     "fsops_gemm_workspace_bytes", "fsops_swiglu_quantize_mxfp8", "fsops_mxfp8_swiglu_mlp",
-    "fsops_mxfp8_swiglu_mlp_unfused", "fsops_mlp_workspace_bytes", "fsops_set_workspace",
+    "fsops_mxfp8_swiglu_mlp_unfused", "fsops_mxfp8_swiglu_mlp_noalloc", "fsops_mlp_workspace_bytes", "fsops_set_workspace",
     "fsops_read_kernel_status", "fsops_set_wait_timeout_ns", "fsops_debug_set_extra_arrivals",
     "fsops_status_string", "fsops_version", "quantize_weight", "MLPWeights", "prepare_mlp_weights",
     "Workspace", "pair_gate_up",
@@ -54,6 +54,7 @@ _SIGS = {
     "fsops_swiglu_quantize_mxfp8": ([_vp, _i, _i, _vp, _vp, _vp], _i),
     "fsops_mxfp8_swiglu_mlp": ([_vp, _vp, _vp, ctypes.POINTER(_MlpScales), _vp, _i, _i, _i, _vp], _i),
     "fsops_mxfp8_swiglu_mlp_unfused": ([_vp, _vp, _vp, ctypes.POINTER(_MlpScales), _vp, _i, _i, _i, _vp], _i),
+    "fsops_mxfp8_swiglu_mlp_noalloc": ([_vp, _vp, _vp, ctypes.POINTER(_MlpScales), _vp, _i, _i, _i, _vp], _i),
     "fsops_mlp_workspace_bytes": ([_i, _i, _i], _sz),
     "fsops_set_workspace": ([_vp, _sz], _i),
     "fsops_read_kernel_status": ([_vp, ctypes.POINTER(_u32)], _i),
@@ -147,6 +148,16 @@ def fsops_mxfp8_swiglu_mlp_unfused(x_bf16, w_gateup, w_down, scales, y_bf16, M: 
     _check(lib.fsops_mxfp8_swiglu_mlp_unfused(_ptr(x_bf16), _ptr(w_gateup), _ptr(w_down), ctypes.byref(sc),
                                               _ptr(y_bf16), M, H, I, _stream(stream)),
            "fsops_mxfp8_swiglu_mlp_unfused")
+
+
+def fsops_mxfp8_swiglu_mlp_noalloc(x_bf16, w_gateup, w_down, scales, y_bf16, M: int, H: int, I: int,
+                                   stream=None) -> None:
+    """The fused MLP without a workspace: for callers that cannot allocate
+    device memory (its scratch is a fixed 8 MiB buffer inside the library)."""
+    sc = _mlp_scales(scales)
+    _check(lib.fsops_mxfp8_swiglu_mlp_noalloc(_ptr(x_bf16), _ptr(w_gateup), _ptr(w_down), ctypes.byref(sc),
+                                              _ptr(y_bf16), M, H, I, _stream(stream)),
+           "fsops_mxfp8_swiglu_mlp_noalloc")
 
 
 def fsops_mlp_workspace_bytes(M: int, H: int, I: int) -> int:

@@ -539,3 +539,130 @@ fsops_status fsops_debug_set_trace_buffer(void* buf) {
 #endif
 
 }  // extern "C"
+
+// ============================================================================
+// No-allocation variant of fsops_mxfp8_swiglu_mlp.
+//
+// Its scratch is a fixed buffer inside the library's device image instead of a
+// caller-registered workspace, so neither the caller nor the library ever
+// allocates device memory for it.
+// ============================================================================
+namespace {
+
+// One buffer per device that loads the library, held until the process exits.
+constexpr size_t kNoAllocScratchBytes = 8u << 20;  // 8 MiB
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+uint8_t* g_noalloc_base[kMaxDevices] = {};
+
+// Byte layout inside the fixed buffer: the MLP workspace layout without the
+// three-launch path's fp32 [M, 2I] buffer, and without the gate/up split-K
+// accumulators when every gate/up tile is done by one block (the kernel never
+// touches them then).
+struct NoAllocLayout {
+  size_t ctl, xq, xq_sf, hq, hq_sf, part0, part1, end;
+};
+NoAllocLayout noalloc_layout(int M, int H, int I, bool gateup_whole) {
+  NoAllocLayout l;
+  l.ctl = 0;
+  l.xq = kCtlRegionBytes;
+  l.xq_sf = l.xq + round_up(static_cast<size_t>(M) * H, 1024);
+  l.hq = l.xq_sf + round_up(static_cast<size_t>(H / 128) * 512, 1024);
+  l.hq_sf = l.hq + round_up(static_cast<size_t>(M) * I, 1024);
+  l.part0 = l.hq_sf + round_up(static_cast<size_t>(I / 128) * 512, 1024);
+  l.part1 = l.part0 + (gateup_whole ? 0 : accum_bytes(M, I / kPairFeatures));
+  l.end = l.part1 + accum_bytes(M, (H + kTileRows - 1) / kTileRows);
+  return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w_gateup, const uint8_t* w_down,
+                                            const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I,
+                                            void* stream) {
+  fsops_status st = mlp_validate(x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I);
+  if (st != FSOPS_OK) return st;
+  int dev;
+  const DeviceInfo* di;
+  st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  const int grid = di->sms;
+  const int Ic = I / 128;
+  const int T0 = I / kPairFeatures;
+  const int T1 = (H + kTileRows - 1) / kTileRows;
+  if (ctl_words_needed(Ic, T0, T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  const bool whole = T0 <= grid && whole_tiles_enabled();
+  const NoAllocLayout l = noalloc_layout(M, H, I, whole);
+  if (l.end > kNoAllocScratchBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;  // does not fit the fixed buffer
+
+  // First call on this device: look up the device address of the buffer (a
+  // host-side reference to the __device__ array is not a device address).
+  uint8_t* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_noalloc_base[dev] == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return FSOPS_ERR_CUDA;
+      }
+      g_noalloc_base[dev] = static_cast<uint8_t*>(p);
+    }
+    ws = g_noalloc_base[dev];
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the buffer keeps whatever the previous call left: clear the counters, flags
+  // and split-K accumulators the kernel needs to start at zero
+  if (cudaMemsetAsync(ws + l.ctl, 0, kCtlRegionBytes, s) != cudaSuccess ||
+      cudaMemsetAsync(ws + l.part0, 0, l.end - l.part0, s) != cudaSuccess) {
+    cudaGetLastError();
+    return FSOPS_ERR_CUDA;
+  }
+
+  KernelArgs ka;
+  init_common(ka, M, reinterpret_cast<uint32_t*>(ws + l.ctl));
+  ka.hflags = ka.ctl + kCtlHeaderWords;
+  ka.nphases = 2;
+  ka.x = static_cast<const uint16_t*>(x_bf16);
+  ka.xq_codes = ws + l.xq;
+  ka.xq_sf = ws + l.xq_sf;
+  ka.H = H;
+  ka.hq_codes = ws + l.hq;
+  ka.hq_sf = ws + l.hq_sf;
+  ka.I = I;
+  ka.out = y_bf16;
+  ka.out_f32 = 0;
+  PhaseArgs& p0 = ka.ph[0];
+  p0.sf_w = scales->gateup;
+  p0.sf_act = ka.xq_sf;
+  p0.tile_cnt = ka.hflags + Ic;
+  p0.accum = reinterpret_cast<float*>(ws + l.part0);
+  p0.KS = H / kTileK;
+  p0.T = T0;
+  p0.rows = 2 * I;
+  p0.whole_tiles = whole ? 1 : 0;
+  ka.local_xq = local_xq_for(ka.npad);
+  p0.dep = ka.local_xq ? kDepNone : kDepXReady;
+  if (ka.local_xq && !encode_x_map(&ka.tm_x, x_bf16, H, M, ka.npad)) return FSOPS_ERR_INVALID_ARG;
+  p0.epi = kEpiSwiGLU;
+  p0.out_ld = I;
+  PhaseArgs& p1 = ka.ph[1];
+  p1.sf_w = scales->down;
+  p1.sf_act = ka.hq_sf;
+  p1.tile_cnt = p0.tile_cnt + T0;
+  p1.accum = reinterpret_cast<float*>(ws + l.part1);
+  p1.KS = I / kTileK;
+  p1.T = T1;
+  p1.rows = H;
+  p1.dep = kDepHFlags;
+  p1.epi = kEpiStore;
+  p1.out_ld = H;
+  if (!encode_map(&ka.tm_w[0], w_gateup, H, 2 * I, kTileRows) ||
+      !encode_map(&ka.tm_act[0], ka.xq_codes, H, M, ka.npad) || !encode_map(&ka.tm_w[1], w_down, I, H, kTileRows) ||
+      !encode_map(&ka.tm_act[1], ka.hq_codes, I, M, ka.npad))
+    return FSOPS_ERR_INVALID_ARG;
+  return launch(ka, grid, s);
+}
+
+}  // extern "C"
