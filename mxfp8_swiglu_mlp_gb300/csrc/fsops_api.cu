@@ -62,7 +62,7 @@ fsops_status current_device(int* dev_out, const DeviceInfo** info) {
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
       d.ok = (major == 10);
-      d.sms = sms;
+      d.sms = sms < 256 ? sms : 256;  // one block per SM; the split arithmetic assumes at most 256
     }
     cudaGetLastError();
     // tuning knob: weight tiles in flight per block (FSOPS_MAX_INFLIGHT=1..12)

@@ -122,7 +122,11 @@ cudaError_t launch_quantize(const uint16_t* x, int rows, int K, int ld, uint8_t*
 // SwiGLU + requantisation (the middle launch of the unfused path).
 // ======================================================================
 // SiLU(g) * u = g * sigmoid(g) * u; for g -> -inf the reciprocal of inf is 0.
-__device__ __forceinline__ float silu_mul(float g, float u) { return g * __frcp_rn(1.0f + __expf(-g)) * u; }
+// SiLU(g) * u in fp32.  The fast divide (reciprocal approximation, 2 ulp)
+// keeps this off the epilogue's critical path; its error is far below the
+// E4M3 step the result is rounded to next.  For g below about -88, 1 + e^-g
+// overflows to +inf and the quotient is 0, the limit of SiLU.
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 __global__ void swiglu_quantize_kernel(const float* __restrict__ gu, int M, int npad, int I,
                                        uint8_t* __restrict__ hc, uint8_t* __restrict__ hs) {
@@ -271,32 +275,35 @@ __device__ __forceinline__ bool wait_counters(const Ctx& cx, const uint32_t* p, 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __device__ __forceinline__ long long range_begin(long long c, long long U, long long G) { return c * U / G; }
+// Stream-K split of U units over G blocks in 32-bit arithmetic (U <= 2^18 and
+// G <= 2^8 keep every product below 2^26): block c owns [c U / G, (c+1) U / G).
+__device__ __forceinline__ uint32_t split_begin(uint32_t c, uint32_t U, uint32_t G) { return c * U / G; }
 // The block whose range holds unit u.
-__device__ __forceinline__ long long owner_of(long long u, long long U, long long G) {
+__device__ __forceinline__ uint32_t split_owner(uint32_t u, uint32_t U, uint32_t G) {
   return ((u + 1) * G + U - 1) / U - 1;
 }
 
 // Walks the segments (tile, ks0, ks1) of one phase assigned to this block.
 struct SegIter {
-  long long u, ue;
-  int KS;
-  __device__ SegIter(const PhaseArgs& p, long long G) {
-    KS = p.KS;
+  uint32_t u, ue, KS;
+  __device__ SegIter(const PhaseArgs& p, uint32_t G) {
+    KS = static_cast<uint32_t>(p.KS);
+    const uint32_t c = blockIdx.x;
     if (p.whole_tiles) {
-      u = blockIdx.x < p.T ? static_cast<long long>(blockIdx.x) * KS : 0;
-      ue = blockIdx.x < p.T ? u + KS : 0;
+      u = c < static_cast<uint32_t>(p.T) ? c * KS : 0;
+      ue = c < static_cast<uint32_t>(p.T) ? u + KS : 0;
     } else {
-      const long long U = static_cast<long long>(p.T) * p.KS;
-      u = range_begin(blockIdx.x, U, G);
-      ue = range_begin(blockIdx.x + 1, U, G);
+      const uint32_t U = static_cast<uint32_t>(p.T) * KS;
+      u = split_begin(c, U, G);
+      ue = split_begin(c + 1, U, G);
     }
   }
   __device__ bool next(int& t, int& ks0, int& ks1) {
     if (u >= ue) return false;
-    t = static_cast<int>(u / KS);
-    ks0 = static_cast<int>(u % KS);
-    const long long rem = ue - u;
-    ks1 = static_cast<int>(min(static_cast<long long>(KS), ks0 + rem));
+    const uint32_t tt = u / KS;
+    t = static_cast<int>(tt);
+    ks0 = static_cast<int>(u - tt * KS);
+    ks1 = static_cast<int>(min(KS, ks0 + (ue - u)));
     u += ks1 - ks0;
     return true;
   }
@@ -468,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     if (a.x != nullptr && !a.local_xq) ok = wait_mbar(cx, x_issued, 0, kSiteEmpty);
     for (int p = 0; p < a.nphases && ok; ++p) {
       const PhaseArgs& ph = a.ph[p];
-      SegIter it(ph, G);
+      SegIter it(ph, static_cast<uint32_t>(G));
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
         const bool v1 = t * kTileRows + 128 < ph.rows;
@@ -510,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     uint32_t xmask = 0, xparity = 0;
     for (int p = 0; p < a.nphases && ok; ++p) {
       const PhaseArgs& ph = a.ph[p];
-      SegIter it(ph, G);
+      SegIter it(ph, static_cast<uint32_t>(G));
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
         if (p == 0 && a.local_xq) {
@@ -611,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     const uint32_t sf_base = tmem + kAccCols;
     for (int p = 0; p < a.nphases && ok; ++p) {
       const PhaseArgs& ph = a.ph[p];
-      SegIter it(ph, G);
+      SegIter it(ph, static_cast<uint32_t>(G));
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
         const bool v1 = t * kTileRows + 128 < ph.rows;
@@ -707,8 +714,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     const uint32_t tlane = tmem + (static_cast<uint32_t>(ew * 32) << 16);
     for (int p = 0; p < a.nphases && ok; ++p) {
       const PhaseArgs& ph = a.ph[p];
-      const long long U = static_cast<long long>(ph.T) * ph.KS;
-      SegIter it(ph, G);
+      const uint32_t U = static_cast<uint32_t>(ph.T * ph.KS);
+      SegIter it(ph, static_cast<uint32_t>(G));
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
         if (!wait_mbar(cx, acc_full, acc_round & 1u, kSiteAccFull)) { ok = false; break; }
@@ -785,10 +792,10 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           // arrives last reads the total, finishes the tile and leaves the
           // accumulator zero for the next launch.
           // (whole_tiles phases never get here)
-          const long long cf = owner_of(static_cast<long long>(t) * ph.KS, U, G);
-          const long long cl = owner_of(static_cast<long long>(t) * ph.KS + ph.KS - 1, U, G);
+          const uint32_t cf = split_owner(static_cast<uint32_t>(t * ph.KS), U, static_cast<uint32_t>(G));
+          const uint32_t cl = split_owner(static_cast<uint32_t>(t * ph.KS + ph.KS - 1), U, static_cast<uint32_t>(G));
           // with U >= G every block owns at least one unit; with U < G each owns at most one
-          const uint32_t expected = static_cast<uint32_t>(U >= G ? cl - cf + 1 : ph.KS);
+          const uint32_t expected = U >= static_cast<uint32_t>(G) ? cl - cf + 1 : static_cast<uint32_t>(ph.KS);
           // the barrier orders every thread's adds before thread 0's acq_rel
           // counter update, which in turn orders the last arriver's reads
           epi_bar();
