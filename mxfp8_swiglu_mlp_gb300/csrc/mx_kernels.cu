@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
             if (!wait_mbar(cx, &full_w[lag_stage], lag_round & 1u, kSiteFullW)) { ok = false; break; }
             if (++lag_stage == S) { lag_stage = 0; ++lag_round; }
           }
-          FSOPS_STAMP_IF(n_issued < 24, 40 + n_issued);
+          FSOPS_STAMP_IF(n_issued < 16, 40 + n_issued);
           ++n_issued;
           uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
           mbar_arrive_expect_tx(&full_w[stage], 32768u + (v1 ? 1024u : 512u));
@@ -701,6 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
         have = false;
         a.xq_sf[(kb >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (kb & 3)] = static_cast<uint8_t>(s);
       }
+      if (et == 0) FSOPS_STAMP(63);
       fence_proxy_async_global();
       epi_bar();
       if (et == 0) {
@@ -742,6 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           tc_fence_before();
           epi_bar();
           mbar_arrive(acc_empty);
+          if (et == 0) FSOPS_STAMP(p == 0 ? 12 : 60);
           if (!whole) {
             // column-major sums: consecutive threads add consecutive tokens of a column
             for (int item = et; item < a.M * ncols; item += 128) {
@@ -786,6 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
         }
         if (whole) {
           if (a.stage_tmem) finish_staged(a, ph, t, ncols, stg, et);
+          if (et == 0) FSOPS_STAMP_IF(p == 0, 13);
         } else {
           // The K range of tile t is split over several blocks: every block
           // added its sums into the tile's accumulator in L2; the block that
@@ -806,36 +809,58 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           epi_bar();
           const bool last = *bcast != 0;
           epi_bar();
+          if (et == 0) FSOPS_STAMP_IF(p == 1, 61);
           if (last) {
             if (a.stage_tmem) {
-              // all loads first (no global store in between to order them behind)
-              for (int item = et; item < a.M * ncols; item += 128) {
-                const int c = item / a.M, r = item % a.M;
-                stg[r * kStageLd + c] = __ldcg(accg + item);
+              // every load is issued before the first store: one L2 round trip
+              // (M * ncols / 128 <= 64 values per thread)
+              float v[64];
+#pragma unroll
+              for (int j = 0; j < 64; ++j) {
+                const int item = et + 128 * j;
+                if (item < a.M * ncols) v[j] = __ldcg(accg + item);
+              }
+#pragma unroll
+              for (int j = 0; j < 64; ++j) {
+                const int item = et + 128 * j;
+                if (item < a.M * ncols) stg[(item % a.M) * kStageLd + item / a.M] = v[j];
               }
               epi_bar();
+              if (et == 0) FSOPS_STAMP_IF(p == 1, 56);
               finish_staged(a, ph, t, ncols, stg, et);
-            } else if (et < a.M) {
-              // column c of token et sits at accg[c * M + et]: a warp reads 32
-              // consecutive floats; a batch of loads is issued before any store
-              const float* col = accg + et;
-              if (ph.epi == kEpiSwiGLU) {
-                for (int b = 0; b < 4; ++b) {
+              if (et == 0) FSOPS_STAMP_IF(p == 1, 57);
+            } else if (ph.epi == kEpiSwiGLU) {
+              // column c of token r sits at accg[c * M + r]: a warp reads 32
+              // consecutive floats; 64 loads are in flight before their use.
+              // With M <= 64 two threads share a token (two 32-blocks each).
+              const int halves = a.M <= 64 ? 2 : 1;
+              const int r = et % a.M, h = et / a.M;
+              if (h < halves) {
+                const float* col = accg + r;
+                for (int b = h * (4 / halves); b < (h + 1) * (4 / halves); ++b) {
                   float g[32], u[32];
 #pragma unroll
                   for (int i = 0; i < 32; ++i) {
                     g[i] = __ldcg(col + static_cast<long long>(32 * b + i) * a.M);
                     u[i] = __ldcg(col + static_cast<long long>(128 + 32 * b + i) * a.M);
                   }
-                  swiglu_block(a, t, b, et, g, u);
+                  swiglu_block(a, t, b, r, g, u);
                 }
-              } else {
-                for (int c0 = 0; c0 < ncols; c0 += 16) {
-                  float v[16];
+              }
+            } else {
+              // plain output: with M <= 64 two threads share a token (one half
+              // of the columns each); batches of 64 loads in flight
+              const int halves = a.M <= 64 ? 2 : 1;
+              const int r = et % a.M, h = et / a.M;
+              if (h < halves) {
+                const int cw = ncols / halves;
+                const float* col = accg + r;
+                for (int c0 = h * cw; c0 < h * cw + cw; c0 += 64) {
+                  float v[64];
 #pragma unroll
-                  for (int i = 0; i < 16; ++i) v[i] = __ldcg(col + static_cast<long long>(c0 + i) * a.M);
-                  store8(a, ph, et, static_cast<long long>(t) * kTileRows + c0, v);
-                  store8(a, ph, et, static_cast<long long>(t) * kTileRows + c0 + 8, v + 8);
+                  for (int i = 0; i < 64; ++i) v[i] = __ldcg(col + static_cast<long long>(c0 + i) * a.M);
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) store8(a, ph, r, static_cast<long long>(t) * kTileRows + c0 + 8 * q, v + 8 * q);
                 }
               }
             }
@@ -846,6 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
               const int n4 = a.M * ncols / 4;
               for (int i = et; i < n4; i += 128) __stcg(z + i, make_float4(0.f, 0.f, 0.f, 0.f));
             }
+            if (et == 0) FSOPS_STAMP_IF(p == 1, 62);
           }
           if (!last) {
             if (et == 0) FSOPS_STAMP(p == 0 ? 4 : 9);
@@ -857,6 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           // publish tile t: each writer orders its stores before later TMA
           // reads, the barrier orders all of them before the release-add
           fence_proxy_async_global();
+          if (et == 0) FSOPS_STAMP(14);
           epi_bar();
           if (et == 0) red_add_release_gpu(a.hflags + t, 1u);
         } else if (a.stage_tmem) {
