@@ -159,9 +159,12 @@ bool encode_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows)
   return r == CUDA_SUCCESS;
 }
 
-int whole_tiles_enabled() {
+// Whole gate/up tiles per block (no split-K before the SwiGLU) pay off when
+// the epilogue works from TMEM (M > 32); with M <= 32 the stream-K split keeps
+// every SM streaming and its staged reduction is cheap.
+int whole_tiles_for(int M) {
   if (const char* env = std::getenv("FSOPS_WHOLE_TILES")) return std::atoi(env) != 0;
-  return 1;
+  return stage_tmem_for(npad_of(M)) ? 0 : 1;
 }
 // bf16 x [M, H] for the local quantisation: box npad rows x 128 elements.
 bool encode_x_map(CUtensorMap* m, const void* x, int H, int M, int npad) {
@@ -440,9 +443,9 @@ fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup,
   p0.KS = H / kTileK;
   p0.T = T0;
   p0.rows = 2 * I;
-  // one whole gate/up tile per block when the tiles fit the grid: the SwiGLU
-  // then needs no split-K reduction before it
-  p0.whole_tiles = (T0 <= grid && whole_tiles_enabled()) ? 1 : 0;
+  // one whole gate/up tile per block when the tiles fit the grid (M > 32): the
+  // SwiGLU then needs no split-K reduction before it
+  p0.whole_tiles = (T0 <= grid && whole_tiles_for(M)) ? 1 : 0;
   ka.local_xq = local_xq_for(ka.npad);
   p0.dep = ka.local_xq ? kDepNone : kDepXReady;
   if (ka.local_xq && !encode_x_map(&ka.tm_x, x_bf16, H, M, ka.npad)) return FSOPS_ERR_INVALID_ARG;
@@ -592,7 +595,7 @@ fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w
   const int T0 = I / kPairFeatures;
   const int T1 = (H + kTileRows - 1) / kTileRows;
   if (ctl_words_needed(Ic, T0, T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
-  const bool whole = T0 <= grid && whole_tiles_enabled();
+  const bool whole = T0 <= grid && whole_tiles_for(M);
   const NoAllocLayout l = noalloc_layout(M, H, I, whole);
   if (l.end > kNoAllocScratchBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;  // does not fit the fixed buffer
 

@@ -44,7 +44,8 @@ struct PhaseArgs {
   const uint8_t* sf_w;    // weight scales (tiled layout)
   const uint8_t* sf_act;  // activation scales (tiled layout, row tile 0)
   uint32_t* tile_cnt;     // [T] arrival counters for split tiles
-  float* accum;           // [T][256][M] fp32 sums of split tiles (column-major), zero between launches
+  float* accum;           // fp32 sums of split tiles, M * 256 per tile, zero between launches:
+                          // [T][M][256] when staged through shared memory (M <= 32), else [T][256][M]
   int KS;                 // K / 128
   int T;                  // number of tiles (ceil(rows / 256))
   int rows;               // weight rows (a multiple of 128)

@@ -358,15 +358,49 @@ __device__ __forceinline__ void store8(const KernelArgs& a, const PhaseArgs& p, 
 }
 
 // Epilogue over a tile staged in shared memory (M <= 32): stg[r * kStageLd + c].
+// The code runs once per tile, mostly cold in the instruction cache, so its
+// loops are kept rolled and free of divisions.
+//   SwiGLU: each 32-block (token r, features 32 b ..) is shared by four
+//   adjacent threads, 8 features each; the block's |max| is combined with
+//   two shuffles.  Plain: 8 columns per item.
 __device__ __forceinline__ void finish_staged(const KernelArgs& a, const PhaseArgs& ph, int t, int ncols,
                                               const float* stg, int et) {
   if (ph.epi == kEpiSwiGLU) {
-    const int r = et >> 2, b = et & 3;
-    if (r < a.M) swiglu_block(a, t, b, r, stg + r * kStageLd + 32 * b, stg + r * kStageLd + 128 + 32 * b);
+    const int tasks = a.M * 16;  // (r, b, part)
+#pragma unroll 1
+    for (int q0 = 0; q0 < tasks; q0 += 128) {
+      const int q = q0 + et;
+      const int r = q >> 4, b = (q >> 2) & 3, part = q & 3;
+      const int rr = r < a.M ? r : a.M - 1;
+      const float4* gp = reinterpret_cast<const float4*>(stg + rr * kStageLd + 32 * b + 8 * part);
+      const float4* up = reinterpret_cast<const float4*>(stg + rr * kStageLd + 128 + 32 * b + 8 * part);
+      const float4 g0 = gp[0], g1 = gp[1], u0 = up[0], u1 = up[1];
+      float h[8];
+      h[0] = silu_mul(g0.x, u0.x); h[1] = silu_mul(g0.y, u0.y); h[2] = silu_mul(g0.z, u0.z); h[3] = silu_mul(g0.w, u0.w);
+      h[4] = silu_mul(g1.x, u1.x); h[5] = silu_mul(g1.y, u1.y); h[6] = silu_mul(g1.z, u1.z); h[7] = silu_mul(g1.w, u1.w);
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const uint32_t sc = ue8m0_from_amax(amax);
+      const float inv = inv_scale_from_ue8m0(sc);
+      const uint32_t lo = e4m3_code(h[0] * inv) | (e4m3_code(h[1] * inv) << 8) | (e4m3_code(h[2] * inv) << 16) |
+                          (e4m3_code(h[3] * inv) << 24);
+      const uint32_t hi = e4m3_code(h[4] * inv) | (e4m3_code(h[5] * inv) << 8) | (e4m3_code(h[6] * inv) << 16) |
+                          (e4m3_code(h[7] * inv) << 24);
+      if (r < a.M) {
+        *reinterpret_cast<uint2*>(a.hq_codes + static_cast<long long>(r) * a.I + t * kPairFeatures + 32 * b + 8 * part) =
+            make_uint2(lo, hi);
+        if (part == 0) a.hq_sf[t * 512 + (r & 31) * 16 + (r >> 5) * 4 + b] = static_cast<uint8_t>(sc);
+      }
+    }
   } else {
-    const int per_row = ncols / 8;
-    for (int item = et; item < a.M * per_row; item += 128) {
-      const int r = item / per_row, c = (item % per_row) * 8;
+    const int lg = ncols == 256 ? 5 : 4;  // log2(items per row), 8 columns per item
+    const int items = a.M << lg;
+#pragma unroll 1
+    for (int item = et; item < items; item += 128) {
+      const int r = item >> lg, c = (item & ((1 << lg) - 1)) * 8;
       store8(a, ph, r, static_cast<long long>(t) * kTileRows + c, stg + r * kStageLd + c);
     }
   }
@@ -725,18 +759,25 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
         if (et == 0) FSOPS_STAMP(p == 0 ? 3 : 8);
         const bool whole = (ks0 == 0 && ks1 == ph.KS);
         const int ncols = (t * kTileRows + 128 < ph.rows) ? 256 : 128;
-        float* accg = ph.accum + static_cast<long long>(t) * a.M * kTileRows;  // [256][M]
+        float* accg = ph.accum + static_cast<long long>(t) * a.M * kTileRows;  // M * 256 floats
         if (a.stage_tmem) {
-          // M <= 32: warp 4 copies TMEM lanes 0..31 to shared memory and the
-          // accumulator is released at once; all four warps share the rest
+          // M <= 32: warp 4 copies TMEM lanes 0..31 to shared memory (four
+          // loads in flight per wait) and the accumulator is released at once;
+          // all four warps share the rest.  Split tiles add their rows into a
+          // row-major [M][256] accumulator, four columns per reduction.
           if (ew == 0) {
-            for (int c0 = 0; c0 < ncols; c0 += 16) {
-              float v[16];
-              tmem_ld16f(tlane + c0, v);
+#pragma unroll 1
+            for (int c0 = 0; c0 < ncols; c0 += 64) {
+              uint32_t v[4][16];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) tmem_ld16(tlane + c0 + 16 * q, v[q]);
+              tmem_ld_wait();
               if (lane < a.M) {
                 float4* d = reinterpret_cast<float4*>(stg + lane * kStageLd + c0);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                for (int q = 0; q < 16; ++q)
+                  d[q] = make_float4(__uint_as_float(v[q >> 2][4 * (q & 3)]), __uint_as_float(v[q >> 2][4 * (q & 3) + 1]),
+                                     __uint_as_float(v[q >> 2][4 * (q & 3) + 2]), __uint_as_float(v[q >> 2][4 * (q & 3) + 3]));
               }
             }
           }
@@ -745,25 +786,37 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           mbar_arrive(acc_empty);
           if (et == 0) FSOPS_STAMP(p == 0 ? 12 : 60);
           if (!whole) {
-            // column-major sums: consecutive threads add consecutive tokens of a column
-            for (int item = et; item < a.M * ncols; item += 128) {
-              const int c = item / a.M, r = item % a.M;
-              red_add_f32(accg + item, stg[r * kStageLd + c]);
+            const int lg = ncols == 256 ? 6 : 5;  // log2(float4 per row)
+#pragma unroll 1
+            for (int q = et; q < (a.M << lg); q += 128) {
+              const int r = q >> lg, c = (q & ((1 << lg) - 1)) * 4;
+              const float4 v = *reinterpret_cast<const float4*>(stg + r * kStageLd + c);
+              red_add_v4_f32(accg + r * kTileRows + c, v.x, v.y, v.z, v.w);
             }
           }
         } else {
-          // M > 32: thread et owns token et
+          // M > 32: thread et owns token et (TMEM lane et); column-major
+          // [256][M] accumulator for split tiles
           if (whole) {
             if (ph.epi == kEpiSwiGLU) {
+#pragma unroll 1
               for (int b = 0; b < 4; ++b) {
+                uint32_t gr[2][16], ur[2][16];
+                tmem_ld16(tlane + 32 * b, gr[0]);
+                tmem_ld16(tlane + 32 * b + 16, gr[1]);
+                tmem_ld16(tlane + 128 + 32 * b, ur[0]);
+                tmem_ld16(tlane + 128 + 32 * b + 16, ur[1]);
+                tmem_ld_wait();
                 float g[32], u[32];
-                tmem_ld16f(tlane + 32 * b, *reinterpret_cast<float(*)[16]>(g));
-                tmem_ld16f(tlane + 32 * b + 16, *reinterpret_cast<float(*)[16]>(g + 16));
-                tmem_ld16f(tlane + 128 + 32 * b, *reinterpret_cast<float(*)[16]>(u));
-                tmem_ld16f(tlane + 128 + 32 * b + 16, *reinterpret_cast<float(*)[16]>(u + 16));
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  g[i] = __uint_as_float(gr[i >> 4][i & 15]);
+                  u[i] = __uint_as_float(ur[i >> 4][i & 15]);
+                }
                 if (et < a.M) swiglu_block(a, t, b, et, g, u);
               }
             } else {
+#pragma unroll 1
               for (int c0 = 0; c0 < ncols; c0 += 16) {
                 float v[16];
                 tmem_ld16f(tlane + c0, v);
@@ -774,12 +827,14 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
               }
             }
           } else {
+#pragma unroll 1
             for (int c0 = 0; c0 < ncols; c0 += 16) {
               float v[16];
               tmem_ld16f(tlane + c0, v);
               if (et < a.M) {
+                float* dst = accg + static_cast<long long>(c0) * a.M + et;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) red_add_f32(accg + static_cast<long long>(c0 + j) * a.M + et, v[j]);
+                for (int j = 0; j < 16; ++j) red_add_f32(dst + j * a.M, v[j]);
               }
             }
           }
@@ -813,17 +868,19 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           if (last) {
             if (a.stage_tmem) {
               // every load is issued before the first store: one L2 round trip
-              // (M * ncols / 128 <= 64 values per thread)
-              float v[64];
+              // (M * ncols / 512 <= 16 float4 per thread)
+              const int lg = ncols == 256 ? 6 : 5;
+              const int n4 = a.M << lg;
+              float4 v[16];
 #pragma unroll
-              for (int j = 0; j < 64; ++j) {
-                const int item = et + 128 * j;
-                if (item < a.M * ncols) v[j] = __ldcg(accg + item);
+              for (int j = 0; j < 16; ++j) {
+                const int q = et + 128 * j;
+                if (q < n4) v[j] = __ldcg(reinterpret_cast<const float4*>(accg + (q >> lg) * kTileRows) + (q & ((1 << lg) - 1)));
               }
 #pragma unroll
-              for (int j = 0; j < 64; ++j) {
-                const int item = et + 128 * j;
-                if (item < a.M * ncols) stg[(item % a.M) * kStageLd + item / a.M] = v[j];
+              for (int j = 0; j < 16; ++j) {
+                const int q = et + 128 * j;
+                if (q < n4) *reinterpret_cast<float4*>(stg + (q >> lg) * kStageLd + (q & ((1 << lg) - 1)) * 4) = v[j];
               }
               epi_bar();
               if (et == 0) FSOPS_STAMP_IF(p == 1, 56);
@@ -837,12 +894,15 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
               const int r = et % a.M, h = et / a.M;
               if (h < halves) {
                 const float* col = accg + r;
+#pragma unroll 1
                 for (int b = h * (4 / halves); b < (h + 1) * (4 / halves); ++b) {
                   float g[32], u[32];
+                  const float* gc = col + static_cast<long long>(32 * b) * a.M;
+                  const float* uc = col + static_cast<long long>(128 + 32 * b) * a.M;
 #pragma unroll
                   for (int i = 0; i < 32; ++i) {
-                    g[i] = __ldcg(col + static_cast<long long>(32 * b + i) * a.M);
-                    u[i] = __ldcg(col + static_cast<long long>(128 + 32 * b + i) * a.M);
+                    g[i] = __ldcg(gc + i * a.M);
+                    u[i] = __ldcg(uc + i * a.M);
                   }
                   swiglu_block(a, t, b, r, g, u);
                 }
@@ -854,21 +914,23 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
               const int r = et % a.M, h = et / a.M;
               if (h < halves) {
                 const int cw = ncols / halves;
-                const float* col = accg + r;
+#pragma unroll 1
                 for (int c0 = h * cw; c0 < h * cw + cw; c0 += 64) {
+                  const float* cc = accg + static_cast<long long>(c0) * a.M + r;
                   float v[64];
 #pragma unroll
-                  for (int i = 0; i < 64; ++i) v[i] = __ldcg(col + static_cast<long long>(c0 + i) * a.M);
+                  for (int i = 0; i < 64; ++i) v[i] = __ldcg(cc + i * a.M);
 #pragma unroll
                   for (int q = 0; q < 8; ++q) store8(a, ph, r, static_cast<long long>(t) * kTileRows + c0 + 8 * q, v + 8 * q);
                 }
               }
             }
-            // leave the tile's accumulator zero for the next launch
+            // leave the tile's accumulator (M * 256 floats) zero for the next launch
             epi_bar();
             {
               float4* z = reinterpret_cast<float4*>(accg);
-              const int n4 = a.M * ncols / 4;
+              const int n4 = a.M * (kTileRows / 4);
+#pragma unroll 1
               for (int i = et; i < n4; i += 128) __stcg(z + i, make_float4(0.f, 0.f, 0.f, 0.f));
             }
             if (et == 0) FSOPS_STAMP_IF(p == 1, 62);
