@@ -18,7 +18,7 @@ enum CtlWord : int {
 // Wait sites reported in the status word.
 enum WaitSite : uint32_t {
   kSiteEmpty = 1, kSiteFullW = 2, kSiteFullA = 3, kSiteAccEmpty = 4, kSiteAccFull = 5,
-  kSiteXReady = 6, kSiteHFlag = 7, kSiteDrain = 8,
+  kSiteXReady = 6, kSiteHFlag = 7, kSiteDrain = 8, kSiteTileSum = 9,
 };
 
 enum : int { kDepNone = 0, kDepXReady = 1, kDepHFlags = 2 };
@@ -37,6 +37,10 @@ constexpr int kMaxSmem = 232448;    // 227 KB opt-in per block
 // intermediate features (its two 512-byte scale tiles are the gate and the up
 // scales of those features).
 constexpr int kPairFeatures = 128;
+// weight loads in flight per block before its activations are available
+constexpr int kPrimeInflight = 2;
+// split tiles whose finish an epilogue defers to the end of a phase
+constexpr int kMaxPend = 4;
 
 // One GEMM phase of the persistent kernel: T tiles of 256 weight rows times
 // KS k-stages of 128, split evenly over the grid (stream-K).
@@ -44,8 +48,7 @@ struct PhaseArgs {
   const uint8_t* sf_w;    // weight scales (tiled layout)
   const uint8_t* sf_act;  // activation scales (tiled layout, row tile 0)
   uint32_t* tile_cnt;     // [T] arrival counters for split tiles
-  float* accum;           // fp32 sums of split tiles, M * 256 per tile, zero between launches:
-                          // [T][M][256] when staged through shared memory (M <= 32), else [T][256][M]
+  float* accum;           // [T][M][256] fp32 sums of split tiles (row-major), zero between launches
   int KS;                 // K / 128
   int T;                  // number of tiles (ceil(rows / 256))
   int rows;               // weight rows (a multiple of 128)

@@ -435,6 +435,50 @@ __device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// Split tile t of a plain-output phase (M > 32): once all `owners` blocks
+// have added their sums, this owner writes the token rows [M a / n, M (a+1) / n)
+// of the tile (a = its arrival order, n = owners) and clears them in the
+// accumulator for the next launch.  pd = (t, arrival, owners, ncols).
+__device__ __noinline__ bool finish_slice(const KernelArgs& a, const PhaseArgs& ph, const Ctx& cx, int4 pd, int et,
+                                          volatile int* bcast) {
+  const int t = pd.x, arrival = pd.y, owners = pd.z, ncols = pd.w;
+  if (et == 0) *bcast = wait_counters(cx, ph.tile_cnt + t, 1, static_cast<uint32_t>(owners), kSiteTileSum) ? 1 : 0;
+  epi_bar();
+  const bool okw = *bcast != 0;
+  epi_bar();
+  if (!okw) return false;
+  float* accg = ph.accum + static_cast<long long>(t) * a.M * kTileRows;
+  const int r0 = a.M * arrival / owners, r1 = a.M * (arrival + 1) / owners;
+  const int lg = ncols == 256 ? 5 : 4;  // log2(8-column items per row)
+  const int items = (r1 - r0) << lg;
+#pragma unroll 1
+  for (int i0 = 0; i0 < items; i0 += 4 * 128) {
+    float4 v[4][2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + et + 128 * j;
+      if (i < items) {
+        const float4* src = reinterpret_cast<const float4*>(accg + (r0 + (i >> lg)) * kTileRows + (i & ((1 << lg) - 1)) * 8);
+        v[j][0] = __ldcg(src);
+        v[j][1] = __ldcg(src + 1);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + et + 128 * j;
+      if (i < items) {
+        const float w[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w, v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
+        store8(a, ph, r0 + (i >> lg), static_cast<long long>(t) * kTileRows + (i & ((1 << lg) - 1)) * 8, w);
+      }
+    }
+  }
+  epi_bar();  // every read of the rows before they are cleared
+  float4* z = reinterpret_cast<float4*>(accg + r0 * kTileRows);
+#pragma unroll 1
+  for (int i = et; i < (r1 - r0) * (kTileRows / 4); i += 128) __stcg(z + i, make_float4(0.f, 0.f, 0.f, 0.f));
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid_constant__ KernelArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -453,6 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_full + kMaxXSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  // 0 until this block's activations are available (x quantised grid-wide,
+  // or the first SwiGLU tiles published): until then the weight producer
+  // keeps only kPrimeInflight loads in flight, so that the x quantisation's
+  // own memory traffic is not queued behind the whole grid's weight stream
+  volatile int* flowing = reinterpret_cast<volatile int*>(tmem_slot + 3);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long G = gridDim.x;
@@ -469,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     mbar_init(x_issued, 128);
     for (int i = 0; i < kMaxXSlots; ++i) mbar_init(&x_full[i], 1);
     *abort_flag = 0;
+    *flowing = (a.x != nullptr && !a.local_xq) ? 0 : 1;
     mbar_fence_init();
   }
   if (warp == 2) {
@@ -503,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     uint32_t round = 0;
     // issuing waits until the load `max_inflight` stages back has landed
     int lag_stage = 0;
-    uint32_t lag_round = 0, n_issued = 0;
+    uint32_t lag_round = 0, n_issued = 0, n_landed = 0;
     bool ok = true;
     // let the epilogue warps' loads of x enter the memory system first
     if (a.x != nullptr && !a.local_xq) ok = wait_mbar(cx, x_issued, 0, kSiteEmpty);
@@ -515,10 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
         const bool v1 = t * kTileRows + 128 < ph.rows;
         for (int ks = ks0; ks < ks1; ++ks) {
           if (!wait_mbar(cx, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty)) { ok = false; break; }
-          if (n_issued >= static_cast<uint32_t>(a.max_inflight)) {
+          for (;;) {
+            const uint32_t cap = *flowing ? static_cast<uint32_t>(a.max_inflight)
+                                          : static_cast<uint32_t>(min(a.max_inflight, kPrimeInflight));
+            if (n_issued - n_landed < cap) break;
             if (!wait_mbar(cx, &full_w[lag_stage], lag_round & 1u, kSiteFullW)) { ok = false; break; }
+            ++n_landed;
             if (++lag_stage == S) { lag_stage = 0; ++lag_round; }
           }
+          if (!ok) break;
           FSOPS_STAMP_IF(n_issued < 16, 40 + n_issued);
           ++n_issued;
           uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
@@ -615,6 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
             }
             fence_proxy_async_global();
             x_ready = true;
+            *flowing = 1;
             FSOPS_STAMP(2);
           } else if (ph.dep == kDepHFlags && ks == ks0) {
             // the whole k-range of the segment: the SwiGLU tile of every 128-feature chunk
@@ -625,6 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
             fence_proxy_async_global();
             if (!h_seen) FSOPS_STAMP(5);
             h_seen = true;
+            *flowing = 1;
             FSOPS_STAMP(6);
           }
           uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
@@ -746,6 +803,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     // (2) accumulators
     uint32_t acc_round = 0;
     bool ok = true;
+    int4 pend[kMaxPend];  // split tiles to finish at the end of the phase: (t, arrival, owners, ncols)
+    int npend = 0;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(ew * 32) << 16);
     for (int p = 0; p < a.nphases && ok; ++p) {
       const PhaseArgs& ph = a.ph[p];
@@ -795,8 +854,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
             }
           }
         } else {
-          // M > 32: thread et owns token et (TMEM lane et); column-major
-          // [256][M] accumulator for split tiles
+          // M > 32: thread et owns token et (TMEM lane et); split tiles add
+          // its 16-column runs into the row-major accumulator, four at a time
           if (whole) {
             if (ph.epi == kEpiSwiGLU) {
 #pragma unroll 1
@@ -832,9 +891,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
               float v[16];
               tmem_ld16f(tlane + c0, v);
               if (et < a.M) {
-                float* dst = accg + static_cast<long long>(c0) * a.M + et;
+                float* dst = accg + et * kTileRows + c0;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) red_add_f32(dst + j * a.M, v[j]);
+                for (int q = 0; q < 4; ++q) red_add_v4_f32(dst + 4 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
               }
             }
           }
@@ -859,11 +918,27 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           epi_bar();
           if (et == 0) {
             const uint32_t old = atom_add_acq_rel_gpu(ph.tile_cnt + t, 1u);
-            *bcast = (old + 1 == expected) ? 1 : 0;
+            *bcast = static_cast<int>(old);
           }
           epi_bar();
-          const bool last = *bcast != 0;
+          const uint32_t arrival = static_cast<uint32_t>(*bcast);
+          const bool last = arrival + 1 == expected;
           epi_bar();
+          if (!a.stage_tmem && ph.epi != kEpiSwiGLU) {
+            // M > 32, plain output: every owner finishes the token rows its
+            // arrival order names, once all owners have added their sums.  The
+            // waits come after the block's last segment, so that no owner
+            // holds up its later tiles (and their owners) while it waits.
+            if (npend == kMaxPend) {
+              ok = finish_slice(a, ph, cx, pend[0], et, bcast);
+              for (int i = 1; i < npend; ++i) pend[i - 1] = pend[i];
+              --npend;
+              if (!ok) break;
+            }
+            pend[npend++] = make_int4(t, static_cast<int>(arrival), static_cast<int>(expected), ncols);
+            if (et == 0) FSOPS_STAMP(p == 0 ? 4 : 9);
+            continue;
+          }
           if (et == 0) FSOPS_STAMP_IF(p == 1, 61);
           if (last) {
             if (a.stage_tmem) {
@@ -887,41 +962,24 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
               finish_staged(a, ph, t, ncols, stg, et);
               if (et == 0) FSOPS_STAMP_IF(p == 1, 57);
             } else if (ph.epi == kEpiSwiGLU) {
-              // column c of token r sits at accg[c * M + r]: a warp reads 32
-              // consecutive floats; 64 loads are in flight before their use.
-              // With M <= 64 two threads share a token (two 32-blocks each).
+              // token r's sums are row r of the accumulator; 64 loads are in
+              // flight before their use.  With M <= 64 two threads share a
+              // token (two 32-blocks each).
               const int halves = a.M <= 64 ? 2 : 1;
               const int r = et % a.M, h = et / a.M;
               if (h < halves) {
-                const float* col = accg + r;
 #pragma unroll 1
                 for (int b = h * (4 / halves); b < (h + 1) * (4 / halves); ++b) {
                   float g[32], u[32];
-                  const float* gc = col + static_cast<long long>(32 * b) * a.M;
-                  const float* uc = col + static_cast<long long>(128 + 32 * b) * a.M;
+                  const float4* gc = reinterpret_cast<const float4*>(accg + r * kTileRows + 32 * b);
+                  const float4* uc = reinterpret_cast<const float4*>(accg + r * kTileRows + 128 + 32 * b);
 #pragma unroll
-                  for (int i = 0; i < 32; ++i) {
-                    g[i] = __ldcg(gc + i * a.M);
-                    u[i] = __ldcg(uc + i * a.M);
+                  for (int i = 0; i < 8; ++i) {
+                    const float4 gv = __ldcg(gc + i), uv = __ldcg(uc + i);
+                    g[4 * i] = gv.x; g[4 * i + 1] = gv.y; g[4 * i + 2] = gv.z; g[4 * i + 3] = gv.w;
+                    u[4 * i] = uv.x; u[4 * i + 1] = uv.y; u[4 * i + 2] = uv.z; u[4 * i + 3] = uv.w;
                   }
                   swiglu_block(a, t, b, r, g, u);
-                }
-              }
-            } else {
-              // plain output: with M <= 64 two threads share a token (one half
-              // of the columns each); batches of 64 loads in flight
-              const int halves = a.M <= 64 ? 2 : 1;
-              const int r = et % a.M, h = et / a.M;
-              if (h < halves) {
-                const int cw = ncols / halves;
-#pragma unroll 1
-                for (int c0 = h * cw; c0 < h * cw + cw; c0 += 64) {
-                  const float* cc = accg + static_cast<long long>(c0) * a.M + r;
-                  float v[64];
-#pragma unroll
-                  for (int i = 0; i < 64; ++i) v[i] = __ldcg(cc + i * a.M);
-#pragma unroll
-                  for (int q = 0; q < 8; ++q) store8(a, ph, r, static_cast<long long>(t) * kTileRows + c0 + 8 * q, v + 8 * q);
                 }
               }
             }
@@ -953,6 +1011,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
         }
         if (et == 0) FSOPS_STAMP(p == 0 ? 4 : 9);
       }
+      for (int i = 0; i < npend && ok; ++i) ok = finish_slice(a, ph, cx, pend[i], et, bcast);
+      npend = 0;
+      if (et == 0) FSOPS_STAMP_IF(p == 1, 62);
     }
     if (!ok) *abort_flag = 1;
   }
