@@ -128,8 +128,8 @@ size_t fsops_gemm_workspace_bytes(int M, int N, int K);
  * I (the second fused kernel of p2 "Resultados de benchmark del kernel": the
  * SwiGLU prologue inside the down GEMM's activation quantisation).
  *   gu      [M, 2I] fp32 in the paired order of W_gateup's rows: columns
- *           256j..256j+127 are gate features 128j..128j+127, columns
- *           256j+128..256j+255 the up features 128j..128j+127 (this is what
+ *           128j..128j+63 are gate features 64j..64j+63, columns
+ *           128j+64..128j+127 the up features 64j..64j+63 (this is what
  *           fsops_mxfp8_gemm_ex writes for A = x and B = W_gateup).
  *   h_codes [M, I] E4M3;  h_scales TCGEN05 layout, I/128 tiles of 512 bytes.
  *   1 <= M <= 128, I % 128 == 0.
@@ -142,10 +142,11 @@ fsops_status fsops_swiglu_quantize_mxfp8(const float* gu, int M, int I, uint8_t*
  *   x^ = MXFP8(x);  g = x^ Wg^T, u = x^ Wu^T (fp32 accumulate);
  *   h = SiLU(g) * u (fp32);  h^ = MXFP8(h) along I;  y = bf16(h^ Wd^T).
  *   x_bf16   [M, H] bf16.
- *   w_gateup [2I, H] E4M3, W_gate and W_up paired in blocks of 128 rows:
- *            rows 256j..256j+127 are W_gate rows 128j..128j+127 and rows
- *            256j+128..256j+255 are W_up rows 128j..128j+127 (so one 256-row
- *            weight tile holds the gate and up rows of 128 features).
+ *   w_gateup [2I, H] E4M3, W_gate and W_up paired in blocks of 64 rows:
+ *            rows 128j..128j+63 are W_gate rows 64j..64j+63 and rows
+ *            128j+64..128j+127 are W_up rows 64j..64j+63 (so every 128-row
+ *            weight tile, and its one 512-byte scale tile, holds the gate and
+ *            up rows of 64 features).
  *   w_down   [H, I] E4M3.
  *   scales   TCGEN05 scales of both.
  *   y_bf16   [M, H] bf16.

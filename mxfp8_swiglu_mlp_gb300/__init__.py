@@ -204,7 +204,7 @@ def quantize_weight(w_bf16, layout: int = SCALES_TCGEN05, stream=None) -> Tuple[
 
 class MLPWeights:
     """Quantised MLP weights: W_gateup ([2I, H], gate/up rows paired in blocks
-    of 128, see ``pair_gate_up``) and W_down ([H, I])."""
+    of 64, see ``pair_gate_up``) and W_down ([H, I])."""
 
     def __init__(self, gateup_codes, gateup_scales, down_codes, down_scales, H: int, I: int):
         self.gateup_codes, self.gateup_scales = gateup_codes, gateup_scales
@@ -216,12 +216,12 @@ class MLPWeights:
         return (self.gateup_scales, self.down_scales)
 
 
-PAIR_ROWS = 128
+PAIR_ROWS = 64
 
 
 def pair_gate_up(w_gate, w_up):
-    """The row order the library expects for W_gateup: 256-row block j holds
-    W_gate rows 128j..128j+127 followed by W_up rows 128j..128j+127."""
+    """The row order the library expects for W_gateup: 128-row block j holds
+    W_gate rows 64j..64j+63 followed by W_up rows 64j..64j+63."""
     import torch
 
     I, H = w_gate.shape

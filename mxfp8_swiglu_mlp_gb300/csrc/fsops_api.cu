@@ -140,8 +140,9 @@ MlpLayout mlp_layout(int M, int H, int I) {
   l.hq = l.xq_sf + round_up(static_cast<size_t>(H / 128) * 512, 1024);
   l.hq_sf = l.hq + round_up(static_cast<size_t>(M) * I, 1024);
   l.part0 = l.hq_sf + round_up(static_cast<size_t>(I / 128) * 512, 1024);
-  l.part1 = l.part0 + accum_bytes(M, I / kPairFeatures);
-  l.gu = l.part1 + accum_bytes(M, (H + kTileRows - 1) / kTileRows);
+  // split-K accumulators for the smallest tiles (128 rows) either phase may use
+  l.part1 = l.part0 + accum_bytes(M, 2 * I / 128);
+  l.gu = l.part1 + accum_bytes(M, H / 128);
   l.total = l.gu + round_up(static_cast<size_t>(M) * 2 * I * 4, 1024);
   return l;
 }
@@ -159,12 +160,38 @@ bool encode_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows)
   return r == CUDA_SUCCESS;
 }
 
-// Whole gate/up tiles per block (no split-K before the SwiGLU) pay off when
-// the epilogue works from TMEM (M > 32); with M <= 32 the stream-K split keeps
-// every SM streaming and its staged reduction is cheap.
-int whole_tiles_for(int M) {
-  if (const char* env = std::getenv("FSOPS_WHOLE_TILES")) return std::atoi(env) != 0;
-  return stage_tmem_for(npad_of(M)) ? 0 : 1;
+// Tile heights and split of one fused MLP launch.
+struct MlpPlan {
+  int TR0, TR1;  // weight rows per tile: gate/up, down (256 or 128)
+  int T0, T1;    // tiles per phase
+  int whole0;    // 1: one whole gate/up tile per block, no split-K before the SwiGLU
+};
+int env_choice(const char* name, int dflt, int a, int b) {
+  if (const char* env = std::getenv(name)) {
+    const int v = std::atoi(env);
+    if (v == a || v == b) return v;
+  }
+  return dflt;
+}
+MlpPlan plan_mlp(int M, int H, int I, int grid) {
+  MlpPlan pl;
+  const int npad = npad_of(M);
+  const bool staged = stage_tmem_for(npad) != 0;  // M <= 32
+  // gate/up: 256-row tiles.  With M > 32 one whole tile per block when they
+  // fit the grid (the SwiGLU then needs no split-K reduction); with M <= 32
+  // the tiles are split over all blocks, whose staged reduction is cheap and
+  // which each quantise only their half of x.  (128-row whole tiles would
+  // need no reduction either, but every block would quantise all of x.)
+  pl.TR0 = env_choice("FSOPS_TR0", 256, 128, 256);
+  pl.T0 = 2 * I / pl.TR0;
+  pl.whole0 = (pl.T0 <= grid && !staged) ? 1 : 0;
+  if (const char* env = std::getenv("FSOPS_WHOLE_TILES")) pl.whole0 = (std::atoi(env) != 0 && pl.T0 <= grid) ? 1 : 0;
+  // down projection: with M > 64, 128-row tiles halve the split-K sums the
+  // blocks add up in L2 (each tile is split over half as many blocks), which
+  // outweighs their halved loads per stage
+  pl.TR1 = env_choice("FSOPS_TR1", npad > 64 ? 128 : 256, 128, 256);
+  pl.T1 = (H + pl.TR1 - 1) / pl.TR1;
+  return pl;
 }
 // bf16 x [M, H] for the local quantisation: box npad rows x 128 elements.
 bool encode_x_map(CUtensorMap* m, const void* x, int H, int M, int npad) {
@@ -205,6 +232,63 @@ fsops_status launch(KernelArgs& a, int grid, cudaStream_t stream) {
   return FSOPS_OK;
 }
 
+// Device buffers of one fused MLP launch (workspace or fixed buffer).
+struct MlpBuffers {
+  uint8_t *ctl, *xq, *xq_sf, *hq, *hq_sf, *part0, *part1;
+};
+// Fills the two phases of the fused MLP: phase 0 gate/up (W_gateup rows in
+// tiles of pl.TR0, SwiGLU epilogue), phase 1 down (W_down in tiles of pl.TR1).
+fsops_status fill_mlp_args(KernelArgs& ka, const MlpPlan& pl, const MlpBuffers& b, const void* x_bf16,
+                           const uint8_t* w_gateup, const uint8_t* w_down, const fsops_mlp_scales* scales,
+                           void* y_bf16, int M, int H, int I) {
+  init_common(ka, M, reinterpret_cast<uint32_t*>(b.ctl));
+  const int Ic = I / 128;  // 128-feature chunks (phase-1 k-stages)
+  if (ctl_words_needed(Ic, pl.T0, pl.T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  ka.hflags = ka.ctl + kCtlHeaderWords;
+  ka.nphases = 2;
+  ka.x = static_cast<const uint16_t*>(x_bf16);
+  ka.xq_codes = b.xq;
+  ka.xq_sf = b.xq_sf;
+  ka.H = H;
+  ka.hq_codes = b.hq;
+  ka.hq_sf = b.hq_sf;
+  ka.I = I;
+  ka.out = y_bf16;
+  ka.out_f32 = 0;
+  PhaseArgs& p0 = ka.ph[0];
+  p0.sf_w = scales->gateup;
+  p0.sf_act = ka.xq_sf;
+  p0.tile_cnt = ka.hflags + Ic;
+  p0.accum = reinterpret_cast<float*>(b.part0);
+  p0.KS = H / kTileK;
+  p0.T = pl.T0;
+  p0.tile_rows = pl.TR0;
+  p0.rows = 2 * I;
+  p0.whole_tiles = pl.whole0;
+  ka.local_xq = local_xq_for(ka.npad);
+  p0.dep = ka.local_xq ? kDepNone : kDepXReady;
+  if (ka.local_xq && !encode_x_map(&ka.tm_x, x_bf16, H, M, ka.npad)) return FSOPS_ERR_INVALID_ARG;
+  p0.epi = kEpiSwiGLU;
+  p0.out_ld = I;
+  PhaseArgs& p1 = ka.ph[1];
+  p1.sf_w = scales->down;
+  p1.sf_act = ka.hq_sf;
+  p1.tile_cnt = p0.tile_cnt + pl.T0;
+  p1.accum = reinterpret_cast<float*>(b.part1);
+  p1.KS = I / kTileK;
+  p1.T = pl.T1;
+  p1.tile_rows = pl.TR1;
+  p1.rows = H;
+  p1.dep = kDepHFlags;
+  p1.epi = kEpiStore;
+  p1.out_ld = H;
+  if (!encode_map(&ka.tm_w[0], w_gateup, H, 2 * I, pl.TR0) ||
+      !encode_map(&ka.tm_act[0], ka.xq_codes, H, M, ka.npad) || !encode_map(&ka.tm_w[1], w_down, I, H, pl.TR1) ||
+      !encode_map(&ka.tm_act[1], ka.hq_codes, I, M, ka.npad))
+    return FSOPS_ERR_INVALID_ARG;
+  return FSOPS_OK;
+}
+
 bool gemm_shape_ok(int M, int N, int K) {
   return M >= 1 && M <= 128 && N >= 128 && K >= 128 && N % 128 == 0 && K % 128 == 0 && N <= 65536 &&
          K <= 65536;
@@ -224,6 +308,7 @@ fsops_status gemm_impl(const void* a, const uint8_t* a_scales, bool a_bf16, cons
   p.sf_w = b_scales;
   p.KS = K / kTileK;
   p.T = (N + kTileRows - 1) / kTileRows;
+  p.tile_rows = kTileRows;
   p.rows = N;
   p.epi = kEpiStore;
   p.out_ld = N;
@@ -417,56 +502,11 @@ fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup,
   st = check_ws(dev, l.total, &ws);
   if (st != FSOPS_OK) return st;
 
+  const MlpPlan pl = plan_mlp(M, H, I, grid);
+  const MlpBuffers bufs{ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.hq, ws + l.hq_sf, ws + l.part0, ws + l.part1};
   KernelArgs ka;
-  init_common(ka, M, reinterpret_cast<uint32_t*>(ws + l.ctl));
-  const int Ic = I / 128;                          // 128-feature chunks (phase-1 k-stages)
-  const int T0 = I / kPairFeatures;                // gate/up pair tiles
-  const int T1 = (H + kTileRows - 1) / kTileRows;  // down-projection tiles
-  if (ctl_words_needed(Ic, T0, T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
-  ka.hflags = ka.ctl + kCtlHeaderWords;
-  ka.nphases = 2;
-  ka.x = static_cast<const uint16_t*>(x_bf16);
-  ka.xq_codes = ws + l.xq;
-  ka.xq_sf = ws + l.xq_sf;
-  ka.H = H;
-  ka.hq_codes = ws + l.hq;
-  ka.hq_sf = ws + l.hq_sf;
-  ka.I = I;
-  ka.out = y_bf16;
-  ka.out_f32 = 0;
-  // phase 0: gate/up, tile t = rows [256t, 256t+256) of the paired W_gateup
-  PhaseArgs& p0 = ka.ph[0];
-  p0.sf_w = scales->gateup;
-  p0.sf_act = ka.xq_sf;
-  p0.tile_cnt = ka.hflags + Ic;
-  p0.accum = reinterpret_cast<float*>(ws + l.part0);
-  p0.KS = H / kTileK;
-  p0.T = T0;
-  p0.rows = 2 * I;
-  // one whole gate/up tile per block when the tiles fit the grid (M > 32): the
-  // SwiGLU then needs no split-K reduction before it
-  p0.whole_tiles = (T0 <= grid && whole_tiles_for(M)) ? 1 : 0;
-  ka.local_xq = local_xq_for(ka.npad);
-  p0.dep = ka.local_xq ? kDepNone : kDepXReady;
-  if (ka.local_xq && !encode_x_map(&ka.tm_x, x_bf16, H, M, ka.npad)) return FSOPS_ERR_INVALID_ARG;
-  p0.epi = kEpiSwiGLU;
-  p0.out_ld = I;
-  // phase 1: down projection, tile t = rows [256t, 256t+256) of W_down
-  PhaseArgs& p1 = ka.ph[1];
-  p1.sf_w = scales->down;
-  p1.sf_act = ka.hq_sf;
-  p1.tile_cnt = p0.tile_cnt + T0;
-  p1.accum = reinterpret_cast<float*>(ws + l.part1);
-  p1.KS = I / kTileK;
-  p1.T = T1;
-  p1.rows = H;
-  p1.dep = kDepHFlags;
-  p1.epi = kEpiStore;
-  p1.out_ld = H;
-  if (!encode_map(&ka.tm_w[0], w_gateup, H, 2 * I, kTileRows) ||
-      !encode_map(&ka.tm_act[0], ka.xq_codes, H, M, ka.npad) || !encode_map(&ka.tm_w[1], w_down, I, H, kTileRows) ||
-      !encode_map(&ka.tm_act[1], ka.hq_codes, I, M, ka.npad))
-    return FSOPS_ERR_INVALID_ARG;
+  st = fill_mlp_args(ka, pl, bufs, x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I);
+  if (st != FSOPS_OK) return st;
   return launch(ka, grid, static_cast<cudaStream_t>(stream));
 }
 
@@ -564,7 +604,7 @@ uint8_t* g_noalloc_base[kMaxDevices] = {};
 struct NoAllocLayout {
   size_t ctl, xq, xq_sf, hq, hq_sf, part0, part1, end;
 };
-NoAllocLayout noalloc_layout(int M, int H, int I, bool gateup_whole) {
+NoAllocLayout noalloc_layout(int M, int H, int I, const MlpPlan& pl) {
   NoAllocLayout l;
   l.ctl = 0;
   l.xq = kCtlRegionBytes;
@@ -572,8 +612,8 @@ NoAllocLayout noalloc_layout(int M, int H, int I, bool gateup_whole) {
   l.hq = l.xq_sf + round_up(static_cast<size_t>(H / 128) * 512, 1024);
   l.hq_sf = l.hq + round_up(static_cast<size_t>(M) * I, 1024);
   l.part0 = l.hq_sf + round_up(static_cast<size_t>(I / 128) * 512, 1024);
-  l.part1 = l.part0 + (gateup_whole ? 0 : accum_bytes(M, I / kPairFeatures));
-  l.end = l.part1 + accum_bytes(M, (H + kTileRows - 1) / kTileRows);
+  l.part1 = l.part0 + (pl.whole0 ? 0 : accum_bytes(M, pl.T0));
+  l.end = l.part1 + accum_bytes(M, pl.T1);
   return l;
 }
 
@@ -591,12 +631,9 @@ fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w
   st = current_device(&dev, &di);
   if (st != FSOPS_OK) return st;
   const int grid = di->sms;
-  const int Ic = I / 128;
-  const int T0 = I / kPairFeatures;
-  const int T1 = (H + kTileRows - 1) / kTileRows;
-  if (ctl_words_needed(Ic, T0, T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
-  const bool whole = T0 <= grid && whole_tiles_for(M);
-  const NoAllocLayout l = noalloc_layout(M, H, I, whole);
+  const MlpPlan pl = plan_mlp(M, H, I, grid);
+  if (ctl_words_needed(I / 128, pl.T0, pl.T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  const NoAllocLayout l = noalloc_layout(M, H, I, pl);
   if (l.end > kNoAllocScratchBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;  // does not fit the fixed buffer
 
   // First call on this device: look up the device address of the buffer (a
@@ -623,48 +660,10 @@ fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w
     return FSOPS_ERR_CUDA;
   }
 
+  const MlpBuffers bufs{ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.hq, ws + l.hq_sf, ws + l.part0, ws + l.part1};
   KernelArgs ka;
-  init_common(ka, M, reinterpret_cast<uint32_t*>(ws + l.ctl));
-  ka.hflags = ka.ctl + kCtlHeaderWords;
-  ka.nphases = 2;
-  ka.x = static_cast<const uint16_t*>(x_bf16);
-  ka.xq_codes = ws + l.xq;
-  ka.xq_sf = ws + l.xq_sf;
-  ka.H = H;
-  ka.hq_codes = ws + l.hq;
-  ka.hq_sf = ws + l.hq_sf;
-  ka.I = I;
-  ka.out = y_bf16;
-  ka.out_f32 = 0;
-  PhaseArgs& p0 = ka.ph[0];
-  p0.sf_w = scales->gateup;
-  p0.sf_act = ka.xq_sf;
-  p0.tile_cnt = ka.hflags + Ic;
-  p0.accum = reinterpret_cast<float*>(ws + l.part0);
-  p0.KS = H / kTileK;
-  p0.T = T0;
-  p0.rows = 2 * I;
-  p0.whole_tiles = whole ? 1 : 0;
-  ka.local_xq = local_xq_for(ka.npad);
-  p0.dep = ka.local_xq ? kDepNone : kDepXReady;
-  if (ka.local_xq && !encode_x_map(&ka.tm_x, x_bf16, H, M, ka.npad)) return FSOPS_ERR_INVALID_ARG;
-  p0.epi = kEpiSwiGLU;
-  p0.out_ld = I;
-  PhaseArgs& p1 = ka.ph[1];
-  p1.sf_w = scales->down;
-  p1.sf_act = ka.hq_sf;
-  p1.tile_cnt = p0.tile_cnt + T0;
-  p1.accum = reinterpret_cast<float*>(ws + l.part1);
-  p1.KS = I / kTileK;
-  p1.T = T1;
-  p1.rows = H;
-  p1.dep = kDepHFlags;
-  p1.epi = kEpiStore;
-  p1.out_ld = H;
-  if (!encode_map(&ka.tm_w[0], w_gateup, H, 2 * I, kTileRows) ||
-      !encode_map(&ka.tm_act[0], ka.xq_codes, H, M, ka.npad) || !encode_map(&ka.tm_w[1], w_down, I, H, kTileRows) ||
-      !encode_map(&ka.tm_act[1], ka.hq_codes, I, M, ka.npad))
-    return FSOPS_ERR_INVALID_ARG;
+  st = fill_mlp_args(ka, pl, bufs, x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I);
+  if (st != FSOPS_OK) return st;
   return launch(ka, grid, s);
 }
 

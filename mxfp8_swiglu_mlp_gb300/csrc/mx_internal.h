@@ -27,30 +27,31 @@ enum : int { kEpiSwiGLU = 0, kEpiStore = 1 };
 constexpr int kThreads = 256;       // 8 warps: 0 weight TMA, 1 activation TMA, 2 MMA, 3 idle, 4-7 epilogue
 constexpr int kMaxStages = 8;
 constexpr int kTileK = 128;         // K elements (bytes) per pipeline stage
-constexpr int kTileRows = 256;      // weight rows per tile = N of the tcgen05 instruction
+constexpr int kTileRows = 256;      // largest weight tile (rows) = N of the tcgen05 instruction; accumulator row stride
 constexpr int kMmaM = 128;          // M of the tcgen05 instruction: token rows (padded)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxSmem = 232448;    // 227 KB opt-in per block
 
-// W_gateup row order: 256-row blocks j = [W_gate rows 128j..128j+127; W_up
-// rows 128j..128j+127], so one weight tile holds a gate/up pair for 128
-// intermediate features (its two 512-byte scale tiles are the gate and the up
-// scales of those features).
-constexpr int kPairFeatures = 128;
+// W_gateup row order: 128-row blocks j = [W_gate rows 64j..64j+63; W_up rows
+// 64j..64j+63], so every 128 rows hold gate/up pairs for 64 intermediate
+// features and one 512-byte scale tile covers them.  A weight tile of 128
+// rows gives 64 features, one of 256 rows 128 (two pair blocks).
+constexpr int kPairRows = 64;
 // weight loads in flight per block before its activations are available
 constexpr int kPrimeInflight = 2;
 // split tiles whose finish an epilogue defers to the end of a phase
 constexpr int kMaxPend = 4;
 
-// One GEMM phase of the persistent kernel: T tiles of 256 weight rows times
-// KS k-stages of 128, split evenly over the grid (stream-K).
+// One GEMM phase of the persistent kernel: T tiles of tile_rows (256 or 128)
+// weight rows times KS k-stages of 128, split evenly over the grid (stream-K).
 struct PhaseArgs {
   const uint8_t* sf_w;    // weight scales (tiled layout)
   const uint8_t* sf_act;  // activation scales (tiled layout, row tile 0)
   uint32_t* tile_cnt;     // [T] arrival counters for split tiles
   float* accum;           // [T][M][256] fp32 sums of split tiles (row-major), zero between launches
   int KS;                 // K / 128
-  int T;                  // number of tiles (ceil(rows / 256))
+  int T;                  // number of tiles (ceil(rows / tile_rows))
+  int tile_rows;          // weight rows per tile = N of the tcgen05 instruction: 256 or 128
   int rows;               // weight rows (a multiple of 128)
   int whole_tiles;        // 1: block t < T does all of tile t (requires T <= grid), no split-K
   int dep;                // what the activation loads wait for (kDep*)
@@ -59,7 +60,7 @@ struct PhaseArgs {
 };
 
 struct KernelArgs {
-  CUtensorMap tm_w[2];    // weight codes [rows, K] u8, box 256 x 128, 128B swizzle
+  CUtensorMap tm_w[2];    // weight codes [rows, K] u8, box tile_rows x 128, 128B swizzle
   CUtensorMap tm_act[2];  // activation codes [M, K] u8, box npad x 128, 128B swizzle
   CUtensorMap tm_x;       // bf16 x [M, H], box npad x 128 elements, no swizzle (local_xq only)
   PhaseArgs ph[2];

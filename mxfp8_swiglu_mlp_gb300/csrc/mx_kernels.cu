@@ -139,9 +139,8 @@ __global__ void swiglu_quantize_kernel(const float* __restrict__ gu, int M, int 
       // gu columns follow the W_gateup row order: 128-column block j holds gate
       // features 64j..64j+63, then up features 64j..64j+63
       const int f0 = kb * 32;
-      const float* g = gu + static_cast<long long>(m) * 2 * I + 2 * (f0 / kPairFeatures) * kPairFeatures +
-                       (f0 % kPairFeatures);
-      const float* u = g + kPairFeatures;
+      const float* g = gu + static_cast<long long>(m) * 2 * I + 2 * (f0 / kPairRows) * kPairRows + (f0 % kPairRows);
+      const float* u = g + kPairRows;
       float h[32];
       float amax = 0.f;
 #pragma unroll
@@ -314,10 +313,18 @@ struct SegIter {
 // when the weight matrix ends half way through the tile).
 // ----------------------------------------------------------------------------
 
-// SwiGLU + requantisation of 32 intermediate features 128 t + 32 b of token r:
+// Scale byte of token r for the 32 intermediate features from f0, in the tiled
+// scale layout (512-byte tiles of 128 features).
+__device__ __forceinline__ uint32_t hq_sf_offset(int r, int f0) {
+  return static_cast<uint32_t>((f0 >> 7) * 512 + (r & 31) * 16 + (r >> 5) * 4 + ((f0 >> 5) & 3));
+}
+// Accumulator column of the gate sums of 32-block b of a gate/up tile; the up
+// sums of the same features sit kPairRows columns further.
+__device__ __forceinline__ int gate_col(int b) { return ((b >> 1) << 7) + ((b & 1) << 5); }
+
+// SwiGLU + requantisation of the 32 intermediate features f0.. of token r:
 // g[i], u[i] are the gate and up sums of those features.
-__device__ __forceinline__ void swiglu_block(const KernelArgs& a, int t, int b, int r, const float* g,
-                                             const float* u) {
+__device__ __forceinline__ void swiglu_block(const KernelArgs& a, int f0, int r, const float* g, const float* u) {
   float h[32];
   float amax = 0.f;
 #pragma unroll
@@ -332,10 +339,10 @@ __device__ __forceinline__ void swiglu_block(const KernelArgs& a, int t, int b, 
   for (int i = 0; i < 8; ++i)
     pk[i] = e4m3_code(h[4 * i] * inv) | (e4m3_code(h[4 * i + 1] * inv) << 8) |
             (e4m3_code(h[4 * i + 2] * inv) << 16) | (e4m3_code(h[4 * i + 3] * inv) << 24);
-  uint4* dst = reinterpret_cast<uint4*>(a.hq_codes + static_cast<long long>(r) * a.I + t * kPairFeatures + 32 * b);
+  uint4* dst = reinterpret_cast<uint4*>(a.hq_codes + static_cast<long long>(r) * a.I + f0);
   dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-  a.hq_sf[t * 512 + (r & 31) * 16 + (r >> 5) * 4 + b] = static_cast<uint8_t>(s);
+  a.hq_sf[hq_sf_offset(r, f0)] = static_cast<uint8_t>(s);
 }
 
 // Plain output: 8 consecutive columns c..c+7 of token r.
@@ -366,14 +373,16 @@ __device__ __forceinline__ void store8(const KernelArgs& a, const PhaseArgs& p, 
 __device__ __forceinline__ void finish_staged(const KernelArgs& a, const PhaseArgs& ph, int t, int ncols,
                                               const float* stg, int et) {
   if (ph.epi == kEpiSwiGLU) {
-    const int tasks = a.M * 16;  // (r, b, part)
+    const int lgb = ncols == 256 ? 4 : 3;  // log2(tasks per token): (ncols / 64) blocks x 4 parts
+    const int tasks = a.M << lgb;
+    const int f_tile = t * (ph.tile_rows >> 1);
 #pragma unroll 1
     for (int q0 = 0; q0 < tasks; q0 += 128) {
       const int q = q0 + et;
-      const int r = q >> 4, b = (q >> 2) & 3, part = q & 3;
+      const int r = q >> lgb, b = (q >> 2) & ((1 << (lgb - 2)) - 1), part = q & 3;
       const int rr = r < a.M ? r : a.M - 1;
-      const float4* gp = reinterpret_cast<const float4*>(stg + rr * kStageLd + 32 * b + 8 * part);
-      const float4* up = reinterpret_cast<const float4*>(stg + rr * kStageLd + 128 + 32 * b + 8 * part);
+      const float4* gp = reinterpret_cast<const float4*>(stg + rr * kStageLd + gate_col(b) + 8 * part);
+      const float4* up = reinterpret_cast<const float4*>(stg + rr * kStageLd + gate_col(b) + kPairRows + 8 * part);
       const float4 g0 = gp[0], g1 = gp[1], u0 = up[0], u1 = up[1];
       float h[8];
       h[0] = silu_mul(g0.x, u0.x); h[1] = silu_mul(g0.y, u0.y); h[2] = silu_mul(g0.z, u0.z); h[3] = silu_mul(g0.w, u0.w);
@@ -390,9 +399,9 @@ __device__ __forceinline__ void finish_staged(const KernelArgs& a, const PhaseAr
       const uint32_t hi = e4m3_code(h[4] * inv) | (e4m3_code(h[5] * inv) << 8) | (e4m3_code(h[6] * inv) << 16) |
                           (e4m3_code(h[7] * inv) << 24);
       if (r < a.M) {
-        *reinterpret_cast<uint2*>(a.hq_codes + static_cast<long long>(r) * a.I + t * kPairFeatures + 32 * b + 8 * part) =
-            make_uint2(lo, hi);
-        if (part == 0) a.hq_sf[t * 512 + (r & 31) * 16 + (r >> 5) * 4 + b] = static_cast<uint8_t>(sc);
+        const int f0 = f_tile + 32 * b;
+        *reinterpret_cast<uint2*>(a.hq_codes + static_cast<long long>(r) * a.I + f0 + 8 * part) = make_uint2(lo, hi);
+        if (part == 0) a.hq_sf[hq_sf_offset(r, f0)] = static_cast<uint8_t>(sc);
       }
     }
   } else {
@@ -401,7 +410,7 @@ __device__ __forceinline__ void finish_staged(const KernelArgs& a, const PhaseAr
 #pragma unroll 1
     for (int item = et; item < items; item += 128) {
       const int r = item >> lg, c = (item & ((1 << lg) - 1)) * 8;
-      store8(a, ph, r, static_cast<long long>(t) * kTileRows + c, stg + r * kStageLd + c);
+      store8(a, ph, r, static_cast<long long>(t) * ph.tile_rows + c, stg + r * kStageLd + c);
     }
   }
 }
@@ -468,14 +477,16 @@ __device__ __noinline__ bool finish_slice(const KernelArgs& a, const PhaseArgs& 
       const int i = i0 + et + 128 * j;
       if (i < items) {
         const float w[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w, v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
-        store8(a, ph, r0 + (i >> lg), static_cast<long long>(t) * kTileRows + (i & ((1 << lg) - 1)) * 8, w);
+        store8(a, ph, r0 + (i >> lg), static_cast<long long>(t) * ph.tile_rows + (i & ((1 << lg) - 1)) * 8, w);
       }
     }
   }
   epi_bar();  // every read of the rows before they are cleared
-  float4* z = reinterpret_cast<float4*>(accg + r0 * kTileRows);
+  // rows [r0, r1), columns [0, ncols) (row stride kTileRows)
 #pragma unroll 1
-  for (int i = et; i < (r1 - r0) * (kTileRows / 4); i += 128) __stcg(z + i, make_float4(0.f, 0.f, 0.f, 0.f));
+  for (int i = et; i < ((r1 - r0) << (lg + 1)); i += 128)
+    __stcg(reinterpret_cast<float4*>(accg + (r0 + (i >> (lg + 1))) * kTileRows) + (i & ((2 << lg) - 1)),
+           make_float4(0.f, 0.f, 0.f, 0.f));
   return true;
 }
 
@@ -562,7 +573,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       SegIter it(ph, static_cast<uint32_t>(G));
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
-        const bool v1 = t * kTileRows + 128 < ph.rows;
+        // a 256-row tile holds two 128-row scale tiles unless the matrix ends half way
+        const bool v1 = ph.tile_rows == 256 && t * 256 + 128 < ph.rows;
+        const uint32_t wbytes = static_cast<uint32_t>(ph.tile_rows) * kTileK;
         for (int ks = ks0; ks < ks1; ++ks) {
           if (!wait_mbar(cx, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty)) { ok = false; break; }
           for (;;) {
@@ -577,9 +590,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           FSOPS_STAMP_IF(n_issued < 16, 40 + n_issued);
           ++n_issued;
           uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
-          mbar_arrive_expect_tx(&full_w[stage], 32768u + (v1 ? 1024u : 512u));
-          tma_load_2d(st + stage_off_w(npad), &a.tm_w[p], &full_w[stage], ks * kTileK, t * kTileRows, pol);
-          const uint8_t* sfw = ph.sf_w + (static_cast<size_t>(2 * t) * ph.KS + ks) * 512;
+          mbar_arrive_expect_tx(&full_w[stage], wbytes + (v1 ? 1024u : 512u));
+          tma_load_2d(st + stage_off_w(npad), &a.tm_w[p], &full_w[stage], ks * kTileK, t * ph.tile_rows, pol);
+          const uint8_t* sfw = ph.sf_w + (static_cast<size_t>(t * (ph.tile_rows >> 7)) * ph.KS + ks) * 512;
           bulk_load(st + stage_off_sfw(npad), sfw, 512, &full_w[stage], pol);
           if (v1) bulk_load(st + stage_off_sfw(npad) + 512, sfw + static_cast<size_t>(ph.KS) * 512, 512, &full_w[stage], pol);
           issued_mask |= 1u << stage;
@@ -674,7 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
             FSOPS_STAMP(2);
           } else if (ph.dep == kDepHFlags && ks == ks0) {
             // the whole k-range of the segment: the SwiGLU tile of every 128-feature chunk
-            if (!wait_counters(cx, a.hflags + ks0, ks1 - ks0, 1u + a.extra_xready, kSiteHFlag)) {
+            const uint32_t tiles_per_chunk = a.ph[0].tile_rows == 128 ? 2u : 1u;
+            if (!wait_counters(cx, a.hflags + ks0, ks1 - ks0, tiles_per_chunk + a.extra_xready, kSiteHFlag)) {
               ok = false;
               break;
             }
@@ -712,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       SegIter it(ph, static_cast<uint32_t>(G));
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
-        const bool v1 = t * kTileRows + 128 < ph.rows;
+        const bool v1 = ph.tile_rows == 256 && t * 256 + 128 < ph.rows;
         const uint32_t idesc0 = idesc_mxf8_e4m3(v1 ? 256u : 128u, 0, 0);
         if (!wait_mbar(cx, acc_empty, (acc_round & 1u) ^ 1u, kSiteAccEmpty)) { ok = false; break; }
         tc_fence_after();
@@ -817,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
         tc_fence_after();
         if (et == 0) FSOPS_STAMP(p == 0 ? 3 : 8);
         const bool whole = (ks0 == 0 && ks1 == ph.KS);
-        const int ncols = (t * kTileRows + 128 < ph.rows) ? 256 : 128;
+        const int ncols = (ph.tile_rows == 256 && t * 256 + 128 < ph.rows) ? 256 : 128;
         float* accg = ph.accum + static_cast<long long>(t) * a.M * kTileRows;  // M * 256 floats
         if (a.stage_tmem) {
           // M <= 32: warp 4 copies TMEM lanes 0..31 to shared memory (four
@@ -859,12 +873,12 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           if (whole) {
             if (ph.epi == kEpiSwiGLU) {
 #pragma unroll 1
-              for (int b = 0; b < 4; ++b) {
+              for (int b = 0; b < (ncols >> 6); ++b) {
                 uint32_t gr[2][16], ur[2][16];
-                tmem_ld16(tlane + 32 * b, gr[0]);
-                tmem_ld16(tlane + 32 * b + 16, gr[1]);
-                tmem_ld16(tlane + 128 + 32 * b, ur[0]);
-                tmem_ld16(tlane + 128 + 32 * b + 16, ur[1]);
+                tmem_ld16(tlane + gate_col(b), gr[0]);
+                tmem_ld16(tlane + gate_col(b) + 16, gr[1]);
+                tmem_ld16(tlane + gate_col(b) + kPairRows, ur[0]);
+                tmem_ld16(tlane + gate_col(b) + kPairRows + 16, ur[1]);
                 tmem_ld_wait();
                 float g[32], u[32];
 #pragma unroll
@@ -872,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
                   g[i] = __uint_as_float(gr[i >> 4][i & 15]);
                   u[i] = __uint_as_float(ur[i >> 4][i & 15]);
                 }
-                if (et < a.M) swiglu_block(a, t, b, et, g, u);
+                if (et < a.M) swiglu_block(a, t * (ph.tile_rows >> 1) + 32 * b, et, g, u);
               }
             } else {
 #pragma unroll 1
@@ -880,8 +894,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
                 float v[16];
                 tmem_ld16f(tlane + c0, v);
                 if (et < a.M) {
-                  store8(a, ph, et, static_cast<long long>(t) * kTileRows + c0, v);
-                  store8(a, ph, et, static_cast<long long>(t) * kTileRows + c0 + 8, v + 8);
+                  store8(a, ph, et, static_cast<long long>(t) * ph.tile_rows + c0, v);
+                  store8(a, ph, et, static_cast<long long>(t) * ph.tile_rows + c0 + 8, v + 8);
                 }
               }
             }
@@ -968,18 +982,19 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
               const int halves = a.M <= 64 ? 2 : 1;
               const int r = et % a.M, h = et / a.M;
               if (h < halves) {
+                const int nbh = (ncols >> 6) / halves;  // 32-blocks per thread
 #pragma unroll 1
-                for (int b = h * (4 / halves); b < (h + 1) * (4 / halves); ++b) {
+                for (int b = h * nbh; b < (h + 1) * nbh; ++b) {
                   float g[32], u[32];
-                  const float4* gc = reinterpret_cast<const float4*>(accg + r * kTileRows + 32 * b);
-                  const float4* uc = reinterpret_cast<const float4*>(accg + r * kTileRows + 128 + 32 * b);
+                  const float4* gc = reinterpret_cast<const float4*>(accg + r * kTileRows + gate_col(b));
+                  const float4* uc = reinterpret_cast<const float4*>(accg + r * kTileRows + gate_col(b) + kPairRows);
 #pragma unroll
                   for (int i = 0; i < 8; ++i) {
                     const float4 gv = __ldcg(gc + i), uv = __ldcg(uc + i);
                     g[4 * i] = gv.x; g[4 * i + 1] = gv.y; g[4 * i + 2] = gv.z; g[4 * i + 3] = gv.w;
                     u[4 * i] = uv.x; u[4 * i + 1] = uv.y; u[4 * i + 2] = uv.z; u[4 * i + 3] = uv.w;
                   }
-                  swiglu_block(a, t, b, r, g, u);
+                  swiglu_block(a, t * (ph.tile_rows >> 1) + 32 * b, r, g, u);
                 }
               }
             }
@@ -1005,7 +1020,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           fence_proxy_async_global();
           if (et == 0) FSOPS_STAMP(14);
           epi_bar();
-          if (et == 0) red_add_release_gpu(a.hflags + t, 1u);
+          // (hflags count per 128-feature chunk: a 128-row tile gives half of one)
+          if (et == 0) red_add_release_gpu(a.hflags + ((t * ph.tile_rows) >> 8), 1u);
         } else if (a.stage_tmem) {
           epi_bar();  // stg is reused by the next accumulator
         }

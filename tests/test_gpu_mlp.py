@@ -57,7 +57,9 @@ def _assert_parity(got_bits, ref, per_row=True):
 
 
 SMALL = [(1, 256, 384, 0), (5, 512, 640, 1), (16, 1024, 1280, 2), (33, 384, 512, 3), (128, 256, 256, 4),
-         (64, 1152, 896, 5), (100, 640, 2048, 6)]
+         (64, 1152, 896, 5), (100, 640, 2048, 6),
+         # small H, large I: many gate/up tiles, short K loops
+         (8, 256, 4864, 7), (32, 384, 5120, 8)]
 
 
 @pytest.mark.parametrize("M,H,I,seed", SMALL)
@@ -66,6 +68,23 @@ def test_small_shapes(fs, M, H, I, seed, fused):
     wl = inputs.make_workload_small("s", M, H, I, seed)
     L = Layer(fs, wl)
     _assert_parity(L.run(fs, fused), L.oracle())
+
+
+@pytest.mark.parametrize("M,env", [
+    (16, {"FSOPS_TR0": "128", "FSOPS_WHOLE_TILES": "0"}),   # 128-row gate/up tiles, split-K
+    (16, {"FSOPS_TR0": "256", "FSOPS_WHOLE_TILES": "1"}),   # 256-row whole tiles, staged epilogue
+    (16, {"FSOPS_TR1": "128"}),                             # 128-row down tiles, staged epilogue
+    (64, {"FSOPS_TR1": "256", "FSOPS_WHOLE_TILES": "0"}),   # 256-row down tiles, split gate/up from TMEM
+    (64, {"FSOPS_TR0": "128"}),                             # 128-row whole gate/up tiles from TMEM
+])
+def test_tile_plans(fs, M, env, monkeypatch):
+    """Every tile height / split combination the kernel supports, forced
+    through the environment knobs, against the oracle."""
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    wl = inputs.make_workload_small("s", M, 512, 2560, 9)
+    L = Layer(fs, wl)
+    _assert_parity(L.run(fs, True), L.oracle())
 
 
 def test_token_scale_spread(fs):
