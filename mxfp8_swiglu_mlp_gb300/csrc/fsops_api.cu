@@ -166,6 +166,13 @@ struct MlpPlan {
   int T0, T1;    // tiles per phase
   int whole0;    // 1: one whole gate/up tile per block, no split-K before the SwiGLU
 };
+int env_int(const char* name, int dflt, int lo, int hi) {
+  if (const char* env = std::getenv(name)) {
+    const int v = std::atoi(env);
+    if (v >= lo && v <= hi) return v;
+  }
+  return dflt;
+}
 int env_choice(const char* name, int dflt, int a, int b) {
   if (const char* env = std::getenv(name)) {
     const int v = std::atoi(env);
@@ -212,6 +219,7 @@ void init_common(KernelArgs& a, int M, uint32_t* ctl) {
   a.nstages = stages_for(a.npad, 0);  // set again once local_xq is known
   a.stage_tmem = stage_tmem_for(a.npad);
   a.max_inflight = g_max_inflight.load() < a.nstages ? g_max_inflight.load() : a.nstages;
+  a.prime_inflight = env_int("FSOPS_PRIME", kPrimeInflight, 1, kMaxStages);
   a.stage_bytes = stage_bytes_for(a.npad);
   a.timeout_ns = g_timeout_ns.load();
   a.extra_xready = g_extra.load();

@@ -38,7 +38,7 @@ constexpr int kMaxSmem = 232448;    // 227 KB opt-in per block
 // rows gives 64 features, one of 256 rows 128 (two pair blocks).
 constexpr int kPairRows = 64;
 // weight loads in flight per block before its activations are available
-constexpr int kPrimeInflight = 2;
+constexpr int kPrimeInflight = 1;
 // split tiles whose finish an epilogue defers to the end of a phase
 constexpr int kMaxPend = 4;
 
@@ -86,6 +86,7 @@ struct KernelArgs {
   int local_xq;           // 1: phase 0's activation tiles are quantised from x by each block itself (npad <= 32)
   int stage_tmem;         // 1: accumulators are copied to shared memory before the epilogue (M <= 32)
   int max_inflight;       // weight tiles a block may have in flight at once
+  int prime_inflight;     // ... before its activations are available (x quantised grid-wide)
   uint32_t stage_bytes;
   uint64_t timeout_ns;
   uint32_t extra_xready;  // test hook: extra arrivals to wait for

@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
   // 0 until this block's activations are available (x quantised grid-wide,
   // or the first SwiGLU tiles published): until then the weight producer
-  // keeps only kPrimeInflight loads in flight, so that the x quantisation's
+  // keeps only prime_inflight loads in flight, so that the x quantisation's
   // own memory traffic is not queued behind the whole grid's weight stream
   volatile int* flowing = reinterpret_cast<volatile int*>(tmem_slot + 3);
 
@@ -580,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           if (!wait_mbar(cx, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty)) { ok = false; break; }
           for (;;) {
             const uint32_t cap = *flowing ? static_cast<uint32_t>(a.max_inflight)
-                                          : static_cast<uint32_t>(min(a.max_inflight, kPrimeInflight));
+                                          : static_cast<uint32_t>(min(a.max_inflight, a.prime_inflight));
             if (n_issued - n_landed < cap) break;
             if (!wait_mbar(cx, &full_w[lag_stage], lag_round & 1u, kSiteFullW)) { ok = false; break; }
             ++n_landed;
