@@ -10,7 +10,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "../../include/fsops.h"
 #include "mx_internal.h"
@@ -165,6 +167,7 @@ struct MlpPlan {
   int TR0, TR1;  // weight rows per tile: gate/up, down (256 or 128)
   int T0, T1;    // tiles per phase
   int whole0;    // 1: one whole gate/up tile per block, no split-K before the SwiGLU
+  int pairs0;    // 1: the two blocks of a cluster split a gate/up tile and add through shared memory
 };
 int env_int(const char* name, int dflt, int lo, int hi) {
   if (const char* env = std::getenv(name)) {
@@ -193,6 +196,15 @@ MlpPlan plan_mlp(int M, int H, int I, int grid) {
   pl.T0 = 2 * I / pl.TR0;
   pl.whole0 = (pl.T0 <= grid && !staged) ? 1 : 0;
   if (const char* env = std::getenv("FSOPS_WHOLE_TILES")) pl.whole0 = (std::atoi(env) != 0 && pl.T0 <= grid) ? 1 : 0;
+  // M <= 32 with between a quarter and a half as many 256-row gate/up tiles
+  // as blocks: each tile goes to one 2-block cluster, whose blocks take a K
+  // half each and add their sums through distributed shared memory (no L2
+  // reduction before the SwiGLU).  The launch falls back to the split over
+  // all blocks when the device cannot hold grid / 2 such clusters at once.
+  pl.pairs0 = (staged && !pl.whole0 && pl.TR0 == 256 && grid % 2 == 0 && 4 * pl.T0 > grid && 2 * pl.T0 <= grid &&
+               env_int("FSOPS_PAIRS", 1, 0, 1))
+                  ? 1
+                  : 0;
   // down projection: with M > 64, 128-row tiles halve the split-K sums the
   // blocks add up in L2 (each tile is split over half as many blocks), which
   // outweighs their halved loads per stage
@@ -229,9 +241,35 @@ void init_common(KernelArgs& a, int M, uint32_t* ctl) {
 #endif
 }
 
+// Whether grid / 2 two-block clusters of the kernel fit the current device at
+// this shared-memory size (queried once per device and size).
+bool pairs_fit(int grid, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, size_t>, bool> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(dev, grid, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  const bool fit = cluster_pairs_fit(grid, smem);
+  cache[key] = fit;
+  return fit;
+}
+
 fsops_status launch(KernelArgs& a, int grid, cudaStream_t stream) {
   a.nstages = stages_for(a.npad, a.local_xq);
   if (a.max_inflight > a.nstages) a.max_inflight = a.nstages;
+  bool pairs = false;
+  for (int p = 0; p < a.nphases; ++p) pairs = pairs || a.ph[p].pairs;
+  if (pairs && !pairs_fit(grid, smem_for(a.npad, a.local_xq))) {
+    for (int p = 0; p < a.nphases; ++p) a.ph[p].pairs = 0;  // split over all blocks instead
+    pairs = false;
+  }
+  a.cluster_pairs = pairs ? 1 : 0;
   cudaError_t e = launch_mx_kernel(a, grid, smem_for(a.npad, a.local_xq), stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -273,6 +311,7 @@ fsops_status fill_mlp_args(KernelArgs& ka, const MlpPlan& pl, const MlpBuffers& 
   p0.tile_rows = pl.TR0;
   p0.rows = 2 * I;
   p0.whole_tiles = pl.whole0;
+  p0.pairs = pl.pairs0;
   ka.local_xq = local_xq_for(ka.npad);
   p0.dep = ka.local_xq ? kDepNone : kDepXReady;
   if (ka.local_xq && !encode_x_map(&ka.tm_x, x_bf16, H, M, ka.npad)) return FSOPS_ERR_INVALID_ARG;

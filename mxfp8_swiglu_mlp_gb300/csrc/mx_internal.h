@@ -18,7 +18,7 @@ enum CtlWord : int {
 // Wait sites reported in the status word.
 enum WaitSite : uint32_t {
   kSiteEmpty = 1, kSiteFullW = 2, kSiteFullA = 3, kSiteAccEmpty = 4, kSiteAccFull = 5,
-  kSiteXReady = 6, kSiteHFlag = 7, kSiteDrain = 8, kSiteTileSum = 9,
+  kSiteXReady = 6, kSiteHFlag = 7, kSiteDrain = 8, kSiteTileSum = 9, kSitePeer = 10,
 };
 
 enum : int { kDepNone = 0, kDepXReady = 1, kDepHFlags = 2 };
@@ -54,6 +54,8 @@ struct PhaseArgs {
   int tile_rows;          // weight rows per tile = N of the tcgen05 instruction: 256 or 128
   int rows;               // weight rows (a multiple of 128)
   int whole_tiles;        // 1: block t < T does all of tile t (requires T <= grid), no split-K
+  int pairs;              // 1: the two blocks of cluster c split tile c in two K halves and add
+                          //    their sums through distributed shared memory (M <= 32, T <= grid / 2)
   int dep;                // what the activation loads wait for (kDep*)
   int epi;                // epilogue kind (kEpi*)
   int out_ld;             // row stride (elements) of the plain output
@@ -85,6 +87,7 @@ struct KernelArgs {
   int nstages;
   int local_xq;           // 1: phase 0's activation tiles are quantised from x by each block itself (npad <= 32)
   int stage_tmem;         // 1: accumulators are copied to shared memory before the epilogue (M <= 32)
+  int cluster_pairs;      // launched as 2-block clusters (a phase uses pairs)
   int max_inflight;       // weight tiles a block may have in flight at once
   int prime_inflight;     // ... before its activations are available (x quantised grid-wide)
   uint32_t stage_bytes;
@@ -120,6 +123,9 @@ constexpr uint32_t kSfColsPerStage = 12;
 
 // Launch wrappers (mx_kernels.cu).
 cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStream_t stream);
+// Whether `grid` blocks of the kernel with `smem` bytes of shared memory run
+// as grid / 2 co-resident 2-block clusters on the current device.
+bool cluster_pairs_fit(int grid, size_t smem);
 cudaError_t launch_quantize(const uint16_t* x, int rows, int K, int ld, uint8_t* codes, uint8_t* scales,
                             int tiled, cudaStream_t stream);
 cudaError_t launch_swiglu_quantize(const float* gu, int M, int I, uint8_t* hc, uint8_t* hs,

@@ -226,6 +226,19 @@ __device__ __forceinline__ bool wait_mbar(const Ctx& cx, uint64_t* bar, uint32_t
   }
   return true;
 }
+// The same on a barrier a CTA of the cluster arrives on (acquire at cluster scope).
+__device__ __forceinline__ bool wait_mbar_cluster(const Ctx& cx, uint64_t* bar, uint32_t parity, uint32_t site) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if ((++n & 15u) == 0) {
+      if (*cx.abort_flag || *cx.status != 0) { *cx.abort_flag = 1; return false; }
+      if (globaltimer_ns() - t0 > cx.timeout_ns) { raise_error(cx, 5u, site); return false; }
+    }
+  }
+  return true;
+}
 // Bounded wait used only while tearing down (no abort check, fixed limit).
 __device__ __forceinline__ void drain_mbar(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
@@ -291,6 +304,11 @@ struct SegIter {
     if (p.whole_tiles) {
       u = c < static_cast<uint32_t>(p.T) ? c * KS : 0;
       ue = c < static_cast<uint32_t>(p.T) ? u + KS : 0;
+    } else if (p.pairs) {
+      // block c takes K half (c & 1) of tile c / 2
+      const uint32_t tile = c >> 1, hk = KS / 2;
+      u = tile < static_cast<uint32_t>(p.T) ? tile * KS + ((c & 1) ? hk : 0) : 0;
+      ue = tile < static_cast<uint32_t>(p.T) ? tile * KS + ((c & 1) ? KS : hk) : 0;
     } else {
       const uint32_t U = static_cast<uint32_t>(p.T) * KS;
       u = split_begin(c, U, G);
@@ -370,16 +388,17 @@ __device__ __forceinline__ void store8(const KernelArgs& a, const PhaseArgs& p, 
 //   SwiGLU: each 32-block (token r, features 32 b ..) is shared by four
 //   adjacent threads, 8 features each; the block's |max| is combined with
 //   two shuffles.  Plain: 8 columns per item.
+// SwiGLU: 32-blocks [b0, b0 + nb) of the tile, nb = 2 or 4.
 __device__ __forceinline__ void finish_staged(const KernelArgs& a, const PhaseArgs& ph, int t, int ncols,
-                                              const float* stg, int et) {
+                                              const float* stg, int et, int b0, int nb) {
   if (ph.epi == kEpiSwiGLU) {
-    const int lgb = ncols == 256 ? 4 : 3;  // log2(tasks per token): (ncols / 64) blocks x 4 parts
+    const int lgb = nb == 4 ? 4 : 3;  // log2(tasks per token): nb blocks x 4 parts
     const int tasks = a.M << lgb;
     const int f_tile = t * (ph.tile_rows >> 1);
 #pragma unroll 1
     for (int q0 = 0; q0 < tasks; q0 += 128) {
       const int q = q0 + et;
-      const int r = q >> lgb, b = (q >> 2) & ((1 << (lgb - 2)) - 1), part = q & 3;
+      const int r = q >> lgb, b = b0 + ((q >> 2) & (nb - 1)), part = q & 3;
       const int rr = r < a.M ? r : a.M - 1;
       const float4* gp = reinterpret_cast<const float4*>(stg + rr * kStageLd + gate_col(b) + 8 * part);
       const float4* up = reinterpret_cast<const float4*>(stg + rr * kStageLd + gate_col(b) + kPairRows + 8 * part);
@@ -505,7 +524,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   uint64_t* drain = acc_empty + 1;
   uint64_t* x_issued = drain + 1;
   uint64_t* x_full = x_issued + 1;          // [kMaxXSlots] bf16 x tile landed (local_xq)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_full + kMaxXSlots);
+  uint64_t* peer_ready = x_full + kMaxXSlots;  // the other block of the pair has staged its sums
+  uint64_t* peer_done = peer_ready + 1;        // ... and has read this block's
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(peer_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
   // 0 until this block's activations are available (x quantised grid-wide,
@@ -528,6 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     mbar_init(drain, 1);
     mbar_init(x_issued, 128);
     for (int i = 0; i < kMaxXSlots; ++i) mbar_init(&x_full[i], 1);
+    mbar_init(peer_ready, 1);
+    mbar_init(peer_done, 1);
     *abort_flag = 0;
     *flowing = (a.x != nullptr && !a.local_xq) ? 0 : 1;
     mbar_fence_init();
@@ -546,6 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the pair's barriers are initialised before either block arrives remotely
+  if (a.cluster_pairs) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) FSOPS_STAMP(0);
 
@@ -687,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
             FSOPS_STAMP(2);
           } else if (ph.dep == kDepHFlags && ks == ks0) {
             // the whole k-range of the segment: the SwiGLU tile of every 128-feature chunk
-            const uint32_t tiles_per_chunk = a.ph[0].tile_rows == 128 ? 2u : 1u;
+            const uint32_t tiles_per_chunk = (a.ph[0].tile_rows == 128 ? 2u : 1u) * (a.ph[0].pairs ? 2u : 1u);
             if (!wait_counters(cx, a.hflags + ks0, ks1 - ks0, tiles_per_chunk + a.extra_xready, kSiteHFlag)) {
               ok = false;
               break;
@@ -858,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           epi_bar();
           mbar_arrive(acc_empty);
           if (et == 0) FSOPS_STAMP(p == 0 ? 12 : 60);
-          if (!whole) {
+          if (!whole && !ph.pairs) {
             const int lg = ncols == 256 ? 6 : 5;  // log2(float4 per row)
 #pragma unroll 1
             for (int q = et; q < (a.M << lg); q += 128) {
@@ -915,8 +940,40 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           mbar_arrive(acc_empty);
         }
         if (whole) {
-          if (a.stage_tmem) finish_staged(a, ph, t, ncols, stg, et);
+          if (a.stage_tmem) finish_staged(a, ph, t, ncols, stg, et, 0, ncols >> 6);
           if (et == 0) FSOPS_STAMP_IF(p == 0, 13);
+        } else if (ph.pairs) {
+          // The two blocks of this cluster hold the two K halves of tile t
+          // (M <= 32, both staged in shared memory).  Each adds the other's sums
+          // of its half of the columns, [128 h, 128 h + 128) = 32-blocks 2h, 2h+1,
+          // read through distributed shared memory, and finishes those features.
+          const uint32_t peer = (blockIdx.x & 1u) ^ 1u;
+          const int h = static_cast<int>(blockIdx.x & 1u);
+          if (et == 0) mbar_arrive_remote(mapa_shared(peer_ready, peer));  // my sums are staged (epi_bar above)
+          if (!wait_mbar_cluster(cx, peer_ready, 0, kSitePeer)) { ok = false; break; }
+          if (et == 0) FSOPS_STAMP(58);
+          const uint32_t pstg = mapa_shared(stg, peer);
+#pragma unroll 1
+          for (int i = et; i < (a.M << 5); i += 128) {
+            const int r = i >> 5, c = 128 * h + (i & 31) * 4;
+            const float4 pv = ld_shared_cluster_v4(pstg + static_cast<uint32_t>(r * kStageLd + c) * 4u);
+            float4* mine = reinterpret_cast<float4*>(stg + r * kStageLd + c);
+            const float4 mv = *mine;
+            *mine = make_float4(mv.x + pv.x, mv.y + pv.y, mv.z + pv.z, mv.w + pv.w);
+          }
+          epi_bar();
+          if (et == 0) FSOPS_STAMP(59);
+          if (et == 0) mbar_arrive_remote(mapa_shared(peer_done, peer));  // done with the peer's stg
+          finish_staged(a, ph, t, 256, stg, et, 2 * h, 2);
+          if (et == 0) FSOPS_STAMP_IF(p == 0, 13);
+          fence_proxy_async_global();
+          epi_bar();
+          if (et == 0) red_add_release_gpu(a.hflags + ((t * ph.tile_rows) >> 8), 1u);
+          if (et == 0) FSOPS_STAMP(14);
+          // the peer reads this block's stg: it is written again only after that
+          if (!wait_mbar_cluster(cx, peer_done, 0, kSitePeer)) { ok = false; break; }
+          if (et == 0) FSOPS_STAMP(p == 0 ? 4 : 9);
+          continue;
         } else {
           // The K range of tile t is split over several blocks: every block
           // added its sums into the tile's accumulator in L2; the block that
@@ -973,7 +1030,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
               }
               epi_bar();
               if (et == 0) FSOPS_STAMP_IF(p == 1, 56);
-              finish_staged(a, ph, t, ncols, stg, et);
+              finish_staged(a, ph, t, ncols, stg, et, 0, ncols >> 6);
               if (et == 0) FSOPS_STAMP_IF(p == 1, 57);
             } else if (ph.epi == kEpiSwiGLU) {
               // token r's sums are row r of the accumulator; 64 loads are in
@@ -1038,6 +1095,11 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // neither block of a pair leaves while the other may still read its shared memory
+  if (a.cluster_pairs) {
+    __syncwarp();
+    cluster_sync_all();
+  }
   if (warp == 2) tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0) {
     FSOPS_STAMP(10);
@@ -1069,12 +1131,42 @@ cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStr
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.cluster_pairs ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, mx_persistent_kernel, a);
+}
+
+bool cluster_pairs_fit(int grid, size_t smem) {
+  if (grid % 2 != 0) return false;
+  if (cudaFuncSetAttribute(mx_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mx_persistent_kernel, a);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mx_persistent_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return 2 * n >= grid;
 }
 
 }  // namespace fsops

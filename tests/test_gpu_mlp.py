@@ -76,13 +76,17 @@ def test_small_shapes(fs, M, H, I, seed, fused):
     (16, {"FSOPS_TR1": "128"}),                             # 128-row down tiles, staged epilogue
     (64, {"FSOPS_TR1": "256", "FSOPS_WHOLE_TILES": "0"}),   # 256-row down tiles, split gate/up from TMEM
     (64, {"FSOPS_TR0": "128"}),                             # 128-row whole gate/up tiles from TMEM
+    (16, {"I": "5120"}),                                    # gate/up tiles split by 2-block clusters
+    (16, {"I": "5120", "FSOPS_PAIRS": "0"}),                # the same shape split over all blocks
 ])
 def test_tile_plans(fs, M, env, monkeypatch):
     """Every tile height / split combination the kernel supports, forced
     through the environment knobs, against the oracle."""
+    env = dict(env)
+    I = int(env.pop("I", "2560"))
     for k, v in env.items():
         monkeypatch.setenv(k, v)
-    wl = inputs.make_workload_small("s", M, 512, 2560, 9)
+    wl = inputs.make_workload_small("s", M, 512, I, 9)
     L = Layer(fs, wl)
     _assert_parity(L.run(fs, True), L.oracle())
 
