@@ -41,7 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_write.sum, mean of the captured launches) from ncu captures, by
 # workload, with the sha256 prefix of the kernel sources they were taken on:
 # reported only while those sources are unchanged (summaries under profiles/).
-NCU_TRAFFIC = {"m16": ("19c8e74308527835", 80.46e6, "profiles/mx_persistent_kernel_m16_memory.md")}
+NCU_TRAFFIC = {"m16": ("97ba5f746dc592f8", 80.57e6, "profiles/mx_persistent_kernel_m16_memory.md "
+                       "(non-cluster launch form, FSOPS_PAIRS=0: ncu cannot launch the 2-block-cluster form)")}
 KERNEL_SOURCES = ("mx_kernels.cu", "mx_internal.h", "sm103.cuh")
 
 
