@@ -42,7 +42,8 @@ FALLBACK_HBM_GBS = 6800.0
 # workload, with the sha256 prefix of the kernel sources they were taken on:
 # reported only while those sources are unchanged (summaries under profiles/).
 NCU_TRAFFIC = {"m16": ("97ba5f746dc592f8", 80.57e6, "profiles/mx_persistent_kernel_m16_memory.md "
-                       "(non-cluster launch form, FSOPS_PAIRS=0: ncu cannot launch the 2-block-cluster form)")}
+                       "(non-cluster launch form, FSOPS_PAIRS=0: ncu cannot launch the 2-block-cluster form)"),
+               "m128": ("97ba5f746dc592f8", 163.79e6, "profiles/mx_persistent_kernel_m128_memory.md")}
 KERNEL_SOURCES = ("mx_kernels.cu", "mx_internal.h", "sm103.cuh")
 
 
@@ -61,6 +62,16 @@ def ncu_traffic(workload):
     if rec is None or rec[0] != kernel_sources_hash():
         return None, None
     return rec[1], rec[2]
+
+
+def fp8_peak_tflops():
+    """Dense FP8 tensor peak: the measured bf16 GEMM rate x 2 (the nominal
+    FP8 : bf16 ratio of the tensor cores), else the nominal 4.5 PFLOP/s."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return 2.0 * float(json.load(f)["bf16_tflops"]), "measured bf16 x 2"
+    except Exception:
+        return 4500.0, "nominal"
 
 
 def peaks():
@@ -213,6 +224,26 @@ class MlpBench:
             t_host1 = time.time()
         return e0.elapsed_time(e1) / 1e3, (t_host0, t_host1)
 
+    def timed_same(self, steps, stream):
+        """Per-call device time of `steps` fused calls on the first weight copy."""
+        import torch
+
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                self.call(0, True, stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(steps):
+                    self.call(0, True, stream)
+            g.replay()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / steps
+
     def per_launch(self, n, stream):
         """Mean duration of single fused launches, each bracketed by events on its stream."""
         import torch
@@ -260,6 +291,10 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.Stream(device=device)
     hbm_peak, peak_kind = peaks()
     wl = inputs.WORKLOADS[args.workload]
+    if args.layers:
+        import dataclasses
+
+        wl = dataclasses.replace(wl, layers=args.layers)
     M, H, I = wl.M, wl.H, wl.I
     B = algorithmic_bytes(M, H, I)
 
@@ -270,7 +305,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    dt, (h0, h1) = bench.timed(args.steps, True, args.warmup, stream)
+    dt, (h0, h1) = bench.timed(args.steps, not args.unfused, args.warmup, stream)
     if world > 1:
         t = torch.tensor([dt], dtype=torch.float64, device=device)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -294,7 +329,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
-        "config": {"workload": "%s: fused MXFP8 SwiGLU MLP, M=%d, H=%d, I=%d, one layer per step" % (wl.name, M, H, I),
+        "config": {"workload": "%s: %s MXFP8 SwiGLU MLP, M=%d, H=%d, I=%d, one layer per step" %
+                               (wl.name, "three-launch" if args.unfused else "fused", M, H, I),
                    "M": M, "H": H, "I": I, "weight_copies_rotated": bench.copies,
                    "l2": "inputs larger than L2: %d rotated weight copies, %.0f MB" %
                          (bench.copies, bench.copies * wl.weight_bytes / 1e6),
@@ -308,7 +344,7 @@ def run_ours(args, rank, world, local_rank):
                      "launch_us": round(t_launch * 1e6, 3)},
         "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "api": "fsops_mxfp8_swiglu_mlp via ctypes, pinned host buffers"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (3 if args.unfused else 1),
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
     if rank == 0 and not args.no_sweep:
@@ -344,6 +380,12 @@ def sweep(fs, device, stream, hbm_peak, args):
         entry["fused"]["launch_frac_hbm"] = round(B / tl / 1e9 / hbm_peak, 4)
         fl = 2.0 * wl.M * 3 * wl.H * wl.I
         entry["fused"]["tensor_TFLOPs"] = round(fl / tl / 1e12, 1)
+        tf = fl / (entry["fused"]["us_per_call"] * 1e-6) / 1e12
+        entry["fused"]["frac_fp8_tensor"] = round(tf / fp8_peak_tflops()[0], 4)
+        # labelled separately: the same weight copy every call, L2-warm where it fits (m1, m16)
+        tw, _ = b.timed_same(max(64, n // 4), stream)
+        entry["fused_l2_warm"] = {"us_per_call": round(tw * 1e6, 3), "tokens_per_s": round(wl.M / tw, 1),
+                                  "note": "one weight copy reused every call; L2-resident only if it fits 129 MB"}
         res[name] = entry
         del b
         torch.cuda.empty_cache()
@@ -437,6 +479,9 @@ def main():
     ap.add_argument("--workload", default="m16")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="distinct weight layers of the workload (0: its own count); profiling runs use fewer")
+    ap.add_argument("--unfused", action="store_true", help="time the three-launch path as the main loop")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
