@@ -97,7 +97,11 @@ size_t fsops_scale_bytes(int rows, int K, fsops_scale_layout layout);
  * that reads MXFP8 weights with a fixed scale stride).  A is bf16 and is
  * quantised inside the same launch; B is MXFP8 (codes + TCGEN05 scales);
  * C is bf16 (round-to-nearest-even of the fp32 accumulation).
- *   1 <= M <= 128; N % 128 == 0; K % 128 == 0; N, K <= 65536.
+ *   1 <= M <= 16384; N % 128 == 0; K % 128 == 0; N, K <= 65536.
+ *   M <= 128 (decode): one launch, the K loop split over all SMs.  M > 128
+ *   (prefill; p2 "Resultados de benchmark del kernel" runs the MLP from M = 1
+ *   to 4096): A is quantised by its own launch when bf16, then every block
+ *   computes whole 128 x 256 output tiles.
  *   workspace: device scratch of at least fsops_gemm_workspace_bytes(M, N, K)
  *   bytes, all zero before its first use.  A successful call leaves its
  *   counters and split-K accumulators zero again, so the same workspace can be
@@ -113,7 +117,7 @@ fsops_status fsops_mxfp8_gemm(const void* a_bf16, const uint8_t* b_codes, const 
 /* General form of fsops_mxfp8_gemm.
  *   a_dtype FSOPS_DTYPE_BF16: `a` is bf16 [M, K], quantised in-kernel, a_scales must be NULL.
  *   a_dtype FSOPS_DTYPE_MXFP8: `a` is E4M3 codes [M, K], a_scales its TCGEN05
- *     scales (K/128 tiles of 512 bytes, rows past M are ignored).
+ *     scales (ceil(M/128) x K/128 tiles of 512 bytes; rows past M are ignored).
  *   c_dtype FSOPS_DTYPE_BF16 or FSOPS_DTYPE_F32.  Other limits as above.
  */
 fsops_status fsops_mxfp8_gemm_ex(const void* a, const uint8_t* a_scales, fsops_dtype a_dtype,

@@ -127,8 +127,9 @@ GemmLayout gemm_layout(int M, int N, int K) {
   l.ctl = 0;
   l.xq = kCtlRegionBytes;
   l.xq_sf = l.xq + round_up(static_cast<size_t>(M) * K, 1024);
-  l.part = l.xq_sf + round_up(static_cast<size_t>(K / 128) * 512, 1024);
-  l.total = l.part + accum_bytes(M, (N + kTileRows - 1) / kTileRows);
+  // scale tiles of ceil(M / 128) row tiles; split-K sums only for M <= 128
+  l.part = l.xq_sf + round_up(static_cast<size_t>((M + 127) / 128) * (K / 128) * 512, 1024);
+  l.total = l.part + (M <= 128 ? accum_bytes(M, (N + kTileRows - 1) / kTileRows) : 0);
   return l;
 }
 struct MlpLayout {
@@ -336,9 +337,50 @@ fsops_status fill_mlp_args(KernelArgs& ka, const MlpPlan& pl, const MlpBuffers& 
   return FSOPS_OK;
 }
 
+// Up to 128 rows: the decode kernel (stream-K split over all SMs); more rows
+// (prefill): whole 128 x 256 output tiles per block.
+constexpr int kMaxGemmRows = 16384;
 bool gemm_shape_ok(int M, int N, int K) {
-  return M >= 1 && M <= 128 && N >= 128 && K >= 128 && N % 128 == 0 && K % 128 == 0 && N <= 65536 &&
+  return M >= 1 && M <= kMaxGemmRows && N >= 128 && K >= 128 && N % 128 == 0 && K % 128 == 0 && N <= 65536 &&
          K <= 65536;
+}
+
+// M > 128: A quantised by its own launch when it is bf16, then the tiled GEMM.
+fsops_status gemm_tiled_impl(const void* a, const uint8_t* a_scales, bool a_bf16, const uint8_t* b_codes,
+                             const uint8_t* b_scales, void* c, bool c_f32, int M, int N, int K, uint8_t* ctl,
+                             uint8_t* xq, uint8_t* xq_sf, const DeviceInfo* di, cudaStream_t stream) {
+  const uint8_t* codes = a_bf16 ? xq : static_cast<const uint8_t*>(a);
+  const uint8_t* sfa = a_bf16 ? xq_sf : a_scales;
+  if (a_bf16) {
+    cudaError_t e = launch_quantize(static_cast<const uint16_t*>(a), M, K, K, xq, xq_sf, 1, stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return FSOPS_ERR_CUDA;
+    }
+  }
+  TiledArgs ta;
+  std::memset(&ta, 0, sizeof(ta));
+  if (!encode_map(&ta.tm_a, codes, K, M, 128) || !encode_map(&ta.tm_b, b_codes, K, N, 256))
+    return FSOPS_ERR_INVALID_ARG;
+  ta.sf_a = sfa;
+  ta.sf_b = b_scales;
+  ta.c = c;
+  ta.c_f32 = c_f32 ? 1 : 0;
+  ta.M = M;
+  ta.N = N;
+  ta.K = K;
+  ta.KS = K / kTileK;
+  ta.MT = (M + 127) / 128;
+  ta.NT = (N + 255) / 256;
+  ta.status = reinterpret_cast<uint32_t*>(ctl) + kCtlStatus;
+  ta.timeout_ns = g_timeout_ns.load();
+  const int tiles = ta.MT * ta.NT;
+  const int grid = tiles < di->sms ? tiles : di->sms;
+  if (launch_gemm_tiled(ta, grid, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FSOPS_ERR_CUDA;
+  }
+  return FSOPS_OK;
 }
 
 // Plain GEMM (one phase) with the operand pointers already validated.
@@ -347,6 +389,7 @@ bool gemm_shape_ok(int M, int N, int K) {
 fsops_status gemm_impl(const void* a, const uint8_t* a_scales, bool a_bf16, const uint8_t* b_codes,
                        const uint8_t* b_scales, void* c, bool c_f32, int M, int N, int K, uint8_t* ctl,
                        uint8_t* xq, uint8_t* xq_sf, uint8_t* part, const DeviceInfo* di, cudaStream_t stream) {
+  if (M > 128) return gemm_tiled_impl(a, a_scales, a_bf16, b_codes, b_scales, c, c_f32, M, N, K, ctl, xq, xq_sf, di, stream);
   const int grid = di->sms;
   KernelArgs ka;
   init_common(ka, M, reinterpret_cast<uint32_t*>(ctl));

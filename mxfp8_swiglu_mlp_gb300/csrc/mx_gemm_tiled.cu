@@ -1,0 +1,238 @@
+// mx_gemm_tiled.cu -- block-scaled MXFP8 GEMM for M > 128 (prefill shapes).
+//
+//   mx_gemm_tiled_kernel   C[M, N] = A^[M, K] * B^[N, K]^T with A and B E4M3
+//                          codes plus UE8M0 scales per 32-block along K
+//                          (tcgen05 tiled scale layout), fp32 accumulation in
+//                          TMEM, bf16 or fp32 output.
+//
+// One block per SM walks the 128 x 256 output tiles (tile i, i + grid, ...).
+// Warp 0 streams the A (128 x 128 B) and B (256 x 128 B) boxes of each K
+// stage and their scale tiles by TMA into a four-stage ring; warp 1 issues
+// the block-scaled MMAs (four K = 32 steps per stage) into one TMEM
+// accumulator; warps 4-7 drain the finished tile (one output row per thread)
+// while the next tile's stages already stream in.  There is no split-K and no
+// communication between blocks: every tile has M rows of 128 tokens, so the
+// work is plentiful and each block owns whole tiles.  The same block-scaled
+// MMA form (kind::mxf8f6f4, scales copied to TMEM with tcgen05.cp) as the
+// decode kernel, per the MXFP8 1x32 format of the Fish Audio post (p2
+// "Estrategia de cuantizacion FP8").
+#include <cuda_bf16.h>
+
+#include "mx_internal.h"
+#include "sm103.cuh"
+
+namespace fsops {
+using namespace dev;
+
+namespace {
+
+constexpr int kTStages = 4;
+constexpr uint32_t kTBytesA = 128u * kTileK;             // 16 KB
+constexpr uint32_t kTBytesB = 256u * kTileK;             // 32 KB (box of 256 rows, zero fill past N)
+constexpr uint32_t kTOffSfa = kTBytesA + kTBytesB;       // 512 B: A scale tile
+constexpr uint32_t kTOffSfb = kTOffSfa + 512u;           // 1024 B: B scale tiles (two row halves)
+constexpr uint32_t kTStageBytes = 51200u;                // 1024-aligned
+constexpr uint32_t kTCtlBytes = 1024u;
+constexpr size_t kTSmem = kTStages * kTStageBytes + kTCtlBytes + 1024u;  // + alignment slack
+
+struct TWait {
+  volatile int* abort;
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+// Bounded mbarrier wait: gives up when the block aborted or the limit passed
+// (then records FSOPS_ERR_TIMEOUT with the wait site and the block).
+__device__ __forceinline__ bool twait(const TWait& w, uint64_t* bar, uint32_t parity, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++n & 15u) == 0) {
+      if (*w.abort) return false;
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        *w.abort = 1;
+        atomicCAS(w.status, 0u, (5u << 24) | ((site & 0xFFu) << 16) | (blockIdx.x & 0xFFFFu));
+        return false;
+      }
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ void tdrain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > 200000000ull) return;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid_constant__ TiledArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ctl = smem + kTStages * kTStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctl);
+  uint64_t* empty = full + kTStages;
+  uint64_t* acc_full = empty + kTStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&a.tm_a);
+    tma_prefetch_desc(&a.tm_b);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const TWait w{abort_flag, a.status, a.timeout_ns};
+  const int G = gridDim.x;
+  const int ntiles = a.MT * a.NT;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer
+    const uint64_t pol_a = l2_policy_evict_last();   // A tiles are re-read by every N tile
+    const uint64_t pol_b = l2_policy_evict_last();   // B tiles by every M tile
+    int stage = 0;
+    uint32_t round = 0, issued_mask = 0, issued_parity = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += G) {
+      const int mt = tile / a.NT, nt = tile % a.NT;
+      const bool v1 = nt * 256 + 128 < a.N;
+      for (int ks = 0; ks < a.KS; ++ks) {
+        if (!twait(w, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty)) { ok = false; break; }
+        uint8_t* st = smem + static_cast<size_t>(stage) * kTStageBytes;
+        mbar_arrive_expect_tx(&full[stage], kTBytesA + kTBytesB + 512u + (v1 ? 1024u : 512u));
+        tma_load_2d(st, &a.tm_a, &full[stage], ks * kTileK, mt * 128, pol_a);
+        tma_load_2d(st + kTBytesA, &a.tm_b, &full[stage], ks * kTileK, nt * 256, pol_b);
+        bulk_load(st + kTOffSfa, a.sf_a + (static_cast<size_t>(mt) * a.KS + ks) * 512, 512, &full[stage], pol_a);
+        const uint8_t* sfb = a.sf_b + (static_cast<size_t>(2 * nt) * a.KS + ks) * 512;
+        bulk_load(st + kTOffSfb, sfb, 512, &full[stage], pol_b);
+        if (v1) bulk_load(st + kTOffSfb + 512, sfb + static_cast<size_t>(a.KS) * 512, 512, &full[stage], pol_b);
+        issued_mask |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | ((round & 1u) << stage);
+        if (++stage == kTStages) { stage = 0; ++round; }
+      }
+    }
+    if (!ok) *abort_flag = 1;
+    for (int s = 0; s < kTStages; ++s)
+      if (issued_mask & (1u << s)) tdrain(&full[s], (issued_parity >> s) & 1u);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t round = 0, acc_round = 0;
+    bool ok = true;
+    const uint32_t sf_base = tmem + kAccCols;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += G) {
+      const int nt = tile % a.NT;
+      const bool v1 = nt * 256 + 128 < a.N;
+      const uint32_t idesc0 = idesc_mxf8_e4m3(v1 ? 256u : 128u, 0, 0);
+      if (!twait(w, acc_empty, (acc_round & 1u) ^ 1u, kSiteAccEmpty)) { ok = false; break; }
+      tc_fence_after();
+      for (int ks = 0; ks < a.KS; ++ks) {
+        if (!twait(w, &full[stage], round & 1u, kSiteFullW)) { ok = false; break; }
+        tc_fence_after();
+        uint8_t* st = smem + static_cast<size_t>(stage) * kTStageBytes;
+        const uint32_t sfc = sf_base + kSfColsPerStage * stage;
+        tc_cp_32x128b_warpx4(sfc, smem_desc(smem_u32(st + kTOffSfa), 0, 128, kSwizzleNone));
+        tc_cp_32x128b_warpx4(sfc + 4, smem_desc(smem_u32(st + kTOffSfb), 0, 128, kSwizzleNone));
+        if (v1) tc_cp_32x128b_warpx4(sfc + 8, smem_desc(smem_u32(st + kTOffSfb + 512), 0, 128, kSwizzleNone));
+        const uint32_t sa = smem_u32(st), sb = smem_u32(st + kTBytesA);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t idesc = idesc0 | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+          tc_mma_mxf8(tmem, smem_desc(sa + 32 * k, 16, 1024, kSwizzle128B), smem_desc(sb + 32 * k, 16, 1024, kSwizzle128B),
+                      idesc, sfc, sfc + 4, (ks > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(&empty[stage]);
+        if (++stage == kTStages) { stage = 0; ++round; }
+      }
+      if (!ok) break;
+      tc_commit(acc_full);
+      ++acc_round;
+    }
+    if (!ok) *abort_flag = 1;
+    tc_commit(drain);
+    tdrain(drain, 0);
+  } else if (warp >= 4) {
+    // ------------------------------------------------ epilogue: thread et = row mt * 128 + et
+    const int et = threadIdx.x - 128, ew = et >> 5;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(ew * 32) << 16);
+    uint32_t acc_round = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += G) {
+      const int mt = tile / a.NT, nt = tile % a.NT;
+      const int ncols = (nt * 256 + 128 < a.N) ? 256 : 128;
+      if (!twait(w, acc_full, acc_round & 1u, kSiteAccFull)) break;
+      ++acc_round;
+      tc_fence_after();
+      const long long row = static_cast<long long>(mt) * 128 + et;
+      const bool live = row < a.M;
+#pragma unroll 1
+      for (int c0 = 0; c0 < ncols; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tlane + c0, v);
+        tmem_ld_wait();
+        if (live) {
+          const long long o = row * a.N + static_cast<long long>(nt) * 256 + c0;
+          if (a.c_f32) {
+            float4* d = reinterpret_cast<float4*>(static_cast<float*>(a.c) + o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              d[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                                 __uint_as_float(v[4 * q + 3]));
+          } else {
+            uint32_t pk[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+              pk[q] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.c) + o);
+            d[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            d[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+    }
+  }
+
+  // ------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+cudaError_t launch_gemm_tiled(const TiledArgs& a, int grid, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(mx_gemm_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kTSmem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  mx_gemm_tiled_kernel<<<grid, kThreads, kTSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace fsops

@@ -85,7 +85,7 @@ def test_gemm_validation(fs):
     assert g(cdt=fs.DTYPE_MXFP8) == fs.ERR_INVALID_ARG
     assert g(asc=FAKE) == fs.ERR_INVALID_ARG                 # bf16 A takes no scales
     assert g(adt=fs.DTYPE_MXFP8) == fs.ERR_INVALID_ARG      # MXFP8 A needs scales
-    for M, N, K in ((0, 256, 256), (129, 256, 256), (4, 200, 256), (4, 256, 100), (4, 256, 65536 + 128)):
+    for M, N, K in ((0, 256, 256), (16385, 256, 256), (4, 200, 256), (4, 256, 100), (4, 256, 65536 + 128)):
         assert g(M=M, N=N, K=K) == fs.ERR_UNSUPPORTED_SHAPE
     assert g(c=FAKE + 2) == fs.ERR_MISALIGNED
     assert g(b=FAKE + 8) == fs.ERR_MISALIGNED

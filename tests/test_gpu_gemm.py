@@ -106,3 +106,38 @@ def test_gemm_zero_blocks_and_scale_spread(fs):
     assert rel_l2(got, ref) < 1e-5
     for m in range(M):
         assert rel_l2(got[m], ref[m]) < 1e-5
+
+
+# M > 128 (prefill): whole 128 x 256 output tiles per block, A quantised by
+# its own launch; ragged last row tile and half-width last column tile.
+PREFILL = [(129, 256, 128), (300, 384, 256), (1000, 640, 640), (4096, 256, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", PREFILL)
+def test_gemm_prefill_fp32_out_matches_oracle(fs, M, N, K):
+    a, b = _operands(M, N, K, seed=3 * M + N + K)
+    bc, bs = oracle.quantize_bf16(b)
+    ref = oracle.gemm(a, bc, bs)["c"]
+    got = _gpu_gemm(fs, a, b, c_f32=True)
+    assert rel_l2(got, ref) < 1e-5, rel_l2(got, ref)
+
+
+@pytest.mark.parametrize("M,N,K", PREFILL[:3])
+def test_gemm_prefill_bf16_out_matches_oracle(fs, M, N, K):
+    a, b = _operands(M, N, K, seed=5 * M + N + K)
+    bc, bs = oracle.quantize_bf16(b)
+    res = oracle.gemm(a, bc, bs)
+    got = _gpu_gemm(fs, a, b)
+    ref = bf16_bits_to_f64(res["c_bf16"])
+    assert rel_l2(got, ref) < 2e-3
+    assert max_abs_norm(got, ref) < 1e-2
+    assert np.mean(got == ref) > 0.9
+
+
+def test_gemm_prefill_prequantised_a(fs):
+    M, N, K = 515, 384, 384
+    a, b = _operands(M, N, K, seed=99)
+    bc, bs = oracle.quantize_bf16(b)
+    ref = oracle.gemm(a, bc, bs)["c"]
+    got = _gpu_gemm(fs, a, b, c_f32=True, prequant=True)
+    assert rel_l2(got, ref) < 1e-5
