@@ -349,6 +349,7 @@ def run_ours(args, rank, world, local_rank):
     }
     if rank == 0 and not args.no_sweep:
         out["sweep"] = sweep(fs, device, stream, hbm_peak, args)
+        out["prefill_gemm"] = prefill_gemm(fs, stream)
     if rank == 0 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(wl)
     del bench
@@ -388,6 +389,61 @@ def sweep(fs, device, stream, hbm_peak, args):
                                   "note": "one weight copy reused every call; L2-resident only if it fits 129 MB"}
         res[name] = entry
         del b
+        torch.cuda.empty_cache()
+    return res
+
+
+def prefill_gemm(fs, stream):
+    """The GEMM API above 128 rows (whole 128 x 256 tiles): the m16 MLP's
+    gate/up and down projections at M = 4096, bf16 A (quantised by its own
+    launch) and pre-quantised A; tensor-bound, so TFLOP/s against the FP8
+    peak.  torch's FP8 GEMM with one scale per tensor (cuBLAS, no 1x32 block
+    scales) is timed beside it for context."""
+    import torch
+
+    peak, peak_kind = fp8_peak_tflops()
+    res = {"fp8_peak_tflops": round(peak, 1), "peak_kind": peak_kind}
+
+    def timeit(fn, n=30):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+            e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    g = torch.Generator(device="cuda").manual_seed(7)
+    for name, (M, N, K) in (("gateup_m4096", (4096, 19456, 2560)), ("down_m4096", (4096, 2560, 9728))):
+        a = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+        w = (torch.randn(N, K, device="cuda", generator=g) / K ** 0.5).to(torch.bfloat16)
+        bc, bs = fs.quantize_weight(w)
+        ac, asc = fs.quantize_weight(a)
+        ws_n = fs.fsops_gemm_workspace_bytes(M, N, K)
+        ws = torch.zeros(ws_n, dtype=torch.uint8, device="cuda")
+        c = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        s = stream.cuda_stream
+        t_bf16 = timeit(lambda: fs.fsops_mxfp8_gemm(a, bc, bs, c, M, N, K, ws, ws_n, stream=s))
+        t_pre = timeit(lambda: fs.fsops_mxfp8_gemm_ex(ac, asc, fs.DTYPE_MXFP8, bc, bs, c, fs.DTYPE_BF16, M, N, K, ws,
+                                                      ws_n, stream=s))
+        fl = 2.0 * M * N * K
+        entry = {"M": M, "N": N, "K": K,
+                 "bf16_a_us": round(t_bf16 * 1e6, 2), "bf16_a_tflops": round(fl / t_bf16 / 1e12, 1),
+                 "mxfp8_a_us": round(t_pre * 1e6, 2), "mxfp8_a_tflops": round(fl / t_pre / 1e12, 1),
+                 "frac_fp8_tensor": round(fl / t_pre / 1e12 / peak, 4)}
+        try:
+            a8, w8 = a.to(torch.float8_e4m3fn), w.to(torch.float8_e4m3fn)
+            one = torch.ones((), device="cuda")
+            t_s = timeit(lambda: torch._scaled_mm(a8, w8.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16))
+            entry["cublas_fp8_per_tensor_us"] = round(t_s * 1e6, 2)
+        except Exception as e:  # not every torch build exposes it
+            entry["cublas_fp8_per_tensor_us"] = None
+        res[name] = entry
+        del a, w, bc, bs, ac, asc, ws, c
         torch.cuda.empty_cache()
     return res
 
