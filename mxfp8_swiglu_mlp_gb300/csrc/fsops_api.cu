@@ -360,7 +360,11 @@ fsops_status gemm_tiled_impl(const void* a, const uint8_t* a_scales, bool a_bf16
   }
   TiledArgs ta;
   std::memset(&ta, 0, sizeof(ta));
-  if (!encode_map(&ta.tm_a, codes, K, M, 128) || !encode_map(&ta.tm_b, b_codes, K, N, 256))
+  // 2-block clusters on vertically adjacent tiles (each loads half of B and
+  // multicasts it) whenever there are two row tiles
+  const int MT = (M + 127) / 128;
+  ta.cluster_ok = (MT >= 2 && di->sms >= 2 && env_int("FSOPS_GEMM_PAIRS", 1, 0, 1)) ? 1 : 0;
+  if (!encode_map(&ta.tm_a, codes, K, M, 128) || !encode_map(&ta.tm_b, b_codes, K, N, ta.cluster_ok ? 128 : 256))
     return FSOPS_ERR_INVALID_ARG;
   ta.sf_a = sfa;
   ta.sf_b = b_scales;
@@ -374,9 +378,7 @@ fsops_status gemm_tiled_impl(const void* a, const uint8_t* a_scales, bool a_bf16
   ta.NT = (N + 255) / 256;
   ta.status = reinterpret_cast<uint32_t*>(ctl) + kCtlStatus;
   ta.timeout_ns = g_timeout_ns.load();
-  const int tiles = ta.MT * ta.NT;
-  const int grid = tiles < di->sms ? tiles : di->sms;
-  if (launch_gemm_tiled(ta, grid, stream) != cudaSuccess) {
+  if (launch_gemm_tiled(ta, di->sms, stream) != cudaSuccess) {
     cudaGetLastError();
     return FSOPS_ERR_CUDA;
   }

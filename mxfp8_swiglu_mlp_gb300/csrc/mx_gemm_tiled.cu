@@ -5,7 +5,11 @@
 //                          (tcgen05 tiled scale layout), fp32 accumulation in
 //                          TMEM, bf16 or fp32 output.
 //
-// One block per SM walks the 128 x 256 output tiles (tile i, i + grid, ...).
+// One block per SM walks the 128 x 256 output tiles.  With CL = 2 the grid
+// runs as 2-block clusters that take vertically adjacent tiles (rows 256 p ..
+// 256 p + 255, same columns): each block loads its own A box and one half of
+// the shared B box, multicast into both blocks, so the pair reads each B
+// stage once from L2 (a third less operand traffic per block).
 // Warp 0 streams the A (128 x 128 B) and B (256 x 128 B) boxes of each K
 // stage and their scale tiles by TMA into a four-stage ring; warp 1 issues
 // the block-scaled MMAs (four K = 32 steps per stage) into one TMEM
@@ -67,6 +71,7 @@ __device__ __forceinline__ void tdrain(uint64_t* bar, uint32_t parity) {
 
 }  // namespace
 
+template <int CL>
 __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid_constant__ TiledArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -83,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CL);  // a stage is free once every block of the cluster has consumed it
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 128);
@@ -102,10 +107,17 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the cluster's barriers are initialised before any multicast reaches them
+  if (CL > 1) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
   const TWait w{abort_flag, a.status, a.timeout_ns};
-  const int G = gridDim.x;
-  const int ntiles = a.MT * a.NT;
+  // work items: CL vertically adjacent tiles (one per block of the cluster)
+  const int rank = CL > 1 ? static_cast<int>(blockIdx.x % CL) : 0;
+  const int G = gridDim.x / CL;
+  const int first = blockIdx.x / CL;
+  const int mrows = (a.MT + CL - 1) / CL;  // row groups of CL tiles
+  const int ntiles = mrows * a.NT;
+  const uint16_t all_ctas = static_cast<uint16_t>((1u << CL) - 1u);
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ TMA producer
@@ -114,16 +126,23 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
     int stage = 0;
     uint32_t round = 0, issued_mask = 0, issued_parity = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += G) {
-      const int mt = tile / a.NT, nt = tile % a.NT;
+    for (int tile = first; tile < ntiles && ok; tile += G) {
+      const int mt = (tile / a.NT) * CL + rank, nt = tile % a.NT;
+      const int mt_sf = mt < a.MT ? mt : a.MT - 1;  // a row tile past M: zero codes, any finite scales
       const bool v1 = nt * 256 + 128 < a.N;
       for (int ks = 0; ks < a.KS; ++ks) {
         if (!twait(w, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty)) { ok = false; break; }
         uint8_t* st = smem + static_cast<size_t>(stage) * kTStageBytes;
         mbar_arrive_expect_tx(&full[stage], kTBytesA + kTBytesB + 512u + (v1 ? 1024u : 512u));
         tma_load_2d(st, &a.tm_a, &full[stage], ks * kTileK, mt * 128, pol_a);
-        tma_load_2d(st + kTBytesA, &a.tm_b, &full[stage], ks * kTileK, nt * 256, pol_b);
-        bulk_load(st + kTOffSfa, a.sf_a + (static_cast<size_t>(mt) * a.KS + ks) * 512, 512, &full[stage], pol_a);
+        if (CL == 1) {
+          tma_load_2d(st + kTBytesA, &a.tm_b, &full[stage], ks * kTileK, nt * 256, pol_b);
+        } else {
+          // this block's 128-row half of B, into the same place in both blocks
+          tma_load_2d_multicast(st + kTBytesA + rank * (kTBytesB / 2), &a.tm_b, &full[stage], ks * kTileK,
+                                nt * 256 + rank * 128, all_ctas, pol_b);
+        }
+        bulk_load(st + kTOffSfa, a.sf_a + (static_cast<size_t>(mt_sf) * a.KS + ks) * 512, 512, &full[stage], pol_a);
         const uint8_t* sfb = a.sf_b + (static_cast<size_t>(2 * nt) * a.KS + ks) * 512;
         bulk_load(st + kTOffSfb, sfb, 512, &full[stage], pol_b);
         if (v1) bulk_load(st + kTOffSfb + 512, sfb + static_cast<size_t>(a.KS) * 512, 512, &full[stage], pol_b);
@@ -141,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
     uint32_t round = 0, acc_round = 0;
     bool ok = true;
     const uint32_t sf_base = tmem + kAccCols;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += G) {
+    for (int tile = first; tile < ntiles && ok; tile += G) {
       const int nt = tile % a.NT;
       const bool v1 = nt * 256 + 128 < a.N;
       const uint32_t idesc0 = idesc_mxf8_e4m3(v1 ? 256u : 128u, 0, 0);
@@ -162,7 +181,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
           tc_mma_mxf8(tmem, smem_desc(sa + 32 * k, 16, 1024, kSwizzle128B), smem_desc(sb + 32 * k, 16, 1024, kSwizzle128B),
                       idesc, sfc, sfc + 4, (ks > 0 || k > 0) ? 1u : 0u);
         }
-        tc_commit(&empty[stage]);
+        // the stage is free in this block and (for the multicast half) in the partner
+        if (CL == 1) tc_commit(&empty[stage]);
+        else tc_commit_multicast(&empty[stage], all_ctas);
         if (++stage == kTStages) { stage = 0; ++round; }
       }
       if (!ok) break;
@@ -177,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
     const int et = threadIdx.x - 128, ew = et >> 5;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(ew * 32) << 16);
     uint32_t acc_round = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += G) {
-      const int mt = tile / a.NT, nt = tile % a.NT;
+    for (int tile = first; tile < ntiles; tile += G) {
+      const int mt = (tile / a.NT) * CL + rank, nt = tile % a.NT;
       const int ncols = (nt * 256 + 128 < a.N) ? 256 : 128;
       if (!twait(w, acc_full, acc_round & 1u, kSiteAccFull)) break;
       ++acc_round;
@@ -220,19 +241,44 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // no block leaves while its partner may still multicast into it or arrive on it
+  if (CL > 1) {
+    __syncwarp();
+    cluster_sync_all();
+  }
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t launch_gemm_tiled(const TiledArgs& a, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm_tiled(const TiledArgs& a, int sms, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mx_gemm_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(mx_gemm_tiled_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kTSmem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mx_gemm_tiled_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kTSmem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  mx_gemm_tiled_kernel<<<grid, kThreads, kTSmem, stream>>>(a);
-  return cudaGetLastError();
+  // pairs of blocks on vertically adjacent tiles when there are at least two
+  // row tiles; grid = one block per SM at most
+  const bool pairs = a.cluster_ok != 0;  // the host chose it and encoded tm_b with 128-row boxes
+  const int cl = pairs ? 2 : 1;
+  const int items = ((a.MT + cl - 1) / cl) * a.NT;
+  const int clusters = items < sms / cl ? items : sms / cl;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters * cl);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kTSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pairs ? 1 : 0;
+  return pairs ? cudaLaunchKernelEx(&cfg, mx_gemm_tiled_kernel<2>, a) : cudaLaunchKernelEx(&cfg, mx_gemm_tiled_kernel<1>, a);
 }
 
 }  // namespace fsops

@@ -125,7 +125,7 @@ constexpr uint32_t kSfColsPerStage = 12;
 // tiles per block, no split-K.
 struct TiledArgs {
   CUtensorMap tm_a;       // A codes [M, K] u8, box 128 rows x 128, 128B swizzle
-  CUtensorMap tm_b;       // B codes [N, K] u8, box 256 rows x 128, 128B swizzle
+  CUtensorMap tm_b;       // B codes [N, K] u8, box 256 rows x 128 (128 rows with cluster_ok), 128B swizzle
   const uint8_t* sf_a;    // A scales, tiled layout, ceil(M / 128) row tiles
   const uint8_t* sf_b;    // B scales, tiled layout, N / 128 row tiles
   void* c;                // [M, N] bf16 or fp32
@@ -134,8 +134,10 @@ struct TiledArgs {
   int MT, NT;             // ceil(M / 128), ceil(N / 256)
   uint32_t* status;       // first error (status << 24 | site << 16 | block)
   uint64_t timeout_ns;
+  int cluster_ok;         // 1: run as 2-block clusters, each loading half of B and multicasting it
 };
-cudaError_t launch_gemm_tiled(const TiledArgs& a, int grid, cudaStream_t stream);
+// Launches at most one block per SM (`sms`).
+cudaError_t launch_gemm_tiled(const TiledArgs& a, int sms, cudaStream_t stream);
 
 // Launch wrappers (mx_kernels.cu).
 cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStream_t stream);
