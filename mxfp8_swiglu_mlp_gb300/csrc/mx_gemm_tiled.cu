@@ -206,29 +206,35 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
       tc_fence_after();
       const long long row = static_cast<long long>(mt) * 128 + et;
       const bool live = row < a.M;
+      // 64 columns per TMEM wait (four loads in flight)
 #pragma unroll 1
-      for (int c0 = 0; c0 < ncols; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(tlane + c0, v);
+      for (int c0 = 0; c0 < ncols; c0 += 64) {
+        uint32_t v[4][16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld16(tlane + c0 + 16 * q, v[q]);
         tmem_ld_wait();
         if (live) {
           const long long o = row * a.N + static_cast<long long>(nt) * 256 + c0;
           if (a.c_f32) {
             float4* d = reinterpret_cast<float4*>(static_cast<float*>(a.c) + o);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              d[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
-                                 __uint_as_float(v[4 * q + 3]));
+            for (int q = 0; q < 16; ++q)
+              d[q] = make_float4(__uint_as_float(v[q >> 2][4 * (q & 3)]), __uint_as_float(v[q >> 2][4 * (q & 3) + 1]),
+                                 __uint_as_float(v[q >> 2][4 * (q & 3) + 2]), __uint_as_float(v[q >> 2][4 * (q & 3) + 3]));
           } else {
-            uint32_t pk[8];
+            uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.c) + o);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
-              pk[q] = *reinterpret_cast<const uint32_t*>(&b2);
+              uint32_t pk[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int e = 8 * q + 2 * j;
+                const __nv_bfloat162 b2 =
+                    __floats2bfloat162_rn(__uint_as_float(v[e >> 4][e & 15]), __uint_as_float(v[(e + 1) >> 4][(e + 1) & 15]));
+                pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              d[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
-            uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.c) + o);
-            d[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            d[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
         }
       }
