@@ -213,6 +213,19 @@ MlpPlan plan_mlp(int M, int H, int I, int grid) {
   pl.T1 = (H + pl.TR1 - 1) / pl.TR1;
   return pl;
 }
+// Output C [M, N] of the tiled GEMM: boxes of 32 rows x 64 bytes (32 bf16 or
+// 16 fp32 columns), written from shared memory by TMA stores.
+bool encode_out_map(CUtensorMap* m, void* c, int M, int N, bool f32) {
+  const cuuint64_t es = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * es};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / es), 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 // bf16 x [M, H] for the local quantisation: box npad rows x 128 elements.
 bool encode_x_map(CUtensorMap* m, const void* x, int H, int M, int npad) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(M)};
@@ -364,7 +377,8 @@ fsops_status gemm_tiled_impl(const void* a, const uint8_t* a_scales, bool a_bf16
   // multicasts it) whenever there are two row tiles
   const int MT = (M + 127) / 128;
   ta.cluster_ok = (MT >= 2 && di->sms >= 2 && env_int("FSOPS_GEMM_PAIRS", 1, 0, 1)) ? 1 : 0;
-  if (!encode_map(&ta.tm_a, codes, K, M, 128) || !encode_map(&ta.tm_b, b_codes, K, N, ta.cluster_ok ? 128 : 256))
+  if (!encode_map(&ta.tm_a, codes, K, M, 128) || !encode_map(&ta.tm_b, b_codes, K, N, ta.cluster_ok ? 128 : 256) ||
+      !encode_out_map(&ta.tm_c, c, M, N, c_f32))
     return FSOPS_ERR_INVALID_ARG;
   ta.sf_a = sfa;
   ta.sf_b = b_scales;

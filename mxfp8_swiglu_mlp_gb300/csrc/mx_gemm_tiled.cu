@@ -37,7 +37,11 @@ constexpr uint32_t kTOffSfa = kTBytesA + kTBytesB;       // 512 B: A scale tile
 constexpr uint32_t kTOffSfb = kTOffSfa + 512u;           // 1024 B: B scale tiles (two row halves)
 constexpr uint32_t kTStageBytes = 51200u;                // 1024-aligned
 constexpr uint32_t kTCtlBytes = 1024u;
-constexpr size_t kTSmem = kTStages * kTStageBytes + kTCtlBytes + 1024u;  // + alignment slack
+// output staging: per epilogue warp two 2 KB chunks of 32 rows (32 bf16 or
+// 16 fp32 columns), written to global memory by TMA stores
+constexpr uint32_t kTChunkBytes = 2048u;
+constexpr uint32_t kTStgBytes = 4u * 2u * kTChunkBytes;
+constexpr size_t kTSmem = kTStages * kTStageBytes + kTCtlBytes + kTStgBytes + 1024u;  // + alignment slack
 
 struct TWait {
   volatile int* abort;
@@ -83,6 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* ostg = ctl + kTCtlBytes;  // [4 warps][2][kTChunkBytes]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -103,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&a.tm_a);
     tma_prefetch_desc(&a.tm_b);
+    tma_prefetch_desc(&a.tm_c);
   }
   tc_fence_before();
   __syncthreads();
@@ -195,52 +201,59 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
     tdrain(drain, 0);
   } else if (warp >= 4) {
     // ------------------------------------------------ epilogue: thread et = row mt * 128 + et
+    // Each warp turns its 32 rows into 2 KB chunks in shared memory (two
+    // buffers) that TMA stores to C; the accumulator is released as soon as
+    // it has been read, while the stores drain.
     const int et = threadIdx.x - 128, ew = et >> 5;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(ew * 32) << 16);
-    uint32_t acc_round = 0;
+    const int cw = a.c_f32 ? 16 : 32;  // columns per chunk
+    uint8_t* wbuf = ostg + ew * 2 * kTChunkBytes;
+    uint32_t acc_round = 0, nchunk = 0;
     for (int tile = first; tile < ntiles; tile += G) {
       const int mt = (tile / a.NT) * CL + rank, nt = tile % a.NT;
       const int ncols = (nt * 256 + 128 < a.N) ? 256 : 128;
       if (!twait(w, acc_full, acc_round & 1u, kSiteAccFull)) break;
       ++acc_round;
       tc_fence_after();
-      const long long row = static_cast<long long>(mt) * 128 + et;
-      const bool live = row < a.M;
-      // 64 columns per TMEM wait (four loads in flight)
 #pragma unroll 1
-      for (int c0 = 0; c0 < ncols; c0 += 64) {
-        uint32_t v[4][16];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld16(tlane + c0 + 16 * q, v[q]);
+      for (int c0 = 0; c0 < ncols; c0 += cw, ++nchunk) {
+        uint32_t v[2][16];
+        tmem_ld16(tlane + c0, v[0]);
+        if (!a.c_f32) tmem_ld16(tlane + c0 + 16, v[1]);
         tmem_ld_wait();
-        if (live) {
-          const long long o = row * a.N + static_cast<long long>(nt) * 256 + c0;
-          if (a.c_f32) {
-            float4* d = reinterpret_cast<float4*>(static_cast<float*>(a.c) + o);
+        uint8_t* buf = wbuf + (nchunk & 1u) * kTChunkBytes;
+        // the store issued from this buffer two chunks ago has read it
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        uint4* rowp = reinterpret_cast<uint4*>(buf + lane * 64);  // 32 rows x 64 B
+        if (a.c_f32) {
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
-              d[q] = make_float4(__uint_as_float(v[q >> 2][4 * (q & 3)]), __uint_as_float(v[q >> 2][4 * (q & 3) + 1]),
-                                 __uint_as_float(v[q >> 2][4 * (q & 3) + 2]), __uint_as_float(v[q >> 2][4 * (q & 3) + 3]));
-          } else {
-            uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.c) + o);
+          for (int q = 0; q < 4; ++q) rowp[q] = make_uint4(v[0][4 * q], v[0][4 * q + 1], v[0][4 * q + 2], v[0][4 * q + 3]);
+        } else {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              uint32_t pk[4];
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pk[4];
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int e = 8 * q + 2 * j;
-                const __nv_bfloat162 b2 =
-                    __floats2bfloat162_rn(__uint_as_float(v[e >> 4][e & 15]), __uint_as_float(v[(e + 1) >> 4][(e + 1) & 15]));
-                pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
-              }
-              d[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int j = 0; j < 4; ++j) {
+              const int e = 8 * q + 2 * j;
+              const __nv_bfloat162 b2 =
+                  __floats2bfloat162_rn(__uint_as_float(v[e >> 4][e & 15]), __uint_as_float(v[(e + 1) >> 4][(e + 1) & 15]));
+              pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
             }
+            rowp[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
+        }
+        fence_proxy_async_shared();  // the TMA store reads what the warp wrote
+        __syncwarp();
+        if (lane == 0 && mt * 128 + ew * 32 < a.M) {  // rows past M are clipped; a box wholly past M is not issued
+          tma_store_2d(&a.tm_c, buf, nt * 256 + c0, mt * 128 + ew * 32);
+          bulk_commit_group();
         }
       }
       tc_fence_before();
       mbar_arrive(acc_empty);
     }
+    if (lane == 0) bulk_wait_all();  // every store has landed before the block ends
   }
 
   // ------------------------------------------------ teardown

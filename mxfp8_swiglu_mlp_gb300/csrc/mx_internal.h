@@ -126,6 +126,7 @@ constexpr uint32_t kSfColsPerStage = 12;
 struct TiledArgs {
   CUtensorMap tm_a;       // A codes [M, K] u8, box 128 rows x 128, 128B swizzle
   CUtensorMap tm_b;       // B codes [N, K] u8, box 256 rows x 128 (128 rows with cluster_ok), 128B swizzle
+  CUtensorMap tm_c;       // C [M, N] bf16 (box 32 rows x 32) or fp32 (box 32 rows x 16), no swizzle
   const uint8_t* sf_a;    // A scales, tiled layout, ceil(M / 128) row tiles
   const uint8_t* sf_b;    // B scales, tiled layout, N / 128 row tiles
   void* c;                // [M, N] bf16 or fp32
