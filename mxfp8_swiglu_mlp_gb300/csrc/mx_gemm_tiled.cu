@@ -37,10 +37,14 @@ constexpr uint32_t kTOffSfa = kTBytesA + kTBytesB;       // 512 B: A scale tile
 constexpr uint32_t kTOffSfb = kTOffSfa + 512u;           // 1024 B: B scale tiles (two row halves)
 constexpr uint32_t kTStageBytes = 51200u;                // 1024-aligned
 constexpr uint32_t kTCtlBytes = 1024u;
-// output staging: per epilogue warp two 2 KB chunks of 32 rows (32 bf16 or
-// 16 fp32 columns), written to global memory by TMA stores
+// 12 warps: 0 TMA, 1 MMA, 4-11 epilogue (two warps per TMEM lane quarter,
+// one per half of the tile's columns)
+constexpr int kTThreads = 384;
+constexpr int kTEpiWarps = 8;
+// output staging: per epilogue warp one 2 KB chunk of 32 rows (32 bf16 or 16
+// fp32 columns), written to global memory by a TMA store
 constexpr uint32_t kTChunkBytes = 2048u;
-constexpr uint32_t kTStgBytes = 4u * 2u * kTChunkBytes;
+constexpr uint32_t kTStgBytes = kTEpiWarps * kTChunkBytes;
 constexpr size_t kTSmem = kTStages * kTStageBytes + kTCtlBytes + kTStgBytes + 1024u;  // + alignment slack
 
 struct TWait {
@@ -76,7 +80,7 @@ __device__ __forceinline__ void tdrain(uint64_t* bar, uint32_t parity) {
 }  // namespace
 
 template <int CL>
-__global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid_constant__ TiledArgs a) {
+__global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __grid_constant__ TiledArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ctl = smem + kTStages * kTStageBytes;
@@ -87,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint8_t* ostg = ctl + kTCtlBytes;  // [4 warps][2][kTChunkBytes]
+  uint8_t* ostg = ctl + kTCtlBytes;  // [kTEpiWarps][kTChunkBytes]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -96,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
       mbar_init(&empty[s], CL);  // a stage is free once every block of the cluster has consumed it
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 128);
+    mbar_init(acc_empty, 32 * kTEpiWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -200,30 +204,31 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
     tc_commit(drain);
     tdrain(drain, 0);
   } else if (warp >= 4) {
-    // ------------------------------------------------ epilogue: thread et = row mt * 128 + et
-    // Each warp turns its 32 rows into 2 KB chunks in shared memory (two
-    // buffers) that TMA stores to C; the accumulator is released as soon as
-    // it has been read, while the stores drain.
-    const int et = threadIdx.x - 128, ew = et >> 5;
-    const uint32_t tlane = tmem + (static_cast<uint32_t>(ew * 32) << 16);
+    // ------------------------------------------------ epilogue
+    // Warp e (4..11) reads TMEM lane quarter e % 4 (rows 32 (e % 4) .. + 31 of
+    // the tile) and half (e - 4) / 4 of the columns.  It turns them into 2 KB
+    // chunks in shared memory that TMA stores to C; the accumulator is
+    // released as soon as every warp has read its part, while the stores drain.
+    const int ew = warp - 4, q4 = warp & 3, half = ew >> 2;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
     const int cw = a.c_f32 ? 16 : 32;  // columns per chunk
-    uint8_t* wbuf = ostg + ew * 2 * kTChunkBytes;
-    uint32_t acc_round = 0, nchunk = 0;
+    uint8_t* buf = ostg + ew * kTChunkBytes;
+    uint32_t acc_round = 0;
     for (int tile = first; tile < ntiles; tile += G) {
       const int mt = (tile / a.NT) * CL + rank, nt = tile % a.NT;
       const int ncols = (nt * 256 + 128 < a.N) ? 256 : 128;
       if (!twait(w, acc_full, acc_round & 1u, kSiteAccFull)) break;
       ++acc_round;
       tc_fence_after();
+      const int cbeg = half * (ncols >> 1), cend = cbeg + (ncols >> 1);
 #pragma unroll 1
-      for (int c0 = 0; c0 < ncols; c0 += cw, ++nchunk) {
+      for (int c0 = cbeg; c0 < cend; c0 += cw) {
         uint32_t v[2][16];
         tmem_ld16(tlane + c0, v[0]);
         if (!a.c_f32) tmem_ld16(tlane + c0 + 16, v[1]);
         tmem_ld_wait();
-        uint8_t* buf = wbuf + (nchunk & 1u) * kTChunkBytes;
-        // the store issued from this buffer two chunks ago has read it
-        if (lane == 0) bulk_wait_read<1>();
+        // the store issued from this buffer before has read it
+        if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
         uint4* rowp = reinterpret_cast<uint4*>(buf + lane * 64);  // 32 rows x 64 B
         if (a.c_f32) {
@@ -245,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_tiled_kernel(const __grid
         }
         fence_proxy_async_shared();  // the TMA store reads what the warp wrote
         __syncwarp();
-        if (lane == 0 && mt * 128 + ew * 32 < a.M) {  // rows past M are clipped; a box wholly past M is not issued
-          tma_store_2d(&a.tm_c, buf, nt * 256 + c0, mt * 128 + ew * 32);
+        if (lane == 0 && mt * 128 + q4 * 32 < a.M) {  // rows past M are clipped; a box wholly past M is not issued
+          tma_store_2d(&a.tm_c, buf, nt * 256 + c0, mt * 128 + q4 * 32);
           bulk_commit_group();
         }
       }
@@ -287,7 +292,7 @@ cudaError_t launch_gemm_tiled(const TiledArgs& a, int sms, cudaStream_t stream) 
   const int clusters = items < sms / cl ? items : sms / cl;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(clusters * cl);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kTThreads);
   cfg.dynamicSmemBytes = kTSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
