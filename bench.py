@@ -384,7 +384,7 @@ def sweep(fs, device, stream, hbm_peak, args):
         tf = fl / (entry["fused"]["us_per_call"] * 1e-6) / 1e12
         entry["fused"]["frac_fp8_tensor"] = round(tf / fp8_peak_tflops()[0], 4)
         # labelled separately: the same weight copy every call, L2-warm where it fits (m1, m16)
-        tw, _ = b.timed_same(max(64, n // 4), stream)
+        tw = b.timed_same(max(64, n // 4), stream)
         entry["fused_l2_warm"] = {"us_per_call": round(tw * 1e6, 3), "tokens_per_s": round(wl.M / tw, 1),
                                   "note": "one weight copy reused every call; L2-resident only if it fits 129 MB"}
         res[name] = entry
