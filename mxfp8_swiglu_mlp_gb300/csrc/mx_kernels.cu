@@ -1,9 +1,12 @@
 // mx_kernels.cu -- the sm_103a kernels of the MXFP8 SwiGLU MLP.
 //
-//   mx_persistent_kernel   one launch per GEMM or per whole MLP: cooperative
-//                          grid of one block per SM; TMA streams weight tiles,
-//                          tcgen05 block-scaled MMAs accumulate in TMEM,
-//                          stream-K split of the K loop over all blocks.
+//   mx_persistent_kernel   one launch per GEMM (M <= 128) or per whole MLP:
+//                          cooperative grid of one block per SM; TMA streams
+//                          weight tiles, tcgen05 block-scaled MMAs accumulate
+//                          in TMEM; per phase either a stream-K split of the
+//                          K loop over all blocks (sums added in L2), one
+//                          whole tile per block, or 2-block clusters that add
+//                          their two K halves through distributed shared memory.
 //   quantize_kernel        bf16 -> E4M3 + UE8M0 (row-major or tiled scales).
 //   swiglu_quantize_kernel SiLU(g) * u -> E4M3 + UE8M0 (the unfused path).
 //
