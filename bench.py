@@ -41,9 +41,9 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_write.sum, mean of the captured launches) from ncu captures, by
 # workload, with the sha256 prefix of the kernel sources they were taken on:
 # reported only while those sources are unchanged (summaries under profiles/).
-NCU_TRAFFIC = {"m16": ("97ba5f746dc592f8", 80.57e6, "profiles/mx_persistent_kernel_m16_memory.md "
+NCU_TRAFFIC = {"m16": ("58b77035fc62aed6", 80.52e6, "profiles/mx_persistent_kernel_m16_memory.md "
                        "(non-cluster launch form, FSOPS_PAIRS=0: ncu cannot launch the 2-block-cluster form)"),
-               "m128": ("97ba5f746dc592f8", 163.79e6, "profiles/mx_persistent_kernel_m128_memory.md")}
+               "m128": ("58b77035fc62aed6", 163.68e6, "profiles/mx_persistent_kernel_m128_memory.md")}
 KERNEL_SOURCES = ("mx_kernels.cu", "mx_internal.h", "sm103.cuh")
 
 
@@ -538,6 +538,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="distinct weight layers of the workload (0: its own count); profiling runs use fewer")
     ap.add_argument("--unfused", action="store_true", help="time the three-launch path as the main loop")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="print only the M=4096 GEMM section (a short run for profiling the prefill kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -549,6 +551,14 @@ def main():
         out = run_reference(args, rank, world)
         if out is not None:
             print(json.dumps(out), flush=True)
+        return
+    if args.prefill_only:
+        import torch
+
+        import mxfp8_swiglu_mlp_gb300 as fs
+
+        torch.cuda.set_device(local_rank)
+        print(json.dumps({"prefill_gemm": prefill_gemm(fs, torch.cuda.Stream())}), flush=True)
         return
     if world > 1:
         import torch
