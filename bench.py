@@ -445,6 +445,28 @@ def prefill_gemm(fs, stream):
         res[name] = entry
         del a, w, bc, bs, ac, asc, ws, c
         torch.cuda.empty_cache()
+    # the whole MLP of the m16 layer at 4096 tokens: x quantisation, the gate/up
+    # GEMM with the SwiGLU + requantisation epilogue, the down GEMM; and the
+    # three-launch ablation (gate/up to fp32 in HBM, SwiGLU-quantise, down)
+    M, H, I = 4096, 2560, 9728
+    x = torch.randn(M, H, device="cuda", generator=g).to(torch.bfloat16)
+    wg, wu = [(torch.randn(I, H, device="cuda", generator=g) / H ** 0.5).to(torch.bfloat16) for _ in range(2)]
+    wd = (torch.randn(H, I, device="cuda", generator=g) / I ** 0.5).to(torch.bfloat16)
+    mw = fs.prepare_mlp_weights(wg, wu, wd)
+    del wg, wu, wd
+    mws = fs.Workspace(M, H, I)
+    y = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+    s = stream.cuda_stream
+    t_f = timeit(lambda: fs.fsops_mxfp8_swiglu_mlp(x, mw.gateup_codes, mw.down_codes, mw.scales, y, M, H, I, stream=s))
+    t_u = timeit(lambda: fs.fsops_mxfp8_swiglu_mlp_unfused(x, mw.gateup_codes, mw.down_codes, mw.scales, y, M, H, I,
+                                                           stream=s))
+    fl = 2.0 * M * 3 * H * I
+    res["mlp_m4096"] = {"M": M, "H": H, "I": I, "launches": 3,
+                        "us": round(t_f * 1e6, 2), "tokens_per_s": round(M / t_f, 1),
+                        "tflops": round(fl / t_f / 1e12, 1), "frac_fp8_tensor": round(fl / t_f / 1e12 / peak, 4),
+                        "unfused_us": round(t_u * 1e6, 2)}
+    del x, mw, mws, y
+    torch.cuda.empty_cache()
     return res
 
 

@@ -16,6 +16,7 @@
 
 #include "../../include/fsops.h"
 #include "mx_internal.h"
+#include "mx_tiled.h"
 
 using namespace fsops;
 
@@ -140,12 +141,14 @@ MlpLayout mlp_layout(int M, int H, int I) {
   l.ctl = 0;
   l.xq = kCtlRegionBytes;
   l.xq_sf = l.xq + round_up(static_cast<size_t>(M) * H, 1024);
-  l.hq = l.xq_sf + round_up(static_cast<size_t>(H / 128) * 512, 1024);
+  const size_t row_tiles = static_cast<size_t>((M + 127) / 128);
+  l.hq = l.xq_sf + round_up(row_tiles * (H / 128) * 512, 1024);
   l.hq_sf = l.hq + round_up(static_cast<size_t>(M) * I, 1024);
-  l.part0 = l.hq_sf + round_up(static_cast<size_t>(I / 128) * 512, 1024);
-  // split-K accumulators for the smallest tiles (128 rows) either phase may use
-  l.part1 = l.part0 + accum_bytes(M, 2 * I / 128);
-  l.gu = l.part1 + accum_bytes(M, H / 128);
+  l.part0 = l.hq_sf + round_up(row_tiles * (I / 128) * 512, 1024);
+  // split-K accumulators for the smallest tiles (128 rows) either phase may
+  // use; above 128 rows every block owns whole tiles and there are none
+  l.part1 = l.part0 + (M <= 128 ? accum_bytes(M, 2 * I / 128) : 0);
+  l.gu = l.part1 + (M <= 128 ? accum_bytes(M, H / 128) : 0);
   l.total = l.gu + round_up(static_cast<size_t>(M) * 2 * I * 4, 1024);
   return l;
 }
@@ -358,45 +361,82 @@ bool gemm_shape_ok(int M, int N, int K) {
          K <= 65536;
 }
 
+// The operand half of the tiled GEMM's arguments: A codes and scales
+// (pre-quantised), B codes and scales, the shape and the status word.
+fsops_status fill_tiled(TiledArgs& ta, const uint8_t* codes, const uint8_t* sfa, const uint8_t* b_codes,
+                        const uint8_t* b_scales, int M, int N, int K, uint8_t* ctl, const DeviceInfo* di) {
+  std::memset(&ta, 0, sizeof(ta));
+  // 2-block clusters on vertically adjacent tiles (each loads half of B and
+  // multicasts it) whenever there are two row tiles
+  const int MT = (M + 127) / 128;
+  ta.cluster_ok = (MT >= 2 && di->sms >= 2 && env_int("FSOPS_GEMM_PAIRS", 1, 0, 1)) ? 1 : 0;
+  if (!encode_map(&ta.tm_a, codes, K, M, 128) || !encode_map(&ta.tm_b, b_codes, K, N, ta.cluster_ok ? 128 : 256))
+    return FSOPS_ERR_INVALID_ARG;
+  ta.sf_a = sfa;
+  ta.sf_b = b_scales;
+  ta.M = M;
+  ta.N = N;
+  ta.K = K;
+  ta.KS = K / kTileK;
+  ta.MT = MT;
+  ta.NT = (N + 255) / 256;
+  ta.status = reinterpret_cast<uint32_t*>(ctl) + kCtlStatus;
+  ta.timeout_ns = g_timeout_ns.load();
+  return FSOPS_OK;
+}
+
+fsops_status quantize_a(const void* a, int M, int K, uint8_t* xq, uint8_t* xq_sf, cudaStream_t stream) {
+  if (launch_quantize(static_cast<const uint16_t*>(a), M, K, K, xq, xq_sf, 1, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FSOPS_ERR_CUDA;
+  }
+  return FSOPS_OK;
+}
+
+fsops_status run_tiled(const TiledArgs& ta, const DeviceInfo* di, cudaStream_t stream) {
+  if (launch_gemm_tiled(ta, di->sms, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FSOPS_ERR_CUDA;
+  }
+  return FSOPS_OK;
+}
+
 // M > 128: A quantised by its own launch when it is bf16, then the tiled GEMM.
 fsops_status gemm_tiled_impl(const void* a, const uint8_t* a_scales, bool a_bf16, const uint8_t* b_codes,
                              const uint8_t* b_scales, void* c, bool c_f32, int M, int N, int K, uint8_t* ctl,
                              uint8_t* xq, uint8_t* xq_sf, const DeviceInfo* di, cudaStream_t stream) {
   const uint8_t* codes = a_bf16 ? xq : static_cast<const uint8_t*>(a);
   const uint8_t* sfa = a_bf16 ? xq_sf : a_scales;
-  if (a_bf16) {
-    cudaError_t e = launch_quantize(static_cast<const uint16_t*>(a), M, K, K, xq, xq_sf, 1, stream);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return FSOPS_ERR_CUDA;
-    }
-  }
   TiledArgs ta;
-  std::memset(&ta, 0, sizeof(ta));
-  // 2-block clusters on vertically adjacent tiles (each loads half of B and
-  // multicasts it) whenever there are two row tiles
-  const int MT = (M + 127) / 128;
-  ta.cluster_ok = (MT >= 2 && di->sms >= 2 && env_int("FSOPS_GEMM_PAIRS", 1, 0, 1)) ? 1 : 0;
-  if (!encode_map(&ta.tm_a, codes, K, M, 128) || !encode_map(&ta.tm_b, b_codes, K, N, ta.cluster_ok ? 128 : 256) ||
-      !encode_out_map(&ta.tm_c, c, M, N, c_f32))
-    return FSOPS_ERR_INVALID_ARG;
-  ta.sf_a = sfa;
-  ta.sf_b = b_scales;
+  fsops_status st = fill_tiled(ta, codes, sfa, b_codes, b_scales, M, N, K, ctl, di);
+  if (st != FSOPS_OK) return st;
+  if (!encode_out_map(&ta.tm_c, c, M, N, c_f32)) return FSOPS_ERR_INVALID_ARG;
   ta.c = c;
   ta.c_f32 = c_f32 ? 1 : 0;
-  ta.M = M;
-  ta.N = N;
-  ta.K = K;
-  ta.KS = K / kTileK;
-  ta.MT = (M + 127) / 128;
-  ta.NT = (N + 255) / 256;
-  ta.status = reinterpret_cast<uint32_t*>(ctl) + kCtlStatus;
-  ta.timeout_ns = g_timeout_ns.load();
-  if (launch_gemm_tiled(ta, di->sms, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return FSOPS_ERR_CUDA;
-  }
-  return FSOPS_OK;
+  if (a_bf16 && (st = quantize_a(a, M, K, xq, xq_sf, stream)) != FSOPS_OK) return st;
+  return run_tiled(ta, di, stream);
+}
+
+// The MLP above 128 token rows, in three launches: x quantised to MXFP8; the
+// gate/up GEMM with the SwiGLU epilogue, which writes h requantised to MXFP8;
+// the down GEMM on h.
+fsops_status mlp_tiled_impl(const void* x_bf16, const uint8_t* w_gateup, const uint8_t* w_down,
+                            const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I, uint8_t* ws,
+                            const MlpLayout& l, const DeviceInfo* di, cudaStream_t stream) {
+  TiledArgs gu;
+  fsops_status st = fill_tiled(gu, ws + l.xq, ws + l.xq_sf, w_gateup, scales->gateup, M, 2 * I, H, ws + l.ctl, di);
+  if (st != FSOPS_OK) return st;
+  gu.swiglu = 1;
+  gu.h_codes = ws + l.hq;
+  gu.h_sf = ws + l.hq_sf;
+  TiledArgs dn;
+  st = fill_tiled(dn, ws + l.hq, ws + l.hq_sf, w_down, scales->down, M, H, I, ws + l.ctl, di);
+  if (st != FSOPS_OK) return st;
+  if (!encode_out_map(&dn.tm_c, y_bf16, M, H, false)) return FSOPS_ERR_INVALID_ARG;
+  dn.c = y_bf16;
+  if ((st = quantize_a(x_bf16, M, H, ws + l.xq, ws + l.xq_sf, stream)) != FSOPS_OK) return st;
+  if ((st = run_tiled(gu, di, stream)) != FSOPS_OK) return st;
+  return run_tiled(dn, di, stream);
 }
 
 // Plain GEMM (one phase) with the operand pointers already validated.
@@ -455,7 +495,8 @@ fsops_status mlp_validate(const void* x, const uint8_t* wgu, const uint8_t* wd, 
   if (x == nullptr || wgu == nullptr || wd == nullptr || sc == nullptr || sc->gateup == nullptr ||
       sc->down == nullptr || y == nullptr)
     return FSOPS_ERR_INVALID_ARG;
-  if (M < 1 || M > 128 || H < 128 || I < 128 || H % 128 != 0 || I % 128 != 0 || H > 65536 || I > 65536)
+  if (M < 1 || M > kMaxGemmRows || H < 128 || I < 128 || H % 128 != 0 || I % 128 != 0 || H > 65536 ||
+      I > 65536)
     return FSOPS_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x) || !aligned16(wgu) || !aligned16(wd) || !aligned16(sc->gateup) || !aligned16(sc->down) ||
       !aligned16(y))
@@ -567,7 +608,7 @@ fsops_status fsops_swiglu_quantize_mxfp8(const float* gu, int M, int I, uint8_t*
 }
 
 size_t fsops_mlp_workspace_bytes(int M, int H, int I) {
-  if (M < 1 || M > 128 || H < 128 || I < 128 || H % 128 != 0 || I % 128 != 0 || H > 65536 || I > 65536) return 0;
+  if (M < 1 || M > kMaxGemmRows || H < 128 || I < 128 || H % 128 != 0 || I % 128 != 0 || H > 65536 || I > 65536) return 0;
   int dev;
   const DeviceInfo* di;
   if (current_device(&dev, &di) != FSOPS_OK) return 0;
@@ -607,6 +648,9 @@ fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup,
   uint8_t* ws;
   st = check_ws(dev, l.total, &ws);
   if (st != FSOPS_OK) return st;
+  if (M > 128)
+    return mlp_tiled_impl(x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I, ws, l, di,
+                          static_cast<cudaStream_t>(stream));
 
   const MlpPlan pl = plan_mlp(M, H, I, grid);
   const MlpBuffers bufs{ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.hq, ws + l.hq_sf, ws + l.part0, ws + l.part1};
@@ -736,6 +780,7 @@ fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w
   const DeviceInfo* di;
   st = current_device(&dev, &di);
   if (st != FSOPS_OK) return st;
+  if (M > 128) return FSOPS_ERR_UNSUPPORTED_SHAPE;  // the fixed buffer serves the single-launch path only
   const int grid = di->sms;
   const MlpPlan pl = plan_mlp(M, H, I, grid);
   if (ctl_words_needed(I / 128, pl.T0, pl.T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;

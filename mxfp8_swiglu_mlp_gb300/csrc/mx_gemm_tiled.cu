@@ -23,6 +23,8 @@
 #include <cuda_bf16.h>
 
 #include "mx_internal.h"
+#include "mx_mxfp8.cuh"
+#include "mx_tiled.h"
 #include "sm103.cuh"
 
 namespace fsops {
@@ -77,6 +79,54 @@ __device__ __forceinline__ void tdrain(uint64_t* bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > 200000000ull) return;
 }
 
+// SwiGLU epilogue of one 128-column chunk of a gate/up tile, read by the
+// warp of TMEM lane quarter q4 (token rows mt * 128 + 32 q4 + lane).  The
+// chunk's columns 0..63 hold the gate sums of features f0 .. f0 + 63 (f0 =
+// 128 nt + 64 half), columns 64..127 the up sums of the same features.  Each
+// thread owns one token row, so the amax of a 32-block is its own: h =
+// SiLU(g) * u, then the block's UE8M0 scale and E4M3 codes (the rule of the
+// standalone quantiser).  Rows past M write their scales only (their sums are
+// 0: TMA zero-fills A past M, so the scale byte is 0).
+__device__ __forceinline__ void swiglu_chunk(const TiledArgs& a, uint32_t tcol, int mt, int nt, int q4, int half,
+                                             int lane) {
+  const int I = a.N >> 1;
+  const int r = mt * 128 + q4 * 32 + lane;
+  const int f0 = nt * 128 + half * 64;
+  uint32_t sbytes = 0;
+#pragma unroll 1
+  for (int b = 0; b < 2; ++b) {
+    uint32_t g[2][16], u[2][16];
+    const uint32_t col = tcol + b * 32;
+    tmem_ld16(col, g[0]);
+    tmem_ld16(col + 16, g[1]);
+    tmem_ld16(col + kPairRows, u[0]);
+    tmem_ld16(col + kPairRows + 16, u[1]);
+    tmem_ld_wait();
+    float h[32];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      h[i] = silu_mul(__uint_as_float(g[i >> 4][i & 15]), __uint_as_float(u[i >> 4][i & 15]));
+      amax = fmaxf(amax, fabsf(h[i]));
+    }
+    const uint32_t sc = ue8m0_from_amax(amax);
+    const float inv = inv_scale_from_ue8m0(sc);
+    sbytes |= sc << (8 * b);
+    if (r < a.M) {
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        pk[i] = e4m3_code(h[4 * i] * inv) | (e4m3_code(h[4 * i + 1] * inv) << 8) |
+                (e4m3_code(h[4 * i + 2] * inv) << 16) | (e4m3_code(h[4 * i + 3] * inv) << 24);
+      uint4* d = reinterpret_cast<uint4*>(a.h_codes + static_cast<size_t>(r) * I + f0 + b * 32);
+      d[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      d[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    }
+  }
+  // the scales of 32-blocks f0 / 32 and f0 / 32 + 1 sit in adjacent bytes
+  *reinterpret_cast<uint16_t*>(a.h_sf + tiled_sf_offset(r, f0 >> 5, I >> 7)) = static_cast<uint16_t>(sbytes);
+}
+
 }  // namespace
 
 template <int CL>
@@ -112,7 +162,7 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&a.tm_a);
     tma_prefetch_desc(&a.tm_b);
-    tma_prefetch_desc(&a.tm_c);
+    if (!a.swiglu) tma_prefetch_desc(&a.tm_c);
   }
   tc_fence_before();
   __syncthreads();
@@ -220,6 +270,12 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
       if (!twait(w, acc_full, acc_round & 1u, kSiteAccFull)) break;
       ++acc_round;
       tc_fence_after();
+      if (a.swiglu) {
+        if (ncols > half * 128) swiglu_chunk(a, tlane + half * 128, mt, nt, q4, half, lane);
+        tc_fence_before();
+        mbar_arrive(acc_empty);
+        continue;
+      }
       const int cbeg = half * (ncols >> 1), cend = cbeg + (ncols >> 1);
 #pragma unroll 1
       for (int c0 = cbeg; c0 < cend; c0 += cw) {

@@ -121,25 +121,6 @@ __host__ __device__ inline uint32_t xring_bytes_for(int npad) { return kMaxXSlot
 constexpr uint32_t kAccCols = 256;
 constexpr uint32_t kSfColsPerStage = 12;
 
-// Block-scaled GEMM for M > 128 (mx_gemm_tiled.cu): whole 128 x 256 output
-// tiles per block, no split-K.
-struct TiledArgs {
-  CUtensorMap tm_a;       // A codes [M, K] u8, box 128 rows x 128, 128B swizzle
-  CUtensorMap tm_b;       // B codes [N, K] u8, box 256 rows x 128 (128 rows with cluster_ok), 128B swizzle
-  CUtensorMap tm_c;       // C [M, N] bf16 (box 32 rows x 32) or fp32 (box 32 rows x 16), no swizzle
-  const uint8_t* sf_a;    // A scales, tiled layout, ceil(M / 128) row tiles
-  const uint8_t* sf_b;    // B scales, tiled layout, N / 128 row tiles
-  void* c;                // [M, N] bf16 or fp32
-  int c_f32;
-  int M, N, K, KS;        // KS = K / 128
-  int MT, NT;             // ceil(M / 128), ceil(N / 256)
-  uint32_t* status;       // first error (status << 24 | site << 16 | block)
-  uint64_t timeout_ns;
-  int cluster_ok;         // 1: run as 2-block clusters, each loading half of B and multicasting it
-};
-// Launches at most one block per SM (`sms`).
-cudaError_t launch_gemm_tiled(const TiledArgs& a, int sms, cudaStream_t stream);
-
 // Launch wrappers (mx_kernels.cu).
 cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStream_t stream);
 // Whether `grid` blocks of the kernel with `smem` bytes of shared memory run

@@ -21,29 +21,15 @@
 #include <cuda_fp8.h>
 
 #include "mx_internal.h"
+#include "mx_mxfp8.cuh"
 #include "sm103.cuh"
 
 namespace fsops {
 using namespace dev;
 
 // ======================================================================
-// MXFP8 helpers (fp32 in, codes out)
+// bf16 blocks to MXFP8 codes
 // ======================================================================
-__device__ __forceinline__ uint32_t ue8m0_from_amax(float amax) {
-  const int be = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-  return static_cast<uint32_t>(be > 8 ? be - 8 : 0);
-}
-// 2^-e for scale byte s = e + 127 (s <= 246 for finite fp32 inputs).
-__device__ __forceinline__ float inv_scale_from_ue8m0(uint32_t s) {
-  return __uint_as_float((254u - s) << 23);
-}
-__device__ __forceinline__ uint32_t e4m3_code(float v) {
-  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
-__device__ __forceinline__ uint32_t tiled_sf_offset(int r, int kb, int n_kg) {
-  return static_cast<uint32_t>(((r >> 7) * n_kg + (kb >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 +
-                               (kb & 3));
-}
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -124,13 +110,8 @@ cudaError_t launch_quantize(const uint16_t* x, int rows, int K, int ld, uint8_t*
 // ======================================================================
 // SwiGLU + requantisation (the middle launch of the unfused path).
 // ======================================================================
-// SiLU(g) * u = g * sigmoid(g) * u; for g -> -inf the reciprocal of inf is 0.
-// SiLU(g) * u in fp32.  The fast divide (reciprocal approximation, 2 ulp)
-// keeps this off the epilogue's critical path; its error is far below the
-// E4M3 step the result is rounded to next.  For g below about -88, 1 + e^-g
-// overflows to +inf and the quotient is 0, the limit of SiLU.
-__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
-
+// SiLU(g) * u = g * sigmoid(g) * u (silu_mul); for g -> -inf the reciprocal
+// of inf is 0.
 __global__ void swiglu_quantize_kernel(const float* __restrict__ gu, int M, int npad, int I,
                                        uint8_t* __restrict__ hc, uint8_t* __restrict__ hs) {
   const int nb = I / 32;

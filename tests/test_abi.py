@@ -60,7 +60,7 @@ def test_mlp_validation(fs):
     assert call(x=None) == fs.ERR_INVALID_ARG
     assert call(y=None) == fs.ERR_INVALID_ARG
     assert call(s=None) == fs.ERR_INVALID_ARG
-    for M in (0, 129, -1):
+    for M in (0, 16385, -1):
         assert call(M=M) == fs.ERR_UNSUPPORTED_SHAPE
     for H, I in ((200, 256), (256, 100), (0, 256), (128 * 513, 256)):
         assert call(H=H, I=I) == fs.ERR_UNSUPPORTED_SHAPE
@@ -112,5 +112,6 @@ def test_quantize_validation(fs):
 
 def test_size_queries_reject_bad_shapes(fs):
     assert fs.fsops_mlp_workspace_bytes(0, 256, 256) == 0
+    assert fs.fsops_mlp_workspace_bytes(16385, 256, 256) == 0
     assert fs.fsops_gemm_workspace_bytes(4, 100, 256) == 0
     assert fs.lib.fsops_set_wait_timeout_ns(0) == fs.ERR_INVALID_ARG
