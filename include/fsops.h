@@ -135,16 +135,22 @@ size_t fsops_gemm_workspace_bytes(int M, int N, int K);
  *           128j..128j+63 are gate features 64j..64j+63, columns
  *           128j+64..128j+127 the up features 64j..64j+63 (this is what
  *           fsops_mxfp8_gemm_ex writes for A = x and B = W_gateup).
- *   h_codes [M, I] E4M3;  h_scales TCGEN05 layout, I/128 tiles of 512 bytes.
- *   1 <= M <= 128, I % 128 == 0.
+ *   h_codes [M, I] E4M3;  h_scales TCGEN05 layout, ceil(M/128) x I/128 tiles
+ *   of 512 bytes (scales of rows past M within the last row tile may be left
+ *   unwritten; the GEMMs ignore those rows).
+ *   1 <= M <= 16384, I % 128 == 0.
  */
 fsops_status fsops_swiglu_quantize_mxfp8(const float* gu, int M, int I, uint8_t* h_codes,
                                          uint8_t* h_scales, void* stream);
 
 /* ------------------------------------------------------------------------
- * fsops_mxfp8_swiglu_mlp -- the whole block in ONE launch:
+ * fsops_mxfp8_swiglu_mlp -- the whole block:
  *   x^ = MXFP8(x);  g = x^ Wg^T, u = x^ Wu^T (fp32 accumulate);
  *   h = SiLU(g) * u (fp32);  h^ = MXFP8(h) along I;  y = bf16(h^ Wd^T).
+ *   M <= 128 (decode): ONE launch; h never leaves the chip except as split
+ *   sums in L2.  M > 128 (prefill): three launches -- x quantised; the gate/up
+ *   GEMM over whole 128 x 256 tiles whose epilogue forms h and requantises it
+ *   (h^ goes to the workspace, M * I bytes plus scales); the down GEMM on h^.
  *   x_bf16   [M, H] bf16.
  *   w_gateup [2I, H] E4M3, W_gate and W_up paired in blocks of 64 rows:
  *            rows 128j..128j+63 are W_gate rows 64j..64j+63 and rows
@@ -154,7 +160,7 @@ fsops_status fsops_swiglu_quantize_mxfp8(const float* gu, int M, int I, uint8_t*
  *   w_down   [H, I] E4M3.
  *   scales   TCGEN05 scales of both.
  *   y_bf16   [M, H] bf16.
- *   1 <= M <= 128; H % 128 == 0; I % 128 == 0; H, I <= 65536.
+ *   1 <= M <= 16384; H % 128 == 0; I % 128 == 0; H, I <= 65536.
  * Uses the workspace registered with fsops_set_workspace for the current
  * device (INVALID_ARG if none or too small).  Calls on one device are ordered
  * by the caller (one stream, or events); concurrent calls would share the
@@ -178,8 +184,9 @@ fsops_status fsops_mxfp8_swiglu_mlp_unfused(const void* x_bf16, const uint8_t* w
  * allocator (cudaMalloc may synchronise the device), or deployments with a
  * fixed memory budget.  It has no counterpart in the paper; it is a packaging
  * of fsops_mxfp8_swiglu_mlp.
- *   Arguments, layouts and limits as fsops_mxfp8_swiglu_mlp, except that no
- *   workspace is used: the scratch is one fixed 8 MiB buffer per device inside
+ *   Arguments, layouts and limits as fsops_mxfp8_swiglu_mlp, with M <= 128
+ *   only (the single-launch path; larger M is FSOPS_ERR_UNSUPPORTED_SHAPE),
+ *   and no workspace is used: the scratch is one fixed 8 MiB buffer per device inside
  *   the library's device image, present from library load until process exit.
  *   A shape whose scratch does not fit in 8 MiB is rejected with
  *   FSOPS_ERR_UNSUPPORTED_SHAPE before anything is launched (with one gate/up
@@ -196,7 +203,8 @@ fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w
                                             void* y_bf16, int M, int H, int I, void* stream);
 
 /* Workspace bytes the MLP entry points need on the current device (0 if the
- * shape is unsupported). */
+ * shape is unsupported).  It covers the unfused path's fp32 [M, 2I]
+ * intermediate too (M * 8I bytes), which dominates for large M. */
 size_t fsops_mlp_workspace_bytes(int M, int H, int I);
 
 /* Register `ws` (device memory of `bytes` bytes, 256-byte aligned) as the MLP

@@ -593,7 +593,7 @@ fsops_status fsops_mxfp8_gemm(const void* a_bf16, const uint8_t* b_codes, const 
 fsops_status fsops_swiglu_quantize_mxfp8(const float* gu, int M, int I, uint8_t* h_codes, uint8_t* h_scales,
                                          void* stream) {
   if (gu == nullptr || h_codes == nullptr || h_scales == nullptr) return FSOPS_ERR_INVALID_ARG;
-  if (M < 1 || M > 128 || I < 128 || I % 128 != 0 || I > 65536) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (M < 1 || M > kMaxGemmRows || I < 128 || I % 128 != 0 || I > 65536) return FSOPS_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(gu) || !aligned16(h_codes)) return FSOPS_ERR_MISALIGNED;
   int dev;
   const DeviceInfo* di;
@@ -608,7 +608,9 @@ fsops_status fsops_swiglu_quantize_mxfp8(const float* gu, int M, int I, uint8_t*
 }
 
 size_t fsops_mlp_workspace_bytes(int M, int H, int I) {
-  if (M < 1 || M > kMaxGemmRows || H < 128 || I < 128 || H % 128 != 0 || I % 128 != 0 || H > 65536 || I > 65536) return 0;
+  if (M < 1 || M > kMaxGemmRows || H < 128 || I < 128 || H % 128 != 0 || I % 128 != 0 || H > 65536 ||
+      I > 65536)
+    return 0;
   int dev;
   const DeviceInfo* di;
   if (current_device(&dev, &di) != FSOPS_OK) return 0;
