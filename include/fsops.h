@@ -236,6 +236,12 @@ fsops_status fsops_debug_set_extra_arrivals(uint32_t n);
 
 const char* fsops_status_string(fsops_status s);
 
+/* The CUDA runtime error (a cudaError_t value) behind the last
+ * FSOPS_ERR_CUDA that a call on this thread returned, 0 if none.  With the
+ * environment variable FSOPS_VERBOSE set, each such failure is also printed
+ * to stderr with the step that failed. */
+int fsops_last_cuda_error(void);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int fsops_version(void);
 

@@ -25,7 +25,7 @@ __all__ = [
     "fsops_gemm_workspace_bytes", "fsops_swiglu_quantize_mxfp8", "fsops_mxfp8_swiglu_mlp",
     "fsops_mxfp8_swiglu_mlp_unfused", "fsops_mxfp8_swiglu_mlp_noalloc", "fsops_mlp_workspace_bytes", "fsops_set_workspace",
     "fsops_read_kernel_status", "fsops_set_wait_timeout_ns", "fsops_debug_set_extra_arrivals",
-    "fsops_status_string", "fsops_version", "quantize_weight", "MLPWeights", "prepare_mlp_weights",
+    "fsops_status_string", "fsops_version", "fsops_last_cuda_error", "quantize_weight", "MLPWeights", "prepare_mlp_weights",
     "Workspace", "pair_gate_up",
 ]
 
@@ -62,6 +62,7 @@ _SIGS = {
     "fsops_debug_set_extra_arrivals": ([_u32], _i),
     "fsops_status_string": ([_i], ctypes.c_char_p),
     "fsops_version": ([], _i),
+    "fsops_last_cuda_error": ([], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -72,7 +73,11 @@ for _name, (_args, _res) in _SIGS.items():
 class FsopsError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__("%s: %s (status %d)" % (where, lib.fsops_status_string(status).decode(), status))
+        self.cuda_error = lib.fsops_last_cuda_error() if status == ERR_CUDA else 0
+        msg = "%s: %s (status %d)" % (where, lib.fsops_status_string(status).decode(), status)
+        if self.cuda_error:
+            msg += ", cudaError %d" % self.cuda_error
+        super().__init__(msg)
 
 
 def _check(status: int, where: str) -> None:
@@ -188,6 +193,10 @@ def fsops_status_string(s: int) -> str:
 
 def fsops_version() -> int:
     return lib.fsops_version()
+
+
+def fsops_last_cuda_error() -> int:
+    return lib.fsops_last_cuda_error()
 
 
 # ---------------------------------------------------------------- tensor helpers

@@ -89,6 +89,17 @@ fsops_status current_device(int* dev_out, const DeviceInfo** info) {
   return FSOPS_OK;
 }
 
+thread_local int g_last_cuda_error = 0;
+// A failed CUDA step: clears the runtime's error state, records the error for
+// fsops_last_cuda_error and, with FSOPS_VERBOSE set, reports it.
+fsops_status cuda_failed(cudaError_t e, const char* where) {
+  cudaGetLastError();
+  g_last_cuda_error = static_cast<int>(e);
+  if (std::getenv("FSOPS_VERBOSE") != nullptr)
+    std::fprintf(stderr, "fsops: %s failed: %s (%d)\n", where, cudaGetErrorString(e), static_cast<int>(e));
+  return FSOPS_ERR_CUDA;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int npad_of(int M) { return (M + 15) / 16 * 16; }
@@ -287,12 +298,8 @@ fsops_status launch(KernelArgs& a, int grid, cudaStream_t stream) {
     pairs = false;
   }
   a.cluster_pairs = pairs ? 1 : 0;
-  cudaError_t e = launch_mx_kernel(a, grid, smem_for(a.npad, a.local_xq), stream);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return FSOPS_ERR_CUDA;
-  }
-  return FSOPS_OK;
+  const cudaError_t e = launch_mx_kernel(a, grid, smem_for(a.npad, a.local_xq), stream);
+  return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "mx_persistent_kernel launch");
 }
 
 // Device buffers of one fused MLP launch (workspace or fixed buffer).
@@ -386,19 +393,13 @@ fsops_status fill_tiled(TiledArgs& ta, const uint8_t* codes, const uint8_t* sfa,
 }
 
 fsops_status quantize_a(const void* a, int M, int K, uint8_t* xq, uint8_t* xq_sf, cudaStream_t stream) {
-  if (launch_quantize(static_cast<const uint16_t*>(a), M, K, K, xq, xq_sf, 1, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return FSOPS_ERR_CUDA;
-  }
-  return FSOPS_OK;
+  const cudaError_t e = launch_quantize(static_cast<const uint16_t*>(a), M, K, K, xq, xq_sf, 1, stream);
+  return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "quantize_kernel launch");
 }
 
 fsops_status run_tiled(const TiledArgs& ta, const DeviceInfo* di, cudaStream_t stream) {
-  if (launch_gemm_tiled(ta, di->sms, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return FSOPS_ERR_CUDA;
-  }
-  return FSOPS_OK;
+  const cudaError_t e = launch_gemm_tiled(ta, di->sms, stream);
+  return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "mx_gemm_tiled_kernel launch");
 }
 
 // M > 128: A quantised by its own launch when it is bf16, then the tiled GEMM.
@@ -510,6 +511,8 @@ extern "C" {
 
 int fsops_version(void) { return 100; }
 
+int fsops_last_cuda_error(void) { return g_last_cuda_error; }
+
 const char* fsops_status_string(fsops_status s) {
   switch (s) {
     case FSOPS_OK: return "ok";
@@ -546,11 +549,7 @@ fsops_status fsops_quantize_mxfp8(const void* x_bf16, int rows, int K, int ld, u
   if (st != FSOPS_OK) return st;
   cudaError_t e = launch_quantize(static_cast<const uint16_t*>(x_bf16), rows, K, ld, codes, scales,
                                   layout == FSOPS_SCALES_TCGEN05 ? 1 : 0, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return FSOPS_ERR_CUDA;
-  }
-  return FSOPS_OK;
+  return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "quantize_kernel launch");
 }
 
 size_t fsops_gemm_workspace_bytes(int M, int N, int K) {
@@ -600,11 +599,7 @@ fsops_status fsops_swiglu_quantize_mxfp8(const float* gu, int M, int I, uint8_t*
   fsops_status st = current_device(&dev, &di);
   if (st != FSOPS_OK) return st;
   cudaError_t e = launch_swiglu_quantize(gu, M, I, h_codes, h_scales, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return FSOPS_ERR_CUDA;
-  }
-  return FSOPS_OK;
+  return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "swiglu_quantize_kernel launch");
 }
 
 size_t fsops_mlp_workspace_bytes(int M, int H, int I) {
@@ -625,10 +620,9 @@ fsops_status fsops_set_workspace(void* ws, size_t bytes) {
   if (ws != nullptr && ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)) return FSOPS_ERR_MISALIGNED;
   if (ws != nullptr && bytes < kCtlRegionBytes) return FSOPS_ERR_INVALID_ARG;
   if (ws != nullptr) {
-    if (cudaMemset(ws, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
-      cudaGetLastError();
-      return FSOPS_ERR_CUDA;
-    }
+    cudaError_t e = cudaMemset(ws, 0, bytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_failed(e, "workspace clear");
   }
   std::lock_guard<std::mutex> lk(g_mu);
   g_ws[dev].ptr = ws;
@@ -683,10 +677,7 @@ fsops_status fsops_mxfp8_swiglu_mlp_unfused(const void* x_bf16, const uint8_t* w
   if (st != FSOPS_OK) return st;
   // launch 2: SiLU(g) * u, requantised to MXFP8, to HBM
   cudaError_t e = launch_swiglu_quantize(gu, M, I, ws + l.hq, ws + l.hq_sf, s);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return FSOPS_ERR_CUDA;
-  }
+  if (e != cudaSuccess) return cuda_failed(e, "swiglu_quantize_kernel launch");
   // launch 3: down GEMM on the requantised intermediate
   return gemm_impl(ws + l.hq, ws + l.hq_sf, false, w_down, scales->down, y_bf16, false, M, H, I, ws + l.ctl,
                    nullptr, nullptr, ws + l.part1, di, s);
@@ -704,12 +695,11 @@ fsops_status fsops_read_kernel_status(void* workspace, uint32_t* word) {
     if (workspace == nullptr) return FSOPS_ERR_INVALID_ARG;
   }
   uint32_t v = 0;
-  if (cudaDeviceSynchronize() != cudaSuccess ||
-      cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
-      cudaMemset(workspace, 0, sizeof(v)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
-    cudaGetLastError();
-    return FSOPS_ERR_CUDA;
-  }
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(workspace, 0, sizeof(v));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_failed(e, "status word read");
   *word = v;
   return FSOPS_OK;
 }
@@ -796,10 +786,8 @@ fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_noalloc_base[dev] == nullptr) {
       void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-        cudaGetLastError();
-        return FSOPS_ERR_CUDA;
-      }
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || p == nullptr) return cuda_failed(e, "scratch buffer address");
       g_noalloc_base[dev] = static_cast<uint8_t*>(p);
     }
     ws = g_noalloc_base[dev];
@@ -807,11 +795,9 @@ fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the buffer keeps whatever the previous call left: clear the counters, flags
   // and split-K accumulators the kernel needs to start at zero
-  if (cudaMemsetAsync(ws + l.ctl, 0, kCtlRegionBytes, s) != cudaSuccess ||
-      cudaMemsetAsync(ws + l.part0, 0, l.end - l.part0, s) != cudaSuccess) {
-    cudaGetLastError();
-    return FSOPS_ERR_CUDA;
-  }
+  cudaError_t e = cudaMemsetAsync(ws + l.ctl, 0, kCtlRegionBytes, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws + l.part0, 0, l.end - l.part0, s);
+  if (e != cudaSuccess) return cuda_failed(e, "scratch buffer clear");
 
   const MlpBuffers bufs{ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.hq, ws + l.hq_sf, ws + l.part0, ws + l.part1};
   KernelArgs ka;

@@ -22,6 +22,8 @@
 // "Estrategia de cuantizacion FP8").
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "mx_internal.h"
 #include "mx_mxfp8.cuh"
 #include "mx_tiled.h"
@@ -79,34 +81,34 @@ __device__ __forceinline__ void tdrain(uint64_t* bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > 200000000ull) return;
 }
 
-// SwiGLU epilogue of one 128-column chunk of a gate/up tile, read by the
-// warp of TMEM lane quarter q4 (token rows mt * 128 + 32 q4 + lane).  The
-// chunk's columns 0..63 hold the gate sums of features f0 .. f0 + 63 (f0 =
-// 128 nt + 64 half), columns 64..127 the up sums of the same features.  Each
-// thread owns one token row, so the amax of a 32-block is its own: h =
-// SiLU(g) * u, then the block's UE8M0 scale and E4M3 codes (the rule of the
-// standalone quantiser).  Rows past M write their scales only (their sums are
-// 0: TMA zero-fills A past M, so the scale byte is 0).
-__device__ __forceinline__ void swiglu_chunk(const TiledArgs& a, uint32_t tcol, int mt, int nt, int q4, int half,
-                                             int lane) {
+// SwiGLU epilogue of one 128-column chunk of a gate/up tile, for the warp of
+// TMEM lane quarter q4 (token rows mt * 128 + 32 q4 + lane).  The chunk's
+// columns 0..63 hold the gate sums of features f0 .. f0 + 63 (f0 = 128 nt +
+// 64 half), columns 64..127 the up sums of the same features.
+// swiglu_load reads the chunk's raw sums into registers, so the accumulator
+// can be released before any arithmetic; swiglu_store then forms h = SiLU(g)
+// * u and quantises each 32-block with the rule of the standalone quantiser.
+// Each thread owns one token row, so a block's amax is its own.
+__device__ __forceinline__ void swiglu_load(uint32_t tcol, uint32_t (&g)[4][16], uint32_t (&u)[4][16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) tmem_ld16(tcol + 16 * j, g[j]);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) tmem_ld16(tcol + kPairRows + 16 * j, u[j]);
+  tmem_ld_wait();
+}
+// Rows past M write their scales only (their sums are 0: TMA zero-fills A
+// past M, so the scale byte is 0).
+__device__ __forceinline__ void swiglu_store(const TiledArgs& a, int r, int f0, const uint32_t (&g)[4][16],
+                                             const uint32_t (&u)[4][16]) {
   const int I = a.N >> 1;
-  const int r = mt * 128 + q4 * 32 + lane;
-  const int f0 = nt * 128 + half * 64;
   uint32_t sbytes = 0;
-#pragma unroll 1
+#pragma unroll
   for (int b = 0; b < 2; ++b) {
-    uint32_t g[2][16], u[2][16];
-    const uint32_t col = tcol + b * 32;
-    tmem_ld16(col, g[0]);
-    tmem_ld16(col + 16, g[1]);
-    tmem_ld16(col + kPairRows, u[0]);
-    tmem_ld16(col + kPairRows + 16, u[1]);
-    tmem_ld_wait();
     float h[32];
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      h[i] = silu_mul(__uint_as_float(g[i >> 4][i & 15]), __uint_as_float(u[i >> 4][i & 15]));
+      h[i] = silu_mul(__uint_as_float(g[2 * b + (i >> 4)][i & 15]), __uint_as_float(u[2 * b + (i >> 4)][i & 15]));
       amax = fmaxf(amax, fabsf(h[i]));
     }
     const uint32_t sc = ue8m0_from_amax(amax);
@@ -118,7 +120,7 @@ __device__ __forceinline__ void swiglu_chunk(const TiledArgs& a, uint32_t tcol, 
       for (int i = 0; i < 8; ++i)
         pk[i] = e4m3_code(h[4 * i] * inv) | (e4m3_code(h[4 * i + 1] * inv) << 8) |
                 (e4m3_code(h[4 * i + 2] * inv) << 16) | (e4m3_code(h[4 * i + 3] * inv) << 24);
-      uint4* d = reinterpret_cast<uint4*>(a.h_codes + static_cast<size_t>(r) * I + f0 + b * 32);
+      uint4* d = reinterpret_cast<uint4*>(a.h_codes + static_cast<size_t>(r) * I + f0 + 32 * b);
       d[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       d[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
     }
@@ -126,10 +128,14 @@ __device__ __forceinline__ void swiglu_chunk(const TiledArgs& a, uint32_t tcol, 
   // the scales of 32-blocks f0 / 32 and f0 / 32 + 1 sit in adjacent bytes
   *reinterpret_cast<uint16_t*>(a.h_sf + tiled_sf_offset(r, f0 >> 5, I >> 7)) = static_cast<uint16_t>(sbytes);
 }
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+  const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<const uint32_t*>(&b2);
+}
 
 }  // namespace
 
-template <int CL>
+template <int CL, bool SWIGLU>
 __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __grid_constant__ TiledArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -162,7 +168,7 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&a.tm_a);
     tma_prefetch_desc(&a.tm_b);
-    if (!a.swiglu) tma_prefetch_desc(&a.tm_c);
+    if (!SWIGLU) tma_prefetch_desc(&a.tm_c);
   }
   tc_fence_before();
   __syncthreads();
@@ -270,13 +276,53 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
       if (!twait(w, acc_full, acc_round & 1u, kSiteAccFull)) break;
       ++acc_round;
       tc_fence_after();
-      if (a.swiglu) {
-        if (ncols > half * 128) swiglu_chunk(a, tlane + half * 128, mt, nt, q4, half, lane);
+      if (SWIGLU) {
+        const bool has = ncols > half * 128;
+        uint32_t g[4][16], u[4][16];
+        if (has) swiglu_load(tlane + half * 128, g, u);
         tc_fence_before();
         mbar_arrive(acc_empty);
+        if (has) swiglu_store(a, mt * 128 + q4 * 32 + lane, nt * 128 + half * 64, g, u);
         continue;
       }
       const int cbeg = half * (ncols >> 1), cend = cbeg + (ncols >> 1);
+      if (!a.c_f32) {
+        // bf16 C: the warp's columns are read and packed in registers first,
+        // so the accumulator is free again before any store work starts
+        const int nch = (cend - cbeg) >> 5;  // 32-column chunks: 4, or 2 on a 128-column tile
+        uint32_t pk[4][16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (j < nch) {
+            uint32_t v[2][16];
+            tmem_ld16(tlane + cbeg + 32 * j, v[0]);
+            tmem_ld16(tlane + cbeg + 32 * j + 16, v[1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[j][i] = pack_bf16x2(v[i >> 3][(2 * i) & 15], v[i >> 3][(2 * i + 1) & 15]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(acc_empty);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (j < nch) {
+            // the store issued from this buffer before has read it
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            uint4* rowp = reinterpret_cast<uint4*>(buf + lane * 64);  // 32 rows x 64 B
+#pragma unroll
+            for (int q = 0; q < 4; ++q) rowp[q] = make_uint4(pk[j][4 * q], pk[j][4 * q + 1], pk[j][4 * q + 2], pk[j][4 * q + 3]);
+            fence_proxy_async_shared();  // the TMA store reads what the warp wrote
+            __syncwarp();
+            if (lane == 0 && mt * 128 + q4 * 32 < a.M) {
+              tma_store_2d(&a.tm_c, buf, nt * 256 + cbeg + 32 * j, mt * 128 + q4 * 32);
+              bulk_commit_group();
+            }
+          }
+        }
+        continue;
+      }
 #pragma unroll 1
       for (int c0 = cbeg; c0 < cend; c0 += cw) {
         uint32_t v[2][16];
@@ -329,36 +375,61 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t launch_gemm_tiled(const TiledArgs& a, int sms, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mx_gemm_tiled_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kTSmem));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mx_gemm_tiled_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kTSmem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  // pairs of blocks on vertically adjacent tiles when there are at least two
-  // row tiles; grid = one block per SM at most
-  const bool pairs = a.cluster_ok != 0;  // the host chose it and encoded tm_b with 128-row boxes
-  const int cl = pairs ? 2 : 1;
-  const int items = ((a.MT + cl - 1) / cl) * a.NT;
-  const int clusters = items < sms / cl ? items : sms / cl;
+namespace {
+// Per device: the four kernel instances' dynamic shared-memory limits have
+// been raised.  Internal linkage (not a static inside a template, which the
+// toolchain would merge across every loaded copy of the library), so each
+// copy sets the limits of its own kernels.
+constexpr int kMaxAttrDevices = 64;
+std::atomic<bool> g_smem_attr_set[kMaxAttrDevices];
+
+cudaError_t set_smem_limits() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxAttrDevices) return cudaErrorInvalidDevice;
+  if (g_smem_attr_set[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const int smem = static_cast<int>(kTSmem);
+  e = cudaFuncSetAttribute(mx_gemm_tiled_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(mx_gemm_tiled_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(mx_gemm_tiled_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(mx_gemm_tiled_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) g_smem_attr_set[dev].store(true, std::memory_order_release);
+  return e;
+}
+
+template <int CL, bool SWIGLU>
+cudaError_t launch_tiled(const TiledArgs& a, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(clusters * cl);
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTThreads);
   cfg.dynamicSmemBytes = kTSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pairs ? 1 : 0;
-  return pairs ? cudaLaunchKernelEx(&cfg, mx_gemm_tiled_kernel<2>, a) : cudaLaunchKernelEx(&cfg, mx_gemm_tiled_kernel<1>, a);
+  cfg.numAttrs = CL > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, mx_gemm_tiled_kernel<CL, SWIGLU>, a);
+}
+}  // namespace
+
+cudaError_t launch_gemm_tiled(const TiledArgs& a, int sms, cudaStream_t stream) {
+  // pairs of blocks on vertically adjacent tiles when there are at least two
+  // row tiles; grid = one block per SM at most
+  const bool pairs = a.cluster_ok != 0;  // the host chose it and encoded tm_b with 128-row boxes
+  const int cl = pairs ? 2 : 1;
+  const int items = ((a.MT + cl - 1) / cl) * a.NT;
+  const int grid = (items < sms / cl ? items : sms / cl) * cl;
+  const cudaError_t e = set_smem_limits();
+  if (e != cudaSuccess) return e;
+  if (a.swiglu) return pairs ? launch_tiled<2, true>(a, grid, stream) : launch_tiled<1, true>(a, grid, stream);
+  return pairs ? launch_tiled<2, false>(a, grid, stream) : launch_tiled<1, false>(a, grid, stream);
 }
 
 }  // namespace fsops

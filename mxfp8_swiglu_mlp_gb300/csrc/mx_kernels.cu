@@ -18,6 +18,7 @@
 // rounding can depend on it, so the codes are bit-exact with an exact
 // computation.
 #include <cuda_bf16.h>
+#include <atomic>
 #include <cuda_fp8.h>
 
 #include "mx_internal.h"
@@ -1102,13 +1103,23 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   }
 }
 
+namespace {
+// Per device: the kernel's dynamic shared-memory limit has been raised.  The
+// flags have internal linkage, so every loaded copy of the library sets the
+// limit of its own kernel.
+constexpr int kMaxAttrDevices = 64;
+std::atomic<bool> g_smem_attr_set[kMaxAttrDevices];
+}  // namespace
+
 cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mx_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kMaxSmem);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxAttrDevices) return cudaErrorInvalidDevice;
+  if (!g_smem_attr_set[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(mx_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    g_smem_attr_set[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -141,3 +141,38 @@ def test_gemm_prefill_prequantised_a(fs):
     ref = oracle.gemm(a, bc, bs)["c"]
     got = _gpu_gemm(fs, a, b, c_f32=True, prequant=True)
     assert rel_l2(got, ref) < 1e-5
+
+
+def test_two_library_copies_in_one_process(fs, tmp_path):
+    """A second copy of the library loaded in the same process launches its
+    own kernels (each copy raises its own kernels' shared-memory limits)."""
+    import ctypes
+    import shutil
+
+    import torch
+
+    from mxfp8_swiglu_mlp_gb300 import build
+
+    path = str(tmp_path / "libfsops_copy.so")
+    shutil.copy(build.LIB, path)
+    other = ctypes.CDLL(path)
+    for name, (args, res) in fs._SIGS.items():
+        f = getattr(other, name)
+        f.argtypes = args
+        f.restype = res
+    for M, N, K in ((16, 512, 256), (256, 512, 256)):  # the persistent and the tiled kernel
+        a_bits, b_bits = _operands(M, N, K, 90 + M)
+        bc, bs = fs.quantize_weight(to_dev_u16(b_bits))
+        a = to_dev_u16(a_bits)
+        outs = []
+        for lib in (fs.lib, other):
+            ws_n = lib.fsops_gemm_workspace_bytes(M, N, K)
+            ws = torch.zeros(ws_n, dtype=torch.uint8, device="cuda")
+            c = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            st = lib.fsops_mxfp8_gemm_ex(a.data_ptr(), None, fs.DTYPE_BF16, bc.data_ptr(), bs.data_ptr(),
+                                         c.data_ptr(), fs.DTYPE_F32, M, N, K, ws.data_ptr(), ws_n,
+                                         torch.cuda.current_stream().cuda_stream)
+            assert st == fs.OK, (M, lib.fsops_last_cuda_error())
+            torch.cuda.synchronize()
+            outs.append(c.cpu().numpy().astype(np.float64))
+        assert rel_l2(outs[1], outs[0]) < 1e-6
