@@ -177,6 +177,19 @@ bool encode_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows)
   return r == CUDA_SUCCESS;
 }
 
+// Scale tiles (512 bytes each, `tiles` of them) as a 2-D tensor of u32 rows of
+// 128 elements, read one tile per TMA box.
+bool encode_scale_map(CUtensorMap* m, const void* base, int tiles) {
+  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(tiles)};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, 1};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Tile heights and split of one fused MLP launch.
 struct MlpPlan {
   int TR0, TR1;  // weight rows per tile: gate/up, down (256 or 128)
@@ -373,11 +386,20 @@ bool gemm_shape_ok(int M, int N, int K) {
 fsops_status fill_tiled(TiledArgs& ta, const uint8_t* codes, const uint8_t* sfa, const uint8_t* b_codes,
                         const uint8_t* b_scales, int M, int N, int K, uint8_t* ctl, const DeviceInfo* di) {
   std::memset(&ta, 0, sizeof(ta));
-  // 2-block clusters on vertically adjacent tiles (each loads half of B and
-  // multicasts it) whenever there are two row tiles
+  // With two or more row tiles, 2-block clusters on vertically adjacent
+  // tiles: the default multicasts half of each B stage into both blocks
+  // (FSOPS_GEMM_FORM=1); FSOPS_GEMM_FORM=2 runs the pair as one 256-row
+  // cta_group::2 MMA (N % 256 == 0); 0 forces one block per tile.
   const int MT = (M + 127) / 128;
-  ta.cluster_ok = (MT >= 2 && di->sms >= 2 && env_int("FSOPS_GEMM_PAIRS", 1, 0, 1)) ? 1 : 0;
-  if (!encode_map(&ta.tm_a, codes, K, M, 128) || !encode_map(&ta.tm_b, b_codes, K, N, ta.cluster_ok ? 128 : 256))
+  const int want = env_int("FSOPS_GEMM_FORM", kTiledMulticast, kTiledSingle, kTiledPairMma);
+  ta.form = (MT < 2 || di->sms < 2) ? kTiledSingle : want;
+  if (ta.form == kTiledPairMma && N % 256 != 0) ta.form = kTiledMulticast;
+  if (!encode_map(&ta.tm_a, codes, K, M, 128) ||
+      !encode_map(&ta.tm_b, b_codes, K, N, ta.form == kTiledSingle ? 256 : 128))
+    return FSOPS_ERR_INVALID_ARG;
+  const int KS = K / kTileK;
+  if (ta.form == kTiledPairMma &&
+      (!encode_scale_map(&ta.tm_sfa, sfa, MT * KS) || !encode_scale_map(&ta.tm_sfb, b_scales, (N / 128) * KS)))
     return FSOPS_ERR_INVALID_ARG;
   ta.sf_a = sfa;
   ta.sf_b = b_scales;

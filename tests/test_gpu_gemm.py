@@ -114,7 +114,12 @@ PREFILL = [(129, 256, 128), (300, 384, 256), (1000, 640, 640), (4096, 256, 256)]
 
 
 @pytest.mark.parametrize("M,N,K", PREFILL)
-def test_gemm_prefill_fp32_out_matches_oracle(fs, M, N, K):
+@pytest.mark.parametrize("form", ["0", "1", "2"])
+def test_gemm_prefill_fp32_out_matches_oracle(fs, M, N, K, form, monkeypatch):
+    """All three launch forms: one block per tile (0), 2-block clusters
+    multicasting half of B (1), and the 256-row pair MMA (2; shapes with an
+    odd number of 128-column halves fall back to form 1)."""
+    monkeypatch.setenv("FSOPS_GEMM_FORM", form)
     a, b = _operands(M, N, K, seed=3 * M + N + K)
     bc, bs = oracle.quantize_bf16(b)
     ref = oracle.gemm(a, bc, bs)["c"]
@@ -123,7 +128,9 @@ def test_gemm_prefill_fp32_out_matches_oracle(fs, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", PREFILL[:3])
-def test_gemm_prefill_bf16_out_matches_oracle(fs, M, N, K):
+@pytest.mark.parametrize("form", ["1", "2"])
+def test_gemm_prefill_bf16_out_matches_oracle(fs, M, N, K, form, monkeypatch):
+    monkeypatch.setenv("FSOPS_GEMM_FORM", form)
     a, b = _operands(M, N, K, seed=5 * M + N + K)
     bc, bs = oracle.quantize_bf16(b)
     res = oracle.gemm(a, bc, bs)
@@ -132,6 +139,19 @@ def test_gemm_prefill_bf16_out_matches_oracle(fs, M, N, K):
     assert rel_l2(got, ref) < 2e-3
     assert max_abs_norm(got, ref) < 1e-2
     assert np.mean(got == ref) > 0.9
+
+
+@pytest.mark.parametrize("form", ["1", "2"])
+def test_gemm_prefill_pair_shapes(fs, form, monkeypatch):
+    """N a multiple of 256 (the pair MMA's shapes): an odd number of row
+    tiles leaves the last pair's second tile wholly past M."""
+    monkeypatch.setenv("FSOPS_GEMM_FORM", form)
+    for M, N, K, seed in ((384, 512, 640, 41), (1000, 768, 256, 42), (256, 256, 1152, 43)):
+        a, b = _operands(M, N, K, seed=seed)
+        bc, bs = oracle.quantize_bf16(b)
+        ref = oracle.gemm(a, bc, bs)["c"]
+        got = _gpu_gemm(fs, a, b, c_f32=True)
+        assert rel_l2(got, ref) < 1e-5, (M, N, K, rel_l2(got, ref))
 
 
 def test_gemm_prefill_prequantised_a(fs):
