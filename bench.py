@@ -418,7 +418,10 @@ def prefill_gemm(fs, stream):
         return e0.elapsed_time(e1) / 1e3 / n
 
     g = torch.Generator(device="cuda").manual_seed(7)
-    for name, (M, N, K) in (("gateup_m4096", (4096, 19456, 2560)), ("down_m4096", (4096, 2560, 9728))):
+    shapes = (("gateup_m4096", (4096, 19456, 2560)), ("down_m4096", (4096, 2560, 9728)),
+              ("square_1024", (1024, 1024, 1024)), ("square_4096", (4096, 4096, 4096)),
+              ("square_8192", (8192, 8192, 8192)), ("square_16384", (16384, 16384, 16384)))
+    for name, (M, N, K) in shapes:
         a = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
         w = (torch.randn(N, K, device="cuda", generator=g) / K ** 0.5).to(torch.bfloat16)
         bc, bs = fs.quantize_weight(w)
@@ -427,9 +430,10 @@ def prefill_gemm(fs, stream):
         ws = torch.zeros(ws_n, dtype=torch.uint8, device="cuda")
         c = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
         s = stream.cuda_stream
-        t_bf16 = timeit(lambda: fs.fsops_mxfp8_gemm(a, bc, bs, c, M, N, K, ws, ws_n, stream=s))
+        reps = 30 if M * N * K <= 8192 ** 3 else 8
+        t_bf16 = timeit(lambda: fs.fsops_mxfp8_gemm(a, bc, bs, c, M, N, K, ws, ws_n, stream=s), reps)
         t_pre = timeit(lambda: fs.fsops_mxfp8_gemm_ex(ac, asc, fs.DTYPE_MXFP8, bc, bs, c, fs.DTYPE_BF16, M, N, K, ws,
-                                                      ws_n, stream=s))
+                                                      ws_n, stream=s), reps)
         fl = 2.0 * M * N * K
         entry = {"M": M, "N": N, "K": K,
                  "bf16_a_us": round(t_bf16 * 1e6, 2), "bf16_a_tflops": round(fl / t_bf16 / 1e12, 1),
@@ -438,10 +442,34 @@ def prefill_gemm(fs, stream):
         try:
             a8, w8 = a.to(torch.float8_e4m3fn), w.to(torch.float8_e4m3fn)
             one = torch.ones((), device="cuda")
-            t_s = timeit(lambda: torch._scaled_mm(a8, w8.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16))
+            t_s = timeit(lambda: torch._scaled_mm(a8, w8.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16),
+                         reps)
             entry["cublas_fp8_per_tensor_us"] = round(t_s * 1e6, 2)
-        except Exception as e:  # not every torch build exposes it
+            del a8, w8
+        except Exception:  # not every torch build exposes it
             entry["cublas_fp8_per_tensor_us"] = None
+        # torch's MXFP8 GEMM (cuBLAS block-scaled) on the same codes and scales:
+        # its block-scale layout is the same 128 x 4 tiling, so the buffers
+        # pass as they are; the outputs must agree
+        try:
+            MT, KS = (M + 127) // 128, K // 128
+            sa = asc.view(torch.float8_e8m0fnu).reshape(MT * 128, KS * 4)
+            sb = bs.view(torch.float8_e8m0fnu).reshape(N, KS * 4)
+            a8, b8 = ac.view(torch.float8_e4m3fn), bc.view(torch.float8_e4m3fn)
+            ref = torch._scaled_mm(a8, b8.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+            fs.fsops_mxfp8_gemm_ex(ac, asc, fs.DTYPE_MXFP8, bc, bs, c, fs.DTYPE_BF16, M, N, K, ws, ws_n, stream=s)
+            stream.synchronize()
+            finite = bool(torch.isfinite(ref).all())
+            diff = ((ref.float() - c.float()).norm() / ref.float().norm()).item() if finite else None
+            t_mx = timeit(lambda: torch._scaled_mm(a8, b8.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16),
+                          reps)
+            entry["cublas_mxfp8_us"] = round(t_mx * 1e6, 2)
+            entry["cublas_mxfp8_output_finite"] = finite
+            entry["cublas_mxfp8_rel_l2_vs_ours"] = None if diff is None else float("%.3g" % diff)
+            del ref
+        except Exception as e:  # older torch / cuBLAS without MX block scaling
+            entry["cublas_mxfp8_us"] = None
+            entry["cublas_mxfp8_error"] = str(e).splitlines()[0][:160] if str(e) else type(e).__name__
         res[name] = entry
         del a, w, bc, bs, ac, asc, ws, c
         torch.cuda.empty_cache()

@@ -196,3 +196,39 @@ def test_two_library_copies_in_one_process(fs, tmp_path):
             torch.cuda.synchronize()
             outs.append(c.cpu().numpy().astype(np.float64))
         assert rel_l2(outs[1], outs[0]) < 1e-6
+
+
+@pytest.mark.parametrize("form", ["1", "2"])
+def test_gemm_square_16384_sampled(fs, form, monkeypatch):
+    """The largest square GEMM (16384^3, bf16 A quantised on the device): the
+    whole output is finite, and 16 sampled rows x 128 sampled columns match
+    the oracle, which quantises the sampled rows of A and B itself."""
+    import torch
+
+    monkeypatch.setenv("FSOPS_GEMM_FORM", form)
+    M = N = K = 16384
+    g = torch.Generator(device="cuda").manual_seed(11)
+    a = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    w = (torch.randn(N, K, device="cuda", generator=g) / K ** 0.5).to(torch.bfloat16)
+    bc, bs = fs.quantize_weight(w)
+    ws_n = fs.fsops_gemm_workspace_bytes(M, N, K)
+    ws = torch.zeros(ws_n, dtype=torch.uint8, device="cuda")
+    c = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    fs.fsops_mxfp8_gemm(a, bc, bs, c, M, N, K, ws, ws_n)
+    torch.cuda.synchronize()
+    assert fs.fsops_read_kernel_status(ws) == 0
+    assert bool(torch.isfinite(c).all())
+    rng = np.random.default_rng(int(form))
+    rows = np.sort(rng.choice(M, 16, replace=False))
+    cols = np.sort(rng.choice(N, 128, replace=False))
+    a_bits = a[torch.from_numpy(rows).cuda()].view(torch.int16).cpu().numpy().view(np.uint16)
+    b_bits = w[torch.from_numpy(cols).cuda()].view(torch.int16).cpu().numpy().view(np.uint16)
+    bc_o, bs_o = oracle.quantize_bf16(b_bits)
+    ref = oracle.gemm(a_bits, bc_o, bs_o)["c_bf16"]
+    got = c[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].view(torch.int16).cpu().numpy()
+    got = bf16_bits_to_f64(got.view(np.uint16))
+    want = bf16_bits_to_f64(ref)
+    assert rel_l2(got, want) < 2e-3, rel_l2(got, want)
+    assert max_abs_norm(got, want) < 1e-2
+    del a, w, bc, bs, ws, c
+    torch.cuda.empty_cache()
