@@ -41,10 +41,10 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_write.sum, mean of the captured launches) from ncu captures, by
 # workload, with the sha256 prefix of the kernel sources they were taken on:
 # reported only while those sources are unchanged (summaries under profiles/).
-NCU_TRAFFIC = {"m16": ("58b77035fc62aed6", 80.52e6, "profiles/mx_persistent_kernel_m16_memory.md "
+NCU_TRAFFIC = {"m16": ("a2942c2bfb196580", 80.52e6, "profiles/mx_persistent_kernel_m16_memory.md "
                        "(non-cluster launch form, FSOPS_PAIRS=0: ncu cannot launch the 2-block-cluster form)"),
-               "m128": ("58b77035fc62aed6", 163.68e6, "profiles/mx_persistent_kernel_m128_memory.md")}
-KERNEL_SOURCES = ("mx_kernels.cu", "mx_internal.h", "sm103.cuh")
+               "m128": ("a2942c2bfb196580", 163.56e6, "profiles/mx_persistent_kernel_m128_memory.md")}
+KERNEL_SOURCES = ("mx_kernels.cu", "mx_internal.h", "mx_mxfp8.cuh", "sm103.cuh")
 
 
 def kernel_sources_hash():
@@ -393,7 +393,7 @@ def sweep(fs, device, stream, hbm_peak, args):
     return res
 
 
-def prefill_gemm(fs, stream):
+def prefill_gemm(fs, stream, only=None):
     """The GEMM API above 128 rows (whole 128 x 256 tiles): the m16 MLP's
     gate/up and down projections at M = 4096, bf16 A (quantised by its own
     launch) and pre-quantised A; tensor-bound, so TFLOP/s against the FP8
@@ -422,6 +422,8 @@ def prefill_gemm(fs, stream):
               ("square_1024", (1024, 1024, 1024)), ("square_4096", (4096, 4096, 4096)),
               ("square_8192", (8192, 8192, 8192)), ("square_16384", (16384, 16384, 16384)))
     for name, (M, N, K) in shapes:
+        if only and name not in only:
+            continue
         a = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
         w = (torch.randn(N, K, device="cuda", generator=g) / K ** 0.5).to(torch.bfloat16)
         bc, bs = fs.quantize_weight(w)
@@ -473,6 +475,8 @@ def prefill_gemm(fs, stream):
         res[name] = entry
         del a, w, bc, bs, ac, asc, ws, c
         torch.cuda.empty_cache()
+    if only:
+        return res
     # the whole MLP of the m16 layer at 4096 tokens: x quantisation, the gate/up
     # GEMM with the SwiGLU + requantisation epilogue, the down GEMM; and the
     # three-launch ablation (gate/up to fp32 in HBM, SwiGLU-quantise, down)
@@ -589,7 +593,9 @@ def main():
                     help="distinct weight layers of the workload (0: its own count); profiling runs use fewer")
     ap.add_argument("--unfused", action="store_true", help="time the three-launch path as the main loop")
     ap.add_argument("--prefill-only", action="store_true",
-                    help="print only the M=4096 GEMM section (a short run for profiling the prefill kernel)")
+                    help="print only the prefill GEMM / MLP section (a short run for profiling the tiled kernel)")
+    ap.add_argument("--prefill-shapes", default="",
+                    help="comma-separated subset of the prefill section's GEMM shapes (default: all)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -608,7 +614,8 @@ def main():
         import mxfp8_swiglu_mlp_gb300 as fs
 
         torch.cuda.set_device(local_rank)
-        print(json.dumps({"prefill_gemm": prefill_gemm(fs, torch.cuda.Stream())}), flush=True)
+        only = [x for x in args.prefill_shapes.split(",") if x]
+        print(json.dumps({"prefill_gemm": prefill_gemm(fs, torch.cuda.Stream(), only)}), flush=True)
         return
     if world > 1:
         import torch
