@@ -23,6 +23,13 @@ What it computes, step by step, and where the step comes from:
    mirrors that quantisation point: h^ = dequant(quant(h)).
 5. The output is rounded once from fp64 to bf16 (round-to-nearest-even); the
    pages do not name the output type, bf16 matches the input activations.
+6. The decoder block around the MLP (``rmsnorm``, ``mlp_block``): the pages
+   name the MLP as Qwen3-4B's (p2, "Resultados de benchmark del kernel"), a
+   pre-norm decoder layer, but never write the norm or the residual out.  The
+   plainest reading, used here: the MLP's input is RMSNorm(x) * gamma =
+   x / sqrt(mean(x^2) + eps) * gamma per token row, in float64, quantised to
+   MXFP8 straight from float64; the block's output is x + MLP(...), rounded
+   once to bf16.
 
 Weight scales may be returned in the row-major layout or in the tiled layout
 the library consumes (``scales_rowmajor_to_tiled``): 128-row x 4-block tiles
@@ -193,8 +200,14 @@ def swiglu_mlp(x_bits: np.ndarray, qw: Dict[str, np.ndarray],
     Returns x^ (dequantised), g, u, h, h^ (dequantised), y (fp64) and
     y_bf16 (uint16 bits).
     """
-    I = qw["gateup_codes"].shape[0] // 2
     xc, xs = quantize_bf16(x_bits)
+    return _mlp_from_quantised(xc, xs, qw, rows_down)
+
+
+def _mlp_from_quantised(xc: np.ndarray, xs: np.ndarray, qw: Dict[str, np.ndarray],
+                        rows_down: Optional[np.ndarray]) -> Dict[str, np.ndarray]:
+    """The MLP from MXFP8 x^ (codes, row-major scales) on: steps 2-5."""
+    I = qw["gateup_codes"].shape[0] // 2
     xd = dequantize(xc, xs)
     wgu = dequantize(qw["gateup_codes"], qw["gateup_scales"])
     g = xd @ wgu[:I].T
@@ -211,6 +224,32 @@ def swiglu_mlp(x_bits: np.ndarray, qw: Dict[str, np.ndarray],
     return {"x_codes": xc, "x_scales": xs, "xd": xd, "g": g, "u": u, "h": h,
             "h_codes": hc, "h_scales": hs, "hd": hd, "y": y,
             "y_bf16": round_bf16_bits(y)}
+
+
+# ---------------------------------------------------------------- the decoder block
+def rmsnorm(x_bits: np.ndarray, gamma_bits: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm of bf16 rows x [M, H] with bf16 gain gamma [H], in float64:
+    x[m, k] / sqrt(mean_j x[m, j]^2 + eps) * gamma[k]."""
+    x = bf16_bits_to_f64(x_bits)
+    g = bf16_bits_to_f64(np.asarray(gamma_bits, np.uint16))
+    mean_sq = np.mean(x * x, axis=1, keepdims=True)
+    return x / np.sqrt(mean_sq + eps) * g[None, :]
+
+
+def mlp_block(x_bits: np.ndarray, gamma_bits: np.ndarray, eps: float, qw: Dict[str, np.ndarray],
+              residual: bool = True, rows_down: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """y = x + MLP(RMSNorm(x) * gamma) (``residual``) or the MLP alone.  The
+    normalised rows are quantised from float64; ``rows_down`` restricts the
+    output features as in ``swiglu_mlp``."""
+    n = rmsnorm(x_bits, gamma_bits, eps)
+    xc, xs = quantize_f64(n)
+    res = _mlp_from_quantised(xc, xs, qw, rows_down)
+    y = res["y"]
+    if residual:
+        x = bf16_bits_to_f64(x_bits)
+        y = y + (x if rows_down is None else x[:, rows_down])
+    res.update({"norm": n, "y": y, "y_bf16": round_bf16_bits(y)})
+    return res
 
 
 def gemm(a_bits: np.ndarray, b_codes: np.ndarray, b_scales: np.ndarray,

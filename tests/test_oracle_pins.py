@@ -9,7 +9,10 @@
 * exact rational arithmetic (fractions.Fraction) for the block-scaled GEMM;
 * torch.nn.functional.silu for SiLU;
 * the whole MLP rebuilt from torch pieces (float8 conversion, fp64 matmul);
-* the quantisation-error band against the unquantised fp64 SwiGLU MLP.
+* the quantisation-error band against the unquantised fp64 SwiGLU MLP;
+* the decoder block: RMSNorm against torch.nn.functional.rms_norm and its
+  closed forms (unit mean square, scale invariance, per-feature gain), and the
+  block y = x + MLP(RMSNorm(x) * gamma) rebuilt from torch pieces.
 """
 import math
 import os
@@ -386,3 +389,94 @@ def test_planted_mistakes_are_caught(mistake):
         wdd = oracle.dequantize(qw["down_codes"], wrong)
     y = hd @ wdd.T
     assert _pin_error(y, x, wg, wu, wd) > 1e-3
+
+
+# ------------------------------------------------------------------ the decoder block
+def _gain(H, seed):
+    rng = np.random.default_rng(seed)
+    return inputs.bf16_bits_from_f32((1.0 + 0.1 * rng.standard_normal(H)).astype(np.float32))
+
+
+def _ones(H):
+    return inputs.bf16_bits_from_f32(np.ones(H, np.float32))
+
+
+def test_rmsnorm_matches_torch():
+    x, *_ = _small_layer(M=7, H=384, seed=31, token_scale_log10=(-2.0, 2.0))
+    g = _gain(384, 1)
+    for eps in (0.0, 1e-6, 0.5):
+        want = torch.nn.functional.rms_norm(_f64(x), (384,), weight=_f64(g), eps=eps)
+        np.testing.assert_allclose(oracle.rmsnorm(x, g, eps), want.numpy(), rtol=1e-13, atol=0)
+
+
+def test_rmsnorm_closed_forms():
+    x, *_ = _small_layer(M=6, H=512, seed=32, token_scale_log10=(-2.0, 2.0))
+    n = oracle.rmsnorm(x, _ones(512), 0.0)
+    # every row has mean square 1 (a norm over the wrong axis, or a missing
+    # square root, breaks this)
+    np.testing.assert_allclose(np.mean(n * n, axis=1), 1.0, rtol=1e-12)
+    # scaling a row by 2^k (exact in bf16) leaves it unchanged; -1 flips it
+    xf = oracle.bf16_bits_to_f64(x)
+    for c in (4.0, 0.125, -1.0):
+        xc = inputs.bf16_bits_from_f32((xf * c).astype(np.float32))
+        np.testing.assert_allclose(oracle.rmsnorm(xc, _ones(512), 0.0), np.sign(c) * n, rtol=1e-13)
+    # the gain multiplies each feature (column), not each token
+    g = _gain(512, 2)
+    np.testing.assert_allclose(oracle.rmsnorm(x, g, 0.0), n * oracle.bf16_bits_to_f64(g)[None, :], rtol=1e-15)
+    # [3, 4] has mean square 12.5
+    x2 = inputs.bf16_bits_from_f32(np.array([[3.0, 4.0]], np.float32))
+    np.testing.assert_allclose(oracle.rmsnorm(x2, _ones(2), 0.0), [[3 / math.sqrt(12.5), 4 / math.sqrt(12.5)]],
+                               rtol=1e-15)
+    # eps keeps an all-zero row at zero
+    z = np.zeros((1, 64), np.uint16)
+    assert np.all(oracle.rmsnorm(z, _ones(64), 1e-6) == 0.0)
+
+
+def _torch_block(x, g, eps, wg, wu, wd, residual=True):
+    xf = _f64(x)
+    n = torch.nn.functional.rms_norm(xf, (xf.shape[1],), weight=_f64(g), eps=eps)
+    qd = _torch_mx_qdq
+    gg = qd(n) @ qd(_f64(wg)).T
+    uu = qd(n) @ qd(_f64(wu)).T
+    y = qd(torch.nn.functional.silu(gg) * uu) @ qd(_f64(wd)).T
+    return y + xf if residual else y
+
+
+@pytest.mark.parametrize("residual", [True, False])
+def test_mlp_block_matches_torch_rebuild(residual):
+    x, wg, wu, wd = _small_layer(M=5, H=256, I=384, seed=33, token_scale_log10=(-1.0, 1.0))
+    g = _gain(256, 3)
+    qw = oracle.quantize_weights(wg, wu, wd)
+    res = oracle.mlp_block(x, g, 1e-6, qw, residual=residual)
+    y_t = _torch_block(x, g, 1e-6, wg, wu, wd, residual)
+    assert oracle.rel_l2(res["y"], y_t.numpy()) < 1e-12
+    assert np.array_equal(res["y_bf16"], oracle.round_bf16_bits(y_t.numpy()))
+    rows = np.array([1, 100, 255])
+    part = oracle.mlp_block(x, g, 1e-6, qw, residual=residual, rows_down=rows)
+    assert np.array_equal(part["y_bf16"], res["y_bf16"][:, rows])
+
+
+@pytest.mark.parametrize("mistake", ["no_gain", "no_residual", "eps_outside_sqrt", "bf16_rounded_norm",
+                                     "norm_over_tokens"])
+def test_mlp_block_planted_mistakes_are_caught(mistake):
+    """Each plausible bug in the block, planted here on the CPU, breaks the
+    torch rebuild pin by far more than its 1e-12 tolerance."""
+    x, wg, wu, wd = _small_layer(M=4, H=256, I=256, seed=34, token_scale_log10=(-1.0, 1.0))
+    g = _gain(256, 4)
+    eps = 1e-2  # large enough for the eps placement to show
+    qw = oracle.quantize_weights(wg, wu, wd)
+    xf = oracle.bf16_bits_to_f64(x)
+    gf = oracle.bf16_bits_to_f64(g)
+    if mistake == "norm_over_tokens":
+        n = xf / np.sqrt(np.mean(xf * xf, axis=0, keepdims=True) + eps) * gf
+    elif mistake == "eps_outside_sqrt":
+        n = xf / (np.sqrt(np.mean(xf * xf, axis=1, keepdims=True)) + eps) * gf
+    else:
+        n = xf / np.sqrt(np.mean(xf * xf, axis=1, keepdims=True) + eps) * (1.0 if mistake == "no_gain" else gf)
+    if mistake == "bf16_rounded_norm":
+        n = oracle.bf16_bits_to_f64(oracle.round_bf16_bits(n))
+    y = oracle.mx_oracle._mlp_from_quantised(*oracle.quantize_f64(n), qw, None)["y"]
+    if mistake != "no_residual":
+        y = y + xf
+    want = _torch_block(x, g, eps, wg, wu, wd).numpy()
+    assert oracle.rel_l2(y, want) > 1e-6, mistake

@@ -30,6 +30,9 @@ Recipe (all draws in float32, then rounded to bf16 with round-to-nearest-even):
   along K (drawn without replacement).
 * x is [M, H] standard normal; for ``token_scale_log10`` = (a, b) each row m is
   multiplied by 10**u_m with u_m ~ U(a, b).
+* The RMSNorm gain of the decoder block (``make_norm_gain``) is [H],
+  1 + 0.1 * standard normal, from ``SeedSequence(s).spawn(1 + layers + 1)``'s
+  last child (the streams above are unchanged); its eps is ``NORM_EPS``.
 
 ``backend="torch-cuda"`` draws the same distributions with a seeded
 ``torch.Generator`` on the GPU (a different random stream); it exists only so
@@ -45,7 +48,10 @@ from typing import Dict, List, Optional, Tuple
 import numpy as np
 
 __all__ = ["Workload", "WORKLOADS", "bf16_bits_from_f32", "bf16_bits_to_f32",
-           "make_activations", "make_layer", "make_workload_small"]
+           "make_activations", "make_layer", "make_workload_small", "make_norm_gain", "NORM_EPS"]
+
+# eps of the decoder block's RMSNorm (the value Qwen3-family configs use)
+NORM_EPS = 1e-6
 
 
 @dataclasses.dataclass(frozen=True)
@@ -143,6 +149,14 @@ def make_activations(wl: Workload, M: Optional[int] = None) -> np.ndarray:
         u = rng.uniform(lo, hi, size=(M, 1))
         x = (x * np.power(10.0, u)).astype(np.float32)
     return bf16_bits_from_f32(x)
+
+
+def make_norm_gain(wl: Workload) -> np.ndarray:
+    """RMSNorm gain gamma [H] as uint16 bf16 bits: 1 + 0.1 * N(0, 1)."""
+    ss = np.random.SeedSequence(wl.seed).spawn(1 + wl.layers + 1)[-1]
+    rng = np.random.Generator(np.random.PCG64(ss))
+    g = 1.0 + 0.1 * rng.standard_normal(wl.H, dtype=np.float32)
+    return bf16_bits_from_f32(g.astype(np.float32))
 
 
 # ---------------------------------------------------------------- torch draws
