@@ -178,12 +178,23 @@ class MlpBench:
         else:
             self.x = inputs.make_activations_torch(wl, M, device)
         self.y = torch.empty((M, self.H), dtype=torch.bfloat16, device=device)
+        gb = inputs.make_norm_gain(wl)
+        self.gamma = torch.from_numpy(np.ascontiguousarray(gb).view(np.int16)).to(device).view(torch.bfloat16)
         self.ws = fs.Workspace(M, self.H, self.I, device=device)
         self.copies = copies
         torch.cuda.synchronize()
 
     def call(self, i, fused=True, stream=None, x=None, y=None):
+        """fused: True (single launch), False (three launches) or "block"
+        (RMSNorm + MLP + residual, fsops_mxfp8_swiglu_mlp_block)."""
         w = self.weights[i % self.copies]
+        if fused == "block":
+            from workloads import inputs
+
+            self.fs.fsops_mxfp8_swiglu_mlp_block(self.x if x is None else x, self.gamma, inputs.NORM_EPS, True,
+                                                 w.gateup_codes, w.down_codes, w.scales, self.y if y is None else y,
+                                                 self.M, self.H, self.I, stream)
+            return
         f = self.fs.fsops_mxfp8_swiglu_mlp if fused else self.fs.fsops_mxfp8_swiglu_mlp_unfused
         f(self.x if x is None else x, w.gateup_codes, w.down_codes, w.scales, self.y if y is None else y,
           self.M, self.H, self.I, stream)
@@ -376,6 +387,11 @@ def sweep(fs, device, stream, hbm_peak, args):
             key = "fused" if fused else "unfused_3_launches"
             entry[key] = {"tokens_per_s": round(wl.M / t, 1), "us_per_call": round(t * 1e6, 3),
                           "GBps": round(B / t / 1e9, 1), "frac_hbm": round(B / t / 1e9 / hbm_peak, 4)}
+        # the decoder block around it: RMSNorm + quantisation launch, the fused
+        # MLP reading the quantised rows, + x in the bf16 store
+        dt, _ = b.timed(n, "block", 5, stream)
+        entry["block_rmsnorm_residual"] = {"us_per_call": round(dt / n * 1e6, 3),
+                                           "tokens_per_s": round(wl.M / (dt / n), 1), "launches": 2}
         tl = b.per_launch(min(n, 200), stream)
         entry["fused"]["launch_us"] = round(tl * 1e6, 3)
         entry["fused"]["launch_frac_hbm"] = round(B / tl / 1e9 / hbm_peak, 4)

@@ -170,6 +170,42 @@ fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup,
                                     const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I,
                                     void* stream);
 
+/* ------------------------------------------------------------------------
+ * The decoder block around the MLP.  The pages name the MLP as a Qwen3-4B
+ * SwiGLU MLP (p2, "Resultados de benchmark del kernel"): in that pre-norm
+ * decoder the MLP's input is RMSNorm(x) * gamma and its output is added back
+ * to x.  The pages do not write either step out; these entry points take the
+ * standard definitions, in fp32:
+ *   RMSNorm(x)[m, k] = x[m, k] * rsqrt(mean_j x[m, j]^2 + eps).
+ *
+ * fsops_rmsnorm_quantize_mxfp8 -- codes/scales of RMSNorm(x) * gamma, quantised
+ * with the MXFP8 rule above (the normalised values are never rounded to bf16).
+ *   x_bf16 [rows, ld] bf16 (first K columns used), gamma_bf16 [K] bf16,
+ *   eps >= 0 (INVALID_ARG for negative, NaN or huge), codes [rows, K], scales
+ *   as in fsops_quantize_mxfp8 (the tiled layout pads rows to 128 with scale 0).
+ *   Limits as fsops_quantize_mxfp8; gamma 16-byte aligned.
+ */
+fsops_status fsops_rmsnorm_quantize_mxfp8(const void* x_bf16, const void* gamma_bf16, float eps, int rows, int K,
+                                          int ld, uint8_t* codes, uint8_t* scales, fsops_scale_layout layout,
+                                          void* stream);
+
+/* fsops_mxfp8_swiglu_mlp_block -- the feed-forward half of a decoder layer:
+ *   y = x + MLP(RMSNorm(x) * gamma)   (residual = 1)
+ *   y = MLP(RMSNorm(x) * gamma)       (residual = 0)
+ * with MLP the computation of fsops_mxfp8_swiglu_mlp and the sum rounded to
+ * bf16 once.  Two launches for M <= 128 (RMSNorm + quantisation, then the
+ * single-launch MLP reading the quantised rows and adding x in its bf16
+ * store); three above.  Arguments, limits and workspace as
+ * fsops_mxfp8_swiglu_mlp, plus gamma_bf16 [H] (16-byte aligned) and eps.
+ * y_bf16 may equal x_bf16 (in place): x is read by the first launch and, for
+ * the residual, only by the thread that then writes the same element of y.
+ * Graph-capture safe, so a chain of layers (y of one block is x of the next)
+ * can be captured once and replayed. */
+fsops_status fsops_mxfp8_swiglu_mlp_block(const void* x_bf16, const void* gamma_bf16, float eps, int residual,
+                                          const uint8_t* w_gateup, const uint8_t* w_down,
+                                          const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I,
+                                          void* stream);
+
 /* The same computation as three launches with the intermediates in HBM (the
  * unfused baseline of p2 "Por que cuBLAS no era suficiente"): GEMM gate/up
  * with fp32 output [M, 2I], SwiGLU + requantisation, GEMM down.  Same

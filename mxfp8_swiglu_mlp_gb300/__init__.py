@@ -25,7 +25,8 @@ __all__ = [
     "fsops_gemm_workspace_bytes", "fsops_swiglu_quantize_mxfp8", "fsops_mxfp8_swiglu_mlp",
     "fsops_mxfp8_swiglu_mlp_unfused", "fsops_mxfp8_swiglu_mlp_noalloc", "fsops_mlp_workspace_bytes", "fsops_set_workspace",
     "fsops_read_kernel_status", "fsops_set_wait_timeout_ns", "fsops_debug_set_extra_arrivals",
-    "fsops_status_string", "fsops_version", "fsops_last_cuda_error", "quantize_weight", "MLPWeights", "prepare_mlp_weights",
+    "fsops_status_string", "fsops_version", "fsops_last_cuda_error", "fsops_rmsnorm_quantize_mxfp8",
+    "fsops_mxfp8_swiglu_mlp_block", "quantize_weight", "MLPWeights", "prepare_mlp_weights",
     "Workspace", "pair_gate_up",
 ]
 
@@ -55,6 +56,9 @@ _SIGS = {
     "fsops_mxfp8_swiglu_mlp": ([_vp, _vp, _vp, ctypes.POINTER(_MlpScales), _vp, _i, _i, _i, _vp], _i),
     "fsops_mxfp8_swiglu_mlp_unfused": ([_vp, _vp, _vp, ctypes.POINTER(_MlpScales), _vp, _i, _i, _i, _vp], _i),
     "fsops_mxfp8_swiglu_mlp_noalloc": ([_vp, _vp, _vp, ctypes.POINTER(_MlpScales), _vp, _i, _i, _i, _vp], _i),
+    "fsops_rmsnorm_quantize_mxfp8": ([_vp, _vp, ctypes.c_float, _i, _i, _i, _vp, _vp, _i, _vp], _i),
+    "fsops_mxfp8_swiglu_mlp_block": ([_vp, _vp, ctypes.c_float, _i, _vp, _vp, ctypes.POINTER(_MlpScales), _vp, _i, _i,
+                                      _i, _vp], _i),
     "fsops_mlp_workspace_bytes": ([_i, _i, _i], _sz),
     "fsops_set_workspace": ([_vp, _sz], _i),
     "fsops_read_kernel_status": ([_vp, ctypes.POINTER(_u32)], _i),
@@ -109,6 +113,12 @@ def fsops_quantize_mxfp8(x, rows: int, K: int, ld: int, codes, scales, layout: i
            "fsops_quantize_mxfp8")
 
 
+def fsops_rmsnorm_quantize_mxfp8(x, gamma, eps: float, rows: int, K: int, ld: int, codes, scales, layout: int,
+                                 stream=None) -> None:
+    _check(lib.fsops_rmsnorm_quantize_mxfp8(_ptr(x), _ptr(gamma), eps, rows, K, ld, _ptr(codes), _ptr(scales), layout,
+                                            _stream(stream)), "fsops_rmsnorm_quantize_mxfp8")
+
+
 def fsops_scale_bytes(rows: int, K: int, layout: int) -> int:
     return lib.fsops_scale_bytes(rows, K, layout)
 
@@ -145,6 +155,15 @@ def fsops_mxfp8_swiglu_mlp(x_bf16, w_gateup, w_down, scales, y_bf16, M: int, H: 
     sc = _mlp_scales(scales)
     _check(lib.fsops_mxfp8_swiglu_mlp(_ptr(x_bf16), _ptr(w_gateup), _ptr(w_down), ctypes.byref(sc), _ptr(y_bf16),
                                       M, H, I, _stream(stream)), "fsops_mxfp8_swiglu_mlp")
+
+
+def fsops_mxfp8_swiglu_mlp_block(x_bf16, gamma_bf16, eps: float, residual: bool, w_gateup, w_down, scales, y_bf16,
+                                 M: int, H: int, I: int, stream=None) -> None:
+    """y = x + MLP(RMSNorm(x) * gamma) (``residual``) or the MLP alone."""
+    sc = _mlp_scales(scales)
+    _check(lib.fsops_mxfp8_swiglu_mlp_block(_ptr(x_bf16), _ptr(gamma_bf16), eps, 1 if residual else 0, _ptr(w_gateup),
+                                            _ptr(w_down), ctypes.byref(sc), _ptr(y_bf16), M, H, I, _stream(stream)),
+           "fsops_mxfp8_swiglu_mlp_block")
 
 
 def fsops_mxfp8_swiglu_mlp_unfused(x_bf16, w_gateup, w_down, scales, y_bf16, M: int, H: int, I: int,

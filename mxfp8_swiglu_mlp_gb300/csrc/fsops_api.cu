@@ -321,9 +321,11 @@ struct MlpBuffers {
 };
 // Fills the two phases of the fused MLP: phase 0 gate/up (W_gateup rows in
 // tiles of pl.TR0, SwiGLU epilogue), phase 1 down (W_down in tiles of pl.TR1).
+// x_bf16 == nullptr: x is already quantised into b.xq / b.xq_sf (the
+// decoder block's RMSNorm launch); residual (bf16 [M, H]) is added to y.
 fsops_status fill_mlp_args(KernelArgs& ka, const MlpPlan& pl, const MlpBuffers& b, const void* x_bf16,
                            const uint8_t* w_gateup, const uint8_t* w_down, const fsops_mlp_scales* scales,
-                           void* y_bf16, int M, int H, int I) {
+                           void* y_bf16, int M, int H, int I, const void* residual = nullptr) {
   init_common(ka, M, reinterpret_cast<uint32_t*>(b.ctl));
   const int Ic = I / 128;  // 128-feature chunks (phase-1 k-stages)
   if (ctl_words_needed(Ic, pl.T0, pl.T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
@@ -338,6 +340,7 @@ fsops_status fill_mlp_args(KernelArgs& ka, const MlpPlan& pl, const MlpBuffers& 
   ka.I = I;
   ka.out = y_bf16;
   ka.out_f32 = 0;
+  ka.residual = static_cast<const uint16_t*>(residual);
   PhaseArgs& p0 = ka.ph[0];
   p0.sf_w = scales->gateup;
   p0.sf_act = ka.xq_sf;
@@ -349,8 +352,8 @@ fsops_status fill_mlp_args(KernelArgs& ka, const MlpPlan& pl, const MlpBuffers& 
   p0.rows = 2 * I;
   p0.whole_tiles = pl.whole0;
   p0.pairs = pl.pairs0;
-  ka.local_xq = local_xq_for(ka.npad);
-  p0.dep = ka.local_xq ? kDepNone : kDepXReady;
+  ka.local_xq = x_bf16 != nullptr ? local_xq_for(ka.npad) : 0;
+  p0.dep = (ka.local_xq || x_bf16 == nullptr) ? kDepNone : kDepXReady;
   if (ka.local_xq && !encode_x_map(&ka.tm_x, x_bf16, H, M, ka.npad)) return FSOPS_ERR_INVALID_ARG;
   p0.epi = kEpiSwiGLU;
   p0.out_ld = I;
@@ -443,9 +446,12 @@ fsops_status gemm_tiled_impl(const void* a, const uint8_t* a_scales, bool a_bf16
 // The MLP above 128 token rows, in three launches: x quantised to MXFP8; the
 // gate/up GEMM with the SwiGLU epilogue, which writes h requantised to MXFP8;
 // the down GEMM on h.
+// x_bf16 == nullptr: x is already quantised in the workspace; residual is
+// added to y by the down GEMM's epilogue.
 fsops_status mlp_tiled_impl(const void* x_bf16, const uint8_t* w_gateup, const uint8_t* w_down,
                             const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I, uint8_t* ws,
-                            const MlpLayout& l, const DeviceInfo* di, cudaStream_t stream) {
+                            const MlpLayout& l, const DeviceInfo* di, cudaStream_t stream,
+                            const void* residual = nullptr) {
   TiledArgs gu;
   fsops_status st = fill_tiled(gu, ws + l.xq, ws + l.xq_sf, w_gateup, scales->gateup, M, 2 * I, H, ws + l.ctl, di);
   if (st != FSOPS_OK) return st;
@@ -457,7 +463,8 @@ fsops_status mlp_tiled_impl(const void* x_bf16, const uint8_t* w_gateup, const u
   if (st != FSOPS_OK) return st;
   if (!encode_out_map(&dn.tm_c, y_bf16, M, H, false)) return FSOPS_ERR_INVALID_ARG;
   dn.c = y_bf16;
-  if ((st = quantize_a(x_bf16, M, H, ws + l.xq, ws + l.xq_sf, stream)) != FSOPS_OK) return st;
+  dn.residual = static_cast<const uint16_t*>(residual);
+  if (x_bf16 != nullptr && (st = quantize_a(x_bf16, M, H, ws + l.xq, ws + l.xq_sf, stream)) != FSOPS_OK) return st;
   if ((st = run_tiled(gu, di, stream)) != FSOPS_OK) return st;
   return run_tiled(dn, di, stream);
 }
@@ -676,6 +683,62 @@ fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup,
   st = fill_mlp_args(ka, pl, bufs, x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I);
   if (st != FSOPS_OK) return st;
   return launch(ka, grid, static_cast<cudaStream_t>(stream));
+}
+
+fsops_status fsops_rmsnorm_quantize_mxfp8(const void* x_bf16, const void* gamma_bf16, float eps, int rows, int K,
+                                          int ld, uint8_t* codes, uint8_t* scales, fsops_scale_layout layout,
+                                          void* stream) {
+  if (layout != FSOPS_SCALES_ROWMAJOR && layout != FSOPS_SCALES_TCGEN05) return FSOPS_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || eps > 1e30f) return FSOPS_ERR_INVALID_ARG;  // also rejects NaN
+  if (rows < 0 || K <= 0 || ld < K) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (K % (layout == FSOPS_SCALES_TCGEN05 ? 128 : 32) != 0 || ld % 8 != 0) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(rows) * ld >= (1LL << 31)) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return FSOPS_OK;
+  if (x_bf16 == nullptr || gamma_bf16 == nullptr || codes == nullptr || scales == nullptr) return FSOPS_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(gamma_bf16) || !aligned16(codes)) return FSOPS_ERR_MISALIGNED;
+  int dev;
+  const DeviceInfo* di;
+  fsops_status st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  const cudaError_t e = launch_rmsnorm_quantize(
+      static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(gamma_bf16), eps, rows, K, ld, codes, scales,
+      layout == FSOPS_SCALES_TCGEN05 ? 1 : 0, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "rmsnorm_quantize_kernel launch");
+}
+
+fsops_status fsops_mxfp8_swiglu_mlp_block(const void* x_bf16, const void* gamma_bf16, float eps, int residual,
+                                          const uint8_t* w_gateup, const uint8_t* w_down,
+                                          const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I,
+                                          void* stream) {
+  fsops_status st = mlp_validate(x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I);
+  if (st != FSOPS_OK) return st;
+  if (gamma_bf16 == nullptr || !(eps >= 0.0f) || eps > 1e30f || (residual != 0 && residual != 1))
+    return FSOPS_ERR_INVALID_ARG;
+  if (!aligned16(gamma_bf16)) return FSOPS_ERR_MISALIGNED;
+  int dev;
+  const DeviceInfo* di;
+  st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  const MlpLayout l = mlp_layout(M, H, I);
+  uint8_t* ws;
+  st = check_ws(dev, l.total, &ws);
+  if (st != FSOPS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // launch 1: RMSNorm(x) * gamma quantised into the workspace's x buffers
+  const cudaError_t e = launch_rmsnorm_quantize(static_cast<const uint16_t*>(x_bf16),
+                                                static_cast<const uint16_t*>(gamma_bf16), eps, M, H, H, ws + l.xq,
+                                                ws + l.xq_sf, 1, s);
+  if (e != cudaSuccess) return cuda_failed(e, "rmsnorm_quantize_kernel launch");
+  const void* res = residual ? x_bf16 : nullptr;
+  // launch 2 (3 above 128 rows): the MLP on the quantised rows, + x
+  if (M > 128) return mlp_tiled_impl(nullptr, w_gateup, w_down, scales, y_bf16, M, H, I, ws, l, di, s, res);
+  const int grid = di->sms;
+  const MlpPlan pl = plan_mlp(M, H, I, grid);
+  const MlpBuffers bufs{ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.hq, ws + l.hq_sf, ws + l.part0, ws + l.part1};
+  KernelArgs ka;
+  st = fill_mlp_args(ka, pl, bufs, nullptr, w_gateup, w_down, scales, y_bf16, M, H, I, res);
+  if (st != FSOPS_OK) return st;
+  return launch(ka, grid, s);
 }
 
 fsops_status fsops_mxfp8_swiglu_mlp_unfused(const void* x_bf16, const uint8_t* w_gateup, const uint8_t* w_down,

@@ -485,6 +485,23 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
             tmem_ld16(tlane + cbeg + 32 * j, v[0]);
             tmem_ld16(tlane + cbeg + 32 * j + 16, v[1]);
             tmem_ld_wait();
+            const int r = mt * 128 + q4 * 32 + lane;
+            if (a.residual != nullptr && r < a.M) {  // C = residual + the sums, rounded once
+              const uint4* rp =
+                  reinterpret_cast<const uint4*>(a.residual + static_cast<size_t>(r) * a.N + nt * 256 + cbeg + 32 * j);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint4 rv = rp[q];
+                const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int e = 8 * q + 2 * i;
+                  v[e >> 4][e & 15] = __float_as_uint(__uint_as_float(v[e >> 4][e & 15]) + __uint_as_float(rw[i] << 16));
+                  v[e >> 4][(e + 1) & 15] =
+                      __float_as_uint(__uint_as_float(v[e >> 4][(e + 1) & 15]) + __uint_as_float(rw[i] & 0xFFFF0000u));
+                }
+              }
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[j][i] = pack_bf16x2(v[i >> 3][(2 * i) & 15], v[i >> 3][(2 * i + 1) & 15]);
           }

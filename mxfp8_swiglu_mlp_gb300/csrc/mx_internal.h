@@ -79,6 +79,7 @@ struct KernelArgs {
   // plain epilogue output
   void* out;              // [M, out_ld]
   int out_f32;
+  const uint16_t* residual;  // bf16 [M, out_ld] added to a bf16 output before its rounding, or null
   // control
   uint32_t* ctl;          // kCtlHeaderWords words
   uint32_t* hflags;       // [I / 128]: 1 once SwiGLU tile t (features 128t..128t+127) is written
@@ -130,5 +131,7 @@ cudaError_t launch_quantize(const uint16_t* x, int rows, int K, int ld, uint8_t*
                             int tiled, cudaStream_t stream);
 cudaError_t launch_swiglu_quantize(const float* gu, int M, int I, uint8_t* hc, uint8_t* hs,
                                    cudaStream_t stream);
+cudaError_t launch_rmsnorm_quantize(const uint16_t* x, const uint16_t* gamma, float eps, int rows, int K, int ld,
+                                    uint8_t* codes, uint8_t* scales, int tiled, cudaStream_t stream);
 
 }  // namespace fsops

@@ -109,6 +109,79 @@ cudaError_t launch_quantize(const uint16_t* x, int rows, int K, int ld, uint8_t*
 }
 
 // ======================================================================
+// RMSNorm + quantisation: one block per row.  The row's mean square is
+// reduced in fp32, then each thread quantises whole 32-blocks of
+// x * rsqrt(mean(x^2) + eps) * gamma (fp32) with the rule above.  Rows of the
+// last 128-row scale tile past `rows` get scale 0 (tiled layout).
+// ======================================================================
+constexpr int kNormThreads = 128;
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_quantize_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps, int rows, int K, int ld,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int tiled) {
+  const int r = blockIdx.x, nb = K / 32;
+  if (r >= rows) {
+    for (int kb = threadIdx.x; kb < nb; kb += kNormThreads) scales[tiled_sf_offset(r, kb, K / 128)] = 0;
+    return;
+  }
+  const uint16_t* xr = x + static_cast<long long>(r) * ld;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < K / 8; i += kNormThreads) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
+      ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+    }
+  }
+  __shared__ float part[kNormThreads / 32];
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormThreads / 32; ++i) tot += part[i];
+  const float inv_rms = rsqrtf(tot / static_cast<float>(K) + eps);
+  for (int kb = threadIdx.x; kb < nb; kb += kNormThreads) {
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr + kb * 32) + q);
+      const uint4 gv = __ldg(reinterpret_cast<const uint4*>(gamma + kb * 32) + q);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[8 * q + 2 * j] = bf16_lo(xw[j]) * inv_rms * bf16_lo(gw[j]);
+        v[8 * q + 2 * j + 1] = bf16_hi(xw[j]) * inv_rms * bf16_hi(gw[j]);
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const uint32_t sc = ue8m0_from_amax(amax);
+    const float inv = inv_scale_from_ue8m0(sc);
+    uint32_t pk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      pk[i] = e4m3_code(v[4 * i] * inv) | (e4m3_code(v[4 * i + 1] * inv) << 8) |
+              (e4m3_code(v[4 * i + 2] * inv) << 16) | (e4m3_code(v[4 * i + 3] * inv) << 24);
+    uint4* d = reinterpret_cast<uint4*>(codes + static_cast<long long>(r) * K + kb * 32);
+    d[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    d[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    if (tiled) scales[tiled_sf_offset(r, kb, K / 128)] = static_cast<uint8_t>(sc);
+    else scales[static_cast<long long>(r) * nb + kb] = static_cast<uint8_t>(sc);
+  }
+}
+
+cudaError_t launch_rmsnorm_quantize(const uint16_t* x, const uint16_t* gamma, float eps, int rows, int K, int ld,
+                                    uint8_t* codes, uint8_t* scales, int tiled, cudaStream_t stream) {
+  const int grid = tiled ? (rows + 127) / 128 * 128 : rows;
+  if (grid == 0) return cudaSuccess;
+  rmsnorm_quantize_kernel<<<grid, kNormThreads, 0, stream>>>(x, gamma, eps, rows, K, ld, codes, scales, tiled);
+  return cudaGetLastError();
+}
+
+// ======================================================================
 // SwiGLU + requantisation (the middle launch of the unfused path).
 // ======================================================================
 // SiLU(g) * u = g * sigmoid(g) * u (silu_mul); for g -> -inf the reciprocal
@@ -352,6 +425,24 @@ __device__ __forceinline__ void swiglu_block(const KernelArgs& a, int f0, int r,
 __device__ __forceinline__ void store8(const KernelArgs& a, const PhaseArgs& p, int r, long long col,
                                        const float* v) {
   const long long o = static_cast<long long>(r) * p.out_ld + col;
+  if (a.residual != nullptr) {  // y = residual + the sums, rounded once
+    const uint4 rv = *reinterpret_cast<const uint4*>(a.residual + o);
+    const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+    float s[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      s[2 * i] = v[2 * i] + bf16_lo(rw[i]);
+      s[2 * i + 1] = v[2 * i + 1] + bf16_hi(rw[i]);
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(s[2 * i], s[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + o) = make_uint4(w[0], w[1], w[2], w[3]);
+    return;
+  }
   if (a.out_f32) {
     float4* d = reinterpret_cast<float4*>(static_cast<float*>(a.out) + o);
     d[0] = make_float4(v[0], v[1], v[2], v[3]);

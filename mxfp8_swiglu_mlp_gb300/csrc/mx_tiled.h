@@ -32,6 +32,7 @@ struct TiledArgs {
   uint32_t* status;       // first error (status << 24 | site << 16 | block)
   uint64_t timeout_ns;
   int form;               // kTiledSingle, kTiledMulticast or kTiledPairMma
+  const uint16_t* residual;  // bf16 [M, N] added to a bf16 C before its rounding, or null
   // SwiGLU epilogue (swiglu = 1): B is W_gateup, whose 128-row blocks hold 64
   // gate rows and then the 64 up rows of the same features, so a 256-column
   // tile covers 128 whole features.  The epilogue writes h = SiLU(g) * u,

@@ -115,3 +115,32 @@ def test_size_queries_reject_bad_shapes(fs):
     assert fs.fsops_mlp_workspace_bytes(16385, 256, 256) == 0
     assert fs.fsops_gemm_workspace_bytes(4, 100, 256) == 0
     assert fs.lib.fsops_set_wait_timeout_ns(0) == fs.ERR_INVALID_ARG
+
+
+def test_rmsnorm_quantize_validation(fs):
+    lib = fs.lib
+    q = lambda x=FAKE, g=FAKE, eps=1e-6, rows=4, K=256, ld=256, c=FAKE, s=FAKE, layout=fs.SCALES_TCGEN05: \
+        lib.fsops_rmsnorm_quantize_mxfp8(x, g, eps, rows, K, ld, c, s, layout, None)
+    assert q(layout=7) == fs.ERR_INVALID_ARG
+    assert q(eps=-1.0) == fs.ERR_INVALID_ARG
+    assert q(eps=float("nan")) == fs.ERR_INVALID_ARG
+    assert q(K=96) == fs.ERR_UNSUPPORTED_SHAPE                 # tiled layout wants K % 128
+    assert q(ld=100) == fs.ERR_UNSUPPORTED_SHAPE               # ld < K
+    assert q(rows=-1) == fs.ERR_UNSUPPORTED_SHAPE
+    assert q(rows=0) == fs.OK                                  # nothing to do, no device needed
+    assert q(g=None) == fs.ERR_INVALID_ARG
+    assert q(g=FAKE + 4) == fs.ERR_MISALIGNED
+
+
+def test_mlp_block_validation(fs):
+    lib = fs.lib
+    sc = fs._MlpScales(FAKE, FAKE)
+    call = lambda g=FAKE, eps=1e-6, res=1, M=16, H=256, I=256: lib.fsops_mxfp8_swiglu_mlp_block(
+        FAKE, g, eps, res, FAKE, FAKE, ctypes.byref(sc), FAKE, M, H, I, None)
+    assert call(g=None) == fs.ERR_INVALID_ARG
+    assert call(eps=float("nan")) == fs.ERR_INVALID_ARG
+    assert call(res=2) == fs.ERR_INVALID_ARG
+    assert call(g=FAKE + 2) == fs.ERR_MISALIGNED
+    for M in (0, 16385):
+        assert call(M=M) == fs.ERR_UNSUPPORTED_SHAPE
+    assert call(H=200) == fs.ERR_UNSUPPORTED_SHAPE

@@ -1,0 +1,182 @@
+"""The decoder block around the MLP: RMSNorm(x) * gamma quantised to MXFP8
+(fsops_rmsnorm_quantize_mxfp8) and y = x + MLP(...) (fsops_mxfp8_swiglu_mlp_block),
+against the oracle's rmsnorm / mlp_block on the workloads' distributions."""
+import numpy as np
+import pytest
+
+import oracle
+from workloads import inputs
+from tests._util import to_dev_u16, from_dev_bf16, bf16_bits_to_f64, rel_l2, max_abs_norm
+from tests.test_gpu_mlp import Layer, _assert_parity
+
+pytestmark = pytest.mark.gpu
+
+EPS = inputs.NORM_EPS
+
+
+@pytest.fixture(scope="module")
+def fs():
+    import mxfp8_swiglu_mlp_gb300 as fs
+
+    return fs
+
+
+def _gain(wl):
+    return inputs.make_norm_gain(wl)
+
+
+@pytest.mark.parametrize("rows,K,spread", [(5, 256, None), (128, 1024, (-2.0, 2.0)), (300, 2560, (-1.0, 1.0)),
+                                           (3, 8192, None)])
+def test_rmsnorm_quantize_matches_oracle(fs, rows, K, spread):
+    """The normalised rows are computed in fp32 on the device and in fp64 by
+    the oracle, so codes may differ where a value sits on a rounding edge.
+    Checked instead: every dequantised element is within the E4M3 rounding
+    bound of the fp64 normalised value, and almost every block has the
+    oracle's scale (a different scale needs the block amax within fp32
+    rounding of a power of two)."""
+    import torch
+
+    wl = inputs.make_workload_small("s", rows, K, 128, 40 + rows, token_scale_log10=spread)
+    x = inputs.make_activations(wl)
+    g = _gain(wl)
+    codes = torch.empty(rows, K, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(rows * K // 32, dtype=torch.uint8, device="cuda")
+    fs.fsops_rmsnorm_quantize_mxfp8(to_dev_u16(x), to_dev_u16(g), EPS, rows, K, K, codes, scales, fs.SCALES_ROWMAJOR)
+    torch.cuda.synchronize()
+    c, s = codes.cpu().numpy(), scales.cpu().numpy().reshape(rows, K // 32)
+    ref = oracle.rmsnorm(x, g, EPS)
+    rc, rs = oracle.quantize_f64(ref)
+    assert np.mean(s == rs) > 0.995
+    deq = oracle.dequantize(c, s)
+    blk_scale = np.repeat(np.ldexp(1.0, s.astype(np.int64) - 127), 32, axis=1)
+    t = np.abs(ref) / blk_scale  # element magnitude in the block's code units
+    bound = np.where(t >= 2.0 ** -6, np.ldexp(1.0, np.floor(np.log2(np.maximum(t, 1e-300))).astype(np.int64) - 4),
+                     2.0 ** -10) * blk_scale
+    sat = np.maximum(t - 448.0, 0.0) * blk_scale  # the MX rule saturates at 448 code units
+    assert np.all(np.abs(deq - ref) <= bound * 1.001 + sat + np.abs(ref) * 1e-6)
+    assert np.mean(c == rc) > 0.99
+    # the tiled layout holds the same bytes in the tcgen05 order (rows padded to 128)
+    st = torch.empty(fs.fsops_scale_bytes(rows, K, fs.SCALES_TCGEN05), dtype=torch.uint8, device="cuda")
+    c2 = torch.empty(rows, K, dtype=torch.uint8, device="cuda")
+    fs.fsops_rmsnorm_quantize_mxfp8(to_dev_u16(x), to_dev_u16(g), EPS, rows, K, K, c2, st, fs.SCALES_TCGEN05)
+    torch.cuda.synchronize()
+    assert np.array_equal(c2.cpu().numpy(), c)
+    assert np.array_equal(oracle.scales_tiled_to_rowmajor(st.cpu().numpy(), rows, K), s)
+
+
+class Block(Layer):
+    def __init__(self, fs, wl, M=None):
+        super().__init__(fs, wl, M=M)
+        self.g = _gain(wl)
+        self.g_dev = to_dev_u16(self.g)
+
+    def run_block(self, fs, residual=True, in_place=False):
+        import torch
+
+        if in_place:
+            y = self.x_dev.clone()
+            x = y
+        else:
+            x = self.x_dev
+            y = torch.empty((self.M, self.H), dtype=torch.bfloat16, device="cuda")
+        fs.fsops_mxfp8_swiglu_mlp_block(x, self.g_dev, EPS, residual, self.w.gateup_codes, self.w.down_codes,
+                                        self.w.scales, y, self.M, self.H, self.I)
+        torch.cuda.synchronize()
+        assert fs.fsops_read_kernel_status() == 0
+        return from_dev_bf16(y)
+
+    def oracle_block(self, residual=True, rows=None):
+        qw = oracle.quantize_weights(self.wg, self.wu, self.wd)
+        return oracle.mlp_block(self.x, self.g, EPS, qw, residual=residual, rows_down=rows)
+
+
+# decode (one fused launch after the norm) and prefill (tiled) shapes
+SHAPES = [(1, 256, 384, 50), (5, 512, 640, 51), (16, 1024, 1280, 52), (33, 384, 512, 53), (128, 256, 256, 54),
+          (64, 1152, 896, 55), (200, 384, 512, 56), (300, 256, 1024, 57)]
+
+
+@pytest.mark.parametrize("M,H,I,seed", SHAPES)
+@pytest.mark.parametrize("residual", [True, False])
+def test_block_matches_oracle(fs, M, H, I, seed, residual):
+    wl = inputs.make_workload_small("s", M, H, I, seed, token_scale_log10=(-1.0, 1.0))
+    B = Block(fs, wl)
+    _assert_parity(B.run_block(fs, residual), B.oracle_block(residual))
+
+
+@pytest.mark.parametrize("M", [16, 256])
+def test_block_in_place(fs, M):
+    """y may be x's own buffer."""
+    wl = inputs.make_workload_small("s", M, 512, 768, 60 + M)
+    B = Block(fs, wl)
+    a = B.run_block(fs, True, in_place=False)
+    b = B.run_block(fs, True, in_place=True)
+    assert rel_l2(bf16_bits_to_f64(b), bf16_bits_to_f64(a)) < 1e-3
+    _assert_parity(b, B.oracle_block(True))
+
+
+def test_block_full_size_m16(fs):
+    wl = inputs.WORKLOADS["m16"]
+    B = Block(fs, wl)
+    _assert_parity(B.run_block(fs, True), B.oracle_block(True))
+    _assert_parity(B.run_block(fs, False), B.oracle_block(False))
+
+
+def test_block_full_size_m128_sampled(fs):
+    """The m128 workload's rows span four decades; RMSNorm brings them all to
+    unit scale, and the rows with x ~ 0.01 are nearly all MLP output.  There a
+    single x^ code that fp32 and fp64 normalisation round differently (one of
+    the 524288 here) moves its row by about 1 %, so the per-row bound of the
+    plain MLP tests (which quantise bf16 x bit-exactly) is not applied; the
+    whole-output tolerances are."""
+    wl = inputs.WORKLOADS["m128"]
+    B = Block(fs, wl)
+    rows = np.sort(np.random.default_rng(3).choice(wl.H, 256, replace=False))
+    _assert_parity(B.run_block(fs, True)[:, rows], B.oracle_block(True, rows), per_row=False)
+
+
+def test_layer_chain_in_one_graph(fs):
+    """Three decoder blocks chained (each one's y is the next one's x), captured
+    once in a CUDA graph and replayed, against the oracle chained the same way
+    on its own outputs.  Differences of the order of one bf16 step per layer
+    propagate, so the bound is twice the single-layer one."""
+    import torch
+
+    M, H, I, L = 16, 512, 768, 3
+    wl = dataclasses_replace(inputs.make_workload_small("s", M, H, I, 70), layers=L)
+    x = inputs.make_activations(wl)
+    g = _gain(wl)
+    layers = [inputs.make_layer(wl, l) for l in range(L)]
+    ws_ = [fs.prepare_mlp_weights(to_dev_u16(a), to_dev_u16(b), to_dev_u16(c)) for a, b, c in layers]
+    ws = fs.Workspace(M, H, I)
+    bufs = [to_dev_u16(x)] + [torch.empty((M, H), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    g_dev = to_dev_u16(g)
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            for l in range(L):
+                w = ws_[l]
+                fs.fsops_mxfp8_swiglu_mlp_block(bufs[l], g_dev, EPS, True, w.gateup_codes, w.down_codes, w.scales,
+                                                bufs[l + 1], M, H, I, stream=s)
+    outs = []
+    for _ in range(2):
+        for b in bufs[1:]:
+            b.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert fs.fsops_read_kernel_status() == 0
+        outs.append(from_dev_bf16(bufs[L]))
+    assert rel_l2(bf16_bits_to_f64(outs[1]), bf16_bits_to_f64(outs[0])) < 1e-3
+    xo = x
+    for l in range(L):
+        qw = oracle.quantize_weights(*layers[l])
+        xo = oracle.mlp_block(xo, g, EPS, qw, residual=True)["y_bf16"]
+    got, want = bf16_bits_to_f64(outs[0]), bf16_bits_to_f64(xo)
+    assert rel_l2(got, want) < 4e-3, rel_l2(got, want)
+    assert max_abs_norm(got, want) < 2e-2
+
+
+def dataclasses_replace(wl, **kw):
+    import dataclasses
+
+    return dataclasses.replace(wl, **kw)
