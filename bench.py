@@ -41,9 +41,9 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_write.sum, mean of the captured launches) from ncu captures, by
 # workload, with the sha256 prefix of the kernel sources they were taken on:
 # reported only while those sources are unchanged (summaries under profiles/).
-NCU_TRAFFIC = {"m16": ("a2942c2bfb196580", 80.52e6, "profiles/mx_persistent_kernel_m16_memory.md "
+NCU_TRAFFIC = {"m16": ("9f50bc4370878cfc", 80.53e6, "profiles/mx_persistent_kernel_m16_memory.md "
                        "(non-cluster launch form, FSOPS_PAIRS=0: ncu cannot launch the 2-block-cluster form)"),
-               "m128": ("a2942c2bfb196580", 163.56e6, "profiles/mx_persistent_kernel_m128_memory.md")}
+               "m128": ("9f50bc4370878cfc", 163.86e6, "profiles/mx_persistent_kernel_m128_memory.md")}
 KERNEL_SOURCES = ("mx_kernels.cu", "mx_internal.h", "mx_mxfp8.cuh", "sm103.cuh")
 
 
