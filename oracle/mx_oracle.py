@@ -31,6 +31,15 @@ What it computes, step by step, and where the step comes from:
    MXFP8 straight from float64; the block's output is x + MLP(...), rounded
    once to bf16.
 
+7. Paged decode attention over an MXFP8 KV cache
+   (``paged_decode_attention``): the pages list MXFP8 FlashAttention with
+   paged decode and GQA through a stride-0 K/V broadcast (p2, "Ya esta
+   disponible") without writing it out.  Read plainly: K and V are cached
+   as MXFP8 (1x32 blocks along the head dimension, the rule of step 1), q
+   and the probabilities stay in full precision, query head h reads KV head
+   h // (Hq / Hkv), scores = sm_scale * q . k, softmax over the sequence,
+   out = p . v, rounded once to bf16.
+
 Weight scales may be returned in the row-major layout or in the tiled layout
 the library consumes (``scales_rowmajor_to_tiled``): 128-row x 4-block tiles
 of 512 bytes, tile (rt, kg) at byte (rt * ceil(K/128) + kg) * 512, entry
@@ -250,6 +259,41 @@ def mlp_block(x_bits: np.ndarray, gamma_bits: np.ndarray, eps: float, qw: Dict[s
         y = y + (x if rows_down is None else x[:, rows_down])
     res.update({"norm": n, "y": y, "y_bf16": round_bf16_bits(y)})
     return res
+
+
+# ---------------------------------------------------------------- paged decode attention
+def paged_decode_attention(q_bits: np.ndarray, k_codes: np.ndarray, k_scales: np.ndarray, v_codes: np.ndarray,
+                           v_scales: np.ndarray, block_table: np.ndarray, seq_lens: np.ndarray,
+                           sm_scale: float) -> Dict[str, np.ndarray]:
+    """One decode step of attention over a paged MXFP8 KV cache, in float64.
+
+    q_bits [B, Hq, D] bf16; k_codes / v_codes [num_pages, Hkv, P, D] E4M3;
+    k_scales / v_scales [num_pages, Hkv, P, D / 32] UE8M0 (row-major per
+    token); block_table [B, max_pages] page ids; seq_lens [B] (>= 1).  Token
+    t of sequence b is slot t % P of page block_table[b, t // P].
+    Returns out (float64 [B, Hq, D]) and out_bf16 (uint16 bits).
+    """
+    q = bf16_bits_to_f64(q_bits)
+    B, Hq, D = q.shape
+    _, Hkv, P, _ = k_codes.shape
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        n = int(seq_lens[b])
+        pages = [int(block_table[b, i]) for i in range(-(-n // P))]
+        for hk in range(Hkv):
+            kc = np.concatenate([k_codes[p, hk] for p in pages])[:n]
+            ks = np.concatenate([k_scales[p, hk] for p in pages])[:n]
+            vc = np.concatenate([v_codes[p, hk] for p in pages])[:n]
+            vs = np.concatenate([v_scales[p, hk] for p in pages])[:n]
+            k = dequantize(kc, ks)
+            v = dequantize(vc, vs)
+            for g in range(G):
+                h = hk * G + g
+                s = sm_scale * (k @ q[b, h])
+                w = np.exp(s - s.max())
+                out[b, h] = (w / w.sum()) @ v
+    return {"out": out, "out_bf16": round_bf16_bits(out)}
 
 
 def gemm(a_bits: np.ndarray, b_codes: np.ndarray, b_scales: np.ndarray,

@@ -480,3 +480,113 @@ def test_mlp_block_planted_mistakes_are_caught(mistake):
         y = y + xf
     want = _torch_block(x, g, eps, wg, wu, wd).numpy()
     assert oracle.rel_l2(y, want) > 1e-6, mistake
+
+
+# ------------------------------------------------------------------ paged decode attention
+def _attn_case(B=3, Hq=8, Hkv=2, D=128, P=16, lo=5, hi=70, seed=1):
+    wl = inputs.AttnWorkload("t", B, Hq, Hkv, D, P, lo, hi, seed)
+    d = inputs.make_attention(wl)
+    npages = d["k"].shape[0]
+    kc, ks = oracle.quantize_bf16(d["k"].reshape(-1, D))
+    vc, vs = oracle.quantize_bf16(d["v"].reshape(-1, D))
+    cache = (kc.reshape(npages, Hkv, P, D), ks.reshape(npages, Hkv, P, D // 32),
+             vc.reshape(npages, Hkv, P, D), vs.reshape(npages, Hkv, P, D // 32))
+    return wl, d, cache
+
+
+def _torch_attention(wl, d, cache, sm_scale, gqa=True):
+    """The same step from torch pieces: the pages gathered into contiguous
+    [Hkv, n, D] tensors, then torch's scaled_dot_product_attention with its
+    GQA broadcast, in float64."""
+    kc, ks, vc, vs = cache
+    npages, Hkv, P, D = kc.shape
+    kd = torch.from_numpy(oracle.dequantize(kc.reshape(-1, D), ks.reshape(-1, D // 32))).reshape(npages, Hkv, P, D)
+    vd = torch.from_numpy(oracle.dequantize(vc.reshape(-1, D), vs.reshape(-1, D // 32))).reshape(npages, Hkv, P, D)
+    q = _f64(d["q"])
+    out = []
+    for b in range(wl.B):
+        n = int(d["seq_lens"][b])
+        pages = torch.from_numpy(d["block_table"][b, : -(-n // P)].astype(np.int64))
+        kb = kd[pages].permute(1, 0, 2, 3).reshape(Hkv, -1, D)[:, :n]
+        vb = vd[pages].permute(1, 0, 2, 3).reshape(Hkv, -1, D)[:, :n]
+        o = torch.nn.functional.scaled_dot_product_attention(q[b][None, :, None, :], kb[None], vb[None], scale=sm_scale,
+                                                             enable_gqa=gqa)
+        out.append(o[0, :, 0, :])
+    return torch.stack(out).numpy()
+
+
+@pytest.mark.parametrize("kw", [{}, {"Hq": 8, "Hkv": 8}, {"Hq": 16, "Hkv": 2, "P": 32, "lo": 1, "hi": 64},
+                                {"B": 2, "Hq": 4, "Hkv": 1, "lo": 32, "hi": 32}])
+def test_attention_matches_torch_sdpa(kw):
+    wl, d, cache = _attn_case(**kw)
+    sm = 1.0 / math.sqrt(wl.D)
+    res = oracle.paged_decode_attention(d["q"], *cache, d["block_table"], d["seq_lens"], sm)
+    want = _torch_attention(wl, d, cache, sm)
+    np.testing.assert_allclose(res["out"], want, rtol=1e-10, atol=1e-12)
+    assert np.array_equal(res["out_bf16"], oracle.round_bf16_bits(want))
+
+
+def test_attention_closed_forms():
+    wl, d, cache = _attn_case(B=2, lo=40, hi=60, seed=3)
+    kc, ks, vc, vs = cache
+    npages, Hkv, P, D = kc.shape
+    table, lens = d["block_table"], d["seq_lens"]
+    # one token: the output is that token's V row
+    one = np.array([1, 1], np.int32)
+    res = oracle.paged_decode_attention(d["q"], kc, ks, vc, vs, table, one, 0.1)
+    for b in range(2):
+        for h in range(wl.Hq):
+            np.testing.assert_array_equal(res["out"][b, h], oracle.dequantize(vc[table[b, 0], h // 4, :1],
+                                                                               vs[table[b, 0], h // 4, :1])[0])
+    # identical keys (or a zero scale): the uniform average of the V rows
+    same_k = np.broadcast_to(kc[:1, :, :1], kc.shape).copy()  # one key per head, in every slot
+    same_s = np.broadcast_to(ks[:1, :, :1], ks.shape).copy()
+    r1 = oracle.paged_decode_attention(d["q"], same_k, same_s, vc, vs, table, lens, 0.1)
+    r2 = oracle.paged_decode_attention(d["q"], kc, ks, vc, vs, table, lens, 0.0)
+    for b in range(2):
+        n = int(lens[b])
+        pages = table[b, : -(-n // P)]
+        for hk in range(Hkv):
+            vrows = oracle.dequantize(np.concatenate([vc[p, hk] for p in pages])[:n],
+                                      np.concatenate([vs[p, hk] for p in pages])[:n])
+            mean = vrows.mean(axis=0)
+            for g in range(4):
+                np.testing.assert_allclose(r1["out"][b, hk * 4 + g], mean, rtol=1e-12, atol=1e-14)
+                np.testing.assert_allclose(r2["out"][b, hk * 4 + g], mean, rtol=1e-12, atol=1e-14)
+    # moving the physical pages (and the table with them) changes nothing
+    perm = np.random.default_rng(5).permutation(npages)
+    inv = np.argsort(perm)
+    moved = tuple(a[perm] for a in cache)
+    table2 = np.where(table >= 0, inv[np.maximum(table, 0)], -1).astype(np.int32)
+    r3 = oracle.paged_decode_attention(d["q"], *moved, table2, lens, 0.1)
+    r4 = oracle.paged_decode_attention(d["q"], *cache, table, lens, 0.1)
+    np.testing.assert_array_equal(r3["out"], r4["out"])
+
+
+@pytest.mark.parametrize("mistake", ["gqa_modulo", "padding_slots", "no_scale", "k_scales_from_v"])
+def test_attention_planted_mistakes_are_caught(mistake):
+    """Each plausible bug, planted here on the CPU, moves the result far from
+    the torch rebuild."""
+    wl, d, cache = _attn_case(B=2, Hq=8, Hkv=2, lo=20, hi=45, seed=7)
+    kc, ks, vc, vs = cache
+    npages, Hkv, P, D = kc.shape
+    sm = 1.0 / math.sqrt(D)
+    q = oracle.bf16_bits_to_f64(d["q"])
+    out = np.zeros_like(q)
+    for b in range(wl.B):
+        n = int(d["seq_lens"][b])
+        npg = -(-n // P)
+        pages = d["block_table"][b, :npg]
+        use = npg * P if mistake == "padding_slots" else n
+        for h in range(wl.Hq):
+            hk = h % Hkv if mistake == "gqa_modulo" else h // (wl.Hq // Hkv)
+            kscale = vs if mistake == "k_scales_from_v" else ks
+            k = oracle.dequantize(np.concatenate([kc[p, hk] for p in pages])[:use],
+                                  np.concatenate([kscale[p, hk] for p in pages])[:use])
+            v = oracle.dequantize(np.concatenate([vc[p, hk] for p in pages])[:use],
+                                  np.concatenate([vs[p, hk] for p in pages])[:use])
+            s = (1.0 if mistake == "no_scale" else sm) * (k @ q[b, h])
+            w = np.exp(s - s.max())
+            out[b, h] = (w / w.sum()) @ v
+    want = _torch_attention(wl, d, cache, sm)
+    assert oracle.rel_l2(out, want) > 1e-3, mistake

@@ -48,7 +48,8 @@ from typing import Dict, List, Optional, Tuple
 import numpy as np
 
 __all__ = ["Workload", "WORKLOADS", "bf16_bits_from_f32", "bf16_bits_to_f32",
-           "make_activations", "make_layer", "make_workload_small", "make_norm_gain", "NORM_EPS"]
+           "make_activations", "make_layer", "make_workload_small", "make_norm_gain", "NORM_EPS",
+           "AttnWorkload", "ATTN_WORKLOADS", "make_attention"]
 
 # eps of the decoder block's RMSNorm (the value Qwen3-family configs use)
 NORM_EPS = 1e-6
@@ -199,3 +200,49 @@ def make_activations_torch(wl: Workload, M: int, device):
         u = torch.rand(M, 1, generator=g, device=device, dtype=torch.float32) * (hi - lo) + lo
         x = x * torch.pow(10.0, u)
     return x.to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------- paged decode attention
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    """One decode step over a paged KV cache: B sequences of lengths drawn
+    uniformly in [len_lo, len_hi], Hq query heads sharing Hkv KV heads (GQA),
+    head dimension D, pages of P tokens."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    P: int
+    len_lo: int
+    len_hi: int
+    seed: int
+
+
+# a64: Qwen3-4B's attention geometry (32 query heads, 8 KV heads, D = 128)
+# at 64 sequences of 2k-6k tokens, pages of 16 tokens
+ATTN_WORKLOADS: Dict[str, AttnWorkload] = {
+    "a64": AttnWorkload("a64", 64, 32, 8, 128, 16, 2048, 6144, 90),
+}
+
+
+def make_attention(wl: AttnWorkload) -> dict:
+    """q [B, Hq, D], the cache's K and V [num_pages, Hkv, P, D] (bf16 bits,
+    standard normal, every slot drawn, also past a sequence's end), seq_lens
+    [B] and block_table [B, max_pages] (int32; each sequence's pages are a
+    random set of the physical pages; unused entries are -1)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(wl.seed)))
+    lens = rng.integers(wl.len_lo, wl.len_hi + 1, size=wl.B).astype(np.int32)
+    npg = [(int(n) + wl.P - 1) // wl.P for n in lens]
+    total = int(sum(npg))
+    perm = rng.permutation(total).astype(np.int32)
+    table = np.full((wl.B, max(npg)), -1, np.int32)
+    o = 0
+    for b, n in enumerate(npg):
+        table[b, :n] = perm[o:o + n]
+        o += n
+    q = rng.standard_normal((wl.B, wl.Hq, wl.D), dtype=np.float32)
+    k = rng.standard_normal((total, wl.Hkv, wl.P, wl.D), dtype=np.float32)
+    v = rng.standard_normal((total, wl.Hkv, wl.P, wl.D), dtype=np.float32)
+    return {"q": bf16_bits_from_f32(q), "k": bf16_bits_from_f32(k), "v": bf16_bits_from_f32(v),
+            "seq_lens": lens, "block_table": table}
