@@ -206,6 +206,46 @@ fsops_status fsops_mxfp8_swiglu_mlp_block(const void* x_bf16, const void* gamma_
                                           const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I,
                                           void* stream);
 
+/* ------------------------------------------------------------------------
+ * fsops_mxfp8_paged_decode_attention -- one decode step of attention over a
+ * paged KV cache held in MXFP8 (the library's MXFP8 FlashAttention with paged
+ * decode and native GQA through a stride-0 K/V broadcast, p2 "Ya esta
+ * disponible").  The pages do not write it out; read plainly:
+ *   for sequence b, query head h, KV head hk = h / (Hq / Hkv):
+ *   s[t] = sm_scale * q[b, h, :] . K^[t, hk, :]   for t < seq_lens[b],
+ *   out[b, h, :] = bf16( sum_t softmax(s)[t] * V^[t, hk, :] ),
+ * with K^ and V^ the dequantised cache (E4M3 codes times one UE8M0 scale per
+ * 32 elements of the head dimension, the rule above) and q, s and the
+ * probabilities in fp32.  The G = Hq / Hkv query heads of a KV head read its
+ * K and V once.
+ *   q_bf16      [B, Hq, D] bf16.
+ *   k_codes, v_codes    [num_pages, Hkv, P, D] E4M3 (P = page_size tokens of
+ *               one KV head contiguous per page).
+ *   k_scales, v_scales  [num_pages, Hkv, P, D / 32] UE8M0, row-major per token
+ *               (fsops_quantize_mxfp8's FSOPS_SCALES_ROWMAJOR of the
+ *               [num_pages * Hkv * P, D] rows).
+ *   block_table [B, max_pages] int32 page ids; token t of sequence b is slot
+ *               t % P of page block_table[b, t / P].  Entries past a
+ *               sequence's last page are not read.
+ *   seq_lens    [B] int32, 1 <= seq_lens[b] <= max_pages * P.
+ *   out_bf16    [B, Hq, D] bf16.
+ *   Limits: D = 128; P in {16, 32, 64, 128}; Hq / Hkv in {1, 2, 4, 8};
+ *   B, Hkv <= 65535.  Pointers 16-byte aligned (block_table, seq_lens 4).
+ *   workspace: 256-byte aligned, fsops_paged_attention_workspace_bytes() of
+ *   device memory whose first word (the status word) is zero; a page id
+ *   outside [0, num_pages) or a bad length is reported there
+ *   (fsops_read_kernel_status) instead of being read.  Two launches (the
+ *   splits of each sequence, then their combination); graph-capture safe. */
+fsops_status fsops_mxfp8_paged_decode_attention(const void* q_bf16, const uint8_t* k_codes, const uint8_t* k_scales,
+                                                const uint8_t* v_codes, const uint8_t* v_scales, int num_pages,
+                                                const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                                                void* out_bf16, int B, int Hq, int Hkv, int D, int page_size,
+                                                float sm_scale, void* workspace, size_t ws_bytes, void* stream);
+
+/* Workspace bytes of fsops_mxfp8_paged_decode_attention on the current device
+ * (0 if the shape is unsupported). */
+size_t fsops_paged_attention_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, int max_pages);
+
 /* The same computation as three launches with the intermediates in HBM (the
  * unfused baseline of p2 "Por que cuBLAS no era suficiente"): GEMM gate/up
  * with fp32 output [M, 2I], SwiGLU + requantisation, GEMM down.  Same

@@ -26,7 +26,8 @@ __all__ = [
     "fsops_mxfp8_swiglu_mlp_unfused", "fsops_mxfp8_swiglu_mlp_noalloc", "fsops_mlp_workspace_bytes", "fsops_set_workspace",
     "fsops_read_kernel_status", "fsops_set_wait_timeout_ns", "fsops_debug_set_extra_arrivals",
     "fsops_status_string", "fsops_version", "fsops_last_cuda_error", "fsops_rmsnorm_quantize_mxfp8",
-    "fsops_mxfp8_swiglu_mlp_block", "quantize_weight", "MLPWeights", "prepare_mlp_weights",
+    "fsops_mxfp8_swiglu_mlp_block", "fsops_mxfp8_paged_decode_attention", "fsops_paged_attention_workspace_bytes",
+    "quantize_weight", "MLPWeights", "prepare_mlp_weights",
     "Workspace", "pair_gate_up",
 ]
 
@@ -59,6 +60,9 @@ _SIGS = {
     "fsops_rmsnorm_quantize_mxfp8": ([_vp, _vp, ctypes.c_float, _i, _i, _i, _vp, _vp, _i, _vp], _i),
     "fsops_mxfp8_swiglu_mlp_block": ([_vp, _vp, ctypes.c_float, _i, _vp, _vp, ctypes.POINTER(_MlpScales), _vp, _i, _i,
                                       _i, _vp], _i),
+    "fsops_mxfp8_paged_decode_attention": ([_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i,
+                                            ctypes.c_float, _vp, _sz, _vp], _i),
+    "fsops_paged_attention_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
     "fsops_mlp_workspace_bytes": ([_i, _i, _i], _sz),
     "fsops_set_workspace": ([_vp, _sz], _i),
     "fsops_read_kernel_status": ([_vp, ctypes.POINTER(_u32)], _i),
@@ -155,6 +159,21 @@ def fsops_mxfp8_swiglu_mlp(x_bf16, w_gateup, w_down, scales, y_bf16, M: int, H: 
     sc = _mlp_scales(scales)
     _check(lib.fsops_mxfp8_swiglu_mlp(_ptr(x_bf16), _ptr(w_gateup), _ptr(w_down), ctypes.byref(sc), _ptr(y_bf16),
                                       M, H, I, _stream(stream)), "fsops_mxfp8_swiglu_mlp")
+
+
+def fsops_paged_attention_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, page_size: int, max_pages: int) -> int:
+    return lib.fsops_paged_attention_workspace_bytes(B, Hq, Hkv, D, page_size, max_pages)
+
+
+def fsops_mxfp8_paged_decode_attention(q, k_codes, k_scales, v_codes, v_scales, num_pages: int, block_table,
+                                       max_pages: int, seq_lens, out, B: int, Hq: int, Hkv: int, D: int, page_size: int,
+                                       sm_scale: float, workspace, ws_bytes: int, stream=None) -> None:
+    """One decode step of attention over the paged MXFP8 KV cache (see fsops.h)."""
+    _check(lib.fsops_mxfp8_paged_decode_attention(_ptr(q), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes),
+                                                  _ptr(v_scales), num_pages, _ptr(block_table), max_pages,
+                                                  _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, page_size, sm_scale,
+                                                  _ptr(workspace), ws_bytes, _stream(stream)),
+           "fsops_mxfp8_paged_decode_attention")
 
 
 def fsops_mxfp8_swiglu_mlp_block(x_bf16, gamma_bf16, eps: float, residual: bool, w_gateup, w_down, scales, y_bf16,

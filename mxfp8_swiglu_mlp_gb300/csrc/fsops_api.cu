@@ -17,6 +17,7 @@
 #include "../../include/fsops.h"
 #include "mx_internal.h"
 #include "mx_tiled.h"
+#include "mx_attention.h"
 
 using namespace fsops;
 
@@ -683,6 +684,79 @@ fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup,
   st = fill_mlp_args(ka, pl, bufs, x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I);
   if (st != FSOPS_OK) return st;
   return launch(ka, grid, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace {
+constexpr size_t kAttnStatusBytes = 256;
+// Shape check of the paged decode attention; FSOPS_OK when supported.
+fsops_status attn_shape(int B, int Hq, int Hkv, int D, int P, int num_pages, int max_pages) {
+  if (B < 1 || B > 65535 || Hkv < 1 || Hkv > 65535 || Hq < Hkv || Hq % Hkv != 0 || Hq > 65535)
+    return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (D != kAttnHeadDim || (P != 16 && P != 32 && P != 64 && P != 128)) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (num_pages < 1 || max_pages < 1 || static_cast<long long>(max_pages) * P > (1LL << 24))
+    return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  return FSOPS_OK;
+}
+}  // namespace
+
+extern "C" {
+
+size_t fsops_paged_attention_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, int max_pages) {
+  if (attn_shape(B, Hq, Hkv, D, page_size, 1, max_pages) != FSOPS_OK) return 0;
+  int dev;
+  const DeviceInfo* di;
+  if (current_device(&dev, &di) != FSOPS_OK) return 0;
+  const int ns = attn_splits(B, Hkv, max_pages, page_size, di->sms);
+  return kAttnStatusBytes + round_up(attn_part_floats(B, Hq, ns) * sizeof(float), 256);
+}
+
+fsops_status fsops_mxfp8_paged_decode_attention(const void* q_bf16, const uint8_t* k_codes, const uint8_t* k_scales,
+                                                const uint8_t* v_codes, const uint8_t* v_scales, int num_pages,
+                                                const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                                                void* out_bf16, int B, int Hq, int Hkv, int D, int page_size,
+                                                float sm_scale, void* workspace, size_t ws_bytes, void* stream) {
+  fsops_status st = attn_shape(B, Hq, Hkv, D, page_size, num_pages, max_pages);
+  if (st != FSOPS_OK) return st;
+  if (q_bf16 == nullptr || k_codes == nullptr || k_scales == nullptr || v_codes == nullptr || v_scales == nullptr ||
+      block_table == nullptr || seq_lens == nullptr || out_bf16 == nullptr || workspace == nullptr)
+    return FSOPS_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale) || sm_scale > 1e30f || sm_scale < -1e30f) return FSOPS_ERR_INVALID_ARG;
+  if (!aligned16(q_bf16) || !aligned16(k_codes) || !aligned16(k_scales) || !aligned16(v_codes) ||
+      !aligned16(v_scales) || !aligned16(out_bf16) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) != 0 || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0)
+    return FSOPS_ERR_MISALIGNED;
+  int dev;
+  const DeviceInfo* di;
+  st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  AttnArgs aa;
+  std::memset(&aa, 0, sizeof(aa));
+  aa.nsplit = attn_splits(B, Hkv, max_pages, page_size, di->sms);
+  if (ws_bytes < kAttnStatusBytes + attn_part_floats(B, Hq, aa.nsplit) * sizeof(float)) return FSOPS_ERR_INVALID_ARG;
+  aa.q = static_cast<const uint16_t*>(q_bf16);
+  aa.k_codes = k_codes;
+  aa.k_scales = k_scales;
+  aa.v_codes = v_codes;
+  aa.v_scales = v_scales;
+  aa.block_table = block_table;
+  aa.seq_lens = seq_lens;
+  aa.out = static_cast<uint16_t*>(out_bf16);
+  aa.status = static_cast<uint32_t*>(workspace);
+  aa.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kAttnStatusBytes);
+  aa.B = B;
+  aa.Hq = Hq;
+  aa.Hkv = Hkv;
+  aa.P = page_size;
+  aa.num_pages = num_pages;
+  aa.max_pages = max_pages;
+  aa.sm_scale = sm_scale;
+  aa.timeout_ns = g_timeout_ns.load();
+  const cudaError_t e = launch_paged_decode(aa, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "paged_decode_kernel launch");
 }
 
 fsops_status fsops_rmsnorm_quantize_mxfp8(const void* x_bf16, const void* gamma_bf16, float eps, int rows, int K,

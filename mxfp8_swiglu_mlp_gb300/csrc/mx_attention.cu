@@ -1,0 +1,335 @@
+// mx_attention.cu -- one decode step of attention over a paged MXFP8 KV cache.
+//
+//   paged_decode_kernel<G>  block (split, kv head, sequence): streams the
+//                           split's chunks of 128 tokens (their K and V pages
+//                           and scale rows, by bulk copies into a two-stage
+//                           shared-memory ring), scores them for the G query
+//                           heads that share the KV head (the GQA broadcast:
+//                           K and V are read once for the group), keeps an
+//                           online softmax and the unnormalised output.
+//   attn_combine_kernel     merges the splits of one (sequence, query head)
+//                           and writes the bf16 output.
+//
+// K and V are MXFP8: E4M3 codes with one UE8M0 scale per 32 elements of the
+// head dimension (the Fish Audio post's mxfp8 format, p2 "Estrategia de
+// cuantizacion FP8", applied to the cache that its MXFP8 FlashAttention
+// reads, p2 "Ya esta disponible").  q, the scores and the probabilities stay
+// in fp32: scores = sm_scale * q . k, p = softmax over the sequence,
+// out = p . v, rounded once to bf16.
+//
+// Cache layout: page p, KV head h holds P tokens' codes contiguously
+// ([num_pages, Hkv, P, D]) and their scales ([num_pages, Hkv, P, D / 32]);
+// token t of a sequence is slot t % P of page block_table[t / P].
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "mx_attention.h"
+#include "sm103.cuh"
+
+namespace fsops {
+using namespace dev;
+
+namespace {
+
+constexpr int kAThreads = 128;
+constexpr int kD = kAttnHeadDim;
+constexpr int kC = kAttnChunk;
+constexpr uint32_t kCodeBytes = kC * kD;      // 16 KB of K (or V) codes per chunk
+constexpr uint32_t kScaleBytes = kC * kD / 32;  // 512 B of scales per chunk
+
+struct __align__(128) AttnStage {
+  uint8_t k[kCodeBytes];
+  uint8_t v[kCodeBytes];
+  uint8_t ks[kScaleBytes];
+  uint8_t vs[kScaleBytes];
+};
+constexpr size_t kAttnSmem = 2 * sizeof(AttnStage) + 128;  // + alignment slack
+
+// Two E4M3 codes (low byte first) as two floats: exact.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
+  return __half22float2(__half2(h));
+}
+// 2^(s - 127) for a UE8M0 byte s (s = 0 is the subnormal 2^-127).
+__device__ __forceinline__ float ue8m0_value(uint32_t s) {
+  return s != 0 ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
+}
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+__device__ __forceinline__ void attn_error(const AttnArgs& a, uint32_t code, uint32_t site) {
+  atomicCAS(a.status, 0u, (code << 24) | ((site & 0xFFu) << 16) | (blockIdx.z & 0xFFFFu));
+}
+
+template <int G>
+__global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_constant__ AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  AttnStage* stg = reinterpret_cast<AttnStage*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ __align__(16) float qs[G * kD];      // q of the group's heads
+  __shared__ __align__(16) float ps[G * kC];      // probabilities of the chunk
+  __shared__ float red_max[4 * G], red_sum[4 * G];
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ int chunk_ok[2];
+
+  const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int len = a.seq_lens[b];
+  const bool len_ok = len >= 1 && len <= a.max_pages * a.P;
+  if (!len_ok && t == 0 && split == 0 && hk == 0) attn_error(a, 1u, 1u);  // FSOPS_ERR_INVALID_ARG
+  const int n = len_ok ? len : 0;
+  const int nchunks = (n + kC - 1) / kC;
+  const int per = (nchunks + a.nsplit - 1) / a.nsplit;
+  const int c0 = split * per, c1 = min(nchunks, c0 + per);
+  const int npages = (n + a.P - 1) / a.P;
+  const int pages_per_chunk = kC / a.P;
+
+  for (int i = t; i < G * kD; i += kAThreads) qs[i] = bf16_bits_to_float(a.q[(static_cast<size_t>(b) * a.Hq + hk * G) * kD + i]);
+  if (t == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  // Thread 0: the bulk copies of chunk c into stage s (pages past the
+  // sequence's last one are not loaded; their tokens are masked).  A page id
+  // outside [0, num_pages) is reported and its page skipped.
+  auto issue = [&](int c, int s) {
+    const int p0 = c * pages_per_chunk;
+    const int np = min(pages_per_chunk, npages - p0);
+    uint32_t bytes = 0;
+    int ok = 1;
+    for (int i = 0; i < np; ++i) {
+      const int pid = a.block_table[static_cast<size_t>(b) * a.max_pages + p0 + i];
+      if (pid < 0 || pid >= a.num_pages) ok = 0;
+      else bytes += 2u * (a.P * kD + a.P * (kD / 32));
+    }
+    if (!ok) attn_error(a, 1u, 2u);
+    chunk_ok[s] = ok;
+    fence_proxy_async_shared();  // the stage's earlier generic reads come before the copies' writes
+    mbar_arrive_expect_tx(&bar[s], bytes);
+    for (int i = 0; i < np; ++i) {
+      const int pid = a.block_table[static_cast<size_t>(b) * a.max_pages + p0 + i];
+      if (pid < 0 || pid >= a.num_pages) continue;
+      const size_t row = (static_cast<size_t>(pid) * a.Hkv + hk) * a.P;  // first token row of the page-head block
+      const uint32_t cb = static_cast<uint32_t>(a.P) * kD, sb = static_cast<uint32_t>(a.P) * (kD / 32);
+      bulk_load(stg[s].k + i * cb, a.k_codes + row * kD, cb, &bar[s], l2_policy_evict_first());
+      bulk_load(stg[s].v + i * cb, a.v_codes + row * kD, cb, &bar[s], l2_policy_evict_first());
+      bulk_load(stg[s].ks + i * sb, a.k_scales + row * (kD / 32), sb, &bar[s], l2_policy_evict_first());
+      bulk_load(stg[s].vs + i * sb, a.v_scales + row * (kD / 32), sb, &bar[s], l2_policy_evict_first());
+    }
+  };
+
+  float m_run[G], l_run[G], acc[G][4];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m_run[g] = -INFINITY;
+    l_run[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[g][e] = 0.f;
+  }
+  bool ok = true;
+  int stalled = -1;  // the chunk whose copies did not land in time
+  if (t == 0 && c0 < c1) issue(c0, 0);
+  for (int c = c0; c < c1 && ok; ++c) {
+    const int s = (c - c0) & 1;
+    if (t == 0 && c + 1 < c1) issue(c + 1, s ^ 1);
+    stalled = c;
+    // bounded wait for the chunk's copies
+    {
+      const uint32_t parity = static_cast<uint32_t>((c - c0) >> 1) & 1u;
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&bar[s], parity)) {
+        if (globaltimer_ns() - t0 > a.timeout_ns) {
+          if (t == 0) attn_error(a, 5u, 3u);  // FSOPS_ERR_TIMEOUT
+          ok = false;
+          break;
+        }
+      }
+    }
+    if (!__syncthreads_and(ok)) break;
+    const bool chunk_valid = chunk_ok[s] != 0;
+
+    // ---- scores: thread t scores token c * 128 + t for the G heads
+    const int tok = c * kC + t;
+    float sc[G];
+    if (tok < n && chunk_valid) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) sc[g] = 0.f;
+      const uint8_t* krow = stg[s].k + t * kD;
+      const uint32_t kscales = *reinterpret_cast<const uint32_t*>(stg[s].ks + t * (kD / 32));
+#pragma unroll 2
+      for (int i = 0; i < 8; ++i) {
+        const int cc = (i + t) & 7;  // 16-code piece, rotated per thread against bank conflicts
+        const uint4 kv = *reinterpret_cast<const uint4*>(krow + 16 * cc);
+        const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
+        float kf[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 lo = e4m3x2_to_float2(w4[j]), hi = e4m3x2_to_float2(w4[j] >> 16);
+          kf[4 * j] = lo.x;
+          kf[4 * j + 1] = lo.y;
+          kf[4 * j + 2] = hi.x;
+          kf[4 * j + 3] = hi.y;
+        }
+        const float scale = ue8m0_value((kscales >> (8 * (cc >> 1))) & 0xFFu);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float4* qv = reinterpret_cast<const float4*>(qs + g * kD + 16 * cc);
+          float dot = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 q4 = qv[j];
+            dot = fmaf(q4.x, kf[4 * j], dot);
+            dot = fmaf(q4.y, kf[4 * j + 1], dot);
+            dot = fmaf(q4.z, kf[4 * j + 2], dot);
+            dot = fmaf(q4.w, kf[4 * j + 3], dot);
+          }
+          sc[g] = fmaf(scale, dot, sc[g]);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) sc[g] *= a.sm_scale;
+    } else {
+#pragma unroll
+      for (int g = 0; g < G; ++g) sc[g] = -INFINITY;
+    }
+
+    // ---- online softmax over the chunk
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float m = sc[g];
+      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+      if (lane == 0) red_max[warp * G + g] = m;
+    }
+    __syncthreads();
+    float alpha[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float cm = fmaxf(fmaxf(red_max[g], red_max[G + g]), fmaxf(red_max[2 * G + g], red_max[3 * G + g]));
+      const float mn = fmaxf(m_run[g], cm);
+      // a chunk with no valid token (a bad page) leaves mn = -inf: nothing to add
+      const float p = (sc[g] == -INFINITY || mn == -INFINITY) ? 0.f : expf(sc[g] - mn);
+      alpha[g] = (m_run[g] == -INFINITY || mn == -INFINITY) ? (mn == -INFINITY ? 1.f : 0.f) : expf(m_run[g] - mn);
+      m_run[g] = mn;
+      ps[g * kC + t] = p;
+      float sum = p;
+      for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+      if (lane == 0) red_sum[warp * G + g] = sum;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      l_run[g] = l_run[g] * alpha[g] + (red_sum[g] + red_sum[G + g] + red_sum[2 * G + g] + red_sum[3 * G + g]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[g][e] *= alpha[g];
+    }
+
+    // ---- p . v: thread (warp, lane) owns dimensions 4 lane .. 4 lane + 3 and
+    // the chunk's tokens warp, warp + 4, ...
+    const int tmax = min(kC, n - c * kC);
+    if (chunk_valid) {
+      for (int tt = warp; tt < tmax; tt += 4) {
+        const uint32_t v4 = *reinterpret_cast<const uint32_t*>(stg[s].v + tt * kD + 4 * lane);
+        const float vscale = ue8m0_value(stg[s].vs[tt * (kD / 32) + (lane >> 3)]);
+        const float2 lo = e4m3x2_to_float2(v4), hi = e4m3x2_to_float2(v4 >> 16);
+        const float vf[4] = {lo.x * vscale, lo.y * vscale, hi.x * vscale, hi.y * vscale};
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float p = ps[g * kC + tt];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[g][e] = fmaf(p, vf[e], acc[g][e]);
+        }
+      }
+    }
+    __syncthreads();  // the stage and ps are rewritten next
+    stalled = -1;
+  }
+  if (stalled >= 0) {
+    // gave up: let the copies still in flight (this chunk's and the next
+    // one's) land before the ring is reused or the block leaves
+    if (t == 0) {
+      for (int c = stalled; c < min(stalled + 2, c1); ++c) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&bar[(c - c0) & 1], static_cast<uint32_t>((c - c0) >> 1) & 1u))
+          if (globaltimer_ns() - t0 > 200000000ull) break;
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- the four warps' partial outputs are summed; one record per head
+  float* wsum = reinterpret_cast<float*>(stg);  // reuse the ring: [4][G][D]
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) wsum[(warp * G + g) * kD + 4 * lane + e] = acc[g][e];
+  __syncthreads();
+  for (int i = t; i < G * kD; i += kAThreads) {
+    const int g = i / kD, d = i % kD;
+    const float o = wsum[g * kD + d] + wsum[(G + g) * kD + d] + wsum[(2 * G + g) * kD + d] + wsum[(3 * G + g) * kD + d];
+    float* rec = a.part + ((static_cast<size_t>(b) * a.Hq + hk * G + g) * a.nsplit + split) * (2 + kD);
+    rec[2 + d] = o;
+    if (d == 0) {
+      rec[0] = m_run[g];
+      rec[1] = l_run[g];
+    }
+  }
+}
+
+// One block per (query head, sequence), one thread per dimension.
+__global__ void __launch_bounds__(kD) attn_combine_kernel(const __grid_constant__ AttnArgs a) {
+  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  const float* rec = a.part + (static_cast<size_t>(b) * a.Hq + h) * a.nsplit * (2 + kD);
+  float M = -INFINITY;
+  for (int s = 0; s < a.nsplit; ++s) M = fmaxf(M, rec[s * (2 + kD)]);
+  float num = 0.f, den = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < a.nsplit; ++s) {
+      const float m = rec[s * (2 + kD)];
+      if (m == -INFINITY) continue;
+      const float w = expf(m - M);
+      num = fmaf(w, rec[s * (2 + kD) + 2 + d], num);
+      den = fmaf(w, rec[s * (2 + kD) + 1], den);
+    }
+  }
+  const float o = den > 0.f ? num / den : 0.f;
+  const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+  a.out[(static_cast<size_t>(b) * a.Hq + h) * kD + d] = *reinterpret_cast<const uint16_t*>(&ob);
+}
+
+template <int G>
+cudaError_t launch_group(const AttnArgs& a, cudaStream_t stream) {
+  static_assert(G <= kAttnMaxGroup, "group");
+  cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kAttnSmem));
+  if (e != cudaSuccess) return e;
+  paged_decode_kernel<G><<<dim3(a.nsplit, a.Hkv, a.B), kAThreads, kAttnSmem, stream>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_combine_kernel<<<dim3(a.Hq, a.B), kD, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int attn_splits(int B, int Hkv, int max_pages, int P, int sms) {
+  // enough blocks for about four per SM, each with at least four chunks
+  const int max_chunks = (max_pages * P + kC - 1) / kC;
+  const int want = (4 * sms + B * Hkv - 1) / (B * Hkv);
+  const int cap = (max_chunks + 3) / 4;
+  int s = want < cap ? want : cap;
+  return s < 1 ? 1 : s;
+}
+
+cudaError_t launch_paged_decode(const AttnArgs& a, cudaStream_t stream) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return launch_group<1>(a, stream);
+    case 2: return launch_group<2>(a, stream);
+    case 4: return launch_group<4>(a, stream);
+    case 8: return launch_group<8>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fsops

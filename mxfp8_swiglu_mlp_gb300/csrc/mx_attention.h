@@ -1,0 +1,38 @@
+// mx_attention.h -- paged decode attention over an MXFP8 KV cache
+// (mx_attention.cu).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fsops {
+
+constexpr int kAttnHeadDim = 128;   // D
+constexpr int kAttnChunk = 128;     // tokens per pipeline chunk (one per thread in the QK pass)
+constexpr int kAttnMaxGroup = 8;    // query heads per KV head
+
+struct AttnArgs {
+  const uint16_t* q;          // bf16 [B, Hq, D]
+  const uint8_t* k_codes;     // [num_pages, Hkv, P, D] E4M3
+  const uint8_t* k_scales;    // [num_pages, Hkv, P, D / 32] UE8M0
+  const uint8_t* v_codes;
+  const uint8_t* v_scales;
+  const int32_t* block_table; // [B, max_pages]
+  const int32_t* seq_lens;    // [B]
+  uint16_t* out;              // bf16 [B, Hq, D]
+  float* part;                // [B, Hq, nsplit, 2 + D]: running max, sum, unnormalised output
+  uint32_t* status;           // first error (status << 24 | site << 16 | sequence)
+  int B, Hq, Hkv, P, num_pages, max_pages, nsplit;
+  float sm_scale;
+  uint64_t timeout_ns;
+};
+
+// Splits of each sequence's chunks (one block each) for B sequences, Hkv KV
+// heads and at most max_pages pages of P tokens, on `sms` SMs.
+int attn_splits(int B, int Hkv, int max_pages, int P, int sms);
+// Partial-result floats of one call.
+inline size_t attn_part_floats(int B, int Hq, int nsplit) {
+  return static_cast<size_t>(B) * Hq * nsplit * (2 + kAttnHeadDim);
+}
+cudaError_t launch_paged_decode(const AttnArgs& a, cudaStream_t stream);
+
+}  // namespace fsops
