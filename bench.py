@@ -361,6 +361,7 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and not args.no_sweep:
         out["sweep"] = sweep(fs, device, stream, hbm_peak, args)
         out["prefill_gemm"] = prefill_gemm(fs, stream)
+        out["attention_decode"] = attention_decode(fs, stream, hbm_peak)
     if rank == 0 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(wl)
     del bench
@@ -518,6 +519,67 @@ def prefill_gemm(fs, stream, only=None):
     return res
 
 
+def attention_decode(fs, stream, hbm_peak):
+    """Paged decode attention over the MXFP8 KV cache, a64 workload (Qwen3-4B
+    attention geometry, 64 sequences of 2k-6k tokens, 16-token pages): µs
+    per call and the cache bytes read per call against the HBM peak."""
+    import math
+
+    import numpy as np
+    import torch
+
+    from workloads import inputs
+
+    wl = inputs.ATTN_WORKLOADS["a64"]
+    d = inputs.make_attention(wl)
+    npages = d["k"].shape[0]
+    rows = npages * wl.Hkv * wl.P
+    cache = []
+    for name in ("k", "v"):
+        x = torch.from_numpy(np.ascontiguousarray(d[name]).view(np.int16).reshape(rows, wl.D)).cuda()
+        codes = torch.empty(rows, wl.D, dtype=torch.uint8, device="cuda")
+        scales = torch.empty(rows * wl.D // 32, dtype=torch.uint8, device="cuda")
+        fs.fsops_quantize_mxfp8(x, rows, wl.D, wl.D, codes, scales, fs.SCALES_ROWMAJOR)
+        cache += [codes, scales]
+        del x
+    q = torch.from_numpy(np.ascontiguousarray(d["q"]).view(np.int16)).cuda()
+    table = torch.from_numpy(d["block_table"]).cuda()
+    lens = torch.from_numpy(d["seq_lens"]).cuda()
+    max_pages = d["block_table"].shape[1]
+    ws_n = fs.fsops_paged_attention_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, wl.P, max_pages)
+    ws = torch.zeros(ws_n + 256, dtype=torch.uint8, device="cuda")
+    ws_ptr = ws.data_ptr() + (-ws.data_ptr()) % 256
+    out = torch.empty(wl.B, wl.Hq, wl.D, dtype=torch.bfloat16, device="cuda")
+    s = stream.cuda_stream
+
+    def call():
+        fs.fsops_mxfp8_paged_decode_attention(q, cache[0], cache[1], cache[2], cache[3], npages, table, max_pages,
+                                              lens, out, wl.B, wl.Hq, wl.Hkv, wl.D, wl.P, 1.0 / math.sqrt(wl.D),
+                                              ws_ptr, ws_n, stream=s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(20):
+            call()
+        e1.record(stream)
+        e1.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / 20
+    tokens = int(d["seq_lens"].sum())
+    kv = tokens * wl.Hkv * 2 * (wl.D + wl.D // 32)
+    status = fs.fsops_read_kernel_status(ws_ptr)
+    res = {"workload": "a64: B=%d, Hq=%d, Hkv=%d, D=%d, page %d, lengths %d-%d (%d tokens)" %
+                       (wl.B, wl.Hq, wl.Hkv, wl.D, wl.P, wl.len_lo, wl.len_hi, tokens),
+           "us": round(t * 1e6, 2), "kv_bytes": kv, "GBps": round(kv / t / 1e9, 1),
+           "frac_hbm": round(kv / t / 1e9 / hbm_peak, 4), "launches": 2, "status": status}
+    del cache, q, table, lens, ws, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def cpu_baseline(wl):
     """The oracle as it stands, timed on this host on one full layer of the workload."""
     import numpy as np
@@ -610,6 +672,8 @@ def main():
     ap.add_argument("--unfused", action="store_true", help="time the three-launch path as the main loop")
     ap.add_argument("--prefill-only", action="store_true",
                     help="print only the prefill GEMM / MLP section (a short run for profiling the tiled kernel)")
+    ap.add_argument("--attention-only", action="store_true",
+                    help="print only the paged decode attention section")
     ap.add_argument("--prefill-shapes", default="",
                     help="comma-separated subset of the prefill section's GEMM shapes (default: all)")
     args = ap.parse_args()
@@ -623,6 +687,14 @@ def main():
         out = run_reference(args, rank, world)
         if out is not None:
             print(json.dumps(out), flush=True)
+        return
+    if args.attention_only:
+        import torch
+
+        import mxfp8_swiglu_mlp_gb300 as fs
+
+        torch.cuda.set_device(local_rank)
+        print(json.dumps({"attention_decode": attention_decode(fs, torch.cuda.Stream(), peaks()[0])}), flush=True)
         return
     if args.prefill_only:
         import torch

@@ -37,6 +37,7 @@ constexpr int kD = kAttnHeadDim;
 constexpr int kC = kAttnChunk;
 constexpr uint32_t kCodeBytes = kC * kD;      // 16 KB of K (or V) codes per chunk
 constexpr uint32_t kScaleBytes = kC * kD / 32;  // 512 B of scales per chunk
+constexpr int kQPiece = 20;                     // floats per padded 16-element piece of q
 
 struct __align__(128) AttnStage {
   uint8_t k[kCodeBytes];
@@ -65,7 +66,10 @@ template <int G>
 __global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   AttnStage* stg = reinterpret_cast<AttnStage*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  __shared__ __align__(16) float qs[G * kD];      // q of the group's heads
+  // q of the group's heads, each 16-element piece padded to 20 floats: the
+  // threads of a quarter warp read eight different pieces at once, and
+  // 80-byte strides put them on distinct banks
+  __shared__ __align__(16) float qs[G * 8 * kQPiece];
   __shared__ __align__(16) float ps[G * kC];      // probabilities of the chunk
   __shared__ float red_max[4 * G], red_sum[4 * G];
   __shared__ __align__(8) uint64_t bar[2];
@@ -83,7 +87,8 @@ __global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_co
   const int npages = (n + a.P - 1) / a.P;
   const int pages_per_chunk = kC / a.P;
 
-  for (int i = t; i < G * kD; i += kAThreads) qs[i] = bf16_bits_to_float(a.q[(static_cast<size_t>(b) * a.Hq + hk * G) * kD + i]);
+  for (int i = t; i < G * kD; i += kAThreads)
+    qs[(i / 16) * kQPiece + i % 16] = bf16_bits_to_float(a.q[(static_cast<size_t>(b) * a.Hq + hk * G) * kD + i]);
   if (t == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_co
         const float scale = ue8m0_value((kscales >> (8 * (cc >> 1))) & 0xFFu);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float4* qv = reinterpret_cast<const float4*>(qs + g * kD + 16 * cc);
+          const float4* qv = reinterpret_cast<const float4*>(qs + (g * 8 + cc) * kQPiece);
           float dot = 0.f;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
