@@ -144,3 +144,27 @@ def test_mlp_block_validation(fs):
     for M in (0, 16385):
         assert call(M=M) == fs.ERR_UNSUPPORTED_SHAPE
     assert call(H=200) == fs.ERR_UNSUPPORTED_SHAPE
+
+
+def test_paged_attention_validation(fs):
+    """Host-side checks of fsops_mxfp8_paged_decode_attention, before any
+    device work."""
+    lib = fs.lib
+    F4 = FAKE
+
+    def call(q=FAKE, kc=FAKE, ks=FAKE, vc=FAKE, vs=FAKE, num_pages=10, table=F4, max_pages=4, lens=F4, out=FAKE,
+             B=2, Hq=8, Hkv=2, D=128, P=16, sm=0.088, ws=FAKE, ws_n=1 << 20):
+        return lib.fsops_mxfp8_paged_decode_attention(q, kc, ks, vc, vs, num_pages, table, max_pages, lens, out, B,
+                                                      Hq, Hkv, D, P, sm, ws, ws_n, None)
+
+    for kw in ({"D": 64}, {"P": 8}, {"P": 48}, {"Hq": 6, "Hkv": 4}, {"Hq": 24, "Hkv": 2}, {"B": 0},
+               {"num_pages": 0}, {"max_pages": 0}, {"Hq": 1, "Hkv": 2}):
+        assert call(**kw) == fs.ERR_UNSUPPORTED_SHAPE, kw
+    assert call(q=None) == fs.ERR_INVALID_ARG
+    assert call(table=None) == fs.ERR_INVALID_ARG
+    assert call(ws=None) == fs.ERR_INVALID_ARG
+    assert call(sm=float("nan")) == fs.ERR_INVALID_ARG
+    assert call(kc=FAKE + 8) == fs.ERR_MISALIGNED
+    assert call(ws=FAKE + 16) == fs.ERR_MISALIGNED  # the workspace wants 256-byte alignment
+    assert call(lens=FAKE + 2) == fs.ERR_MISALIGNED
+    assert fs.fsops_paged_attention_workspace_bytes(2, 8, 2, 64, 16, 4) == 0
