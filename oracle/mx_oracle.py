@@ -40,6 +40,16 @@ What it computes, step by step, and where the step comes from:
    h // (Hq / Hkv), scores = sm_scale * q . k, softmax over the sequence,
    out = p . v, rounded once to bf16.
 
+8. The second scale format of the same library, "bsgemm" (p1 "Custom
+   kernels for the shapes TTS actually uses"; p2 "Estrategia de
+   cuantizacion FP8": FP8 with 128x128 block scales, for Hopper), read
+   plainly: weights in 128x128 blocks, activations in 1x128 groups along K
+   (one token's block), each with an fp32 scale s = amax / 448 (1 for an
+   all-zero block) and E4M3 codes RNE-satfinite of v / s.  s and v / s are
+   computed in IEEE fp32, the precision a kernel takes that decision in, so
+   the codes are defined bit for bit (``quantize_blockscale``); the GEMM
+   (``gemm_blockscale``) is then exact up to float64 rounding.
+
 Weight scales may be returned in the row-major layout or in the tiled layout
 the library consumes (``scales_rowmajor_to_tiled``): 128-row x 4-block tiles
 of 512 bytes, tile (rt, kg) at byte (rt * ceil(K/128) + kg) * 512, entry
@@ -294,6 +304,49 @@ def paged_decode_attention(q_bits: np.ndarray, k_codes: np.ndarray, k_scales: np
                 w = np.exp(s - s.max())
                 out[b, h] = (w / w.sum()) @ v
     return {"out": out, "out_bf16": round_bf16_bits(out)}
+
+
+# ---------------------------------------------------------------- 128x128 block scales
+def quantize_blockscale(bits: np.ndarray, block_rows: int, block_cols: int = 128):
+    """bf16 bit patterns [rows, K] -> (E4M3 codes [rows, K], fp32 scales
+    [ceil(rows / block_rows), K / block_cols]).  Each block's scale is
+    fl32(amax / 448) (1 when the block is all zero); each element's code is
+    the E4M3 round-to-nearest-even, saturated at 448, of fl32(v / scale)."""
+    v = bf16_bits_to_f64(np.asarray(bits, np.uint16)).astype(np.float32)
+    rows, K = v.shape
+    assert K % block_cols == 0
+    rb = -(-rows // block_rows)
+    scales = np.ones((rb, K // block_cols), np.float32)
+    codes = np.empty((rows, K), np.uint8)
+    for i in range(rb):
+        for j in range(K // block_cols):
+            blk = v[i * block_rows:(i + 1) * block_rows, j * block_cols:(j + 1) * block_cols]
+            amax = np.float32(np.abs(blk).max())
+            if amax > 0:
+                scales[i, j] = np.float32(amax / np.float32(448.0))
+            t = (blk / scales[i, j]).astype(np.float32)
+            mag = np.vectorize(e4m3_round_code, otypes=[np.uint8])(np.abs(t).astype(np.float64))
+            # the sign bit is kept, also where the magnitude rounds to zero
+            codes[i * block_rows:(i + 1) * block_rows, j * block_cols:(j + 1) * block_cols] = \
+                mag | np.where(np.signbit(t), 0x80, 0).astype(np.uint8)
+    return codes, scales
+
+
+def dequantize_blockscale(codes: np.ndarray, scales: np.ndarray, block_rows: int, block_cols: int = 128) -> np.ndarray:
+    """codes [rows, K] times their blocks' fp32 scales, in float64."""
+    codes = np.asarray(codes, np.uint8)
+    vals = e4m3_table()[codes & 0x7F] * np.where(codes & 0x80, -1.0, 1.0)
+    s = np.repeat(np.repeat(scales.astype(np.float64), block_rows, axis=0), block_cols, axis=1)
+    return vals * s[: codes.shape[0], : codes.shape[1]]
+
+
+def gemm_blockscale(a_bits: np.ndarray, w_bits: np.ndarray) -> Dict[str, np.ndarray]:
+    """C [M, N] = A^ W^^T with A [M, K] in 1x128 groups and W [N, K] in 128x128
+    blocks (both bf16 in, quantised here)."""
+    ac, as_ = quantize_blockscale(a_bits, 1)
+    wc, ws = quantize_blockscale(w_bits, 128)
+    c = dequantize_blockscale(ac, as_, 1) @ dequantize_blockscale(wc, ws, 128).T
+    return {"a_codes": ac, "a_scales": as_, "w_codes": wc, "w_scales": ws, "c": c, "c_bf16": round_bf16_bits(c)}
 
 
 def gemm(a_bits: np.ndarray, b_codes: np.ndarray, b_scales: np.ndarray,

@@ -590,3 +590,99 @@ def test_attention_planted_mistakes_are_caught(mistake):
             out[b, h] = (w / w.sum()) @ v
     want = _torch_attention(wl, d, cache, sm)
     assert oracle.rel_l2(out, want) > 1e-3, mistake
+
+
+# ------------------------------------------------------------------ 128x128 block scales (bsgemm)
+def _torch_blockscale(bits, block_rows, block_cols=128):
+    """Codes and scales from torch pieces: block amax in float32, the scale
+    amax / 448 in float32, v / scale in float32, saturated, then torch's
+    float8_e4m3fn conversion (round-to-nearest-even)."""
+    v = torch.from_numpy(oracle.bf16_bits_to_f64(bits)).to(torch.float32)
+    rows, K = v.shape
+    rb = -(-rows // block_rows)
+    pad = torch.zeros(rb * block_rows, K, dtype=torch.float32)
+    pad[:rows] = v
+    blk = pad.reshape(rb, block_rows, K // block_cols, block_cols)
+    amax = blk.abs().amax(dim=(1, 3))
+    scale = torch.where(amax > 0, amax / torch.tensor(448.0, dtype=torch.float32), torch.ones_like(amax))
+    t = blk / scale[:, None, :, None]
+    codes = t.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).reshape(rb * block_rows, K)[:rows]
+    return codes.numpy(), scale.numpy()
+
+
+@pytest.mark.parametrize("rows,K,block_rows,seed", [(3, 256, 1, 1), (130, 384, 128, 2), (256, 128, 128, 3),
+                                                    (5, 512, 1, 4)])
+def test_blockscale_codes_match_torch(rows, K, block_rows, seed):
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal((rows, K)) * np.exp(rng.uniform(-6, 6, size=(rows, 1)))
+    v.reshape(-1)[rng.choice(v.size, 3, replace=False)] = 0.0
+    bits = inputs.bf16_bits_from_f32(v.astype(np.float32))
+    c, s = oracle.quantize_blockscale(bits, block_rows)
+    tc, ts = _torch_blockscale(bits, block_rows)
+    assert np.array_equal(s, ts)
+    assert np.array_equal(c, tc)
+
+
+def test_blockscale_gemm_exact_rational():
+    rng = np.random.default_rng(5)
+    a = inputs.bf16_bits_from_f32(rng.standard_normal((2, 256)).astype(np.float32))
+    w = inputs.bf16_bits_from_f32((rng.standard_normal((130, 256)) * 0.05).astype(np.float32))
+    res = oracle.gemm_blockscale(a, w)
+    table = [Fraction(float(x)) for x in oracle.e4m3_table()]
+    val = lambda code: (-1 if code & 0x80 else 1) * table[code & 0x7F]
+    for m in range(2):
+        for n in (0, 77, 129):
+            exact = Fraction(0)
+            for kb in range(2):
+                dot = sum(val(int(res["a_codes"][m, k])) * val(int(res["w_codes"][n, k]))
+                          for k in range(128 * kb, 128 * kb + 128))
+                exact += Fraction(float(res["a_scales"][m, kb])) * Fraction(float(res["w_scales"][n // 128, kb])) * dot
+            assert abs(float(exact) - res["c"][m, n]) <= 1e-12 * max(abs(float(exact)), 1e-30)
+
+
+def test_blockscale_closed_forms():
+    # a block of exact E4M3 values whose amax is 448 * 2^-3 has scale 2^-3
+    # and round-trips exactly
+    rng = np.random.default_rng(6)
+    table = oracle.e4m3_table()
+    vals = rng.choice(table, size=(1, 128)) * rng.choice([-1.0, 1.0], size=(1, 128))
+    vals[0, 17] = 448.0
+    v = vals * 0.125
+    bits = inputs.bf16_bits_from_f32(v.astype(np.float32))
+    c, s = oracle.quantize_blockscale(bits, 1)
+    assert s[0, 0] == np.float32(0.125)
+    np.testing.assert_array_equal(oracle.dequantize_blockscale(c, s, 1), v)
+    # an all-zero block: scale 1, codes 0
+    z = np.zeros((1, 128), np.uint16)
+    cz, sz = oracle.quantize_blockscale(z, 1)
+    assert sz[0, 0] == 1.0 and np.all(cz == 0)
+    # blocks are independent: changing one 128x128 block leaves the others' bytes
+    w = inputs.bf16_bits_from_f32(rng.standard_normal((256, 256)).astype(np.float32))
+    c1, s1 = oracle.quantize_blockscale(w, 128)
+    w2 = w.copy()
+    w2[200, 200] = inputs.bf16_bits_from_f32(np.array([[1000.0]], np.float32))[0, 0]
+    c2, s2 = oracle.quantize_blockscale(w2, 128)
+    assert np.array_equal(c1[:128], c2[:128]) and np.array_equal(c1[128:, :128], c2[128:, :128])
+    assert s1[1, 1] != s2[1, 1] and np.array_equal(np.delete(s1.ravel(), 3), np.delete(s2.ravel(), 3))
+
+
+@pytest.mark.parametrize("mistake", ["int8_scale", "groups_along_m", "per_tensor"])
+def test_blockscale_planted_mistakes_are_caught(mistake):
+    """Each plausible bug in the scale rule or the block shape, planted here on
+    the CPU, changes the codes the torch pin fixes."""
+    rng = np.random.default_rng(7)
+    v = rng.standard_normal((4, 256)) * np.exp(rng.uniform(-3, 3, size=(4, 1)))
+    bits = inputs.bf16_bits_from_f32(v.astype(np.float32))
+    tc, _ = _torch_blockscale(bits, 1)
+    f = oracle.bf16_bits_to_f64(bits).astype(np.float32)
+    if mistake == "int8_scale":
+        s = np.abs(f.reshape(4, 2, 128)).max(axis=2) / np.float32(127.0)
+        t = f.reshape(4, 2, 128) / s[:, :, None]
+    elif mistake == "groups_along_m":
+        s = np.abs(f).max(axis=0, keepdims=True) / np.float32(448.0)  # one scale per column over the tokens
+        t = (f / s).reshape(4, 2, 128)
+    else:
+        t = (f / (np.abs(f).max() / np.float32(448.0))).reshape(4, 2, 128)
+    t = torch.from_numpy(t.astype(np.float32)).clamp(-448.0, 448.0)
+    codes = t.to(torch.float8_e4m3fn).view(torch.uint8).reshape(4, 256).numpy()
+    assert np.mean(codes != tc) > 0.05, mistake
