@@ -291,6 +291,25 @@ class MlpBench:
         return e0.elapsed_time(e1) / 1e3, nbytes, self.y.numel() * 2
 
 
+def max_over_ranks(dt, world, device=None):
+    """The job's time: the slowest rank's (a MAX all-reduce, then a barrier);
+    every rank gets it.  One rank: dt itself."""
+    if world <= 1:
+        return dt
+    import torch
+
+    t = torch.tensor([dt], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.barrier()
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_step, steps, dt):
+    """Whole-job throughput: every replica processes its own batch of
+    tokens_per_step tokens per step (weak scaling), timed by the slowest."""
+    return world * tokens_per_step * steps / dt
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -317,23 +336,19 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     dt, (h0, h1) = bench.timed(args.steps, not args.unfused, args.warmup, stream)
-    if world > 1:
-        t = torch.tensor([dt], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
-        torch.distributed.barrier()
+    dt = max_over_ranks(dt, world, device)
     time.sleep(0.1)
     sampler.stop()
     clocks = sampler.summary(h0, h1)
 
     t_launch = bench.per_launch(min(args.steps, 200), stream)
     ms_per_step = dt / args.steps * 1e3
-    value = world * M * args.steps / dt
+    value = job_tokens_per_s(world, M, args.steps, dt)
     achieved = B / t_launch / 1e9
 
     n_e2e = min(args.steps, 5000)
     e2e_t, h2d, d2h = bench.e2e(n_e2e, args.warmup, stream)
-    e2e_val = world * M * n_e2e / e2e_t
+    e2e_val = job_tokens_per_s(world, M, n_e2e, max_over_ranks(e2e_t, world, device))
 
     traffic, traffic_src = ncu_traffic(wl.name)
     out = {
