@@ -39,11 +39,10 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes per launch of the fused kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum, mean of the captured launches) from ncu captures, by
-# workload, with the sha256 prefix of the kernel sources they were taken on:
-# reported only while those sources are unchanged (summaries under profiles/).
-NCU_TRAFFIC = {"m16": ("9f50bc4370878cfc", 80.53e6, "profiles/mx_persistent_kernel_m16_memory.md "
-                       "(non-cluster launch form, FSOPS_PAIRS=0: ncu cannot launch the 2-block-cluster form)"),
-               "m128": ("9f50bc4370878cfc", 163.86e6, "profiles/mx_persistent_kernel_m128_memory.md")}
+# workload: the sha256 prefix of the kernel sources they were taken on (the
+# number is reported only while those sources are unchanged), the bytes, the
+# launch form captured and the summary under profiles/.
+NCU_TRAFFIC = {}
 KERNEL_SOURCES = ("mx_kernels.cu", "mx_internal.h", "mx_mxfp8.cuh", "sm103.cuh")
 
 
@@ -59,9 +58,9 @@ def kernel_sources_hash():
 
 def ncu_traffic(workload):
     rec = NCU_TRAFFIC.get(workload)
-    if rec is None or rec[0] != kernel_sources_hash():
+    if rec is None or rec["sha"] != kernel_sources_hash():
         return None, None
-    return rec[1], rec[2]
+    return rec["bytes"], "%s; launch form: %s" % (rec["source"], rec["form"])
 
 
 def fp8_peak_tflops():
@@ -344,7 +343,10 @@ def run_ours(args, rank, world, local_rank):
     t_launch = bench.per_launch(min(args.steps, 200), stream)
     ms_per_step = dt / args.steps * 1e3
     value = job_tokens_per_s(world, M, args.steps, dt)
-    achieved = B / t_launch / 1e9
+    # the dominant (and, fused, the only) kernel of a step: its average
+    # duration over the timed region is the region's time over its launches
+    t_kernel = dt / args.steps / (3 if args.unfused else 1)
+    achieved = B / (dt / args.steps) / 1e9
 
     n_e2e = min(args.steps, 5000)
     e2e_t, h2d, d2h = bench.e2e(n_e2e, args.warmup, stream)
@@ -365,9 +367,14 @@ def run_ours(args, rank, world, local_rank):
         "weight_GBps": round(value / world / M * wl.weight_bytes / 1e9, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic, "traffic_source": traffic_src,
-                     "peak_kind": peak_kind,
-                     "kernel": "mx_persistent_kernel (fused MLP)", "bytes_per_launch": B,
-                     "launch_us": round(t_launch * 1e6, 3)},
+                     "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+                     "kernel": decode_kernel_name(fs, M) + (" (three-launch path)" if args.unfused else ""),
+                     "bytes_per_launch": B,
+                     "achieved_from": "bytes_per_launch / (timed region / steps): CUDA events around the "
+                                      "graph replays of the timed region",
+                     "kernel_us_in_timed_region": round(t_kernel * 1e6, 3),
+                     "single_launch_us_event_bracketed": round(t_launch * 1e6, 3),
+                     "single_launch_frac": round(B / t_launch / 1e9 / hbm_peak, 4)},
         "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "api": "fsops_mxfp8_swiglu_mlp via ctypes, pinned host buffers"},
         "gpu_launches": args.steps * (3 if args.unfused else 1),
@@ -375,6 +382,7 @@ def run_ours(args, rank, world, local_rank):
     }
     if rank == 0 and not args.no_sweep:
         out["sweep"] = sweep(fs, device, stream, hbm_peak, args)
+        out["sweep_c5"] = sweep_c5(fs, device, stream, hbm_peak)
         out["prefill_gemm"] = prefill_gemm(fs, stream)
         out["attention_decode"] = attention_decode(fs, stream, hbm_peak)
     if rank == 0 and not args.no_cpu:
@@ -422,6 +430,91 @@ def sweep(fs, device, stream, hbm_peak, args):
         res[name] = entry
         del b
         torch.cuda.empty_cache()
+    return res
+
+
+def decode_kernel_name(fs, M):
+    """The kernel the fused MLP call runs for M tokens."""
+    return "mx_persistent_kernel (fused MLP, one launch)" if M <= 128 else "mx_gemm_tiled_kernel (3 launches)"
+
+
+def gemm_bytes(M, N, K):
+    """Algorithmic bytes of one GEMM call: B codes + scales, bf16 A in, bf16 C out."""
+    return N * K + N * K // 32 + 2 * M * K + 2 * M * N
+
+
+def sweep_c5(fs, device, stream, hbm_peak, Ms=None):
+    """The H = 5120, I = 17408 sweep over M in {1, 2, 4, 8, 16, 32, 64, 128}
+    (16 distinct layers, 1% all-zero 32-blocks): the standalone GEMM entry
+    point on the gate/up (N = 2I, K = H) and down (N = H, K = I) shapes, and
+    the fused and three-launch MLP, each timed as CUDA-graph replays that
+    rotate over the 16 layers (4.4 GB of weights, far beyond L2)."""
+    import torch
+
+    from workloads import inputs
+
+    wl = inputs.WORKLOADS["sweep"]
+    H, I, L = wl.H, wl.I, wl.layers
+    layers = []
+    for layer in range(L):
+        wg, wu, wd = inputs.make_layer_torch(wl, layer, device)
+        layers.append(fs.prepare_mlp_weights(wg, wu, wd))
+        del wg, wu, wd
+    torch.cuda.synchronize()
+    res = {"H": H, "I": I, "layers": L, "weight_bytes_per_layer": wl.weight_bytes,
+           "timing": "CUDA graph replays rotating over the 16 layers; us per call"}
+    Ms = Ms or wl.M_sweep
+    for M in Ms:
+        x = inputs.make_activations_torch(wl, M, device)
+        h_in = inputs.make_activations_torch(inputs.Workload("h", M, I, H, 1, wl.seed + 1), M, device)
+        y = torch.empty(M, H, dtype=torch.bfloat16, device=device)
+        cgu = torch.empty(M, 2 * I, dtype=torch.bfloat16, device=device)
+        ws = fs.Workspace(M, H, I, device=device)
+        gws_n = max(fs.fsops_gemm_workspace_bytes(M, 2 * I, H), fs.fsops_gemm_workspace_bytes(M, H, I))
+        gws = torch.zeros(gws_n, dtype=torch.uint8, device=device)
+        s = stream.cuda_stream
+        calls = {
+            "gemm_gateup": (lambda w: fs.fsops_mxfp8_gemm(x, w.gateup_codes, w.gateup_scales, cgu, M, 2 * I, H, gws,
+                                                          gws_n, stream=s), gemm_bytes(M, 2 * I, H), 2.0 * M * 2 * I * H),
+            "gemm_down": (lambda w: fs.fsops_mxfp8_gemm(h_in, w.down_codes, w.down_scales, y, M, H, I, gws, gws_n,
+                                                        stream=s), gemm_bytes(M, H, I), 2.0 * M * H * I),
+            "mlp_fused": (lambda w: fs.fsops_mxfp8_swiglu_mlp(x, w.gateup_codes, w.down_codes, w.scales, y, M, H, I,
+                                                              stream=s), algorithmic_bytes(M, H, I),
+                          2.0 * M * 3 * H * I),
+            "mlp_unfused_3_launches": (lambda w: fs.fsops_mxfp8_swiglu_mlp_unfused(
+                x, w.gateup_codes, w.down_codes, w.scales, y, M, H, I, stream=s), algorithmic_bytes(M, H, I),
+                2.0 * M * 3 * H * I),
+        }
+        entry = {}
+        for name, (fn, nbytes, flops) in calls.items():
+            n = 4 * L
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    fn(layers[i % L])
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(n):
+                        fn(layers[i % L])
+                g.replay()
+                stream.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(3):
+                    g.replay()
+                e1.record(stream)
+                e1.synchronize()
+            t = e0.elapsed_time(e1) / 1e3 / (3 * n)
+            entry[name] = {"us_per_call": round(t * 1e6, 3), "GBps": round(nbytes / t / 1e9, 1),
+                           "frac_hbm": round(nbytes / t / 1e9 / hbm_peak, 4),
+                           "TFLOPs": round(flops / t / 1e12, 1)}
+            if name.startswith("mlp"):
+                entry[name]["tokens_per_s"] = round(M / t, 1)
+            del g
+        res["M%d" % M] = entry
+        del x, h_in, y, cgu, ws, gws
+        torch.cuda.empty_cache()
+    del layers
+    torch.cuda.empty_cache()
     return res
 
 

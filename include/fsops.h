@@ -88,6 +88,24 @@ typedef struct {
 fsops_status fsops_quantize_mxfp8(const void* x_bf16, int rows, int K, int ld, uint8_t* codes,
                                   uint8_t* scales, fsops_scale_layout layout, void* stream);
 
+/* fsops_quantize_mxfp8_gateup -- W_gate and W_up (bf16) to the MXFP8 W_gateup
+ * that fsops_mxfp8_swiglu_mlp reads, in one launch: the rows are quantised
+ * along H with the rule above and written in the paired order (rows
+ * 128j..128j+63 from W_gate rows 64j..64j+63, rows 128j+64..128j+127 from
+ * W_up rows 64j..64j+63), with TCGEN05 scales.  The pages do not say how
+ * gate and up are stored; pairing keeps the gate and up sums of a feature in
+ * one accumulator tile, and doing it here keeps a caller from handing over a
+ * stacked [W_gate; W_up], which the MLP would not detect (p2 "Estrategia de
+ * cuantizacion FP8": a weight layout mismatch gives wrong values at full
+ * speed).
+ *   w_gate_bf16, w_up_bf16  [I, ld] bf16 each, the first H columns used;
+ *                           ld % 8 == 0.
+ *   codes   [2I, H] E4M3;  scales fsops_scale_bytes(2I, H, TCGEN05) bytes.
+ *   I % 64 == 0, H % 128 == 0, 2I * H < 2^31.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA. */
+fsops_status fsops_quantize_mxfp8_gateup(const void* w_gate_bf16, const void* w_up_bf16, int I, int H, int ld,
+                                         uint8_t* codes, uint8_t* scales, void* stream);
+
 /* Size in bytes of a scale buffer for a [rows, K] matrix (0 for an invalid layout). */
 size_t fsops_scale_bytes(int rows, int K, fsops_scale_layout layout);
 
@@ -262,21 +280,35 @@ fsops_status fsops_mxfp8_swiglu_mlp_unfused(const void* x_bf16, const uint8_t* w
  * of fsops_mxfp8_swiglu_mlp.
  *   Arguments, layouts and limits as fsops_mxfp8_swiglu_mlp, with M <= 128
  *   only (the single-launch path; larger M is FSOPS_ERR_UNSUPPORTED_SHAPE),
- *   and no workspace is used: the scratch is one fixed 8 MiB buffer per device inside
- *   the library's device image, present from library load until process exit.
- *   A shape whose scratch does not fit in 8 MiB is rejected with
- *   FSOPS_ERR_UNSUPPORTED_SHAPE before anything is launched (with one gate/up
- *   tile per block it needs about 16 KiB + M*(H+I) bytes + 1 KiB*M*ceil(H/256)).
+ *   and no workspace is used: the scratch is one fixed 8 MiB buffer per device
+ *   inside the library's device image, present from library load until
+ *   process exit.  A shape whose scratch does not fit in 8 MiB is rejected
+ *   with FSOPS_ERR_UNSUPPORTED_SHAPE before anything is launched.  The scratch
+ *   is 16 KiB + M * (H + I) bytes (quantised x and h) + about
+ *   (H + I) * 4 bytes of scales + the split-K sums: 1 KiB * M * ceil(H / TR1)
+ *   for the down projection, with TR1 = 128 for M > 64 and 256 otherwise,
+ *   plus 1 KiB * M * (2 I / 256) for M <= 32 (split gate/up tiles).  Example:
+ *   M = 128, H = 4096, I = 12288 needs about 6.1 MiB.
  *   The first call on a device looks up the buffer's device address
- *   (cudaGetSymbolAddress); make that first call outside any stream capture.
- *   Each call clears the counters and accumulators it needs with
- *   cudaMemsetAsync on `stream`, then launches the kernel; neither step
- *   allocates.  All calls on a device share the one buffer, so calls whose
- *   execution overlaps on the GPU (different streams without ordering) race;
- *   order them. */
+ *   (cudaGetSymbolAddress) and clears the buffer (cudaMemsetAsync on
+ *   `stream`); make that first call outside any stream capture.  A launch
+ *   that succeeds leaves the buffer ready for the next call, so later calls
+ *   only launch the kernel; the buffer is cleared again before the next call
+ *   after a call that failed, or after fsops_read_noalloc_status reported a
+ *   kernel error.  Neither step allocates.  All calls on a device share the
+ *   one buffer, so calls whose execution overlaps on the GPU (different
+ *   streams without ordering) race; order them. */
 fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w_gateup,
                                             const uint8_t* w_down, const fsops_mlp_scales* scales,
                                             void* y_bf16, int M, int H, int I, void* stream);
+
+/* fsops_read_noalloc_status -- the status word of the fixed buffer of
+ * fsops_mxfp8_swiglu_mlp_noalloc on the current device, read and cleared
+ * like fsops_read_kernel_status (synchronises the device).  A nonzero word
+ * (a kernel wait that ran out) also makes the next no-allocation call clear
+ * the buffer first.  INVALID_ARG before the first no-allocation call on the
+ * device. */
+fsops_status fsops_read_noalloc_status(uint32_t* word);
 
 /* Workspace bytes the MLP entry points need on the current device (0 if the
  * shape is unsupported).  It covers the unfused path's fp32 [M, 2I]
@@ -309,6 +341,39 @@ fsops_status fsops_set_wait_timeout_ns(uint64_t ns);
  * SwiGLU tiles) than any launch produces, so those waits run out and report
  * FSOPS_ERR_TIMEOUT.  0 (the default) disables it. */
 fsops_status fsops_debug_set_extra_arrivals(uint32_t n);
+
+/* Plan overrides for tests and tuning (fsops_debug_set_knob).  Each knob
+ * holds -1 (the default: the library picks) or a forced value; a forced value
+ * that a shape cannot use is ignored for that call.  They apply to calls made
+ * after the change, in every thread of the process.
+ *   TR0, TR1          weight tile rows of the gate/up and down phases of the
+ *                     single-launch MLP on the grid-wide path: 128 or 256.
+ *   WHOLE_TILES       1: one whole gate/up tile per block; 0: split-K.
+ *   PAIRS             0: no 2-block cluster split of gate/up tiles.
+ *   GEMM_FORM         tiled GEMM above 128 rows: 0 one block per 128 x 256
+ *                     tile, 1 a 2-block cluster per 256 x 256 tile
+ *                     (cta_group::2 MMA; N % 256 == 0, two or more row tiles).
+ *   PRIME             weight loads in flight before the activations exist.
+ *   MAX_INFLIGHT      weight loads in flight per block (1..8).
+ *   LOCAL_XQ          0: quantise x grid-wide even for M <= 16.
+ *   DECODE_PATH       M <= 32: 0 the grid-wide two-phase kernel, 1 the
+ *                     cluster-sliced kernel. */
+typedef enum {
+  FSOPS_KNOB_TR0 = 0,
+  FSOPS_KNOB_TR1 = 1,
+  FSOPS_KNOB_WHOLE_TILES = 2,
+  FSOPS_KNOB_PAIRS = 3,
+  FSOPS_KNOB_GEMM_FORM = 4,
+  FSOPS_KNOB_PRIME = 5,
+  FSOPS_KNOB_MAX_INFLIGHT = 6,
+  FSOPS_KNOB_LOCAL_XQ = 7,
+  FSOPS_KNOB_DECODE_PATH = 8,
+  FSOPS_KNOB_COUNT = 9
+} fsops_knob;
+
+/* Set knob `knob` (an fsops_knob) to `value` (negative = back to the
+ * default).  INVALID_ARG for an unknown knob. */
+fsops_status fsops_debug_set_knob(int knob, int value);
 
 const char* fsops_status_string(fsops_status s);
 

@@ -21,10 +21,11 @@ from . import build as _build
 __all__ = [
     "FsopsError", "lib", "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_CUDA",
     "ERR_TIMEOUT", "ERR_NO_DEVICE", "SCALES_ROWMAJOR", "SCALES_TCGEN05", "DTYPE_BF16", "DTYPE_F32",
-    "DTYPE_MXFP8", "fsops_quantize_mxfp8", "fsops_scale_bytes", "fsops_mxfp8_gemm", "fsops_mxfp8_gemm_ex",
+    "DTYPE_MXFP8", "fsops_quantize_mxfp8", "fsops_quantize_mxfp8_gateup", "fsops_scale_bytes", "fsops_mxfp8_gemm", "fsops_mxfp8_gemm_ex",
     "fsops_gemm_workspace_bytes", "fsops_swiglu_quantize_mxfp8", "fsops_mxfp8_swiglu_mlp",
     "fsops_mxfp8_swiglu_mlp_unfused", "fsops_mxfp8_swiglu_mlp_noalloc", "fsops_mlp_workspace_bytes", "fsops_set_workspace",
     "fsops_read_kernel_status", "fsops_set_wait_timeout_ns", "fsops_debug_set_extra_arrivals",
+    "fsops_debug_set_knob", "KNOBS", "fsops_read_noalloc_status",
     "fsops_status_string", "fsops_version", "fsops_last_cuda_error", "fsops_rmsnorm_quantize_mxfp8",
     "fsops_mxfp8_swiglu_mlp_block", "fsops_mxfp8_paged_decode_attention", "fsops_paged_attention_workspace_bytes",
     "quantize_weight", "MLPWeights", "prepare_mlp_weights",
@@ -33,6 +34,9 @@ __all__ = [
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_CUDA, ERR_TIMEOUT, ERR_NO_DEVICE = range(7)
 SCALES_ROWMAJOR, SCALES_TCGEN05 = 0, 1
+# fsops_knob values (include/fsops.h)
+KNOBS = {"TR0": 0, "TR1": 1, "WHOLE_TILES": 2, "PAIRS": 3, "GEMM_FORM": 4, "PRIME": 5, "MAX_INFLIGHT": 6,
+         "LOCAL_XQ": 7, "DECODE_PATH": 8}
 DTYPE_BF16, DTYPE_F32, DTYPE_MXFP8 = 0, 1, 2
 
 if not os.path.exists(_build.LIB):
@@ -50,6 +54,7 @@ class _MlpScales(ctypes.Structure):
 _SIGS = {
     "fsops_quantize_mxfp8": ([_vp, _i, _i, _i, _vp, _vp, _i, _vp], _i),
     "fsops_scale_bytes": ([_i, _i, _i], _sz),
+    "fsops_quantize_mxfp8_gateup": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
     "fsops_mxfp8_gemm": ([_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp], _i),
     "fsops_mxfp8_gemm_ex": ([_vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp], _i),
     "fsops_gemm_workspace_bytes": ([_i, _i, _i], _sz),
@@ -66,8 +71,10 @@ _SIGS = {
     "fsops_mlp_workspace_bytes": ([_i, _i, _i], _sz),
     "fsops_set_workspace": ([_vp, _sz], _i),
     "fsops_read_kernel_status": ([_vp, ctypes.POINTER(_u32)], _i),
+    "fsops_read_noalloc_status": ([ctypes.POINTER(_u32)], _i),
     "fsops_set_wait_timeout_ns": ([_u64], _i),
     "fsops_debug_set_extra_arrivals": ([_u32], _i),
+    "fsops_debug_set_knob": ([_i, _i], _i),
     "fsops_status_string": ([_i], ctypes.c_char_p),
     "fsops_version": ([], _i),
     "fsops_last_cuda_error": ([], _i),
@@ -115,6 +122,11 @@ def _stream(stream) -> Optional[int]:
 def fsops_quantize_mxfp8(x, rows: int, K: int, ld: int, codes, scales, layout: int, stream=None) -> None:
     _check(lib.fsops_quantize_mxfp8(_ptr(x), rows, K, ld, _ptr(codes), _ptr(scales), layout, _stream(stream)),
            "fsops_quantize_mxfp8")
+
+
+def fsops_quantize_mxfp8_gateup(w_gate, w_up, I: int, H: int, ld: int, codes, scales, stream=None) -> None:
+    _check(lib.fsops_quantize_mxfp8_gateup(_ptr(w_gate), _ptr(w_up), I, H, ld, _ptr(codes), _ptr(scales),
+                                           _stream(stream)), "fsops_quantize_mxfp8_gateup")
 
 
 def fsops_rmsnorm_quantize_mxfp8(x, gamma, eps: float, rows: int, K: int, ld: int, codes, scales, layout: int,
@@ -217,12 +229,24 @@ def fsops_read_kernel_status(workspace=None) -> int:
     return w.value
 
 
+def fsops_read_noalloc_status() -> int:
+    w = _u32(0)
+    _check(lib.fsops_read_noalloc_status(ctypes.byref(w)), "fsops_read_noalloc_status")
+    return w.value
+
+
 def fsops_set_wait_timeout_ns(ns: int) -> None:
     _check(lib.fsops_set_wait_timeout_ns(ns), "fsops_set_wait_timeout_ns")
 
 
 def fsops_debug_set_extra_arrivals(n: int) -> None:
     _check(lib.fsops_debug_set_extra_arrivals(n), "fsops_debug_set_extra_arrivals")
+
+
+def fsops_debug_set_knob(knob, value: int) -> None:
+    """Force a plan knob (a name of ``KNOBS`` or its number); -1 restores the default."""
+    k = KNOBS[knob] if isinstance(knob, str) else int(knob)
+    _check(lib.fsops_debug_set_knob(k, int(value)), "fsops_debug_set_knob")
 
 
 def fsops_status_string(s: int) -> str:
@@ -267,8 +291,10 @@ PAIR_ROWS = 64
 
 
 def pair_gate_up(w_gate, w_up):
-    """The row order the library expects for W_gateup: 128-row block j holds
-    W_gate rows 64j..64j+63 followed by W_up rows 64j..64j+63."""
+    """The row order of W_gateup as a bf16 tensor (for inspection and tests;
+    ``prepare_mlp_weights`` quantises straight into this order on the device):
+    128-row block j holds W_gate rows 64j..64j+63 followed by W_up rows
+    64j..64j+63."""
     import torch
 
     I, H = w_gate.shape
@@ -277,10 +303,18 @@ def pair_gate_up(w_gate, w_up):
 
 
 def prepare_mlp_weights(w_gate, w_up, w_down, stream=None) -> MLPWeights:
-    """bf16 CUDA tensors W_gate [I, H], W_up [I, H], W_down [H, I] -> MLPWeights."""
+    """bf16 CUDA tensors W_gate [I, H], W_up [I, H], W_down [H, I] -> MLPWeights
+    (W_gateup quantised into the paired row order by fsops_quantize_mxfp8_gateup)."""
+    import torch
+
     I, H = w_gate.shape
-    gu = pair_gate_up(w_gate, w_up)
-    gc, gs = quantize_weight(gu, SCALES_TCGEN05, stream)
+    if w_up.shape != (I, H) or w_down.shape != (H, I):
+        raise ValueError("W_gate, W_up must be [I, H] and W_down [H, I]")
+    if w_gate.stride(1) != 1 or w_up.stride(1) != 1 or w_gate.stride(0) != w_up.stride(0):
+        w_gate, w_up = w_gate.contiguous(), w_up.contiguous()
+    gc = torch.empty((2 * I, H), dtype=torch.uint8, device=w_gate.device)
+    gs = torch.empty(fsops_scale_bytes(2 * I, H, SCALES_TCGEN05), dtype=torch.uint8, device=w_gate.device)
+    fsops_quantize_mxfp8_gateup(w_gate, w_up, I, H, w_gate.stride(0), gc, gs, stream)
     dc, ds = quantize_weight(w_down.contiguous(), SCALES_TCGEN05, stream)
     return MLPWeights(gc, gs, dc, ds, H, I)
 

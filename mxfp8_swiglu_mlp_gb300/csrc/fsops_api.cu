@@ -45,11 +45,28 @@ std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 unsigned long long* g_trace = nullptr;
 #endif
 std::atomic<uint32_t> g_extra{0};
-// Weight tiles (32 KB each) a block keeps in flight: 4 x 32 KB per SM covers
-// the loaded HBM latency (~1.5 us) at the SM's share of the bandwidth even
-// when only half the SMs stream; deeper queues only add latency to every other
-// memory round trip.
-std::atomic<int> g_max_inflight{4};
+// Weight tiles (32 KB each) a block keeps in flight by default: 4 x 32 KB per
+// SM covers the loaded HBM latency (~1.5 us) at the SM's share of the
+// bandwidth even when only half the SMs stream; deeper queues only add latency
+// to every other memory round trip.
+constexpr int kDefaultMaxInflight = 4;
+// Plan overrides set through fsops_debug_set_knob (-1: the library's own
+// choice).  Read with one atomic load per use; nothing is read from the
+// process environment on the call path.
+std::atomic<int> g_knob[FSOPS_KNOB_COUNT];
+struct KnobInit {
+  KnobInit() {
+    for (auto& k : g_knob) k.store(-1);
+  }
+} g_knob_init;
+int knob(fsops_knob k) { return g_knob[k].load(std::memory_order_relaxed); }
+// The knob's value when it is one of the accepted ones, else `dflt`.
+int knob_or(fsops_knob k, int dflt, int lo, int hi) {
+  const int v = knob(k);
+  return (v >= lo && v <= hi) ? v : dflt;
+}
+// FSOPS_VERBOSE, read once when the library is loaded.
+const bool g_verbose = std::getenv("FSOPS_VERBOSE") != nullptr;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 fsops_status current_device(int* dev_out, const DeviceInfo** info) {
@@ -69,11 +86,6 @@ fsops_status current_device(int* dev_out, const DeviceInfo** info) {
       d.sms = sms < 256 ? sms : 256;  // one block per SM; the split arithmetic assumes at most 256
     }
     cudaGetLastError();
-    // tuning knob: weight tiles in flight per block (FSOPS_MAX_INFLIGHT=1..12)
-    if (const char* env = std::getenv("FSOPS_MAX_INFLIGHT")) {
-      const int v = std::atoi(env);
-      if (v >= 1 && v <= kMaxStages) g_max_inflight.store(v);
-    }
     if (g_encode == nullptr) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -96,7 +108,7 @@ thread_local int g_last_cuda_error = 0;
 fsops_status cuda_failed(cudaError_t e, const char* where) {
   cudaGetLastError();
   g_last_cuda_error = static_cast<int>(e);
-  if (std::getenv("FSOPS_VERBOSE") != nullptr)
+  if (g_verbose)
     std::fprintf(stderr, "fsops: %s failed: %s (%d)\n", where, cudaGetErrorString(e), static_cast<int>(e));
   return FSOPS_ERR_CUDA;
 }
@@ -112,8 +124,8 @@ int stage_tmem_for(int npad) { return npad <= 32 ? 1 : 0; }
 // grid-wide exchange before the first MMA; one warp, two 32-blocks per lane per
 // stage).  Larger M: x is quantised once, each block a slice, shared through L2.
 int local_xq_for(int npad) {
-  if (const char* env = std::getenv("FSOPS_LOCAL_XQ")) return std::atoi(env) != 0 && npad <= 16;
-  return npad <= 16 ? 1 : 0;
+  if (npad > 16) return 0;
+  return knob_or(FSOPS_KNOB_LOCAL_XQ, 1, 0, 1);
 }
 // Shared memory besides the stage ring (local_xq is only used with x quantised in-kernel).
 uint32_t extra_smem(int npad, int local_xq) {
@@ -198,19 +210,10 @@ struct MlpPlan {
   int whole0;    // 1: one whole gate/up tile per block, no split-K before the SwiGLU
   int pairs0;    // 1: the two blocks of a cluster split a gate/up tile and add through shared memory
 };
-int env_int(const char* name, int dflt, int lo, int hi) {
-  if (const char* env = std::getenv(name)) {
-    const int v = std::atoi(env);
-    if (v >= lo && v <= hi) return v;
-  }
-  return dflt;
-}
-int env_choice(const char* name, int dflt, int a, int b) {
-  if (const char* env = std::getenv(name)) {
-    const int v = std::atoi(env);
-    if (v == a || v == b) return v;
-  }
-  return dflt;
+// 128 or 256 from the knob, else `dflt`.
+int tile_rows_knob(fsops_knob k, int dflt) {
+  const int v = knob(k);
+  return (v == 128 || v == 256) ? v : dflt;
 }
 MlpPlan plan_mlp(int M, int H, int I, int grid) {
   MlpPlan pl;
@@ -221,23 +224,23 @@ MlpPlan plan_mlp(int M, int H, int I, int grid) {
   // the tiles are split over all blocks, whose staged reduction is cheap and
   // which each quantise only their half of x.  (128-row whole tiles would
   // need no reduction either, but every block would quantise all of x.)
-  pl.TR0 = env_choice("FSOPS_TR0", 256, 128, 256);
+  pl.TR0 = tile_rows_knob(FSOPS_KNOB_TR0, 256);
   pl.T0 = 2 * I / pl.TR0;
   pl.whole0 = (pl.T0 <= grid && !staged) ? 1 : 0;
-  if (const char* env = std::getenv("FSOPS_WHOLE_TILES")) pl.whole0 = (std::atoi(env) != 0 && pl.T0 <= grid) ? 1 : 0;
+  if (knob(FSOPS_KNOB_WHOLE_TILES) >= 0) pl.whole0 = (knob(FSOPS_KNOB_WHOLE_TILES) != 0 && pl.T0 <= grid) ? 1 : 0;
   // M <= 32 with between a quarter and a half as many 256-row gate/up tiles
   // as blocks: each tile goes to one 2-block cluster, whose blocks take a K
   // half each and add their sums through distributed shared memory (no L2
   // reduction before the SwiGLU).  The launch falls back to the split over
   // all blocks when the device cannot hold grid / 2 such clusters at once.
   pl.pairs0 = (staged && !pl.whole0 && pl.TR0 == 256 && grid % 2 == 0 && 4 * pl.T0 > grid && 2 * pl.T0 <= grid &&
-               env_int("FSOPS_PAIRS", 1, 0, 1))
+               knob_or(FSOPS_KNOB_PAIRS, 1, 0, 1))
                   ? 1
                   : 0;
   // down projection: with M > 64, 128-row tiles halve the split-K sums the
   // blocks add up in L2 (each tile is split over half as many blocks), which
   // outweighs their halved loads per stage
-  pl.TR1 = env_choice("FSOPS_TR1", npad > 64 ? 128 : 256, 128, 256);
+  pl.TR1 = tile_rows_knob(FSOPS_KNOB_TR1, npad > 64 ? 128 : 256);
   pl.T1 = (H + pl.TR1 - 1) / pl.TR1;
   return pl;
 }
@@ -272,8 +275,9 @@ void init_common(KernelArgs& a, int M, uint32_t* ctl) {
   a.npad = npad_of(M);
   a.nstages = stages_for(a.npad, 0);  // set again once local_xq is known
   a.stage_tmem = stage_tmem_for(a.npad);
-  a.max_inflight = g_max_inflight.load() < a.nstages ? g_max_inflight.load() : a.nstages;
-  a.prime_inflight = env_int("FSOPS_PRIME", kPrimeInflight, 1, kMaxStages);
+  const int inflight = knob_or(FSOPS_KNOB_MAX_INFLIGHT, kDefaultMaxInflight, 1, kMaxStages);
+  a.max_inflight = inflight < a.nstages ? inflight : a.nstages;
+  a.prime_inflight = knob_or(FSOPS_KNOB_PRIME, kPrimeInflight, 1, kMaxStages);
   a.stage_bytes = stage_bytes_for(a.npad);
   a.timeout_ns = g_timeout_ns.load();
   a.extra_xready = g_extra.load();
@@ -390,14 +394,12 @@ bool gemm_shape_ok(int M, int N, int K) {
 fsops_status fill_tiled(TiledArgs& ta, const uint8_t* codes, const uint8_t* sfa, const uint8_t* b_codes,
                         const uint8_t* b_scales, int M, int N, int K, uint8_t* ctl, const DeviceInfo* di) {
   std::memset(&ta, 0, sizeof(ta));
-  // With two or more row tiles, 2-block clusters on vertically adjacent
-  // tiles: the default multicasts half of each B stage into both blocks
-  // (FSOPS_GEMM_FORM=1); FSOPS_GEMM_FORM=2 runs the pair as one 256-row
-  // cta_group::2 MMA (N % 256 == 0); 0 forces one block per tile.
+  // One block per 128 x 256 tile by default.  FSOPS_KNOB_GEMM_FORM = 1 runs
+  // 2-block clusters on vertically adjacent row tiles as one 256-row
+  // cta_group::2 MMA (N % 256 == 0, two or more row tiles).
   const int MT = (M + 127) / 128;
-  const int want = env_int("FSOPS_GEMM_FORM", kTiledMulticast, kTiledSingle, kTiledPairMma);
-  ta.form = (MT < 2 || di->sms < 2) ? kTiledSingle : want;
-  if (ta.form == kTiledPairMma && N % 256 != 0) ta.form = kTiledMulticast;
+  ta.form = knob_or(FSOPS_KNOB_GEMM_FORM, kTiledSingle, kTiledSingle, kTiledPairMma);
+  if (MT < 2 || di->sms < 2 || N % 256 != 0) ta.form = kTiledSingle;
   if (!encode_map(&ta.tm_a, codes, K, M, 128) ||
       !encode_map(&ta.tm_b, b_codes, K, N, ta.form == kTiledSingle ? 256 : 128))
     return FSOPS_ERR_INVALID_ARG;
@@ -579,6 +581,23 @@ fsops_status fsops_quantize_mxfp8(const void* x_bf16, int rows, int K, int ld, u
   if (st != FSOPS_OK) return st;
   cudaError_t e = launch_quantize(static_cast<const uint16_t*>(x_bf16), rows, K, ld, codes, scales,
                                   layout == FSOPS_SCALES_TCGEN05 ? 1 : 0, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "quantize_kernel launch");
+}
+
+fsops_status fsops_quantize_mxfp8_gateup(const void* w_gate_bf16, const void* w_up_bf16, int I, int H, int ld,
+                                         uint8_t* codes, uint8_t* scales, void* stream) {
+  if (I < 64 || I % 64 != 0 || H < 128 || H % 128 != 0 || ld < H || ld % 8 != 0) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(I) * ld >= (1LL << 31) || static_cast<long long>(2 * I) * H >= (1LL << 31))
+    return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (w_gate_bf16 == nullptr || w_up_bf16 == nullptr || codes == nullptr || scales == nullptr)
+    return FSOPS_ERR_INVALID_ARG;
+  if (!aligned16(w_gate_bf16) || !aligned16(w_up_bf16) || !aligned16(codes)) return FSOPS_ERR_MISALIGNED;
+  int dev;
+  const DeviceInfo* di;
+  fsops_status st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  const cudaError_t e = launch_quantize(static_cast<const uint16_t*>(w_gate_bf16), 2 * I, H, ld, codes, scales, 1,
+                                        static_cast<cudaStream_t>(stream), static_cast<const uint16_t*>(w_up_bf16));
   return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "quantize_kernel launch");
 }
 
@@ -874,6 +893,12 @@ fsops_status fsops_debug_set_extra_arrivals(uint32_t n) {
   return FSOPS_OK;
 }
 
+fsops_status fsops_debug_set_knob(int k, int value) {
+  if (k < 0 || k >= FSOPS_KNOB_COUNT) return FSOPS_ERR_INVALID_ARG;
+  g_knob[k].store(value < 0 ? -1 : value);
+  return FSOPS_OK;
+}
+
 #ifdef FSOPS_TRACE
 // Profiling builds only: device buffer of [grid][64] uint64 timeline stamps.
 fsops_status fsops_debug_set_trace_buffer(void* buf) {
@@ -897,6 +922,12 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = 8u << 20;  // 8 MiB
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 uint8_t* g_noalloc_base[kMaxDevices] = {};
+// Per device: the buffer must be cleared before the next call -- before the
+// first call, after a call that failed on the host, and after
+// fsops_read_noalloc_status found a kernel error (an aborted launch can
+// leave split-K sums behind).  A launch that succeeds leaves its counters and
+// accumulators zero itself, so calls in between need no clearing.
+bool g_noalloc_dirty[kMaxDevices] = {};
 
 // Byte layout inside the fixed buffer: the MLP workspace layout without the
 // three-launch path's fp32 [M, 2I] buffer, and without the gate/up split-K
@@ -916,6 +947,21 @@ NoAllocLayout noalloc_layout(int M, int H, int I, const MlpPlan& pl) {
   l.part1 = l.part0 + (pl.whole0 ? 0 : accum_bytes(M, pl.T0));
   l.end = l.part1 + accum_bytes(M, pl.T1);
   return l;
+}
+
+// Device address of this device's fixed buffer (looked up on first use: the
+// host-side name of a __device__ array is not a device address).
+fsops_status noalloc_base(int dev, uint8_t** base) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_noalloc_base[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return cuda_failed(e, "scratch buffer address");
+    g_noalloc_base[dev] = static_cast<uint8_t*>(p);
+    g_noalloc_dirty[dev] = true;
+  }
+  *base = g_noalloc_base[dev];
+  return FSOPS_OK;
 }
 
 }  // namespace
@@ -938,31 +984,51 @@ fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w
   const NoAllocLayout l = noalloc_layout(M, H, I, pl);
   if (l.end > kNoAllocScratchBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;  // does not fit the fixed buffer
 
-  // First call on this device: look up the device address of the buffer (a
-  // host-side reference to the __device__ array is not a device address).
   uint8_t* ws = nullptr;
+  if ((st = noalloc_base(dev, &ws)) != FSOPS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool dirty;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_noalloc_base[dev] == nullptr) {
-      void* p = nullptr;
-      const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-      if (e != cudaSuccess || p == nullptr) return cuda_failed(e, "scratch buffer address");
-      g_noalloc_base[dev] = static_cast<uint8_t*>(p);
-    }
-    ws = g_noalloc_base[dev];
+    dirty = g_noalloc_dirty[dev];
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the buffer keeps whatever the previous call left: clear the counters, flags
-  // and split-K accumulators the kernel needs to start at zero
-  cudaError_t e = cudaMemsetAsync(ws + l.ctl, 0, kCtlRegionBytes, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(ws + l.part0, 0, l.end - l.part0, s);
-  if (e != cudaSuccess) return cuda_failed(e, "scratch buffer clear");
-
+  if (dirty) {
+    // zero the counters, flags and split-K accumulators the kernel expects at
+    // zero (the whole buffer: a different shape may have used other offsets)
+    const cudaError_t e = cudaMemsetAsync(ws, 0, kNoAllocScratchBytes, s);
+    if (e != cudaSuccess) return cuda_failed(e, "scratch buffer clear");
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_noalloc_dirty[dev] = false;
+  }
   const MlpBuffers bufs{ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.hq, ws + l.hq_sf, ws + l.part0, ws + l.part1};
   KernelArgs ka;
   st = fill_mlp_args(ka, pl, bufs, x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I);
+  if (st == FSOPS_OK) st = launch(ka, grid, s);
+  if (st != FSOPS_OK) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_noalloc_dirty[dev] = true;
+  }
+  return st;
+}
+
+fsops_status fsops_read_noalloc_status(uint32_t* word) {
+  if (word == nullptr) return FSOPS_ERR_INVALID_ARG;
+  int dev;
+  const DeviceInfo* di;
+  fsops_status st = current_device(&dev, &di);
   if (st != FSOPS_OK) return st;
-  return launch(ka, grid, s);
+  uint8_t* base;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    base = g_noalloc_base[dev];
+  }
+  if (base == nullptr) return FSOPS_ERR_INVALID_ARG;  // no no-allocation call on this device yet
+  st = fsops_read_kernel_status(base, word);
+  if (st == FSOPS_OK && *word != 0) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_noalloc_dirty[dev] = true;
+  }
+  return st;
 }
 
 }  // extern "C"

@@ -5,11 +5,10 @@
 //                          (tcgen05 tiled scale layout), fp32 accumulation in
 //                          TMEM, bf16 or fp32 output.
 //
-// One block per SM walks the 128 x 256 output tiles.  With CL = 2 the grid
-// runs as 2-block clusters that take vertically adjacent tiles (rows 256 p ..
-// 256 p + 255, same columns): each block loads its own A box and one half of
-// the shared B box, multicast into both blocks, so the pair reads each B
-// stage once from L2 (a third less operand traffic per block).
+// One block per SM walks the 128 x 256 output tiles.  In the pair form the
+// grid runs as 2-block clusters that compute one 256 x 256 tile with
+// cta_group::2 MMAs: each block loads its own A box and one half of the B box,
+// and the pair's tensor cores read both halves.
 // Warp 0 streams the A (128 x 128 B) and B (256 x 128 B) boxes of each K
 // stage and their scale tiles by TMA into a four-stage ring; warp 1 issues
 // the block-scaled MMAs (four K = 32 steps per stage) into one TMEM
@@ -49,8 +48,6 @@ constexpr uint32_t kTStgBytes = kTEpiWarps * kTChunkBytes;
 // Per launch form: blocks per cluster, pipeline stages and the stage layout.
 //   single     one block per 128 x 256 tile; stage = A 16 KB | B 32 KB |
 //              A scales 512 B | B scales 2 x 512 B.
-//   multicast  2-block clusters on vertically adjacent tiles; each block loads
-//              one 128-row half of the B box and multicasts it into both.
 //   pair MMA   2-block clusters computing one 256 x 256 tile with
 //              cta_group::2 MMAs; each block holds its 128 A rows and its
 //              128-row half of B (the pair's tensor cores read both halves),
@@ -263,9 +260,9 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      // multicast: a stage is free once both blocks' MMAs have consumed it;
-      // pair MMA: once the one pair MMA (committed to both blocks) has
-      mbar_init(&empty[s], FORM == kTiledMulticast ? 2 : 1);
+      // pair MMA: a stage is free once the one pair MMA (committed to both
+      // blocks) has consumed it
+      mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
     // one arrival per epilogue warp (of both blocks for the pair MMA)
@@ -296,7 +293,7 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   // the cluster's barriers are initialised before any block arrives on its
-  // partner's or multicasts into it
+  // partner's
   if (CL > 1) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
   const TWait w{abort_flag, a.status, a.timeout_ns};
@@ -305,7 +302,7 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
   const int first = blockIdx.x / CL;
   const int mrows = (a.MT + CL - 1) / CL;  // row groups of CL tiles
   const int ntiles = mrows * a.NT;
-  const uint16_t all_ctas = static_cast<uint16_t>((1u << CL) - 1u);
+  const uint16_t all_ctas = static_cast<uint16_t>((1u << CL) - 1u);  // the commit arrives in both blocks of a pair
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ TMA producer
@@ -343,13 +340,7 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
         }
         mbar_arrive_expect_tx(&full[stage], kTBytesA + kTBytesB + 512u + (v1 ? 1024u : 512u));
         tma_load_2d(st, &a.tm_a, &full[stage], ks * kTileK, mt * 128, pol_a);
-        if (FORM == kTiledSingle) {
-          tma_load_2d(st + kTBytesA, &a.tm_b, &full[stage], ks * kTileK, nt * 256, pol_b);
-        } else if (FORM == kTiledMulticast) {
-          // this block's 128-row half of B, into the same place in both blocks
-          tma_load_2d_multicast(st + kTBytesA + rank * (kTBytesB / 2), &a.tm_b, &full[stage], ks * kTileK,
-                                nt * 256 + rank * 128, all_ctas, pol_b);
-        }
+        tma_load_2d(st + kTBytesA, &a.tm_b, &full[stage], ks * kTileK, nt * 256, pol_b);
         bulk_load(st + F::kOffSfa, a.sf_a + (static_cast<size_t>(mt_sf) * a.KS + ks) * 512, 512, &full[stage],
                   pol_a);
         const uint8_t* sfb = a.sf_b + (static_cast<size_t>(2 * nt) * a.KS + ks) * 512;
@@ -417,9 +408,8 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
           if constexpr (PAIR) tc_mma_mxf8_pair(tmem, da, db, idesc, sfc, sfc + 4, (ks > 0 || k > 0) ? 1u : 0u);
           else tc_mma_mxf8(tmem, da, db, idesc, sfc, sfc + 4, (ks > 0 || k > 0) ? 1u : 0u);
         }
-        // the stage is free in this block and (multicast, pair MMA) in the partner
+        // the stage is free in this block (and, for the pair MMA, in the partner)
         if constexpr (FORM == kTiledSingle) tc_commit(&empty[stage]);
-        else if constexpr (FORM == kTiledMulticast) tc_commit_multicast(&empty[stage], all_ctas);
         else tc_commit_pair(&empty[stage], all_ctas);
         if (++stage == NS) { stage = 0; ++round; }
       }
@@ -569,7 +559,7 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // no block leaves while its partner may still multicast into it or arrive on it
+  // no block leaves while its partner may still arrive on its barriers
   if (CL > 1) {
     __syncwarp();
     cluster_sync_all();
@@ -581,7 +571,7 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
 }
 
 namespace {
-// Per device: the four kernel instances' dynamic shared-memory limits have
+// Per device: the kernel instances' dynamic shared-memory limits have
 // been raised.  Internal linkage (not a static inside a template, which the
 // toolchain would merge across every loaded copy of the library), so each
 // copy sets the limits of its own kernels.
@@ -599,9 +589,8 @@ cudaError_t set_smem_limits() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxAttrDevices) return cudaErrorInvalidDevice;
   if (g_smem_attr_set[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  const cudaError_t es[6] = {set_smem_limit<kTiledSingle, false>(),    set_smem_limit<kTiledSingle, true>(),
-                             set_smem_limit<kTiledMulticast, false>(), set_smem_limit<kTiledMulticast, true>(),
-                             set_smem_limit<kTiledPairMma, false>(),   set_smem_limit<kTiledPairMma, true>()};
+  const cudaError_t es[4] = {set_smem_limit<kTiledSingle, false>(), set_smem_limit<kTiledSingle, true>(),
+                             set_smem_limit<kTiledPairMma, false>(), set_smem_limit<kTiledPairMma, true>()};
   for (cudaError_t x : es)
     if (x != cudaSuccess) return x;
   g_smem_attr_set[dev].store(true, std::memory_order_release);
@@ -628,15 +617,14 @@ cudaError_t launch_tiled(const TiledArgs& a, int grid, cudaStream_t stream) {
 template <bool SWIGLU>
 cudaError_t launch_form(const TiledArgs& a, int grid, cudaStream_t stream) {
   if (a.form == kTiledPairMma) return launch_tiled<kTiledPairMma, SWIGLU>(a, grid, stream);
-  if (a.form == kTiledMulticast) return launch_tiled<kTiledMulticast, SWIGLU>(a, grid, stream);
   return launch_tiled<kTiledSingle, SWIGLU>(a, grid, stream);
 }
 }  // namespace
 
 cudaError_t launch_gemm_tiled(const TiledArgs& a, int sms, cudaStream_t stream) {
   // The host chose the form (and encoded tm_b with 128-row boxes for the
-  // cluster forms).  The cluster forms take CL = 2 vertically adjacent row
-  // tiles per work item; grid = one block per SM at most.
+  // pair form).  The pair form takes CL = 2 vertically adjacent row tiles per
+  // work item; grid = one block per SM at most.
   if (a.form == kTiledPairMma && (a.N % 256 != 0 || a.MT < 2)) return cudaErrorInvalidValue;
   const int cl = a.form == kTiledSingle ? 1 : 2;
   const int items = ((a.MT + cl - 1) / cl) * a.NT;

@@ -127,8 +127,10 @@ cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStr
 // Whether `grid` blocks of the kernel with `smem` bytes of shared memory run
 // as grid / 2 co-resident 2-block clusters on the current device.
 bool cluster_pairs_fit(int grid, size_t smem);
+// up != nullptr: x is W_gate [rows / 2, K], up is W_up [rows / 2, K], and the
+// rows are quantised in the paired W_gateup order (blocks of kPairRows).
 cudaError_t launch_quantize(const uint16_t* x, int rows, int K, int ld, uint8_t* codes, uint8_t* scales,
-                            int tiled, cudaStream_t stream);
+                            int tiled, cudaStream_t stream, const uint16_t* up = nullptr);
 cudaError_t launch_swiglu_quantize(const float* gu, int M, int I, uint8_t* hc, uint8_t* hs,
                                    cudaStream_t stream);
 cudaError_t launch_rmsnorm_quantize(const uint16_t* x, const uint16_t* gamma, float eps, int rows, int K, int ld,

@@ -76,17 +76,30 @@ __device__ __forceinline__ uint32_t quantize_block_bf16(const uint16_t* src, uin
 
 // ======================================================================
 // Standalone quantiser: one thread per 32-block.
+// With `up` != null the rows come from two matrices in the paired order of
+// W_gateup: destination row r of block j = r / 128 is row 64 j + r % 128 of
+// `x` (W_gate) for r % 128 < 64, else row 64 j + r % 128 - 64 of `up` (W_up).
 // ======================================================================
-__global__ void quantize_kernel(const uint16_t* __restrict__ x, int rows, int rows_pad, int K, int ld,
-                                uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int tiled) {
+__global__ void quantize_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ up, int rows,
+                                int rows_pad, int K, int ld, uint8_t* __restrict__ codes,
+                                uint8_t* __restrict__ scales, int tiled) {
   const int nb = K / 32;
   const long long total = static_cast<long long>(rows_pad) * nb;
   for (long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; b < total;
        b += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int r = static_cast<int>(b / nb), kb = static_cast<int>(b % nb);
     uint32_t s = 0;
-    if (r < rows) s = quantize_block_bf16(x + static_cast<long long>(r) * ld + kb * 32,
-                                          codes + static_cast<long long>(r) * K + kb * 32);
+    if (r < rows) {
+      const uint16_t* src = x;
+      int sr = r;
+      if (up != nullptr) {
+        const int j = r >> 7, w = r & 127;
+        src = w < kPairRows ? x : up;
+        sr = j * kPairRows + (w & (kPairRows - 1));
+      }
+      s = quantize_block_bf16(src + static_cast<long long>(sr) * ld + kb * 32,
+                              codes + static_cast<long long>(r) * K + kb * 32);
+    }
     if (tiled) {
       scales[tiled_sf_offset(r, kb, K / 128)] = static_cast<uint8_t>(s);
     } else if (r < rows) {
@@ -96,14 +109,14 @@ __global__ void quantize_kernel(const uint16_t* __restrict__ x, int rows, int ro
 }
 
 cudaError_t launch_quantize(const uint16_t* x, int rows, int K, int ld, uint8_t* codes, uint8_t* scales,
-                            int tiled, cudaStream_t stream) {
+                            int tiled, cudaStream_t stream, const uint16_t* up) {
   const int rows_pad = tiled ? (rows + 127) / 128 * 128 : rows;
   const long long total = static_cast<long long>(rows_pad) * (K / 32);
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   long long blocks = (total + threads - 1) / threads;
   if (blocks > 65535LL * 16) blocks = 65535LL * 16;
-  quantize_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(x, rows, rows_pad, K, ld, codes,
+  quantize_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(x, up, rows, rows_pad, K, ld, codes,
                                                                           scales, tiled);
   return cudaGetLastError();
 }

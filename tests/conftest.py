@@ -22,3 +22,20 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture
+def knob():
+    """Sets library plan knobs (fsops_debug_set_knob) for one test and puts
+    every knob it touched back to its default afterwards."""
+    import mxfp8_swiglu_mlp_gb300 as fs
+
+    touched = []
+
+    def set_knob(name, value):
+        fs.fsops_debug_set_knob(name, int(value))
+        touched.append(name)
+
+    yield set_knob
+    for name in touched:
+        fs.fsops_debug_set_knob(name, -1)

@@ -168,3 +168,25 @@ def test_paged_attention_validation(fs):
     assert call(ws=FAKE + 16) == fs.ERR_MISALIGNED  # the workspace wants 256-byte alignment
     assert call(lens=FAKE + 2) == fs.ERR_MISALIGNED
     assert fs.fsops_paged_attention_workspace_bytes(2, 8, 2, 64, 16, 4) == 0
+
+
+def test_gateup_quantize_validation(fs):
+    lib = fs.lib
+    q = lambda g=FAKE, u=FAKE, I=256, H=256, ld=256, c=FAKE, s=FAKE: \
+        lib.fsops_quantize_mxfp8_gateup(g, u, I, H, ld, c, s, None)
+    for kw in ({"I": 96}, {"I": 0}, {"H": 200}, {"ld": 128}, {"ld": 260}, {"I": 1 << 20, "H": 1 << 14}):
+        assert q(**kw) == fs.ERR_UNSUPPORTED_SHAPE, kw
+    assert q(g=None) == fs.ERR_INVALID_ARG
+    assert q(u=None) == fs.ERR_INVALID_ARG
+    assert q(s=None) == fs.ERR_INVALID_ARG
+    assert q(u=FAKE + 2) == fs.ERR_MISALIGNED
+    assert q(c=FAKE + 8) == fs.ERR_MISALIGNED
+
+
+def test_knobs_and_noalloc_status_validation(fs):
+    lib = fs.lib
+    assert lib.fsops_debug_set_knob(-1, 0) == fs.ERR_INVALID_ARG
+    assert lib.fsops_debug_set_knob(len(fs.KNOBS), 0) == fs.ERR_INVALID_ARG
+    for k in fs.KNOBS.values():
+        assert lib.fsops_debug_set_knob(k, -1) == fs.OK
+    assert lib.fsops_read_noalloc_status(None) == fs.ERR_INVALID_ARG

@@ -114,12 +114,11 @@ PREFILL = [(129, 256, 128), (300, 384, 256), (1000, 640, 640), (4096, 256, 256)]
 
 
 @pytest.mark.parametrize("M,N,K", PREFILL)
-@pytest.mark.parametrize("form", ["0", "1", "2"])
-def test_gemm_prefill_fp32_out_matches_oracle(fs, M, N, K, form, monkeypatch):
-    """All three launch forms: one block per tile (0), 2-block clusters
-    multicasting half of B (1), and the 256-row pair MMA (2; shapes with an
-    odd number of 128-column halves fall back to form 1)."""
-    monkeypatch.setenv("FSOPS_GEMM_FORM", form)
+@pytest.mark.parametrize("form", [0, 1])
+def test_gemm_prefill_fp32_out_matches_oracle(fs, M, N, K, form, knob):
+    """Both launch forms: one block per tile (0) and the 256-row pair MMA (1;
+    shapes with an odd number of 128-column halves fall back to form 0)."""
+    knob("GEMM_FORM", form)
     a, b = _operands(M, N, K, seed=3 * M + N + K)
     bc, bs = oracle.quantize_bf16(b)
     ref = oracle.gemm(a, bc, bs)["c"]
@@ -128,9 +127,9 @@ def test_gemm_prefill_fp32_out_matches_oracle(fs, M, N, K, form, monkeypatch):
 
 
 @pytest.mark.parametrize("M,N,K", PREFILL[:3])
-@pytest.mark.parametrize("form", ["1", "2"])
-def test_gemm_prefill_bf16_out_matches_oracle(fs, M, N, K, form, monkeypatch):
-    monkeypatch.setenv("FSOPS_GEMM_FORM", form)
+@pytest.mark.parametrize("form", [0, 1])
+def test_gemm_prefill_bf16_out_matches_oracle(fs, M, N, K, form, knob):
+    knob("GEMM_FORM", form)
     a, b = _operands(M, N, K, seed=5 * M + N + K)
     bc, bs = oracle.quantize_bf16(b)
     res = oracle.gemm(a, bc, bs)
@@ -141,11 +140,11 @@ def test_gemm_prefill_bf16_out_matches_oracle(fs, M, N, K, form, monkeypatch):
     assert np.mean(got == ref) > 0.9
 
 
-@pytest.mark.parametrize("form", ["1", "2"])
-def test_gemm_prefill_pair_shapes(fs, form, monkeypatch):
+@pytest.mark.parametrize("form", [0, 1])
+def test_gemm_prefill_pair_shapes(fs, form, knob):
     """N a multiple of 256 (the pair MMA's shapes): an odd number of row
     tiles leaves the last pair's second tile wholly past M."""
-    monkeypatch.setenv("FSOPS_GEMM_FORM", form)
+    knob("GEMM_FORM", form)
     for M, N, K, seed in ((384, 512, 640, 41), (1000, 768, 256, 42), (256, 256, 1152, 43)):
         a, b = _operands(M, N, K, seed=seed)
         bc, bs = oracle.quantize_bf16(b)
@@ -198,14 +197,14 @@ def test_two_library_copies_in_one_process(fs, tmp_path):
         assert rel_l2(outs[1], outs[0]) < 1e-6
 
 
-@pytest.mark.parametrize("form", ["1", "2"])
-def test_gemm_square_16384_sampled(fs, form, monkeypatch):
+@pytest.mark.parametrize("form", [0, 1])
+def test_gemm_square_16384_sampled(fs, form, knob):
     """The largest square GEMM (16384^3, bf16 A quantised on the device): the
     whole output is finite, and 16 sampled rows x 128 sampled columns match
     the oracle, which quantises the sampled rows of A and B itself."""
     import torch
 
-    monkeypatch.setenv("FSOPS_GEMM_FORM", form)
+    knob("GEMM_FORM", form)
     M = N = K = 16384
     g = torch.Generator(device="cuda").manual_seed(11)
     a = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
@@ -218,7 +217,7 @@ def test_gemm_square_16384_sampled(fs, form, monkeypatch):
     torch.cuda.synchronize()
     assert fs.fsops_read_kernel_status(ws) == 0
     assert bool(torch.isfinite(c).all())
-    rng = np.random.default_rng(int(form))
+    rng = np.random.default_rng(int(form) + 1)
     rows = np.sort(rng.choice(M, 16, replace=False))
     cols = np.sort(rng.choice(N, 128, replace=False))
     a_bits = a[torch.from_numpy(rows).cuda()].view(torch.int16).cpu().numpy().view(np.uint16)

@@ -70,22 +70,24 @@ def test_small_shapes(fs, M, H, I, seed, fused):
     _assert_parity(L.run(fs, fused), L.oracle())
 
 
-@pytest.mark.parametrize("M,env", [
-    (16, {"FSOPS_TR0": "128", "FSOPS_WHOLE_TILES": "0"}),   # 128-row gate/up tiles, split-K
-    (16, {"FSOPS_TR0": "256", "FSOPS_WHOLE_TILES": "1"}),   # 256-row whole tiles, staged epilogue
-    (16, {"FSOPS_TR1": "128"}),                             # 128-row down tiles, staged epilogue
-    (64, {"FSOPS_TR1": "256", "FSOPS_WHOLE_TILES": "0"}),   # 256-row down tiles, split gate/up from TMEM
-    (64, {"FSOPS_TR0": "128"}),                             # 128-row whole gate/up tiles from TMEM
-    (16, {"I": "5120"}),                                    # gate/up tiles split by 2-block clusters
-    (16, {"I": "5120", "FSOPS_PAIRS": "0"}),                # the same shape split over all blocks
+@pytest.mark.parametrize("M,kn", [
+    (16, {"TR0": 128, "WHOLE_TILES": 0, "DECODE_PATH": 0}),   # 128-row gate/up tiles, split-K
+    (16, {"TR0": 256, "WHOLE_TILES": 1, "DECODE_PATH": 0}),   # 256-row whole tiles, staged epilogue
+    (16, {"TR1": 128, "DECODE_PATH": 0}),                     # 128-row down tiles, staged epilogue
+    (64, {"TR1": 256, "WHOLE_TILES": 0}),                     # 256-row down tiles, split gate/up from TMEM
+    (64, {"TR0": 128}),                                       # 128-row whole gate/up tiles from TMEM
+    (16, {"I": 5120, "DECODE_PATH": 0}),                      # gate/up tiles split by 2-block clusters
+    (16, {"I": 5120, "PAIRS": 0, "DECODE_PATH": 0}),          # the same shape split over all blocks
+    (16, {"LOCAL_XQ": 0, "DECODE_PATH": 0}),                  # x quantised grid-wide at M <= 16
+    (16, {"PRIME": 3, "MAX_INFLIGHT": 2, "DECODE_PATH": 0}),  # other weight-load depths
 ])
-def test_tile_plans(fs, M, env, monkeypatch):
-    """Every tile height / split combination the kernel supports, forced
-    through the environment knobs, against the oracle."""
-    env = dict(env)
-    I = int(env.pop("I", "2560"))
-    for k, v in env.items():
-        monkeypatch.setenv(k, v)
+def test_tile_plans(fs, M, kn, knob):
+    """Every tile height / split combination the grid-wide kernel supports,
+    forced through the plan knobs, against the oracle."""
+    kn = dict(kn)
+    I = int(kn.pop("I", 2560))
+    for k, v in kn.items():
+        knob(k, v)
     wl = inputs.make_workload_small("s", M, 512, I, 9)
     L = Layer(fs, wl)
     _assert_parity(L.run(fs, True), L.oracle())

@@ -34,11 +34,11 @@ def test_prefill_small_shapes(fs, M, H, I, seed, fused):
     _assert_parity(L.run(fs, fused), L.oracle())
 
 
-@pytest.mark.parametrize("form", ["0", "1", "2"])
-def test_prefill_cluster_forms(fs, form, monkeypatch):
-    """The three launch forms of the tiled GEMMs: single blocks, 2-block
-    clusters that multicast half of each B stage, and 256-row pair MMAs."""
-    monkeypatch.setenv("FSOPS_GEMM_FORM", form)
+@pytest.mark.parametrize("form", [0, 1])
+def test_prefill_cluster_forms(fs, form, knob):
+    """Both launch forms of the tiled GEMMs: single blocks and 256-row pair
+    MMAs of 2-block clusters."""
+    knob("GEMM_FORM", form)
     wl = inputs.make_workload_small("s", 640, 512, 768, 26)
     L = Layer(fs, wl)
     _assert_parity(L.run(fs), L.oracle())

@@ -686,3 +686,64 @@ def test_blockscale_planted_mistakes_are_caught(mistake):
     t = torch.from_numpy(t.astype(np.float32)).clamp(-448.0, 448.0)
     codes = t.to(torch.float8_e4m3fn).view(torch.uint8).reshape(4, 256).numpy()
     assert np.mean(codes != tc) > 0.05, mistake
+
+
+# ------------------------------------------------------------------ SwiGLU + requantisation (the unfused middle step)
+def _torch_mx_codes(v: torch.Tensor):
+    """MXFP8 codes and row-major scale bytes of float64 rows, from torch
+    pieces: the block exponent from torch.frexp, the element rounding from
+    torch's float8_e4m3fn conversion after the saturation of the MX rule."""
+    rows, K = v.shape
+    blk = v.reshape(rows, K // 32, 32)
+    amax = blk.abs().amax(dim=-1, keepdim=True)
+    _, ex = torch.frexp(amax)
+    e = torch.where(amax == 0, torch.full_like(ex, -127), (ex - 1 - 8).clamp(-127, 127))
+    t = (blk / torch.ldexp(torch.ones_like(amax), e.to(torch.float64))).clamp(-448.0, 448.0)
+    codes = t.to(torch.float8_e4m3fn).view(torch.uint8).reshape(rows, K)
+    return codes.numpy(), (e[..., 0] + 127).to(torch.uint8).numpy()
+
+
+def test_swiglu_quantize_matches_torch_rebuild():
+    """oracle.swiglu_quantize (h = SiLU(g) * u, requantised along I) against
+    torch's silu and float8 conversion, bit for bit, on gate sums spread over
+    six decades, a zero block and a block of negative gates."""
+    rng = np.random.default_rng(21)
+    M, I = 9, 256
+    g = rng.standard_normal((M, I)) * np.power(10.0, rng.uniform(-3, 3, size=(M, 1)))
+    u = rng.standard_normal((M, I))
+    g[2, 32:64] = 0.0
+    g[3, 64:96] = -np.abs(g[3, 64:96]) - 5.0
+    codes, scales = oracle.swiglu_quantize(np.concatenate([g, u], axis=1))
+    h = torch.nn.functional.silu(torch.from_numpy(g)) * torch.from_numpy(u)
+    tc, ts = _torch_mx_codes(h)
+    assert np.array_equal(codes, tc)
+    assert np.array_equal(scales, ts)
+
+
+def test_swiglu_quantize_closed_forms():
+    """SiLU(64) = 64 exactly in float64 (1 + e^-64 rounds to 1), so gate 64
+    with up values on the E4M3 grid gives h = 64 u, which requantises
+    exactly; a zero gate gives a zero block (scale byte 0) whose codes carry
+    the sign of u; swapping gate and up is caught."""
+    rng = np.random.default_rng(22)
+    I = 64
+    # block maximum 14 = 1.75 * 2^3: h's amax 896 gives e = 9 - 8 = 1 and
+    # 896 / 2 = 448 exactly (a mantissa above 1.75 would saturate); every
+    # other value is at most 14 and at least 2^-4, so h / 2 stays on the grid
+    mags = np.array([(1 + m / 8) * 2.0 ** k for k in range(-4, 4) for m in range(8)])
+    mags = mags[mags <= 14.0]
+    u = rng.choice(mags, size=(1, I)) * rng.choice([-1.0, 1.0], size=(1, I))
+    u[0, 0] = 14.0
+    g = np.full((1, I), 64.0)
+    codes, scales = oracle.swiglu_quantize(np.concatenate([g, u], axis=1))
+    back = oracle.dequantize(codes, scales)
+    assert np.array_equal(back, 64.0 * u)
+    zc, zs = oracle.swiglu_quantize(np.concatenate([np.zeros((1, I)), u], axis=1))
+    assert np.all(zs == 0)
+    assert np.array_equal(zc[0] & 0x7F, np.zeros(I, np.uint8))
+    assert np.array_equal(zc[0] >> 7, (u[0] < 0).astype(np.uint8))
+    gr = rng.standard_normal((3, I)) * 3
+    ur = rng.standard_normal((3, I))
+    right = oracle.swiglu_quantize(np.concatenate([gr, ur], axis=1))[0]
+    swapped = oracle.swiglu_quantize(np.concatenate([ur, gr], axis=1))[0]
+    assert np.mean(right == swapped) < 0.5
