@@ -368,7 +368,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic, "traffic_source": traffic_src,
                      "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
-                     "kernel": decode_kernel_name(fs, M) + (" (three-launch path)" if args.unfused else ""),
+                     "kernel": decode_kernel_name(fs, M, H, I) + (" (three-launch path)" if args.unfused else ""),
                      "bytes_per_launch": B,
                      "achieved_from": "bytes_per_launch / (timed region / steps): CUDA events around the "
                                       "graph replays of the timed region",
@@ -433,8 +433,10 @@ def sweep(fs, device, stream, hbm_peak, args):
     return res
 
 
-def decode_kernel_name(fs, M):
-    """The kernel the fused MLP call runs for M tokens."""
+def decode_kernel_name(fs, M, H=4096, I=12288):
+    """The kernel the fused MLP call runs for M tokens (the library's default plan)."""
+    if M <= 16 and H >= 256 and I // 128 < 76:
+        return "mx_slice_kernel (fused MLP, one launch, 2-block clusters)"
     return "mx_persistent_kernel (fused MLP, one launch)" if M <= 128 else "mx_gemm_tiled_kernel (3 launches)"
 
 

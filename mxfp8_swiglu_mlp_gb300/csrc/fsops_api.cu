@@ -18,6 +18,7 @@
 #include "mx_internal.h"
 #include "mx_tiled.h"
 #include "mx_attention.h"
+#include "mx_slice.h"
 
 using namespace fsops;
 
@@ -381,6 +382,79 @@ fsops_status fill_mlp_args(KernelArgs& ka, const MlpPlan& pl, const MlpBuffers& 
   return FSOPS_OK;
 }
 
+// The cluster-sliced decode kernel (mx_slice.cu) for up to 32 tokens: NP
+// 2-block clusters, each owning NC / NP (at most kSliceMaxChunks) 128-feature
+// chunks of I; RT = H / 128 row tiles in the down projection.
+struct SlicePlan {
+  int NC, NP, RT, npad;
+};
+bool slice_plan(int M, int H, int I, int sms, SlicePlan* sp) {
+  if (M < 1 || M > kSliceMaxM || H < 256 || sms < kSliceCluster) return false;
+  const int NC = I / 128;
+  const int NP = sms / kSliceCluster < NC ? sms / kSliceCluster : NC;
+  if ((NC + NP - 1) / NP > kSliceMaxChunks) return false;
+  const int RT = H / 128;
+  if ((RT + 1) / 2 > 256 || ctl_words_needed(0, 0, RT) * 4 > kCtlRegionBytes) return false;
+  sp->NC = NC;
+  sp->NP = NP;
+  sp->RT = RT;
+  sp->npad = M <= 16 ? 16 : 32;
+  return true;
+}
+// fp32 [M, H] partial sums of the sliced kernel.
+size_t slice_accum_bytes(int M, int H) { return round_up(static_cast<size_t>(M) * H * 4, 1024); }
+// Whether the fused MLP call runs the sliced kernel.  By default only where
+// it was measured faster than the grid-wide kernel: up to 16 tokens with
+// fewer 128-feature chunks than 2-block clusters (a small I, as at M = 1,
+// H = 1024, I = 2816: 14.6 against 16.6 us per call).  With more chunks the
+// grid-wide kernel wins (M = 16, H = 2560, I = 9728: 29.7 against 33.7 us):
+// every cluster adds a full [M, H] fp32 partial of y into L2, 12.5 MB of L2
+// reductions there.  FSOPS_KNOB_DECODE_PATH = 1 / 0 forces either.
+bool use_slice(int M, int H, int I, const DeviceInfo* di, SlicePlan* sp) {
+  const int k = knob(FSOPS_KNOB_DECODE_PATH);
+  if (k == 0) return false;
+  if (!slice_plan(M, H, I, di->sms, sp)) return false;
+  return k == 1 || (M <= 16 && sp->NC < di->sms / kSliceCluster);
+}
+// One launch of the sliced kernel.  ctl: the control words (status word,
+// then RT tile counters), accum: fp32 [M, H], both zero between launches.  gamma != null: x is normalised (RMSNorm with eps) before its
+// quantisation; residual != null is added to y before the bf16 rounding.
+fsops_status launch_slice(const SlicePlan& sp, uint8_t* ctl, uint8_t* accum, const void* x_bf16, const void* gamma,
+                          float eps, const void* residual, const uint8_t* w_gateup, const uint8_t* w_down,
+                          const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I, cudaStream_t stream) {
+  SliceArgs sa;
+  std::memset(&sa, 0, sizeof(sa));
+  if (!encode_map(&sa.tm_wgu, w_gateup, H, 2 * I, 128) || !encode_map(&sa.tm_wd, w_down, I, H, 128) ||
+      !encode_x_map(&sa.tm_x, x_bf16, H, M, sp.npad))
+    return FSOPS_ERR_INVALID_ARG;
+  sa.sf_gu = scales->gateup;
+  sa.sf_d = scales->down;
+  sa.x = static_cast<const uint16_t*>(x_bf16);
+  sa.gamma = static_cast<const uint16_t*>(gamma);
+  sa.eps = eps;
+  sa.y = static_cast<uint16_t*>(y_bf16);
+  sa.residual = static_cast<const uint16_t*>(residual);
+  sa.accum = reinterpret_cast<float*>(accum);
+  uint32_t* cw = reinterpret_cast<uint32_t*>(ctl);
+  sa.status = cw + kCtlStatus;
+  sa.tile_cnt = cw + kCtlHeaderWords;
+  sa.M = M;
+  sa.H = H;
+  sa.I = I;
+  sa.NC = sp.NC;
+  sa.NP = sp.NP;
+  sa.KS0 = H / kTileK;
+  sa.RT = sp.RT;
+  sa.nstages = slice_stages(sp.npad);
+  sa.timeout_ns = g_timeout_ns.load();
+  sa.extra_arrivals = g_extra.load();
+#ifdef FSOPS_TRACE
+  sa.trace = g_trace;
+#endif
+  const cudaError_t e = launch_slice_kernel(sa, sp.npad, stream);
+  return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "mx_slice_kernel launch");
+}
+
 // Up to 128 rows: the decode kernel (stream-K split over all SMs); more rows
 // (prefill): whole 128 x 256 output tiles per block.
 constexpr int kMaxGemmRows = 16384;
@@ -696,6 +770,10 @@ fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup,
   if (M > 128)
     return mlp_tiled_impl(x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I, ws, l, di,
                           static_cast<cudaStream_t>(stream));
+  SlicePlan sp;
+  if (use_slice(M, H, I, di, &sp))
+    return launch_slice(sp, ws + l.ctl, ws + l.part1, x_bf16, nullptr, 0.f, nullptr, w_gateup, w_down, scales,
+                        y_bf16, M, H, I, static_cast<cudaStream_t>(stream));
 
   const MlpPlan pl = plan_mlp(M, H, I, grid);
   const MlpBuffers bufs{ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.hq, ws + l.hq_sf, ws + l.part0, ws + l.part1};
@@ -817,6 +895,10 @@ fsops_status fsops_mxfp8_swiglu_mlp_block(const void* x_bf16, const void* gamma_
   st = check_ws(dev, l.total, &ws);
   if (st != FSOPS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SlicePlan sp;
+  if (M <= 128 && use_slice(M, H, I, di, &sp))  // one launch: the norm runs inside the MLP kernel
+    return launch_slice(sp, ws + l.ctl, ws + l.part1, x_bf16, gamma_bf16, eps, residual ? x_bf16 : nullptr,
+                        w_gateup, w_down, scales, y_bf16, M, H, I, s);
   // launch 1: RMSNorm(x) * gamma quantised into the workspace's x buffers
   const cudaError_t e = launch_rmsnorm_quantize(static_cast<const uint16_t*>(x_bf16),
                                                 static_cast<const uint16_t*>(gamma_bf16), eps, M, H, H, ws + l.xq,
@@ -979,10 +1061,14 @@ fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w
   if (st != FSOPS_OK) return st;
   if (M > 128) return FSOPS_ERR_UNSUPPORTED_SHAPE;  // the fixed buffer serves the single-launch path only
   const int grid = di->sms;
+  SlicePlan sp;
+  const bool sliced = use_slice(M, H, I, di, &sp);
   const MlpPlan pl = plan_mlp(M, H, I, grid);
-  if (ctl_words_needed(I / 128, pl.T0, pl.T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (!sliced && ctl_words_needed(I / 128, pl.T0, pl.T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  // the sliced kernel needs the control words and its row-tile sums only
+  const size_t slice_end = kCtlRegionBytes + (sliced ? slice_accum_bytes(M, H) : 0);
   const NoAllocLayout l = noalloc_layout(M, H, I, pl);
-  if (l.end > kNoAllocScratchBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;  // does not fit the fixed buffer
+  if ((sliced ? slice_end : l.end) > kNoAllocScratchBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;  // does not fit
 
   uint8_t* ws = nullptr;
   if ((st = noalloc_base(dev, &ws)) != FSOPS_OK) return st;
@@ -1000,10 +1086,15 @@ fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w
     std::lock_guard<std::mutex> lk(g_mu);
     g_noalloc_dirty[dev] = false;
   }
-  const MlpBuffers bufs{ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.hq, ws + l.hq_sf, ws + l.part0, ws + l.part1};
-  KernelArgs ka;
-  st = fill_mlp_args(ka, pl, bufs, x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I);
-  if (st == FSOPS_OK) st = launch(ka, grid, s);
+  if (sliced) {
+    st = launch_slice(sp, ws, ws + kCtlRegionBytes, x_bf16, nullptr, 0.f, nullptr, w_gateup, w_down, scales, y_bf16,
+                      M, H, I, s);
+  } else {
+    const MlpBuffers bufs{ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.hq, ws + l.hq_sf, ws + l.part0, ws + l.part1};
+    KernelArgs ka;
+    st = fill_mlp_args(ka, pl, bufs, x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I);
+    if (st == FSOPS_OK) st = launch(ka, grid, s);
+  }
   if (st != FSOPS_OK) {
     std::lock_guard<std::mutex> lk(g_mu);
     g_noalloc_dirty[dev] = true;

@@ -22,57 +22,12 @@
 #include <cuda_fp8.h>
 
 #include "mx_internal.h"
+#include "mx_device.cuh"
 #include "mx_mxfp8.cuh"
 #include "sm103.cuh"
 
 namespace fsops {
 using namespace dev;
-
-// ======================================================================
-// bf16 blocks to MXFP8 codes
-// ======================================================================
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Quantise one 32-element bf16 block already in registers (raw = 64 bytes)
-// into 32 codes packed four to a word; returns the scale byte.
-__device__ __forceinline__ uint32_t quantize_block_pack(const uint4 (&raw)[4], uint32_t (&packed)[8]) {
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(raw);
-  uint32_t amax_bits = 0;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    amax_bits = max(amax_bits, (w[i] & 0x7FFFu) << 16);
-    amax_bits = max(amax_bits, w[i] & 0x7FFF0000u);
-  }
-  const uint32_t s = ue8m0_from_amax(__uint_as_float(amax_bits));
-  const float inv = inv_scale_from_ue8m0(s);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t c0 = e4m3_code(bf16_lo(w[2 * i]) * inv);
-    const uint32_t c1 = e4m3_code(bf16_hi(w[2 * i]) * inv);
-    const uint32_t c2 = e4m3_code(bf16_lo(w[2 * i + 1]) * inv);
-    const uint32_t c3 = e4m3_code(bf16_hi(w[2 * i + 1]) * inv);
-    packed[i] = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
-  }
-  return s;
-}
-// Same, storing the 32 codes at `dst` (16-byte aligned).
-__device__ __forceinline__ uint32_t quantize_block_regs(const uint4 (&raw)[4], uint8_t* dst) {
-  uint32_t packed[8];
-  const uint32_t s = quantize_block_pack(raw, packed);
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  d[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  d[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-  return s;
-}
-
-// Same, loading the block from `src` (16-byte aligned) first.
-__device__ __forceinline__ uint32_t quantize_block_bf16(const uint16_t* src, uint8_t* dst) {
-  uint4 raw[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
-  return quantize_block_regs(raw, dst);
-}
 
 // ======================================================================
 // Standalone quantiser: one thread per 32-block.
@@ -271,71 +226,6 @@ cudaError_t launch_swiglu_quantize(const float* gu, int M, int I, uint8_t* hc, u
 //   warps 4-7      quantise x (grid slice, or each stage's tile when M <= 32),
 //                  then run the epilogue of every accumulator
 // ======================================================================
-struct Ctx {
-  volatile int* abort_flag;
-  volatile uint32_t* status;
-  uint64_t timeout_ns;
-};
-
-__device__ __noinline__ void raise_error(const Ctx& cx, uint32_t code, uint32_t site) {
-  *cx.abort_flag = 1;
-  const uint32_t word = (code << 24) | ((site & 0xFFu) << 16) | (blockIdx.x & 0xFFFFu);
-  atomicCAS(const_cast<uint32_t*>(cx.status), 0u, word);
-}
-
-// Bounded wait on an mbarrier phase.  Gives up (returns false) when the block
-// was told to abort, another block reported an error, or the timeout passes.
-__device__ __forceinline__ bool wait_mbar(const Ctx& cx, uint64_t* bar, uint32_t parity, uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t n = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if ((++n & 15u) == 0) {
-      if (*cx.abort_flag || *cx.status != 0) { *cx.abort_flag = 1; return false; }
-      if (globaltimer_ns() - t0 > cx.timeout_ns) { raise_error(cx, 5u, site); return false; }
-    }
-  }
-  return true;
-}
-// The same on a barrier a CTA of the cluster arrives on (acquire at cluster scope).
-__device__ __forceinline__ bool wait_mbar_cluster(const Ctx& cx, uint64_t* bar, uint32_t parity, uint32_t site) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t n = 0;
-  while (!mbar_try_wait_cluster(bar, parity)) {
-    if ((++n & 15u) == 0) {
-      if (*cx.abort_flag || *cx.status != 0) { *cx.abort_flag = 1; return false; }
-      if (globaltimer_ns() - t0 > cx.timeout_ns) { raise_error(cx, 5u, site); return false; }
-    }
-  }
-  return true;
-}
-// Bounded wait used only while tearing down (no abort check, fixed limit).
-__device__ __forceinline__ void drain_mbar(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > limit_ns) return;
-  }
-}
-// Bounded spin until every counter p[0..n) is >= target.  The polls are
-// relaxed loads issued together (one round trip per try); an acquire fence
-// follows the successful try.
-__device__ __forceinline__ bool wait_counters(const Ctx& cx, const uint32_t* p, int n, uint32_t target,
-                                              uint32_t site) {
-  uint64_t t0 = 0;
-  for (;;) {
-    bool all = true;
-    for (int i = 0; i < n; ++i) all &= (ld_relaxed_gpu(p + i) >= target);
-    if (all) break;
-    if (t0 == 0) t0 = globaltimer_ns();
-    if (*cx.abort_flag || *cx.status != 0) { *cx.abort_flag = 1; return false; }
-    if (globaltimer_ns() - t0 > cx.timeout_ns) { raise_error(cx, 5u, site); return false; }
-    __nanosleep(20);
-  }
-  fence_acq_rel_gpu();
-  return true;
-}
-
 // Timeline stamps for profiling builds (compiled with -DFSOPS_TRACE).
 #ifdef FSOPS_TRACE
 #define FSOPS_STAMP(idx)                                                         \
@@ -355,7 +245,6 @@ __device__ __forceinline__ bool wait_counters(const Ctx& cx, const uint32_t* p, 
   } while (0)
 #endif
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __device__ __forceinline__ long long range_begin(long long c, long long U, long long G) { return c * U / G; }
 // Stream-K split of U units over G blocks in 32-bit arithmetic (U <= 2^18 and

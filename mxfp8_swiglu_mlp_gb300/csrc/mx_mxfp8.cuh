@@ -23,6 +23,17 @@ __device__ __forceinline__ float inv_scale_from_ue8m0(uint32_t s) {
 __device__ __forceinline__ uint32_t e4m3_code(float v) {
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
+// Two values to two E4M3 codes in one conversion instruction (round to
+// nearest even, saturating): lo in bits 0..7, hi in bits 8..15.
+__device__ __forceinline__ uint32_t e4m3x2_code(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Four values to four codes, a in bits 0..7 up to d in bits 24..31.
+__device__ __forceinline__ uint32_t e4m3x4_code(float a, float b, float c, float d) {
+  return e4m3x2_code(a, b) | (e4m3x2_code(c, d) << 16);
+}
 // Byte offset of the scale of row r, 32-block kb in the tcgen05 tiled layout
 // (512-byte tiles of 128 rows x 4 blocks; n_kg = K / 128 tiles per row tile).
 __device__ __forceinline__ uint32_t tiled_sf_offset(int r, int kb, int n_kg) {

@@ -103,6 +103,29 @@ def test_block_matches_oracle(fs, M, H, I, seed, residual):
     _assert_parity(B.run_block(fs, residual), B.oracle_block(residual))
 
 
+@pytest.mark.parametrize("M,H,I,seed", [s for s in SHAPES if s[0] <= 32] + [(32, 512, 640, 58)])
+@pytest.mark.parametrize("residual", [True, False])
+def test_block_sliced_one_launch(fs, M, H, I, seed, residual, knob):
+    """The decoder block on the cluster-sliced kernel, which computes the
+    RMSNorm of x inside the MLP launch (one launch for the whole block)."""
+    knob("DECODE_PATH", 1)
+    wl = inputs.make_workload_small("s", M, H, I, seed, token_scale_log10=(-1.0, 1.0))
+    B = Block(fs, wl)
+    _assert_parity(B.run_block(fs, residual), B.oracle_block(residual))
+
+
+@pytest.mark.parametrize("path", [0, 1])
+def test_block_in_place_sliced_and_grid(fs, path, knob):
+    """In place (y is x's buffer) on both decode paths."""
+    knob("DECODE_PATH", path)
+    wl = inputs.make_workload_small("s", 16, 512, 768, 76)
+    B = Block(fs, wl)
+    a = B.run_block(fs, True, in_place=False)
+    b = B.run_block(fs, True, in_place=True)
+    assert rel_l2(bf16_bits_to_f64(b), bf16_bits_to_f64(a)) < 1e-3
+    _assert_parity(b, B.oracle_block(True))
+
+
 @pytest.mark.parametrize("M", [16, 256])
 def test_block_in_place(fs, M):
     """y may be x's own buffer."""

@@ -59,7 +59,11 @@ def _assert_parity(got_bits, ref, per_row=True):
 SMALL = [(1, 256, 384, 0), (5, 512, 640, 1), (16, 1024, 1280, 2), (33, 384, 512, 3), (128, 256, 256, 4),
          (64, 1152, 896, 5), (100, 640, 2048, 6),
          # small H, large I: many gate/up tiles, short K loops
-         (8, 256, 4864, 7), (32, 384, 5120, 8)]
+         (8, 256, 4864, 7), (32, 384, 5120, 8),
+         # more 128-feature chunks than 2-block clusters: 2, 3 and 4 chunks per cluster
+         (17, 256, 9856, 17), (4, 256, 25600, 18), (3, 512, 38912, 19),
+         # H of one row tile of 128 (the grid-wide kernel) and an odd number of row tiles
+         (6, 128, 512, 20), (20, 640, 768, 21)]
 
 
 @pytest.mark.parametrize("M,H,I,seed", SMALL)
@@ -68,6 +72,16 @@ def test_small_shapes(fs, M, H, I, seed, fused):
     wl = inputs.make_workload_small("s", M, H, I, seed)
     L = Layer(fs, wl)
     _assert_parity(L.run(fs, fused), L.oracle())
+
+
+@pytest.mark.parametrize("M,H,I,seed", [s for s in SMALL if s[0] <= 32 and s[1] >= 256])
+def test_small_shapes_sliced(fs, M, H, I, seed, knob):
+    """The cluster-sliced kernel forced on every small shape it serves
+    (1-4 chunks per cluster, one row tile, odd row tiles, M up to 32)."""
+    knob("DECODE_PATH", 1)
+    wl = inputs.make_workload_small("s", M, H, I, seed)
+    L = Layer(fs, wl)
+    _assert_parity(L.run(fs), L.oracle())
 
 
 @pytest.mark.parametrize("M,kn", [
@@ -91,6 +105,22 @@ def test_tile_plans(fs, M, kn, knob):
     wl = inputs.make_workload_small("s", M, 512, I, 9)
     L = Layer(fs, wl)
     _assert_parity(L.run(fs, True), L.oracle())
+
+
+@pytest.mark.parametrize("M,H,I,seed", [(1, 512, 1024, 30), (16, 768, 2560, 31), (32, 512, 896, 32)])
+def test_decode_paths_agree(fs, M, H, I, seed, knob):
+    """The cluster-sliced kernel and the grid-wide kernel on the same inputs:
+    both within the oracle's tolerance, and close to each other."""
+    wl = inputs.make_workload_small("s", M, H, I, seed)
+    L = Layer(fs, wl)
+    ref = L.oracle()
+    knob("DECODE_PATH", 1)
+    a = L.run(fs)
+    knob("DECODE_PATH", 0)
+    b = L.run(fs)
+    _assert_parity(a, ref)
+    _assert_parity(b, ref)
+    assert rel_l2(bf16_bits_to_f64(a), bf16_bits_to_f64(b)) < 1e-3
 
 
 def test_token_scale_spread(fs):
