@@ -357,7 +357,10 @@ fsops_status fsops_debug_set_extra_arrivals(uint32_t n);
  *   MAX_INFLIGHT      weight loads in flight per block (1..8).
  *   LOCAL_XQ          0: quantise x grid-wide even for M <= 16.
  *   DECODE_PATH       M <= 32: 0 the grid-wide two-phase kernel, 1 the
- *                     cluster-sliced kernel. */
+ *                     cluster-sliced kernel.
+ *   COOPERATIVE       1: launch the grid-wide kernel cooperatively instead
+ *                     of as a plain launch that may start while the previous
+ *                     kernel on the stream finishes. */
 typedef enum {
   FSOPS_KNOB_TR0 = 0,
   FSOPS_KNOB_TR1 = 1,
@@ -368,7 +371,8 @@ typedef enum {
   FSOPS_KNOB_MAX_INFLIGHT = 6,
   FSOPS_KNOB_LOCAL_XQ = 7,
   FSOPS_KNOB_DECODE_PATH = 8,
-  FSOPS_KNOB_COUNT = 9
+  FSOPS_KNOB_COOPERATIVE = 9,
+  FSOPS_KNOB_COUNT = 10
 } fsops_knob;
 
 /* Set knob `knob` (an fsops_knob) to `value` (negative = back to the

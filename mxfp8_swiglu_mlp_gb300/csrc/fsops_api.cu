@@ -307,6 +307,24 @@ bool pairs_fit(int grid, size_t smem) {
   return fit;
 }
 
+// grid_fits, queried once per device, grid and shared-memory size.
+bool grid_fits_cached(int grid, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, size_t>, bool> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(dev, grid, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  const bool fit = grid_fits(grid, smem);
+  cache[key] = fit;
+  return fit;
+}
+
 fsops_status launch(KernelArgs& a, int grid, cudaStream_t stream) {
   a.nstages = stages_for(a.npad, a.local_xq);
   if (a.max_inflight > a.nstages) a.max_inflight = a.nstages;
@@ -317,7 +335,12 @@ fsops_status launch(KernelArgs& a, int grid, cudaStream_t stream) {
     pairs = false;
   }
   a.cluster_pairs = pairs ? 1 : 0;
-  const cudaError_t e = launch_mx_kernel(a, grid, smem_for(a.npad, a.local_xq), stream);
+  const size_t smem = smem_for(a.npad, a.local_xq);
+  // a plain launch with programmatic dependent launch by default (see
+  // launch_mx_kernel); cooperative when forced or when the grid might not be
+  // resident at once
+  const bool coop = knob(FSOPS_KNOB_COOPERATIVE) == 1 || !grid_fits_cached(grid, smem);
+  const cudaError_t e = launch_mx_kernel(a, grid, smem, stream, coop);
   return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "mx_persistent_kernel launch");
 }
 

@@ -123,6 +123,14 @@ __device__ __forceinline__ bool wait_counters(const Ctx& cx, const uint32_t* p, 
   return true;
 }
 
+// Programmatic dependent launch: wait until the kernels this grid depends on
+// have completed and their memory is visible (holds the whole warp), and let
+// the next kernel on the stream be scheduled as this grid's blocks leave.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // The 128 epilogue threads (warps 4-7) of a block.
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 

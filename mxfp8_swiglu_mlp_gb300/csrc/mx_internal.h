@@ -122,8 +122,15 @@ __host__ __device__ inline uint32_t xring_bytes_for(int npad) { return kMaxXSlot
 constexpr uint32_t kAccCols = 256;
 constexpr uint32_t kSfColsPerStage = 12;
 
-// Launch wrappers (mx_kernels.cu).
-cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStream_t stream);
+// Launch wrappers (mx_kernels.cu).  The persistent kernel's blocks wait on
+// one another, so all `grid` of them must be resident at once.  A cooperative
+// launch guarantees that; the plain launch (with programmatic stream
+// serialization: it may start while the previous kernel on the stream
+// finishes) relies on it holding once that kernel has completed -- every
+// wait on another block comes after the grid dependency wait -- which
+// grid_fits checks against the device's resources.
+cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStream_t stream, bool cooperative);
+bool grid_fits(int grid, size_t smem);
 // Whether `grid` blocks of the kernel with `smem` bytes of shared memory run
 // as grid / 2 co-resident 2-block clusters on the current device.
 bool cluster_pairs_fit(int grid, size_t smem);

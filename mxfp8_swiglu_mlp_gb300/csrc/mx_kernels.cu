@@ -549,6 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   tc_fence_after();
   // the pair's barriers are initialised before either block arrives remotely
   if (a.cluster_pairs) cluster_sync_all();
+  // the next kernel on the stream may be scheduled as this grid's blocks leave
+  griddep_launch_dependents();
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) FSOPS_STAMP(0);
 
@@ -609,6 +611,11 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       if (issued_mask & (1u << s)) drain_mbar(&full_w[s], (issued_parity >> s) & 1u, 200000000ull);
   } else if (warp == 1) {
     // ------------------------------------------------ activation producer
+    // x, the quantised activations and the readiness counters may be in use by
+    // the previous kernel on the stream until it completes (the launch lets
+    // this grid start while it finishes); the weights never are, so the
+    // weight producer starts at once.
+    griddep_wait();
     // Lane 0 issues the TMA loads.  With local_xq the whole warp quantises
     // phase 0's activation tiles itself: lane 0 streams the bf16 x tiles of the
     // segment into a ring (kMaxXSlots ahead), every lane quantises its 32-blocks
@@ -776,6 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     // ------------------------------------------------ epilogue warps
     const int et = threadIdx.x - 128;  // token row of the accumulator (TMEM lane)
     const int ew = et >> 5;
+    griddep_wait();  // x, the workspace and y may be in use by the previous kernel until here
     // (1) grid-wide: quantise this block's slice of x, the 32-blocks [b0, b1)
     // of the row-major [npad, H/32] block grid (rows >= M only get a zero scale)
     if (a.x != nullptr && !a.local_xq) {
@@ -1070,6 +1078,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   }
 
   // ------------------------------------------------ teardown
+  griddep_wait();  // (immediate by now) before thread 0 touches the control words
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1104,7 +1113,7 @@ constexpr int kMaxAttrDevices = 64;
 std::atomic<bool> g_smem_attr_set[kMaxAttrDevices];
 }  // namespace
 
-cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStream_t stream) {
+cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStream_t stream, bool cooperative) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1119,16 +1128,40 @@ cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStr
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[3];
+  int n = 0;
+  if (cooperative) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n++].val.cooperative = 1;
+  } else {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n++].val.programmaticStreamSerializationAllowed = 1;
+  }
+  if (a.cluster_pairs) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n++].val.clusterDim.z = 1;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = a.cluster_pairs ? 2 : 1;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, mx_persistent_kernel, a);
+}
+
+bool grid_fits(int grid, size_t smem) {
+  if (cudaFuncSetAttribute(mx_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  int per_sm = 0, dev = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_persistent_kernel, kThreads, smem) != cudaSuccess ||
+      cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return per_sm * sms >= grid;
 }
 
 bool cluster_pairs_fit(int grid, size_t smem) {

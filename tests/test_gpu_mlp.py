@@ -94,6 +94,8 @@ def test_small_shapes_sliced(fs, M, H, I, seed, knob):
     (16, {"I": 5120, "PAIRS": 0, "DECODE_PATH": 0}),          # the same shape split over all blocks
     (16, {"LOCAL_XQ": 0, "DECODE_PATH": 0}),                  # x quantised grid-wide at M <= 16
     (16, {"PRIME": 3, "MAX_INFLIGHT": 2, "DECODE_PATH": 0}),  # other weight-load depths
+    (16, {"COOPERATIVE": 1, "DECODE_PATH": 0}),               # cooperative launch of the grid-wide kernel
+    (64, {"COOPERATIVE": 1}),
 ])
 def test_tile_plans(fs, M, kn, knob):
     """Every tile height / split combination the grid-wide kernel supports,
