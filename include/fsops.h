@@ -211,12 +211,16 @@ fsops_status fsops_rmsnorm_quantize_mxfp8(const void* x_bf16, const void* gamma_
  *   y = x + MLP(RMSNorm(x) * gamma)   (residual = 1)
  *   y = MLP(RMSNorm(x) * gamma)       (residual = 0)
  * with MLP the computation of fsops_mxfp8_swiglu_mlp and the sum rounded to
- * bf16 once.  Two launches for M <= 128 (RMSNorm + quantisation, then the
- * single-launch MLP reading the quantised rows and adding x in its bf16
- * store); three above.  Arguments, limits and workspace as
- * fsops_mxfp8_swiglu_mlp, plus gamma_bf16 [H] (16-byte aligned) and eps.
- * y_bf16 may equal x_bf16 (in place): x is read by the first launch and, for
- * the residual, only by the thread that then writes the same element of y.
+ * bf16 once.  ONE launch for M <= 128: the MLP kernel computes each row's
+ * mean square in its x-quantisation prologue, quantises x * rsqrt(ms + eps) *
+ * gamma straight to MXFP8 (never rounded to bf16) and adds x in its bf16
+ * store.  Three launches above 128 rows (RMSNorm + quantisation, then the
+ * tiled MLP).  Arguments, limits and workspace as fsops_mxfp8_swiglu_mlp,
+ * plus gamma_bf16 [H] (16-byte aligned) and eps.
+ * y_bf16 may equal x_bf16 (in place): every read of x for the norm and the
+ * quantisation happens before any block writes y (the MLP's phases wait for
+ * the whole grid's quantisation), and the residual is read only by the thread
+ * that then writes the same element of y.
  * Graph-capture safe, so a chain of layers (y of one block is x of the next)
  * can be captured once and replayed. */
 fsops_status fsops_mxfp8_swiglu_mlp_block(const void* x_bf16, const void* gamma_bf16, float eps, int residual,

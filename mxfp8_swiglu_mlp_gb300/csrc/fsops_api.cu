@@ -354,7 +354,8 @@ struct MlpBuffers {
 // decoder block's RMSNorm launch); residual (bf16 [M, H]) is added to y.
 fsops_status fill_mlp_args(KernelArgs& ka, const MlpPlan& pl, const MlpBuffers& b, const void* x_bf16,
                            const uint8_t* w_gateup, const uint8_t* w_down, const fsops_mlp_scales* scales,
-                           void* y_bf16, int M, int H, int I, const void* residual = nullptr) {
+                           void* y_bf16, int M, int H, int I, const void* residual = nullptr,
+                           const void* gamma = nullptr, float eps = 0.f) {
   init_common(ka, M, reinterpret_cast<uint32_t*>(b.ctl));
   const int Ic = I / 128;  // 128-feature chunks (phase-1 k-stages)
   if (ctl_words_needed(Ic, pl.T0, pl.T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
@@ -381,7 +382,11 @@ fsops_status fill_mlp_args(KernelArgs& ka, const MlpPlan& pl, const MlpBuffers& 
   p0.rows = 2 * I;
   p0.whole_tiles = pl.whole0;
   p0.pairs = pl.pairs0;
-  ka.local_xq = x_bf16 != nullptr ? local_xq_for(ka.npad) : 0;
+  ka.gamma = static_cast<const uint16_t*>(gamma);
+  ka.eps = eps;
+  // with RMSNorm x is quantised grid-wide: every read of x then precedes the
+  // readiness count that every phase waits on, so y may be x itself
+  ka.local_xq = (x_bf16 != nullptr && gamma == nullptr) ? local_xq_for(ka.npad) : 0;
   p0.dep = (ka.local_xq || x_bf16 == nullptr) ? kDepNone : kDepXReady;
   if (ka.local_xq && !encode_x_map(&ka.tm_x, x_bf16, H, M, ka.npad)) return FSOPS_ERR_INVALID_ARG;
   p0.epi = kEpiSwiGLU;
@@ -922,21 +927,24 @@ fsops_status fsops_mxfp8_swiglu_mlp_block(const void* x_bf16, const void* gamma_
   if (M <= 128 && use_slice(M, H, I, di, &sp))  // one launch: the norm runs inside the MLP kernel
     return launch_slice(sp, ws + l.ctl, ws + l.part1, x_bf16, gamma_bf16, eps, residual ? x_bf16 : nullptr,
                         w_gateup, w_down, scales, y_bf16, M, H, I, s);
-  // launch 1: RMSNorm(x) * gamma quantised into the workspace's x buffers
+  const void* res = residual ? x_bf16 : nullptr;
+  if (M <= 128) {
+    // one launch: the MLP kernel normalises x in its quantisation prologue
+    const int grid = di->sms;
+    const MlpPlan pl = plan_mlp(M, H, I, grid);
+    const MlpBuffers bufs{ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.hq, ws + l.hq_sf, ws + l.part0, ws + l.part1};
+    KernelArgs ka;
+    st = fill_mlp_args(ka, pl, bufs, x_bf16, w_gateup, w_down, scales, y_bf16, M, H, I, res, gamma_bf16, eps);
+    if (st != FSOPS_OK) return st;
+    return launch(ka, grid, s);
+  }
+  // above 128 rows: RMSNorm(x) * gamma quantised into the workspace's x
+  // buffers, then the tiled MLP on them, + x
   const cudaError_t e = launch_rmsnorm_quantize(static_cast<const uint16_t*>(x_bf16),
                                                 static_cast<const uint16_t*>(gamma_bf16), eps, M, H, H, ws + l.xq,
                                                 ws + l.xq_sf, 1, s);
   if (e != cudaSuccess) return cuda_failed(e, "rmsnorm_quantize_kernel launch");
-  const void* res = residual ? x_bf16 : nullptr;
-  // launch 2 (3 above 128 rows): the MLP on the quantised rows, + x
-  if (M > 128) return mlp_tiled_impl(nullptr, w_gateup, w_down, scales, y_bf16, M, H, I, ws, l, di, s, res);
-  const int grid = di->sms;
-  const MlpPlan pl = plan_mlp(M, H, I, grid);
-  const MlpBuffers bufs{ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.hq, ws + l.hq_sf, ws + l.part0, ws + l.part1};
-  KernelArgs ka;
-  st = fill_mlp_args(ka, pl, bufs, nullptr, w_gateup, w_down, scales, y_bf16, M, H, I, res);
-  if (st != FSOPS_OK) return st;
-  return launch(ka, grid, s);
+  return mlp_tiled_impl(nullptr, w_gateup, w_down, scales, y_bf16, M, H, I, ws, l, di, s, res);
 }
 
 fsops_status fsops_mxfp8_swiglu_mlp_unfused(const void* x_bf16, const uint8_t* w_gateup, const uint8_t* w_down,

@@ -35,6 +35,50 @@ __device__ __forceinline__ uint32_t quantize_block_pack(const uint4 (&raw)[4], u
                             bf16_hi(w[2 * i + 1]) * inv);
   return s;
 }
+// The same for RMSNorm(x) * gamma: the 32 values x * rn * gamma (fp32, in
+// that order; rn = 1 / rms of the block's row, gamma 16-byte aligned bf16),
+// quantised with the rule above.  Returns the scale byte.
+__device__ __forceinline__ uint32_t quantize_block_pack_norm(const uint4 (&raw)[4], const uint16_t* gamma, float rn,
+                                                             uint32_t (&packed)[8]) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(raw);
+  const uint4* gp = reinterpret_cast<const uint4*>(gamma);
+  float v[32];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 gv = __ldg(gp + q);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[8 * q + 2 * i] = bf16_lo(w[4 * q + i]) * rn * bf16_lo(gw[i]);
+      v[8 * q + 2 * i + 1] = bf16_hi(w[4 * q + i]) * rn * bf16_hi(gw[i]);
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const uint32_t s = ue8m0_from_amax(amax);
+  const float inv = inv_scale_from_ue8m0(s);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) packed[i] = e4m3x4_code(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+  return s;
+}
+// 1 / sqrt(mean(x^2) + eps) of a bf16 row of K elements, reduced in fp32 by
+// the calling warp (every lane gets the result).
+__device__ __forceinline__ float row_rnorm(const uint16_t* xr, int K, float eps, int lane) {
+  float ss = 0.f;
+  for (int i = lane; i < K / 8; i += 32) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo = bf16_lo(w[k]), hi = bf16_hi(w[k]);
+      ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  return rsqrtf(ss / static_cast<float>(K) + eps);
+}
 // Same, storing the 32 codes at `dst` (16-byte aligned).
 __device__ __forceinline__ uint32_t quantize_block_regs(const uint4 (&raw)[4], uint8_t* dst) {
   uint32_t packed[8];
@@ -133,5 +177,21 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 // The 128 epilogue threads (warps 4-7) of a block.
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// AND of `v` over the 128 epilogue threads (a barrier among them): every
+// epilogue thread takes the same branch after a wait, so none of them is left
+// alone at a later barrier when another gave up.
+__device__ __forceinline__ bool epi_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
 
 }  // namespace fsops

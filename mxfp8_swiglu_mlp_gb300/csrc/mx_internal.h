@@ -69,6 +69,8 @@ struct KernelArgs {
   int nphases;
   // activation quantisation (x != nullptr)
   const uint16_t* x;      // bf16 [M, H]
+  const uint16_t* gamma;  // bf16 [H]: x is RMSNorm(x) * gamma before quantisation (grid-wide path only), or null
+  float eps;
   uint8_t* xq_codes;      // [M, H] (grid-wide quantisation only)
   uint8_t* xq_sf;         // tiled, H / 128 tiles
   int H;

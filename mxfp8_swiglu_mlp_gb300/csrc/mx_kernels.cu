@@ -512,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   // keeps only prime_inflight loads in flight, so that the x quantisation's
   // own memory traffic is not queued behind the whole grid's weight stream
   volatile int* flowing = reinterpret_cast<volatile int*>(tmem_slot + 3);
+  float* rnorm = reinterpret_cast<float*>(tmem_slot + 4);  // [kMmaM] 1 / rms of the rows this block quantises
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long G = gridDim.x;
@@ -790,6 +791,17 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       const int nbk = a.H / 32;
       const long long NB = static_cast<long long>(npad) * nbk;
       const long long b0 = range_begin(blockIdx.x, NB, G), b1 = range_begin(blockIdx.x + 1, NB, G);
+      const bool norm = a.gamma != nullptr;
+      if (norm && b1 > b0) {
+        // RMSNorm: 1 / rms of every row the slice touches, over the whole row
+        // (one warp per row in turn)
+        const int m0 = static_cast<int>(b0 / nbk), m1 = static_cast<int>((b1 - 1) / nbk);
+        for (int m = m0 + ew; m <= m1 && m < a.M; m += 4) {
+          const float rn = row_rnorm(a.x + static_cast<long long>(m) * a.H, a.H, a.eps, lane);
+          if (lane == 0) rnorm[m] = rn;
+        }
+        epi_bar();
+      }
       long long b = b0 + et;
       uint4 raw[4];
       bool have = false;
@@ -812,7 +824,15 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
 #pragma unroll
             for (int i = 0; i < 4; ++i) raw[i] = __ldcg(src + i);
           }
-          s = quantize_block_regs(raw, a.xq_codes + static_cast<long long>(m) * a.H + kb * 32);
+          if (norm) {
+            uint32_t pk[8];
+            s = quantize_block_pack_norm(raw, a.gamma + kb * 32, rnorm[m], pk);
+            uint4* d = reinterpret_cast<uint4*>(a.xq_codes + static_cast<long long>(m) * a.H + kb * 32);
+            d[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            d[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          } else {
+            s = quantize_block_regs(raw, a.xq_codes + static_cast<long long>(m) * a.H + kb * 32);
+          }
         }
         have = false;
         a.xq_sf[(kb >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (kb & 3)] = static_cast<uint8_t>(s);
@@ -837,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       SegIter it(ph, static_cast<uint32_t>(G));
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
-        if (!wait_mbar(cx, acc_full, acc_round & 1u, kSiteAccFull)) { ok = false; break; }
+        if (!epi_and(wait_mbar(cx, acc_full, acc_round & 1u, kSiteAccFull))) { ok = false; break; }
         ++acc_round;
         tc_fence_after();
         if (et == 0) FSOPS_STAMP(p == 0 ? 3 : 8);
@@ -936,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           const uint32_t peer = (blockIdx.x & 1u) ^ 1u;
           const int h = static_cast<int>(blockIdx.x & 1u);
           if (et == 0) mbar_arrive_remote(mapa_shared(peer_ready, peer));  // my sums are staged (epi_bar above)
-          if (!wait_mbar_cluster(cx, peer_ready, 0, kSitePeer)) { ok = false; break; }
+          if (!epi_and(wait_mbar_cluster(cx, peer_ready, 0, kSitePeer))) { ok = false; break; }
           if (et == 0) FSOPS_STAMP(58);
           const uint32_t pstg = mapa_shared(stg, peer);
 #pragma unroll 1
@@ -957,7 +977,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           if (et == 0) red_add_release_gpu(a.hflags + ((t * ph.tile_rows) >> 8), 1u);
           if (et == 0) FSOPS_STAMP(14);
           // the peer reads this block's stg: it is written again only after that
-          if (!wait_mbar_cluster(cx, peer_done, 0, kSitePeer)) { ok = false; break; }
+          if (!epi_and(wait_mbar_cluster(cx, peer_done, 0, kSitePeer))) { ok = false; break; }
           if (et == 0) FSOPS_STAMP(p == 0 ? 4 : 9);
           continue;
         } else {

@@ -76,21 +76,6 @@ __device__ __forceinline__ void fence_proxy_async_shared_cluster() {
   asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-// AND of `v` over the 128 epilogue threads (a barrier among them): every
-// epilogue thread takes the same branch after a wait, so none of them is left
-// alone at a later barrier when another gave up.
-__device__ __forceinline__ bool epi_and(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}\n"
-      : "=r"(r)
-      : "r"(v ? 1u : 0u)
-      : "memory");
-  return r != 0;
-}
 
 // One 32-element block of bf16 x (row r, k-group j of a 128-wide k-chunk),
 // already in registers, quantised into the stage's activation tile (128-byte
@@ -104,33 +89,7 @@ __device__ __forceinline__ void store_x_block(int M, uint8_t* st, int b, const u
   uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
   if (r < M) {
     uint32_t pk[8];
-    if (!norm) {
-      s = quantize_block_pack(raw, pk);
-    } else {
-      // RMSNorm(x) * gamma in fp32, then the MXFP8 rule
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(raw);
-      const uint4* gp = reinterpret_cast<const uint4*>(gam);
-      float v[32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 gv = gp[q];
-        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[8 * q + 2 * i] = bf16_lo(w[4 * q + i]) * scale_row * bf16_lo(gw[i]);
-          v[8 * q + 2 * i + 1] = bf16_hi(w[4 * q + i]) * scale_row * bf16_hi(gw[i]);
-        }
-      }
-      float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-      s = ue8m0_from_amax(amax);
-      const float inv = inv_scale_from_ue8m0(s);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        pk[i] = e4m3_code(v[4 * i] * inv) | (e4m3_code(v[4 * i + 1] * inv) << 8) |
-                (e4m3_code(v[4 * i + 2] * inv) << 16) | (e4m3_code(v[4 * i + 3] * inv) << 24);
-    }
+    s = norm ? quantize_block_pack_norm(raw, gam, scale_row, pk) : quantize_block_pack(raw, pk);
     c0 = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     c1 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
   }
@@ -415,20 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_slice_kernel(const __grid_cons
       // RMSNorm: the mean square of each token row over all of H (fp32), one
       // warp per row in turn; the activation warp waits for it
       for (int r = q4; r < M; r += 4) {
-        const uint16_t* xr = a.x + static_cast<size_t>(r) * a.H;
-        float ss = 0.f;
-        for (int i = lane; i < a.H / 8; i += 32) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + i);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float lo = bf16_lo(w[k]), hi = bf16_hi(w[k]);
-            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
-          }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-        if (lane == 0) rnorm[r] = rsqrtf(ss / static_cast<float>(a.H) + a.eps);
+        const float rn = row_rnorm(a.x + static_cast<size_t>(r) * a.H, a.H, a.eps, lane);
+        if (lane == 0) rnorm[r] = rn;
       }
       epi_bar();  // every row's norm is in rnorm before any quantisation
     }
