@@ -268,6 +268,46 @@ fsops_status fsops_mxfp8_paged_decode_attention(const void* q_bf16, const uint8_
  * (0 if the shape is unsupported). */
 size_t fsops_paged_attention_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size, int max_pages);
 
+/* ------------------------------------------------------------------------
+ * FP8 with 128 x 128 block scales -- the second scale format the Fish Audio
+ * post names beside mxfp8 ("bsgemm", X copy "Custom kernels for the shapes
+ * TTS actually uses"; p2 "Estrategia de cuantizacion FP8").  The pages give
+ * no formula; read plainly:
+ *   weights W [N, K]: one fp32 scale per 128 x 128 block, activations A [M, K]:
+ *   one fp32 scale per 1 x 128 group along K (a 128 x 128 block of activations
+ *   would span every token of a decode step); scale = amax / 448 in fp32 (1
+ *   for an all-zero block); code = E4M3 round-to-nearest-even, saturating at
+ *   448, of v / scale in fp32 (correctly rounded division), sign kept.
+ *
+ * fsops_quantize_fp8_blockscale -- bf16 x [rows, ld] (first K columns) to
+ *   codes [rows, K] and fp32 scales [ceil(rows / block_rows), K / 128]
+ *   (row-major), block_rows 1 (activations) or 128 (weights).  K % 128 == 0,
+ *   ld % 8 == 0, rows * ld < 2^31.  Scales 4-byte aligned.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA. */
+fsops_status fsops_quantize_fp8_blockscale(const void* x_bf16, int rows, int K, int ld, int block_rows, uint8_t* codes,
+                                           float* scales, void* stream);
+
+/* Number of fp32 scales of a [rows, K] matrix in blocks of block_rows x 128
+ * (0 for an invalid argument). */
+size_t fsops_blockscale_scale_count(int rows, int K, int block_rows);
+
+/* fsops_fp8_blockscale_gemm -- C[M, N] = sum over 128-deep K-blocks kb of
+ *   a_scales[m, kb] * w_scales[n / 128, kb] * (A^ W^T over kb), in fp32, for
+ *   A = a_codes [M, K] with its 1 x 128 scales and W = w_codes [N, K] with its
+ *   128 x 128 scales (as fsops_quantize_fp8_blockscale writes them).  C is
+ *   bf16 (rounded once) or fp32.  One launch.  1 <= M <= 128, N % 128 == 0,
+ *   K % 128 == 0, N, K <= 65536.
+ *   workspace: 256-byte aligned, fsops_blockscale_gemm_workspace_bytes(M, N, K)
+ *   bytes, zero before its first use; a successful call leaves it zero again
+ *   (zero it again after a call that reported an error).  Calls that share a
+ *   workspace must be ordered.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA. */
+fsops_status fsops_fp8_blockscale_gemm(const uint8_t* a_codes, const float* a_scales, const uint8_t* w_codes,
+                                       const float* w_scales, void* c, fsops_dtype c_dtype, int M, int N, int K,
+                                       void* workspace, size_t ws_bytes, void* stream);
+
+size_t fsops_blockscale_gemm_workspace_bytes(int M, int N, int K);
+
 /* The same computation as three launches with the intermediates in HBM (the
  * unfused baseline of p2 "Por que cuBLAS no era suficiente"): GEMM gate/up
  * with fp32 output [M, 2I], SwiGLU + requantisation, GEMM down.  Same

@@ -25,10 +25,11 @@ __all__ = [
     "fsops_gemm_workspace_bytes", "fsops_swiglu_quantize_mxfp8", "fsops_mxfp8_swiglu_mlp",
     "fsops_mxfp8_swiglu_mlp_unfused", "fsops_mxfp8_swiglu_mlp_noalloc", "fsops_mlp_workspace_bytes", "fsops_set_workspace",
     "fsops_read_kernel_status", "fsops_set_wait_timeout_ns", "fsops_debug_set_extra_arrivals",
-    "fsops_debug_set_knob", "KNOBS", "fsops_read_noalloc_status",
+    "fsops_debug_set_knob", "KNOBS", "fsops_read_noalloc_status", "fsops_quantize_fp8_blockscale",
+    "fsops_blockscale_scale_count", "fsops_fp8_blockscale_gemm", "fsops_blockscale_gemm_workspace_bytes",
     "fsops_status_string", "fsops_version", "fsops_last_cuda_error", "fsops_rmsnorm_quantize_mxfp8",
     "fsops_mxfp8_swiglu_mlp_block", "fsops_mxfp8_paged_decode_attention", "fsops_paged_attention_workspace_bytes",
-    "quantize_weight", "MLPWeights", "prepare_mlp_weights",
+    "quantize_weight", "MLPWeights", "prepare_mlp_weights", "quantize_blockscale",
     "Workspace", "pair_gate_up",
 ]
 
@@ -55,6 +56,10 @@ _SIGS = {
     "fsops_quantize_mxfp8": ([_vp, _i, _i, _i, _vp, _vp, _i, _vp], _i),
     "fsops_scale_bytes": ([_i, _i, _i], _sz),
     "fsops_quantize_mxfp8_gateup": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
+    "fsops_quantize_fp8_blockscale": ([_vp, _i, _i, _i, _i, _vp, _vp, _vp], _i),
+    "fsops_blockscale_scale_count": ([_i, _i, _i], _sz),
+    "fsops_fp8_blockscale_gemm": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp], _i),
+    "fsops_blockscale_gemm_workspace_bytes": ([_i, _i, _i], _sz),
     "fsops_mxfp8_gemm": ([_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp], _i),
     "fsops_mxfp8_gemm_ex": ([_vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp], _i),
     "fsops_gemm_workspace_bytes": ([_i, _i, _i], _sz),
@@ -127,6 +132,40 @@ def fsops_quantize_mxfp8(x, rows: int, K: int, ld: int, codes, scales, layout: i
 def fsops_quantize_mxfp8_gateup(w_gate, w_up, I: int, H: int, ld: int, codes, scales, stream=None) -> None:
     _check(lib.fsops_quantize_mxfp8_gateup(_ptr(w_gate), _ptr(w_up), I, H, ld, _ptr(codes), _ptr(scales),
                                            _stream(stream)), "fsops_quantize_mxfp8_gateup")
+
+
+def fsops_quantize_fp8_blockscale(x, rows: int, K: int, ld: int, block_rows: int, codes, scales,
+                                  stream=None) -> None:
+    _check(lib.fsops_quantize_fp8_blockscale(_ptr(x), rows, K, ld, block_rows, _ptr(codes), _ptr(scales),
+                                             _stream(stream)), "fsops_quantize_fp8_blockscale")
+
+
+def fsops_blockscale_scale_count(rows: int, K: int, block_rows: int) -> int:
+    return lib.fsops_blockscale_scale_count(rows, K, block_rows)
+
+
+def fsops_fp8_blockscale_gemm(a_codes, a_scales, w_codes, w_scales, c, c_dtype: int, M: int, N: int, K: int,
+                              workspace, ws_bytes: int, stream=None) -> None:
+    _check(lib.fsops_fp8_blockscale_gemm(_ptr(a_codes), _ptr(a_scales), _ptr(w_codes), _ptr(w_scales), _ptr(c),
+                                         c_dtype, M, N, K, _ptr(workspace), ws_bytes, _stream(stream)),
+           "fsops_fp8_blockscale_gemm")
+
+
+def fsops_blockscale_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return lib.fsops_blockscale_gemm_workspace_bytes(M, N, K)
+
+
+def quantize_blockscale(x_bf16, block_rows: int, stream=None):
+    """bf16 CUDA tensor [rows, K] -> (E4M3 codes uint8 [rows, K], fp32 scales
+    [ceil(rows / block_rows), K / 128]) in blocks of block_rows x 128."""
+    import torch
+
+    rows, K = x_bf16.shape
+    codes = torch.empty((rows, K), dtype=torch.uint8, device=x_bf16.device)
+    scales = torch.empty(((rows + block_rows - 1) // block_rows, K // 128), dtype=torch.float32,
+                         device=x_bf16.device)
+    fsops_quantize_fp8_blockscale(x_bf16, rows, K, x_bf16.stride(0), block_rows, codes, scales, stream)
+    return codes, scales
 
 
 def fsops_rmsnorm_quantize_mxfp8(x, gamma, eps: float, rows: int, K: int, ld: int, codes, scales, layout: int,

@@ -19,6 +19,7 @@
 #include "mx_tiled.h"
 #include "mx_attention.h"
 #include "mx_slice.h"
+#include "mx_blockscale.h"
 
 using namespace fsops;
 
@@ -972,6 +973,75 @@ fsops_status fsops_mxfp8_swiglu_mlp_unfused(const void* x_bf16, const uint8_t* w
   // launch 3: down GEMM on the requantised intermediate
   return gemm_impl(ws + l.hq, ws + l.hq_sf, false, w_down, scales->down, y_bf16, false, M, H, I, ws + l.ctl,
                    nullptr, nullptr, ws + l.part1, di, s);
+}
+
+size_t fsops_blockscale_scale_count(int rows, int K, int block_rows) {
+  if (rows < 0 || K <= 0 || K % 128 != 0 || (block_rows != 1 && block_rows != 128)) return 0;
+  return static_cast<size_t>((rows + block_rows - 1) / block_rows) * (K / 128);
+}
+
+fsops_status fsops_quantize_fp8_blockscale(const void* x_bf16, int rows, int K, int ld, int block_rows, uint8_t* codes,
+                                           float* scales, void* stream) {
+  if (block_rows != 1 && block_rows != 128) return FSOPS_ERR_INVALID_ARG;
+  if (rows < 0 || K <= 0 || K % 128 != 0 || ld < K || ld % 8 != 0) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(rows) * ld >= (1LL << 31)) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return FSOPS_OK;
+  if (x_bf16 == nullptr || codes == nullptr || scales == nullptr) return FSOPS_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
+    return FSOPS_ERR_MISALIGNED;
+  int dev;
+  const DeviceInfo* di;
+  fsops_status st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  const cudaError_t e = launch_bs_quantize(static_cast<const uint16_t*>(x_bf16), rows, K, ld, block_rows, codes, scales,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "blockscale quantise launch");
+}
+
+size_t fsops_blockscale_gemm_workspace_bytes(int M, int N, int K) {
+  if (M < 1 || M > 128 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0 || N > 65536 || K > 65536) return 0;
+  return kCtlRegionBytes + round_up(static_cast<size_t>(M) * N * 4, 1024);
+}
+
+fsops_status fsops_fp8_blockscale_gemm(const uint8_t* a_codes, const float* a_scales, const uint8_t* w_codes,
+                                       const float* w_scales, void* c, fsops_dtype c_dtype, int M, int N, int K,
+                                       void* workspace, size_t ws_bytes, void* stream) {
+  if (a_codes == nullptr || a_scales == nullptr || w_codes == nullptr || w_scales == nullptr || c == nullptr ||
+      workspace == nullptr)
+    return FSOPS_ERR_INVALID_ARG;
+  if (c_dtype != FSOPS_DTYPE_BF16 && c_dtype != FSOPS_DTYPE_F32) return FSOPS_ERR_INVALID_ARG;
+  const size_t need = fsops_blockscale_gemm_workspace_bytes(M, N, K);
+  if (need == 0) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if ((N / 128) + kCtlHeaderWords > static_cast<int>(kCtlRegionBytes / 4)) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < need) return FSOPS_ERR_INVALID_ARG;
+  if (!aligned16(a_codes) || !aligned16(w_codes) || !aligned16(c) || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      (reinterpret_cast<uintptr_t>(a_scales) & 3u) || (reinterpret_cast<uintptr_t>(w_scales) & 3u))
+    return FSOPS_ERR_MISALIGNED;
+  int dev;
+  const DeviceInfo* di;
+  fsops_status st = current_device(&dev, &di);
+  if (st != FSOPS_OK) return st;
+  const int npad = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  BsArgs ba;
+  std::memset(&ba, 0, sizeof(ba));
+  if (!encode_map(&ba.tm_a, a_codes, K, M, npad) || !encode_map(&ba.tm_w, w_codes, K, N, 128))
+    return FSOPS_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ba.a_scales = a_scales;
+  ba.w_scales = w_scales;
+  ba.c = c;
+  ba.c_f32 = c_dtype == FSOPS_DTYPE_F32 ? 1 : 0;
+  ba.accum = reinterpret_cast<float*>(ws + kCtlRegionBytes);
+  ba.status = reinterpret_cast<uint32_t*>(ws) + kCtlStatus;
+  ba.tile_cnt = reinterpret_cast<uint32_t*>(ws) + kCtlHeaderWords;
+  ba.M = M;
+  ba.N = N;
+  ba.K = K;
+  ba.T = N / 128;
+  ba.KB = K / 128;
+  ba.timeout_ns = g_timeout_ns.load();
+  const cudaError_t e = launch_bs_gemm(ba, npad, di->sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "bs_gemm_kernel launch");
 }
 
 fsops_status fsops_read_kernel_status(void* workspace, uint32_t* word) {

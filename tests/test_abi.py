@@ -190,3 +190,32 @@ def test_knobs_and_noalloc_status_validation(fs):
     for k in fs.KNOBS.values():
         assert lib.fsops_debug_set_knob(k, -1) == fs.OK
     assert lib.fsops_read_noalloc_status(None) == fs.ERR_INVALID_ARG
+
+
+def test_blockscale_validation(fs):
+    lib = fs.lib
+    q = lambda x=FAKE, rows=4, K=256, ld=256, br=1, c=FAKE, s=FAKE: \
+        lib.fsops_quantize_fp8_blockscale(x, rows, K, ld, br, c, s, None)
+    assert q(br=64) == fs.ERR_INVALID_ARG
+    assert q(K=96) == fs.ERR_UNSUPPORTED_SHAPE
+    assert q(ld=128) == fs.ERR_UNSUPPORTED_SHAPE
+    assert q(ld=260) == fs.ERR_UNSUPPORTED_SHAPE
+    assert q(rows=0, x=None) == fs.OK
+    assert q(x=None) == fs.ERR_INVALID_ARG
+    assert q(x=FAKE + 2) == fs.ERR_MISALIGNED
+    assert q(s=FAKE + 2) == fs.ERR_MISALIGNED
+    assert fs.fsops_blockscale_scale_count(300, 384, 128) == 3 * 3
+    assert fs.fsops_blockscale_scale_count(300, 384, 1) == 300 * 3
+    assert fs.fsops_blockscale_scale_count(300, 100, 1) == 0
+    g = lambda a=FAKE, sa=FAKE, w=FAKE, sw=FAKE, c=FAKE, cdt=fs.DTYPE_BF16, M=4, N=256, K=256, ws=FAKE, n=1 << 30: \
+        lib.fsops_fp8_blockscale_gemm(a, sa, w, sw, c, cdt, M, N, K, ws, n, None)
+    assert g(a=None) == fs.ERR_INVALID_ARG
+    assert g(sw=None) == fs.ERR_INVALID_ARG
+    assert g(cdt=fs.DTYPE_MXFP8) == fs.ERR_INVALID_ARG
+    for M, N, K in ((0, 256, 256), (129, 256, 256), (4, 200, 256), (4, 256, 100)):
+        assert g(M=M, N=N, K=K) == fs.ERR_UNSUPPORTED_SHAPE
+    assert g(n=16) == fs.ERR_INVALID_ARG
+    assert g(ws=FAKE + 16) == fs.ERR_MISALIGNED
+    assert g(c=FAKE + 2) == fs.ERR_MISALIGNED
+    assert fs.fsops_blockscale_gemm_workspace_bytes(129, 256, 256) == 0
+    assert fs.fsops_blockscale_gemm_workspace_bytes(16, 256, 256) == 16384 + 16 * 256 * 4
