@@ -42,8 +42,14 @@ FALLBACK_HBM_GBS = 6800.0
 # workload: the sha256 prefix of the kernel sources they were taken on (the
 # number is reported only while those sources are unchanged), the bytes, the
 # launch form captured and the summary under profiles/.
-NCU_TRAFFIC = {}
-KERNEL_SOURCES = ("mx_kernels.cu", "mx_internal.h", "mx_mxfp8.cuh", "sm103.cuh")
+NCU_TRAFFIC = {
+    "m16": {"sha": "b8167044a5b47541", "bytes": 80.61e6, "source": "profiles/mx_persistent_kernel_m16_memory.md",
+            "form": "gate/up split over all blocks (--knob PAIRS=0); the timed default splits gate/up tiles by "
+                    "2-block clusters, same weight stream"},
+    "m128": {"sha": "b8167044a5b47541", "bytes": 163.94e6, "source": "profiles/mx_persistent_kernel_m128_memory.md",
+             "form": "the default (no cluster split at M > 32)"},
+}
+KERNEL_SOURCES = ("mx_kernels.cu", "mx_internal.h", "mx_mxfp8.cuh", "sm103.cuh", "mx_device.cuh")
 
 
 def kernel_sources_hash():
@@ -383,6 +389,7 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and not args.no_sweep:
         out["sweep"] = sweep(fs, device, stream, hbm_peak, args)
         out["sweep_c5"] = sweep_c5(fs, device, stream, hbm_peak)
+        out["blockscale_gemm"] = blockscale_gemm(fs, stream, hbm_peak)
         out["prefill_gemm"] = prefill_gemm(fs, stream)
         out["attention_decode"] = attention_decode(fs, stream, hbm_peak)
     if rank == 0 and not args.no_cpu:
@@ -517,6 +524,71 @@ def sweep_c5(fs, device, stream, hbm_peak, Ms=None):
         torch.cuda.empty_cache()
     del layers
     torch.cuda.empty_cache()
+    return res
+
+
+def blockscale_gemm(fs, stream, hbm_peak):
+    """The 128 x 128 block-scaled FP8 GEMM (fsops_fp8_blockscale_gemm) on the
+    H = 5120, I = 17408 decode shapes (gate/up N = 34816, K = 5120; down
+    N = 5120, K = 17408) at M = 1, 16, 128, with pre-quantised A, rotating
+    over enough weight copies to exceed L2; the MXFP8 GEMM
+    (fsops_mxfp8_gemm_ex, pre-quantised A) on the same shapes beside it."""
+    import torch
+
+    res = {"timing": "CUDA graph replays rotating over weight copies (> 2x L2); us per call"}
+    g = torch.Generator(device="cuda").manual_seed(5)
+    for name, (N, K) in (("gateup", (34816, 5120)), ("down", (5120, 17408))):
+        w = (torch.randn(N, K, device="cuda", generator=g) / K ** 0.5).to(torch.bfloat16)
+        copies = max(2, -(-2 * L2_BYTES // (N * K)) + 1)
+        bs_w = [fs.quantize_blockscale(w, 128) for _ in range(copies)]
+        mx_w = [fs.quantize_weight(w) for _ in range(copies)]
+        del w
+        for M in (1, 16, 128):
+            a = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+            ac, asc = fs.quantize_blockscale(a, 1)
+            mc, msc = fs.quantize_weight(a)
+            c = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+            n_bs = fs.fsops_blockscale_gemm_workspace_bytes(M, N, K)
+            ws_bs = torch.zeros(n_bs + 256, dtype=torch.uint8, device="cuda")
+            p_bs = ws_bs.data_ptr() + (-ws_bs.data_ptr()) % 256
+            n_mx = fs.fsops_gemm_workspace_bytes(M, N, K)
+            ws_mx = torch.zeros(n_mx, dtype=torch.uint8, device="cuda")
+            s = stream.cuda_stream
+            calls = {
+                "blockscale": (lambda i: fs.fsops_fp8_blockscale_gemm(ac, asc, bs_w[i % copies][0], bs_w[i % copies][1], c,
+                                                                      fs.DTYPE_BF16, M, N, K, p_bs, n_bs, stream=s),
+                               N * K + (N // 128) * (K // 128) * 4 + M * K + M * (K // 128) * 4 + 2 * M * N),
+                "mxfp8": (lambda i: fs.fsops_mxfp8_gemm_ex(mc, msc, fs.DTYPE_MXFP8, mx_w[i % copies][0], mx_w[i % copies][1],
+                                                           c, fs.DTYPE_BF16, M, N, K, ws_mx, n_mx, stream=s),
+                          N * K + N * K // 32 + M * K + M * K // 32 + 2 * M * N),
+            }
+            entry = {}
+            for kind, (fn, nbytes) in calls.items():
+                n = 8 * copies
+                with torch.cuda.stream(stream):
+                    for i in range(3):
+                        fn(i)
+                    gr = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gr, stream=stream):
+                        for i in range(n):
+                            fn(i)
+                    gr.replay()
+                    stream.synchronize()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(3):
+                        gr.replay()
+                    e1.record(stream)
+                    e1.synchronize()
+                t = e0.elapsed_time(e1) / 1e3 / (3 * n)
+                entry[kind] = {"us_per_call": round(t * 1e6, 3), "GBps": round(nbytes / t / 1e9, 1),
+                               "frac_hbm": round(nbytes / t / 1e9 / hbm_peak, 4),
+                               "TFLOPs": round(2.0 * M * N * K / t / 1e12, 1)}
+                del gr
+            res["%s_N%d_K%d_M%d" % (name, N, K, M)] = entry
+            del a, ac, asc, mc, msc, c, ws_bs, ws_mx
+        del bs_w, mx_w
+        torch.cuda.empty_cache()
     return res
 
 
@@ -784,12 +856,23 @@ def main():
                     help="print only the prefill GEMM / MLP section (a short run for profiling the tiled kernel)")
     ap.add_argument("--attention-only", action="store_true",
                     help="print only the paged decode attention section")
+    ap.add_argument("--blockscale-only", action="store_true",
+                    help="print only the 128 x 128 block-scaled GEMM section")
+    ap.add_argument("--knob", action="append", default=[],
+                    help="NAME=VALUE plan knob of the library (fsops_debug_set_knob), e.g. PAIRS=0 for the launch form "
+                         "an ncu capture uses; repeatable")
     ap.add_argument("--prefill-shapes", default="",
                     help="comma-separated subset of the prefill section's GEMM shapes (default: all)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
+    if args.knob and args.impl == "ours":
+        import mxfp8_swiglu_mlp_gb300 as fs
+
+        for kv in args.knob:
+            k, v = kv.split("=")
+            fs.fsops_debug_set_knob(k.strip(), int(v))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -805,6 +888,14 @@ def main():
 
         torch.cuda.set_device(local_rank)
         print(json.dumps({"attention_decode": attention_decode(fs, torch.cuda.Stream(), peaks()[0])}), flush=True)
+        return
+    if args.blockscale_only:
+        import torch
+
+        import mxfp8_swiglu_mlp_gb300 as fs
+
+        torch.cuda.set_device(local_rank)
+        print(json.dumps({"blockscale_gemm": blockscale_gemm(fs, torch.cuda.Stream(), peaks()[0])}), flush=True)
         return
     if args.prefill_only:
         import torch

@@ -50,3 +50,23 @@ MAX_ABS_TOL = 1e-2
 # 1e-3 for a large h_k.  Whole-output rel-L2 stays far below 2e-3; a single
 # row may not, so rows get the max-abs bound.
 PER_ROW_TOL = 1e-2
+
+
+def assert_repeat_close(a_bits: np.ndarray, b_bits: np.ndarray, max_diff_frac: float = 1e-3) -> None:
+    """Two runs of a kernel whose split-K partial sums are added in arrival
+    order: every element agrees to one bf16 step (fp32 reassociation can move
+    a value across one rounding boundary, no further), and few elements differ
+    at all.  A race that loses or doubles a partial sum moves an element by a
+    whole partial sum, far more than one step."""
+    a = bf16_bits_to_f64(a_bits)
+    b = bf16_bits_to_f64(b_bits)
+    mag = np.maximum(np.abs(a), np.abs(b))
+    _, e = np.frexp(np.where(mag > 0, mag, 1.0))
+    step = np.ldexp(1.0, e - 8)  # spacing of bf16 values (8 significant bits) at that magnitude
+    # an element near zero is a sum whose partials nearly cancel; fp32
+    # reassociation error there is relative to the partials, so it gets an
+    # absolute floor of 2^-16 of the output's largest magnitude
+    floor = np.ldexp(float(np.max(mag)), -16) if mag.size else 0.0
+    bad = np.abs(a - b) > np.maximum(step, floor)
+    assert not np.any(bad), (np.argwhere(bad)[:5], a[bad][:5], b[bad][:5])
+    assert np.mean(a != b) <= max_diff_frac, np.mean(a != b)

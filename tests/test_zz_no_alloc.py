@@ -12,7 +12,8 @@ import pytest
 
 import oracle
 from workloads import inputs
-from tests._util import to_dev_u16, from_dev_bf16, bf16_bits_to_f64, rel_l2, REL_L2_TOL, MAX_ABS_TOL, max_abs_norm
+from tests._util import (to_dev_u16, from_dev_bf16, bf16_bits_to_f64, rel_l2, REL_L2_TOL, MAX_ABS_TOL, max_abs_norm,
+                         assert_repeat_close)
 
 pytestmark = pytest.mark.gpu
 
@@ -55,7 +56,7 @@ def test_noalloc_matches_workspace_entry_point(name, M, nrows):
     y_ref = torch.empty((M, wl.H), dtype=torch.bfloat16, device="cuda")
     fs.fsops_mxfp8_swiglu_mlp(xd, w.gateup_codes, w.down_codes, w.scales, y_ref, M, wl.H, wl.I)
     torch.cuda.synchronize()
-    ref = bf16_bits_to_f64(from_dev_bf16(y_ref))
+    ref_bits = from_dev_bf16(y_ref)
     rows = None if nrows is None else np.sort(np.random.default_rng(M).choice(wl.H, nrows, replace=False))
     want = bf16_bits_to_f64(oracle.swiglu_mlp(x, oracle.quantize_weights(wg, wu, wd), rows_down=rows)["y_bf16"])
     for _ in range(2):  # the second call runs on what the first one left in the buffer
@@ -63,10 +64,11 @@ def test_noalloc_matches_workspace_entry_point(name, M, nrows):
         assert _call_noalloc(fs, xd, w, y, M, wl.H, wl.I) == fs.OK
         torch.cuda.synchronize()
         assert _read_status(fs) == 0
-        got = bf16_bits_to_f64(from_dev_bf16(y))
-        # split-K sums are added in arrival order: the two entry points agree to fp32 rounding
-        assert rel_l2(got, ref) < 1e-3
-        assert np.mean(got == ref) > 0.999
+        got_bits = from_dev_bf16(y)
+        # split-K sums are added in arrival order: the two entry points agree to
+        # fp32 rounding, one bf16 step at most per element
+        assert_repeat_close(got_bits, ref_bits)
+        got = bf16_bits_to_f64(got_bits)
         sub = got if rows is None else got[:, rows]
         assert rel_l2(sub, want) <= REL_L2_TOL and max_abs_norm(sub, want) <= MAX_ABS_TOL
     del ws
