@@ -1098,7 +1098,11 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   }
 
   // ------------------------------------------------ teardown
-  griddep_wait();  // (immediate by now) before thread 0 touches the control words
+  // Thread 0 (the weight producer, done by now) waits for the previous grid
+  // before it touches the control words.  The wait holds the whole warp, so
+  // no other lane of warp 0 (or of warp 2, the MMA issuer's) executes it:
+  // those lanes reach this point while lane 0 is still streaming.
+  if (threadIdx.x == 0) griddep_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

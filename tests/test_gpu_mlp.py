@@ -189,7 +189,7 @@ def test_repeat_calls_full_size(fs):
     bf16 step of the first call's."""
     for name in ("m16", "m128"):
         wl = inputs.WORKLOADS[name]
-        L = Layer(fs, wl, layer=1)
+        L = Layer(fs, wl, layer=wl.layers - 1)
         runs = [L.run(fs) for _ in range(4)]
         for r in runs[1:]:
             assert_repeat_close(runs[0], r)
