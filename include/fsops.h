@@ -121,11 +121,12 @@ size_t fsops_scale_bytes(int rows, int K, fsops_scale_layout layout);
  *   to 4096): A is quantised by its own launch when bf16, then every block
  *   computes whole 128 x 256 output tiles.
  *   workspace: device scratch of at least fsops_gemm_workspace_bytes(M, N, K)
- *   bytes, all zero before its first use.  A successful call leaves its
- *   counters and split-K accumulators zero again, so the same workspace can be
- *   reused without clearing; after a call that reported an error (see
- *   fsops_read_kernel_status) zero it again.  One call at a time per
- *   workspace: calls that share a workspace must be ordered (same stream).
+ *   bytes, all zero before its first use.  Every call leaves its readiness
+ *   counters and split-K accumulators zero again (a call whose wait ran out
+ *   clears them before it returns), so the same workspace is reused without
+ *   clearing; bytes 8..15 keep a running count of the blocks that have left
+ *   the decode kernel.  One call at a time per workspace: calls that share a
+ *   workspace must be ordered (same stream).
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
  */
 fsops_status fsops_mxfp8_gemm(const void* a_bf16, const uint8_t* b_codes, const uint8_t* b_scales,
@@ -183,6 +184,13 @@ fsops_status fsops_swiglu_quantize_mxfp8(const float* gu, int M, int I, uint8_t*
  * device (INVALID_ARG if none or too small).  Calls on one device are ordered
  * by the caller (one stream, or events); concurrent calls would share the
  * workspace.
+ * Launch order: the decode launch (M <= 128) may begin while the previous
+ * kernel on the stream is finishing.  It starts streaming w_gateup, w_down
+ * and their scales at once and waits for that kernel before it touches
+ * anything else (x, y, the workspace).  So the weights must not be written
+ * by the kernel launched just before this call on the same stream (the
+ * library's own weight quantisers make their writes visible before they
+ * finish, so they may precede it).
  */
 fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup, const uint8_t* w_down,
                                     const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I,
@@ -373,7 +381,9 @@ fsops_status fsops_set_workspace(void* ws, size_t bytes);
  * (workspace NULL = the registered MLP workspace of the current device).
  * *word is 0 when no kernel failed; otherwise bits 31..24 hold an
  * fsops_status, bits 23..16 the wait site and bits 15..0 the block index.
- * After a failure the workspace counters are reset by the kernel itself. */
+ * After a failure the workspace counters are reset by the kernel itself: the
+ * blocks of a launch that gave up clear them once every block has left its
+ * waits. */
 fsops_status fsops_read_kernel_status(void* workspace, uint32_t* word);
 
 /* Upper bound, in nanoseconds, for every wait inside the kernels launched
@@ -404,7 +414,12 @@ fsops_status fsops_debug_set_extra_arrivals(uint32_t n);
  *                     cluster-sliced kernel.
  *   COOPERATIVE       1: launch the grid-wide kernel cooperatively instead
  *                     of as a plain launch that may start while the previous
- *                     kernel on the stream finishes. */
+ *                     kernel on the stream finishes.
+ *   EARLY_W           M > 16: 1 lets the weight producer fill its stages
+ *                     before x is available (PRIME loads in flight), 0
+ *                     holds it until the block's x loads are issued.
+ *   ALIGNED           split phases: 1 gives each block K stages of one tile
+ *                     only, 0 the even split over all tiles' stages. */
 typedef enum {
   FSOPS_KNOB_TR0 = 0,
   FSOPS_KNOB_TR1 = 1,
@@ -416,7 +431,9 @@ typedef enum {
   FSOPS_KNOB_LOCAL_XQ = 7,
   FSOPS_KNOB_DECODE_PATH = 8,
   FSOPS_KNOB_COOPERATIVE = 9,
-  FSOPS_KNOB_COUNT = 10
+  FSOPS_KNOB_EARLY_W = 10,
+  FSOPS_KNOB_ALIGNED = 11,
+  FSOPS_KNOB_COUNT = 12
 } fsops_knob;
 
 /* Set knob `knob` (an fsops_knob) to `value` (negative = back to the

@@ -178,8 +178,9 @@ MlpLayout mlp_layout(int M, int H, int I) {
   l.total = l.gu + round_up(static_cast<size_t>(M) * 2 * I * 4, 1024);
   return l;
 }
-// control words: header | hflags[I/128] | tile counters phase 0 | tile counters phase 1
-size_t ctl_words_needed(int I_chunks, int T0, int T1) { return kCtlHeaderWords + I_chunks + T0 + T1; }
+// control words of the grid-wide kernel: header | x readiness per block |
+// h readiness per block | tile counters phase 0 | tile counters phase 1
+size_t ctl_words_needed(int T0, int T1) { return kCtlHeaderWords + 2 * kMaxGrid + T0 + T1; }
 
 bool encode_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
@@ -280,6 +281,7 @@ void init_common(KernelArgs& a, int M, uint32_t* ctl) {
   const int inflight = knob_or(FSOPS_KNOB_MAX_INFLIGHT, kDefaultMaxInflight, 1, kMaxStages);
   a.max_inflight = inflight < a.nstages ? inflight : a.nstages;
   a.prime_inflight = knob_or(FSOPS_KNOB_PRIME, kPrimeInflight, 1, kMaxStages);
+  a.early_w = knob_or(FSOPS_KNOB_EARLY_W, 0, 0, 1);
   a.stage_bytes = stage_bytes_for(a.npad);
   a.timeout_ns = g_timeout_ns.load();
   a.extra_xready = g_extra.load();
@@ -326,7 +328,24 @@ bool grid_fits_cached(int grid, size_t smem) {
   return fit;
 }
 
+// Stream-K (an even split of the T x KS units, so a block may hold the end of
+// one tile and the start of the next) or the tile-aligned split (each block
+// on one tile; with T <= grid and at least one stage per block).  A block
+// holding two tiles runs two accumulator rounds, two readiness waits and two
+// split-K reductions, and the tiles it holds finish only after both.  The
+// aligned split is taken wherever it applies, although its largest share can
+// be a few stages above stream-K's: it measured faster at every decode shape
+// (H = 4096, I = 12288, M = 64: 43.4 against 46.9 us; H = 5120, I = 17408,
+// M = 32: 60.8 against 66.4 us; equal at M = 128).
+void choose_split(PhaseArgs& ph, int grid) {
+  ph.aligned = 0;
+  if (ph.whole_tiles || ph.pairs || ph.T > grid) return;
+  if (ph.KS < (grid + ph.T - 1) / ph.T) return;
+  ph.aligned = knob(FSOPS_KNOB_ALIGNED) == 0 ? 0 : 1;
+}
+
 fsops_status launch(KernelArgs& a, int grid, cudaStream_t stream) {
+  if (grid > kMaxGrid) return FSOPS_ERR_UNSUPPORTED_SHAPE;  // one readiness counter per block
   a.nstages = stages_for(a.npad, a.local_xq);
   if (a.max_inflight > a.nstages) a.max_inflight = a.nstages;
   bool pairs = false;
@@ -336,6 +355,7 @@ fsops_status launch(KernelArgs& a, int grid, cudaStream_t stream) {
     pairs = false;
   }
   a.cluster_pairs = pairs ? 1 : 0;
+  for (int p = 0; p < a.nphases; ++p) choose_split(a.ph[p], grid);
   const size_t smem = smem_for(a.npad, a.local_xq);
   // a plain launch with programmatic dependent launch by default (see
   // launch_mx_kernel); cooperative when forced or when the grid might not be
@@ -358,9 +378,9 @@ fsops_status fill_mlp_args(KernelArgs& ka, const MlpPlan& pl, const MlpBuffers& 
                            void* y_bf16, int M, int H, int I, const void* residual = nullptr,
                            const void* gamma = nullptr, float eps = 0.f) {
   init_common(ka, M, reinterpret_cast<uint32_t*>(b.ctl));
-  const int Ic = I / 128;  // 128-feature chunks (phase-1 k-stages)
-  if (ctl_words_needed(Ic, pl.T0, pl.T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
-  ka.hflags = ka.ctl + kCtlHeaderWords;
+  if (ctl_words_needed(pl.T0, pl.T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  ka.xready = ka.ctl + kCtlHeaderWords;
+  ka.hflags = ka.xready + kMaxGrid;
   ka.nphases = 2;
   ka.x = static_cast<const uint16_t*>(x_bf16);
   ka.xq_codes = b.xq;
@@ -375,7 +395,7 @@ fsops_status fill_mlp_args(KernelArgs& ka, const MlpPlan& pl, const MlpBuffers& 
   PhaseArgs& p0 = ka.ph[0];
   p0.sf_w = scales->gateup;
   p0.sf_act = ka.xq_sf;
-  p0.tile_cnt = ka.hflags + Ic;
+  p0.tile_cnt = ka.hflags + kMaxGrid;
   p0.accum = reinterpret_cast<float*>(b.part0);
   p0.KS = H / kTileK;
   p0.T = pl.T0;
@@ -423,7 +443,7 @@ bool slice_plan(int M, int H, int I, int sms, SlicePlan* sp) {
   const int NP = sms / kSliceCluster < NC ? sms / kSliceCluster : NC;
   if ((NC + NP - 1) / NP > kSliceMaxChunks) return false;
   const int RT = H / 128;
-  if ((RT + 1) / 2 > 256 || ctl_words_needed(0, 0, RT) * 4 > kCtlRegionBytes) return false;
+  if ((RT + 1) / 2 > 256 || (kCtlHeaderWords + RT) * 4 > static_cast<int>(kCtlRegionBytes)) return false;
   sp->NC = NC;
   sp->NP = NP;
   sp->RT = RT;
@@ -594,7 +614,9 @@ fsops_status gemm_impl(const void* a, const uint8_t* a_scales, bool a_bf16, cons
   p.rows = N;
   p.epi = kEpiStore;
   p.out_ld = N;
-  p.tile_cnt = ka.ctl + kCtlHeaderWords;
+  if (kCtlHeaderWords + kMaxGrid + p.T > static_cast<int>(kCtlRegionBytes / 4)) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  ka.xready = ka.ctl + kCtlHeaderWords;
+  p.tile_cnt = ka.xready + kMaxGrid;
   p.accum = reinterpret_cast<float*>(part);
   const uint8_t* act_codes;
   if (a_bf16) {
@@ -1165,7 +1187,7 @@ fsops_status fsops_mxfp8_swiglu_mlp_noalloc(const void* x_bf16, const uint8_t* w
   SlicePlan sp;
   const bool sliced = use_slice(M, H, I, di, &sp);
   const MlpPlan pl = plan_mlp(M, H, I, grid);
-  if (!sliced && ctl_words_needed(I / 128, pl.T0, pl.T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  if (!sliced && ctl_words_needed(pl.T0, pl.T1) * 4 > kCtlRegionBytes) return FSOPS_ERR_UNSUPPORTED_SHAPE;
   // the sliced kernel needs the control words and its row-tile sums only
   const size_t slice_end = kCtlRegionBytes + (sliced ? slice_accum_bytes(M, H) : 0);
   const NoAllocLayout l = noalloc_layout(M, H, I, pl);

@@ -119,6 +119,9 @@ __global__ void __launch_bounds__(256) bs_quantize_blocks_kernel(const uint16_t*
       dst[i] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
   }
+  // the GEMM launched next may stream these weights before it waits for this
+  // kernel (programmatic launch): the writes are visible before the block leaves
+  __threadfence();
 }
 
 }  // namespace

@@ -21,12 +21,16 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // into 32 codes packed four to a word; returns the scale byte.
 __device__ __forceinline__ uint32_t quantize_block_pack(const uint4 (&raw)[4], uint32_t (&packed)[8]) {
   const uint32_t* w = reinterpret_cast<const uint32_t*>(raw);
-  uint32_t amax_bits = 0;
+  // largest magnitude: the bf16 bit patterns without sign compare as unsigned
+  // integers; a tree of per-halfword maxima keeps the dependency chain short
+  uint32_t m[8];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    amax_bits = max(amax_bits, (w[i] & 0x7FFFu) << 16);
-    amax_bits = max(amax_bits, w[i] & 0x7FFF0000u);
-  }
+  for (int i = 0; i < 8; ++i) m[i] = __vmaxu2(w[2 * i] & 0x7FFF7FFFu, w[2 * i + 1] & 0x7FFF7FFFu);
+#pragma unroll
+  for (int d = 4; d >= 1; d >>= 1)
+#pragma unroll
+    for (int i = 0; i < d; ++i) m[i] = __vmaxu2(m[i], m[i + d]);
+  const uint32_t amax_bits = max(m[0] & 0xFFFFu, m[0] >> 16) << 16;
   const uint32_t s = ue8m0_from_amax(__uint_as_float(amax_bits));
   const float inv = inv_scale_from_ue8m0(s);
 #pragma unroll

@@ -11,10 +11,15 @@ namespace fsops {
 // Control words at the start of every workspace (uint32 indices).
 enum CtlWord : int {
   kCtlStatus = 0,   // first error: (status << 24) | (site << 16) | block
-  kCtlXReady = 1,   // number of blocks that finished quantising their slice of x
-  kCtlDone = 2,     // number of blocks that finished the launch
+  kCtlCleanup = 1,  // taken by the block that clears the control words after a launch gave up
+  kCtlExits = 2,    // words 2-3: 64-bit count of blocks that have left, over all launches
   kCtlHeaderWords = 16,
 };
+// Readiness counters kept per consuming block (at most kMaxGrid blocks): each
+// producer adds to the counter of every block that will read what it wrote,
+// and each block clears its own counter once it has seen it complete, so a
+// launch that succeeds leaves them zero without a grid-wide last step.
+constexpr int kMaxGrid = 256;
 // Wait sites reported in the status word.
 enum WaitSite : uint32_t {
   kSiteEmpty = 1, kSiteFullW = 2, kSiteFullA = 3, kSiteAccEmpty = 4, kSiteAccFull = 5,
@@ -56,6 +61,9 @@ struct PhaseArgs {
   int whole_tiles;        // 1: block t < T does all of tile t (requires T <= grid), no split-K
   int pairs;              // 1: the two blocks of cluster c split tile c in two K halves and add
                           //    their sums through distributed shared memory (M <= 32, T <= grid / 2)
+  int aligned;            // 1: tile t goes to blocks [ceil(t G / T), ceil((t+1) G / T)), which split
+                          //    its K range evenly (T <= grid, KS >= ceil(G / T)): no block holds
+                          //    parts of two tiles
   int dep;                // what the activation loads wait for (kDep*)
   int epi;                // epilogue kind (kEpi*)
   int out_ld;             // row stride (elements) of the plain output
@@ -84,7 +92,8 @@ struct KernelArgs {
   const uint16_t* residual;  // bf16 [M, out_ld] added to a bf16 output before its rounding, or null
   // control
   uint32_t* ctl;          // kCtlHeaderWords words
-  uint32_t* hflags;       // [I / 128]: 1 once SwiGLU tile t (features 128t..128t+127) is written
+  uint32_t* xready;       // [grid]: x slices quantised for block b (grid-wide x quantisation)
+  uint32_t* hflags;       // [grid]: SwiGLU tiles written that block b's down-projection stages read
   int M;
   int npad;               // M rounded up to 16: activation rows held in shared memory
   int nstages;
@@ -93,10 +102,11 @@ struct KernelArgs {
   int cluster_pairs;      // launched as 2-block clusters (a phase uses pairs)
   int max_inflight;       // weight tiles a block may have in flight at once
   int prime_inflight;     // ... before its activations are available (x quantised grid-wide)
+  int early_w;            // 1: the weight producer starts before the block's x loads are issued
   uint32_t stage_bytes;
   uint64_t timeout_ns;
   uint32_t extra_xready;  // test hook: extra arrivals to wait for
-  unsigned long long* trace;  // [grid][64] %globaltimer stamps, builds with FSOPS_TRACE only
+  unsigned long long* trace;  // [grid][128] %globaltimer stamps, builds with FSOPS_TRACE only
 };
 
 // Shared-memory stage layout: X (activations, npad x 128 B), W (weights,

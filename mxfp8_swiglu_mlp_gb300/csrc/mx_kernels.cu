@@ -61,6 +61,10 @@ __global__ void quantize_kernel(const uint16_t* __restrict__ x, const uint16_t* 
       scales[static_cast<long long>(r) * nb + kb] = static_cast<uint8_t>(s);
     }
   }
+  // weights quantised here may be streamed by the next kernel on the stream
+  // before it waits for this one (the decode kernels' programmatic launch):
+  // the writes are made visible before the block leaves
+  __threadfence();
 }
 
 cudaError_t launch_quantize(const uint16_t* x, int rows, int K, int ld, uint8_t* codes, uint8_t* scales,
@@ -230,7 +234,7 @@ cudaError_t launch_swiglu_quantize(const float* gu, int M, int I, uint8_t* hc, u
 #ifdef FSOPS_TRACE
 #define FSOPS_STAMP(idx)                                                         \
   do {                                                                           \
-    if (a.trace != nullptr) a.trace[blockIdx.x * 64 + (idx)] = globaltimer_ns(); \
+    if (a.trace != nullptr) a.trace[blockIdx.x * 128 + (idx)] = globaltimer_ns(); \
   } while (0)
 #define FSOPS_STAMP_IF(cond, idx) \
   do {                            \
@@ -255,13 +259,33 @@ __device__ __forceinline__ uint32_t split_owner(uint32_t u, uint32_t U, uint32_t
   return ((u + 1) * G + U - 1) / U - 1;
 }
 
+// Tile-aligned split: the first block of tile t, ceil(t G / T).
+__device__ __forceinline__ uint32_t aligned_first(uint32_t t, uint32_t T, uint32_t G) { return (t * G + T - 1) / T; }
+// The blocks that add split sums into tile t of phase ph.
+__device__ __forceinline__ uint32_t tile_owners(const PhaseArgs& ph, int t, uint32_t G) {
+  const uint32_t T = static_cast<uint32_t>(ph.T), KS = static_cast<uint32_t>(ph.KS);
+  if (ph.aligned) return aligned_first(t + 1, T, G) - aligned_first(t, T, G);
+  const uint32_t U = T * KS;
+  const uint32_t cf = split_owner(t * KS, U, G), cl = split_owner(t * KS + KS - 1, U, G);
+  // with U >= G every block owns at least one unit; with U < G each owns at most one
+  return U >= G ? cl - cf + 1 : KS;
+}
+
 // Walks the segments (tile, ks0, ks1) of one phase assigned to this block.
 struct SegIter {
   uint32_t u, ue, KS;
-  __device__ SegIter(const PhaseArgs& p, uint32_t G) {
+  __device__ SegIter(const PhaseArgs& p, uint32_t G) : SegIter(p, G, blockIdx.x) {}
+  // the segments of block c
+  __device__ SegIter(const PhaseArgs& p, uint32_t G, uint32_t c) {
     KS = static_cast<uint32_t>(p.KS);
-    const uint32_t c = blockIdx.x;
-    if (p.whole_tiles) {
+    if (p.aligned) {
+      // block c works on tile t = floor(c T / G), as its j-th of n blocks
+      const uint32_t T = static_cast<uint32_t>(p.T);
+      const uint32_t t = c * T / G, f = aligned_first(t, T, G), n = aligned_first(t + 1, T, G) - f;
+      const uint32_t j = c - f;
+      u = t * KS + j * KS / n;
+      ue = t * KS + (j + 1) * KS / n;
+    } else if (p.whole_tiles) {
       u = c < static_cast<uint32_t>(p.T) ? c * KS : 0;
       ue = c < static_cast<uint32_t>(p.T) ? u + KS : 0;
     } else if (p.pairs) {
@@ -285,6 +309,35 @@ struct SegIter {
     return true;
   }
 };
+
+// The block that holds unit (tile t, k-stage ks) of phase ph.
+__device__ __forceinline__ uint32_t unit_owner(const PhaseArgs& ph, uint32_t t, uint32_t ks, uint32_t G) {
+  const uint32_t T = static_cast<uint32_t>(ph.T), KS = static_cast<uint32_t>(ph.KS);
+  if (ph.whole_tiles) return t;
+  if (ph.pairs) return 2 * t + (ks >= KS / 2 ? 1u : 0u);
+  if (ph.aligned) {
+    const uint32_t f = aligned_first(t, T, G);
+    return f + split_owner(ks, KS, aligned_first(t + 1, T, G) - f);
+  }
+  return split_owner(t * KS + ks, T * KS, G);
+}
+// Whether block c holds any unit of phase ph.
+__device__ __forceinline__ bool has_units(const PhaseArgs& ph, uint32_t c, uint32_t G) {
+  const SegIter it(ph, G, c);
+  return it.ue > it.u;
+}
+// SwiGLU tiles of phase 0 per 128-feature chunk of h.
+__device__ __forceinline__ uint32_t tiles_per_chunk(const KernelArgs& a) {
+  return (a.ph[0].tile_rows == 128 ? 2u : 1u) * (a.ph[0].pairs ? 2u : 1u);
+}
+// After SwiGLU tile t of phase 0 (h features [t R / 2, (t + 1) R / 2), R its
+// rows) is written and ordered by a barrier: epilogue thread et tells the
+// blocks whose down-projection stages read its 128-feature chunk.
+__device__ __forceinline__ void publish_h(const KernelArgs& a, int t, int et, uint32_t G) {
+  const PhaseArgs& p1 = a.ph[1];
+  const uint32_t c = static_cast<uint32_t>((t * a.ph[0].tile_rows) >> 8);
+  for (int t1 = et; t1 < p1.T; t1 += 128) red_add_release_gpu(a.hflags + unit_owner(p1, t1, c, G), 1u);
+}
 
 // ----------------------------------------------------------------------------
 // Epilogue pieces.  A tile's result row for token r is 256 fp32 values (128
@@ -391,10 +444,8 @@ __device__ __forceinline__ void finish_staged(const KernelArgs& a, const PhaseAr
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       const uint32_t sc = ue8m0_from_amax(amax);
       const float inv = inv_scale_from_ue8m0(sc);
-      const uint32_t lo = e4m3_code(h[0] * inv) | (e4m3_code(h[1] * inv) << 8) | (e4m3_code(h[2] * inv) << 16) |
-                          (e4m3_code(h[3] * inv) << 24);
-      const uint32_t hi = e4m3_code(h[4] * inv) | (e4m3_code(h[5] * inv) << 8) | (e4m3_code(h[6] * inv) << 16) |
-                          (e4m3_code(h[7] * inv) << 24);
+      const uint32_t lo = e4m3x4_code(h[0] * inv, h[1] * inv, h[2] * inv, h[3] * inv);
+      const uint32_t hi = e4m3x4_code(h[4] * inv, h[5] * inv, h[6] * inv, h[7] * inv);
       if (r < a.M) {
         const int f0 = f_tile + 32 * b;
         *reinterpret_cast<uint2*>(a.hq_codes + static_cast<long long>(r) * a.I + f0 + 8 * part) = make_uint2(lo, hi);
@@ -453,6 +504,10 @@ __device__ __noinline__ bool finish_slice(const KernelArgs& a, const PhaseArgs& 
   const bool okw = *bcast != 0;
   epi_bar();
   if (!okw) return false;
+  // a second count: the owner that brings it to 2 owners clears the counter,
+  // after every owner's wait has seen it complete
+  uint32_t seen = 0;
+  if (et == 0) seen = atom_add_acq_rel_gpu(ph.tile_cnt + t, 1u);
   float* accg = ph.accum + static_cast<long long>(t) * a.M * kTileRows;
   const int r0 = a.M * arrival / owners, r1 = a.M * (arrival + 1) / owners;
   const int lg = ncols == 256 ? 5 : 4;  // log2(8-column items per row)
@@ -478,6 +533,7 @@ __device__ __noinline__ bool finish_slice(const KernelArgs& a, const PhaseArgs& 
       }
     }
   }
+  if (et == 0 && seen + 1 == 2u * static_cast<uint32_t>(owners)) ph.tile_cnt[t] = 0u;
   epi_bar();  // every read of the rows before they are cleared
   // rows [r0, r1), columns [0, ncols) (row stride kTileRows)
 #pragma unroll 1
@@ -502,9 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   uint64_t* drain = acc_empty + 1;
   uint64_t* x_issued = drain + 1;
   uint64_t* x_full = x_issued + 1;          // [kMaxXSlots] bf16 x tile landed (local_xq)
-  uint64_t* peer_ready = x_full + kMaxXSlots;  // the other block of the pair has staged its sums
-  uint64_t* peer_done = peer_ready + 1;        // ... and has read this block's
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(peer_done + 1);
+  uint64_t* peer_ready = x_full + kMaxXSlots;  // the other block of the pair has pushed its sums of this block's half
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(peer_ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
   // 0 until this block's activations are available (x quantised grid-wide,
@@ -529,7 +584,6 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     mbar_init(x_issued, 128);
     for (int i = 0; i < kMaxXSlots; ++i) mbar_init(&x_full[i], 1);
     mbar_init(peer_ready, 1);
-    mbar_init(peer_done, 1);
     *abort_flag = 0;
     *flowing = (a.x != nullptr && !a.local_xq) ? 0 : 1;
     mbar_fence_init();
@@ -573,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     uint32_t lag_round = 0, n_issued = 0, n_landed = 0;
     bool ok = true;
     // let the epilogue warps' loads of x enter the memory system first
-    if (a.x != nullptr && !a.local_xq) ok = wait_mbar(cx, x_issued, 0, kSiteEmpty);
+    if (a.x != nullptr && !a.local_xq && !a.early_w) ok = wait_mbar(cx, x_issued, 0, kSiteEmpty);
     for (int p = 0; p < a.nphases && ok; ++p) {
       const PhaseArgs& ph = a.ph[p];
       SegIter it(ph, static_cast<uint32_t>(G));
@@ -617,66 +671,22 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     // this grid start while it finishes); the weights never are, so the
     // weight producer starts at once.
     griddep_wait();
-    // Lane 0 issues the TMA loads.  With local_xq the whole warp quantises
-    // phase 0's activation tiles itself: lane 0 streams the bf16 x tiles of the
-    // segment into a ring (kMaxXSlots ahead), every lane quantises its 32-blocks
-    // straight into the stage, in step with the stage ring.
+    if (lane == 0) FSOPS_STAMP(64);
+    // Lane 0 issues the TMA loads.  With local_xq phase 0's activation tiles
+    // are quantised by the epilogue warps, which fill those stages themselves.
     const uint64_t pol = l2_policy_evict_last();
     uint32_t issued_mask = 0, issued_parity = 0;
     int stage = 0;
     uint32_t round = 0;
     bool ok = true, x_ready = false, h_seen = false;
-    uint32_t xc = 0;  // x tiles streamed so far (slot xc % kMaxXSlots, parity (xc / kMaxXSlots) & 1)
-    uint32_t xmask = 0, xparity = 0;
     for (int p = 0; p < a.nphases && ok; ++p) {
       const PhaseArgs& ph = a.ph[p];
       SegIter it(ph, static_cast<uint32_t>(G));
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
         if (p == 0 && a.local_xq) {
-          const int n = ks1 - ks0;
-          auto issue_x = [&](int i) {  // lane 0: x tile of stage ks0 + i into its slot
-            const uint32_t c = xc + i, slot = c % kMaxXSlots;
-            mbar_arrive_expect_tx(&x_full[slot], 256u * npad);
-            tma_load_2d(xring + slot * 256 * npad, &a.tm_x, &x_full[slot], (ks0 + i) * kTileK, 0, pol);
-            xmask |= 1u << slot;
-            xparity = (xparity & ~(1u << slot)) | (((c / kMaxXSlots) & 1u) << slot);
-          };
-          if (lane == 0)
-            for (int i = 0; i < n && i < kMaxXSlots; ++i) issue_x(i);
-          for (int i = 0; i < n; ++i) {
-            const uint32_t c = xc + i, slot = c % kMaxXSlots;
-            ok = __all_sync(0xFFFFFFFFu, wait_mbar(cx, &x_full[slot], (c / kMaxXSlots) & 1u, kSiteFullA));
-            if (!ok) break;
-            // each lane: blocks b = lane, lane + 32, ... of the npad x 4 block grid
-            uint4 raw[2][4];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const int b = lane + 32 * q;
-              if (b < 4 * npad) {
-                const uint4* src = reinterpret_cast<const uint4*>(xring + slot * 256 * npad + (b >> 2) * 256 + (b & 3) * 64);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) raw[q][k] = src[k];
-              }
-            }
-            // the slot may be refilled once every lane has read it
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0 && i + kMaxXSlots < n) issue_x(i + kMaxXSlots);
-            ok = __all_sync(0xFFFFFFFFu, wait_mbar(cx, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty));
-            if (!ok) break;
-            uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const int b = lane + 32 * q;
-              if (b < 4 * npad) store_x_block(a, st, b, raw[q]);
-            }
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full_a[stage]);
+          for (int ks = ks0; ks < ks1; ++ks)
             if (++stage == S) { stage = 0; ++round; }
-          }
-          xc += n;
           continue;
         }
         if (lane != 0) {
@@ -687,24 +697,28 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
         for (int ks = ks0; ks < ks1; ++ks) {
           if (!wait_mbar(cx, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty)) { ok = false; break; }
           if (ph.dep == kDepXReady && !x_ready) {
-            if (!wait_counters(cx, a.ctl + kCtlXReady, 1, static_cast<uint32_t>(G) + a.extra_xready,
+            // every block's slice of x
+            if (!wait_counters(cx, a.xready + blockIdx.x, 1, static_cast<uint32_t>(G) + a.extra_xready,
                                kSiteXReady)) {
               ok = false;
               break;
             }
+            a.xready[blockIdx.x] = 0u;  // complete: no further adds this launch
             fence_proxy_async_global();
             x_ready = true;
             *flowing = 1;
             FSOPS_STAMP(2);
-          } else if (ph.dep == kDepHFlags && ks == ks0) {
-            // the whole k-range of the segment: the SwiGLU tile of every 128-feature chunk
-            const uint32_t tiles_per_chunk = (a.ph[0].tile_rows == 128 ? 2u : 1u) * (a.ph[0].pairs ? 2u : 1u);
-            if (!wait_counters(cx, a.hflags + ks0, ks1 - ks0, tiles_per_chunk + a.extra_xready, kSiteHFlag)) {
+          } else if (ph.dep == kDepHFlags && !h_seen) {
+            // the SwiGLU tiles of every 128-feature chunk of every stage of this phase
+            const SegIter all(ph, static_cast<uint32_t>(G));
+            const uint32_t want = (all.ue - all.u) * tiles_per_chunk(a) + a.extra_xready;
+            if (!wait_counters(cx, a.hflags + blockIdx.x, 1, want, kSiteHFlag)) {
               ok = false;
               break;
             }
+            a.hflags[blockIdx.x] = 0u;  // complete: no further adds this launch
             fence_proxy_async_global();
-            if (!h_seen) FSOPS_STAMP(5);
+            FSOPS_STAMP(5);
             h_seen = true;
             *flowing = 1;
             FSOPS_STAMP(6);
@@ -723,8 +737,6 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     if (lane == 0) {
       for (int s = 0; s < S; ++s)
         if (issued_mask & (1u << s)) drain_mbar(&full_a[s], (issued_parity >> s) & 1u, 200000000ull);
-      for (int s = 0; s < kMaxXSlots; ++s)
-        if (xmask & (1u << s)) drain_mbar(&x_full[s], (xparity >> s) & 1u, 200000000ull);
     }
   } else if (warp == 2 && lane == 0) {
     // ------------------------------------------------ MMA issuer
@@ -784,7 +796,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     // ------------------------------------------------ epilogue warps
     const int et = threadIdx.x - 128;  // token row of the accumulator (TMEM lane)
     const int ew = et >> 5;
+    const uint32_t pair_h = blockIdx.x & 1u, pair_peer = pair_h ^ 1u;  // cluster pairs: rank, partner
     griddep_wait();  // x, the workspace and y may be in use by the previous kernel until here
+    if (et == 0) FSOPS_STAMP(65);
     // (1) grid-wide: quantise this block's slice of x, the 32-blocks [b0, b1)
     // of the row-major [npad, H/32] block grid (rows >= M only get a zero scale)
     if (a.x != nullptr && !a.local_xq) {
@@ -840,10 +854,11 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       if (et == 0) FSOPS_STAMP(63);
       fence_proxy_async_global();
       epi_bar();
-      if (et == 0) {
-        red_add_release_gpu(a.ctl + kCtlXReady, 1u);
-        FSOPS_STAMP(1);
-      }
+      // to every block whose first phase reads x (each waits for all G slices)
+      for (int c = et; c < static_cast<int>(G); c += 128)
+        if (has_units(a.ph[0], static_cast<uint32_t>(c), static_cast<uint32_t>(G)))
+          red_add_release_gpu(a.xready + c, 1u);
+      if (et == 0) FSOPS_STAMP(1);
     }
     // (2) accumulators
     uint32_t acc_round = 0;
@@ -851,12 +866,85 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     int4 pend[kMaxPend];  // split tiles to finish at the end of the phase: (t, arrival, owners, ncols)
     int npend = 0;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(ew * 32) << 16);
+    // With local_xq the epilogue warps fill phase 0's activation stages.  The
+    // block's phase-0 stages are its consecutive units u0, u0 + 1, ... (stage
+    // c: ring position c % S, k-stage (u0 + c) % KS).  Stage c belongs to warp
+    // c % 4, which streams the stage's bf16 x tile into its own slot of the x
+    // ring one tile ahead and quantises it straight into the stage: four
+    // stages are in work at once.  Before the accumulator of a segment ending
+    // at stage e is awaited, every stage below e + S is filled: those need no
+    // MMA of a later segment (whose accumulator is not yet free) to release
+    // their ring position, and the next segment's first stages are ready
+    // while this one's epilogue runs.
+    uint32_t xu0 = 0, xn0 = 0, xks = 1;
+    if (a.local_xq) {
+      SegIter it0(a.ph[0], static_cast<uint32_t>(G));
+      xu0 = it0.u;
+      xn0 = it0.ue - it0.u;
+      xks = it0.KS;
+    }
+    uint32_t xc = static_cast<uint32_t>(ew);  // next stage of this warp
+    uint32_t x_pend = 0xFFFFFFFFu;            // stage whose tile is in flight into this warp's slot
+    const uint64_t x_pol = l2_policy_evict_last();
+    uint8_t* xslot = xring + ew * 256 * npad;
+    auto issue_x = [&](uint32_t c) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&x_full[ew], 256u * npad);
+        tma_load_2d(xslot, &a.tm_x, &x_full[ew], static_cast<int>((xu0 + c) % xks) * kTileK, 0, x_pol);
+      }
+      x_pend = c;
+    };
+    if (a.local_xq && xc < xn0) issue_x(xc);
+    auto quantize_upto = [&](uint32_t L) -> bool {
+      for (; xc < L; xc += 4) {
+        const uint32_t c = xc;
+        if (!__all_sync(0xFFFFFFFFu, wait_mbar(cx, &x_full[ew], (c >> 2) & 1u, kSiteFullA))) return false;
+        x_pend = 0xFFFFFFFFu;
+        if (lane == 0) FSOPS_STAMP_IF(c < 6, 66 + c);
+        // each lane: blocks b = lane, lane + 32 of the npad x 4 block grid
+        uint4 raw[2][4];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int b = lane + 32 * q;
+          if (b < 4 * npad) {
+            const uint4* src = reinterpret_cast<const uint4*>(xslot + (b >> 2) * 256 + (b & 3) * 64);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) raw[q][k] = src[k];
+          }
+        }
+        // the slot may be refilled once every lane has read it
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (c + 4 < xn0) issue_x(c + 4);
+        if (lane == 0) FSOPS_STAMP_IF(c == 2, 80);
+        const int stage = static_cast<int>(c % static_cast<uint32_t>(S));
+        const uint32_t round = c / static_cast<uint32_t>(S);
+        if (!__all_sync(0xFFFFFFFFu, wait_mbar(cx, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty))) return false;
+        if (lane == 0) FSOPS_STAMP_IF(c == 2, 81);
+        uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int b = lane + 32 * q;
+          if (b < 4 * npad) store_x_block(a, st, b, raw[q]);
+        }
+        if (lane == 0) FSOPS_STAMP_IF(c == 2, 82);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_a[stage]);
+        if (lane == 0) FSOPS_STAMP_IF(c < 6, 72 + c);
+      }
+      return true;
+    };
+    uint32_t xseg_end = 0;  // phase-0 stages up to the end of the current segment
     for (int p = 0; p < a.nphases && ok; ++p) {
       const PhaseArgs& ph = a.ph[p];
-      const uint32_t U = static_cast<uint32_t>(ph.T * ph.KS);
       SegIter it(ph, static_cast<uint32_t>(G));
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
+        if (p == 0 && a.local_xq) {
+          xseg_end += static_cast<uint32_t>(ks1 - ks0);
+          if (!epi_and(quantize_upto(min(xn0, xseg_end + static_cast<uint32_t>(S))))) { ok = false; break; }
+        }
         if (!epi_and(wait_mbar(cx, acc_full, acc_round & 1u, kSiteAccFull))) { ok = false; break; }
         ++acc_round;
         tc_fence_after();
@@ -869,7 +957,13 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           // loads in flight per wait) and the accumulator is released at once;
           // all four warps share the rest.  Split tiles add their rows into a
           // row-major [M][256] accumulator, four columns per reduction.
+          // A cluster pair (ph.pairs) splits the tile's K range: each block
+          // keeps the sums of its own half of the columns, [128 h, 128 h + 128),
+          // and pushes the other half into the partner's stg, at the columns of
+          // its own half there (which the partner does not use), then arrives
+          // on the partner's peer_ready.
           if (ew == 0) {
+            const uint32_t pstg = ph.pairs ? mapa_shared(stg, pair_peer) : 0u;
 #pragma unroll 1
             for (int c0 = 0; c0 < ncols; c0 += 64) {
               uint32_t v[4][16];
@@ -877,12 +971,25 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
               for (int q = 0; q < 4; ++q) tmem_ld16(tlane + c0 + 16 * q, v[q]);
               tmem_ld_wait();
               if (lane < a.M) {
-                float4* d = reinterpret_cast<float4*>(stg + lane * kStageLd + c0);
+                if (ph.pairs && static_cast<uint32_t>(c0 >> 7) != pair_h) {
+                  const uint32_t dst = pstg + static_cast<uint32_t>(lane * kStageLd + (c0 ^ 128)) * 4u;
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
-                  d[q] = make_float4(__uint_as_float(v[q >> 2][4 * (q & 3)]), __uint_as_float(v[q >> 2][4 * (q & 3) + 1]),
-                                     __uint_as_float(v[q >> 2][4 * (q & 3) + 2]), __uint_as_float(v[q >> 2][4 * (q & 3) + 3]));
+                  for (int q = 0; q < 16; ++q)
+                    st_shared_cluster_v4(dst + 16u * q, make_uint4(v[q >> 2][4 * (q & 3)], v[q >> 2][4 * (q & 3) + 1],
+                                                                   v[q >> 2][4 * (q & 3) + 2], v[q >> 2][4 * (q & 3) + 3]));
+                } else {
+                  float4* d = reinterpret_cast<float4*>(stg + lane * kStageLd + c0);
+#pragma unroll
+                  for (int q = 0; q < 16; ++q)
+                    d[q] = make_float4(__uint_as_float(v[q >> 2][4 * (q & 3)]), __uint_as_float(v[q >> 2][4 * (q & 3) + 1]),
+                                       __uint_as_float(v[q >> 2][4 * (q & 3) + 2]), __uint_as_float(v[q >> 2][4 * (q & 3) + 3]));
+                }
               }
+            }
+            if (ph.pairs) {
+              fence_acq_rel_cluster();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_remote(mapa_shared(peer_ready, pair_peer));
             }
           }
           tc_fence_before();
@@ -950,34 +1057,30 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           if (et == 0) FSOPS_STAMP_IF(p == 0, 13);
         } else if (ph.pairs) {
           // The two blocks of this cluster hold the two K halves of tile t
-          // (M <= 32, both staged in shared memory).  Each adds the other's sums
-          // of its half of the columns, [128 h, 128 h + 128) = 32-blocks 2h, 2h+1,
-          // read through distributed shared memory, and finishes those features.
-          const uint32_t peer = (blockIdx.x & 1u) ^ 1u;
-          const int h = static_cast<int>(blockIdx.x & 1u);
-          if (et == 0) mbar_arrive_remote(mapa_shared(peer_ready, peer));  // my sums are staged (epi_bar above)
+          // (M <= 32, staged in shared memory).  Once the partner's sums of
+          // this block's half of the columns, [128 h, 128 h + 128) = 32-blocks
+          // 2h, 2h+1, have arrived (pushed into this block's stg at the
+          // partner's half's columns), they are added and those features
+          // finished.  The partner writes nothing here after that arrival.
+          const int h = static_cast<int>(pair_h);
           if (!epi_and(wait_mbar_cluster(cx, peer_ready, 0, kSitePeer))) { ok = false; break; }
           if (et == 0) FSOPS_STAMP(58);
-          const uint32_t pstg = mapa_shared(stg, peer);
 #pragma unroll 1
           for (int i = et; i < (a.M << 5); i += 128) {
             const int r = i >> 5, c = 128 * h + (i & 31) * 4;
-            const float4 pv = ld_shared_cluster_v4(pstg + static_cast<uint32_t>(r * kStageLd + c) * 4u);
+            const float4 pv = *reinterpret_cast<const float4*>(stg + r * kStageLd + (c ^ 128));
             float4* mine = reinterpret_cast<float4*>(stg + r * kStageLd + c);
             const float4 mv = *mine;
             *mine = make_float4(mv.x + pv.x, mv.y + pv.y, mv.z + pv.z, mv.w + pv.w);
           }
           epi_bar();
           if (et == 0) FSOPS_STAMP(59);
-          if (et == 0) mbar_arrive_remote(mapa_shared(peer_done, peer));  // done with the peer's stg
           finish_staged(a, ph, t, 256, stg, et, 2 * h, 2);
           if (et == 0) FSOPS_STAMP_IF(p == 0, 13);
           fence_proxy_async_global();
           epi_bar();
-          if (et == 0) red_add_release_gpu(a.hflags + ((t * ph.tile_rows) >> 8), 1u);
+          publish_h(a, t, et, static_cast<uint32_t>(G));
           if (et == 0) FSOPS_STAMP(14);
-          // the peer reads this block's stg: it is written again only after that
-          if (!epi_and(wait_mbar_cluster(cx, peer_done, 0, kSitePeer))) { ok = false; break; }
           if (et == 0) FSOPS_STAMP(p == 0 ? 4 : 9);
           continue;
         } else {
@@ -986,16 +1089,17 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           // arrives last reads the total, finishes the tile and leaves the
           // accumulator zero for the next launch.
           // (whole_tiles phases never get here)
-          const uint32_t cf = split_owner(static_cast<uint32_t>(t * ph.KS), U, static_cast<uint32_t>(G));
-          const uint32_t cl = split_owner(static_cast<uint32_t>(t * ph.KS + ph.KS - 1), U, static_cast<uint32_t>(G));
-          // with U >= G every block owns at least one unit; with U < G each owns at most one
-          const uint32_t expected = U >= static_cast<uint32_t>(G) ? cl - cf + 1 : static_cast<uint32_t>(ph.KS);
+          const uint32_t expected = tile_owners(ph, t, static_cast<uint32_t>(G));
           // the barrier orders every thread's adds before thread 0's acq_rel
           // counter update, which in turn orders the last arriver's reads
           epi_bar();
           if (et == 0) {
             const uint32_t old = atom_add_acq_rel_gpu(ph.tile_cnt + t, 1u);
             *bcast = static_cast<int>(old);
+            // the last arrival finishes the tile (except plain output at
+            // M > 32, where every owner finishes rows and finish_slice clears
+            // the counter): nothing reads the counter again this launch
+            if (old + 1 == expected && (a.stage_tmem || ph.epi == kEpiSwiGLU)) ph.tile_cnt[t] = 0u;
           }
           epi_bar();
           const uint32_t arrival = static_cast<uint32_t>(*bcast);
@@ -1083,8 +1187,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           fence_proxy_async_global();
           if (et == 0) FSOPS_STAMP(14);
           epi_bar();
-          // (hflags count per 128-feature chunk: a 128-row tile gives half of one)
-          if (et == 0) red_add_release_gpu(a.hflags + ((t * ph.tile_rows) >> 8), 1u);
+          publish_h(a, t, et, static_cast<uint32_t>(G));
         } else if (a.stage_tmem) {
           epi_bar();  // stg is reused by the next accumulator
         }
@@ -1095,14 +1198,19 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       if (et == 0) FSOPS_STAMP_IF(p == 1, 62);
     }
     if (!ok) *abort_flag = 1;
+    // a tile still in flight into this warp's x slot lands before the block leaves
+    if (x_pend != 0xFFFFFFFFu && lane == 0) drain_mbar(&x_full[ew], (x_pend >> 2) & 1u, 200000000ull);
+    if (et == 0) FSOPS_STAMP(79);
   }
 
   // ------------------------------------------------ teardown
-  // Thread 0 (the weight producer, done by now) waits for the previous grid
-  // before it touches the control words.  The wait holds the whole warp, so
-  // no other lane of warp 0 (or of warp 2, the MMA issuer's) executes it:
-  // those lanes reach this point while lane 0 is still streaming.
-  if (threadIdx.x == 0) griddep_wait();
+  // After a launch that completes, every control word it used is back at
+  // zero already: each readiness counter was cleared by the block it counts
+  // for, each split tile's counter by its last arrival.  A block leaves by
+  // counting itself out (a release-add, without waiting for it).  A block that
+  // gave up waits (bounded) until every block of the launch has counted
+  // itself out, and then one such block clears the counters the launch may
+  // have left set.
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1113,19 +1221,28 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   }
   if (warp == 2) tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0) {
-    FSOPS_STAMP(10);
-    __threadfence();
-    const uint32_t old = atom_add_acq_rel_gpu(a.ctl + kCtlDone, 1u);
-    if (old + 1 == static_cast<uint32_t>(G)) {
-      // every block has finished: leave the control words zero for the next launch
-      for (int p = 0; p < a.nphases; ++p)
-        for (int t = 0; t < a.ph[p].T; ++t) a.ph[p].tile_cnt[t] = 0u;
-      if (a.hflags != nullptr)
-        for (int t = 0; t < a.I / 128; ++t) a.hflags[t] = 0u;
-      a.ctl[kCtlXReady] = 0u;
-      __threadfence();
-      a.ctl[kCtlDone] = 0u;
+    unsigned long long* exits = reinterpret_cast<unsigned long long*>(a.ctl + kCtlExits);
+    if (!*abort_flag) {
+      red_add_release_gpu_u64(exits, 1ull);
+    } else {
+      // this launch's blocks bring the count from a multiple of G to the next
+      const unsigned long long before = atom_add_acq_rel_gpu_u64(exits, 1ull);
+      const unsigned long long all = (before / static_cast<unsigned long long>(G) + 1ull) * static_cast<unsigned long long>(G);
+      const uint64_t t0 = globaltimer_ns();
+      bool gone = false;
+      while (!(gone = ld_acquire_gpu_u64(exits) >= all) && globaltimer_ns() - t0 < 200000000ull) __nanosleep(256);
+      if (gone && atomicCAS(a.ctl + kCtlCleanup, 0u, 1u) == 0u) {
+        for (int p = 0; p < a.nphases; ++p)
+          for (int t = 0; t < a.ph[p].T; ++t) a.ph[p].tile_cnt[t] = 0u;
+        for (int c = 0; c < static_cast<int>(G); ++c) {
+          if (a.xready != nullptr) a.xready[c] = 0u;
+          if (a.hflags != nullptr) a.hflags[c] = 0u;
+        }
+        __threadfence();
+        a.ctl[kCtlCleanup] = 0u;
+      }
     }
+    FSOPS_STAMP(78);
   }
 }
 

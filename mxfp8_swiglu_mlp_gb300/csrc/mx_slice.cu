@@ -65,17 +65,12 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
 __device__ __forceinline__ void st_shared_cluster_u16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_shared_cluster() {
   asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 // One 32-element block of bf16 x (row r, k-group j of a 128-wide k-chunk),
 // already in registers, quantised into the stage's activation tile (128-byte

@@ -70,3 +70,12 @@ def assert_repeat_close(a_bits: np.ndarray, b_bits: np.ndarray, max_diff_frac: f
     bad = np.abs(a - b) > np.maximum(step, floor)
     assert not np.any(bad), (np.argwhere(bad)[:5], a[bad][:5], b[bad][:5])
     assert np.mean(a != b) <= max_diff_frac, np.mean(a != b)
+
+
+def control_words_clear(ctl_u8) -> bool:
+    """Whether a workspace's control region (a uint8 device tensor) is back at
+    zero between launches.  Bytes 8-15 are left out: they hold the 64-bit
+    count of grid-wide kernel blocks that have left, over all launches."""
+    c = ctl_u8.clone()
+    c[8:16] = 0
+    return int(c.count_nonzero()) == 0

@@ -6,7 +6,7 @@ import pytest
 import oracle
 from workloads import inputs
 from tests._util import (to_dev_u16, from_dev_bf16, bf16_bits_to_f64, rel_l2, max_abs_norm, per_row_rel_l2,
-                         REL_L2_TOL, MAX_ABS_TOL, PER_ROW_TOL, assert_repeat_close)
+                         REL_L2_TOL, MAX_ABS_TOL, PER_ROW_TOL, assert_repeat_close, control_words_clear)
 
 pytestmark = pytest.mark.gpu
 
@@ -96,15 +96,23 @@ def test_small_shapes_sliced(fs, M, H, I, seed, knob):
     (16, {"PRIME": 3, "MAX_INFLIGHT": 2, "DECODE_PATH": 0}),  # other weight-load depths
     (16, {"COOPERATIVE": 1, "DECODE_PATH": 0}),               # cooperative launch of the grid-wide kernel
     (64, {"COOPERATIVE": 1}),
+    # tile-aligned splits (each block on one tile) and stream-K forced, where
+    # both phases allow either (KS >= blocks per tile)
+    (16, {"H": 2560, "ALIGNED": 1, "PAIRS": 0, "DECODE_PATH": 0}),
+    (16, {"H": 2560, "ALIGNED": 0, "PAIRS": 0, "DECODE_PATH": 0}),
+    (5, {"H": 1280, "I": 4096, "ALIGNED": 1, "DECODE_PATH": 0}),
+    (64, {"H": 2560, "ALIGNED": 1}),
+    (64, {"H": 2560, "ALIGNED": 0}),
 ])
 def test_tile_plans(fs, M, kn, knob):
     """Every tile height / split combination the grid-wide kernel supports,
     forced through the plan knobs, against the oracle."""
     kn = dict(kn)
     I = int(kn.pop("I", 2560))
+    H = int(kn.pop("H", 512))
     for k, v in kn.items():
         knob(k, v)
-    wl = inputs.make_workload_small("s", M, 512, I, 9)
+    wl = inputs.make_workload_small("s", M, H, I, 9)
     L = Layer(fs, wl)
     _assert_parity(L.run(fs, True), L.oracle())
 
@@ -244,13 +252,24 @@ def test_output_guard_band(fs):
     _assert_parity(from_dev_bf16(y), L.oracle())
 
 
-def test_wait_timeout_reports_and_recovers(fs):
+# (M, H, I, knobs): the cluster-sliced kernel; the grid-wide kernel with
+# stream-K gate/up; with 2-block cluster pairs exchanging gate/up halves through
+# distributed shared memory (I / 128 = 40 tiles for 76 pairs); with whole
+# gate/up tiles and per-owner finishing (M = 64); cooperative.
+TIMEOUT_CASES = [(4, 256, 384, {}), (4, 256, 384, {"DECODE_PATH": 0}), (16, 256, 5120, {"DECODE_PATH": 0}),
+                 (64, 256, 1024, {}), (16, 256, 5120, {"DECODE_PATH": 0, "COOPERATIVE": 1})]
+
+
+@pytest.mark.parametrize("M,H,I,knobs", TIMEOUT_CASES)
+def test_wait_timeout_reports_and_recovers(fs, knob, M, H, I, knobs):
     """A wait that can never be satisfied (one arrival more than any block
-    makes) runs out, the kernel reports FSOPS_ERR_TIMEOUT and returns; the
-    next launch is correct."""
+    makes) runs out, the kernel reports FSOPS_ERR_TIMEOUT and returns; every
+    block of a cluster pair leaves together; the next launch is correct."""
     import torch
 
-    wl = inputs.make_workload_small("s", 4, 256, 384, 16)
+    for k, v in knobs.items():
+        knob(k, v)
+    wl = inputs.make_workload_small("s", M, H, I, 16)
     L = Layer(fs, wl)
     y = torch.empty((L.M, L.H), dtype=torch.bfloat16, device="cuda")
     fs.fsops_set_wait_timeout_ns(20_000_000)
@@ -263,5 +282,5 @@ def test_wait_timeout_reports_and_recovers(fs):
         fs.fsops_debug_set_extra_arrivals(0)
         fs.fsops_set_wait_timeout_ns(1_000_000_000)
     assert (word >> 24) == fs.ERR_TIMEOUT, hex(word)
-    assert int(L.ws.buf[(L.ws.ptr - L.ws.buf.data_ptr()):][:8192].count_nonzero()) == 0
+    assert control_words_clear(L.ws.buf[(L.ws.ptr - L.ws.buf.data_ptr()):][:16384])
     _assert_parity(L.run(fs), L.oracle())
