@@ -410,14 +410,15 @@ fsops_status fsops_debug_set_extra_arrivals(uint32_t n);
  *   PRIME             weight loads in flight before the activations exist.
  *   MAX_INFLIGHT      weight loads in flight per block (1..8).
  *   LOCAL_XQ          0: quantise x grid-wide even for M <= 16.
- *   DECODE_PATH       M <= 32: 0 the grid-wide two-phase kernel, 1 the
- *                     cluster-sliced kernel.
+ *   DECODE_PATH       M <= 32: 1 runs the cluster-sliced kernel instead of
+ *                     the grid-wide two-phase kernel (the default).
  *   COOPERATIVE       1: launch the grid-wide kernel cooperatively instead
  *                     of as a plain launch that may start while the previous
  *                     kernel on the stream finishes.
- *   EARLY_W           M > 16: 1 lets the weight producer fill its stages
- *                     before x is available (PRIME loads in flight), 0
- *                     holds it until the block's x loads are issued.
+ *   EARLY_W           M > 16: 1 (the default) lets the weight producer
+ *                     fill its stages before x is available (PRIME loads in
+ *                     flight), 0 holds it until the block's x loads are
+ *                     issued.
  *   ALIGNED           split phases: 1 gives each block K stages of one tile
  *                     only, 0 the even split over all tiles' stages. */
 typedef enum {

@@ -240,10 +240,13 @@ MlpPlan plan_mlp(int M, int H, int I, int grid) {
                knob_or(FSOPS_KNOB_PAIRS, 1, 0, 1))
                   ? 1
                   : 0;
-  // down projection: with M > 64, 128-row tiles halve the split-K sums the
-  // blocks add up in L2 (each tile is split over half as many blocks), which
-  // outweighs their halved loads per stage
-  pl.TR1 = tile_rows_knob(FSOPS_KNOB_TR1, npad > 64 ? 128 : 256);
+  // down projection: 256-row tiles.  128-row tiles would halve the split-K
+  // sums the blocks add up in L2, but need twice the MMAs for the same
+  // weights, and an MMA costs its issuing thread the same whatever its N:
+  // with the tile-aligned split 256 rows measured faster at every M (M = 128,
+  // H = 5120, I = 17408: 62.2 against 66.7 us; H = 4096, I = 12288: 45.2
+  // against 45.7)
+  pl.TR1 = tile_rows_knob(FSOPS_KNOB_TR1, 256);
   pl.T1 = (H + pl.TR1 - 1) / pl.TR1;
   return pl;
 }
@@ -281,7 +284,7 @@ void init_common(KernelArgs& a, int M, uint32_t* ctl) {
   const int inflight = knob_or(FSOPS_KNOB_MAX_INFLIGHT, kDefaultMaxInflight, 1, kMaxStages);
   a.max_inflight = inflight < a.nstages ? inflight : a.nstages;
   a.prime_inflight = knob_or(FSOPS_KNOB_PRIME, kPrimeInflight, 1, kMaxStages);
-  a.early_w = knob_or(FSOPS_KNOB_EARLY_W, 0, 0, 1);
+  a.early_w = knob_or(FSOPS_KNOB_EARLY_W, 1, 0, 1);
   a.stage_bytes = stage_bytes_for(a.npad);
   a.timeout_ns = g_timeout_ns.load();
   a.extra_xready = g_extra.load();
@@ -452,18 +455,15 @@ bool slice_plan(int M, int H, int I, int sms, SlicePlan* sp) {
 }
 // fp32 [M, H] partial sums of the sliced kernel.
 size_t slice_accum_bytes(int M, int H) { return round_up(static_cast<size_t>(M) * H * 4, 1024); }
-// Whether the fused MLP call runs the sliced kernel.  By default only where
-// it was measured faster than the grid-wide kernel: up to 16 tokens with
-// fewer 128-feature chunks than 2-block clusters (a small I, as at M = 1,
-// H = 1024, I = 2816: 14.6 against 16.6 us per call).  With more chunks the
-// grid-wide kernel wins (M = 16, H = 2560, I = 9728: 29.7 against 33.7 us):
-// every cluster adds a full [M, H] fp32 partial of y into L2, 12.5 MB of L2
-// reductions there.  FSOPS_KNOB_DECODE_PATH = 1 / 0 forces either.
+// Whether the fused MLP call runs the sliced kernel: only when forced
+// (FSOPS_KNOB_DECODE_PATH = 1).  The grid-wide kernel measured faster at
+// every decode shape, including the small-I one the sliced kernel was built
+// for (M = 1, H = 1024, I = 2816: 14.0 against 14.6 us per call; M = 16,
+// H = 2560, I = 9728: 23.6 against 33.9 us), where every cluster adds a full
+// [M, H] fp32 partial of y into L2 (12.5 MB of L2 reductions at M = 16).
 bool use_slice(int M, int H, int I, const DeviceInfo* di, SlicePlan* sp) {
-  const int k = knob(FSOPS_KNOB_DECODE_PATH);
-  if (k == 0) return false;
-  if (!slice_plan(M, H, I, di->sms, sp)) return false;
-  return k == 1 || (M <= 16 && sp->NC < di->sms / kSliceCluster);
+  if (knob(FSOPS_KNOB_DECODE_PATH) != 1) return false;
+  return slice_plan(M, H, I, di->sms, sp);
 }
 // One launch of the sliced kernel.  ctl: the control words (status word,
 // then RT tile counters), accum: fp32 [M, H], both zero between launches.  gamma != null: x is normalised (RMSNorm with eps) before its

@@ -181,6 +181,21 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 // The 128 epilogue threads (warps 4-7) of a block.
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Warp pair q (warps 4 + 2q, 5 + 2q) of the epilogue warps (barriers 2 and 3).
+__device__ __forceinline__ void pair_bar(uint32_t q) { asm volatile("bar.sync %0, 64;" ::"r"(2u + q) : "memory"); }
+// AND of `v` over warp pair q (a barrier among its 64 threads).
+__device__ __forceinline__ bool pair_and(uint32_t q, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %2, 0;\n\t"
+      "bar.red.and.pred q, %1, 64, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(2u + q), "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
 // AND of `v` over the 128 epilogue threads (a barrier among them): every
 // epilogue thread takes the same branch after a wait, so none of them is left
 // alone at a later barrier when another gave up.

@@ -129,6 +129,10 @@ __host__ __device__ inline uint32_t stg_bytes_for(int npad) {
 // activation producer warp fills by TMA and quantises into the stages.
 constexpr int kMaxXSlots = 4;
 __host__ __device__ inline uint32_t xring_bytes_for(int npad) { return kMaxXSlots * 256u * npad; }
+// Cluster pairs at npad = 16: once the x stages are filled, the x ring's first
+// half holds this block's sums of the partner's half of the columns (16 rows
+// x 128 fp32) and its second half receives the partner's.
+constexpr uint32_t kPairRecvOff = 8192;
 // TMEM columns: accumulator [0, 256), then per pipeline stage 12 scale columns
 // (activation tile: 4, weight tiles: 8).
 constexpr uint32_t kAccCols = 256;

@@ -463,7 +463,7 @@ __device__ __forceinline__ void finish_staged(const KernelArgs& a, const PhaseAr
   }
 }
 
-// Local activation tiles (M <= 32): block b of a stage is the 32-element block
+// Local activation tiles (M <= 16): block b of a stage is the 32-element block
 // (row b / 4, block b % 4) of a 128-wide k-chunk of x.  Quantise it into the
 // stage's activation tile (128-byte swizzled rows, as the TMA would have
 // written them) and its scale tile; rows >= M get zeros.
@@ -543,13 +543,19 @@ __device__ __noinline__ bool finish_slice(const KernelArgs& a, const PhaseArgs& 
   return true;
 }
 
+// STAGED: the instance for M <= 32 (accumulators staged through shared
+// memory, local x quantisation possible); the other serves M > 32.  Each
+// instance holds only its own epilogue paths, which keeps the run-once
+// epilogue code of a call compact for the instruction caches.
+template <bool STAGED>
 __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid_constant__ KernelArgs a) {
+  const bool local_xq = STAGED && a.local_xq != 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.nstages;
   float* stg = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * a.stage_bytes);
-  uint8_t* xring = reinterpret_cast<uint8_t*>(stg) + (a.stage_tmem ? stg_bytes_for(a.npad) : 0u);
-  uint8_t* ctl_smem = xring + (a.local_xq ? xring_bytes_for(a.npad) : 0u);
+  uint8_t* xring = reinterpret_cast<uint8_t*>(stg) + (STAGED ? stg_bytes_for(a.npad) : 0u);
+  uint8_t* ctl_smem = xring + (local_xq ? xring_bytes_for(a.npad) : 0u);
   uint64_t* full_w = reinterpret_cast<uint64_t*>(ctl_smem);
   uint64_t* full_a = full_w + kMaxStages;
   uint64_t* empty = full_a + kMaxStages;
@@ -559,7 +565,9 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   uint64_t* x_issued = drain + 1;
   uint64_t* x_full = x_issued + 1;          // [kMaxXSlots] bf16 x tile landed (local_xq)
   uint64_t* peer_ready = x_full + kMaxXSlots;  // the other block of the pair has pushed its sums of this block's half
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(peer_ready + 1);
+  uint64_t* peer_free = peer_ready + 1;          // ... may push them (the receiving buffer is free)
+  uint64_t* peer_done = peer_free + 1;           // ... has received this block's push
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(peer_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
   // 0 until this block's activations are available (x quantised grid-wide,
@@ -584,8 +592,10 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     mbar_init(x_issued, 128);
     for (int i = 0; i < kMaxXSlots; ++i) mbar_init(&x_full[i], 1);
     mbar_init(peer_ready, 1);
+    mbar_init(peer_free, 1);
+    mbar_init(peer_done, 1);
     *abort_flag = 0;
-    *flowing = (a.x != nullptr && !a.local_xq) ? 0 : 1;
+    *flowing = (a.x != nullptr && !local_xq) ? 0 : 1;
     mbar_fence_init();
   }
   if (warp == 2) {
@@ -597,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       tma_prefetch_desc(&a.tm_w[p]);
       tma_prefetch_desc(&a.tm_act[p]);
     }
-    if (a.local_xq) tma_prefetch_desc(&a.tm_x);
+    if (local_xq) tma_prefetch_desc(&a.tm_x);
   }
   tc_fence_before();
   __syncthreads();
@@ -627,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     uint32_t lag_round = 0, n_issued = 0, n_landed = 0;
     bool ok = true;
     // let the epilogue warps' loads of x enter the memory system first
-    if (a.x != nullptr && !a.local_xq && !a.early_w) ok = wait_mbar(cx, x_issued, 0, kSiteEmpty);
+    if (a.x != nullptr && !local_xq && !a.early_w) ok = wait_mbar(cx, x_issued, 0, kSiteEmpty);
     for (int p = 0; p < a.nphases && ok; ++p) {
       const PhaseArgs& ph = a.ph[p];
       SegIter it(ph, static_cast<uint32_t>(G));
@@ -684,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       SegIter it(ph, static_cast<uint32_t>(G));
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
-        if (p == 0 && a.local_xq) {
+        if (p == 0 && local_xq) {
           for (int ks = ks0; ks < ks1; ++ks)
             if (++stage == S) { stage = 0; ++round; }
           continue;
@@ -797,11 +807,14 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     const int et = threadIdx.x - 128;  // token row of the accumulator (TMEM lane)
     const int ew = et >> 5;
     const uint32_t pair_h = blockIdx.x & 1u, pair_peer = pair_h ^ 1u;  // cluster pairs: rank, partner
+    // bulk pair exchange (thread et == 0): this block's x ring armed to
+    // receive, the partner's sums received, this block's sums sent
+    bool pair_armed = false, pair_received = false, pair_sent = false;
     griddep_wait();  // x, the workspace and y may be in use by the previous kernel until here
     if (et == 0) FSOPS_STAMP(65);
     // (1) grid-wide: quantise this block's slice of x, the 32-blocks [b0, b1)
     // of the row-major [npad, H/32] block grid (rows >= M only get a zero scale)
-    if (a.x != nullptr && !a.local_xq) {
+    if (a.x != nullptr && !local_xq) {
       const int nbk = a.H / 32;
       const long long NB = static_cast<long long>(npad) * nbk;
       const long long b0 = range_begin(blockIdx.x, NB, G), b1 = range_begin(blockIdx.x + 1, NB, G);
@@ -866,72 +879,64 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     int4 pend[kMaxPend];  // split tiles to finish at the end of the phase: (t, arrival, owners, ncols)
     int npend = 0;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(ew * 32) << 16);
-    // With local_xq the epilogue warps fill phase 0's activation stages.  The
-    // block's phase-0 stages are its consecutive units u0, u0 + 1, ... (stage
-    // c: ring position c % S, k-stage (u0 + c) % KS).  Stage c belongs to warp
-    // c % 4, which streams the stage's bf16 x tile into its own slot of the x
-    // ring one tile ahead and quantises it straight into the stage: four
-    // stages are in work at once.  Before the accumulator of a segment ending
-    // at stage e is awaited, every stage below e + S is filled: those need no
-    // MMA of a later segment (whose accumulator is not yet free) to release
-    // their ring position, and the next segment's first stages are ready
-    // while this one's epilogue runs.
+    // With local_xq the epilogue warps fill phase 0's activation stages: two
+    // stages at a time, stage c by warp pair c % 2 (warps 4 + 2 (c % 2) and
+    // the next; thread pt of the pair quantises 32-element block pt), so a
+    // stage reaches the tensor core soon after its x tile lands and the pairs
+    // together keep ahead of the MMAs.  The block's phase-0 stages are its
+    // consecutive units u0, u0 + 1, ... (stage c: ring position c % S,
+    // k-stage (u0 + c) % KS); their bf16 x tiles stream through a four-slot
+    // ring (tile c in slot c % 4: the pair's two slots), issued by the pair's
+    // first thread two tiles ahead.  Before the accumulator of a segment
+    // ending at stage e is awaited, every stage below e + S is filled: those
+    // need no MMA of a later segment (whose accumulator is not yet free) to
+    // release their ring position, and the next segment's first stages are
+    // ready while this one's epilogue runs.
     uint32_t xu0 = 0, xn0 = 0, xks = 1;
-    if (a.local_xq) {
+    if (local_xq) {
       SegIter it0(a.ph[0], static_cast<uint32_t>(G));
       xu0 = it0.u;
       xn0 = it0.ue - it0.u;
       xks = it0.KS;
     }
-    uint32_t xc = static_cast<uint32_t>(ew);  // next stage of this warp
-    uint32_t x_pend = 0xFFFFFFFFu;            // stage whose tile is in flight into this warp's slot
+    const uint32_t xq = static_cast<uint32_t>(ew >> 1);  // this warp's pair
+    const int pt = et & 63;                              // thread of the pair
+    uint32_t xc = xq;                                    // next stage of the pair
+    uint32_t xi = xq;                                    // next tile the pair issues
     const uint64_t x_pol = l2_policy_evict_last();
-    uint8_t* xslot = xring + ew * 256 * npad;
-    auto issue_x = [&](uint32_t c) {
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&x_full[ew], 256u * npad);
-        tma_load_2d(xslot, &a.tm_x, &x_full[ew], static_cast<int>((xu0 + c) % xks) * kTileK, 0, x_pol);
-      }
-      x_pend = c;
+    auto issue_x = [&]() {  // the pair's first thread: tile xi into slot xi % 4
+      const uint32_t slot = xi & 3u;
+      mbar_arrive_expect_tx(&x_full[slot], 256u * npad);
+      tma_load_2d(xring + slot * 256 * npad, &a.tm_x, &x_full[slot], static_cast<int>((xu0 + xi) % xks) * kTileK, 0,
+                  x_pol);
+      xi += 2;
     };
-    if (a.local_xq && xc < xn0) issue_x(xc);
+    if (pt == 0)
+      while (xi < xn0 && xi < xq + 4) issue_x();
     auto quantize_upto = [&](uint32_t L) -> bool {
-      for (; xc < L; xc += 4) {
-        const uint32_t c = xc;
-        if (!__all_sync(0xFFFFFFFFu, wait_mbar(cx, &x_full[ew], (c >> 2) & 1u, kSiteFullA))) return false;
-        x_pend = 0xFFFFFFFFu;
-        if (lane == 0) FSOPS_STAMP_IF(c < 6, 66 + c);
-        // each lane: blocks b = lane, lane + 32 of the npad x 4 block grid
-        uint4 raw[2][4];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int b = lane + 32 * q;
-          if (b < 4 * npad) {
-            const uint4* src = reinterpret_cast<const uint4*>(xslot + (b >> 2) * 256 + (b & 3) * 64);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) raw[q][k] = src[k];
-          }
-        }
-        // the slot may be refilled once every lane has read it
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (c + 4 < xn0) issue_x(c + 4);
-        if (lane == 0) FSOPS_STAMP_IF(c == 2, 80);
+      for (; xc < L; xc += 2) {
+        const uint32_t c = xc, slot = c & 3u;
         const int stage = static_cast<int>(c % static_cast<uint32_t>(S));
         const uint32_t round = c / static_cast<uint32_t>(S);
-        if (!__all_sync(0xFFFFFFFFu, wait_mbar(cx, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty))) return false;
-        if (lane == 0) FSOPS_STAMP_IF(c == 2, 81);
+        if (!pair_and(xq, wait_mbar(cx, &x_full[slot], (c >> 2) & 1u, kSiteFullA) &&
+                              wait_mbar(cx, &empty[stage], (round & 1u) ^ 1u, kSiteEmpty)))
+          return false;
+        if (pt == 0) FSOPS_STAMP_IF(c < 6, 66 + c);
         uint8_t* st = smem + static_cast<size_t>(stage) * a.stage_bytes;
+        if (pt < 4 * npad) {
+          const uint4* src = reinterpret_cast<const uint4*>(xring + slot * 256 * npad + (pt >> 2) * 256 + (pt & 3) * 64);
+          uint4 raw[4];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int b = lane + 32 * q;
-          if (b < 4 * npad) store_x_block(a, st, b, raw[q]);
+          for (int k = 0; k < 4; ++k) raw[k] = src[k];
+          store_x_block(a, st, pt, raw);
         }
-        if (lane == 0) FSOPS_STAMP_IF(c == 2, 82);
         fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full_a[stage]);
-        if (lane == 0) FSOPS_STAMP_IF(c < 6, 72 + c);
+        pair_bar(xq);  // the stage is filled and the slot read by both warps
+        if (pt == 0) {
+          mbar_arrive(&full_a[stage]);
+          if (xi < xn0) issue_x();
+          FSOPS_STAMP_IF(c < 6, 72 + c);
+        }
       }
       return true;
     };
@@ -941,9 +946,15 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       SegIter it(ph, static_cast<uint32_t>(G));
       int t, ks0, ks1;
       while (ok && it.next(t, ks0, ks1)) {
-        if (p == 0 && a.local_xq) {
+        if (p == 0 && local_xq) {
           xseg_end += static_cast<uint32_t>(ks1 - ks0);
           if (!epi_and(quantize_upto(min(xn0, xseg_end + static_cast<uint32_t>(S))))) { ok = false; break; }
+          if (ph.pairs && et == 0) {
+            // every x tile is consumed: the x ring receives the partner's sums
+            mbar_arrive_expect_tx(peer_ready, 512u * a.M);
+            mbar_arrive_remote(mapa_shared(peer_free, pair_peer));
+            pair_armed = true;
+          }
         }
         if (!epi_and(wait_mbar(cx, acc_full, acc_round & 1u, kSiteAccFull))) { ok = false; break; }
         ++acc_round;
@@ -952,7 +963,8 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
         const bool whole = (ks0 == 0 && ks1 == ph.KS);
         const int ncols = (ph.tile_rows == 256 && t * 256 + 128 < ph.rows) ? 256 : 128;
         float* accg = ph.accum + static_cast<long long>(t) * a.M * kTileRows;  // M * 256 floats
-        if (a.stage_tmem) {
+        bool send_ok = true;  // the bulk pair exchange could send (thread et == 0)
+        if (STAGED) {
           // M <= 32: warp 4 copies TMEM lanes 0..31 to shared memory (four
           // loads in flight per wait) and the accumulator is released at once;
           // all four warps share the rest.  Split tiles add their rows into a
@@ -962,16 +974,29 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           // and pushes the other half into the partner's stg, at the columns of
           // its own half there (which the partner does not use), then arrives
           // on the partner's peer_ready.
+          // With local_xq (M <= 16) the push is one bulk copy instead: warp 4
+          // writes the partner's half as contiguous 512-byte rows into the
+          // first half of this block's x ring, and one thread copies them into
+          // the second half of the partner's (both rings are free once their
+          // block's x stages are all filled).
+          const bool push_st = ph.pairs && !local_xq, push_bulk = ph.pairs && local_xq;
           if (ew == 0) {
-            const uint32_t pstg = ph.pairs ? mapa_shared(stg, pair_peer) : 0u;
+            const uint32_t pstg = push_st ? mapa_shared(stg, pair_peer) : 0u;
 #pragma unroll 1
             for (int c0 = 0; c0 < ncols; c0 += 64) {
               uint32_t v[4][16];
 #pragma unroll
               for (int q = 0; q < 4; ++q) tmem_ld16(tlane + c0 + 16 * q, v[q]);
               tmem_ld_wait();
+              if (lane == 0 && p == 0) FSOPS_STAMP_IF(c0 < 256, 83 + (c0 >> 6));
               if (lane < a.M) {
-                if (ph.pairs && static_cast<uint32_t>(c0 >> 7) != pair_h) {
+                if (push_bulk && static_cast<uint32_t>(c0 >> 7) != pair_h) {
+                  float4* d = reinterpret_cast<float4*>(xring + lane * 512 + (c0 & 127) * 4);
+#pragma unroll
+                  for (int q = 0; q < 16; ++q)
+                    d[q] = make_float4(__uint_as_float(v[q >> 2][4 * (q & 3)]), __uint_as_float(v[q >> 2][4 * (q & 3) + 1]),
+                                       __uint_as_float(v[q >> 2][4 * (q & 3) + 2]), __uint_as_float(v[q >> 2][4 * (q & 3) + 3]));
+                } else if (push_st && static_cast<uint32_t>(c0 >> 7) != pair_h) {
                   const uint32_t dst = pstg + static_cast<uint32_t>(lane * kStageLd + (c0 ^ 128)) * 4u;
 #pragma unroll
                   for (int q = 0; q < 16; ++q)
@@ -986,15 +1011,26 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
                 }
               }
             }
-            if (ph.pairs) {
+            if (push_st) {
               fence_acq_rel_cluster();
               __syncwarp();
               if (lane == 0) mbar_arrive_remote(mapa_shared(peer_ready, pair_peer));
             }
+            if (push_bulk) fence_proxy_async_shared();  // the copy engine reads those rows
+            if (lane == 0 && p == 0) FSOPS_STAMP(87);
           }
+          if (et == 32 && p == 0) FSOPS_STAMP(88);
           tc_fence_before();
           epi_bar();
           mbar_arrive(acc_empty);
+          if (push_bulk && et == 0) {
+            send_ok = wait_mbar_cluster(cx, peer_free, 0, kSitePeer);
+            if (send_ok) {
+              bulk_copy_to_cluster(mapa_shared(xring + kPairRecvOff, pair_peer), xring, 512u * a.M,
+                                   mapa_shared(peer_ready, pair_peer));
+              pair_sent = true;
+            }
+          }
           if (et == 0) FSOPS_STAMP(p == 0 ? 12 : 60);
           if (!whole && !ph.pairs) {
             const int lg = ncols == 256 ? 6 : 5;  // log2(float4 per row)
@@ -1053,7 +1089,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           mbar_arrive(acc_empty);
         }
         if (whole) {
-          if (a.stage_tmem) finish_staged(a, ph, t, ncols, stg, et, 0, ncols >> 6);
+          if (STAGED) finish_staged(a, ph, t, ncols, stg, et, 0, ncols >> 6);
           if (et == 0) FSOPS_STAMP_IF(p == 0, 13);
         } else if (ph.pairs) {
           // The two blocks of this cluster hold the two K halves of tile t
@@ -1063,17 +1099,25 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           // partner's half's columns), they are added and those features
           // finished.  The partner writes nothing here after that arrival.
           const int h = static_cast<int>(pair_h);
-          if (!epi_and(wait_mbar_cluster(cx, peer_ready, 0, kSitePeer))) { ok = false; break; }
+          if (!epi_and(send_ok && wait_mbar_cluster(cx, peer_ready, 0, kSitePeer))) { ok = false; break; }
           if (et == 0) FSOPS_STAMP(58);
+          // the partner's sums: pushed by stores into this stg at the other
+          // half's columns, or copied into the x ring (row r at 512 r bytes)
+          const float* recv = local_xq ? reinterpret_cast<const float*>(xring + kPairRecvOff) : stg;
+          const int rld = local_xq ? 128 : kStageLd;
 #pragma unroll 1
           for (int i = et; i < (a.M << 5); i += 128) {
             const int r = i >> 5, c = 128 * h + (i & 31) * 4;
-            const float4 pv = *reinterpret_cast<const float4*>(stg + r * kStageLd + (c ^ 128));
+            const float4 pv = *reinterpret_cast<const float4*>(recv + r * rld + (local_xq ? (i & 31) * 4 : (c ^ 128)));
             float4* mine = reinterpret_cast<float4*>(stg + r * kStageLd + c);
             const float4 mv = *mine;
             *mine = make_float4(mv.x + pv.x, mv.y + pv.y, mv.z + pv.z, mv.w + pv.w);
           }
           epi_bar();
+          if (et == 0 && local_xq) {
+            pair_received = true;
+            mbar_arrive_remote(mapa_shared(peer_done, pair_peer));
+          }
           if (et == 0) FSOPS_STAMP(59);
           finish_staged(a, ph, t, 256, stg, et, 2 * h, 2);
           if (et == 0) FSOPS_STAMP_IF(p == 0, 13);
@@ -1099,13 +1143,13 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
             // the last arrival finishes the tile (except plain output at
             // M > 32, where every owner finishes rows and finish_slice clears
             // the counter): nothing reads the counter again this launch
-            if (old + 1 == expected && (a.stage_tmem || ph.epi == kEpiSwiGLU)) ph.tile_cnt[t] = 0u;
+            if (old + 1 == expected && (STAGED || ph.epi == kEpiSwiGLU)) ph.tile_cnt[t] = 0u;
           }
           epi_bar();
           const uint32_t arrival = static_cast<uint32_t>(*bcast);
           const bool last = arrival + 1 == expected;
           epi_bar();
-          if (!a.stage_tmem && ph.epi != kEpiSwiGLU) {
+          if (!STAGED && ph.epi != kEpiSwiGLU) {
             // M > 32, plain output: every owner finishes the token rows its
             // arrival order names, once all owners have added their sums.  The
             // waits come after the block's last segment, so that no owner
@@ -1122,7 +1166,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           }
           if (et == 0) FSOPS_STAMP_IF(p == 1, 61);
           if (last) {
-            if (a.stage_tmem) {
+            if (STAGED) {
               // every load is issued before the first store: one L2 round trip
               // (M * ncols / 512 <= 16 float4 per thread)
               const int lg = ncols == 256 ? 6 : 5;
@@ -1177,7 +1221,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           }
           if (!last) {
             if (et == 0) FSOPS_STAMP(p == 0 ? 4 : 9);
-            if (a.stage_tmem) epi_bar();  // stg is reused by the next accumulator
+            if (STAGED) epi_bar();  // stg is reused by the next accumulator
             continue;
           }
         }
@@ -1188,7 +1232,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           if (et == 0) FSOPS_STAMP(14);
           epi_bar();
           publish_h(a, t, et, static_cast<uint32_t>(G));
-        } else if (a.stage_tmem) {
+        } else if (STAGED) {
           epi_bar();  // stg is reused by the next accumulator
         }
         if (et == 0) FSOPS_STAMP(p == 0 ? 4 : 9);
@@ -1198,8 +1242,19 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       if (et == 0) FSOPS_STAMP_IF(p == 1, 62);
     }
     if (!ok) *abort_flag = 1;
-    // a tile still in flight into this warp's x slot lands before the block leaves
-    if (x_pend != 0xFFFFFFFFu && lane == 0) drain_mbar(&x_full[ew], (x_pend >> 2) & 1u, 200000000ull);
+    // tiles still in flight into the x ring land before the block leaves
+    if (pt == 0)
+      for (uint32_t c = xc; c < xi; c += 2) drain_mbar(&x_full[c & 3u], (c >> 2) & 1u, 200000000ull);
+    // a copy into this block's x ring has landed, and the partner has
+    // received this block's copy, before either block leaves (already so
+    // unless the launch gave up)
+    if (et == 0) {
+      if (pair_armed && !pair_received) {
+        drain_mbar(peer_ready, 0, 200000000ull);
+        mbar_arrive_remote(mapa_shared(peer_done, pair_peer));
+      }
+      if (pair_sent) drain_mbar(peer_done, 0, 200000000ull);
+    }
     if (et == 0) FSOPS_STAMP(79);
   }
 
@@ -1214,7 +1269,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // neither block of a pair leaves while the other may still read its shared memory
+  // neither block of a pair leaves while the other may still touch its shared memory
   if (a.cluster_pairs) {
     __syncwarp();
     cluster_sync_all();
@@ -1260,7 +1315,9 @@ cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStr
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxAttrDevices) return cudaErrorInvalidDevice;
   if (!g_smem_attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(mx_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    e = cudaFuncSetAttribute(mx_persistent_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mx_persistent_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e != cudaSuccess) return e;
     g_smem_attr_set[dev].store(true, std::memory_order_release);
   }
@@ -1286,17 +1343,18 @@ cudaError_t launch_mx_kernel(const KernelArgs& a, int grid, size_t smem, cudaStr
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, mx_persistent_kernel, a);
+  return a.stage_tmem ? cudaLaunchKernelEx(&cfg, mx_persistent_kernel<true>, a)
+                      : cudaLaunchKernelEx(&cfg, mx_persistent_kernel<false>, a);
 }
 
 bool grid_fits(int grid, size_t smem) {
-  if (cudaFuncSetAttribute(mx_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
+  if (cudaFuncSetAttribute(mx_persistent_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
       cudaSuccess) {
     cudaGetLastError();
     return false;
   }
   int per_sm = 0, dev = 0, sms = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_persistent_kernel, kThreads, smem) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_persistent_kernel<true>, kThreads, smem) != cudaSuccess ||
       cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();
@@ -1307,7 +1365,7 @@ bool grid_fits(int grid, size_t smem) {
 
 bool cluster_pairs_fit(int grid, size_t smem) {
   if (grid % 2 != 0) return false;
-  if (cudaFuncSetAttribute(mx_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
+  if (cudaFuncSetAttribute(mx_persistent_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
       cudaSuccess) {
     cudaGetLastError();
     return false;
@@ -1324,7 +1382,7 @@ bool cluster_pairs_fit(int grid, size_t smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, mx_persistent_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, mx_persistent_kernel<true>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }

@@ -88,7 +88,8 @@ def test_small_shapes_sliced(fs, M, H, I, seed, knob):
     (16, {"TR0": 128, "WHOLE_TILES": 0, "DECODE_PATH": 0}),   # 128-row gate/up tiles, split-K
     (16, {"TR0": 256, "WHOLE_TILES": 1, "DECODE_PATH": 0}),   # 256-row whole tiles, staged epilogue
     (16, {"TR1": 128, "DECODE_PATH": 0}),                     # 128-row down tiles, staged epilogue
-    (64, {"TR1": 256, "WHOLE_TILES": 0}),                     # 256-row down tiles, split gate/up from TMEM
+    (64, {"TR1": 128, "WHOLE_TILES": 0}),                     # 128-row down tiles, split gate/up from TMEM
+    (100, {"TR1": 128}),                                      # 128-row down tiles, per-owner finishing
     (64, {"TR0": 128}),                                       # 128-row whole gate/up tiles from TMEM
     (16, {"I": 5120, "DECODE_PATH": 0}),                      # gate/up tiles split by 2-block clusters
     (16, {"I": 5120, "PAIRS": 0, "DECODE_PATH": 0}),          # the same shape split over all blocks
@@ -256,7 +257,7 @@ def test_output_guard_band(fs):
 # stream-K gate/up; with 2-block cluster pairs exchanging gate/up halves through
 # distributed shared memory (I / 128 = 40 tiles for 76 pairs); with whole
 # gate/up tiles and per-owner finishing (M = 64); cooperative.
-TIMEOUT_CASES = [(4, 256, 384, {}), (4, 256, 384, {"DECODE_PATH": 0}), (16, 256, 5120, {"DECODE_PATH": 0}),
+TIMEOUT_CASES = [(4, 256, 384, {"DECODE_PATH": 1}), (4, 256, 384, {"DECODE_PATH": 0}), (16, 256, 5120, {"DECODE_PATH": 0}),
                  (64, 256, 1024, {}), (16, 256, 5120, {"DECODE_PATH": 0, "COOPERATIVE": 1})]
 
 
