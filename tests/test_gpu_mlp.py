@@ -194,9 +194,9 @@ def test_repeat_calls_agree(fs, M, path, knob):
 
 
 def test_repeat_calls_full_size(fs):
-    """The m16 and m128 layers, four calls each: every element within one
-    bf16 step of the first call's."""
-    for name in ("m16", "m128"):
+    """The m1, m16, m64 and m128 layers, four calls each: every element within
+    one bf16 step of the first call's."""
+    for name in ("m1", "m16", "m64", "m128"):
         wl = inputs.WORKLOADS[name]
         L = Layer(fs, wl, layer=wl.layers - 1)
         runs = [L.run(fs) for _ in range(4)]
