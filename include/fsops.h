@@ -226,9 +226,10 @@ fsops_status fsops_rmsnorm_quantize_mxfp8(const void* x_bf16, const void* gamma_
  * tiled MLP).  Arguments, limits and workspace as fsops_mxfp8_swiglu_mlp,
  * plus gamma_bf16 [H] (16-byte aligned) and eps.
  * y_bf16 may equal x_bf16 (in place): every read of x for the norm and the
- * quantisation happens before any block writes y (the MLP's phases wait for
- * the whole grid's quantisation), and the residual is read only by the thread
- * that then writes the same element of y.
+ * quantisation happens before any block writes y (each block reads x before
+ * its gate/up products, and every tile of y needs every gate/up tile), and
+ * the residual is read only by the thread that then writes the same element
+ * of y.
  * Graph-capture safe, so a chain of layers (y of one block is x of the next)
  * can be captured once and replayed. */
 fsops_status fsops_mxfp8_swiglu_mlp_block(const void* x_bf16, const void* gamma_bf16, float eps, int residual,

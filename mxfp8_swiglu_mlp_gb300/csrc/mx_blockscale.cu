@@ -42,6 +42,11 @@ constexpr uint32_t kBsWBytes = 128u * 128u;
 
 template <int NPAD>
 struct BsCfg {
+  // epilogue warps: two per TMEM lane quarter from 64 tokens on, each with
+  // half of the token columns (128 running sums per thread would spill)
+  static constexpr int EW = NPAD >= 64 ? 8 : 4;
+  static constexpr int THREADS = 128 + 32 * EW;
+  static constexpr int COLS = NPAD / (EW / 4);  // token columns per epilogue thread
   static constexpr uint32_t SB = 128u * NPAD + kBsWBytes;  // stage: A tile (NPAD x 128) | W tile (128 x 128)
   static constexpr uint32_t FIXED = 512u + 1024u + 1024u;  // unit scale tile, control words (+ 512 B of token scales), alignment
   static constexpr int STAGES = (kMaxSmem - FIXED) / SB < kBsMaxStages ? (kMaxSmem - FIXED) / SB : kBsMaxStages;
@@ -126,9 +131,29 @@ __global__ void __launch_bounds__(256) bs_quantize_blocks_kernel(const uint16_t*
 
 }  // namespace
 
+// Barrier 1 among the EW epilogue warps, and the AND of a wait's outcome over them.
+template <int EW>
+__device__ __forceinline__ void bs_epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");
+}
+template <int EW>
+__device__ __forceinline__ bool bs_epi_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "n"(32 * EW)
+      : "memory");
+  return r != 0;
+}
+
 template <int NPAD>
-__global__ void __launch_bounds__(kThreads, 1) bs_gemm_kernel(const __grid_constant__ BsArgs a) {
+__global__ void __launch_bounds__(BsCfg<NPAD>::THREADS, 1) bs_gemm_kernel(const __grid_constant__ BsArgs a) {
   using Cfg = BsCfg<NPAD>;
+  constexpr int EW = Cfg::EW, COLS = Cfg::COLS;
   constexpr int S = Cfg::STAGES;
   constexpr uint32_t SB = Cfg::SB;
   constexpr int NB = kBsAccBufs;
@@ -158,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) bs_gemm_kernel(const __grid_const
     }
     for (int b = 0; b < NB; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[b], EW);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -238,34 +263,36 @@ __global__ void __launch_bounds__(kThreads, 1) bs_gemm_kernel(const __grid_const
     tc_commit(drain);
     drain_mbar(drain, 0, 200000000ull);
   } else if (warp >= 4) {
-    // ------------------------------------------------ epilogue: thread et holds row n of the tile
-    const int et = threadIdx.x - 128, q4 = warp & 3;
+    // ------------------------------------------------ epilogue: thread et holds row n = et % 128 of
+    // the tile for token columns [r0, r0 + COLS)
+    const int et = threadIdx.x - 128, q4 = warp & 3, row = et & 127, r0 = (et >> 7) * COLS;
     griddep_wait();  // C, the accumulator and the counters may be in use by the previous kernel
     const int M = a.M, KB = a.KB;
-    float run[NPAD];
+    float run[COLS];
 #pragma unroll
-    for (int r = 0; r < NPAD; ++r) run[r] = 0.f;
+    for (int r = 0; r < COLS; ++r) run[r] = 0.f;
     bool ok = true;
     int split_t[2], nsplit = 0;  // tiles this block shares with another (at most its first and last)
     // this block's sums of tile t (row n = 128 t + et), over all of K (whole) or a part of it
     auto flush = [&](int t, bool whole) {
-      const size_t n = static_cast<size_t>(t) * 128 + et;
+      const size_t n = static_cast<size_t>(t) * 128 + row;
       if (whole) {
 #pragma unroll
-        for (int r = 0; r < NPAD; ++r) {
+        for (int i = 0; i < COLS; ++i) {
+          const int r = r0 + i;
           if (r < M) {
-            if (a.c_f32) static_cast<float*>(a.c)[r * static_cast<size_t>(a.N) + n] = run[r];
-            else static_cast<__nv_bfloat16*>(a.c)[r * static_cast<size_t>(a.N) + n] = __float2bfloat16_rn(run[r]);
+            if (a.c_f32) static_cast<float*>(a.c)[r * static_cast<size_t>(a.N) + n] = run[i];
+            else static_cast<__nv_bfloat16*>(a.c)[r * static_cast<size_t>(a.N) + n] = __float2bfloat16_rn(run[i]);
           }
         }
       } else {
 #pragma unroll
-        for (int r = 0; r < NPAD; ++r)
-          if (r < M) red_add_f32(a.accum + r * static_cast<size_t>(a.N) + n, run[r]);
+        for (int i = 0; i < COLS; ++i)
+          if (r0 + i < M) red_add_f32(a.accum + (r0 + i) * static_cast<size_t>(a.N) + n, run[i]);
         if (nsplit < 2) split_t[nsplit++] = t;
       }
 #pragma unroll
-      for (int r = 0; r < NPAD; ++r) run[r] = 0.f;
+      for (int i = 0; i < COLS; ++i) run[i] = 0.f;
     };
     int cur_t = -1, first_kb = 0, last_kb = 0;
     uint32_t seq = 0;
@@ -279,22 +306,23 @@ __global__ void __launch_bounds__(kThreads, 1) bs_gemm_kernel(const __grid_const
       last_kb = kb;
       const uint32_t b = seq % NB;
       // the K-block's token scales, one per thread, through shared memory
-      epi_bar();  // the previous unit's reads of sa_s are done
+      bs_epi_bar<EW>();  // the previous unit's reads of sa_s are done
       if (et < NPAD) sa_s[et] = et < M ? __ldg(a.a_scales + static_cast<size_t>(et) * KB + kb) : 0.f;
-      if (!epi_and(wait_mbar(cx, &acc_full[b], (seq / NB) & 1u, kSiteAccFull))) { ok = false; break; }
+      if (!bs_epi_and<EW>(wait_mbar(cx, &acc_full[b], (seq / NB) & 1u, kSiteAccFull))) { ok = false; break; }
       tc_fence_after();
       const float sw = __ldg(a.w_scales + static_cast<size_t>(t) * KB + kb);
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + b * NPAD;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + b * NPAD + r0;
+      // up to 32 columns of loads in flight per wait
+      constexpr int kBatch = COLS < 32 ? COLS : 32;
 #pragma unroll
-      for (int j = 0; j < NPAD / 16; ++j) {
-        uint32_t v[16];
-        tmem_ld16(taddr + 16 * j, v);
+      for (int c = 0; c < COLS; c += kBatch) {
+        uint32_t v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch / 16; ++j)
+          tmem_ld16(taddr + c + 16 * j, *reinterpret_cast<uint32_t(*)[16]>(&v[16 * j]));
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int r = 16 * j + i;
-          run[r] = fmaf(__uint_as_float(v[i]), sw * sa_s[r], run[r]);
-        }
+        for (int i = 0; i < kBatch; ++i) run[c + i] = fmaf(__uint_as_float(v[i]), sw * sa_s[r0 + c + i], run[c + i]);
       }
       tc_fence_before();
       __syncwarp();
@@ -305,28 +333,28 @@ __global__ void __launch_bounds__(kThreads, 1) bs_gemm_kernel(const __grid_const
     // accumulator and the counter zero
     if (ok && nsplit > 0) {
       fence_acq_rel_gpu();  // this thread's adds are performed before any ticket
-      epi_bar();
+      bs_epi_bar<EW>();
       if (et < nsplit) {
         const int t = split_t[et];
         const uint32_t ub = static_cast<uint32_t>(t) * KB, ue = ub + KB - 1;
         const uint32_t owners = ((ue + 1) * G + U - 1) / U - ((ub + 1) * G + U - 1) / U + 1;
         bcast[et] = atom_add_acq_rel_gpu(a.tile_cnt + t, 1u) + 1 == owners ? 1 : 0;
       }
-      epi_bar();
+      bs_epi_bar<EW>();
       for (int i = 0; i < nsplit; ++i) {
         if (!bcast[i]) continue;
         const int t = split_t[i];
-        const size_t n = static_cast<size_t>(t) * 128 + et;
+        const size_t n = static_cast<size_t>(t) * 128 + row;
         // every load is issued before the first store: one L2 round trip
 #pragma unroll
-        for (int r = 0; r < NPAD; ++r)
-          if (r < M) run[r] = __ldcg(a.accum + r * static_cast<size_t>(a.N) + n);
+        for (int j = 0; j < COLS; ++j)
+          if (r0 + j < M) run[j] = __ldcg(a.accum + (r0 + j) * static_cast<size_t>(a.N) + n);
 #pragma unroll
-        for (int r = 0; r < NPAD; ++r) {
-          if (r < M) {
-            const size_t o = r * static_cast<size_t>(a.N) + n;
-            if (a.c_f32) static_cast<float*>(a.c)[o] = run[r];
-            else static_cast<__nv_bfloat16*>(a.c)[o] = __float2bfloat16_rn(run[r]);
+        for (int j = 0; j < COLS; ++j) {
+          if (r0 + j < M) {
+            const size_t o = (r0 + j) * static_cast<size_t>(a.N) + n;
+            if (a.c_f32) static_cast<float*>(a.c)[o] = run[j];
+            else static_cast<__nv_bfloat16*>(a.c)[o] = __float2bfloat16_rn(run[j]);
             __stcg(a.accum + o, 0.f);
           }
         }
@@ -350,7 +378,7 @@ template <int NPAD>
 cudaError_t launch_npad(const BsArgs& a, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(BsCfg<NPAD>::THREADS);
   cfg.dynamicSmemBytes = BsCfg<NPAD>::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -467,13 +467,16 @@ __device__ __forceinline__ void finish_staged(const KernelArgs& a, const PhaseAr
 // (row b / 4, block b % 4) of a 128-wide k-chunk of x.  Quantise it into the
 // stage's activation tile (128-byte swizzled rows, as the TMA would have
 // written them) and its scale tile; rows >= M get zeros.
-__device__ __forceinline__ void store_x_block(const KernelArgs& a, uint8_t* st, int b, const uint4 (&raw)[4]) {
+// gam != null: the block is of RMSNorm(x) * gamma (x * rn * gamma, gam the
+// block's 32 gains, rn the row's 1 / rms).
+__device__ __forceinline__ void store_x_block(const KernelArgs& a, uint8_t* st, int b, const uint4 (&raw)[4],
+                                              const uint16_t* gam = nullptr, float rn = 1.0f) {
   const int r = b >> 2, j = b & 3;
   uint32_t s = 0;
   uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
   if (r < a.M) {
     uint32_t pk[8];
-    s = quantize_block_pack(raw, pk);
+    s = gam != nullptr ? quantize_block_pack_norm(raw, gam, rn, pk) : quantize_block_pack(raw, pk);
     c0 = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     c1 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
   }
@@ -913,6 +916,43 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
     };
     if (pt == 0)
       while (xi < xn0 && xi < xq + 4) issue_x();
+    if (local_xq && a.gamma != nullptr) {
+      // RMSNorm: 1 / rms of every row (M <= 16), each over all of H, before
+      // any stage is quantised.  Warp ew takes rows ew, ew + 4, ew + 8 and
+      // ew + 12 together (the loads of all four in flight); each row's sum
+      // runs in the order of row_rnorm, so every path gets the same norms.
+      // (five of each row's 16-byte loads in flight per lane: 20 in all)
+      float ss[4] = {0.f, 0.f, 0.f, 0.f};
+      const int n8 = a.H / 8;
+      for (int i0 = lane; i0 < n8; i0 += 5 * 32) {
+        uint4 v[5][4];
+#pragma unroll
+        for (int u = 0; u < 5; ++u)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (ew + 4 * k < a.M && i0 + 32 * u < n8)
+              v[u][k] = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<long long>(ew + 4 * k) * a.H) + i0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 5; ++u)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (ew + 4 * k >= a.M || i0 + 32 * u >= n8) continue;
+            const uint32_t w[4] = {v[u][k].x, v[u][k].y, v[u][k].z, v[u][k].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float lo = bf16_lo(w[q]), hi = bf16_hi(w[q]);
+              ss[k] = fmaf(lo, lo, fmaf(hi, hi, ss[k]));
+            }
+          }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss[k] += __shfl_xor_sync(0xFFFFFFFFu, ss[k], o);
+        if (lane == 0 && ew + 4 * k < a.M) rnorm[ew + 4 * k] = rsqrtf(ss[k] / static_cast<float>(a.H) + a.eps);
+      }
+      epi_bar();  // every row's norm is in rnorm before any stage is quantised
+    }
     auto quantize_upto = [&](uint32_t L) -> bool {
       for (; xc < L; xc += 2) {
         const uint32_t c = xc, slot = c & 3u;
@@ -928,7 +968,13 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           uint4 raw[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) raw[k] = src[k];
-          store_x_block(a, st, pt, raw);
+          if (a.gamma != nullptr) {
+            const int ksx = static_cast<int>((xu0 + c) % xks);
+            store_x_block(a, st, pt, raw, a.gamma + ksx * kTileK + (pt & 3) * 32,
+                          (pt >> 2) < a.M ? rnorm[pt >> 2] : 1.0f);
+          } else {
+            store_x_block(a, st, pt, raw);
+          }
         }
         fence_proxy_async_shared();
         pair_bar(xq);  // the stage is filled and the slot read by both warps
@@ -983,29 +1029,31 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           if (ew == 0) {
             const uint32_t pstg = push_st ? mapa_shared(stg, pair_peer) : 0u;
 #pragma unroll 1
-            for (int c0 = 0; c0 < ncols; c0 += 64) {
-              uint32_t v[4][16];
+            for (int c0 = 0; c0 < ncols; c0 += 128) {
+              // 128 columns per wait (eight loads in flight)
+              uint32_t v[8][16];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) tmem_ld16(tlane + c0 + 16 * q, v[q]);
+              for (int q = 0; q < 8; ++q) tmem_ld16(tlane + c0 + 16 * q, v[q]);
               tmem_ld_wait();
               if (lane == 0 && p == 0) FSOPS_STAMP_IF(c0 < 256, 83 + (c0 >> 6));
               if (lane < a.M) {
-                if (push_bulk && static_cast<uint32_t>(c0 >> 7) != pair_h) {
-                  float4* d = reinterpret_cast<float4*>(xring + lane * 512 + (c0 & 127) * 4);
+                const bool other = ph.pairs && static_cast<uint32_t>(c0 >> 7) != pair_h;
+                if (push_bulk && other) {
+                  float4* d = reinterpret_cast<float4*>(xring + lane * 512);
 #pragma unroll
-                  for (int q = 0; q < 16; ++q)
+                  for (int q = 0; q < 32; ++q)
                     d[q] = make_float4(__uint_as_float(v[q >> 2][4 * (q & 3)]), __uint_as_float(v[q >> 2][4 * (q & 3) + 1]),
                                        __uint_as_float(v[q >> 2][4 * (q & 3) + 2]), __uint_as_float(v[q >> 2][4 * (q & 3) + 3]));
-                } else if (push_st && static_cast<uint32_t>(c0 >> 7) != pair_h) {
+                } else if (push_st && other) {
                   const uint32_t dst = pstg + static_cast<uint32_t>(lane * kStageLd + (c0 ^ 128)) * 4u;
 #pragma unroll
-                  for (int q = 0; q < 16; ++q)
+                  for (int q = 0; q < 32; ++q)
                     st_shared_cluster_v4(dst + 16u * q, make_uint4(v[q >> 2][4 * (q & 3)], v[q >> 2][4 * (q & 3) + 1],
                                                                    v[q >> 2][4 * (q & 3) + 2], v[q >> 2][4 * (q & 3) + 3]));
                 } else {
                   float4* d = reinterpret_cast<float4*>(stg + lane * kStageLd + c0);
 #pragma unroll
-                  for (int q = 0; q < 16; ++q)
+                  for (int q = 0; q < 32; ++q)
                     d[q] = make_float4(__uint_as_float(v[q >> 2][4 * (q & 3)]), __uint_as_float(v[q >> 2][4 * (q & 3) + 1]),
                                        __uint_as_float(v[q >> 2][4 * (q & 3) + 2]), __uint_as_float(v[q >> 2][4 * (q & 3) + 3]));
                 }
@@ -1114,10 +1162,6 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
             *mine = make_float4(mv.x + pv.x, mv.y + pv.y, mv.z + pv.z, mv.w + pv.w);
           }
           epi_bar();
-          if (et == 0 && local_xq) {
-            pair_received = true;
-            mbar_arrive_remote(mapa_shared(peer_done, pair_peer));
-          }
           if (et == 0) FSOPS_STAMP(59);
           finish_staged(a, ph, t, 256, stg, et, 2 * h, 2);
           if (et == 0) FSOPS_STAMP_IF(p == 0, 13);
@@ -1125,6 +1169,12 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           epi_bar();
           publish_h(a, t, et, static_cast<uint32_t>(G));
           if (et == 0) FSOPS_STAMP(14);
+          // the partner's copy into the x ring is consumed (told after the
+          // publication, off the path to the down projection)
+          if (et == 0 && local_xq) {
+            pair_received = true;
+            mbar_arrive_remote(mapa_shared(peer_done, pair_peer));
+          }
           if (et == 0) FSOPS_STAMP(p == 0 ? 4 : 9);
           continue;
         } else {
