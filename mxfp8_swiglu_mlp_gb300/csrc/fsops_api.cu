@@ -909,6 +909,10 @@ fsops_status fsops_mxfp8_paged_decode_attention(const void* q_bf16, const uint8_
   aa.max_pages = max_pages;
   aa.sm_scale = sm_scale;
   aa.timeout_ns = g_timeout_ns.load();
+  aa.trace = nullptr;
+#ifdef FSOPS_TRACE
+  aa.trace = g_trace;
+#endif
   const cudaError_t e = launch_paged_decode(aa, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "paged_decode_kernel launch");
 }

@@ -32,7 +32,8 @@ using namespace dev;
 
 namespace {
 
-constexpr int kAThreads = 128;
+constexpr int kAThreads = 256;  // two threads per token of a chunk
+constexpr int kAWarps = kAThreads / 32;
 constexpr int kD = kAttnHeadDim;
 constexpr int kC = kAttnChunk;
 constexpr uint32_t kCodeBytes = kC * kD;      // 16 KB of K (or V) codes per chunk
@@ -62,8 +63,21 @@ __device__ __forceinline__ void attn_error(const AttnArgs& a, uint32_t code, uin
   atomicCAS(a.status, 0u, (code << 24) | ((site & 0xFFu) << 16) | (blockIdx.z & 0xFFFFu));
 }
 
+// Timeline stamps for profiling builds (compiled with -DFSOPS_TRACE).
+#ifdef FSOPS_TRACE
+#define ATTN_STAMP(idx)                                                                                   \
+  do {                                                                                                    \
+    if (a.trace != nullptr)                                                                               \
+      a.trace[((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * 64 + (idx)] = globaltimer_ns(); \
+  } while (0)
+#else
+#define ATTN_STAMP(idx) \
+  do {                  \
+  } while (0)
+#endif
+
 template <int G>
-__global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(kAThreads, 3) paged_decode_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   AttnStage* stg = reinterpret_cast<AttnStage*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   // q of the group's heads, each 16-element piece padded to 20 floats: the
@@ -71,7 +85,7 @@ __global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_co
   // 80-byte strides put them on distinct banks
   __shared__ __align__(16) float qs[G * 8 * kQPiece];
   __shared__ __align__(16) float ps[G * kC];      // probabilities of the chunk
-  __shared__ float red_max[4 * G], red_sum[4 * G];
+  __shared__ float red_max[kAWarps * G], red_sum[kAWarps * G];
   __shared__ __align__(8) uint64_t bar[2];
   __shared__ int chunk_ok[2];
 
@@ -93,35 +107,40 @@ __global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_co
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
     mbar_fence_init();
+    ATTN_STAMP(0);
   }
   __syncthreads();
 
-  // Thread 0: the bulk copies of chunk c into stage s (pages past the
-  // sequence's last one are not loaded; their tokens are masked).  A page id
-  // outside [0, num_pages) is reported and its page skipped.
+  // Warp 0: the bulk copies of chunk c into stage s, lane i those of the
+  // chunk's page i, all in flight together (pages past the sequence's last
+  // one are not loaded; their tokens are masked).  A page id outside
+  // [0, num_pages) is reported and its page skipped.
   auto issue = [&](int c, int s) {
     const int p0 = c * pages_per_chunk;
     const int np = min(pages_per_chunk, npages - p0);
-    uint32_t bytes = 0;
-    int ok = 1;
-    for (int i = 0; i < np; ++i) {
-      const int pid = a.block_table[static_cast<size_t>(b) * a.max_pages + p0 + i];
-      if (pid < 0 || pid >= a.num_pages) ok = 0;
-      else bytes += 2u * (a.P * kD + a.P * (kD / 32));
+    int pid = -1;
+    bool mine = lane < np, good = true;
+    if (mine) {
+      pid = a.block_table[static_cast<size_t>(b) * a.max_pages + p0 + lane];
+      good = pid >= 0 && pid < a.num_pages;
     }
-    if (!ok) attn_error(a, 1u, 2u);
-    chunk_ok[s] = ok;
+    const bool ok = __all_sync(0xFFFFFFFFu, good);
+    const uint32_t npg = __popc(__ballot_sync(0xFFFFFFFFu, mine && good));
+    if (lane == 0) {
+      if (!ok) attn_error(a, 1u, 2u);
+      chunk_ok[s] = ok ? 1 : 0;
+    }
     fence_proxy_async_shared();  // the stage's earlier generic reads come before the copies' writes
-    mbar_arrive_expect_tx(&bar[s], bytes);
-    for (int i = 0; i < np; ++i) {
-      const int pid = a.block_table[static_cast<size_t>(b) * a.max_pages + p0 + i];
-      if (pid < 0 || pid >= a.num_pages) continue;
+    if (lane == 0) mbar_arrive_expect_tx(&bar[s], npg * 2u * (a.P * kD + a.P * (kD / 32)));
+    __syncwarp();
+    if (mine && good) {
       const size_t row = (static_cast<size_t>(pid) * a.Hkv + hk) * a.P;  // first token row of the page-head block
       const uint32_t cb = static_cast<uint32_t>(a.P) * kD, sb = static_cast<uint32_t>(a.P) * (kD / 32);
-      bulk_load(stg[s].k + i * cb, a.k_codes + row * kD, cb, &bar[s], l2_policy_evict_first());
-      bulk_load(stg[s].v + i * cb, a.v_codes + row * kD, cb, &bar[s], l2_policy_evict_first());
-      bulk_load(stg[s].ks + i * sb, a.k_scales + row * (kD / 32), sb, &bar[s], l2_policy_evict_first());
-      bulk_load(stg[s].vs + i * sb, a.v_scales + row * (kD / 32), sb, &bar[s], l2_policy_evict_first());
+      const uint64_t pol = l2_policy_evict_first();
+      bulk_load(stg[s].k + lane * cb, a.k_codes + row * kD, cb, &bar[s], pol);
+      bulk_load(stg[s].v + lane * cb, a.v_codes + row * kD, cb, &bar[s], pol);
+      bulk_load(stg[s].ks + lane * sb, a.k_scales + row * (kD / 32), sb, &bar[s], pol);
+      bulk_load(stg[s].vs + lane * sb, a.v_scales + row * (kD / 32), sb, &bar[s], pol);
     }
   };
 
@@ -135,10 +154,10 @@ __global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_co
   }
   bool ok = true;
   int stalled = -1;  // the chunk whose copies did not land in time
-  if (t == 0 && c0 < c1) issue(c0, 0);
+  if (warp == 0 && c0 < c1) issue(c0, 0);
   for (int c = c0; c < c1 && ok; ++c) {
     const int s = (c - c0) & 1;
-    if (t == 0 && c + 1 < c1) issue(c + 1, s ^ 1);
+    if (warp == 0 && c + 1 < c1) issue(c + 1, s ^ 1);
     stalled = c;
     // bounded wait for the chunk's copies
     {
@@ -154,18 +173,22 @@ __global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_co
     }
     if (!__syncthreads_and(ok)) break;
     const bool chunk_valid = chunk_ok[s] != 0;
+    if (t == 0 && c - c0 < 12) ATTN_STAMP(4 + 4 * (c - c0));
 
-    // ---- scores: thread t scores token c * 128 + t for the G heads
-    const int tok = c * kC + t;
+    // ---- scores: threads 2 j and 2 j + 1 score token c * 128 + j for the G
+    // heads, over dimensions [0, 64) and [64, 128), and add their halves
+    const int tt0 = t >> 1, half = t & 1;
+    const int tok = c * kC + tt0;
     float sc[G];
-    if (tok < n && chunk_valid) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) sc[g] = 0.f;
-      const uint8_t* krow = stg[s].k + t * kD;
-      const uint32_t kscales = *reinterpret_cast<const uint32_t*>(stg[s].ks + t * (kD / 32));
+    for (int g = 0; g < G; ++g) sc[g] = 0.f;
+    if (tok < n && chunk_valid) {
+      const uint8_t* krow = stg[s].k + tt0 * kD;
+      const uint32_t kscales = *reinterpret_cast<const uint32_t*>(stg[s].ks + tt0 * (kD / 32));
 #pragma unroll 2
-      for (int i = 0; i < 8; ++i) {
-        const int cc = (i + t) & 7;  // 16-code piece, rotated per thread against bank conflicts
+      for (int i = 0; i < 4; ++i) {
+        // 16-code piece of this half, rotated per token against bank conflicts
+        const int cc = 4 * half + ((i + tt0) & 3);
         const uint4 kv = *reinterpret_cast<const uint4*>(krow + 16 * cc);
         const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
         float kf[16];
@@ -193,14 +216,15 @@ __global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_co
           sc[g] = fmaf(scale, dot, sc[g]);
         }
       }
+    }
 #pragma unroll
-      for (int g = 0; g < G; ++g) sc[g] *= a.sm_scale;
-    } else {
-#pragma unroll
-      for (int g = 0; g < G; ++g) sc[g] = -INFINITY;
+    for (int g = 0; g < G; ++g) {
+      sc[g] += __shfl_xor_sync(0xFFFFFFFFu, sc[g], 1);
+      sc[g] = (tok < n && chunk_valid) ? sc[g] * a.sm_scale : -INFINITY;
     }
 
     // ---- online softmax over the chunk
+    if (t == 0 && c - c0 < 12) ATTN_STAMP(5 + 4 * (c - c0));
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       float m = sc[g];
@@ -211,30 +235,36 @@ __global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_co
     float alpha[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const float cm = fmaxf(fmaxf(red_max[g], red_max[G + g]), fmaxf(red_max[2 * G + g], red_max[3 * G + g]));
+      float cm = red_max[g];
+#pragma unroll
+      for (int w = 1; w < kAWarps; ++w) cm = fmaxf(cm, red_max[w * G + g]);
       const float mn = fmaxf(m_run[g], cm);
       // a chunk with no valid token (a bad page) leaves mn = -inf: nothing to add
       const float p = (sc[g] == -INFINITY || mn == -INFINITY) ? 0.f : expf(sc[g] - mn);
       alpha[g] = (m_run[g] == -INFINITY || mn == -INFINITY) ? (mn == -INFINITY ? 1.f : 0.f) : expf(m_run[g] - mn);
       m_run[g] = mn;
-      ps[g * kC + t] = p;
-      float sum = p;
+      if (half == 0) ps[g * kC + tt0] = p;
+      float sum = half == 0 ? p : 0.f;  // each token once
       for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
       if (lane == 0) red_sum[warp * G + g] = sum;
     }
     __syncthreads();
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      l_run[g] = l_run[g] * alpha[g] + (red_sum[g] + red_sum[G + g] + red_sum[2 * G + g] + red_sum[3 * G + g]);
+      float tot = red_sum[g];
+#pragma unroll
+      for (int w = 1; w < kAWarps; ++w) tot += red_sum[w * G + g];
+      l_run[g] = l_run[g] * alpha[g] + tot;
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[g][e] *= alpha[g];
     }
 
     // ---- p . v: thread (warp, lane) owns dimensions 4 lane .. 4 lane + 3 and
-    // the chunk's tokens warp, warp + 4, ...
+    // the chunk's tokens warp, warp + kAWarps, ...
+    if (t == 0 && c - c0 < 12) ATTN_STAMP(6 + 4 * (c - c0));
     const int tmax = min(kC, n - c * kC);
     if (chunk_valid) {
-      for (int tt = warp; tt < tmax; tt += 4) {
+      for (int tt = warp; tt < tmax; tt += kAWarps) {
         const uint32_t v4 = *reinterpret_cast<const uint32_t*>(stg[s].v + tt * kD + 4 * lane);
         const float vscale = ue8m0_value(stg[s].vs[tt * (kD / 32) + (lane >> 3)]);
         const float2 lo = e4m3x2_to_float2(v4), hi = e4m3x2_to_float2(v4 >> 16);
@@ -248,6 +278,7 @@ __global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_co
       }
     }
     __syncthreads();  // the stage and ps are rewritten next
+    if (t == 0 && c - c0 < 12) ATTN_STAMP(7 + 4 * (c - c0));
     stalled = -1;
   }
   if (stalled >= 0) {
@@ -263,8 +294,12 @@ __global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_co
     __syncthreads();
   }
 
-  // ---- the four warps' partial outputs are summed; one record per head
-  float* wsum = reinterpret_cast<float*>(stg);  // reuse the ring: [4][G][D]
+  if (t == 0) {
+    ATTN_STAMP(1);
+    if (a.trace != nullptr) a.trace[((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * 64 + 2] = c1 - c0;
+  }
+  // ---- the warps' partial outputs are summed; one record per head
+  float* wsum = reinterpret_cast<float*>(stg);  // reuse the ring: [kAWarps][G][D]
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -272,7 +307,9 @@ __global__ void __launch_bounds__(kAThreads) paged_decode_kernel(const __grid_co
   __syncthreads();
   for (int i = t; i < G * kD; i += kAThreads) {
     const int g = i / kD, d = i % kD;
-    const float o = wsum[g * kD + d] + wsum[(G + g) * kD + d] + wsum[(2 * G + g) * kD + d] + wsum[(3 * G + g) * kD + d];
+    float o = wsum[g * kD + d];
+#pragma unroll
+    for (int w = 1; w < kAWarps; ++w) o += wsum[(w * G + g) * kD + d];
     float* rec = a.part + ((static_cast<size_t>(b) * a.Hq + hk * G + g) * a.nsplit + split) * (2 + kD);
     rec[2 + d] = o;
     if (d == 0) {

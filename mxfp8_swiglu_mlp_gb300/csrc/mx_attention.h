@@ -24,6 +24,7 @@ struct AttnArgs {
   int B, Hq, Hkv, P, num_pages, max_pages, nsplit;
   float sm_scale;
   uint64_t timeout_ns;
+  unsigned long long* trace;  // [blocks][64] %globaltimer stamps, builds with FSOPS_TRACE only
 };
 
 // Splits of each sequence's chunks (one block each) for B sequences, Hkv KV
