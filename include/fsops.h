@@ -421,7 +421,10 @@ fsops_status fsops_debug_set_extra_arrivals(uint32_t n);
  *                     flight), 0 holds it until the block's x loads are
  *                     issued.
  *   ALIGNED           split phases: 1 gives each block K stages of one tile
- *                     only, 0 the even split over all tiles' stages. */
+ *                     only, 0 the even split over all tiles' stages.
+ *   ATTN_CHUNKS       paged decode attention: 128-token chunks per block
+ *                     (the workspace size depends on it: query it again
+ *                     after a change). */
 typedef enum {
   FSOPS_KNOB_TR0 = 0,
   FSOPS_KNOB_TR1 = 1,
@@ -435,7 +438,8 @@ typedef enum {
   FSOPS_KNOB_COOPERATIVE = 9,
   FSOPS_KNOB_EARLY_W = 10,
   FSOPS_KNOB_ALIGNED = 11,
-  FSOPS_KNOB_COUNT = 12
+  FSOPS_KNOB_ATTN_CHUNKS = 12,
+  FSOPS_KNOB_COUNT = 13
 } fsops_knob;
 
 /* Set knob `knob` (an fsops_knob) to `value` (negative = back to the

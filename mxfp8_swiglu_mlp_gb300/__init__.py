@@ -38,7 +38,7 @@ SCALES_ROWMAJOR, SCALES_TCGEN05 = 0, 1
 # fsops_knob values (include/fsops.h)
 KNOBS = {"TR0": 0, "TR1": 1, "WHOLE_TILES": 2, "PAIRS": 3, "GEMM_FORM": 4, "PRIME": 5, "MAX_INFLIGHT": 6,
          "LOCAL_XQ": 7, "DECODE_PATH": 8, "COOPERATIVE": 9,
-         "EARLY_W": 10, "ALIGNED": 11}
+         "EARLY_W": 10, "ALIGNED": 11, "ATTN_CHUNKS": 12}
 DTYPE_BF16, DTYPE_F32, DTYPE_MXFP8 = 0, 1, 2
 
 if not os.path.exists(_build.LIB):

@@ -461,6 +461,10 @@ bool slice_plan(int M, int H, int I, int sms, SlicePlan* sp) {
 }
 // fp32 [M, H] partial sums of the sliced kernel.
 size_t slice_accum_bytes(int M, int H) { return round_up(static_cast<size_t>(M) * H * 4, 1024); }
+// 128-token chunks per paged-attention block (knob ATTN_CHUNKS, else the
+// library's choice).
+int attn_chunks_per_block() { return knob_or(FSOPS_KNOB_ATTN_CHUNKS, kAttnChunksPerBlock, 1, 64); }
+
 // Whether the fused MLP call runs the sliced kernel: only when forced
 // (FSOPS_KNOB_DECODE_PATH = 1).  The grid-wide kernel measured faster at
 // every decode shape, including the small-I one the sliced kernel was built
@@ -864,7 +868,7 @@ size_t fsops_paged_attention_workspace_bytes(int B, int Hq, int Hkv, int D, int 
   int dev;
   const DeviceInfo* di;
   if (current_device(&dev, &di) != FSOPS_OK) return 0;
-  const int ns = attn_splits(B, Hkv, max_pages, page_size, di->sms);
+  const int ns = attn_splits(B, Hkv, max_pages, page_size, di->sms, attn_chunks_per_block());
   return kAttnStatusBytes + round_up(attn_part_floats(B, Hq, ns) * sizeof(float), 256);
 }
 
@@ -889,7 +893,7 @@ fsops_status fsops_mxfp8_paged_decode_attention(const void* q_bf16, const uint8_
   if (st != FSOPS_OK) return st;
   AttnArgs aa;
   std::memset(&aa, 0, sizeof(aa));
-  aa.nsplit = attn_splits(B, Hkv, max_pages, page_size, di->sms);
+  aa.nsplit = attn_splits(B, Hkv, max_pages, page_size, di->sms, attn_chunks_per_block());
   if (ws_bytes < kAttnStatusBytes + attn_part_floats(B, Hq, aa.nsplit) * sizeof(float)) return FSOPS_ERR_INVALID_ARG;
   aa.q = static_cast<const uint16_t*>(q_bf16);
   aa.k_codes = k_codes;

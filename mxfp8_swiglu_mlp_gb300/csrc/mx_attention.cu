@@ -84,7 +84,8 @@ __global__ void __launch_bounds__(kAThreads, 3) paged_decode_kernel(const __grid
   // threads of a quarter warp read eight different pieces at once, and
   // 80-byte strides put them on distinct banks
   __shared__ __align__(16) float qs[G * 8 * kQPiece];
-  __shared__ __align__(16) float ps[G * kC];      // probabilities of the chunk
+  // probabilities of each warp's 16 tokens of the chunk: [warp][G][16]
+  __shared__ __align__(16) float ps[kAWarps * G * 16];
   __shared__ float red_max[kAWarps * G], red_sum[kAWarps * G];
   __shared__ __align__(8) uint64_t bar[2];
   __shared__ int chunk_ok[2];
@@ -96,8 +97,9 @@ __global__ void __launch_bounds__(kAThreads, 3) paged_decode_kernel(const __grid
   if (!len_ok && t == 0 && split == 0 && hk == 0) attn_error(a, 1u, 1u);  // FSOPS_ERR_INVALID_ARG
   const int n = len_ok ? len : 0;
   const int nchunks = (n + kC - 1) / kC;
-  const int per = (nchunks + a.nsplit - 1) / a.nsplit;
-  const int c0 = split * per, c1 = min(nchunks, c0 + per);
+  // every split the same number of chunks of the longest sequence's
+  const int per = (a.max_pages * a.P + kC * a.nsplit - 1) / (kC * a.nsplit);
+  const int c0 = min(nchunks, split * per), c1 = min(nchunks, c0 + per);
   const int npages = (n + a.P - 1) / a.P;
   const int pages_per_chunk = kC / a.P;
 
@@ -144,6 +146,11 @@ __global__ void __launch_bounds__(kAThreads, 3) paged_decode_kernel(const __grid
     }
   };
 
+  // Warp w owns tokens w, w + 8, ..., w + 120 of every chunk: it scores them
+  // (lanes 2k and 2k + 1 token w + 8k, half of the dimensions each), keeps
+  // its own online softmax over them, and adds their p . v into its lanes'
+  // four output dimensions.  The warps' states are merged once at the end,
+  // so a chunk needs no block barrier besides the one on its copies.
   float m_run[G], l_run[G], acc[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -153,11 +160,13 @@ __global__ void __launch_bounds__(kAThreads, 3) paged_decode_kernel(const __grid
     for (int e = 0; e < 4; ++e) acc[g][e] = 0.f;
   }
   bool ok = true;
+  int issued = c0;   // chunks whose copies were issued
   int stalled = -1;  // the chunk whose copies did not land in time
   if (warp == 0 && c0 < c1) issue(c0, 0);
+  issued = c0 < c1 ? c0 + 1 : c0;
+  float* pw = ps + warp * G * 16;
   for (int c = c0; c < c1 && ok; ++c) {
     const int s = (c - c0) & 1;
-    if (warp == 0 && c + 1 < c1) issue(c + 1, s ^ 1);
     stalled = c;
     // bounded wait for the chunk's copies
     {
@@ -171,13 +180,17 @@ __global__ void __launch_bounds__(kAThreads, 3) paged_decode_kernel(const __grid
         }
       }
     }
+    // every warp is past the previous chunk: its stage may be refilled
     if (!__syncthreads_and(ok)) break;
+    if (warp == 0 && c + 1 < c1) issue(c + 1, s ^ 1);
+    issued = c + 1 < c1 ? c + 2 : issued;
     const bool chunk_valid = chunk_ok[s] != 0;
     if (t == 0 && c - c0 < 12) ATTN_STAMP(4 + 4 * (c - c0));
 
-    // ---- scores: threads 2 j and 2 j + 1 score token c * 128 + j for the G
-    // heads, over dimensions [0, 64) and [64, 128), and add their halves
-    const int tt0 = t >> 1, half = t & 1;
+    // ---- scores: lanes 2k and 2k + 1 score token w + 8k of the chunk for
+    // the G heads over dimensions [0, 64) and [64, 128), and add their halves
+    const int kk = lane >> 1, half = lane & 1;
+    const int tt0 = warp + 8 * kk;
     const int tok = c * kC + tt0;
     float sc[G];
 #pragma unroll
@@ -188,7 +201,7 @@ __global__ void __launch_bounds__(kAThreads, 3) paged_decode_kernel(const __grid
 #pragma unroll 2
       for (int i = 0; i < 4; ++i) {
         // 16-code piece of this half, rotated per token against bank conflicts
-        const int cc = 4 * half + ((i + tt0) & 3);
+        const int cc = 4 * half + ((i + kk) & 3);
         const uint4 kv = *reinterpret_cast<const uint4*>(krow + 16 * cc);
         const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
         float kf[16];
@@ -222,99 +235,106 @@ __global__ void __launch_bounds__(kAThreads, 3) paged_decode_kernel(const __grid
       sc[g] += __shfl_xor_sync(0xFFFFFFFFu, sc[g], 1);
       sc[g] = (tok < n && chunk_valid) ? sc[g] * a.sm_scale : -INFINITY;
     }
-
-    // ---- online softmax over the chunk
     if (t == 0 && c - c0 < 12) ATTN_STAMP(5 + 4 * (c - c0));
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float m = sc[g];
-      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-      if (lane == 0) red_max[warp * G + g] = m;
-    }
-    __syncthreads();
-    float alpha[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float cm = red_max[g];
-#pragma unroll
-      for (int w = 1; w < kAWarps; ++w) cm = fmaxf(cm, red_max[w * G + g]);
-      const float mn = fmaxf(m_run[g], cm);
-      // a chunk with no valid token (a bad page) leaves mn = -inf: nothing to add
-      const float p = (sc[g] == -INFINITY || mn == -INFINITY) ? 0.f : expf(sc[g] - mn);
-      alpha[g] = (m_run[g] == -INFINITY || mn == -INFINITY) ? (mn == -INFINITY ? 1.f : 0.f) : expf(m_run[g] - mn);
-      m_run[g] = mn;
-      if (half == 0) ps[g * kC + tt0] = p;
-      float sum = half == 0 ? p : 0.f;  // each token once
-      for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-      if (lane == 0) red_sum[warp * G + g] = sum;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float tot = red_sum[g];
-#pragma unroll
-      for (int w = 1; w < kAWarps; ++w) tot += red_sum[w * G + g];
-      l_run[g] = l_run[g] * alpha[g] + tot;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[g][e] *= alpha[g];
-    }
 
-    // ---- p . v: thread (warp, lane) owns dimensions 4 lane .. 4 lane + 3 and
-    // the chunk's tokens warp, warp + kAWarps, ...
+    // ---- the warp's online softmax over its 16 tokens
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float cm = sc[g];
+#pragma unroll
+      for (int o = 16; o >= 2; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, o));
+      const float mn = fmaxf(m_run[g], cm);
+      // no valid token yet (a bad page, or the tokens past the sequence):
+      // mn = -inf and nothing is added
+      const float p = (sc[g] == -INFINITY || mn == -INFINITY) ? 0.f : expf(sc[g] - mn);
+      const float alpha = (m_run[g] == -INFINITY || mn == -INFINITY) ? (mn == -INFINITY ? 1.f : 0.f)
+                                                                      : expf(m_run[g] - mn);
+      m_run[g] = mn;
+      if (half == 0) pw[g * 16 + kk] = p;
+      float sum = half == 0 ? p : 0.f;  // each token once
+#pragma unroll
+      for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+      l_run[g] = l_run[g] * alpha + sum;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[g][e] *= alpha;
+    }
+    __syncwarp();  // pw is written before the lanes read it
     if (t == 0 && c - c0 < 12) ATTN_STAMP(6 + 4 * (c - c0));
+
+    // ---- p . v: lane l owns dimensions 4 l .. 4 l + 3 of the warp's tokens
     const int tmax = min(kC, n - c * kC);
     if (chunk_valid) {
-      for (int tt = warp; tt < tmax; tt += kAWarps) {
+#pragma unroll 4
+      for (int k = 0; k < 16; ++k) {
+        const int tt = warp + 8 * k;
+        if (tt >= tmax) break;
         const uint32_t v4 = *reinterpret_cast<const uint32_t*>(stg[s].v + tt * kD + 4 * lane);
         const float vscale = ue8m0_value(stg[s].vs[tt * (kD / 32) + (lane >> 3)]);
         const float2 lo = e4m3x2_to_float2(v4), hi = e4m3x2_to_float2(v4 >> 16);
         const float vf[4] = {lo.x * vscale, lo.y * vscale, hi.x * vscale, hi.y * vscale};
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float p = ps[g * kC + tt];
+          const float p = pw[g * 16 + k];
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[g][e] = fmaf(p, vf[e], acc[g][e]);
         }
       }
     }
-    __syncthreads();  // the stage and ps are rewritten next
+    __syncwarp();  // pw is rewritten by the next chunk
     if (t == 0 && c - c0 < 12) ATTN_STAMP(7 + 4 * (c - c0));
     stalled = -1;
   }
   if (stalled >= 0) {
-    // gave up: let the copies still in flight (this chunk's and the next
-    // one's) land before the ring is reused or the block leaves
+    // gave up: let the copies still in flight land before the ring is reused
+    // or the block leaves
     if (t == 0) {
-      for (int c = stalled; c < min(stalled + 2, c1); ++c) {
+      for (int c = stalled; c < issued; ++c) {
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(&bar[(c - c0) & 1], static_cast<uint32_t>((c - c0) >> 1) & 1u))
           if (globaltimer_ns() - t0 > 200000000ull) break;
       }
     }
-    __syncthreads();
   }
+  __syncthreads();  // every warp is done with the ring
 
   if (t == 0) {
     ATTN_STAMP(1);
     if (a.trace != nullptr) a.trace[((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * 64 + 2] = c1 - c0;
   }
-  // ---- the warps' partial outputs are summed; one record per head
-  float* wsum = reinterpret_cast<float*>(stg);  // reuse the ring: [kAWarps][G][D]
+  // ---- merge the warps' states: the block's max, sum and unnormalised
+  // output per head, one record each
+  float* wacc = reinterpret_cast<float*>(stg);  // reuse the ring: [kAWarps][G][D]
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+  for (int g = 0; g < G; ++g) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) wsum[(warp * G + g) * kD + 4 * lane + e] = acc[g][e];
+    for (int e = 0; e < 4; ++e) wacc[(warp * G + g) * kD + 4 * lane + e] = acc[g][e];
+    if (lane == 0) {
+      red_max[warp * G + g] = m_run[g];
+      red_sum[warp * G + g] = l_run[g];
+    }
+  }
   __syncthreads();
   for (int i = t; i < G * kD; i += kAThreads) {
     const int g = i / kD, d = i % kD;
-    float o = wsum[g * kD + d];
+    float M = red_max[g];
 #pragma unroll
-    for (int w = 1; w < kAWarps; ++w) o += wsum[(w * G + g) * kD + d];
+    for (int w = 1; w < kAWarps; ++w) M = fmaxf(M, red_max[w * G + g]);
+    float o = 0.f, l = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kAWarps; ++w) {
+        const float mw = red_max[w * G + g];
+        if (mw == -INFINITY) continue;
+        const float f = expf(mw - M);
+        o = fmaf(f, wacc[(w * G + g) * kD + d], o);
+        l = fmaf(f, red_sum[w * G + g], l);
+      }
+    }
     float* rec = a.part + ((static_cast<size_t>(b) * a.Hq + hk * G + g) * a.nsplit + split) * (2 + kD);
     rec[2 + d] = o;
     if (d == 0) {
-      rec[0] = m_run[g];
-      rec[1] = l_run[g];
+      rec[0] = M;
+      rec[1] = l;
     }
   }
 }
@@ -355,13 +375,17 @@ cudaError_t launch_group(const AttnArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-int attn_splits(int B, int Hkv, int max_pages, int P, int sms) {
-  // enough blocks for about four per SM, each with at least four chunks
+int attn_splits(int B, int Hkv, int max_pages, int P, int sms, int chunks_per_block) {
+  // Every block takes the same number of chunks (the last of a sequence
+  // fewer, and splits past a short sequence's end none), so the blocks are
+  // of even size whatever the length mix; with fewer (B, KV head) pairs than
+  // about three blocks per SM the chunks are spread thinner.
   const int max_chunks = (max_pages * P + kC - 1) / kC;
-  const int want = (4 * sms + B * Hkv - 1) / (B * Hkv);
-  const int cap = (max_chunks + 3) / 4;
-  int s = want < cap ? want : cap;
-  return s < 1 ? 1 : s;
+  int per = chunks_per_block;
+  const int want = (3 * sms + B * Hkv - 1) / (B * Hkv);  // splits for three blocks per SM
+  if ((max_chunks + per - 1) / per < want) per = (max_chunks + want - 1) / want;
+  if (per < 1) per = 1;
+  return (max_chunks + per - 1) / per;
 }
 
 cudaError_t launch_paged_decode(const AttnArgs& a, cudaStream_t stream) {

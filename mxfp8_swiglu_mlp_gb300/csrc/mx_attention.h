@@ -29,7 +29,8 @@ struct AttnArgs {
 
 // Splits of each sequence's chunks (one block each) for B sequences, Hkv KV
 // heads and at most max_pages pages of P tokens, on `sms` SMs.
-int attn_splits(int B, int Hkv, int max_pages, int P, int sms);
+int attn_splits(int B, int Hkv, int max_pages, int P, int sms, int chunks_per_block);
+constexpr int kAttnChunksPerBlock = 6;
 // Partial-result floats of one call.
 inline size_t attn_part_floats(int B, int Hq, int nsplit) {
   return static_cast<size_t>(B) * Hq * nsplit * (2 + kAttnHeadDim);

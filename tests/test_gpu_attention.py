@@ -100,6 +100,21 @@ def test_attention_matches_oracle(fs, B, Hq, Hkv, P, lo, hi, seed):
     _check(from_dev_bf16(out), c.oracle())
 
 
+@pytest.mark.parametrize("chunks", [1, 3, 64])
+def test_attention_chunks_per_block(fs, knob, chunks):
+    """Blocks of 1, 3 and up to 64 chunks (splits past a short sequence's end
+    run no chunk and leave an empty partial result), on a mix of lengths."""
+    import torch
+
+    knob("ATTN_CHUNKS", chunks)  # before the workspace is sized
+    wl = inputs.AttnWorkload("t", 4, 8, 2, 128, 16, 90, 2100, 7)
+    c = Cache(fs, wl)
+    out = c.run(fs)
+    torch.cuda.synchronize()
+    assert fs.fsops_read_kernel_status(c.ws_ptr) == 0
+    _check(from_dev_bf16(out), c.oracle())
+
+
 def test_attention_long_sequences_split(fs):
     """Sequences long enough to be split over several blocks (partial results
     merged by the second launch), and a zero softmax scale (uniform weights)."""
