@@ -857,6 +857,8 @@ fsops_status attn_shape(int B, int Hq, int Hkv, int D, int P, int num_pages, int
   if (D != kAttnHeadDim || (P != 16 && P != 32 && P != 64 && P != 128)) return FSOPS_ERR_UNSUPPORTED_SHAPE;
   if (num_pages < 1 || max_pages < 1 || static_cast<long long>(max_pages) * P > (1LL << 24))
     return FSOPS_ERR_UNSUPPORTED_SHAPE;
+  // the cache's token rows are TMA coordinates (int32)
+  if (static_cast<long long>(num_pages) * Hkv * P >= (1LL << 31)) return FSOPS_ERR_UNSUPPORTED_SHAPE;
   return FSOPS_OK;
 }
 }  // namespace
@@ -896,9 +898,11 @@ fsops_status fsops_mxfp8_paged_decode_attention(const void* q_bf16, const uint8_
   aa.nsplit = attn_splits(B, Hkv, max_pages, page_size, di->sms, attn_chunks_per_block());
   if (ws_bytes < kAttnStatusBytes + attn_part_floats(B, Hq, aa.nsplit) * sizeof(float)) return FSOPS_ERR_INVALID_ARG;
   aa.q = static_cast<const uint16_t*>(q_bf16);
-  aa.k_codes = k_codes;
+  const int cache_rows = num_pages * Hkv * page_size;
+  if (!encode_map(&aa.tm_k, k_codes, D, cache_rows, page_size) ||
+      !encode_map(&aa.tm_v, v_codes, D, cache_rows, page_size))
+    return FSOPS_ERR_INVALID_ARG;
   aa.k_scales = k_scales;
-  aa.v_codes = v_codes;
   aa.v_scales = v_scales;
   aa.block_table = block_table;
   aa.seq_lens = seq_lens;

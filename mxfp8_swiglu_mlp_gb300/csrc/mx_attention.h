@@ -2,19 +2,22 @@
 // (mx_attention.cu).
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace fsops {
 
 constexpr int kAttnHeadDim = 128;   // D
-constexpr int kAttnChunk = 128;     // tokens per pipeline chunk (one per thread in the QK pass)
+constexpr int kAttnChunk = 128;     // tokens per pipeline chunk (16 per consumer warp)
 constexpr int kAttnMaxGroup = 8;    // query heads per KV head
 
 struct AttnArgs {
+  // K and V codes as 2-D u8 tensors [num_pages * Hkv * P, D]: one box of P
+  // rows x D bytes per (page, KV head), 128-byte swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
   const uint16_t* q;          // bf16 [B, Hq, D]
-  const uint8_t* k_codes;     // [num_pages, Hkv, P, D] E4M3
   const uint8_t* k_scales;    // [num_pages, Hkv, P, D / 32] UE8M0
-  const uint8_t* v_codes;
   const uint8_t* v_scales;
   const int32_t* block_table; // [B, max_pages]
   const int32_t* seq_lens;    // [B]

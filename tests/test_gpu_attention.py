@@ -22,11 +22,13 @@ def fs():
 class Cache:
     """A workload's paged cache on the device, quantised by the library."""
 
-    def __init__(self, fs, wl):
+    def __init__(self, fs, wl, mutate=None):
         import torch
 
         self.wl = wl
         self.d = inputs.make_attention(wl)
+        if mutate is not None:
+            mutate(self.d)
         npages = self.d["k"].shape[0]
         self.npages = npages
         rows = npages * wl.Hkv * wl.P
@@ -109,6 +111,53 @@ def test_attention_chunks_per_block(fs, knob, chunks):
     knob("ATTN_CHUNKS", chunks)  # before the workspace is sized
     wl = inputs.AttnWorkload("t", 4, 8, 2, 128, 16, 90, 2100, 7)
     c = Cache(fs, wl)
+    out = c.run(fs)
+    torch.cuda.synchronize()
+    assert fs.fsops_read_kernel_status(c.ws_ptr) == 0
+    _check(from_dev_bf16(out), c.oracle())
+
+
+def _pow2(bits, k):
+    """bf16 bit patterns times 2^k (exact while the result stays normal)."""
+    return inputs.bf16_bits_from_f32(bf16_bits_to_f64(bits).astype(np.float32) * np.float32(2.0 ** k))
+
+
+def _spread_v(d):
+    """Every third token's V 2^-20 times smaller (its block scales 2^20 below
+    its neighbours'), and a few all-zero 32-element V blocks (scale byte 0)."""
+    v = d["v"]
+    v[:, :, 1::3, :] = _pow2(v[:, :, 1::3, :], -20)
+    v[::2, 0, 5, 32:64] = 0
+    v[1::3, -1, 12, 96:128] = 0
+
+
+def _q_range(d):
+    """Query heads far from unit size: one 2^40 times larger (a one-hot
+    softmax), one 2^-40 times smaller (uniform weights), one with a single
+    large element."""
+    q = d["q"]
+    q[:, 0, :] = _pow2(q[:, 0, :], 40)
+    q[:, 1, :] = _pow2(q[:, 1, :], -40)
+    q[:, 2, 7] = _pow2(q[:, 2, 7], 20)
+
+
+def _k_spread(d):
+    """Every fifth token's K 2^-12 times smaller, every seventh 2^6 larger."""
+    k = d["k"]
+    k[:, :, 0::5, :] = _pow2(k[:, :, 0::5, :], -12)
+    k[:, :, 3::7, :] = _pow2(k[:, :, 3::7, :], 6)
+
+
+@pytest.mark.parametrize("mutate", [_spread_v, _q_range, _k_spread], ids=["v_spread", "q_range", "k_spread"])
+def test_attention_scale_ranges(fs, mutate):
+    """Scales far apart within one tensor-core step: V block scales 2^15 and
+    more apart among 16 neighbouring tokens (and zero blocks), which the
+    kernel adds with fp32 FMAs; query heads of very different size (the
+    power-of-two prescale of q); K scales spread over 2^18."""
+    import torch
+
+    wl = inputs.AttnWorkload("t", 3, 8, 2, 128, 16, 100, 700, 11)
+    c = Cache(fs, wl, mutate)
     out = c.run(fs)
     torch.cuda.synchronize()
     assert fs.fsops_read_kernel_status(c.ws_ptr) == 0
