@@ -263,10 +263,13 @@ fsops_status fsops_mxfp8_swiglu_mlp_block(const void* x_bf16, const void* gamma_
  *   Limits: D = 128; P in {16, 32, 64, 128}; Hq / Hkv in {1, 2, 4, 8};
  *   B, Hkv <= 65535.  Pointers 16-byte aligned (block_table, seq_lens 4).
  *   workspace: 256-byte aligned, fsops_paged_attention_workspace_bytes() of
- *   device memory whose first word (the status word) is zero; a page id
- *   outside [0, num_pages) or a bad length is reported there
- *   (fsops_read_kernel_status) instead of being read.  Two launches (the
- *   splits of each sequence, then their combination); graph-capture safe. */
+ *   device memory whose first 256 bytes are zero before the first call: the
+ *   status word, where a page id outside [0, num_pages) or a bad length is
+ *   reported (fsops_read_kernel_status) instead of being read, and the
+ *   counter from which the first launch's persistent blocks take their work
+ *   (each call leaves it zero).  Two launches (the splits of each sequence,
+ *   then their combination); graph-capture safe.  Calls sharing a workspace
+ *   are serialised by their stream. */
 fsops_status fsops_mxfp8_paged_decode_attention(const void* q_bf16, const uint8_t* k_codes, const uint8_t* k_scales,
                                                 const uint8_t* v_codes, const uint8_t* v_scales, int num_pages,
                                                 const int32_t* block_table, int max_pages, const int32_t* seq_lens,

@@ -896,6 +896,7 @@ fsops_status fsops_mxfp8_paged_decode_attention(const void* q_bf16, const uint8_
   AttnArgs aa;
   std::memset(&aa, 0, sizeof(aa));
   aa.nsplit = attn_splits(B, Hkv, max_pages, page_size, di->sms, attn_chunks_per_block());
+  aa.grid = attn_grid(aa.nsplit * B * Hkv, di->sms);
   if (ws_bytes < kAttnStatusBytes + attn_part_floats(B, Hq, aa.nsplit) * sizeof(float)) return FSOPS_ERR_INVALID_ARG;
   aa.q = static_cast<const uint16_t*>(q_bf16);
   const int cache_rows = num_pages * Hkv * page_size;
@@ -908,6 +909,7 @@ fsops_status fsops_mxfp8_paged_decode_attention(const void* q_bf16, const uint8_
   aa.seq_lens = seq_lens;
   aa.out = static_cast<uint16_t*>(out_bf16);
   aa.status = static_cast<uint32_t*>(workspace);
+  aa.work = static_cast<uint32_t*>(workspace) + 1;
   aa.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kAttnStatusBytes);
   aa.B = B;
   aa.Hq = Hq;

@@ -52,7 +52,7 @@ using namespace dev;
 namespace {
 
 constexpr int kCWarps = 8;                        // consumer warps, 16 tokens of a chunk each
-constexpr int kAThreads = 32 * (kCWarps + 1);     // + the producer warp
+constexpr int kAThreads = 32 * (kCWarps + 2);     // + the copy warp and the scale warp
 constexpr int kAStages = 3;
 constexpr int kD = kAttnHeadDim;
 constexpr int kC = kAttnChunk;
@@ -68,6 +68,15 @@ struct __align__(1024) AttnStage {
   uint8_t vs[kScaleBytes];
 };
 static_assert(sizeof(AttnStage) % 1024 == 0, "stages stay 1024-byte aligned");
+// What the producer derives from a chunk's V scales once, for the consumer
+// lanes (warp w, column pair tq) that share tokens rv = 16 w + 2 tq +
+// {0, 1, 8, 9}: per 32-dimension block bb the f16x2 multipliers 2^(s - s_max)
+// of the token pairs (rv, rv + 1) and (rv + 8, rv + 9), s_max the block's
+// largest scale among the warp's 16 tokens (byte bb of smax[w]).
+struct AttnPrep {
+  uint4 vm[kCWarps * 4][2];
+  uint32_t smax[kCWarps];
+};
 constexpr size_t kAttnSmem = kAStages * sizeof(AttnStage) + 1024;  // + alignment slack
 
 // Byte offset of (row, byte) in a 128-byte-swizzled tile whose base is
@@ -157,6 +166,48 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint6
   } while (0)
 #endif
 
+// One work item: chunks [c0, c1) of KV head hk of sequence b (its split
+// `split`); n is the sequence's length (0 when it is out of range).
+struct AttnItem {
+  int b, hk, split, n, c0, c1;
+};
+// Items are numbered with the KV head fastest, then the sequence, then the
+// split, so that the blocks take the full-size splits first.
+__device__ __forceinline__ AttnItem attn_item(const AttnArgs& a, int it) {
+  AttnItem w;
+  w.hk = it % a.Hkv;
+  const int r = it / a.Hkv;
+  w.b = r % a.B;
+  w.split = r / a.B;
+  const int len = a.seq_lens[w.b];
+  w.n = (len >= 1 && len <= a.max_pages * a.P) ? len : 0;
+  // every split the same number of chunks of the longest sequence's
+  const int per = (a.max_pages * a.P + kC * a.nsplit - 1) / (kC * a.nsplit);
+  const int nchunks = (w.n + kC - 1) / kC;
+  w.c0 = min(nchunks, w.split * per);
+  w.c1 = min(nchunks, w.c0 + per);
+  return w;
+}
+
+// What a stage holds, written by the producer: the chunk's item and position.
+enum : uint32_t {
+  kMetaFirst = 1,  // the item's first chunk
+  kMetaLast = 2,   // the item's last chunk
+  kMetaOk = 4,     // every page id of the chunk was in range (else the chunk is skipped)
+  kMetaFar = 8,    // p . v in fp32 FMAs (a V scale 2^15 or more below its group's largest)
+  kMetaEnd = 16,   // no more work: the consumers leave
+};
+struct ChunkMeta {
+  int b, hk, split, n, c;
+  uint32_t flags;
+};
+
+// Persistent: each block takes work items from a counter shared by the grid
+// (largest first, by the item order) and streams their chunks as one
+// sequence through the ring, so the copies of an item's first chunks are in
+// flight while the previous item is finished; at an item's end the consumer
+// warps merge their states in the stage of its last chunk and write the
+// item's record.  The second launch resets the counter.
 template <int G>
 __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -164,70 +215,29 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
   // each consumer warp's probabilities of its 16 tokens: [warp][head][token]
   __shared__ __align__(16) float pws[kCWarps * 8 * kPwLd];
   __shared__ float red_max[kCWarps * G], red_sum[kCWarps * G];
-  __shared__ __align__(8) uint64_t full[kAStages], empty[kAStages];
-  __shared__ int chunk_ok[kAStages];
-  // q of the group as the B operand of the score MMA, per lane: block bb's
-  // two k-steps in qfrag[bb][lane]; sm_scale / 2^e per head
-  __shared__ uint4 qfrag[4][32];
-  __shared__ float qscale[8];
+  __shared__ __align__(8) uint64_t full[kAStages], ready[kAStages], empty[kAStages], qfree[2], mrg[2];
+  __shared__ AttnPrep prep[kAStages];
+  __shared__ ChunkMeta meta[kAStages];
+  // q of an item's group as the B operand of the score MMA (two buffers, by
+  // item parity), per lane: block bb's two k-steps in qfrag[.][bb][lane];
+  // sm_scale log2(e) / 2^e per head (the softmax runs in base 2)
+  __shared__ uint4 qfrag[2][4][32];
+  __shared__ float qscale[2][8];
 
-  const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int len = a.seq_lens[b];
-  const bool len_ok = len >= 1 && len <= a.max_pages * a.P;
-  if (!len_ok && t == 0 && split == 0 && hk == 0) attn_error(a, 1u, 1u);  // FSOPS_ERR_INVALID_ARG
-  const int n = len_ok ? len : 0;
-  const int nchunks = (n + kC - 1) / kC;
-  // every split the same number of chunks of the longest sequence's
-  const int per = (a.max_pages * a.P + kC * a.nsplit - 1) / (kC * a.nsplit);
-  const int c0 = min(nchunks, split * per), c1 = min(nchunks, c0 + per);
+  const int items = a.nsplit * a.B * a.Hkv;
 
-  if (warp == 0) {
-    // Lane (g, tq) holds head g's B fragments: k-step j (dimensions of block
-    // j / 2) pairs mma column k = 2 tq + {0, 1} with dimension
-    // 32 (j / 2) + 8 tq + 4 (j % 2) + {0, 1} and k = 2 tq + 8 + {0, 1} with
-    // + {2, 3}, so that a lane's 8-byte K load feeds two k-steps.  Each head
-    // is scaled by the power of two 2^e that puts its largest |q| in
-    // [2^13, 2^14): exact in f16.
-    const int g = lane >> 2, tq = lane & 3;
-    float qv[32];
-    if (g < G) {
-      const uint4* qp = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + hk * G + g) * kD);
-#pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
-        const uint4 w = qp[4 * bb + tq];
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          qv[8 * bb + 2 * j] = bf16_bits_to_float(ws[j] & 0xFFFFu);
-          qv[8 * bb + 2 * j + 1] = bf16_bits_to_float(ws[j] >> 16);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) qv[j] = 0.f;
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(qv[j]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-    int e = 0;
-    if (amax > 0.f) e = min(140 - static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu), 126);
-    const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
-#pragma unroll
-    for (int bb = 0; bb < 4; ++bb)
-      qfrag[bb][lane] = make_uint4(f16x2_rn(qv[8 * bb] * up, qv[8 * bb + 1] * up),
-                                   f16x2_rn(qv[8 * bb + 2] * up, qv[8 * bb + 3] * up),
-                                   f16x2_rn(qv[8 * bb + 4] * up, qv[8 * bb + 5] * up),
-                                   f16x2_rn(qv[8 * bb + 6] * up, qv[8 * bb + 7] * up));
-    if (tq == 0) qscale[g] = ldexpf(a.sm_scale, -e);
-  }
   if (t == 0) {
 #pragma unroll
     for (int s = 0; s < kAStages; ++s) {
       mbar_init(&full[s], 1);
+      mbar_init(&ready[s], 32);
       mbar_init(&empty[s], kCWarps);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qfree[i], kCWarps);
+      mbar_init(&mrg[i], kCWarps);
     }
     mbar_fence_init();
     ATTN_STAMP(0);
@@ -235,27 +245,15 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
   __syncthreads();
 
   const int g = lane >> 2, tq = lane & 3;  // mma fragment row group and column pair
-  // consumer state: the p . v sums O^T[d][head] of the warp's tokens (blocks
-  // of 32 dimensions bb, two 16-row tiles each: rows g and g + 8 are
-  // dimensions 32 bb + 4 g + {0, 1} of tile 0 and + {2, 3} of tile 1; columns
-  // heads 2 tq and 2 tq + 1), and the running max and partial sums of the
-  // lane's two heads
-  float O[4][2][4];
-#pragma unroll
-  for (int bb = 0; bb < 4; ++bb)
-#pragma unroll
-    for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) O[bb][tt][e] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
 
-  if (warp == kCWarps) {
-    // ---- producer: chunk c into stage (c - c0) % kAStages once every
-    // consumer warp has left the chunk that held it; lane i copies the
-    // chunk's page i.  Pages past the sequence's last one are not loaded
-    // (their tokens are masked); a page id outside [0, num_pages) is reported
-    // and the chunk skipped.
-    const int npages = (n + a.P - 1) / a.P;
+  if (warp >= kCWarps) {
+    // ---- producers.  The copy warp puts chunk number q of the block's
+    // stream into stage q % kAStages as soon as the consumers have left the
+    // chunk that held it; lane i copies the chunk's page i.  Pages past a
+    // sequence's last one are not loaded (their tokens are masked); a page id
+    // outside [0, num_pages) is reported and the chunk skipped.  The scale
+    // warp, once a chunk has landed, derives its V-scale multipliers (and an
+    // item's q fragments) and marks it ready.
     const int ppc = kC / a.P;
     const uint32_t cb = static_cast<uint32_t>(a.P) * kD, sb = static_cast<uint32_t>(a.P) * (kD / 32);
     const uint64_t pol = l2_policy_evict_first();
@@ -263,271 +261,472 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
       tma_prefetch_desc(&a.tm_k);
       tma_prefetch_desc(&a.tm_v);
     }
-    int issued = c0;
-    for (int c = c0; c < c1; ++c) {
-      const int i = c - c0, s = i % kAStages;
-      if (i >= kAStages && !wait_phase(&empty[s], static_cast<uint32_t>(i / kAStages - 1) & 1u, a.timeout_ns)) {
-        if (lane == 0) attn_error(a, 5u, 4u);  // FSOPS_ERR_TIMEOUT
-        break;
+    // the next non-empty item from the shared counter (false: none left)
+    auto grab = [&](AttnItem& w) -> bool {
+      int found = 0;
+      if (lane == 0) {
+        for (;;) {
+          const int it = static_cast<int>(atomicAdd(a.work, 1u));
+          if (it >= items) break;
+          w = attn_item(a, it);
+          if (w.n == 0 && w.split == 0 && w.hk == 0) attn_error(a, 1u, 1u);  // a length outside [1, max_pages P]
+          if (w.c0 < w.c1) {
+            found = 1;
+            break;
+          }
+        }
       }
-      const int p0 = c * ppc;
-      const int np = min(ppc, npages - p0);
-      int pid = -1;
+      found = __shfl_sync(0xFFFFFFFFu, found, 0);
+      w.b = __shfl_sync(0xFFFFFFFFu, w.b, 0);
+      w.hk = __shfl_sync(0xFFFFFFFFu, w.hk, 0);
+      w.split = __shfl_sync(0xFFFFFFFFu, w.split, 0);
+      w.n = __shfl_sync(0xFFFFFFFFu, w.n, 0);
+      w.c0 = __shfl_sync(0xFFFFFFFFu, w.c0, 0);
+      w.c1 = __shfl_sync(0xFFFFFFFFu, w.c1, 0);
+      return found != 0;
+    };
+    // issue cursor: chunk c of item cur (item nxt grabbed one ahead); lane i
+    // holds page id pid of the chunk's page i (loaded one issue ahead)
+    AttnItem cur{}, nxt{};
+    bool have_cur = false, have_nxt = false;
+    int c = 0;
+    int pid = -1, np = 0;
+    auto load_pids = [&]() {
+      const int npages = (cur.n + a.P - 1) / a.P;
+      np = min(ppc, npages - c * ppc);
+      pid = lane < np ? a.block_table[static_cast<size_t>(cur.b) * a.max_pages + c * ppc + lane] : -1;
+    };
+    bool ended = false;
+    auto issue_next = [&](int s) {
+      if (!have_cur) {
+        if (lane == 0) {
+          meta[s].flags = kMetaEnd;
+          mbar_arrive(&full[s]);
+        }
+        ended = true;
+        return;
+      }
       const bool mine = lane < np;
-      bool good = true;
-      if (mine) {
-        pid = a.block_table[static_cast<size_t>(b) * a.max_pages + p0 + lane];
-        good = pid >= 0 && pid < a.num_pages;
-      }
+      const bool good = !mine || (pid >= 0 && pid < a.num_pages);
       const bool all_good = __all_sync(0xFFFFFFFFu, good);
       const uint32_t npg = __popc(__ballot_sync(0xFFFFFFFFu, mine && good));
       if (lane == 0) {
         if (!all_good) attn_error(a, 1u, 2u);
-        chunk_ok[s] = all_good ? 1 : 0;
+        meta[s].b = cur.b;
+        meta[s].hk = cur.hk;
+        meta[s].split = cur.split;
+        meta[s].n = cur.n;
+        meta[s].c = c;
+        meta[s].flags = (c == cur.c0 ? kMetaFirst : 0u) | (c + 1 == cur.c1 ? kMetaLast : 0u) |
+                        (all_good ? kMetaOk : 0u);
       }
       fence_proxy_async_shared();  // the stage's earlier generic reads come before the copies' writes
       if (lane == 0) mbar_arrive_expect_tx(&full[s], npg * 2u * (cb + sb));
       __syncwarp();
       if (mine && good) {
-        const int y = (pid * a.Hkv + hk) * a.P;  // first row of the (page, head) block
+        const int y = (pid * a.Hkv + cur.hk) * a.P;  // first row of the (page, head) block
         tma_load_2d(stg[s].k + lane * cb, &a.tm_k, &full[s], 0, y, pol);
         tma_load_2d(stg[s].v + lane * cb, &a.tm_v, &full[s], 0, y, pol);
         bulk_load(stg[s].ks + lane * sb, a.k_scales + static_cast<size_t>(y) * (kD / 32), sb, &full[s], pol);
         bulk_load(stg[s].vs + lane * sb, a.v_scales + static_cast<size_t>(y) * (kD / 32), sb, &full[s], pol);
       }
-      issued = c + 1;
-    }
-    // the last chunks' copies land before the ring is reused (every earlier
-    // chunk of a stage was consumed before the stage was refilled)
-    for (int c = max(c0, issued - kAStages); c < issued; ++c)
-      wait_phase(&full[(c - c0) % kAStages], static_cast<uint32_t>((c - c0) / kAStages) & 1u, 200000000ull);
-  } else {
-    // ---- consumer warp: tokens 16 warp .. 16 warp + 15 of every chunk
-    const int wrow = 16 * warp;
-    float hs[2];  // sm_scale / 2^e of heads 2 tq and 2 tq + 1
-    hs[0] = qscale[2 * tq];
-    hs[1] = qscale[2 * tq + 1];
-    float* pw = pws + warp * 8 * kPwLd;
+      if (++c >= cur.c1) {
+        have_cur = have_nxt;
+        cur = nxt;
+        c = cur.c0;
+        if (have_cur) have_nxt = grab(nxt);
+      }
+      if (have_cur) load_pids();
+    };
+    // q of item (b, hk) into buffer qb: lane (g, tq) holds head g's B
+    // fragments: k-step j (dimensions of block j / 2) pairs mma column
+    // k = 2 tq + {0, 1} with dimension 32 (j / 2) + 8 tq + 4 (j % 2) + {0, 1}
+    // and k = 2 tq + 8 + {0, 1} with + {2, 3}, so that a consumer lane's
+    // 8-byte K load feeds two k-steps.  Each head is scaled by the power of
+    // two 2^e that puts its largest |q| in [2^13, 2^14): exact in f16.
+    auto load_q = [&](int b, int hk, int qb) {
+      float qv[32];
+      if (g < G) {
+        const uint4* qp = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + hk * G + g) * kD);
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+          const uint4 v = qp[4 * bb + tq];
+          const uint32_t vs4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            qv[8 * bb + 2 * j] = bf16_bits_to_float(vs4[j] & 0xFFFFu);
+            qv[8 * bb + 2 * j + 1] = bf16_bits_to_float(vs4[j] >> 16);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) qv[j] = 0.f;
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(qv[j]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+      int e = 0;
+      if (amax > 0.f) e = min(140 - static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu), 126);
+      const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb)
+        qfrag[qb][bb][lane] = make_uint4(f16x2_rn(qv[8 * bb] * up, qv[8 * bb + 1] * up),
+                                         f16x2_rn(qv[8 * bb + 2] * up, qv[8 * bb + 3] * up),
+                                         f16x2_rn(qv[8 * bb + 4] * up, qv[8 * bb + 5] * up),
+                                         f16x2_rn(qv[8 * bb + 6] * up, qv[8 * bb + 7] * up));
+      if (tq == 0) qscale[qb][g] = ldexpf(a.sm_scale * 1.4426950408889634f, -e);
+    };
+    // the V-scale multipliers of the chunk in stage s, lane 4 w + tq those of
+    // consumer warp w's column pair tq
+    auto prepare = [&](int s) {
+      const int pwp = lane >> 2, ptq = lane & 3;
+      const int tmax = min(kC, meta[s].n - meta[s].c * kC);
+      const int rv = 16 * pwp + 2 * ptq;
+      const int rows[4] = {rv, rv + 1, rv + 8, rv + 9};
+      uint32_t sw[4], ex[4];
+      bool tv[4];
+      uint32_t mref = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        tv[k] = rows[k] < tmax;
+        sw[k] = *reinterpret_cast<const uint32_t*>(stg[s].vs + 4 * rows[k]);
+        if (tv[k]) mref = __vmaxu4(mref, sw[k]);
+      }
+      mref = __vmaxu4(mref, __shfl_xor_sync(0xFFFFFFFFu, mref, 1));
+      mref = __vmaxu4(mref, __shfl_xor_sync(0xFFFFFFFFu, mref, 2));
+      bool far = false;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        ex[k] = tv[k] ? __vsubus4(0x0F0F0F0Fu, __vsub4(mref, sw[k])) : 0u;  // 15 - (s_max - s), at least 0
+        far |= tv[k] && __vcmpeq4(ex[k], 0u) != 0u;
+      }
+      far = __any_sync(0xFFFFFFFFu, far);
+      uint32_t m01[4], m89[4];
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        // bytes (s0, 0, s1, 0) of the pair's exponents, shifted into f16 exponent fields
+        const uint32_t sel = 0xC480u + 0x1111u * bb;
+        m01[bb] = prmt(ex[0], ex[1], sel) << 10;
+        m89[bb] = prmt(ex[2], ex[3], sel) << 10;
+      }
+      prep[s].vm[lane][0] = make_uint4(m01[0], m01[1], m01[2], m01[3]);
+      prep[s].vm[lane][1] = make_uint4(m89[0], m89[1], m89[2], m89[3]);
+      if (ptq == 0) prep[s].smax[pwp] = mref;
+      // one warp's far chunk sends the whole chunk to the fp32 path
+      if (lane == 0 && far) meta[s].flags |= kMetaFar;
+    };
 
-    for (int c = c0; c < c1; ++c) {
-      const int i = c - c0, s = i % kAStages;
-      if (!wait_phase(&full[s], static_cast<uint32_t>(i / kAStages) & 1u, a.timeout_ns)) {
+    if (warp == kCWarps) {
+      // (only this warp takes work from the counter)
+      have_cur = grab(cur);
+      c = cur.c0;
+      if (have_cur) {
+        have_nxt = grab(nxt);
+        load_pids();
+      }
+      int issued = 0;
+      for (int q = 0; !ended; ++q) {
+        const int s = q % kAStages;
+        if (q >= kAStages && !wait_phase(&empty[s], static_cast<uint32_t>(q / kAStages - 1) & 1u, a.timeout_ns)) {
+          if (lane == 0) attn_error(a, 5u, 4u);  // FSOPS_ERR_TIMEOUT
+          break;
+        }
+        issue_next(s);
+        if (lane == 0 && q < 10) ATTN_STAMP(54 + q);
+        issued = q + 1;
+      }
+      // the last chunks' copies land before the block leaves (every earlier
+      // chunk of a stage was consumed before the stage was refilled)
+      for (int q = max(0, issued - kAStages); q < issued; ++q)
+        wait_phase(&full[q % kAStages], static_cast<uint32_t>(q / kAStages) & 1u, 200000000ull);
+    } else {
+      int kq = 0;  // items begun
+      for (int q = 0;; ++q) {
+        const int s = q % kAStages;
+        if (!wait_phase(&full[s], static_cast<uint32_t>(q / kAStages) & 1u, a.timeout_ns)) {
+          if (lane == 0) attn_error(a, 5u, 3u);  // FSOPS_ERR_TIMEOUT
+          break;
+        }
+        if (lane == 0 && q < 10) ATTN_STAMP(44 + q);
+        const uint32_t fl = meta[s].flags;
+        if (fl & kMetaEnd) {
+          __syncwarp();
+          mbar_arrive(&ready[s]);
+          break;
+        }
+        if (fl & kMetaFirst) {
+          // the buffer's previous item (two back) is done with it
+          const int qb = kq & 1;
+          if (kq >= 2 && !wait_phase(&qfree[qb], static_cast<uint32_t>((kq >> 1) - 1) & 1u, a.timeout_ns)) {
+            if (lane == 0) attn_error(a, 5u, 5u);  // FSOPS_ERR_TIMEOUT
+            break;
+          }
+          load_q(meta[s].b, meta[s].hk, qb);
+          ++kq;
+        }
+        prepare(s);
+        __syncwarp();
+        mbar_arrive(&ready[s]);
+      }
+    }
+  } else {
+    // ---- consumer warp: tokens 16 warp .. 16 warp + 15 of every chunk.
+    // Its state: the p . v sums O^T[d][head] of the warp's tokens (blocks of
+    // 32 dimensions bb, two 16-row tiles each: rows g and g + 8 are
+    // dimensions 32 bb + 4 g + {0, 1} of tile 0 and + {2, 3} of tile 1;
+    // columns heads 2 tq and 2 tq + 1), and the running max and partial sums
+    // of the lane's two heads.
+    const int wrow = 16 * warp;
+    float* pw = pws + warp * 8 * kPwLd;
+    int kq = 0, qb = 0;
+    float O[4][2][4];
+    float m_run[2], l_part[2];
+    float hs[2] = {0.f, 0.f};  // sm_scale log2(e) / 2^e of heads 2 tq and 2 tq + 1
+    for (int seq = 0;; ++seq) {
+      const int s = seq % kAStages;
+      const uint32_t par = static_cast<uint32_t>(seq / kAStages) & 1u;
+      if (t == 0 && seq < 10) ATTN_STAMP(4 + 4 * seq);
+      if (!wait_phase(&full[s], par, a.timeout_ns) || !wait_phase(&ready[s], par, a.timeout_ns)) {
         if (lane == 0) attn_error(a, 5u, 3u);  // FSOPS_ERR_TIMEOUT
         break;
       }
-      const int tmax = min(kC, n - c * kC);  // valid rows of the chunk
-      if (chunk_ok[s] != 0 && wrow < tmax) {
-        const uint8_t* kb = stg[s].k;
-        const uint8_t* vb = stg[s].v;
-        // ---- scores of tokens r0 and r1 (mma rows g, g + 8) for heads 2 tq, 2 tq + 1
-        const int r0 = wrow + g, r1 = r0 + 8;
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          const uint32_t kw0 = *reinterpret_cast<const uint32_t*>(stg[s].ks + 4 * r0);
-          const uint32_t kw1 = *reinterpret_cast<const uint32_t*>(stg[s].ks + 4 * r1);
+      if (t == 0 && seq < 10) ATTN_STAMP(5 + 4 * seq);
+      const ChunkMeta m = meta[s];
+      if (m.flags & kMetaEnd) break;
+      if (m.flags & kMetaFirst) {
 #pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            const uint2 x0 = *reinterpret_cast<const uint2*>(kb + swz(r0, 32 * bb + 8 * tq));
-            const uint2 x1 = *reinterpret_cast<const uint2*>(kb + swz(r1, 32 * bb + 8 * tq));
-            const uint4 bq = qfrag[bb][lane];
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_16816(d, e4m3_lo_f16x2(x0.x), e4m3_lo_f16x2(x1.x), e4m3_hi_f16x2(x0.x), e4m3_hi_f16x2(x1.x), bq.x,
-                      bq.y);
-            mma_16816(d, e4m3_lo_f16x2(x0.y), e4m3_lo_f16x2(x1.y), e4m3_hi_f16x2(x0.y), e4m3_hi_f16x2(x1.y), bq.z,
-                      bq.w);
-            const float f0 = ue8m0_value((kw0 >> (8 * bb)) & 0xFFu), f1 = ue8m0_value((kw1 >> (8 * bb)) & 0xFFu);
-            sc[0] = fmaf(f0, d[0], sc[0]);
-            sc[1] = fmaf(f0, d[1], sc[1]);
-            sc[2] = fmaf(f1, d[2], sc[2]);
-            sc[3] = fmaf(f1, d[3], sc[3]);
-          }
-        }
-        // ---- the warp's online softmax over its 16 tokens, per head
-        const bool v0 = r0 < tmax, v1 = r1 < tmax;
-        float al[2];
+        for (int bb = 0; bb < 4; ++bb)
 #pragma unroll
-        for (int i2 = 0; i2 < 2; ++i2) {
-          const int hh = 2 * tq + i2;
-          const bool hv = hh < G;
-          const float x0 = (v0 && hv) ? sc[i2] * hs[i2] : -INFINITY;
-          const float x1 = (v1 && hv) ? sc[2 + i2] * hs[i2] : -INFINITY;
-          float cm = fmaxf(x0, x1);
-          cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 4));
-          cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 8));
-          cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 16));
-          const float mn = fmaxf(m_run[i2], cm);
-          // no valid token yet: mn = -inf and nothing is added
-          al[i2] = mn == -INFINITY ? 1.f : expf(m_run[i2] - mn);
-          const float p0 = x0 == -INFINITY ? 0.f : expf(x0 - mn);
-          const float p1 = x1 == -INFINITY ? 0.f : expf(x1 - mn);
-          m_run[i2] = mn;
-          l_part[i2] = fmaf(l_part[i2], al[i2], p0 + p1);
-          pw[hh * kPwLd + g] = p0;
-          pw[hh * kPwLd + g + 8] = p1;
-        }
-        if (al[0] != 1.f || al[1] != 1.f) {
+          for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
-          for (int bb = 0; bb < 4; ++bb)
-#pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-              O[bb][tt][0] *= al[0];
-              O[bb][tt][1] *= al[1];
-              O[bb][tt][2] *= al[0];
-              O[bb][tt][3] *= al[1];
-            }
-        }
-        __syncwarp();  // pw is written before the lanes read it
-
-        // ---- p . v: A = V^T (rows: dimensions, k: tokens rv, rv + 1, rv + 8,
-        // rv + 9 of the lane), B = p of head g
-        const int rv = wrow + 2 * tq;
-        const int rvk[4] = {rv, rv + 1, rv + 8, rv + 9};
-        uint32_t sw[4], ex[4];
-        bool tv[4];
-        uint32_t mref = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          tv[k] = rvk[k] < tmax;
-          sw[k] = *reinterpret_cast<const uint32_t*>(stg[s].vs + 4 * rvk[k]);
-          if (tv[k]) mref = __vmaxu4(mref, sw[k]);
-        }
-        mref = __vmaxu4(mref, __shfl_xor_sync(0xFFFFFFFFu, mref, 1));
-        mref = __vmaxu4(mref, __shfl_xor_sync(0xFFFFFFFFu, mref, 2));
-        bool far = false;  // a valid token's block scale 2^15 or more below its group's largest
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          ex[k] = tv[k] ? __vsubus4(0x0F0F0F0Fu, __vsub4(mref, sw[k])) : 0u;  // 15 - (s_max - s), at least 0
-          far |= tv[k] && __vcmpeq4(ex[k], 0u) != 0u;
-        }
-        if (!__any_sync(0xFFFFFFFFu, far)) {
-          uint32_t bh0, bh1, bl0, bl1;
-          split_f16x2(*reinterpret_cast<const float2*>(pw + g * kPwLd + 2 * tq), bh0, bl0);
-          split_f16x2(*reinterpret_cast<const float2*>(pw + g * kPwLd + 2 * tq + 8), bh1, bl1);
-          const bool full16 = wrow + 16 <= tmax;
-          const uint32_t k01 = (tv[0] ? 0x0000FFFFu : 0u) | (tv[1] ? 0xFFFF0000u : 0u);
-          const uint32_t k89 = (tv[2] ? 0x0000FFFFu : 0u) | (tv[3] ? 0xFFFF0000u : 0u);
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            const int off = 32 * bb + 4 * g;
-            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vb + swz(rvk[0], off));
-            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vb + swz(rvk[1], off));
-            const uint32_t w8 = *reinterpret_cast<const uint32_t*>(vb + swz(rvk[2], off));
-            const uint32_t w9 = *reinterpret_cast<const uint32_t*>(vb + swz(rvk[3], off));
-            // f16x2 2^(s - s_max) of the token pairs (rv, rv + 1), (rv + 8, rv + 9)
-            const uint32_t sel = static_cast<uint32_t>(bb) | ((8u | bb) << 4) | ((4u + bb) << 8) | ((12u + bb) << 12);
-            const uint32_t m01 = prmt(ex[0], ex[1], sel) << 10, m89 = prmt(ex[2], ex[3], sel) << 10;
-            // dimension pairs (d, d + 1) and (d + 2, d + 3) of the token pairs
-            const uint32_t x01 = prmt(w0, w1, 0x5140u), y01 = prmt(w0, w1, 0x7362u);
-            const uint32_t x89 = prmt(w8, w9, 0x5140u), y89 = prmt(w8, w9, 0x7362u);
-            uint32_t A0[4] = {hmul2(e4m3_lo_f16x2(x01), m01), hmul2(e4m3_hi_f16x2(x01), m01),
-                              hmul2(e4m3_lo_f16x2(x89), m89), hmul2(e4m3_hi_f16x2(x89), m89)};
-            uint32_t A1[4] = {hmul2(e4m3_lo_f16x2(y01), m01), hmul2(e4m3_hi_f16x2(y01), m01),
-                              hmul2(e4m3_lo_f16x2(y89), m89), hmul2(e4m3_hi_f16x2(y89), m89)};
-            if (!full16) {  // tokens past the sequence: their stale codes may not be finite
-              A0[0] &= k01;
-              A0[1] &= k01;
-              A0[2] &= k89;
-              A0[3] &= k89;
-              A1[0] &= k01;
-              A1[1] &= k01;
-              A1[2] &= k89;
-              A1[3] &= k89;
-            }
-            float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_16816(d0, A0[0], A0[1], A0[2], A0[3], bh0, bh1);
-            mma_16816(d0, A0[0], A0[1], A0[2], A0[3], bl0, bl1);
-            mma_16816(d1, A1[0], A1[1], A1[2], A1[3], bh0, bh1);
-            mma_16816(d1, A1[0], A1[1], A1[2], A1[3], bl0, bl1);
-            const float rf = ue8m0_value((mref >> (8 * bb)) & 0xFFu);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              O[bb][0][e] = fmaf(rf, d0[e], O[bb][0][e]);
-              O[bb][1][e] = fmaf(rf, d1[e], O[bb][1][e]);
-            }
-          }
-        } else {
-          // fp32 FMAs: each lane its 16 dimensions x 2 heads over the 16 tokens
-#pragma unroll 1
-          for (int kk = 0; kk < 16; ++kk) {
-            const int r = wrow + kk;
-            if (r >= tmax) break;
-            const float q0 = pw[(2 * tq) * kPwLd + kk], q1 = pw[(2 * tq + 1) * kPwLd + kk];
-            const uint32_t swd = *reinterpret_cast<const uint32_t*>(stg[s].vs + 4 * r);
-#pragma unroll
+            for (int e = 0; e < 4; ++e) O[bb][tt][e] = 0.f;
+        m_run[0] = m_run[1] = -INFINITY;
+        l_part[0] = l_part[1] = 0.f;
+        qb = kq & 1;
+        hs[0] = qscale[qb][2 * tq];
+        hs[1] = qscale[qb][2 * tq + 1];
+      }
+        const int tmax = min(kC, m.n - m.c * kC);  // valid rows of the chunk
+        if ((m.flags & kMetaOk) != 0 && wrow < tmax) {
+          const uint8_t* kb = stg[s].k;
+          const uint8_t* vb = stg[s].v;
+          // ---- scores of tokens r0 and r1 (mma rows g, g + 8) for heads 2 tq, 2 tq + 1
+          const int r0 = wrow + g, r1 = r0 + 8;
+          float sc[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            const uint32_t kw0 = *reinterpret_cast<const uint32_t*>(stg[s].ks + 4 * r0);
+            const uint32_t kw1 = *reinterpret_cast<const uint32_t*>(stg[s].ks + 4 * r1);
+  #pragma unroll
             for (int bb = 0; bb < 4; ++bb) {
-              const uint32_t w = *reinterpret_cast<const uint32_t*>(vb + swz(r, 32 * bb + 4 * g));
-              const float f = ue8m0_value((swd >> (8 * bb)) & 0xFFu);
-              const float2 lo = e4m3x2_to_float2(w), hi = e4m3x2_to_float2(w >> 16);
-              const float vv[4] = {lo.x * f, lo.y * f, hi.x * f, hi.y * f};
-#pragma unroll
+              const uint2 x0 = *reinterpret_cast<const uint2*>(kb + swz(r0, 32 * bb + 8 * tq));
+              const uint2 x1 = *reinterpret_cast<const uint2*>(kb + swz(r1, 32 * bb + 8 * tq));
+              const uint4 bq = qfrag[qb][bb][lane];
+              float d[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_16816(d, e4m3_lo_f16x2(x0.x), e4m3_lo_f16x2(x1.x), e4m3_hi_f16x2(x0.x), e4m3_hi_f16x2(x1.x), bq.x,
+                        bq.y);
+              mma_16816(d, e4m3_lo_f16x2(x0.y), e4m3_lo_f16x2(x1.y), e4m3_hi_f16x2(x0.y), e4m3_hi_f16x2(x1.y), bq.z,
+                        bq.w);
+              const float f0 = ue8m0_value((kw0 >> (8 * bb)) & 0xFFu), f1 = ue8m0_value((kw1 >> (8 * bb)) & 0xFFu);
+              sc[0] = fmaf(f0, d[0], sc[0]);
+              sc[1] = fmaf(f0, d[1], sc[1]);
+              sc[2] = fmaf(f1, d[2], sc[2]);
+              sc[3] = fmaf(f1, d[3], sc[3]);
+            }
+          }
+          // ---- the warp's online softmax over its 16 tokens, per head
+          const bool v0 = r0 < tmax, v1 = r1 < tmax;
+          float al[2];
+  #pragma unroll
+          for (int i2 = 0; i2 < 2; ++i2) {
+            const int hh = 2 * tq + i2;
+            const bool hv = hh < G;
+            const float x0 = (v0 && hv) ? sc[i2] * hs[i2] : -INFINITY;
+            const float x1 = (v1 && hv) ? sc[2 + i2] * hs[i2] : -INFINITY;
+            float cm = fmaxf(x0, x1);
+            cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 4));
+            cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 8));
+            cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 16));
+            const float mn = fmaxf(m_run[i2], cm);
+            // no valid token yet: mn = -inf and nothing is added
+            al[i2] = mn == -INFINITY ? 1.f : exp2f(m_run[i2] - mn);
+            const float p0 = x0 == -INFINITY ? 0.f : exp2f(x0 - mn);
+            const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - mn);
+            m_run[i2] = mn;
+            l_part[i2] = fmaf(l_part[i2], al[i2], p0 + p1);
+            pw[hh * kPwLd + g] = p0;
+            pw[hh * kPwLd + g + 8] = p1;
+          }
+          if (al[0] != 1.f || al[1] != 1.f) {
+  #pragma unroll
+            for (int bb = 0; bb < 4; ++bb)
+  #pragma unroll
               for (int tt = 0; tt < 2; ++tt) {
-                O[bb][tt][0] = fmaf(q0, vv[2 * tt], O[bb][tt][0]);
-                O[bb][tt][1] = fmaf(q1, vv[2 * tt], O[bb][tt][1]);
-                O[bb][tt][2] = fmaf(q0, vv[2 * tt + 1], O[bb][tt][2]);
-                O[bb][tt][3] = fmaf(q1, vv[2 * tt + 1], O[bb][tt][3]);
+                O[bb][tt][0] *= al[0];
+                O[bb][tt][1] *= al[1];
+                O[bb][tt][2] *= al[0];
+                O[bb][tt][3] *= al[1];
+              }
+          }
+          __syncwarp();  // pw is written before the lanes read it
+          if (t == 0 && seq < 10) ATTN_STAMP(6 + 4 * seq);
+
+          // ---- p . v: A = V^T (rows: dimensions, k: tokens rv, rv + 1, rv + 8,
+          // rv + 9 of the lane), B = p of head g
+          const int rv = wrow + 2 * tq;
+          const int rvk[4] = {rv, rv + 1, rv + 8, rv + 9};
+          const AttnPrep& pr = prep[s];
+          const bool far = (m.flags & kMetaFar) != 0;
+          if (!far) {
+            uint32_t bh0, bh1, bl0, bl1;
+            split_f16x2(*reinterpret_cast<const float2*>(pw + g * kPwLd + 2 * tq), bh0, bl0);
+            split_f16x2(*reinterpret_cast<const float2*>(pw + g * kPwLd + 2 * tq + 8), bh1, bl1);
+            const bool full16 = wrow + 16 <= tmax;
+            const uint32_t k01 = (rvk[0] < tmax ? 0x0000FFFFu : 0u) | (rvk[1] < tmax ? 0xFFFF0000u : 0u);
+            const uint32_t k89 = (rvk[2] < tmax ? 0x0000FFFFu : 0u) | (rvk[3] < tmax ? 0xFFFF0000u : 0u);
+            const uint4 vm01 = pr.vm[4 * warp + tq][0], vm89 = pr.vm[4 * warp + tq][1];
+            const uint32_t smax = pr.smax[warp];
+            const uint32_t m01s[4] = {vm01.x, vm01.y, vm01.z, vm01.w}, m89s[4] = {vm89.x, vm89.y, vm89.z, vm89.w};
+  
+  #pragma unroll
+            for (int bb = 0; bb < 4; ++bb) {
+              const int off = 32 * bb + 4 * g;
+              const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vb + swz(rvk[0], off));
+              const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vb + swz(rvk[1], off));
+              const uint32_t w8 = *reinterpret_cast<const uint32_t*>(vb + swz(rvk[2], off));
+              const uint32_t w9 = *reinterpret_cast<const uint32_t*>(vb + swz(rvk[3], off));
+              const uint32_t m01 = m01s[bb], m89 = m89s[bb];
+              // dimension pairs (d, d + 1) and (d + 2, d + 3) of the token pairs
+              const uint32_t x01 = prmt(w0, w1, 0x5140u), y01 = prmt(w0, w1, 0x7362u);
+              const uint32_t x89 = prmt(w8, w9, 0x5140u), y89 = prmt(w8, w9, 0x7362u);
+              uint32_t A0[4] = {hmul2(e4m3_lo_f16x2(x01), m01), hmul2(e4m3_hi_f16x2(x01), m01),
+                                hmul2(e4m3_lo_f16x2(x89), m89), hmul2(e4m3_hi_f16x2(x89), m89)};
+              uint32_t A1[4] = {hmul2(e4m3_lo_f16x2(y01), m01), hmul2(e4m3_hi_f16x2(y01), m01),
+                                hmul2(e4m3_lo_f16x2(y89), m89), hmul2(e4m3_hi_f16x2(y89), m89)};
+              if (!full16) {  // tokens past the sequence: their stale codes may not be finite
+                A0[0] &= k01;
+                A0[1] &= k01;
+                A0[2] &= k89;
+                A0[3] &= k89;
+                A1[0] &= k01;
+                A1[1] &= k01;
+                A1[2] &= k89;
+                A1[3] &= k89;
+              }
+              float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_16816(d0, A0[0], A0[1], A0[2], A0[3], bh0, bh1);
+              mma_16816(d0, A0[0], A0[1], A0[2], A0[3], bl0, bl1);
+              mma_16816(d1, A1[0], A1[1], A1[2], A1[3], bh0, bh1);
+              mma_16816(d1, A1[0], A1[1], A1[2], A1[3], bl0, bl1);
+              const float rf = ue8m0_value((smax >> (8 * bb)) & 0xFFu);
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                O[bb][0][e] = fmaf(rf, d0[e], O[bb][0][e]);
+                O[bb][1][e] = fmaf(rf, d1[e], O[bb][1][e]);
+              }
+            }
+          } else {
+            // fp32 FMAs: each lane its 16 dimensions x 2 heads over the 16 tokens
+  #pragma unroll 1
+            for (int kk = 0; kk < 16; ++kk) {
+              const int r = wrow + kk;
+              if (r >= tmax) break;
+              const float q0 = pw[(2 * tq) * kPwLd + kk], q1 = pw[(2 * tq + 1) * kPwLd + kk];
+              const uint32_t swd = *reinterpret_cast<const uint32_t*>(stg[s].vs + 4 * r);
+  #pragma unroll
+              for (int bb = 0; bb < 4; ++bb) {
+                const uint32_t vw = *reinterpret_cast<const uint32_t*>(vb + swz(r, 32 * bb + 4 * g));
+                const float f = ue8m0_value((swd >> (8 * bb)) & 0xFFu);
+                const float2 lo = e4m3x2_to_float2(vw), hi = e4m3x2_to_float2(vw >> 16);
+                const float vv[4] = {lo.x * f, lo.y * f, hi.x * f, hi.y * f};
+  #pragma unroll
+                for (int tt = 0; tt < 2; ++tt) {
+                  O[bb][tt][0] = fmaf(q0, vv[2 * tt], O[bb][tt][0]);
+                  O[bb][tt][1] = fmaf(q1, vv[2 * tt], O[bb][tt][1]);
+                  O[bb][tt][2] = fmaf(q0, vv[2 * tt + 1], O[bb][tt][2]);
+                  O[bb][tt][3] = fmaf(q1, vv[2 * tt + 1], O[bb][tt][3]);
+                }
               }
             }
           }
         }
+      if (!(m.flags & kMetaLast)) {
+        __syncwarp();  // the warp is done with the stage (and pw) before it releases it
+        if (t == 0 && seq < 10) ATTN_STAMP(7 + 4 * seq);
+        if (lane == 0) mbar_arrive(&empty[s]);
+        continue;
       }
-      __syncwarp();  // the warp is done with the stage (and pw) before it releases it
-      if (lane == 0) mbar_arrive(&empty[s]);
-    }
+      // ---- the item's end: merge the warps' states in its last chunk's
+      // stage (the item's max, sum and unnormalised output per head, one
+      // record each); the stage is released afterwards
+      float l_sum[2];
 #pragma unroll
-    for (int i2 = 0; i2 < 2; ++i2) {
-      l_part[i2] += __shfl_xor_sync(0xFFFFFFFFu, l_part[i2], 4);
-      l_part[i2] += __shfl_xor_sync(0xFFFFFFFFu, l_part[i2], 8);
-      l_part[i2] += __shfl_xor_sync(0xFFFFFFFFu, l_part[i2], 16);
-    }
-  }
-  __syncthreads();  // every warp is done with the ring and every copy has landed
-
-  if (t == 0) {
-    ATTN_STAMP(1);
-    if (a.trace != nullptr) a.trace[((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * 64 + 2] = c1 - c0;
-  }
-  // ---- merge the warps' states: the block's max, sum and unnormalised
-  // output per head, one record each
-  float* wacc = reinterpret_cast<float*>(stg);  // reuse the ring: [kCWarps][G][D]
-  if (warp < kCWarps) {
+      for (int i2 = 0; i2 < 2; ++i2) {
+        l_sum[i2] = l_part[i2];
+        l_sum[i2] += __shfl_xor_sync(0xFFFFFFFFu, l_sum[i2], 4);
+        l_sum[i2] += __shfl_xor_sync(0xFFFFFFFFu, l_sum[i2], 8);
+        l_sum[i2] += __shfl_xor_sync(0xFFFFFFFFu, l_sum[i2], 16);
+      }
+      const uint32_t mpar = static_cast<uint32_t>(kq) & 1u;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mrg[0]);
+      if (!wait_phase(&mrg[0], mpar, a.timeout_ns)) {  // every warp is done with the stage
+        if (lane == 0) attn_error(a, 5u, 6u);  // FSOPS_ERR_TIMEOUT
+        break;
+      }
+      float* wacc = reinterpret_cast<float*>(&stg[s]);  // [kCWarps][G][D]
 #pragma unroll
-    for (int i2 = 0; i2 < 2; ++i2) {
-      const int hh = 2 * tq + i2;
-      if (hh < G) {
+      for (int i2 = 0; i2 < 2; ++i2) {
+        const int hh = 2 * tq + i2;
+        if (hh < G) {
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb)
-          *reinterpret_cast<float4*>(wacc + (warp * G + hh) * kD + 32 * bb + 4 * g) =
-              make_float4(O[bb][0][i2], O[bb][0][2 + i2], O[bb][1][i2], O[bb][1][2 + i2]);
-        if (g == 0) {
-          red_max[warp * G + hh] = m_run[i2];
-          red_sum[warp * G + hh] = l_part[i2];
+          for (int bb = 0; bb < 4; ++bb)
+            *reinterpret_cast<float4*>(wacc + (warp * G + hh) * kD + 32 * bb + 4 * g) =
+                make_float4(O[bb][0][i2], O[bb][0][2 + i2], O[bb][1][i2], O[bb][1][2 + i2]);
+          if (g == 0) {
+            red_max[warp * G + hh] = m_run[i2];
+            red_sum[warp * G + hh] = l_sum[i2];
+          }
         }
       }
-    }
-  }
-  __syncthreads();
-  for (int i = t; i < G * kD; i += kAThreads) {
-    const int hh = i / kD, d = i % kD;
-    float M = red_max[hh];
-#pragma unroll
-    for (int w = 1; w < kCWarps; ++w) M = fmaxf(M, red_max[w * G + hh]);
-    float o = 0.f, l = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kCWarps; ++w) {
-        const float mw = red_max[w * G + hh];
-        if (mw == -INFINITY) continue;
-        const float f = expf(mw - M);
-        o = fmaf(f, wacc[(w * G + hh) * kD + d], o);
-        l = fmaf(f, red_sum[w * G + hh], l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mrg[1]);
+      if (!wait_phase(&mrg[1], mpar, a.timeout_ns)) {
+        if (lane == 0) attn_error(a, 5u, 6u);  // FSOPS_ERR_TIMEOUT
+        break;
       }
+      for (int i = t; i < G * kD; i += 32 * kCWarps) {
+        const int hh = i / kD, d = i % kD;
+        float M = red_max[hh];
+#pragma unroll
+        for (int w2 = 1; w2 < kCWarps; ++w2) M = fmaxf(M, red_max[w2 * G + hh]);
+        float o = 0.f, l = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w2 = 0; w2 < kCWarps; ++w2) {
+            const float mw = red_max[w2 * G + hh];
+            if (mw == -INFINITY) continue;
+            const float f = exp2f(mw - M);
+            o = fmaf(f, wacc[(w2 * G + hh) * kD + d], o);
+            l = fmaf(f, red_sum[w2 * G + hh], l);
+          }
+        }
+        float* rec = a.part + ((static_cast<size_t>(m.b) * a.Hq + m.hk * G + hh) * a.nsplit + m.split) * (2 + kD);
+        rec[2 + d] = o;
+        if (d == 0) {
+          rec[0] = M;
+          rec[1] = l;
+        }
+      }
+      __syncwarp();  // the warp is done with wacc and with this item's q
+      if (lane == 0) {
+        mbar_arrive(&empty[s]);
+        mbar_arrive(&qfree[qb]);
+      }
+      ++kq;
     }
-    float* rec = a.part + ((static_cast<size_t>(b) * a.Hq + hk * G + hh) * a.nsplit + split) * (2 + kD);
-    rec[2 + d] = o;
-    if (d == 0) {
-      rec[0] = M;
-      rec[1] = l;
-    }
+    if (t == 0) ATTN_STAMP(1);
   }
 }
 
@@ -535,18 +734,25 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
 __global__ void __launch_bounds__(kD) attn_combine_kernel(const __grid_constant__ AttnArgs a) {
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
   const float* rec = a.part + (static_cast<size_t>(b) * a.Hq + h) * a.nsplit * (2 + kD);
+  // the splits that hold chunks of the sequence (only those wrote a record)
+  const int len = a.seq_lens[b];
+  const int n = (len >= 1 && len <= a.max_pages * a.P) ? len : 0;
+  const int per = (a.max_pages * a.P + kC * a.nsplit - 1) / (kC * a.nsplit);
+  const int ns = min(a.nsplit, ((n + kC - 1) / kC + per - 1) / per);
   float M = -INFINITY;
-  for (int s = 0; s < a.nsplit; ++s) M = fmaxf(M, rec[s * (2 + kD)]);
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, rec[s * (2 + kD)]);
   float num = 0.f, den = 0.f;
   if (M != -INFINITY) {
-    for (int s = 0; s < a.nsplit; ++s) {
+    for (int s = 0; s < ns; ++s) {
       const float m = rec[s * (2 + kD)];
       if (m == -INFINITY) continue;
-      const float w = expf(m - M);
+      const float w = exp2f(m - M);
       num = fmaf(w, rec[s * (2 + kD) + 2 + d], num);
       den = fmaf(w, rec[s * (2 + kD) + 1], den);
     }
   }
+  // the decode launch has finished: its work counter starts the next call at zero
+  if (h == 0 && b == 0 && d == 0) *a.work = 0u;
   const float o = den > 0.f ? num / den : 0.f;
   const __nv_bfloat16 ob = __float2bfloat16_rn(o);
   a.out[(static_cast<size_t>(b) * a.Hq + h) * kD + d] = *reinterpret_cast<const uint16_t*>(&ob);
@@ -558,7 +764,7 @@ cudaError_t launch_group(const AttnArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kAttnSmem));
   if (e != cudaSuccess) return e;
-  paged_decode_kernel<G><<<dim3(a.nsplit, a.Hkv, a.B), kAThreads, kAttnSmem, stream>>>(a);
+  paged_decode_kernel<G><<<a.grid, kAThreads, kAttnSmem, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_combine_kernel<<<dim3(a.Hq, a.B), kD, 0, stream>>>(a);
@@ -579,6 +785,11 @@ int attn_splits(int B, int Hkv, int max_pages, int P, int sms, int chunks_per_bl
   if ((max_chunks + per - 1) / per < want) per = (max_chunks + want - 1) / want;
   if (per < 1) per = 1;
   return (max_chunks + per - 1) / per;
+}
+
+int attn_grid(int items, int sms) {
+  const int resident = 2 * sms;  // the ring's shared memory lets two blocks share an SM
+  return items < resident ? items : resident;
 }
 
 cudaError_t launch_paged_decode(const AttnArgs& a, cudaStream_t stream) {
