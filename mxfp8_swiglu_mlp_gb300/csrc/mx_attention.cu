@@ -68,11 +68,12 @@ struct __align__(1024) AttnStage {
   uint8_t vs[kScaleBytes];
 };
 static_assert(sizeof(AttnStage) % 1024 == 0, "stages stay 1024-byte aligned");
-// What the producer derives from a chunk's V scales once, for the consumer
+// What the scale warp derives from a chunk's V scales once, for the consumer
 // lanes (warp w, column pair tq) that share tokens rv = 16 w + 2 tq +
 // {0, 1, 8, 9}: per 32-dimension block bb the f16x2 multipliers 2^(s - s_max)
 // of the token pairs (rv, rv + 1) and (rv + 8, rv + 9), s_max the block's
-// largest scale among the warp's 16 tokens (byte bb of smax[w]).
+// largest scale among warp w's tokens of the item so far (byte bb of
+// smax[w]; it only grows within an item).
 struct AttnPrep {
   uint4 vm[kCWarps * 4][2];
   uint32_t smax[kCWarps];
@@ -100,6 +101,13 @@ __device__ __forceinline__ uint32_t e4m3_hi_f16x2(uint32_t w) {
 __device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// 2^x (the special-function unit's approximation, relative error below
+// 2^-22; results below 2^-126 flush to 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
@@ -130,6 +138,12 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
 // 2^(s - 127) for a UE8M0 byte s (s = 0 is the subnormal 2^-127).
 __device__ __forceinline__ float ue8m0_value(uint32_t s) {
   return s != 0 ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
+}
+// 2^(s - 127) for byte bb of a word of UE8M0 scales, with s = 0 read as 0
+// (a block whose scale is 2^-127 holds values below 2^-118)
+template <int bb>
+__device__ __forceinline__ float ue8m0_byte(uint32_t w) {
+  return __uint_as_float((bb < 3 ? (w << (23 - 8 * bb)) : (w >> 1)) & 0x7F800000u);
 }
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 // p as the f16 pair hi + lo: hi keeps p's upper 11 significant bits (exact in
@@ -288,7 +302,7 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
     // issue cursor: chunk c of item cur (item nxt grabbed one ahead); lane i
     // holds page id pid of the chunk's page i (loaded one issue ahead)
     AttnItem cur{}, nxt{};
-    bool have_cur = false, have_nxt = false;
+    bool have_cur = false, have_nxt = false, nxt_taken = false;
     int c = 0;
     int pid = -1, np = 0;
     auto load_pids = [&]() {
@@ -330,11 +344,16 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
         bulk_load(stg[s].ks + lane * sb, a.k_scales + static_cast<size_t>(y) * (kD / 32), sb, &full[s], pol);
         bulk_load(stg[s].vs + lane * sb, a.v_scales + static_cast<size_t>(y) * (kD / 32), sb, &full[s], pol);
       }
+      // the next item is taken once its predecessor's first chunk is on its way
+      if (!nxt_taken) {
+        have_nxt = grab(nxt);
+        nxt_taken = true;
+      }
       if (++c >= cur.c1) {
         have_cur = have_nxt;
         cur = nxt;
         c = cur.c0;
-        if (have_cur) have_nxt = grab(nxt);
+        nxt_taken = false;
       }
       if (have_cur) load_pids();
     };
@@ -379,7 +398,8 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
       if (tq == 0) qscale[qb][g] = ldexpf(a.sm_scale * 1.4426950408889634f, -e);
     };
     // the V-scale multipliers of the chunk in stage s, lane 4 w + tq those of
-    // consumer warp w's column pair tq
+    // consumer warp w's column pair tq; rref is warp w's running maximum
+    uint32_t rref = 0;
     auto prepare = [&](int s) {
       const int pwp = lane >> 2, ptq = lane & 3;
       const int tmax = min(kC, meta[s].n - meta[s].c * kC);
@@ -396,6 +416,9 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
       }
       mref = __vmaxu4(mref, __shfl_xor_sync(0xFFFFFFFFu, mref, 1));
       mref = __vmaxu4(mref, __shfl_xor_sync(0xFFFFFFFFu, mref, 2));
+      if (meta[s].flags & kMetaFirst) rref = 0;
+      mref = __vmaxu4(mref, rref);
+      rref = mref;
       bool far = false;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -422,10 +445,7 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
       // (only this warp takes work from the counter)
       have_cur = grab(cur);
       c = cur.c0;
-      if (have_cur) {
-        have_nxt = grab(nxt);
-        load_pids();
-      }
+      if (have_cur) load_pids();
       int issued = 0;
       for (int q = 0; !ended; ++q) {
         const int s = q % kAStages;
@@ -473,16 +493,20 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
     }
   } else {
     // ---- consumer warp: tokens 16 warp .. 16 warp + 15 of every chunk.
-    // Its state: the p . v sums O^T[d][head] of the warp's tokens (blocks of
-    // 32 dimensions bb, two 16-row tiles each: rows g and g + 8 are
-    // dimensions 32 bb + 4 g + {0, 1} of tile 0 and + {2, 3} of tile 1;
-    // columns heads 2 tq and 2 tq + 1), and the running max and partial sums
-    // of the lane's two heads.
+    // Its state: the p . v sums O^T[d][head] of the warp's tokens in eight
+    // 16-row tiles T (rows g and g + 8 are dimensions 16 g + 2 T and
+    // 16 g + 2 T + 1, so a lane's 16 dimensions lie in one 32-dimension V
+    // scale block, g / 2; columns heads 2 tq and 2 tq + 1) in units of
+    // 2^(ref_e - 127), ref_e that block's running largest scale among the
+    // warp's tokens; and the running max and partial sums of the lane's two
+    // heads.
     const int wrow = 16 * warp;
     float* pw = pws + warp * 8 * kPwLd;
     int kq = 0, qb = 0;
-    float O[4][2][4];
+    const int vbb = g >> 1;  // the lane's V scale block
+    float O[8][4];
     float m_run[2], l_part[2];
+    int ref_e = 0;
     float hs[2] = {0.f, 0.f};  // sm_scale log2(e) / 2^e of heads 2 tq and 2 tq + 1
     for (int seq = 0;; ++seq) {
       const int s = seq % kAStages;
@@ -497,13 +521,12 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
       if (m.flags & kMetaEnd) break;
       if (m.flags & kMetaFirst) {
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb)
+        for (int tt = 0; tt < 8; ++tt)
 #pragma unroll
-          for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) O[bb][tt][e] = 0.f;
+          for (int e = 0; e < 4; ++e) O[tt][e] = 0.f;
         m_run[0] = m_run[1] = -INFINITY;
         l_part[0] = l_part[1] = 0.f;
+        ref_e = 0;  // the item's running scale maximum starts below any chunk's
         qb = kq & 1;
         hs[0] = qscale[qb][2 * tq];
         hs[1] = qscale[qb][2 * tq + 1];
@@ -518,7 +541,7 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
           {
             const uint32_t kw0 = *reinterpret_cast<const uint32_t*>(stg[s].ks + 4 * r0);
             const uint32_t kw1 = *reinterpret_cast<const uint32_t*>(stg[s].ks + 4 * r1);
-  #pragma unroll
+#pragma unroll
             for (int bb = 0; bb < 4; ++bb) {
               const uint2 x0 = *reinterpret_cast<const uint2*>(kb + swz(r0, 32 * bb + 8 * tq));
               const uint2 x1 = *reinterpret_cast<const uint2*>(kb + swz(r1, 32 * bb + 8 * tq));
@@ -528,124 +551,136 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
                         bq.y);
               mma_16816(d, e4m3_lo_f16x2(x0.y), e4m3_lo_f16x2(x1.y), e4m3_hi_f16x2(x0.y), e4m3_hi_f16x2(x1.y), bq.z,
                         bq.w);
-              const float f0 = ue8m0_value((kw0 >> (8 * bb)) & 0xFFu), f1 = ue8m0_value((kw1 >> (8 * bb)) & 0xFFu);
+              const float f0 = bb == 0   ? ue8m0_byte<0>(kw0)
+                             : bb == 1 ? ue8m0_byte<1>(kw0)
+                             : bb == 2 ? ue8m0_byte<2>(kw0)
+                                       : ue8m0_byte<3>(kw0);
+            const float f1 = bb == 0   ? ue8m0_byte<0>(kw1)
+                             : bb == 1 ? ue8m0_byte<1>(kw1)
+                             : bb == 2 ? ue8m0_byte<2>(kw1)
+                                       : ue8m0_byte<3>(kw1);
               sc[0] = fmaf(f0, d[0], sc[0]);
               sc[1] = fmaf(f0, d[1], sc[1]);
               sc[2] = fmaf(f1, d[2], sc[2]);
               sc[3] = fmaf(f1, d[3], sc[3]);
             }
           }
-          // ---- the warp's online softmax over its 16 tokens, per head
+          // ---- the warp's online softmax over its 16 tokens, per head (the
+          // running max is only reduced again when some score exceeds it)
           const bool v0 = r0 < tmax, v1 = r1 < tmax;
-          float al[2];
-  #pragma unroll
+          float x[2][2];
+          bool grow = false;
+#pragma unroll
+          for (int i2 = 0; i2 < 2; ++i2) {
+            const bool hv = 2 * tq + i2 < G;
+            x[i2][0] = (v0 && hv) ? sc[i2] * hs[i2] : -INFINITY;
+            x[i2][1] = (v1 && hv) ? sc[2 + i2] * hs[i2] : -INFINITY;
+            grow |= fmaxf(x[i2][0], x[i2][1]) > m_run[i2];
+          }
+          float al[2] = {1.f, 1.f};
+          if (__any_sync(0xFFFFFFFFu, grow)) {
+#pragma unroll
+            for (int i2 = 0; i2 < 2; ++i2) {
+              float cm = fmaxf(x[i2][0], x[i2][1]);
+              cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 4));
+              cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 8));
+              cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 16));
+              const float mn = fmaxf(m_run[i2], cm);
+              // no valid token yet: mn = -inf and nothing is added
+              al[i2] = mn == -INFINITY ? 1.f : ex2_approx(m_run[i2] - mn);
+              m_run[i2] = mn;
+            }
+            if (al[0] != 1.f || al[1] != 1.f) {
+#pragma unroll
+              for (int tt = 0; tt < 8; ++tt) {
+                O[tt][0] *= al[0];
+                O[tt][1] *= al[1];
+                O[tt][2] *= al[0];
+                O[tt][3] *= al[1];
+              }
+            }
+          }
+#pragma unroll
           for (int i2 = 0; i2 < 2; ++i2) {
             const int hh = 2 * tq + i2;
-            const bool hv = hh < G;
-            const float x0 = (v0 && hv) ? sc[i2] * hs[i2] : -INFINITY;
-            const float x1 = (v1 && hv) ? sc[2 + i2] * hs[i2] : -INFINITY;
-            float cm = fmaxf(x0, x1);
-            cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 4));
-            cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 8));
-            cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 16));
-            const float mn = fmaxf(m_run[i2], cm);
-            // no valid token yet: mn = -inf and nothing is added
-            al[i2] = mn == -INFINITY ? 1.f : exp2f(m_run[i2] - mn);
-            const float p0 = x0 == -INFINITY ? 0.f : exp2f(x0 - mn);
-            const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - mn);
-            m_run[i2] = mn;
+            const float ms = m_run[i2] == -INFINITY ? 0.f : m_run[i2];
+            const float p0 = ex2_approx(x[i2][0] - ms), p1 = ex2_approx(x[i2][1] - ms);  // 0 for -inf
             l_part[i2] = fmaf(l_part[i2], al[i2], p0 + p1);
             pw[hh * kPwLd + g] = p0;
             pw[hh * kPwLd + g + 8] = p1;
-          }
-          if (al[0] != 1.f || al[1] != 1.f) {
-  #pragma unroll
-            for (int bb = 0; bb < 4; ++bb)
-  #pragma unroll
-              for (int tt = 0; tt < 2; ++tt) {
-                O[bb][tt][0] *= al[0];
-                O[bb][tt][1] *= al[1];
-                O[bb][tt][2] *= al[0];
-                O[bb][tt][3] *= al[1];
-              }
           }
           __syncwarp();  // pw is written before the lanes read it
           if (t == 0 && seq < 10) ATTN_STAMP(6 + 4 * seq);
 
           // ---- p . v: A = V^T (rows: dimensions, k: tokens rv, rv + 1, rv + 8,
-          // rv + 9 of the lane), B = p of head g
+          // rv + 9 of the lane), B = p of head g; the sums stay in units of
+          // 2^(ref_e - 127), ref_e the running largest scale of block vbb
           const int rv = wrow + 2 * tq;
           const int rvk[4] = {rv, rv + 1, rv + 8, rv + 9};
           const AttnPrep& pr = prep[s];
-          const bool far = (m.flags & kMetaFar) != 0;
-          if (!far) {
+          {
+            const int ne = static_cast<int>((pr.smax[warp] >> (8 * vbb)) & 0xFFu);
+            if (ne != ref_e) {
+              const float f = __uint_as_float(static_cast<uint32_t>(max(127 + ref_e - ne, 0)) << 23);
+#pragma unroll
+              for (int tt = 0; tt < 8; ++tt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) O[tt][e] *= f;
+              ref_e = ne;
+            }
+          }
+          uint4 W[4];  // the lane's 16 dimensions of its four tokens
+#pragma unroll
+          for (int k = 0; k < 4; ++k) W[k] = *reinterpret_cast<const uint4*>(vb + swz(rvk[k], 16 * g));
+          if ((m.flags & kMetaFar) == 0) {
             uint32_t bh0, bh1, bl0, bl1;
             split_f16x2(*reinterpret_cast<const float2*>(pw + g * kPwLd + 2 * tq), bh0, bl0);
             split_f16x2(*reinterpret_cast<const float2*>(pw + g * kPwLd + 2 * tq + 8), bh1, bl1);
             const bool full16 = wrow + 16 <= tmax;
             const uint32_t k01 = (rvk[0] < tmax ? 0x0000FFFFu : 0u) | (rvk[1] < tmax ? 0xFFFF0000u : 0u);
             const uint32_t k89 = (rvk[2] < tmax ? 0x0000FFFFu : 0u) | (rvk[3] < tmax ? 0xFFFF0000u : 0u);
-            const uint4 vm01 = pr.vm[4 * warp + tq][0], vm89 = pr.vm[4 * warp + tq][1];
-            const uint32_t smax = pr.smax[warp];
-            const uint32_t m01s[4] = {vm01.x, vm01.y, vm01.z, vm01.w}, m89s[4] = {vm89.x, vm89.y, vm89.z, vm89.w};
-  
-  #pragma unroll
-            for (int bb = 0; bb < 4; ++bb) {
-              const int off = 32 * bb + 4 * g;
-              const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vb + swz(rvk[0], off));
-              const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vb + swz(rvk[1], off));
-              const uint32_t w8 = *reinterpret_cast<const uint32_t*>(vb + swz(rvk[2], off));
-              const uint32_t w9 = *reinterpret_cast<const uint32_t*>(vb + swz(rvk[3], off));
-              const uint32_t m01 = m01s[bb], m89 = m89s[bb];
-              // dimension pairs (d, d + 1) and (d + 2, d + 3) of the token pairs
-              const uint32_t x01 = prmt(w0, w1, 0x5140u), y01 = prmt(w0, w1, 0x7362u);
-              const uint32_t x89 = prmt(w8, w9, 0x5140u), y89 = prmt(w8, w9, 0x7362u);
-              uint32_t A0[4] = {hmul2(e4m3_lo_f16x2(x01), m01), hmul2(e4m3_hi_f16x2(x01), m01),
-                                hmul2(e4m3_lo_f16x2(x89), m89), hmul2(e4m3_hi_f16x2(x89), m89)};
-              uint32_t A1[4] = {hmul2(e4m3_lo_f16x2(y01), m01), hmul2(e4m3_hi_f16x2(y01), m01),
-                                hmul2(e4m3_lo_f16x2(y89), m89), hmul2(e4m3_hi_f16x2(y89), m89)};
+            // f16x2 2^(s - ref) of the token pairs (rv, rv + 1) and (rv + 8, rv + 9)
+            const uint32_t m01 = reinterpret_cast<const uint32_t*>(&pr.vm[4 * warp + tq][0])[vbb];
+            const uint32_t m89 = reinterpret_cast<const uint32_t*>(&pr.vm[4 * warp + tq][1])[vbb];
+            const uint32_t w0[4] = {W[0].x, W[0].y, W[0].z, W[0].w}, w1[4] = {W[1].x, W[1].y, W[1].z, W[1].w};
+            const uint32_t w8[4] = {W[2].x, W[2].y, W[2].z, W[2].w}, w9[4] = {W[3].x, W[3].y, W[3].z, W[3].w};
+#pragma unroll
+            for (int tt = 0; tt < 8; ++tt) {
+              // dimensions 16 g + 2 tt and + 1 of the token pairs
+              const uint32_t sel = (tt & 1) ? 0x7362u : 0x5140u;
+              const uint32_t x01 = prmt(w0[tt >> 1], w1[tt >> 1], sel), x89 = prmt(w8[tt >> 1], w9[tt >> 1], sel);
+              uint32_t A[4] = {hmul2(e4m3_lo_f16x2(x01), m01), hmul2(e4m3_hi_f16x2(x01), m01),
+                               hmul2(e4m3_lo_f16x2(x89), m89), hmul2(e4m3_hi_f16x2(x89), m89)};
               if (!full16) {  // tokens past the sequence: their stale codes may not be finite
-                A0[0] &= k01;
-                A0[1] &= k01;
-                A0[2] &= k89;
-                A0[3] &= k89;
-                A1[0] &= k01;
-                A1[1] &= k01;
-                A1[2] &= k89;
-                A1[3] &= k89;
+                A[0] &= k01;
+                A[1] &= k01;
+                A[2] &= k89;
+                A[3] &= k89;
               }
-              float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_16816(d0, A0[0], A0[1], A0[2], A0[3], bh0, bh1);
-              mma_16816(d0, A0[0], A0[1], A0[2], A0[3], bl0, bl1);
-              mma_16816(d1, A1[0], A1[1], A1[2], A1[3], bh0, bh1);
-              mma_16816(d1, A1[0], A1[1], A1[2], A1[3], bl0, bl1);
-              const float rf = ue8m0_value((smax >> (8 * bb)) & 0xFFu);
-  #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                O[bb][0][e] = fmaf(rf, d0[e], O[bb][0][e]);
-                O[bb][1][e] = fmaf(rf, d1[e], O[bb][1][e]);
-              }
+              mma_16816(O[tt], A[0], A[1], A[2], A[3], bh0, bh1);
+              mma_16816(O[tt], A[0], A[1], A[2], A[3], bl0, bl1);
             }
           } else {
             // fp32 FMAs: each lane its 16 dimensions x 2 heads over the 16 tokens
-  #pragma unroll 1
+#pragma unroll 1
             for (int kk = 0; kk < 16; ++kk) {
               const int r = wrow + kk;
               if (r >= tmax) break;
               const float q0 = pw[(2 * tq) * kPwLd + kk], q1 = pw[(2 * tq + 1) * kPwLd + kk];
-              const uint32_t swd = *reinterpret_cast<const uint32_t*>(stg[s].vs + 4 * r);
-  #pragma unroll
-              for (int bb = 0; bb < 4; ++bb) {
-                const uint32_t vw = *reinterpret_cast<const uint32_t*>(vb + swz(r, 32 * bb + 4 * g));
-                const float f = ue8m0_value((swd >> (8 * bb)) & 0xFFu);
-                const float2 lo = e4m3x2_to_float2(vw), hi = e4m3x2_to_float2(vw >> 16);
+              const int se = static_cast<int>(stg[s].vs[4 * r + vbb]);
+              const float f = __uint_as_float(static_cast<uint32_t>(max(127 + se - ref_e, 0)) << 23);
+              const uint4 vw = *reinterpret_cast<const uint4*>(vb + swz(r, 16 * g));
+              const uint32_t vws[4] = {vw.x, vw.y, vw.z, vw.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float2 lo = e4m3x2_to_float2(vws[j]), hi = e4m3x2_to_float2(vws[j] >> 16);
                 const float vv[4] = {lo.x * f, lo.y * f, hi.x * f, hi.y * f};
-  #pragma unroll
-                for (int tt = 0; tt < 2; ++tt) {
-                  O[bb][tt][0] = fmaf(q0, vv[2 * tt], O[bb][tt][0]);
-                  O[bb][tt][1] = fmaf(q1, vv[2 * tt], O[bb][tt][1]);
-                  O[bb][tt][2] = fmaf(q0, vv[2 * tt + 1], O[bb][tt][2]);
-                  O[bb][tt][3] = fmaf(q1, vv[2 * tt + 1], O[bb][tt][3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  // dimension 16 g + 4 j + e: tile (4 j + e) / 2, row half e % 2
+                  float* o = O[2 * j + (e >> 1)] + 2 * (e & 1);
+                  o[0] = fmaf(q0, vv[e], o[0]);
+                  o[1] = fmaf(q1, vv[e], o[1]);
                 }
               }
             }
@@ -676,14 +711,16 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
         break;
       }
       float* wacc = reinterpret_cast<float*>(&stg[s]);  // [kCWarps][G][D]
+      const float unit = ue8m0_value(static_cast<uint32_t>(ref_e));  // the sums' unit 2^(ref_e - 127)
 #pragma unroll
       for (int i2 = 0; i2 < 2; ++i2) {
         const int hh = 2 * tq + i2;
         if (hh < G) {
 #pragma unroll
-          for (int bb = 0; bb < 4; ++bb)
-            *reinterpret_cast<float4*>(wacc + (warp * G + hh) * kD + 32 * bb + 4 * g) =
-                make_float4(O[bb][0][i2], O[bb][0][2 + i2], O[bb][1][i2], O[bb][1][2 + i2]);
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<float4*>(wacc + (warp * G + hh) * kD + 16 * g + 4 * j) =
+                make_float4(O[2 * j][i2] * unit, O[2 * j][2 + i2] * unit, O[2 * j + 1][i2] * unit,
+                            O[2 * j + 1][2 + i2] * unit);
           if (g == 0) {
             red_max[warp * G + hh] = m_run[i2];
             red_sum[warp * G + hh] = l_sum[i2];
