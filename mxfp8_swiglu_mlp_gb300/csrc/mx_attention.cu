@@ -58,7 +58,7 @@ constexpr int kD = kAttnHeadDim;
 constexpr int kC = kAttnChunk;
 constexpr uint32_t kCodeBytes = kC * kD;          // 16 KB of K (or V) codes per chunk
 constexpr uint32_t kScaleBytes = kC * kD / 32;    // 512 B of scales per chunk
-constexpr int kPwLd = 20;                         // row stride (floats) of a warp's p[head][token]
+constexpr int kPwLd = 16;                         // row stride (floats) of a warp's p[head][token]
 static_assert(kC == 16 * kCWarps, "a consumer warp owns 16 tokens of a chunk");
 
 struct __align__(1024) AttnStage {
@@ -214,6 +214,7 @@ enum : uint32_t {
 struct ChunkMeta {
   int b, hk, split, n, c;
   uint32_t flags;
+  int pid[kC / 16];  // the chunk's page ids (-1: not loaded)
 };
 
 // Persistent: each block takes work items from a counter shared by the grid
@@ -229,7 +230,8 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
   // each consumer warp's probabilities of its 16 tokens: [warp][head][token]
   __shared__ __align__(16) float pws[kCWarps * 8 * kPwLd];
   __shared__ float red_max[kCWarps * G], red_sum[kCWarps * G];
-  __shared__ __align__(8) uint64_t full[kAStages], ready[kAStages], empty[kAStages], qfree[2], mrg[2];
+  __shared__ __align__(8) uint64_t full[kAStages], posted[kAStages], ready[kAStages], empty[kAStages], qfree[2],
+      mrg[2];
   __shared__ AttnPrep prep[kAStages];
   __shared__ ChunkMeta meta[kAStages];
   // q of an item's group as the B operand of the score MMA (two buffers, by
@@ -245,6 +247,7 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
 #pragma unroll
     for (int s = 0; s < kAStages; ++s) {
       mbar_init(&full[s], 1);
+      mbar_init(&posted[s], 32);
       mbar_init(&ready[s], 32);
       mbar_init(&empty[s], kCWarps);
     }
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
     // warp, once a chunk has landed, derives its V-scale multipliers (and an
     // item's q fragments) and marks it ready.
     const int ppc = kC / a.P;
-    const uint32_t cb = static_cast<uint32_t>(a.P) * kD, sb = static_cast<uint32_t>(a.P) * (kD / 32);
+    const uint32_t cb = static_cast<uint32_t>(a.P) * kD;
     const uint64_t pol = l2_policy_evict_first();
     if (lane == 0) {
       tma_prefetch_desc(&a.tm_k);
@@ -317,6 +320,8 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
           meta[s].flags = kMetaEnd;
           mbar_arrive(&full[s]);
         }
+        __syncwarp();
+        mbar_arrive(&posted[s]);
         ended = true;
         return;
       }
@@ -334,16 +339,16 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
         meta[s].flags = (c == cur.c0 ? kMetaFirst : 0u) | (c + 1 == cur.c1 ? kMetaLast : 0u) |
                         (all_good ? kMetaOk : 0u);
       }
+      if (lane < kC / 16) meta[s].pid[lane] = (mine && good) ? pid : -1;
       fence_proxy_async_shared();  // the stage's earlier generic reads come before the copies' writes
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], npg * 2u * (cb + sb));
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], npg * 2u * cb);
       __syncwarp();
       if (mine && good) {
         const int y = (pid * a.Hkv + cur.hk) * a.P;  // first row of the (page, head) block
         tma_load_2d(stg[s].k + lane * cb, &a.tm_k, &full[s], 0, y, pol);
         tma_load_2d(stg[s].v + lane * cb, &a.tm_v, &full[s], 0, y, pol);
-        bulk_load(stg[s].ks + lane * sb, a.k_scales + static_cast<size_t>(y) * (kD / 32), sb, &full[s], pol);
-        bulk_load(stg[s].vs + lane * sb, a.v_scales + static_cast<size_t>(y) * (kD / 32), sb, &full[s], pol);
       }
+      mbar_arrive(&posted[s]);  // the chunk's meta is written: its scales may be fetched
       // the next item is taken once its predecessor's first chunk is on its way
       if (!nxt_taken) {
         have_nxt = grab(nxt);
@@ -465,17 +470,37 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
       int kq = 0;  // items begun
       for (int q = 0;; ++q) {
         const int s = q % kAStages;
-        if (!wait_phase(&full[s], static_cast<uint32_t>(q / kAStages) & 1u, a.timeout_ns)) {
+        const uint32_t par = static_cast<uint32_t>(q / kAStages) & 1u;
+        if (!wait_phase(&posted[s], par, a.timeout_ns)) {
+          if (lane == 0) attn_error(a, 5u, 3u);  // FSOPS_ERR_TIMEOUT
+          break;
+        }
+        // the chunk's K and V scales (tokens 4 lane .. 4 lane + 3, 16 bytes
+        // each), loaded while its codes are on the way
+        const uint32_t fl = meta[s].flags;
+        uint4 ksv = make_uint4(0u, 0u, 0u, 0u), vsv = ksv;
+        if (!(fl & kMetaEnd)) {
+          const int tok = 4 * lane;
+          const int id = meta[s].pid[tok / a.P];
+          if (id >= 0) {
+            const size_t row = (static_cast<size_t>(id) * a.Hkv + meta[s].hk) * a.P + tok % a.P;
+            ksv = *reinterpret_cast<const uint4*>(a.k_scales + row * (kD / 32));
+            vsv = *reinterpret_cast<const uint4*>(a.v_scales + row * (kD / 32));
+          }
+        }
+        if (!wait_phase(&full[s], par, a.timeout_ns)) {
           if (lane == 0) attn_error(a, 5u, 3u);  // FSOPS_ERR_TIMEOUT
           break;
         }
         if (lane == 0 && q < 10) ATTN_STAMP(44 + q);
-        const uint32_t fl = meta[s].flags;
         if (fl & kMetaEnd) {
           __syncwarp();
           mbar_arrive(&ready[s]);
           break;
         }
+        reinterpret_cast<uint4*>(stg[s].ks)[lane] = ksv;
+        reinterpret_cast<uint4*>(stg[s].vs)[lane] = vsv;
+        __syncwarp();
         if (fl & kMetaFirst) {
           // the buffer's previous item (two back) is done with it
           const int qb = kq & 1;
