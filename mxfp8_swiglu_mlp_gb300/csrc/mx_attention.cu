@@ -544,6 +544,7 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
       if (t == 0 && seq < 10) ATTN_STAMP(5 + 4 * seq);
       const ChunkMeta m = meta[s];
       if (m.flags & kMetaEnd) break;
+      bool released = false;  // the stage was released before the chunk's p . v
       if (m.flags & kMetaFirst) {
 #pragma unroll
         for (int tt = 0; tt < 8; ++tt)
@@ -658,15 +659,22 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
 #pragma unroll
           for (int k = 0; k < 4; ++k) W[k] = *reinterpret_cast<const uint4*>(vb + swz(rvk[k], 16 * g));
           if ((m.flags & kMetaFar) == 0) {
+            // f16x2 2^(s - ref) of the token pairs (rv, rv + 1) and (rv + 8, rv + 9)
+            const uint32_t m01 = reinterpret_cast<const uint32_t*>(&pr.vm[4 * warp + tq][0])[vbb];
+            const uint32_t m89 = reinterpret_cast<const uint32_t*>(&pr.vm[4 * warp + tq][1])[vbb];
+            if (!(m.flags & kMetaLast)) {
+              // everything the warp reads of the stage is in registers: release it now
+              __syncwarp();
+              if (t == 0 && seq < 10) ATTN_STAMP(7 + 4 * seq);
+              if (lane == 0) mbar_arrive(&empty[s]);
+              released = true;
+            }
             uint32_t bh0, bh1, bl0, bl1;
             split_f16x2(*reinterpret_cast<const float2*>(pw + g * kPwLd + 2 * tq), bh0, bl0);
             split_f16x2(*reinterpret_cast<const float2*>(pw + g * kPwLd + 2 * tq + 8), bh1, bl1);
             const bool full16 = wrow + 16 <= tmax;
             const uint32_t k01 = (rvk[0] < tmax ? 0x0000FFFFu : 0u) | (rvk[1] < tmax ? 0xFFFF0000u : 0u);
             const uint32_t k89 = (rvk[2] < tmax ? 0x0000FFFFu : 0u) | (rvk[3] < tmax ? 0xFFFF0000u : 0u);
-            // f16x2 2^(s - ref) of the token pairs (rv, rv + 1) and (rv + 8, rv + 9)
-            const uint32_t m01 = reinterpret_cast<const uint32_t*>(&pr.vm[4 * warp + tq][0])[vbb];
-            const uint32_t m89 = reinterpret_cast<const uint32_t*>(&pr.vm[4 * warp + tq][1])[vbb];
             const uint32_t w0[4] = {W[0].x, W[0].y, W[0].z, W[0].w}, w1[4] = {W[1].x, W[1].y, W[1].z, W[1].w};
             const uint32_t w8[4] = {W[2].x, W[2].y, W[2].z, W[2].w}, w9[4] = {W[3].x, W[3].y, W[3].z, W[3].w};
 #pragma unroll
@@ -712,9 +720,11 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
           }
         }
       if (!(m.flags & kMetaLast)) {
-        __syncwarp();  // the warp is done with the stage (and pw) before it releases it
-        if (t == 0 && seq < 10) ATTN_STAMP(7 + 4 * seq);
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (!released) {
+          __syncwarp();  // the warp is done with the stage before it releases it
+          if (t == 0 && seq < 10) ATTN_STAMP(7 + 4 * seq);
+          if (lane == 0) mbar_arrive(&empty[s]);
+        }
         continue;
       }
       // ---- the item's end: merge the warps' states in its last chunk's

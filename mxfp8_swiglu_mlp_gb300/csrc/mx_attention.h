@@ -38,7 +38,7 @@ struct AttnArgs {
 // at most) for B sequences, Hkv KV heads and at most max_pages pages of P
 // tokens, on `sms` SMs.
 int attn_splits(int B, int Hkv, int max_pages, int P, int sms, int chunks_per_block);
-constexpr int kAttnChunksPerBlock = 6;
+constexpr int kAttnChunksPerBlock = 8;
 // Partial-result floats of one call.
 inline size_t attn_part_floats(int B, int Hq, int nsplit) {
   return static_cast<size_t>(B) * Hq * nsplit * (2 + kAttnHeadDim);
