@@ -425,9 +425,9 @@ fsops_status fsops_debug_set_extra_arrivals(uint32_t n);
  *                     issued.
  *   ALIGNED           split phases: 1 gives each block K stages of one tile
  *                     only, 0 the even split over all tiles' stages.
- *   ATTN_CHUNKS       paged decode attention: 128-token chunks per block
- *                     (the workspace size depends on it: query it again
- *                     after a change). */
+ *   ATTN_CHUNKS       paged decode attention: 128-token chunks per work
+ *                     item (8 by default; the workspace size depends on it:
+ *                     query it again after a change). */
 typedef enum {
   FSOPS_KNOB_TR0 = 0,
   FSOPS_KNOB_TR1 = 1,
