@@ -10,8 +10,8 @@
 //                           read once for the group) and add p . v, both
 //                           products on the tensor cores, keeping an online
 //                           softmax per warp.
-//   attn_combine_kernel     merges the splits of one (sequence, query head)
-//                           and writes the bf16 output.
+//   attn_combine_kernel<G>  merges the splits of one (sequence, KV head)'s
+//                           G query heads and writes the bf16 output.
 //
 // K and V are MXFP8: E4M3 codes with one UE8M0 scale per 32 elements of the
 // head dimension (the Fish Audio post's mxfp8 format, p2 "Estrategia de
@@ -242,6 +242,8 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int items = a.nsplit * a.B * a.Hkv;
+  // the combining launch may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (t == 0) {
 #pragma unroll
@@ -802,11 +804,15 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
   }
 }
 
-// One block per (query head, sequence), one thread per dimension.
-__global__ void __launch_bounds__(kD) attn_combine_kernel(const __grid_constant__ AttnArgs a) {
-  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+// One block per (KV head, sequence): thread (g, d) merges dimension d of
+// query head hk G + g over the splits that hold chunks of the sequence (only
+// those wrote a record).  Launched as the decode launch's programmatic
+// dependent: it waits for that grid before reading.
+template <int G>
+__global__ void __launch_bounds__(G * kD) attn_combine_kernel(const __grid_constant__ AttnArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int hk = blockIdx.x, b = blockIdx.y, h = hk * G + threadIdx.x / kD, d = threadIdx.x % kD;
   const float* rec = a.part + (static_cast<size_t>(b) * a.Hq + h) * a.nsplit * (2 + kD);
-  // the splits that hold chunks of the sequence (only those wrote a record)
   const int len = a.seq_lens[b];
   const int n = (len >= 1 && len <= a.max_pages * a.P) ? len : 0;
   const int per = (a.max_pages * a.P + kC * a.nsplit - 1) / (kC * a.nsplit);
@@ -815,16 +821,16 @@ __global__ void __launch_bounds__(kD) attn_combine_kernel(const __grid_constant_
   for (int s = 0; s < ns; ++s) M = fmaxf(M, rec[s * (2 + kD)]);
   float num = 0.f, den = 0.f;
   if (M != -INFINITY) {
+#pragma unroll 4
     for (int s = 0; s < ns; ++s) {
       const float m = rec[s * (2 + kD)];
-      if (m == -INFINITY) continue;
-      const float w = exp2f(m - M);
+      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
       num = fmaf(w, rec[s * (2 + kD) + 2 + d], num);
       den = fmaf(w, rec[s * (2 + kD) + 1], den);
     }
   }
   // the decode launch has finished: its work counter starts the next call at zero
-  if (h == 0 && b == 0 && d == 0) *a.work = 0u;
+  if (hk == 0 && b == 0 && threadIdx.x == 0) *a.work = 0u;
   const float o = den > 0.f ? num / den : 0.f;
   const __nv_bfloat16 ob = __float2bfloat16_rn(o);
   a.out[(static_cast<size_t>(b) * a.Hq + h) * kD + d] = *reinterpret_cast<const uint16_t*>(&ob);
@@ -839,8 +845,17 @@ cudaError_t launch_group(const AttnArgs& a, cudaStream_t stream) {
   paged_decode_kernel<G><<<a.grid, kAThreads, kAttnSmem, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<dim3(a.Hq, a.B), kD, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.Hkv, a.B);
+  cfg.blockDim = dim3(G * kD);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_combine_kernel<G>, a);
 }
 
 }  // namespace
