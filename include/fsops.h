@@ -414,8 +414,12 @@ fsops_status fsops_debug_set_extra_arrivals(uint32_t n);
  *   PRIME             weight loads in flight before the activations exist.
  *   MAX_INFLIGHT      weight loads in flight per block (1..8).
  *   LOCAL_XQ          0: quantise x grid-wide even for M <= 16.
- *   DECODE_PATH       M <= 32: 1 runs the cluster-sliced kernel instead of
- *                     the grid-wide two-phase kernel (the default).
+ *   DECODE_PATH       M <= 128: 0 the grid-wide two-phase kernel, 1 the
+ *                     cluster-sliced kernel (M <= 32), 2 the small-M kernel
+ *                     (M <= 8, one block per 32 intermediate features and
+ *                     per 16 output rows on the SMs, each block's weights
+ *                     in shared memory).  Default: the small-M kernel where
+ *                     it applies, else the grid-wide kernel.
  *   COOPERATIVE       1: launch the grid-wide kernel cooperatively instead
  *                     of as a plain launch that may start while the previous
  *                     kernel on the stream finishes.

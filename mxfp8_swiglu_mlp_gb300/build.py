@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libfsops.so")
-SOURCES = ["mx_kernels.cu", "mx_slice.cu", "mx_blockscale.cu", "mx_gemm_tiled.cu", "mx_attention.cu", "fsops_api.cu"]
+SOURCES = ["mx_kernels.cu", "mx_slice.cu", "mx_small.cu", "mx_blockscale.cu", "mx_gemm_tiled.cu", "mx_attention.cu",
+           "fsops_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

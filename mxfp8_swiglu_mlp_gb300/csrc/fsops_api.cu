@@ -19,6 +19,7 @@
 #include "mx_tiled.h"
 #include "mx_attention.h"
 #include "mx_slice.h"
+#include "mx_small.h"
 #include "mx_blockscale.h"
 
 using namespace fsops;
@@ -475,6 +476,48 @@ bool use_slice(int M, int H, int I, const DeviceInfo* di, SlicePlan* sp) {
   if (knob(FSOPS_KNOB_DECODE_PATH) != 1) return false;
   return slice_plan(M, H, I, di->sms, sp);
 }
+// Whether the fused MLP call runs the small-M kernel (mx_small.cu): by
+// default wherever it applies (M <= 8, one block per 32 intermediate
+// features and per 16 output rows, each block's weights in shared memory),
+// or only when FSOPS_KNOB_DECODE_PATH = 2; never with 0 or 1.
+bool use_small(int M, int H, int I, const DeviceInfo* di) {
+  const int k = knob(FSOPS_KNOB_DECODE_PATH);
+  if (k == 0 || k == 1) return false;
+  return small_fits(M, H, I, di->sms);
+}
+// One launch of the small-M kernel on the workspace's control words and h
+// buffers.  gamma != null: RMSNorm(x) * gamma is quantised; residual != null
+// is added to y before the bf16 rounding.
+fsops_status launch_small(const MlpLayout& l, uint8_t* ws, const void* x_bf16, const void* gamma, float eps,
+                          const void* residual, const uint8_t* w_gateup, const uint8_t* w_down,
+                          const fsops_mlp_scales* scales, void* y_bf16, int M, int H, int I, const DeviceInfo* di,
+                          cudaStream_t stream) {
+  SmallArgs sa;
+  std::memset(&sa, 0, sizeof(sa));
+  if (!encode_map(&sa.tm_wgu, w_gateup, H, 2 * I, 32) || !encode_map(&sa.tm_wd, w_down, I, H, 16))
+    return FSOPS_ERR_INVALID_ARG;
+  sa.sf_gu = scales->gateup;
+  sa.sf_d = scales->down;
+  sa.x = static_cast<const uint16_t*>(x_bf16);
+  sa.gamma = static_cast<const uint16_t*>(gamma);
+  sa.eps = eps;
+  sa.residual = static_cast<const uint16_t*>(residual);
+  sa.y = static_cast<uint16_t*>(y_bf16);
+  sa.hq = ws + l.hq;
+  sa.hs = ws + l.hq_sf;
+  sa.ctl = reinterpret_cast<uint32_t*>(ws + l.ctl);
+  sa.M = M;
+  sa.H = H;
+  sa.I = I;
+  sa.U = I / 32;
+  sa.T = H / 16;
+  sa.split = small_split(H, I, di->sms);
+  sa.timeout_ns = g_timeout_ns.load();
+  sa.extra_arrivals = g_extra.load();
+  const int grid = sa.split ? sa.U + sa.T : (sa.U > sa.T ? sa.U : sa.T);
+  const cudaError_t e = launch_small_kernel(sa, grid, stream);
+  return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "mx_small_kernel launch");
+}
 // One launch of the sliced kernel.  ctl: the control words (status word,
 // then RT tile counters), accum: fp32 [M, H], both zero between launches.  gamma != null: x is normalised (RMSNorm with eps) before its
 // quantisation; residual != null is added to y before the bf16 rounding.
@@ -835,6 +878,9 @@ fsops_status fsops_mxfp8_swiglu_mlp(const void* x_bf16, const uint8_t* w_gateup,
   if (use_slice(M, H, I, di, &sp))
     return launch_slice(sp, ws + l.ctl, ws + l.part1, x_bf16, nullptr, 0.f, nullptr, w_gateup, w_down, scales,
                         y_bf16, M, H, I, static_cast<cudaStream_t>(stream));
+  if (use_small(M, H, I, di))
+    return launch_small(l, ws, x_bf16, nullptr, 0.f, nullptr, w_gateup, w_down, scales, y_bf16, M, H, I, di,
+                        static_cast<cudaStream_t>(stream));
 
   const MlpPlan pl = plan_mlp(M, H, I, grid);
   const MlpBuffers bufs{ws + l.ctl, ws + l.xq, ws + l.xq_sf, ws + l.hq, ws + l.hq_sf, ws + l.part0, ws + l.part1};
@@ -970,6 +1016,9 @@ fsops_status fsops_mxfp8_swiglu_mlp_block(const void* x_bf16, const void* gamma_
   if (M <= 128 && use_slice(M, H, I, di, &sp))  // one launch: the norm runs inside the MLP kernel
     return launch_slice(sp, ws + l.ctl, ws + l.part1, x_bf16, gamma_bf16, eps, residual ? x_bf16 : nullptr,
                         w_gateup, w_down, scales, y_bf16, M, H, I, s);
+  if (use_small(M, H, I, di))  // one launch, the norm inside
+    return launch_small(l, ws, x_bf16, gamma_bf16, eps, residual ? x_bf16 : nullptr, w_gateup, w_down, scales,
+                        y_bf16, M, H, I, di, s);
   const void* res = residual ? x_bf16 : nullptr;
   if (M <= 128) {
     // one launch: the MLP kernel normalises x in its quantisation prologue

@@ -114,11 +114,11 @@ def test_block_sliced_one_launch(fs, M, H, I, seed, residual, knob):
     _assert_parity(B.run_block(fs, residual), B.oracle_block(residual))
 
 
-@pytest.mark.parametrize("path", [0, 1])
-def test_block_in_place_sliced_and_grid(fs, path, knob):
-    """In place (y is x's buffer) on both decode paths."""
+@pytest.mark.parametrize("path,M", [(0, 16), (1, 16), (2, 8), (0, 8)])
+def test_block_in_place_sliced_and_grid(fs, path, M, knob):
+    """In place (y is x's buffer) on every decode path."""
     knob("DECODE_PATH", path)
-    wl = inputs.make_workload_small("s", 16, 512, 768, 76)
+    wl = inputs.make_workload_small("s", M, 512, 768, 76)
     B = Block(fs, wl)
     a = B.run_block(fs, True, in_place=False)
     b = B.run_block(fs, True, in_place=True)

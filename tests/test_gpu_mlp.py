@@ -118,20 +118,32 @@ def test_tile_plans(fs, M, kn, knob):
     _assert_parity(L.run(fs, True), L.oracle())
 
 
-@pytest.mark.parametrize("M,H,I,seed", [(1, 512, 1024, 30), (16, 768, 2560, 31), (32, 512, 896, 32)])
+@pytest.mark.parametrize("M,H,I,seed", [(1, 512, 1024, 30), (16, 768, 2560, 31), (32, 512, 896, 32),
+                                        (8, 1024, 2816, 33), (2, 2048, 1024, 34)])
 def test_decode_paths_agree(fs, M, H, I, seed, knob):
-    """The cluster-sliced kernel and the grid-wide kernel on the same inputs:
-    both within the oracle's tolerance, and close to each other."""
+    """The cluster-sliced kernel, the grid-wide kernel and (M <= 8) the
+    small-M kernel on the same inputs: each within the oracle's tolerance,
+    and close to one another."""
     wl = inputs.make_workload_small("s", M, H, I, seed)
     L = Layer(fs, wl)
     ref = L.oracle()
-    knob("DECODE_PATH", 1)
-    a = L.run(fs)
+    outs = []
+    for path in ([0, 1, 2] if M <= 8 else [0, 1]):
+        knob("DECODE_PATH", path)
+        outs.append(L.run(fs))
+        _assert_parity(outs[-1], ref)
+    for o in outs[1:]:
+        assert rel_l2(bf16_bits_to_f64(o), bf16_bits_to_f64(outs[0])) < 1e-3
+
+
+@pytest.mark.parametrize("M,H,I,seed", [s for s in SMALL if s[0] <= 8])
+def test_small_shapes_grid_wide(fs, M, H, I, seed, knob):
+    """The shapes of up to 8 tokens (which the small-M kernel takes by
+    default where it applies) on the grid-wide kernel."""
     knob("DECODE_PATH", 0)
-    b = L.run(fs)
-    _assert_parity(a, ref)
-    _assert_parity(b, ref)
-    assert rel_l2(bf16_bits_to_f64(a), bf16_bits_to_f64(b)) < 1e-3
+    wl = inputs.make_workload_small("s", M, H, I, seed)
+    L = Layer(fs, wl)
+    _assert_parity(L.run(fs), L.oracle())
 
 
 def test_token_scale_spread(fs):
@@ -258,7 +270,8 @@ def test_output_guard_band(fs):
 # distributed shared memory (I / 128 = 40 tiles for 76 pairs); with whole
 # gate/up tiles and per-owner finishing (M = 64); cooperative.
 TIMEOUT_CASES = [(4, 256, 384, {"DECODE_PATH": 1}), (4, 256, 384, {"DECODE_PATH": 0}), (16, 256, 5120, {"DECODE_PATH": 0}),
-                 (64, 256, 1024, {}), (16, 256, 5120, {"DECODE_PATH": 0, "COOPERATIVE": 1})]
+                 (64, 256, 1024, {}), (16, 256, 5120, {"DECODE_PATH": 0, "COOPERATIVE": 1}),
+                 (4, 256, 384, {"DECODE_PATH": 2}), (8, 256, 4864, {"DECODE_PATH": 2})]
 
 
 @pytest.mark.parametrize("M,H,I,knobs", TIMEOUT_CASES)
