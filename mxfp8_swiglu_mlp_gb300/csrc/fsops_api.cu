@@ -514,6 +514,9 @@ fsops_status launch_small(const MlpLayout& l, uint8_t* ws, const void* x_bf16, c
   sa.split = small_split(H, I, di->sms);
   sa.timeout_ns = g_timeout_ns.load();
   sa.extra_arrivals = g_extra.load();
+#ifdef FSOPS_TRACE
+  sa.trace = g_trace;
+#endif
   const int grid = sa.split ? sa.U + sa.T : (sa.U > sa.T ? sa.U : sa.T);
   const cudaError_t e = launch_small_kernel(sa, grid, stream);
   return e == cudaSuccess ? FSOPS_OK : cuda_failed(e, "mx_small_kernel launch");

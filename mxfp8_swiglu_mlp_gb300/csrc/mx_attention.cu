@@ -85,18 +85,6 @@ constexpr size_t kAttnSmem = kAStages * sizeof(AttnStage) + 1024;  // + alignmen
 __device__ __forceinline__ int swz(int row, int off) {
   return row * 128 + ((((off >> 4) ^ row) & 7) << 4) + (off & 15);
 }
-// E4M3 codes in bytes 0-1 (or 2-3) of w as f16x2 (exact), the lower byte in
-// the lower half.
-__device__ __forceinline__ uint32_t e4m3_lo_f16x2(uint32_t w) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}" : "=r"(r) : "r"(w));
-  return r;
-}
-__device__ __forceinline__ uint32_t e4m3_hi_f16x2(uint32_t w) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(r) : "r"(w));
-  return r;
-}
 // Two floats as f16x2 (round to nearest even), `lo` in the lower half.
 __device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
   uint32_t r;
@@ -121,14 +109,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
-}
-// d += A . B on the tensor core: A 16 x 16 f16 (row), B 16 x 8 f16 (col), fp32 d.
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 // Two E4M3 codes (low byte first) as two floats: exact.
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
@@ -226,7 +206,7 @@ struct ChunkMeta {
 template <int G>
 __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  AttnStage* stg = reinterpret_cast<AttnStage*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  AttnStage* stg = reinterpret_cast<AttnStage*>(smem_align(smem_raw, 1024));
   // each consumer warp's probabilities of its 16 tokens: [warp][head][token]
   __shared__ __align__(16) float pws[kCWarps * 8 * kPwLd];
   __shared__ float red_max[kCWarps * G], red_sum[kCWarps * G];

@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(BsCfg<NPAD>::THREADS, 1) bs_gemm_kernel(const 
   constexpr uint32_t SB = Cfg::SB;
   constexpr int NB = kBsAccBufs;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align(smem_raw, 1024);
   uint8_t* ring = smem;
   uint8_t* unit_sf = smem + static_cast<size_t>(S) * SB;  // 512 bytes of UE8M0 2^0
   uint8_t* ctl = unit_sf + 512;

@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kTThreads, 1) mx_gemm_tiled_kernel(const __gri
   constexpr bool PAIR = F::PAIR;
   constexpr int NS = F::kStages;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align(smem_raw, 1024);
   uint8_t* ctl = smem + NS * F::kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctl);  // this block's stage has landed
   uint64_t* empty = full + NS;                         // the stage's MMAs have completed

@@ -554,7 +554,7 @@ template <bool STAGED>
 __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid_constant__ KernelArgs a) {
   const bool local_xq = STAGED && a.local_xq != 0;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align(smem_raw, 1024);
   const int S = a.nstages;
   float* stg = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * a.stage_bytes);
   uint8_t* xring = reinterpret_cast<uint8_t*>(stg) + (STAGED ? stg_bytes_for(a.npad) : 0u);

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_slice_kernel(const __grid_cons
   constexpr int NB = kSliceAccBufs;
   constexpr uint32_t UL = NPAD + 4;       // ubuf row stride (floats)
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align(smem_raw, 1024);
   const int S = a.nstages;
   constexpr uint32_t SB = 384u * NPAD + kSliceWBytes + 1024u;  // slice_stage_bytes
   uint8_t* htile = smem;

@@ -36,7 +36,20 @@ namespace fsops {
 
 namespace {
 
-constexpr int kSmallThreads = 256;  // 8 warps
+constexpr int kSmallWarps = 16;
+constexpr int kSmallThreads = 32 * kSmallWarps;
+
+// Timeline stamps for profiling builds (compiled with -DFSOPS_TRACE).
+#ifdef FSOPS_TRACE
+#define SMALL_STAMP(idx)                                                                   \
+  do {                                                                                     \
+    if (a.trace != nullptr) a.trace[blockIdx.x * 128 + (idx)] = globaltimer_ns();          \
+  } while (0)
+#else
+#define SMALL_STAMP(idx) \
+  do {                   \
+  } while (0)
+#endif
 
 __device__ __forceinline__ void small_error(const SmallArgs& a, uint32_t code, uint32_t site) {
   atomicCAS(a.ctl + kCtlStatus, 0u, (code << 24) | ((site & 0xFFu) << 16) | (blockIdx.x & 0xFFFFu));
@@ -52,7 +65,8 @@ __device__ __forceinline__ bool small_wait(uint64_t* bar, uint32_t parity, uint6
 __device__ __forceinline__ float ue8m0_f32(uint32_t s) {
   return s != 0 ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
 }
-// d = A . B on the tensor core: A 16 x 32 E4M3 (row), B 32 x 8 E4M3 (col), fp32 d.
+// d = A . B on the tensor core: A 16 x 32 E4M3 (row), B 32 x 8 E4M3 (col),
+// fp32 d (the products are exact).
 __device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -60,42 +74,83 @@ __device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint3
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// Four 8 x 16-byte matrices from shared memory, one row address per lane
+// (lanes 8i .. 8i + 7 the rows of matrix i); lane l gets bytes 4 (l % 4) ..
+// 4 (l % 4) + 3 of row l / 4 of each.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& m0, uint32_t& m1, uint32_t& m2, uint32_t& m3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(m0), "=r"(m1), "=r"(m2), "=r"(m3)
+               : "r"(addr));
+}
 
 // One warp's share of a 16-row weight tile times 8 token columns, over the
-// 32-element K blocks j = j0, j0 + dj, ... < j1 (nk blocks in a row of
-// scales ws and xsc).  The weight rows sit in
-// TMA boxes of 128-byte rows (128-byte swizzle; box kt of the tile at
-// w + kt * box_bytes, the tile's first row at row0 of its box); the
-// tokens' codes in rows of `ld` bytes.  The MMA's k index 4 tq + e is K
-// element 8 tq + e of the block and 16 + 4 tq + e is 8 tq + 4 + e, so that a
-// lane's operand bytes are 8 consecutive codes of each row.  acc[0..3]: rows
-// g, g, g + 8, g + 8 of the tile x tokens 2 tq, 2 tq + 1.
+// 32-element K blocks j = j0, j0 + dj, ... < j1.
+//   w, box_bytes, row0  the tile's rows: TMA boxes of 128-byte rows (128-byte
+//                       swizzle, box j / 4 at w + (j / 4) box_bytes), the
+//                       tile's first row at row0 of its box;
+//   ws, wst, wof        the rows' scale bytes: rows g and g + 8 of block j at
+//                       ws + (8 j + g) wst + wof and + 1;
+//   xc, ld              the tokens' codes, rows of ld bytes, each 32-element
+//                       block stored as [tq][half][4 codes]: codes 16 h + 4 tq
+//                       .. + 3 at byte 8 tq + 4 h of the block;
+//   xsc                 the tokens' scales as floats, [block][8 tokens].
+// A block is one E4M3 MMA (m16n8k32, fp32 sums): k index 4 tq + e is code
+// 4 tq + e of the block's first 16-code half and 16 + 4 tq + e code 4 tq + e
+// of its second, for the weight rows (ldmatrix from the swizzled boxes) and
+// the tokens alike.  acc[0..3]: rows g, g, g + 8, g + 8 of the tile x
+// tokens 2 tq, 2 tq + 1.
 __device__ __forceinline__ void tile_products(float (&acc)[4], const uint8_t* w, uint32_t box_bytes, int row0,
-                                              const uint8_t* ws, const uint8_t* xcodes, int ld, const float* xsc,
-                                              int nk, int j0, int j1, int dj, int lane) {
+                                              const uint8_t* ws, int wst, int wof, const uint8_t* xc, int ld,
+                                              const float* xsc, int j0, int j1, int dj, int lane) {
   const int g = lane >> 2, tq = lane & 3;
-  const int r0 = row0 + g, r1 = r0 + 8;
-  for (int j = j0; j < j1; j += dj) {
-    const uint8_t* box = w + (j >> 2) * box_bytes;
-    const int c16 = 2 * (j & 3) + (tq >> 1);  // 16-byte piece of the lane's 8 bytes
-    const uint2 A0 = *reinterpret_cast<const uint2*>(box + r0 * 128 + ((c16 ^ (r0 & 7)) << 4) + 8 * (tq & 1));
-    const uint2 A1 = *reinterpret_cast<const uint2*>(box + r1 * 128 + ((c16 ^ (r1 & 7)) << 4) + 8 * (tq & 1));
-    const uint2 Bv = *reinterpret_cast<const uint2*>(xcodes + g * ld + 32 * j + 8 * tq);
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_e4m3_16832(d, A0.x, A1.x, A0.y, A1.y, Bv.x, Bv.y);
-    const float w0 = ue8m0_f32(ws[g * nk + j]), w1 = ue8m0_f32(ws[(g + 8) * nk + j]);
-    const float x0 = xsc[(2 * tq) * nk + j], x1 = xsc[(2 * tq + 1) * nk + j];
-    acc[0] = fmaf(d[0], w0 * x0, acc[0]);
-    acc[1] = fmaf(d[1], w0 * x1, acc[1]);
-    acc[2] = fmaf(d[2], w1 * x0, acc[2]);
-    acc[3] = fmaf(d[3], w1 * x1, acc[3]);
+  // ldmatrix rows: lane l gives row row0 + (l & 7) + 8 ((l >> 3) & 1) of half (l >> 4)
+  const int lrow = row0 + (lane & 7) + 8 * ((lane >> 3) & 1), lhalf = lane >> 4;
+  const uint32_t lbase = smem_u32(w) + lrow * 128;
+  // two blocks per step, every load of both issued first
+  float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int j = j0; j < j1; j += 2 * dj) {
+    const bool two = j + dj < j1;
+    uint32_t m[2][4];
+    uint2 Bv[2];
+    uint16_t wsv[2];
+    float2 xv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int jj = two ? j + u * dj : j;
+      ldmatrix_x4(lbase + (jj >> 2) * box_bytes + (((2 * (jj & 3) + lhalf) ^ (lrow & 7)) << 4), m[u][0], m[u][1],
+                  m[u][2], m[u][3]);
+      Bv[u] = *reinterpret_cast<const uint2*>(xc + g * ld + 32 * jj + 8 * tq);
+      wsv[u] = *reinterpret_cast<const uint16_t*>(ws + (8 * jj + g) * wst + wof);
+      xv[u] = *reinterpret_cast<const float2*>(xsc + 8 * jj + 2 * tq);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (u == 1 && !two) break;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_e4m3_16832(d, m[u][0], m[u][1], m[u][2], m[u][3], Bv[u].x, Bv[u].y);
+      const float w0 = ue8m0_f32(wsv[u] & 0xFFu), w1 = ue8m0_f32(wsv[u] >> 8);
+      float* ac = u ? acc2 : acc;
+      ac[0] = fmaf(d[0], w0 * xv[u].x, ac[0]);
+      ac[1] = fmaf(d[1], w0 * xv[u].y, ac[1]);
+      ac[2] = fmaf(d[2], w1 * xv[u].x, ac[2]);
+      ac[3] = fmaf(d[3], w1 * xv[u].y, ac[3]);
+    }
   }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
+}
+// Store a 32-code block (packed[i] = codes 4i .. 4i + 3) in the [tq][half]
+// order tile_products reads.
+__device__ __forceinline__ void store_block_codes(uint8_t* dst, const uint32_t (&packed)[8]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(packed[0], packed[4], packed[1], packed[5]);
+  d[1] = make_uint4(packed[2], packed[6], packed[3], packed[7]);
 }
 
 template <bool NORM>
-__global__ void __launch_bounds__(kSmallThreads, 1) mx_small_kernel(const __grid_constant__ SmallArgs a) {
+__global__ void __launch_bounds__(kSmallThreads, 2) mx_small_kernel(const __grid_constant__ SmallArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sm = smem_align(smem_raw, 1024);
   __shared__ __align__(8) uint64_t bar_a, bar_b;
   __shared__ int failed;
 
@@ -110,14 +165,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mx_small_kernel(const __grid
   // shared memory (every region 16-byte aligned; the weight boxes 1024)
   uint8_t* wa = sm;                                        // [2][KA][32 rows][128]: gate rows, then up rows
   uint8_t* wb = a.split ? sm : wa + 64 * H;                // [KB][16 rows][128]
-  uint8_t* xs = sm + small_weight_bytes(H, I, a.split);    // [8][H + 16] x codes
-  uint8_t* hsm = xs + 8 * (H + 16);                        // [8][I + 16] h codes
-  float* xsc = reinterpret_cast<float*>(hsm + 8 * (I + 16));  // [8][nka]
-  float* hsc = xsc + 8 * nka;                              // [8][nkb]
-  uint8_t* wsa = reinterpret_cast<uint8_t*>(hsc + 8 * nkb);  // [64][nka]
-  uint8_t* wsb = wsa + 64 * nka;                           // [16][nkb]
-  float* red = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(wsb + 16 * nkb) + 15) & ~uintptr_t(15));
-  float* h32 = red + 8 * 16 * 8;                           // [8 tokens][32 features]
+  // token codes in rows of H + 32 (I + 32) bytes: 8 tq + 2 tq' mod 32 banks
+  // apart for the 16 lanes of a half warp
+  uint8_t* xs = sm + small_weight_bytes(H, I, a.split);    // [8][H + 32] x codes ([tq][half] per block)
+  uint8_t* hsm = xs + 8 * (H + 32);                        // [8][I + 32] h codes (likewise)
+  float* xsc = reinterpret_cast<float*>(hsm + 8 * (I + 32));  // [nka][8 tokens]
+  float* hsc = xsc + 8 * nka;                              // [nkb][8 tokens]
+  uint8_t* wsa = reinterpret_cast<uint8_t*>(hsc + 8 * nkb);  // [nka][g][tile rt][row half]: 64 nka bytes
+  uint8_t* wsb = wsa + 64 * nka;                           // [nkb][g][row half]: 16 nkb bytes
+  float* red = reinterpret_cast<float*>(smem_align(wsb + 16 * nkb, 16));
+  float* h32 = red + kSmallWarps * 16 * 8;                 // [8 tokens][32 features]
 
   // unit b's gate rows (32) and up rows (32) in W_gateup's paired order:
   // 128-row blocks of 64 gate rows then the same features' 64 up rows
@@ -127,6 +184,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mx_small_kernel(const __grid
     mbar_init(&bar_b, 1);
     mbar_fence_init();
     failed = 0;
+    SMALL_STAMP(0);
   }
   __syncthreads();
   // ---- the weights do not depend on earlier work: fetched before the wait
@@ -146,26 +204,29 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mx_small_kernel(const __grid
       for (int kt = 0; kt < KB; ++kt) tma_load_2d(wb + kt * 2048, &a.tm_wd, &bar_b, 128 * kt, 16 * tb, pol);
     }
   }
-  // weight scales, from the tcgen05 tiled layout into [row][block] bytes
+  // weight scales, from the tcgen05 tiled layout into the order the
+  // products read: block kb, lane group g, then rows 16 rt + g (+ 8)
   if (do_a)
     for (int i = t; i < 64 * nka; i += kSmallThreads) {
-      const int r = i / nka, kb = i % nka;
+      const int kb = i >> 6, g = (i >> 3) & 7, rt = (i >> 1) & 3, hf = i & 1;
+      const int r = 16 * rt + 8 * hf + g;  // unit row: gate 0-31, up 32-63
       wsa[i] = a.sf_gu[tiled_sf_offset(r < 32 ? gate_row + r : up_row + r - 32, kb, KA)];
     }
   if (do_b)
     for (int i = t; i < 16 * nkb; i += kSmallThreads) {
-      const int r = i / nkb, kb = i % nkb;
-      wsb[i] = a.sf_d[tiled_sf_offset(16 * tb + r, kb, KB)];
+      const int kb = i >> 4, g = (i >> 1) & 7, hf = i & 1;
+      wsb[i] = a.sf_d[tiled_sf_offset(16 * tb + 8 * hf + g, kb, KB)];
     }
   griddep_wait();
   griddep_launch_dependents();
+  if (t == 0) SMALL_STAMP(1);
 
   // ---- x (the units only): token m by warp m, one 32-element block per lane
   // at a time.  The tiles never read x, and write y only once every unit has
   // read it, so y may be x's buffer.
-  if (do_a) {
+  if (do_a && warp < kSmallMaxM) {
     const int m = warp;
-    uint8_t* xr = xs + m * (H + 16);
+    uint8_t* xr = xs + m * (H + 32);
     if (m < M) {
       const uint16_t* src = a.x + static_cast<size_t>(m) * H;
       const float rn = NORM ? row_rnorm(src, H, a.eps, lane) : 1.f;
@@ -176,32 +237,35 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mx_small_kernel(const __grid
         uint32_t packed[8];
         const uint32_t s = NORM ? quantize_block_pack_norm(raw, a.gamma + 32 * kb, rn, packed)
                                 : quantize_block_pack(raw, packed);
-        uint4* d = reinterpret_cast<uint4*>(xr + 32 * kb);
-        d[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        d[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        xsc[m * nka + kb] = ue8m0_f32(s);
+        store_block_codes(xr + 32 * kb, packed);
+        xsc[kb * 8 + m] = ue8m0_f32(s);
       }
     } else {
       for (int i = lane; i < H / 16; i += 32) reinterpret_cast<uint4*>(xr)[i] = make_uint4(0u, 0u, 0u, 0u);
-      for (int kb = lane; kb < nka; kb += 32) xsc[m * nka + kb] = 0.f;
+      for (int kb = lane; kb < nka; kb += 32) xsc[kb * 8 + m] = 0.f;
     }
   }
   __syncthreads();
 
   // ---- unit b: gate and up sums of 32 features, SwiGLU, h requantised
   if (do_a) {
+    if (t == 0) SMALL_STAMP(2);
     if (!small_wait(&bar_a, 0, a.timeout_ns)) {
       if (lane == 0) small_error(a, 5u, 20u);  // FSOPS_ERR_TIMEOUT
       failed = 1;
     }
     __syncthreads();
+    if (t == 0) SMALL_STAMP(3);
     if (!failed) {
       // warp w: 16-row tile w % 4 (gate rows 0-15, 16-31, up rows 0-15,
-      // 16-31) over half w / 4 of the K blocks
+      // 16-31) over the K blocks w / 4, w / 4 + 4, ...
       const int rt = warp & 3, kh = warp >> 2;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      tile_products(acc, wa + (rt >> 1) * KA * 4096, 4096, 16 * (rt & 1), wsa + 16 * rt * nka, xs, H + 16, xsc,
-                    nka, kh * (nka / 2), (kh + 1) * (nka / 2), 1, lane);
+      if (t == 0) SMALL_STAMP(10);
+      tile_products(acc, wa + (rt >> 1) * KA * 4096, 4096, 16 * (rt & 1), wsa, 8, 2 * rt, xs, H + 32, xsc, kh, nka,
+                    kSmallWarps / 4, lane);
+      if (lane == 0 && warp == 0) SMALL_STAMP(11);
+      if (lane == 0 && warp == kSmallWarps - 1) SMALL_STAMP(12);
       const int g = lane >> 2, tq = lane & 3;
       red[(warp * 16 + g) * 8 + 2 * tq] = acc[0];
       red[(warp * 16 + g) * 8 + 2 * tq + 1] = acc[1];
@@ -209,12 +273,17 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mx_small_kernel(const __grid
       red[(warp * 16 + g + 8) * 8 + 2 * tq + 1] = acc[3];
     }
     __syncthreads();
-    if (!failed) {
-      // feature f = t / 8 of the unit for token m = t % 8: gate in tiles
-      // f / 16 (warps f / 16 and 4 + f / 16), up in tiles 2 + f / 16
+    if (t == 0) SMALL_STAMP(4);
+    if (!failed && t < 256) {
+      // feature f = t / 8 of the unit for token m = t % 8: gate in tile
+      // f / 16 (warps f / 16 + 4 q), up in tile 2 + f / 16
       const int f = t >> 3, m = t & 7, gt = f >> 4, fr = f & 15;
-      const float gs = red[(gt * 16 + fr) * 8 + m] + red[((4 + gt) * 16 + fr) * 8 + m];
-      const float us = red[((2 + gt) * 16 + fr) * 8 + m] + red[((6 + gt) * 16 + fr) * 8 + m];
+      float gs = 0.f, us = 0.f;
+#pragma unroll
+      for (int q = 0; q < kSmallWarps / 4; ++q) {
+        gs += red[((4 * q + gt) * 16 + fr) * 8 + m];
+        us += red[((4 * q + 2 + gt) * 16 + fr) * 8 + m];
+      }
       h32[m * 32 + f] = silu_mul(gs, us);
     }
     __syncthreads();
@@ -227,15 +296,24 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mx_small_kernel(const __grid
       const uint32_t s = ue8m0_from_amax(amax);
       a.hq[static_cast<size_t>(warp) * I + 32 * b + lane] = static_cast<uint8_t>(e4m3_code(v * inv_scale_from_ue8m0(s)));
       if (lane == 0) a.hs[static_cast<size_t>(warp) * nkb + b] = static_cast<uint8_t>(s);
-      __threadfence();
     }
     __syncthreads();
+    // the release (cumulative over the block's writes before the barrier)
+    // publishes the unit
     if (t == 0 && !failed) red_add_release_gpu(a.ctl + kCtlSmallPublished, 1u);
+    if (t == 0) SMALL_STAMP(5);
   }
 
   // ---- tile tb: rows 16 tb .. 16 tb + 15 of y over all of I
   if (do_b) {
+    // the rows of h past the tokens hold zeros
+    for (int i = t; i < (kSmallMaxM - M) * (I / 16); i += kSmallThreads) {
+      const int m = M + i / (I / 16), c = i % (I / 16);
+      reinterpret_cast<uint4*>(hsm + m * (I + 32))[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int i = t; i < (kSmallMaxM - M) * nkb; i += kSmallThreads) hsc[(i % nkb) * 8 + M + i / nkb] = 0.f;
     if (t == 0) {
+      SMALL_STAMP(6);
       if (!small_wait(&bar_b, 0, a.timeout_ns)) {
         small_error(a, 5u, 21u);  // FSOPS_ERR_TIMEOUT
         failed = 1;
@@ -251,27 +329,33 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mx_small_kernel(const __grid
           }
         }
       }
+      SMALL_STAMP(7);
     }
     __syncthreads();
     if (!failed) {
       // h codes and scales of the tokens (written by other blocks in this
       // launch: read through L2)
-      const int n16 = I / 16;
-      for (int i = t; i < kSmallMaxM * n16; i += kSmallThreads) {
-        const int m = i / n16, c = i % n16;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (m < M) v = __ldcg(reinterpret_cast<const uint4*>(a.hq + static_cast<size_t>(m) * I) + c);
-        reinterpret_cast<uint4*>(hsm + m * (I + 16))[c] = v;
-      }
-      for (int i = t; i < kSmallMaxM * nkb; i += kSmallThreads) {
-        const int m = i / nkb, kb = i % nkb;
-        hsc[i] = m < M ? ue8m0_f32(__ldcg(a.hs + static_cast<size_t>(m) * nkb + kb)) : 0.f;
+      // (codes and scales in one pass: one round trip; a block's two 16-code
+      // halves are read by one thread and stored in the [tq][half] order)
+      const int n32 = I / 32, nblocks = M * n32;
+      for (int i = t; i < nblocks + M * nkb; i += kSmallThreads) {
+        if (i < nblocks) {
+          const int m = i / n32, kb = i % n32;
+          const uint4* src = reinterpret_cast<const uint4*>(a.hq + static_cast<size_t>(m) * I + 32 * kb);
+          const uint4 lo = __ldcg(src), hi = __ldcg(src + 1);
+          const uint32_t packed[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+          store_block_codes(hsm + m * (I + 32) + 32 * kb, packed);
+        } else {
+          const int k = i - nblocks, m = k / nkb, kb = k % nkb;
+          hsc[kb * 8 + m] = ue8m0_f32(__ldcg(a.hs + k));
+        }
       }
     }
     __syncthreads();
+    if (t == 0) SMALL_STAMP(8);
     if (!failed) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      tile_products(acc, wb, 2048, 0, wsb, hsm, I + 16, hsc, nkb, warp, nkb, 8, lane);
+      tile_products(acc, wb, 2048, 0, wsb, 2, 0, hsm, I + 32, hsc, warp, nkb, kSmallWarps, lane);
       const int g = lane >> 2, tq = lane & 3;
       red[(warp * 16 + g) * 8 + 2 * tq] = acc[0];
       red[(warp * 16 + g) * 8 + 2 * tq + 1] = acc[1];
@@ -284,7 +368,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mx_small_kernel(const __grid
       if (m < M) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) v += red[(w * 16 + r) * 8 + m];
+        for (int w = 0; w < kSmallWarps; ++w) v += red[(w * 16 + r) * 8 + m];
         const size_t o = static_cast<size_t>(m) * H + 16 * tb + r;
         if (a.residual != nullptr) v += __uint_as_float(static_cast<uint32_t>(a.residual[o]) << 16);
         const __nv_bfloat16 ob = __float2bfloat16_rn(v);
@@ -296,6 +380,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) mx_small_kernel(const __grid
   // ---- the last block to leave sets the launch's counters back to zero
   __syncthreads();
   if (t == 0) {
+    SMALL_STAMP(9);
     const uint32_t left = atom_add_acq_rel_gpu(a.ctl + kCtlSmallExits, 1u);
     if (left == gridDim.x - 1) {
       a.ctl[kCtlSmallPublished] = 0u;

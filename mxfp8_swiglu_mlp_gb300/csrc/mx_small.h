@@ -37,6 +37,7 @@ struct SmallArgs {
                         //    computes tile t after its unit (max(U, T) blocks)
   uint64_t timeout_ns;
   uint32_t extra_arrivals;  // test hook: units more than any launch publishes
+  unsigned long long* trace;  // [grid][128] %globaltimer stamps, builds with FSOPS_TRACE only
 };
 
 // Weight bytes of one block: a unit's 64 W_gateup rows and a tile's 16
@@ -48,10 +49,10 @@ __host__ __device__ inline size_t small_weight_bytes(int H, int I, int split) {
 // Dynamic shared memory of one block (from a 1024-byte aligned base).
 __host__ __device__ inline size_t small_smem_bytes(int H, int I, int split) {
   return small_weight_bytes(H, I, split)                                  // weights
-         + 8u * (H + 16) + 8u * (I + 16)                                 // x and h codes
+         + 8u * (H + 32) + 8u * (I + 32)                                 // x and h codes
          + 4u * 8 * (H / 32) + 4u * 8 * (I / 32)                         // x and h scales
          + 64u * (H / 32) + 16u * (I / 32)                               // weight scales
-         + 16 + 4u * 8 * 16 * 8 + 4u * 8 * 32                            // reduction, h in fp32
+         + 16 + 4u * 16 * 16 * 8 + 4u * 8 * 32                           // reduction (16 warps), h in fp32
          + 1024;                                                         // alignment
 }
 // Whether the shape runs on this kernel: M <= 8, H and I multiples of 128,

@@ -17,6 +17,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first address at or after p (in shared memory) aligned to `align`
+// bytes (a power of two), computed on the pointer itself so that the compiler
+// keeps it a shared-memory pointer (an integer round trip would make every
+// access through it generic).
+__device__ __forceinline__ uint8_t* smem_align(uint8_t* p, uint32_t align) {
+  return p + ((align - (smem_u32(p) & (align - 1))) & (align - 1));
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -207,6 +215,28 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+// ---------------------------------------------------------------- warp-level MMA
+// E4M3 codes in bytes 0-1 (or 2-3) of w as f16x2 (exact), the lower byte in
+// the lower half.
+__device__ __forceinline__ uint32_t e4m3_lo_f16x2(uint32_t w) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}" : "=r"(r) : "r"(w));
+  return r;
+}
+__device__ __forceinline__ uint32_t e4m3_hi_f16x2(uint32_t w) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(r) : "r"(w));
+  return r;
+}
+// d += A . B on the tensor core: A 16 x 16 f16 (row), B 16 x 8 f16 (col), fp32 d.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // ---------------------------------------------------------------- tcgen05
