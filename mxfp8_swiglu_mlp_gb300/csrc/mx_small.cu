@@ -88,8 +88,9 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& m0, uint32_
 //   w, box_bytes, row0  the tile's rows: TMA boxes of 128-byte rows (128-byte
 //                       swizzle, box j / 4 at w + (j / 4) box_bytes), the
 //                       tile's first row at row0 of its box;
-//   ws, wst, wof        the rows' scale bytes: rows g and g + 8 of block j at
-//                       ws + (8 j + g) wst + wof and + 1;
+//   ws, wjs, wof        the rows' scale bytes: rows g and g + 8 of block j at
+//                       ws + j wjs + 2 g + wof and + 1 (a warp's 16 bytes
+//                       contiguous);
 //   xc, ld              the tokens' codes, rows of ld bytes, each 32-element
 //                       block stored as [tq][half][4 codes]: codes 16 h + 4 tq
 //                       .. + 3 at byte 8 tq + 4 h of the block;
@@ -100,7 +101,7 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& m0, uint32_
 // the tokens alike.  acc[0..3]: rows g, g, g + 8, g + 8 of the tile x
 // tokens 2 tq, 2 tq + 1.
 __device__ __forceinline__ void tile_products(float (&acc)[4], const uint8_t* w, uint32_t box_bytes, int row0,
-                                              const uint8_t* ws, int wst, int wof, const uint8_t* xc, int ld,
+                                              const uint8_t* ws, int wjs, int wof, const uint8_t* xc, int ld,
                                               const float* xsc, int j0, int j1, int dj, int lane) {
   const int g = lane >> 2, tq = lane & 3;
   // ldmatrix rows: lane l gives row row0 + (l & 7) + 8 ((l >> 3) & 1) of half (l >> 4)
@@ -120,7 +121,7 @@ __device__ __forceinline__ void tile_products(float (&acc)[4], const uint8_t* w,
       ldmatrix_x4(lbase + (jj >> 2) * box_bytes + (((2 * (jj & 3) + lhalf) ^ (lrow & 7)) << 4), m[u][0], m[u][1],
                   m[u][2], m[u][3]);
       Bv[u] = *reinterpret_cast<const uint2*>(xc + g * ld + 32 * jj + 8 * tq);
-      wsv[u] = *reinterpret_cast<const uint16_t*>(ws + (8 * jj + g) * wst + wof);
+      wsv[u] = *reinterpret_cast<const uint16_t*>(ws + jj * wjs + 2 * g + wof);
       xv[u] = *reinterpret_cast<const float2*>(xsc + 8 * jj + 2 * tq);
     }
 #pragma unroll
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2) mx_small_kernel(const __grid
   uint8_t* hsm = xs + 8 * (H + 32);                        // [8][I + 32] h codes (likewise)
   float* xsc = reinterpret_cast<float*>(hsm + 8 * (I + 32));  // [nka][8 tokens]
   float* hsc = xsc + 8 * nka;                              // [nkb][8 tokens]
-  uint8_t* wsa = reinterpret_cast<uint8_t*>(hsc + 8 * nkb);  // [nka][g][tile rt][row half]: 64 nka bytes
+  uint8_t* wsa = reinterpret_cast<uint8_t*>(hsc + 8 * nkb);  // [nka][tile rt][g][row half]: 64 nka bytes
   uint8_t* wsb = wsa + 64 * nka;                           // [nkb][g][row half]: 16 nkb bytes
   float* red = reinterpret_cast<float*>(smem_align(wsb + 16 * nkb, 16));
   float* h32 = red + kSmallWarps * 16 * 8;                 // [8 tokens][32 features]
@@ -205,10 +206,10 @@ __global__ void __launch_bounds__(kSmallThreads, 2) mx_small_kernel(const __grid
     }
   }
   // weight scales, from the tcgen05 tiled layout into the order the
-  // products read: block kb, lane group g, then rows 16 rt + g (+ 8)
+  // products read: block kb, tile rt, lane group g, rows 16 rt + g (+ 8)
   if (do_a)
     for (int i = t; i < 64 * nka; i += kSmallThreads) {
-      const int kb = i >> 6, g = (i >> 3) & 7, rt = (i >> 1) & 3, hf = i & 1;
+      const int kb = i >> 6, rt = (i >> 4) & 3, g = (i >> 1) & 7, hf = i & 1;
       const int r = 16 * rt + 8 * hf + g;  // unit row: gate 0-31, up 32-63
       wsa[i] = a.sf_gu[tiled_sf_offset(r < 32 ? gate_row + r : up_row + r - 32, kb, KA)];
     }
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2) mx_small_kernel(const __grid
       const int rt = warp & 3, kh = warp >> 2;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       if (t == 0) SMALL_STAMP(10);
-      tile_products(acc, wa + (rt >> 1) * KA * 4096, 4096, 16 * (rt & 1), wsa, 8, 2 * rt, xs, H + 32, xsc, kh, nka,
+      tile_products(acc, wa + (rt >> 1) * KA * 4096, 4096, 16 * (rt & 1), wsa, 64, 16 * rt, xs, H + 32, xsc, kh, nka,
                     kSmallWarps / 4, lane);
       if (lane == 0 && warp == 0) SMALL_STAMP(11);
       if (lane == 0 && warp == kSmallWarps - 1) SMALL_STAMP(12);
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2) mx_small_kernel(const __grid
     if (t == 0) SMALL_STAMP(8);
     if (!failed) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      tile_products(acc, wb, 2048, 0, wsb, 2, 0, hsm, I + 32, hsc, warp, nkb, kSmallWarps, lane);
+      tile_products(acc, wb, 2048, 0, wsb, 16, 0, hsm, I + 32, hsc, warp, nkb, kSmallWarps, lane);
       const int g = lane >> 2, tq = lane & 3;
       red[(warp * 16 + g) * 8 + 2 * tq] = acc[0];
       red[(warp * 16 + g) * 8 + 2 * tq + 1] = acc[1];
