@@ -84,7 +84,7 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& m0, uint32_
 }
 
 // One warp's share of a 16-row weight tile times 8 token columns, over the
-// 32-element K blocks j = j0, j0 + dj, ... < j1.
+// 32-element K blocks j = j0, j0 + dj, ... < j1 (dj a multiple of 4).
 //   w, box_bytes, row0  the tile's rows: TMA boxes of 128-byte rows (128-byte
 //                       swizzle, box j / 4 at w + (j / 4) box_bytes), the
 //                       tile's first row at row0 of its box;
@@ -104,32 +104,42 @@ __device__ __forceinline__ void tile_products(float (&acc)[4], const uint8_t* w,
                                               const uint8_t* ws, int wjs, int wof, const uint8_t* xc, int ld,
                                               const float* xsc, int j0, int j1, int dj, int lane) {
   const int g = lane >> 2, tq = lane & 3;
-  // ldmatrix rows: lane l gives row row0 + (l & 7) + 8 ((l >> 3) & 1) of half (l >> 4)
+  // dj is a multiple of 4, so every block this warp takes sits at the same
+  // place in its 128-byte box: the addresses only step by a constant
   const int lrow = row0 + (lane & 7) + 8 * ((lane >> 3) & 1), lhalf = lane >> 4;
-  const uint32_t lbase = smem_u32(w) + lrow * 128;
+  uint32_t a_addr = smem_u32(w) + lrow * 128 + (((2 * (j0 & 3) + lhalf) ^ (lrow & 7)) << 4) + (j0 >> 2) * box_bytes;
+  const uint32_t a_step = (dj >> 2) * box_bytes;
+  const uint8_t* bp = xc + g * ld + 32 * j0 + 8 * tq;
+  const uint8_t* wp = ws + j0 * wjs + 2 * g + wof;
+  const float* xp = xsc + 8 * j0 + 2 * tq;
   // two blocks per step, every load of both issued first
   float acc2[4] = {0.f, 0.f, 0.f, 0.f};
   for (int j = j0; j < j1; j += 2 * dj) {
     const bool two = j + dj < j1;
     uint32_t m[2][4];
     uint2 Bv[2];
-    uint16_t wsv[2];
+    uint32_t wsv[2];
     float2 xv[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const int jj = two ? j + u * dj : j;
-      ldmatrix_x4(lbase + (jj >> 2) * box_bytes + (((2 * (jj & 3) + lhalf) ^ (lrow & 7)) << 4), m[u][0], m[u][1],
-                  m[u][2], m[u][3]);
-      Bv[u] = *reinterpret_cast<const uint2*>(xc + g * ld + 32 * jj + 8 * tq);
-      wsv[u] = *reinterpret_cast<const uint16_t*>(ws + jj * wjs + 2 * g + wof);
-      xv[u] = *reinterpret_cast<const float2*>(xsc + 8 * jj + 2 * tq);
+      const int o = (u && two) ? 1 : 0;  // the second load repeats the first past the end
+      ldmatrix_x4(a_addr + o * a_step, m[u][0], m[u][1], m[u][2], m[u][3]);
+      Bv[u] = *reinterpret_cast<const uint2*>(bp + o * 32 * dj);
+      wsv[u] = *reinterpret_cast<const uint16_t*>(wp + o * dj * wjs);
+      xv[u] = *reinterpret_cast<const float2*>(xp + o * 8 * dj);
     }
+    a_addr += 2 * a_step;
+    bp += 64 * dj;
+    wp += 2 * dj * wjs;
+    xp += 16 * dj;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       if (u == 1 && !two) break;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       mma_e4m3_16832(d, m[u][0], m[u][1], m[u][2], m[u][3], Bv[u].x, Bv[u].y);
-      const float w0 = ue8m0_f32(wsv[u] & 0xFFu), w1 = ue8m0_f32(wsv[u] >> 8);
+      // 2^(s - 127) of each row's scale byte (s = 0: 2^-127, the subnormal)
+      const float w0 = __uint_as_float(max((wsv[u] << 23) & 0x7F800000u, 0x00400000u));
+      const float w1 = __uint_as_float(max((wsv[u] << 15) & 0x7F800000u, 0x00400000u));
       float* ac = u ? acc2 : acc;
       ac[0] = fmaf(d[0], w0 * xv[u].x, ac[0]);
       ac[1] = fmaf(d[1], w0 * xv[u].y, ac[1]);
