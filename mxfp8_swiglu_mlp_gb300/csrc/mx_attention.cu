@@ -509,6 +509,12 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
     // heads.
     const int wrow = 16 * warp;
     float* pw = pws + warp * 8 * kPwLd;
+    // the lane's swizzled offsets in a stage: K rows wrow + g (+ 8), bytes
+    // 32 bb + 8 tq at kofs + ((32 bb) ^ kxor); V rows wrow + 2 tq (+ 1, + 8,
+    // + 9), bytes 16 g .. 16 g + 15 at vofs[k & 1] + 1024 (k >> 1)
+    const int kofs = (wrow + g) * 128 + 16 * (((tq >> 1) ^ g) & 1) + 8 * (tq & 1), kxor = 32 * (g >> 1);
+    const int vofs[2] = {(wrow + 2 * tq) * 128 + ((g ^ (2 * tq)) << 4),
+                         (wrow + 2 * tq + 1) * 128 + ((g ^ (2 * tq + 1)) << 4)};
     int kq = 0, qb = 0;
     const int vbb = g >> 1;  // the lane's V scale block
     float O[8][4];
@@ -551,8 +557,10 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
             const uint32_t kw1 = *reinterpret_cast<const uint32_t*>(stg[s].ks + 4 * r1);
 #pragma unroll
             for (int bb = 0; bb < 4; ++bb) {
-              const uint2 x0 = *reinterpret_cast<const uint2*>(kb + swz(r0, 32 * bb + 8 * tq));
-              const uint2 x1 = *reinterpret_cast<const uint2*>(kb + swz(r1, 32 * bb + 8 * tq));
+              // swz(r0, 32 bb + 8 tq): rows r0 and r0 + 8 share r0 % 8 = g
+              const int ko = kofs + ((32 * bb) ^ kxor);
+              const uint2 x0 = *reinterpret_cast<const uint2*>(kb + ko);
+              const uint2 x1 = *reinterpret_cast<const uint2*>(kb + ko + 1024);
               const uint4 bq = qfrag[qb][bb][lane];
               float d[4] = {0.f, 0.f, 0.f, 0.f};
               mma_16816(d, e4m3_lo_f16x2(x0.x), e4m3_lo_f16x2(x1.x), e4m3_hi_f16x2(x0.x), e4m3_hi_f16x2(x1.x), bq.x,
@@ -639,7 +647,7 @@ __global__ void __launch_bounds__(kAThreads, 2) paged_decode_kernel(const __grid
           }
           uint4 W[4];  // the lane's 16 dimensions of its four tokens
 #pragma unroll
-          for (int k = 0; k < 4; ++k) W[k] = *reinterpret_cast<const uint4*>(vb + swz(rvk[k], 16 * g));
+          for (int k = 0; k < 4; ++k) W[k] = *reinterpret_cast<const uint4*>(vb + vofs[k & 1] + 1024 * (k >> 1));
           if ((m.flags & kMetaFar) == 0) {
             // f16x2 2^(s - ref) of the token pairs (rv, rv + 1) and (rv + 8, rv + 9)
             const uint32_t m01 = reinterpret_cast<const uint32_t*>(&pr.vm[4 * warp + tq][0])[vbb];
