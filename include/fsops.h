@@ -413,7 +413,9 @@ fsops_status fsops_debug_set_extra_arrivals(uint32_t n);
  *                     (cta_group::2 MMA; N % 256 == 0, two or more row tiles).
  *   PRIME             weight loads in flight before the activations exist.
  *   MAX_INFLIGHT      weight loads in flight per block (1..8).
- *   LOCAL_XQ          0: quantise x grid-wide even for M <= 16.
+ *   LOCAL_XQ          0: quantise x grid-wide even for M <= 16; 2: every
+ *                     block quantises x itself also with RMSNorm (by
+ *                     default only where M * H <= 16384).
  *   DECODE_PATH       M <= 128: 0 the grid-wide two-phase kernel, 1 the
  *                     cluster-sliced kernel (M <= 32), 2 the small-M kernel
  *                     (M <= 8, one block per 32 intermediate features and

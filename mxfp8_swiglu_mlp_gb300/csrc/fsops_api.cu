@@ -128,7 +128,7 @@ int stage_tmem_for(int npad) { return npad <= 32 ? 1 : 0; }
 // stage).  Larger M: x is quantised once, each block a slice, shared through L2.
 int local_xq_for(int npad) {
   if (npad > 16) return 0;
-  return knob_or(FSOPS_KNOB_LOCAL_XQ, 1, 0, 1);
+  return knob_or(FSOPS_KNOB_LOCAL_XQ, 1, 0, 2) ? 1 : 0;
 }
 // Shared memory besides the stage ring (local_xq is only used with x quantised in-kernel).
 uint32_t extra_smem(int npad, int local_xq) {
@@ -413,10 +413,12 @@ fsops_status fill_mlp_args(KernelArgs& ka, const MlpPlan& pl, const MlpBuffers& 
   // comes before its block's gate/up MMAs, and no tile of y is finished before
   // every gate/up tile is (each down-projection tile reads every chunk of h).
   // With RMSNorm every block quantising locally first reads all M rows of x
-  // for their norms: that pays only for short rows (M = 1, H = 1024: 16.0
-  // against 17.4 us for the block; M = 16, H = 2560: 27.5 against 27.0 with
-  // x quantised grid-wide, each block a slice)
-  const bool norm_local = gamma == nullptr || static_cast<long long>(M) * H <= 16384;
+  // for their norms, all blocks the same rows at once: that pays only for
+  // short rows (M = 1, H = 1024: 16.0 against 17.4 us for the block; M = 16,
+  // H = 2560: 27.6 against 26.0 with x quantised grid-wide, each block a
+  // slice; LOCAL_XQ = 2 forces it)
+  const bool norm_local = gamma == nullptr || static_cast<long long>(M) * H <= 16384 ||
+                          knob(FSOPS_KNOB_LOCAL_XQ) == 2;
   ka.local_xq = (x_bf16 != nullptr && norm_local) ? local_xq_for(ka.npad) : 0;
   p0.dep = (ka.local_xq || x_bf16 == nullptr) ? kDepNone : kDepXReady;
   if (ka.local_xq && !encode_x_map(&ka.tm_x, x_bf16, H, M, ka.npad)) return FSOPS_ERR_INVALID_ARG;

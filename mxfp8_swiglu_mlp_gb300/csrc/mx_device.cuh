@@ -40,17 +40,15 @@ __device__ __forceinline__ uint32_t quantize_block_pack(const uint4 (&raw)[4], u
   return s;
 }
 // The same for RMSNorm(x) * gamma: the 32 values x * rn * gamma (fp32, in
-// that order; rn = 1 / rms of the block's row, gamma 16-byte aligned bf16),
-// quantised with the rule above.  Returns the scale byte.
-__device__ __forceinline__ uint32_t quantize_block_pack_norm(const uint4 (&raw)[4], const uint16_t* gamma, float rn,
+// that order; rn = 1 / rms of the block's row, gv the block's 32 gains as
+// bf16), quantised with the rule above.  Returns the scale byte.
+__device__ __forceinline__ uint32_t quantize_block_pack_norm(const uint4 (&raw)[4], const uint4 (&gv)[4], float rn,
                                                              uint32_t (&packed)[8]) {
   const uint32_t* w = reinterpret_cast<const uint32_t*>(raw);
-  const uint4* gp = reinterpret_cast<const uint4*>(gamma);
   float v[32];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 gv = __ldg(gp + q);
-    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    const uint32_t gw[4] = {gv[q].x, gv[q].y, gv[q].z, gv[q].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       v[8 * q + 2 * i] = bf16_lo(w[4 * q + i]) * rn * bf16_lo(gw[i]);
@@ -65,6 +63,14 @@ __device__ __forceinline__ uint32_t quantize_block_pack_norm(const uint4 (&raw)[
 #pragma unroll
   for (int i = 0; i < 8; ++i) packed[i] = e4m3x4_code(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
   return s;
+}
+// The same with the gains read from global memory (16-byte aligned bf16).
+__device__ __forceinline__ uint32_t quantize_block_pack_norm(const uint4 (&raw)[4], const uint16_t* gamma, float rn,
+                                                             uint32_t (&packed)[8]) {
+  uint4 gv[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) gv[q] = __ldg(reinterpret_cast<const uint4*>(gamma) + q);
+  return quantize_block_pack_norm(raw, gv, rn, packed);
 }
 // 1 / sqrt(mean(x^2) + eps) of a bf16 row of K elements, reduced in fp32 by
 // the calling warp (every lane gets the result).

@@ -822,6 +822,25 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       const long long NB = static_cast<long long>(npad) * nbk;
       const long long b0 = range_begin(blockIdx.x, NB, G), b1 = range_begin(blockIdx.x + 1, NB, G);
       const bool norm = a.gamma != nullptr;
+      long long b = b0 + et;
+      uint4 raw[4], gv[4];
+      bool have = false;
+      // the first block's x (and gamma) loads go out before the norms' row
+      // loads and the weight stream, so that both round trips overlap
+      if (b < b1) {
+        const int m = static_cast<int>(b / nbk), kb = static_cast<int>(b % nbk);
+        if (m < a.M) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<long long>(m) * a.H + kb * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) raw[i] = __ldcg(src + i);
+          if (norm) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) gv[i] = __ldg(reinterpret_cast<const uint4*>(a.gamma + kb * 32) + i);
+          }
+          have = true;
+        }
+      }
+      mbar_arrive(x_issued);
       if (norm && b1 > b0) {
         // RMSNorm: 1 / rms of every row the slice touches, over the whole row
         // (one warp per row in turn)
@@ -832,19 +851,6 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
         }
         epi_bar();
       }
-      long long b = b0 + et;
-      uint4 raw[4];
-      bool have = false;
-      if (b < b1) {  // issue the first block's loads before the weight stream starts
-        const int m = static_cast<int>(b / nbk), kb = static_cast<int>(b % nbk);
-        if (m < a.M) {
-          const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<long long>(m) * a.H + kb * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) raw[i] = __ldcg(src + i);
-          have = true;
-        }
-      }
-      mbar_arrive(x_issued);
       for (; b < b1; b += 128) {
         const int m = static_cast<int>(b / nbk), kb = static_cast<int>(b % nbk);
         uint32_t s = 0;
@@ -853,10 +859,14 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
             const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<long long>(m) * a.H + kb * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i) raw[i] = __ldcg(src + i);
+            if (norm) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) gv[i] = __ldg(reinterpret_cast<const uint4*>(a.gamma + kb * 32) + i);
+            }
           }
           if (norm) {
             uint32_t pk[8];
-            s = quantize_block_pack_norm(raw, a.gamma + kb * 32, rnorm[m], pk);
+            s = quantize_block_pack_norm(raw, gv, rnorm[m], pk);
             uint4* d = reinterpret_cast<uint4*>(a.xq_codes + static_cast<long long>(m) * a.H + kb * 32);
             d[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             d[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
@@ -870,10 +880,13 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
       if (et == 0) FSOPS_STAMP(63);
       fence_proxy_async_global();
       epi_bar();
-      // to every block whose first phase reads x (each waits for all G slices)
+      // to every block whose first phase reads x (each waits for all G
+      // slices): one fence orders the whole slice (every epilogue thread's
+      // stores, through the barrier) before this thread's relaxed adds
+      if (et < static_cast<int>(G)) fence_acq_rel_gpu();
       for (int c = et; c < static_cast<int>(G); c += 128)
         if (has_units(a.ph[0], static_cast<uint32_t>(c), static_cast<uint32_t>(G)))
-          red_add_release_gpu(a.xready + c, 1u);
+          red_add_relaxed_gpu(a.xready + c, 1u);
       if (et == 0) FSOPS_STAMP(1);
     }
     // (2) accumulators
