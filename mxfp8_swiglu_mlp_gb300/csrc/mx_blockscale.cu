@@ -296,6 +296,16 @@ __global__ void __launch_bounds__(BsCfg<NPAD>::THREADS, 1) bs_gemm_kernel(const 
     };
     int cur_t = -1, first_kb = 0, last_kb = 0;
     uint32_t seq = 0;
+    // a unit's scales (this thread's token scale, the weight block's scale)
+    // are loaded one unit ahead: their L2 round trip overlaps the previous
+    // unit's accumulator wait and sums instead of adding to every unit
+    float sa_next = 0.f, sw_next = 0.f;
+    auto load_scales = [&](uint32_t u) {
+      const int t = static_cast<int>(u / KB), kb = static_cast<int>(u % KB);
+      sa_next = et < NPAD && et < M ? __ldg(a.a_scales + static_cast<size_t>(et) * KB + kb) : 0.f;
+      sw_next = __ldg(a.w_scales + static_cast<size_t>(t) * KB + kb);
+    };
+    if (u0 < u1) load_scales(u0);
     for (uint32_t u = u0; u < u1; ++u, ++seq) {
       const int t = static_cast<int>(u / KB), kb = static_cast<int>(u % KB);
       if (t != cur_t) {
@@ -305,12 +315,13 @@ __global__ void __launch_bounds__(BsCfg<NPAD>::THREADS, 1) bs_gemm_kernel(const 
       }
       last_kb = kb;
       const uint32_t b = seq % NB;
+      const float sa = sa_next, sw = sw_next;
+      if (u + 1 < u1) load_scales(u + 1);
       // the K-block's token scales, one per thread, through shared memory
       bs_epi_bar<EW>();  // the previous unit's reads of sa_s are done
-      if (et < NPAD) sa_s[et] = et < M ? __ldg(a.a_scales + static_cast<size_t>(et) * KB + kb) : 0.f;
+      if (et < NPAD) sa_s[et] = sa;
       if (!bs_epi_and<EW>(wait_mbar(cx, &acc_full[b], (seq / NB) & 1u, kSiteAccFull))) { ok = false; break; }
       tc_fence_after();
-      const float sw = __ldg(a.w_scales + static_cast<size_t>(t) * KB + kb);
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + b * NPAD + r0;
       // up to 32 columns of loads in flight per wait
       constexpr int kBatch = COLS < 32 ? COLS : 32;
