@@ -50,14 +50,15 @@ struct BsCfg {
   static constexpr int THREADS = 128 + 32 * EW;
   static constexpr int COLS = NPAD / (EW / 4);  // token columns per epilogue thread
   static constexpr uint32_t SB = 128u * NPAD + kBsWBytes;  // stage: A tile (NPAD x 128) | W tile (128 x 128)
-  static constexpr uint32_t FIXED = 512u + 1536u + 1024u;  // unit scale tile, control words (+ 1 KB of token scales), alignment
+  // unit scale tile, control words (512 B) and the token scales of each accumulator, alignment
+  static constexpr uint32_t FIXED = 512u + 512u + kBsAccBufs * 512u + 1024u;
   static constexpr int STAGES = (kMaxSmem - FIXED) / SB < kBsMaxStages ? (kMaxSmem - FIXED) / SB : kBsMaxStages;
   static constexpr size_t SMEM = STAGES * SB + FIXED;
   // TMEM: the accumulators, then 8 columns of unit scales
   static constexpr uint32_t COLS_USED = kBsAccBufs * NPAD + 8;
   static constexpr uint32_t TMEM_COLS = COLS_USED <= 64 ? 64 : COLS_USED <= 128 ? 128 : COLS_USED <= 256 ? 256 : 512;
   // the barriers and words below the token scales (which start 512 bytes in)
-  static_assert((2 * kBsMaxStages + 2 * kBsAccBufs + 1) * 8 + 16 <= 512, "control words overlap the token scales");
+  static_assert((2 * kBsMaxStages + 3 * kBsAccBufs + 1) * 8 + 16 <= 512, "control words overlap the token scales");
   static_assert(COLS % 4 == 0, "token columns are read four at a time");
 };
 
@@ -172,10 +173,11 @@ __global__ void __launch_bounds__(BsCfg<NPAD>::THREADS, 1) bs_gemm_kernel(const 
   uint64_t* acc_full = empty + S;                     // [NB]
   uint64_t* acc_empty = acc_full + NB;                // [NB]
   uint64_t* drain = acc_empty + NB;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* scl_full = drain + 1;                     // [NB] the unit's scales are in sa_s[b]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(scl_full + NB);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2] last arrivals
-  float* sa_s = reinterpret_cast<float*>(ctl + 512);  // [2][128] the units' token scales x weight scale (16-byte aligned)
+  float* sa_s = reinterpret_cast<float*>(ctl + 512);  // [NB][128] the units' token scales x weight scale (16-byte aligned)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t U = static_cast<uint32_t>(a.T) * a.KB, G = gridDim.x;
@@ -189,6 +191,7 @@ __global__ void __launch_bounds__(BsCfg<NPAD>::THREADS, 1) bs_gemm_kernel(const 
     for (int b = 0; b < NB; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], EW);  // one arrival per epilogue warp
+      mbar_init(&scl_full[b], 32);   // every lane of the scale warp
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -267,6 +270,43 @@ __global__ void __launch_bounds__(BsCfg<NPAD>::THREADS, 1) bs_gemm_kernel(const 
     if (!ok) *abort_flag = 1;
     tc_commit(drain);
     drain_mbar(drain, 0, 200000000ull);
+  } else if (warp == 1) {
+    // ------------------------------------------------ scale warp: each unit's token scales times the
+    // weight block's scale into the shared slot of its accumulator (lane l: tokens l, l + 32, ...),
+    // loaded one unit ahead, written once the epilogue has released the slot
+    griddep_wait();  // the token scales may be the output of the previous kernel
+    const int M = a.M, KB = a.KB;
+    float sa_next[4] = {0.f, 0.f, 0.f, 0.f}, sw_next = 0.f;
+    auto load_scales = [&](uint32_t u) {
+      const int t = static_cast<int>(u / KB), kb = static_cast<int>(u % KB);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = lane + 32 * j;
+        sa_next[j] = i < NPAD && i < M ? __ldg(a.a_scales + static_cast<size_t>(i) * KB + kb) : 0.f;
+      }
+      sw_next = __ldg(a.w_scales + static_cast<size_t>(t) * KB + kb);
+    };
+    bool ok = true;
+    uint32_t seq = 0;
+    if (u0 < u1) load_scales(u0);
+    for (uint32_t u = u0; u < u1; ++u, ++seq) {
+      const uint32_t b = seq % NB;
+      float sa[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sa[j] = sa_next[j];
+      const float sw = sw_next;
+      if (u + 1 < u1) load_scales(u + 1);
+      if (!__all_sync(0xFFFFFFFFu, wait_mbar(cx, &acc_empty[b], ((seq / NB) & 1u) ^ 1u, kSiteAccEmpty))) {
+        ok = false;
+        break;
+      }
+      float* dst = sa_s + b * 128;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (lane + 32 * j < NPAD) dst[lane + 32 * j] = sw * sa[j];
+      mbar_arrive(&scl_full[b]);
+    }
+    if (!ok) *abort_flag = 1;
   } else if (warp >= 4) {
     // ------------------------------------------------ epilogue: thread et holds row n = et % 128 of
     // the tile for token columns [r0, r0 + COLS)
@@ -301,16 +341,8 @@ __global__ void __launch_bounds__(BsCfg<NPAD>::THREADS, 1) bs_gemm_kernel(const 
     };
     int cur_t = -1, first_kb = 0, last_kb = 0;
     uint32_t seq = 0;
-    // a unit's scales (this thread's token scale, the weight block's scale)
-    // are loaded one unit ahead: their L2 round trip overlaps the previous
-    // unit's accumulator wait and sums instead of adding to every unit
-    float sa_next = 0.f, sw_next = 0.f;
-    auto load_scales = [&](uint32_t u) {
-      const int t = static_cast<int>(u / KB), kb = static_cast<int>(u % KB);
-      sa_next = et < NPAD && et < M ? __ldg(a.a_scales + static_cast<size_t>(et) * KB + kb) : 0.f;
-      sw_next = __ldg(a.w_scales + static_cast<size_t>(t) * KB + kb);
-    };
-    if (u0 < u1) load_scales(u0);
+    // each warp runs on its own: it waits for the unit's accumulator and its
+    // scales (the scale warp's), no barrier with the other epilogue warps
     for (uint32_t u = u0; u < u1; ++u, ++seq) {
       const int t = static_cast<int>(u / KB), kb = static_cast<int>(u % KB);
       if (t != cur_t) {
@@ -319,16 +351,14 @@ __global__ void __launch_bounds__(BsCfg<NPAD>::THREADS, 1) bs_gemm_kernel(const 
         first_kb = kb;
       }
       last_kb = kb;
-      const uint32_t b = seq % NB;
-      const float sa = sa_next, sw = sw_next;
-      if (u + 1 < u1) load_scales(u + 1);
-      // the K-block's token scales, one per thread, through shared memory
-      // (two slots: a warp writes unit u + 1's only after the barrier of
-      // unit u, which every warp reaches after its reads of unit u - 1's)
-      float* sa_u = sa_s + (seq & 1u) * 128;
-      if (et < NPAD) sa_u[et] = sw * sa;
-      if (!bs_epi_and<EW>(wait_mbar(cx, &acc_full[b], (seq / NB) & 1u, kSiteAccFull))) { ok = false; break; }
+      const uint32_t b = seq % NB, par = (seq / NB) & 1u;
+      if (!__all_sync(0xFFFFFFFFu, wait_mbar(cx, &acc_full[b], par, kSiteAccFull) &&
+                                       wait_mbar(cx, &scl_full[b], par, kSiteAccFull))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
+      const float* sa_u = sa_s + b * 128;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + b * NPAD + r0;
       // up to 32 columns of loads in flight per wait
       constexpr int kBatch = COLS < 32 ? COLS : 32;
@@ -352,6 +382,8 @@ __global__ void __launch_bounds__(BsCfg<NPAD>::THREADS, 1) bs_gemm_kernel(const 
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
     }
+    if (!ok) *abort_flag = 1;  // the other warps' waits end at once
+    ok = bs_epi_and<EW>(ok);   // every epilogue warp agrees before the tiles' finish
     if (ok && cur_t >= 0) flush(cur_t, first_kb == 0 && last_kb == KB - 1);
     // shared tiles: the block that adds last writes C and leaves the
     // accumulator and the counter zero
