@@ -1230,24 +1230,70 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           if (et == 0) FSOPS_STAMP_IF(p == 1, 61);
           if (last) {
             if (STAGED) {
-              // every load is issued before the first store: one L2 round trip
-              // (M * ncols / 512 <= 16 float4 per thread)
+              // a pass's loads are all issued before its first store: one L2
+              // round trip per eight float4 per thread (M * ncols / 512 <= 16)
               const int lg = ncols == 256 ? 6 : 5;
               const int n4 = a.M << lg;
-              float4 v[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int q = et + 128 * j;
-                if (q < n4) v[j] = __ldcg(reinterpret_cast<const float4*>(accg + (q >> lg) * kTileRows) + (q & ((1 << lg) - 1)));
-              }
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int q = et + 128 * j;
-                if (q < n4) *reinterpret_cast<float4*>(stg + (q >> lg) * kStageLd + (q & ((1 << lg) - 1)) * 4) = v[j];
-              }
-              epi_bar();
+              // plain output: each thread writes the four columns of each
+              // float4 it read straight from registers (with the residual's
+              // loads in the same round trip), eight float4 per pass; SwiGLU
+              // goes through stg, whose 32-blocks span several threads' loads.
+              // Each thread leaves what it read zero for the next launch at
+              // once (the stores follow its own loads of the same words).
+              const bool plain = ph.epi != kEpiSwiGLU, res = plain && a.residual != nullptr;
               if (et == 0) FSOPS_STAMP_IF(p == 1, 56);
-              finish_staged(a, ph, t, ncols, stg, et, 0, ncols >> 6);
+#pragma unroll 1
+              for (int q0 = 0; q0 < n4; q0 += 8 * 128) {
+                float4 v[8];
+                uint2 rv[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const int q = q0 + et + 128 * j;
+                  if (q < n4) {
+                    v[j] = __ldcg(reinterpret_cast<const float4*>(accg + (q >> lg) * kTileRows) + (q & ((1 << lg) - 1)));
+                    if (res)
+                      rv[j] = __ldcg(reinterpret_cast<const uint2*>(
+                          a.residual + static_cast<long long>(q >> lg) * ph.out_ld +
+                          static_cast<long long>(t) * ph.tile_rows + (q & ((1 << lg) - 1)) * 4));
+                  }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const int q = q0 + et + 128 * j;
+                  if (q < n4)
+                    __stcg(reinterpret_cast<float4*>(accg + (q >> lg) * kTileRows) + (q & ((1 << lg) - 1)),
+                           make_float4(0.f, 0.f, 0.f, 0.f));
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const int q = q0 + et + 128 * j;
+                  if (q >= n4) continue;
+                  if (!plain) {
+                    *reinterpret_cast<float4*>(stg + (q >> lg) * kStageLd + (q & ((1 << lg) - 1)) * 4) = v[j];
+                    continue;
+                  }
+                  const long long o = static_cast<long long>(q >> lg) * ph.out_ld +
+                                      static_cast<long long>(t) * ph.tile_rows + (q & ((1 << lg) - 1)) * 4;
+                  float4 y = v[j];
+                  if (res) {  // y = residual + the sums, rounded once
+                    y.x += bf16_lo(rv[j].x);
+                    y.y += bf16_hi(rv[j].x);
+                    y.z += bf16_lo(rv[j].y);
+                    y.w += bf16_hi(rv[j].y);
+                  }
+                  if (a.out_f32 && !res) {
+                    *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o) = y;
+                  } else {
+                    const __nv_bfloat162 b0 = __floats2bfloat162_rn(y.x, y.y), b1 = __floats2bfloat162_rn(y.z, y.w);
+                    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + o) =
+                        make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+                  }
+                }
+              }
+              if (!plain) {
+                epi_bar();
+                finish_staged(a, ph, t, ncols, stg, et, 0, ncols >> 6);
+              }
               if (et == 0) FSOPS_STAMP_IF(p == 1, 57);
             } else if (ph.epi == kEpiSwiGLU) {
               // token r's sums are row r of the accumulator; 64 loads are in
@@ -1272,9 +1318,10 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
                 }
               }
             }
-            // leave the tile's accumulator (M * 256 floats) zero for the next launch
-            epi_bar();
-            {
+            // leave the tile's accumulator (M * 256 floats) zero for the next
+            // launch (the staged path zeroed it as it read it)
+            if (!STAGED) {
+              epi_bar();
               float4* z = reinterpret_cast<float4*>(accg);
               const int n4 = a.M * (kTileRows / 4);
 #pragma unroll 1
