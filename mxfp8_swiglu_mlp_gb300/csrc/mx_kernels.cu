@@ -378,10 +378,10 @@ __device__ __forceinline__ void swiglu_block(const KernelArgs& a, int f0, int r,
 
 // Plain output: 8 consecutive columns c..c+7 of token r.
 __device__ __forceinline__ void store8(const KernelArgs& a, const PhaseArgs& p, int r, long long col,
-                                       const float* v) {
+                                       const float* v, bool have_res = false, uint4 res = uint4{}) {
   const long long o = static_cast<long long>(r) * p.out_ld + col;
-  if (a.residual != nullptr) {  // y = residual + the sums, rounded once
-    const uint4 rv = *reinterpret_cast<const uint4*>(a.residual + o);
+  if (a.residual != nullptr) {  // y = residual + the sums, rounded once (res: the 8 values, if already loaded)
+    const uint4 rv = have_res ? res : *reinterpret_cast<const uint4*>(a.residual + o);
     const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
     float s[8];
 #pragma unroll
@@ -515,9 +515,13 @@ __device__ __noinline__ bool finish_slice(const KernelArgs& a, const PhaseArgs& 
   const int r0 = a.M * arrival / owners, r1 = a.M * (arrival + 1) / owners;
   const int lg = ncols == 256 ? 5 : 4;  // log2(8-column items per row)
   const int items = (r1 - r0) << lg;
+  // each pass issues its sums' loads (and the residual's) together; each
+  // thread clears what it read right after the loads (its stores follow its
+  // own loads of the same words), rows [r0, r1) x columns [0, ncols)
 #pragma unroll 1
   for (int i0 = 0; i0 < items; i0 += 4 * 128) {
     float4 v[4][2];
+    uint4 rv[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int i = i0 + et + 128 * j;
@@ -525,6 +529,20 @@ __device__ __noinline__ bool finish_slice(const KernelArgs& a, const PhaseArgs& 
         const float4* src = reinterpret_cast<const float4*>(accg + (r0 + (i >> lg)) * kTileRows + (i & ((1 << lg) - 1)) * 8);
         v[j][0] = __ldcg(src);
         v[j][1] = __ldcg(src + 1);
+        if (a.residual != nullptr)
+          rv[j] = __ldcg(reinterpret_cast<const uint4*>(
+              a.residual + static_cast<long long>(r0 + (i >> lg)) * ph.out_ld +
+              static_cast<long long>(t) * ph.tile_rows + (i & ((1 << lg) - 1)) * 8));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + et + 128 * j;
+      if (i < items) {
+        float4* dst = const_cast<float4*>(reinterpret_cast<const float4*>(accg + (r0 + (i >> lg)) * kTileRows +
+                                                                            (i & ((1 << lg) - 1)) * 8));
+        __stcg(dst, make_float4(0.f, 0.f, 0.f, 0.f));
+        __stcg(dst + 1, make_float4(0.f, 0.f, 0.f, 0.f));
       }
     }
 #pragma unroll
@@ -532,17 +550,12 @@ __device__ __noinline__ bool finish_slice(const KernelArgs& a, const PhaseArgs& 
       const int i = i0 + et + 128 * j;
       if (i < items) {
         const float w[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w, v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
-        store8(a, ph, r0 + (i >> lg), static_cast<long long>(t) * ph.tile_rows + (i & ((1 << lg) - 1)) * 8, w);
+        store8(a, ph, r0 + (i >> lg), static_cast<long long>(t) * ph.tile_rows + (i & ((1 << lg) - 1)) * 8, w,
+               a.residual != nullptr, rv[j]);
       }
     }
   }
   if (et == 0 && seen + 1 == 2u * static_cast<uint32_t>(owners)) ph.tile_cnt[t] = 0u;
-  epi_bar();  // every read of the rows before they are cleared
-  // rows [r0, r1), columns [0, ncols) (row stride kTileRows)
-#pragma unroll 1
-  for (int i = et; i < ((r1 - r0) << (lg + 1)); i += 128)
-    __stcg(reinterpret_cast<float4*>(accg + (r0 + (i >> (lg + 1))) * kTileRows) + (i & ((2 << lg) - 1)),
-           make_float4(0.f, 0.f, 0.f, 0.f));
   return true;
 }
 
