@@ -43,10 +43,10 @@ FALLBACK_HBM_GBS = 6800.0
 # number is reported only while those sources are unchanged), the bytes, the
 # launch form captured and the summary under profiles/.
 NCU_TRAFFIC = {
-    "m16": {"sha": "febe865ccf607e88", "bytes": 80.49e6, "source": "profiles/mx_persistent_kernel_m16_memory.md",
+    "m16": {"sha": "bd499e4d97a04d3e", "bytes": 80.53e6, "source": "profiles/mx_persistent_kernel_m16_memory.md",
             "form": "gate/up split over all blocks (--knob PAIRS=0); the timed default splits gate/up tiles by "
                     "2-block clusters, same weight stream"},
-    "m128": {"sha": "febe865ccf607e88", "bytes": 164.28e6, "source": "profiles/mx_persistent_kernel_m128_memory.md",
+    "m128": {"sha": "bd499e4d97a04d3e", "bytes": 164.32e6, "source": "profiles/mx_persistent_kernel_m128_memory.md",
              "form": "the default (no cluster split at M > 32)"},
 }
 KERNEL_SOURCES = ("mx_kernels.cu", "mx_internal.h", "mx_mxfp8.cuh", "sm103.cuh", "mx_device.cuh")
@@ -843,8 +843,11 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=20)
+    # defaults: 20000 steps and 20 warm-up calls for the GPU arm (about half a
+    # second of timed work at m16); 20 and 5 for the CPU oracle arm, whose
+    # every call costs at least ~50 ms whatever its sample
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="m16")
     ap.add_argument("--no-sweep", action="store_true")
@@ -864,6 +867,10 @@ def main():
     ap.add_argument("--prefill-shapes", default="",
                     help="comma-separated subset of the prefill section's GEMM shapes (default: all)")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 20 if args.impl == "reference" else 20000
+    if args.warmup is None:
+        args.warmup = 5 if args.impl == "reference" else 20
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
