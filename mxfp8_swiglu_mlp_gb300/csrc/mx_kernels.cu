@@ -1065,10 +1065,12 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
               if (lane < a.M) {
                 const bool other = ph.pairs && static_cast<uint32_t>(c0 >> 7) != pair_h;
                 if (push_bulk && other) {
+                  // row `lane` of 512 bytes, its 16-byte slots XOR-swizzled by
+                  // the row (the rows' same slot would share four banks)
                   float4* d = reinterpret_cast<float4*>(xring + lane * 512);
 #pragma unroll
                   for (int q = 0; q < 32; ++q)
-                    d[q] = make_float4(__uint_as_float(v[q >> 2][4 * (q & 3)]), __uint_as_float(v[q >> 2][4 * (q & 3) + 1]),
+                    d[q ^ lane] = make_float4(__uint_as_float(v[q >> 2][4 * (q & 3)]), __uint_as_float(v[q >> 2][4 * (q & 3) + 1]),
                                        __uint_as_float(v[q >> 2][4 * (q & 3) + 2]), __uint_as_float(v[q >> 2][4 * (q & 3) + 3]));
                 } else if (push_st && other) {
                   const uint32_t dst = pstg + static_cast<uint32_t>(lane * kStageLd + (c0 ^ 128)) * 4u;
@@ -1176,13 +1178,15 @@ __global__ void __launch_bounds__(kThreads, 1) mx_persistent_kernel(const __grid
           if (!epi_and(send_ok && wait_mbar_cluster(cx, peer_ready, 0, kSitePeer))) { ok = false; break; }
           if (et == 0) FSOPS_STAMP(58);
           // the partner's sums: pushed by stores into this stg at the other
-          // half's columns, or copied into the x ring (row r at 512 r bytes)
+          // half's columns, or copied into the x ring (row r at 512 r bytes,
+          // 16-byte slot q of it at q ^ r)
           const float* recv = local_xq ? reinterpret_cast<const float*>(xring + kPairRecvOff) : stg;
           const int rld = local_xq ? 128 : kStageLd;
 #pragma unroll 1
           for (int i = et; i < (a.M << 5); i += 128) {
             const int r = i >> 5, c = 128 * h + (i & 31) * 4;
-            const float4 pv = *reinterpret_cast<const float4*>(recv + r * rld + (local_xq ? (i & 31) * 4 : (c ^ 128)));
+            const float4 pv =
+                *reinterpret_cast<const float4*>(recv + r * rld + (local_xq ? ((i ^ r) & 31) * 4 : (c ^ 128)));
             float4* mine = reinterpret_cast<float4*>(stg + r * kStageLd + c);
             const float4 mv = *mine;
             *mine = make_float4(mv.x + pv.x, mv.y + pv.y, mv.z + pv.z, mv.w + pv.w);
