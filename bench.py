@@ -43,10 +43,10 @@ FALLBACK_HBM_GBS = 6800.0
 # number is reported only while those sources are unchanged), the bytes, the
 # launch form captured and the summary under profiles/.
 NCU_TRAFFIC = {
-    "m16": {"sha": "bd499e4d97a04d3e", "bytes": 80.53e6, "source": "profiles/mx_persistent_kernel_m16_memory.md",
+    "m16": {"sha": "bda093efa9298a67", "bytes": 80.59e6, "source": "profiles/mx_persistent_kernel_m16_memory.md",
             "form": "gate/up split over all blocks (--knob PAIRS=0); the timed default splits gate/up tiles by "
                     "2-block clusters, same weight stream"},
-    "m128": {"sha": "bd499e4d97a04d3e", "bytes": 164.32e6, "source": "profiles/mx_persistent_kernel_m128_memory.md",
+    "m128": {"sha": "bda093efa9298a67", "bytes": 164.39e6, "source": "profiles/mx_persistent_kernel_m128_memory.md",
              "form": "the default (no cluster split at M > 32)"},
 }
 KERNEL_SOURCES = ("mx_kernels.cu", "mx_internal.h", "mx_mxfp8.cuh", "sm103.cuh", "mx_device.cuh")
