@@ -48,11 +48,12 @@ std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 unsigned long long* g_trace = nullptr;
 #endif
 std::atomic<uint32_t> g_extra{0};
-// Weight tiles (32 KB each) a block keeps in flight by default: 4 x 32 KB per
+// Weight tiles (32 KB each) a block keeps in flight by default: 3 x 32 KB per
 // SM covers the loaded HBM latency (~1.5 us) at the SM's share of the
-// bandwidth even when only half the SMs stream; deeper queues only add latency
-// to every other memory round trip.
-constexpr int kDefaultMaxInflight = 4;
+// bandwidth; deeper queues only add latency to every other memory round trip
+// (against 4: M = 16, H = 2560, I = 9728: 22.0 against 22.4 us; H = 5120,
+// I = 17408: 0.2-0.5 us less at M = 1-32, equal at M = 64-128).
+constexpr int kDefaultMaxInflight = 3;
 // Plan overrides set through fsops_debug_set_knob (-1: the library's own
 // choice).  Read with one atomic load per use; nothing is read from the
 // process environment on the call path.
